@@ -1,0 +1,476 @@
+"""Benchmark of the GB300 chunk-parallel KDA forward pass.
+
+One step = one full forward pass (every kernel of the path) over the
+long-context workload B=1, T=65536, H=HV=32, K=V=128, chunk 64, bf16, safe gate
+(lower_bound -5), on synthetic seeded inputs already resident in HBM.  Inputs
+(2.7 GB per step) are larger than L2 (129 MB), so no L2 flush is needed between
+steps.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun), every rank runs its own replica of the workload on its
+own GPU (weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the max over ranks is reported.  ``--impl reference``
+times the CPU fp64 oracle on the host cores (rank 0 only), each step a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import platform
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from kimi_delta_attention_gate_gb300 import inputs as kin  # noqa: E402
+
+METRIC = "KDA chunk fwd tokens/s at T=64K,H=32,K=V=128 bf16; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def elem(dtype: str) -> int:
+    return 2 if dtype == "bf16" else 4
+
+
+def essential_bytes(inp: kin.Inputs) -> float:
+    """Bytes the method must move: q, k, v, g, beta read once, o written once, plus
+    the initial / final state and the gate parameters."""
+    wl = inp.wl
+    e = elem(wl.dtype)
+    ntok = inp.n_tokens
+    per_tok = e * (2 * wl.H * wl.K + wl.HV * (wl.V + wl.K + 1) + wl.HV * wl.V)
+    state = inp.N * wl.HV * wl.K * wl.V * 4 * ((inp.h0 is not None) + 1)
+    params = 4 * wl.HV * (1 + wl.K)
+    return float(ntok * per_tok + state + params)
+
+
+def dense_flops(inp: kin.Inputs) -> float:
+    """2C(3K+2V) + 6KV flops per token per value head (chunk tiles counted dense)."""
+    wl = inp.wl
+    C, K, V = wl.chunk_size, wl.K, wl.V
+    return float(inp.n_tokens * wl.HV * (2 * C * (3 * K + 2 * V) + 6 * K * V))
+
+
+def stage_bytes(name: str, inp: kin.Inputs, p, lib) -> float:
+    """Algorithmic bytes of one launch of the named stage."""
+    wl = inp.wl
+    e = elem(wl.dtype)
+    ntok = inp.n_tokens
+    C, K, V, H, HV = wl.chunk_size, wl.K, wl.V, wl.H, wl.HV
+    lens = np.diff(inp.cu_seqlens) if inp.cu_seqlens is not None else np.full(wl.B, wl.T)
+    nct = int(np.sum((lens + C - 1) // C))
+    inter = nct * HV * (4 * (C * (3 * K + V + C) + K))
+    state = inp.N * HV * K * V * 4
+    if name == "simt_intra":
+        return float(ntok * (e * (2 * H * K + HV * (K + V + 1))) + 4 * HV * (1 + K) + inter)
+    if name == "simt_recur":
+        return float(inter + ntok * HV * V * e + state * ((inp.h0 is not None) + 1))
+    if name == "chunk_table":
+        return float(16 * (inp.N + 1))
+    return essential_bytes(inp)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "kimi_delta_attention_gate_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(stage: str, workload: str):
+    """DRAM bytes per launch of `stage` from a committed ncu summary, if it was taken
+    from the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{stage}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax, power = [], [], []
+        for _, parts in inside:
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                pass
+            for i, n in enumerate(names):
+                if parts[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "power_w_max": float(max(power)) if power else None,
+                "samples": len(inside), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ---------------------------------------------------------------------------------------
+
+def oracle_sample_time(inp: kin.Inputs, tokens: int, heads: int, nthreads: int):
+    """Time the oracle on the first `tokens` tokens of every sequence-0 head in
+    range(heads).  Returns seconds."""
+    import oracle
+    wl = inp.wl
+    sl = slice(0, tokens)
+    hs = slice(0, heads)
+    q = inp.q[:1, sl, hs]
+    k = inp.k[:1, sl, hs]
+    v = inp.v[:1, sl, hs]
+    g = inp.g[:1, sl, hs]
+    b = inp.beta[:1, sl, hs]
+    A_log = None if inp.A_log is None else inp.A_log[hs]
+    dt = None if inp.dt_bias is None else inp.dt_bias.reshape(wl.HV, wl.K)[hs].reshape(-1)
+    h0 = None if inp.h0 is None else inp.h0[:1, hs]
+    lb = wl.lower_bound if wl.gate == kin.GATE_SAFE else None
+    t = time.perf_counter()
+    oracle.fwd(q, k, v, g, b, A_log=A_log, dt_bias=dt, gate_mode=wl.gate, lower_bound=lb,
+               scale=inp.scale, initial_state=h0, nthreads=nthreads)
+    return time.perf_counter() - t
+
+
+def cpu_sample_plan(inp: kin.Inputs, target_s: float, nthreads: int):
+    """Pick a bounded oracle sample (all heads of the first sequence, a prefix of its
+    tokens) expected to take about target_s seconds; returns (tokens, heads)."""
+    wl = inp.wl
+    heads = min(wl.HV, max(1, nthreads)) if wl.H == wl.HV else wl.HV
+    probe = min(wl.T, 256)
+    dt = max(oracle_sample_time(inp, probe, heads, nthreads), 1e-4)
+    tokens = int(min(wl.T, max(probe, probe * target_s / dt)))
+    return tokens, heads
+
+
+def run_reference(args, wl):
+    """--impl reference: the oracle, as it stands, on the host cores."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    oracle.build()
+    inp = kin.make_inputs(wl)
+    nthreads = oracle.max_threads()
+    tokens, heads = cpu_sample_plan(inp, 4.0, nthreads)
+    for _ in range(args.warmup):
+        oracle_sample_time(inp, tokens, heads, nthreads)
+    times = [oracle_sample_time(inp, tokens, heads, nthreads) for _ in range(args.steps)]
+    tot = float(np.sum(times))
+    equiv_tokens = tokens * heads / wl.HV          # tokens of the full-head workload
+    value = equiv_tokens * args.steps / tot
+    sample = (f"oracle (C fp64 token recurrence, OpenMP) on {heads} of {wl.HV} heads x first "
+              f"{tokens} tokens of {wl.name} per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(inp, args),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads,
+                             "kind": "oracle", "sample": sample,
+                             "cpu": platform.processor() or platform.machine()},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(inp: kin.Inputs, args):
+    wl = inp.wl
+    return {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "HV": wl.HV, "K": wl.K,
+            "V": wl.V, "chunk_size": wl.chunk_size, "gate": {2: "safe", 1: "plain", 0: "pregated"}[wl.gate],
+            "lower_bound": wl.lower_bound, "tokens_per_step": inp.n_tokens,
+            "l2_flush": ("none: inputs per step (%.2f GB) exceed L2 (129 MB)" % (essential_bytes(inp) / 1e9)
+                         if essential_bytes(inp) > 129e6 else
+                         "none: inputs fit in L2, warm-cache figure"),
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+# ---------------------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_bf16", choices=sorted(kin.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = kin.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import kimi_delta_attention_gate_gb300 as kda
+    from kimi_delta_attention_gate_gb300 import _binding as kb
+    from kimi_delta_attention_gate_gb300 import build as kbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    if rank == 0:
+        kbuild.build()
+    barrier()
+    kb.load()
+
+    # Inputs: each rank its own replica (seed offset by rank), uploaded once.
+    inp = kin.make_inputs(wl, seed=wl.seed + 1000 * rank)
+    dev = torch.device("cuda", local_rank)
+
+    def up(x, dtype):
+        if x is None:
+            return None
+        if dtype == "bf16":
+            return torch.from_numpy(kin.to_bf16_bits(x).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
+
+    q, k, v, g, b = (up(x, wl.dtype) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    A_log, dt_bias, h0 = (up(x, "f32") for x in (inp.A_log, inp.dt_bias, inp.h0))
+    cu = cu_cpu = None
+    if inp.cu_seqlens is not None:
+        cu_cpu = torch.from_numpy(inp.cu_seqlens)
+        cu = cu_cpu.to(dev)
+    N = inp.N
+    o = torch.zeros((wl.B, wl.T, wl.HV, wl.V), dtype=v.dtype, device=dev)
+    fs = torch.empty((N, wl.HV, wl.K, wl.V), dtype=torch.float32, device=dev)
+    gate = {} if wl.gate == kin.GATE_PLAIN else ({"use_gate_in_kernel": False}
+                                                  if wl.gate == kin.GATE_PREGATED
+                                                  else {"lower_bound": wl.lower_bound})
+    p = kda.make_params(q, k, v, g, b, A_log=A_log, dt_bias=dt_bias, scale=inp.scale,
+                        initial_state=h0, final_state=fs, o=o, cu_seqlens=cu, cu_seqlens_cpu=cu_cpu,
+                        chunk_size=wl.chunk_size, **gate)
+    kb.raise_for(kb.kda_fwd_check(p))
+    ws = torch.empty(max(kb.kda_fwd_workspace_size(p), 1), dtype=torch.uint8, device=dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    nst = kb.kda_fwd_num_stages(p)
+    names = [kb.kda_fwd_stage_name(p, i) for i in range(nst)]
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step(evs=None):
+        for i in range(nst):
+            kb.raise_for(kb.kda_fwd_stage(p, sh, i))
+            if evs is not None:
+                evs[i].record(stream)
+
+    sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else local_rank)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = kb.kda_get_device_status(sh)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+
+    # Timed region: K steps, events after every stage on the launching stream.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for s_ in range(args.steps):
+        step(evs[s_])
+    barrier_ev = evs[-1][-1]
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    clocks = sampler.stop(t_wall0, t_wall1)
+    total_ms = start.elapsed_time(barrier_ev)
+    stage_ms = np.zeros(nst)
+    prev = start
+    for s_ in range(args.steps):
+        for i in range(nst):
+            stage_ms[i] += prev.elapsed_time(evs[s_][i])
+            prev = evs[s_][i]
+    stage_ms /= args.steps
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens_all = inp.n_tokens * world
+    value = tokens_all / (ms_per_step / 1e3)
+    status = kb.kda_get_device_status(sh)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} after the timed region")
+
+    # End to end through the public API: pinned host inputs -> device -> kda_fwd -> host.
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 10))
+    pin = lambda t: t.cpu().pin_memory()
+    hq, hk, hv_, hg, hb = (pin(x) for x in (q, k, v, g, b))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hfs = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+    dq, dk, dv, dg, db = (torch.empty_like(x) for x in (q, k, v, g, b))
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv_, hg, hb))
+    d2h = ho.numel() * ho.element_size() + hfs.numel() * hfs.element_size()
+
+    def e2e_step():
+        for d, h in ((dq, hq), (dk, hk), (dv, hv_), (dg, hg), (db, hb)):
+            d.copy_(h, non_blocking=True)
+        oo, ff = kda.kda_fwd(dq, dk, dv, dg, db, A_log=A_log, dt_bias=dt_bias, scale=inp.scale,
+                             initial_state=h0, cu_seqlens=cu, cu_seqlens_cpu=cu_cpu,
+                             chunk_size=wl.chunk_size, workspace=ws, o=o, final_state=fs,
+                             stream=stream, **gate)
+        ho.copy_(oo, non_blocking=True)
+        hfs.copy_(ff, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = tokens_all / (e2e_ms / 1e3)
+
+    # Roofline of the dominant kernel.
+    peaks, peak_kind = load_peaks()
+    dom = int(np.argmax(stage_ms))
+    dom_bytes = stage_bytes(names[dom], inp, p, kb)
+    achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    roofline = {"kernel": names[dom], "bound": "hbm", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                "bytes_per_launch": dom_bytes, "ms_per_launch": float(stage_ms[dom]),
+                "traffic": profiled_traffic(names[dom], wl.name)}
+    ess = essential_bytes(inp)
+    flops = dense_flops(inp)
+    t_roof = max(ess / (peak * 1e9), flops / (float(peaks["bf16_tflops"]) * 1e12))
+    path = {"essential_bytes": ess, "dense_flops": flops,
+            "achieved_gbs": ess / (ms_per_step / 1e3) / 1e9,
+            "tflops": flops / (ms_per_step / 1e3) / 1e12,
+            "roofline_ms": 1e3 * t_roof,
+            "frac": (1e3 * t_roof) / ms_per_step}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic (seeded PCG64, shapes and distributions of the workload)",
+            "config": config_of(inp, args), "roofline": roofline, "path_roofline": path,
+            "stages": {n: float(t) for n, t in zip(names, stage_ms)},
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+            "gpu_launches": int(nst * args.steps), "clocks": clocks,
+            "kernel_source_sha": kernel_source_hash()}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        nthreads = oracle.max_threads()
+        tokens, heads = cpu_sample_plan(inp, args.cpu_seconds, nthreads)
+        secs = oracle_sample_time(inp, tokens, heads, nthreads)
+        line["cpu_baseline"] = {
+            "value": tokens * heads / wl.HV / secs, "unit": "tokens/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{heads} of {wl.HV} heads x first {tokens} tokens of {wl.name} "
+                      f"({secs:.1f} s, C fp64 token recurrence, OpenMP)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,143 @@
+"""GB300 (sm_103a) chunk-parallel Kimi Delta Attention forward pass.
+
+``kda_fwd`` takes PyTorch CUDA tensors, allocates the outputs and the
+workspace with PyTorch, fills the C parameter block and calls the C ABI
+(``include/kda.h``).  Every step of the computation runs in the library's own
+CUDA kernels; there is no CPU or PyTorch fallback.
+
+The keyword arguments follow FLA's ``chunk_kda`` ("FLA-KDA engineering notes",
+section 2.2; "Reading Notes: Implementation Notes for KDA in FLA", forward
+entry): ``use_gate_in_kernel`` selects the in-kernel gate, and with it
+``lower_bound`` given selects the safe gate
+``lower_bound * sigmoid(exp(A_log) * (g + dt_bias))``, otherwise the plain gate
+``-exp(A_log) * softplus(g + dt_bias)``.
+"""
+from __future__ import annotations
+
+from typing import Optional, Tuple
+
+from . import _binding
+from ._binding import (KDA_BF16, KDA_F32, KDA_GATE_PLAIN, KDA_GATE_PREGATED, KDA_GATE_SAFE,
+                       KdaError, kda_abi_version, kda_fwd_params, kda_get_device_status,
+                       kda_last_error, kda_status_string)
+
+__all__ = ["kda_fwd", "kda_fwd_workspace_size", "make_params", "KdaError", "kda_get_device_status",
+           "kda_last_error", "kda_status_string", "kda_abi_version", "KDA_GATE_SAFE",
+           "KDA_GATE_PLAIN", "KDA_GATE_PREGATED", "KDA_BF16", "KDA_F32"]
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _gate_mode(use_gate_in_kernel: bool, safe_gate: Optional[bool], lower_bound) -> int:
+    if not use_gate_in_kernel:
+        return KDA_GATE_PREGATED
+    if safe_gate and lower_bound is None:
+        raise ValueError("safe_gate=True needs lower_bound (-5 <= lower_bound < 0)")
+    if safe_gate is False and lower_bound is not None:
+        raise ValueError("lower_bound given with safe_gate=False")
+    return KDA_GATE_SAFE if lower_bound is not None else KDA_GATE_PLAIN
+
+
+def make_params(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None, scale=None,
+                initial_state=None, final_state=None, o=None, cu_seqlens=None,
+                cu_seqlens_cpu=None, chunk_size: int = 64, use_gate_in_kernel: bool = True,
+                safe_gate: Optional[bool] = None, use_qk_l2norm_in_kernel: bool = True,
+                use_beta_sigmoid_in_kernel: bool = True, workspace=None) -> kda_fwd_params:
+    """Fill a ``kda_fwd_params`` from tensors (no checks beyond shapes; the C layer checks)."""
+    import torch
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or g.dim() != 4 or beta.dim() != 3:
+        raise ValueError("expected q,k [B,T,H,K], v [B,T,HV,V], g [B,T,HV,K], beta [B,T,HV]")
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    if tuple(g.shape) != (B, T, HV, K) or tuple(beta.shape) != (B, T, HV) or v.shape[:2] != q.shape[:2]:
+        raise ValueError("g must be [B,T,HV,K] and beta [B,T,HV]")
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("q,k,v,g,beta must be bfloat16 or float32")
+    for name, t in (("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if t.dtype != dt:
+            raise ValueError(f"{name} must have q's dtype {dt}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("A_log", A_log),
+                    ("dt_bias", dt_bias), ("initial_state", initial_state)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    for name, t in (("A_log", A_log), ("dt_bias", dt_bias), ("initial_state", initial_state)):
+        if t is not None and t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32")
+    if A_log is not None and tuple(A_log.shape) != (HV,):
+        raise ValueError("A_log must be [HV]")
+    if dt_bias is not None and dt_bias.numel() != HV * K:
+        raise ValueError("dt_bias must be [HV*K] (or [HV, K])")
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if initial_state is not None and tuple(initial_state.shape) != (N, HV, K, V):
+        raise ValueError("initial_state must be [N,HV,K,V] float32")
+    p = kda_fwd_params()
+    p.B, p.T, p.H, p.HV, p.K, p.V = B, T, H, HV, K, V
+    p.chunk_size = int(chunk_size)
+    p.in_dtype = KDA_BF16 if dt == torch.bfloat16 else KDA_F32
+    p.gate_mode = _gate_mode(use_gate_in_kernel, safe_gate, lower_bound)
+    p.lower_bound = 0.0 if lower_bound is None else float(lower_bound)
+    p.scale = float(K ** -0.5 if scale is None else scale)
+    p.qk_l2norm = int(bool(use_qk_l2norm_in_kernel))
+    p.beta_sigmoid = int(bool(use_beta_sigmoid_in_kernel))
+    p.N = N
+    p.q, p.k, p.v, p.g, p.beta = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
+    p.A_log, p.dt_bias, p.h0 = _ptr(A_log), _ptr(dt_bias), _ptr(initial_state)
+    p.cu_seqlens = _ptr(cu_seqlens)
+    p.cu_seqlens_host = _ptr(cu_seqlens_cpu)
+    p.o, p.final_state = _ptr(o), _ptr(final_state)
+    if workspace is not None:
+        p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    return p
+
+
+def kda_fwd_workspace_size(p: kda_fwd_params) -> int:
+    return _binding.kda_fwd_workspace_size(p)
+
+
+def kda_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None, scale=None,
+            initial_state=None, output_final_state: bool = True, cu_seqlens=None,
+            cu_seqlens_cpu=None, chunk_size: int = 64, use_gate_in_kernel: bool = True,
+            safe_gate: Optional[bool] = None, use_qk_l2norm_in_kernel: bool = True,
+            use_beta_sigmoid_in_kernel: bool = True, workspace=None, o=None, final_state=None,
+            stream=None) -> Tuple["torch.Tensor", Optional["torch.Tensor"]]:
+    """Chunk-parallel KDA forward on the current CUDA device.  Returns (o, final_state).
+
+    o has v's dtype and shape [B,T,HV,V]; final_state is fp32 [N,HV,K,V] (None if
+    ``output_final_state`` is False).  With ``cu_seqlens`` (int64 [N+1], B == 1),
+    rows of o outside every sequence are zero.  Asynchronous on ``stream``
+    (default: the current PyTorch stream).
+    """
+    import torch
+    if not q.is_cuda:
+        raise ValueError("kda_fwd runs on CUDA tensors only")
+    if cu_seqlens is not None and cu_seqlens_cpu is None:
+        cu_seqlens_cpu = cu_seqlens.to("cpu")
+    if cu_seqlens_cpu is not None:
+        cu_seqlens_cpu = cu_seqlens_cpu.to(torch.int64).contiguous()
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        padded = cu_seqlens is not None and int(cu_seqlens_cpu[-1]) < B * T
+        o = (torch.zeros if padded else torch.empty)((B, T, HV, V), dtype=v.dtype, device=v.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, HV, K, V), dtype=torch.float32, device=v.device)
+    p = make_params(q, k, v, g, beta, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound,
+                    scale=scale, initial_state=initial_state, final_state=final_state, o=o,
+                    cu_seqlens=cu_seqlens, cu_seqlens_cpu=cu_seqlens_cpu, chunk_size=chunk_size,
+                    use_gate_in_kernel=use_gate_in_kernel, safe_gate=safe_gate,
+                    use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel,
+                    use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel)
+    _binding.raise_for(_binding.kda_fwd_check(p))
+    need = _binding.kda_fwd_workspace_size(p)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=v.device)
+    p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
+    if stream is None:
+        stream = torch.cuda.current_stream(v.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _binding.raise_for(_binding.kda_fwd(p, handle))
+    return o, final_state

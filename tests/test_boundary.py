@@ -1,0 +1,177 @@
+"""Host-only tests of the C ABI: the library builds and loads, exports every
+symbol the header declares, and every argument rule returns its status before
+any CUDA call.  No test here touches a GPU (fake, never-dereferenced pointers
+are only passed to the checking entry points)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from kimi_delta_attention_gate_gb300 import _binding as kb
+from kimi_delta_attention_gate_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kb.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_what_binding_expects():
+    assert declared_functions() == sorted(kb.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert kb.kda_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert kb.kda_status_string(s)
+    assert kb.kda_status_string(0) == "ok"
+
+
+def test_struct_layout_matches_header():
+    # int32 x 9, float x 2, int32 x 3 -> 56 bytes, then 13 pointers and a size_t
+    assert kb.kda_fwd_params.q.offset == 56
+    assert kb.kda_fwd_params.workspace_bytes.offset == 56 + 13 * 8
+    assert ctypes.sizeof(kb.kda_fwd_params) == 56 + 14 * 8
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced by the checks
+
+
+def valid_params(**over):
+    p = kb.kda_fwd_params()
+    p.B, p.T, p.H, p.HV, p.K, p.V = 2, 100, 2, 4, 128, 64
+    p.chunk_size = 64
+    p.in_dtype = kb.KDA_BF16
+    p.gate_mode = kb.KDA_GATE_SAFE
+    p.lower_bound = -5.0
+    p.scale = 128 ** -0.5
+    p.qk_l2norm = 1
+    p.beta_sigmoid = 1
+    p.N = 2
+    for f in ("q", "k", "v", "g", "beta", "o"):
+        setattr(p, f, FAKE)
+    for k_, v_ in over.items():
+        setattr(p, k_, v_)
+    return p
+
+
+def check(p):
+    return kb.kda_fwd_check(p)
+
+
+def test_valid_params_pass_and_have_workspace(lib):
+    p = valid_params()
+    assert check(p) == kb.KDA_OK
+    assert kb.kda_fwd_workspace_size(p) > 0
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(gate_mode=kb.KDA_GATE_PLAIN), kb.KDA_ERR_INVALID_ARG),            # A_log required
+    (dict(lower_bound=-5.5), kb.KDA_ERR_INVALID_ARG),                        # lb >= -5
+    (dict(lower_bound=0.0), kb.KDA_ERR_INVALID_ARG),                         # lb < 0
+    (dict(lower_bound=float("nan")), kb.KDA_ERR_INVALID_ARG),
+    (dict(chunk_size=16), kb.KDA_ERR_SHAPE),                                 # 32 or 64 only
+    (dict(chunk_size=128), kb.KDA_ERR_SHAPE),
+    (dict(K=257), kb.KDA_ERR_SHAPE),                                         # K <= 256
+    (dict(V=257), kb.KDA_ERR_SHAPE),
+    (dict(HV=3), kb.KDA_ERR_SHAPE),                                          # HV % H == 0
+    (dict(in_dtype=7), kb.KDA_ERR_DTYPE),
+    (dict(gate_mode=9), kb.KDA_ERR_INVALID_ARG),
+    (dict(q=0), kb.KDA_ERR_INVALID_ARG),                                     # NULL input
+    (dict(o=0), kb.KDA_ERR_INVALID_ARG),
+    (dict(k=FAKE + 4), kb.KDA_ERR_INVALID_ARG),                              # misaligned
+    (dict(dt_bias=FAKE + 8), kb.KDA_ERR_INVALID_ARG),
+    (dict(N=3), kb.KDA_ERR_SHAPE),                                           # N == B without varlen
+    (dict(qk_l2norm=2), kb.KDA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), kb.KDA_ERR_INVALID_ARG),
+    (dict(B=0), kb.KDA_ERR_SHAPE),
+])
+def test_rule_rejections(lib, over, status):
+    p = valid_params(**over)
+    assert check(p) == status
+    assert kb.kda_last_error() != ""
+    assert kb.kda_fwd_workspace_size(p) == 0
+
+
+def test_plain_gate_with_alog_and_safe_without_alog_pass(lib):
+    assert check(valid_params(gate_mode=kb.KDA_GATE_PLAIN, A_log=FAKE)) == kb.KDA_OK
+    assert check(valid_params(gate_mode=kb.KDA_GATE_SAFE, A_log=0)) == kb.KDA_OK
+    assert check(valid_params(gate_mode=kb.KDA_GATE_PREGATED, lower_bound=0.0)) == kb.KDA_OK
+
+
+def cu_params(cu, T=200, **over):
+    arr = (ctypes.c_int64 * len(cu))(*cu)
+    p = valid_params(B=1, T=T, N=len(cu) - 1, cu_seqlens=FAKE, **over)
+    p.cu_seqlens_host = ctypes.addressof(arr)
+    return p, arr
+
+
+def test_varlen_rules(lib):
+    p, keep = cu_params([0, 5, 64, 200])
+    assert check(p) == kb.KDA_OK
+    p, keep = cu_params([0, 5, 64, 201])
+    assert check(p) == kb.KDA_ERR_SHAPE                                       # beyond T
+    p, keep = cu_params([0, 70, 64, 100])
+    assert check(p) == kb.KDA_ERR_SHAPE                                       # decreasing
+    p, keep = cu_params([1, 5, 64, 100])
+    assert check(p) == kb.KDA_ERR_SHAPE                                       # must start at 0
+    p, keep = cu_params([0, 5, 64, 100])
+    p.B = 2
+    assert check(p) == kb.KDA_ERR_SHAPE                                       # B == 1
+    p, keep = cu_params([0, 5, 64, 100])
+    p.cu_seqlens_host = None
+    assert check(p) == kb.KDA_ERR_INVALID_ARG                                 # host copy needed
+
+
+def test_workspace_grows_with_chunks(lib):
+    a = kb.kda_fwd_workspace_size(valid_params(T=64))
+    b = kb.kda_fwd_workspace_size(valid_params(T=65))
+    assert b > a > 0
+    p, keep = cu_params([0, 1, 2, 3], T=3)
+    c = kb.kda_fwd_workspace_size(p)
+    assert c > 0
+
+
+def test_fwd_rejects_small_workspace_before_cuda(lib):
+    p = valid_params()
+    p.workspace = FAKE
+    p.workspace_bytes = 16
+    assert kb.kda_fwd(p, 0) == kb.KDA_ERR_WORKSPACE
+    p.workspace_bytes = kb.kda_fwd_workspace_size(p)
+    p.workspace = FAKE + 16
+    assert kb.kda_fwd(p, 0) == kb.KDA_ERR_WORKSPACE                           # 256-byte alignment
+
+
+def test_fwd_without_gpu_reports_cuda_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("would launch on fake pointers; only meaningful without a GPU")
+    p = valid_params()
+    p.workspace = FAKE
+    p.workspace_bytes = kb.kda_fwd_workspace_size(p)
+    assert kb.kda_fwd(p, 0) == kb.KDA_ERR_CUDA
+
+
+def test_python_wrapper_gate_selection():
+    from kimi_delta_attention_gate_gb300 import _gate_mode
+    assert _gate_mode(False, None, None) == kb.KDA_GATE_PREGATED
+    assert _gate_mode(True, None, -5.0) == kb.KDA_GATE_SAFE
+    assert _gate_mode(True, None, None) == kb.KDA_GATE_PLAIN
+    with pytest.raises(ValueError):
+        _gate_mode(True, True, None)

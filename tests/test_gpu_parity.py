@@ -1,0 +1,136 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs.  Tolerances on o and final_state: bf16 inputs rel-L2 <= 5e-3
+and max-abs <= 3e-2; fp32 inputs rel-L2 <= 1e-4."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+from kimi_delta_attention_gate_gb300 import inputs as kin
+
+from kda_testlib import assert_close, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from kimi_delta_attention_gate_gb300 import build
+    build.build()
+
+
+def small(name="s", *, B=1, T=100, H=2, HV=2, K=64, V=64, C=64, dtype="bf16",
+          gate=kin.GATE_SAFE, lb=-5.0, h0=0.1, varlen=0, maxlen=0, seed=7, dt=True, alog=True):
+    return kin.Workload(name, B=B, T=T, H=H, HV=HV, K=K, V=V, chunk_size=C, dtype=dtype, gate=gate,
+                        lower_bound=lb if gate == kin.GATE_SAFE else None, h0_std=h0,
+                        varlen_n=varlen, varlen_max_len=maxlen, seed=seed, has_dt_bias=dt,
+                        has_a_log=alog, a_log_mean=-1.0 if gate == kin.GATE_PLAIN else 0.0,
+                        a_log_std=0.5 if gate == kin.GATE_PLAIN else 1.0)
+
+
+def check_case(wl, chunk_size=None, heads=None):
+    inp = kin.make_inputs(wl)
+    o, fs = run_gpu(inp, chunk_size=chunk_size)
+    ro, rfs = run_oracle(inp, heads=heads)
+    if heads is not None:
+        o, fs = o[:, :, heads], fs[:, heads]
+    assert_close(o, ro, wl.dtype, "o")
+    assert_close(fs, rfs, wl.dtype, "final_state")
+
+
+# ---- the five workloads --------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "equal_bf16", "gva_bf16", "varlen_bf16"])
+def test_workload_full(name):
+    check_case(kin.WORKLOADS[name])
+
+
+def test_long_bf16_sampled_heads():
+    """T=65536, H=32: the full launch, compared on sampled value heads."""
+    check_case(kin.WORKLOADS["long_bf16"], heads=[0, 13, 31])
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "equal_bf16"])
+def test_workload_chunk32(name):
+    check_case(kin.WORKLOADS[name], chunk_size=32)
+
+
+# ---- edge cases -----------------------------------------------------------------------
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 130])
+@pytest.mark.parametrize("C", [32, 64])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_ragged_lengths(T, C, dtype):
+    check_case(small(T=T, C=C, dtype=dtype, seed=T * 3 + C))
+
+
+@pytest.mark.parametrize("gate", [kin.GATE_SAFE, kin.GATE_PLAIN, kin.GATE_PREGATED])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_gate_modes(gate, dtype):
+    wl = small(T=150, gate=gate, dtype=dtype, seed=40 + gate)
+    if gate == kin.GATE_PREGATED:
+        inp = kin.make_inputs(wl)
+        inp.g[:] = -np.abs(inp.g) * 0.5            # a non-positive log decay
+        o, fs = run_gpu(inp)
+        ro, rfs = run_oracle(inp)
+        assert_close(o, ro, dtype, "o")
+        assert_close(fs, rfs, dtype, "final_state")
+    else:
+        check_case(wl)
+
+
+def test_safe_gate_without_alog_and_dt_bias():
+    check_case(small(T=90, alog=False, dt=False, seed=51))
+
+
+@pytest.mark.parametrize("K,V", [(48, 40), (256, 256), (128, 32), (32, 200)])
+def test_head_dims(K, V):
+    check_case(small(T=80, K=K, V=V, seed=K + V))
+
+
+def test_gva_groups():
+    check_case(small(T=130, H=2, HV=6, seed=61))
+
+
+def test_varlen_with_empty_and_single_token_sequences():
+    wl = small(T=400, varlen=6, maxlen=120, seed=71)
+    inp = kin.make_inputs(wl)
+    inp.cu_seqlens[:] = np.array([0, 1, 1, 65, 66, 130, 300], dtype=np.int64)
+    o, fs = run_gpu(inp)
+    ro, rfs = run_oracle(inp)
+    assert_close(o, ro, "bf16", "o")
+    assert_close(fs, rfs, "bf16", "final_state")
+    assert np.all(o[:, 300:] == 0)
+
+
+def test_empty_sequence_axis():
+    """T = 0: nothing to compute; final_state equals the initial state."""
+    wl = small(T=0, seed=81)
+    inp = kin.make_inputs(wl)
+    o, fs = run_gpu(inp)
+    assert o.shape == (1, 0, 2, 64)
+    assert np.array_equal(fs, inp.h0.astype(np.float64))
+
+
+def test_resume_chaining_matches_one_call():
+    wl = small(T=200, dtype="f32", seed=91)
+    inp = kin.make_inputs(wl)
+    o, fs = run_gpu(inp)
+    a = dataclasses.replace(inp, q=inp.q[:, :77].copy(), k=inp.k[:, :77].copy(),
+                            v=inp.v[:, :77].copy(), g=inp.g[:, :77].copy(),
+                            beta=inp.beta[:, :77].copy(), wl=dataclasses.replace(wl, T=77))
+    oa, fa = run_gpu(a)
+    b = dataclasses.replace(inp, q=inp.q[:, 77:].copy(), k=inp.k[:, 77:].copy(),
+                            v=inp.v[:, 77:].copy(), g=inp.g[:, 77:].copy(),
+                            beta=inp.beta[:, 77:].copy(), h0=fa.astype(np.float32),
+                            wl=dataclasses.replace(wl, T=123))
+    ob, fb = run_gpu(b)
+    assert_close(np.concatenate([oa, ob], axis=1), o, "f32", "o")
+    assert_close(fb, fs, "f32", "final_state")
+
+
+def test_repeat_calls_are_deterministic():
+    inp = kin.make_inputs(small(T=100, seed=101))
+    o1, f1 = run_gpu(inp)
+    o2, f2 = run_gpu(inp)
+    assert np.array_equal(o1, o2) and np.array_equal(f1, f2)
