@@ -276,8 +276,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--T", type=int, default=None,
+                    help="override the workload's sequence length (small profiling captures)")
     args = ap.parse_args()
     wl = kin.WORKLOADS[args.workload]
+    if args.T is not None:
+        import dataclasses
+        wl = dataclasses.replace(wl, T=args.T, name=f"{wl.name}_T{args.T}")
 
     if args.impl == "reference":
         return run_reference(args, wl)
