@@ -126,6 +126,31 @@ const char* kda_fwd_stage_name(const kda_fwd_params* p, int32_t stage);
    put timing events between the kernels.  Same checks and errors as kda_fwd. */
 kda_status kda_fwd_stage(const kda_fwd_params* p, void* stream, int32_t stage);
 
+/* Size of the static device scratch that kda_fwd_noalloc uses: 32 MiB. */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* kda_fwd for callers that cannot allocate device memory.  The source pages
+   have no counterpart to this entry point.
+   Some callers cannot call cudaMalloc or hand the library a workspace: code that
+   runs where an allocator is unavailable or forbidden (inside a framework that
+   owns all device memory, a real-time loop that must not allocate, a plugin
+   with no allocator handle).  This entry point takes the same parameters as
+   kda_fwd, ignores p->workspace / p->workspace_bytes, and puts its scratch in a
+   library-owned static device array of KDA_NOALLOC_SCRATCH_BYTES bytes instead.
+   Every GPU that loads the library holds that array until the process exits.
+   It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+   - Sizes whose kda_fwd_workspace_size exceeds KDA_NOALLOC_SCRATCH_BYTES are
+     rejected with KDA_ERR_WORKSPACE and a message giving both sizes.
+   - The first call on each device looks up the array's device address
+     (cudaGetSymbolAddress) with that device current; make that first call
+     before any stream capture.
+   - All calls share the one array and it keeps the last call's contents.
+     Nothing in it needs to start at zero: every call writes each scratch
+     element it later reads.  Calls whose kernels overlap on the GPU (on
+     different streams, or from several host threads) race on the array: order
+     them on one stream or synchronise between them. */
+kda_status kda_fwd_noalloc(const kda_fwd_params* p, void* stream);
+
 /* Synchronises `stream`, returns the device status bits accumulated by earlier
    calls (KDA_DEV_*) and clears them.  0 means no kernel flagged anything. */
 uint32_t kda_get_device_status(void* stream);

@@ -193,6 +193,9 @@ kda_status prepare(const kda_fwd_params* p, FwdArgs& a) {
 }
 
 }  // namespace
+
+void set_last_error(const char* msg) { t_last_error = msg; }
+
 }  // namespace kda
 
 using namespace kda;

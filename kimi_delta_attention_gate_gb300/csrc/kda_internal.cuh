@@ -134,6 +134,9 @@ __device__ __forceinline__ bool seq_range(const FwdArgs& a, int n, int64_t& bos,
 // ---------------------------------------------------------------------------------------
 // Launchers (each returns the cudaError_t of its launch)
 // ---------------------------------------------------------------------------------------
+// Sets the message kda_last_error() returns on the calling thread.
+void set_last_error(const char* msg);
+
 cudaError_t launch_chunk_table(const FwdArgs& a, cudaStream_t s);
 size_t simt_inter_block_bytes(int C, int K, int V);
 cudaError_t launch_simt_intra(const FwdArgs& a, cudaStream_t s);
