@@ -131,7 +131,9 @@ Plan make_plan(const kda_fwd_params* p) {
   pl.off_chunk_table = off;
   if (pl.varlen) off += round_up(sizeof(int64_t) * (size_t)(p->N + 1), 256);
   pl.off_inter = off;
-  pl.inter_block_bytes = simt_inter_block_bytes(pl.C, pl.K, pl.V);
+  pl.tensor_core = tc_eligible(pl, p->in_dtype);
+  pl.inter_block_bytes =
+      pl.tensor_core ? tc_inter_block_bytes() : simt_inter_block_bytes(pl.C, pl.K, pl.V);
   off += pl.inter_block_bytes * (size_t)pl.nct * (size_t)pl.HV;
   pl.total_bytes = off;
   return pl;
@@ -161,8 +163,13 @@ struct Stage {
 int stages_for(const Plan& pl, Stage* out) {
   int n = 0;
   if (pl.varlen) out[n++] = {"chunk_table", launch_chunk_table};
-  out[n++] = {"simt_intra", launch_simt_intra};
-  out[n++] = {"simt_recur", launch_simt_recur};
+  if (pl.tensor_core) {
+    out[n++] = {"tc_intra", launch_tc_intra};
+    out[n++] = {"tc_recur", launch_tc_recur};
+  } else {
+    out[n++] = {"simt_intra", launch_simt_intra};
+    out[n++] = {"simt_recur", launch_simt_recur};
+  }
   return n;
 }
 

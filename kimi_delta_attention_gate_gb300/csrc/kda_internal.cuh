@@ -23,6 +23,7 @@ struct Plan {
   size_t off_chunk_table;   // int64 [N + 1] chunk offsets (varlen only)
   size_t off_inter;         // per chunk-head intermediates
   size_t inter_block_bytes; // bytes per (chunk, value head)
+  bool tensor_core;         // bf16 tensor-core kernels (else the fp32 CUDA-core kernels)
   size_t total_bytes;
 };
 
@@ -141,5 +142,11 @@ cudaError_t launch_chunk_table(const FwdArgs& a, cudaStream_t s);
 size_t simt_inter_block_bytes(int C, int K, int V);
 cudaError_t launch_simt_intra(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_simt_recur(const FwdArgs& a, cudaStream_t s);
+
+// bf16 tensor-core path (K = V = 128, chunk 64)
+bool tc_eligible(const Plan& p, int dtype);
+size_t tc_inter_block_bytes();
+cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_tc_recur(const FwdArgs& a, cudaStream_t s);
 
 }  // namespace kda

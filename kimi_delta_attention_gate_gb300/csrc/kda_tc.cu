@@ -1,0 +1,775 @@
+// bf16 tensor-core path of the KDA chunk forward (K = V = 128, chunk 64).
+//
+// Two kernels exchange, per (chunk, value head), one packed block laid out exactly
+// as the recurrence kernel's shared-memory MMA operands (128-byte-swizzled panels):
+//
+//   tc_intra  one CTA per (chunk, value head), all chunks in parallel.
+//             "Reading Notes: Implementation Notes for KDA in FLA", forward steps 1-3:
+//             gate activation + chunk-local cumsum (log2 units), q/k L2 norm, beta
+//             sigmoid; Aqk and Akk by tcgen05 MMAs; A = (I + Akk)^-1 by blocked
+//             forward substitution; W = A Diag(beta) (e^Gamma . K) by a tcgen05 MMA;
+//             Qg, Kg^T, e^gamma_C.
+//   tc_recur  one CTA per (sequence, value head, 64-wide V tile), chunks in order.
+//             Steps 4-5 in transposed form so that the MMA M dimension is the V tile:
+//               V_new^T = V^T T^T - S^T W^T          (T = A Diag(beta))
+//               O^T     = S^T Qg^T + V_new^T Aqk^T
+//               S^T     = S^T Diag(e^gamma_C) + V_new^T Kg
+//             S^T stays in registers in fp32 and is rounded to bf16 only as an MMA
+//             operand.
+//
+// Exponent range (FLA-KDA engineering notes, section 3): the decay inside a chunk
+// reaches 2^-461 at lower_bound = -5, so (Q e^Gamma)(K e^-Gamma)^T cannot be formed
+// over a whole chunk.  Each 16-row block I uses its own reference r_I = Gamma just
+// before the block: the query side q_i 2^(Gamma_i - r_I) <= 1 and the key side
+// k_j 2^(r_I - Gamma_j), which is <= 1 for earlier blocks and at most 2^115 inside the
+// block at lower_bound = -5 (16 tokens x 5 nat), within the fp32/bf16 exponent range.
+// A block whose in-block decay exceeds 2^120 (possible only for the plain or
+// pre-gated gate) takes its diagonal 16 x 16 entries from an exact element-wise
+// evaluation instead.
+#include <cudaTypedefs.h>
+#include <stdio.h>
+
+#include "kda_internal.cuh"
+#include "tc_common.cuh"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+
+constexpr int TC_C = 64;
+constexpr int TC_K = 128;
+constexpr int TC_V = 128;
+constexpr int TC_BV = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kGuardLog2 = 120.0f;
+
+// Packed block (bytes).  All panels 1024-byte aligned within the block.
+constexpr uint32_t OFF_QG = 0;        // Qg   [64 tokens x 128 ch]  2 panels of 64 rows
+constexpr uint32_t OFF_W = 16384;     // W    [64 tokens x 128 ch]  2 panels of 64 rows
+constexpr uint32_t OFF_KGT = 32768;   // Kg^T [128 ch x 64 tokens]  1 panel of 128 rows
+constexpr uint32_t OFF_AQK = 49152;   // Aqk  [64 x 64]             1 panel
+constexpr uint32_t OFF_T = 57344;     // T = A Diag(beta) [64 x 64] 1 panel
+constexpr uint32_t OFF_D = 65536;     // e^gamma_C  fp32 [128]
+constexpr uint32_t BLOCK_BYTES = 66048;
+constexpr uint32_t BLOCK_SLOT = 66560;  // 1024-aligned slot in shared memory
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t ldg_u32(const void* p) {
+  return __ldg(reinterpret_cast<const unsigned int*>(p));
+}
+__device__ __forceinline__ void sts_u32(uint8_t* base, uint32_t off, uint32_t v) {
+  *reinterpret_cast<uint32_t*>(base + off) = v;
+}
+__device__ __forceinline__ void sts_u16(uint8_t* base, uint32_t off, float v) {
+  *reinterpret_cast<__nv_bfloat16*>(base + off) = __float2bfloat16_rn(v);
+}
+__device__ __forceinline__ void sts_v4(uint8_t* base, uint32_t off, uint32_t a, uint32_t b,
+                                       uint32_t c, uint32_t d) {
+  *reinterpret_cast<uint4*>(base + off) = make_uint4(a, b, c, d);
+}
+// sigmoid through ex2 / rcp: absolute error ~1e-7, far below bf16 resolution
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  return __frcp_rn(1.0f + ex2(-x * kLog2e));
+}
+__device__ __forceinline__ float softplus_fast(float x) {
+  return x > 20.0f ? x : log1pf(ex2(x * kLog2e));
+}
+template <int GATE>
+__device__ __forceinline__ float gate_fast(float x, float a, float lb) {
+  if (GATE == KDA_GATE_PLAIN) return -a * softplus_fast(x);
+  if (GATE == KDA_GATE_SAFE) return lb * sigmoid_fast(a * x);
+  return x;
+}
+
+// ======================================================================================
+// tc_intra
+// ======================================================================================
+constexpr uint32_t P_QSKS = 0;       // [Qs;Ks] A operand: 128 rows x 128 ch, 2 panels x 16 KB
+constexpr uint32_t P_KA = 32768;     // Ka_0..Ka_3 B operands (16/32/48/64 rows x 128 ch); later solve
+constexpr uint32_t P_XT = 73728;     // X^T [128 ch x 64 tokens] A operand of the W MMA
+constexpr uint32_t P_OUT = 90112;    // packed block
+constexpr uint32_t P_BETA = P_OUT + BLOCK_BYTES;  // fp32 [64]
+constexpr uint32_t P_BSUM = P_BETA + 256;         // fp32 [4][128] block sums of the gate
+constexpr uint32_t P_ROWSQ = P_BSUM + 2048;       // fp32 [64 rows][2 halves][2 (q,k)]
+constexpr uint32_t P_DIAG = P_ROWSQ + 1024;       // fp32 [4][2][16][16] exact diagonal blocks
+constexpr uint32_t P_DT = P_DIAG + 8192;          // fp32 [128] dt_bias row
+constexpr uint32_t P_FLAG = P_DT + 512;
+constexpr uint32_t P_BAR = P_FLAG + 16;
+constexpr uint32_t P_TMEM = P_BAR + 16;
+constexpr uint32_t P_END = P_TMEM + 16;
+constexpr uint32_t P_SMEM = P_END + 1024;
+// Ka_I (16(I+1) rows, 2 panels) offsets within P_KA: 0, 4096, 12288, 24576
+__host__ __device__ constexpr uint32_t ka_off(int I) { return 1024u * (uint32_t)(I * (I + 1) * 2); }
+// TMEM columns of the Aqk/Akk accumulators D_I (16(I+1) columns each): 0, 32, 64, 128
+__host__ __device__ constexpr uint32_t d_col(int I) { return I < 3 ? 32u * (uint32_t)I : 128u; }
+constexpr uint32_t WT_COL = 192;
+constexpr int SOLVE_LD = 65;
+
+template <int GATE>
+__global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const Plan& p = a.plan;
+  const int64_t c = blockIdx.x;
+  const int hv = blockIdx.y;
+  const int h = hv / p.G;
+  int n, L;
+  int64_t t0;
+  if (!locate_chunk(a, c, n, t0, L)) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* sBeta = reinterpret_cast<float*>(sm + P_BETA);
+  float* sBsum = reinterpret_cast<float*>(sm + P_BSUM);
+  float* sRowsq = reinterpret_cast<float*>(sm + P_ROWSQ);
+  float* sDiag = reinterpret_cast<float*>(sm + P_DIAG);
+  float* sDt = reinterpret_cast<float*>(sm + P_DT);
+  int* sFlag = reinterpret_cast<int*>(sm + P_FLAG);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + P_BAR);
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + P_TMEM);
+  uint8_t* out = sm + P_OUT;
+
+  if (warp == 0) {
+    tmem_alloc(sTmem, 256);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+    sFlag[0] = 0;
+  }
+  for (int i = tid; i < 4 * 2 * 256; i += 256) sDiag[i] = 0.f;
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  // dt_bias row: one bulk copy, overlapped with the loads below
+  if (tid == 0 && a.dt_bias != nullptr && GATE != KDA_GATE_PREGATED) {
+    mbar_arrive_expect_tx(&bars[1], TC_K * 4);
+    bulk_g2s(sDt, a.dt_bias + (size_t)hv * TC_K, TC_K * 4, &bars[1]);
+  }
+
+  // ---- element-wise phase: thread = 16-row block rg x channel pair (c0, c0+1) ----
+  const int rg = tid >> 6, cp = tid & 63, c0 = 2 * cp;
+  const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(a.g);
+  const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.beta);
+  uint32_t q2[16], k2[16], g2[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int row = 16 * rg + r;
+    q2[r] = k2[r] = g2[r] = 0u;
+    if (row < L) {
+      const int64_t tok = t0 + row;
+      q2[r] = ldg_u32(gq + (tok * p.H + h) * TC_K + c0);
+      k2[r] = ldg_u32(gk + (tok * p.H + h) * TC_K + c0);
+      g2[r] = ldg_u32(gg + (tok * p.HV + hv) * TC_K + c0);
+    }
+  }
+  if (tid < TC_C) {
+    float b = 0.f;
+    if (tid < L) {
+      b = __bfloat162float(gb[(t0 + tid) * p.HV + hv]);
+      if (a.beta_sigmoid) b = sigmoid_fast(b);
+    }
+    sBeta[tid] = b;
+  }
+  const float lb = a.lower_bound;
+  const float aexp = (GATE != KDA_GATE_PREGATED && a.A_log != nullptr) ? expf(a.A_log[hv]) : 1.f;
+  float dt0 = 0.f, dt1 = 0.f;
+  if (a.dt_bias != nullptr && GATE != KDA_GATE_PREGATED) {
+    if (!mbar_wait(&bars[1], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
+    dt0 = sDt[c0];
+    dt1 = sDt[c0 + 1];
+  }
+  // gate + in-block cumsum (log2 units); G <= 0 for every non-positive gate
+  float G0[16], G1[16];
+  float acc0 = 0.f, acc1 = 0.f, span = 0.f;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    float g0 = 0.f, g1 = 0.f;
+    if (16 * rg + r < L) {
+      g0 = gate_fast<GATE>(bf_lo(g2[r]) + dt0, aexp, lb);
+      g1 = gate_fast<GATE>(bf_hi(g2[r]) + dt1, aexp, lb);
+    }
+    acc0 = fmaf(g0, kLog2e, acc0);
+    acc1 = fmaf(g1, kLog2e, acc1);
+    G0[r] = acc0;
+    G1[r] = acc1;
+    span = fmaxf(span, fmaxf(fabsf(acc0), fabsf(acc1)));
+  }
+  sBsum[rg * 128 + c0] = acc0;
+  sBsum[rg * 128 + c0 + 1] = acc1;
+  if (span > kGuardLog2) atomicOr(sFlag, 1 << rg);
+  // row sums of squares of q and k (each warp covers 64 channels of its block's rows)
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    float sq = bf_lo(q2[r]) * bf_lo(q2[r]) + bf_hi(q2[r]) * bf_hi(q2[r]);
+    float sk = bf_lo(k2[r]) * bf_lo(k2[r]) + bf_hi(k2[r]) * bf_hi(k2[r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    }
+    if (lane == 0) {
+      const int row = 16 * rg + r;
+      sRowsq[(row * 2 + (warp & 1)) * 2 + 0] = sq;
+      sRowsq[(row * 2 + (warp & 1)) * 2 + 1] = sk;
+    }
+  }
+  __syncthreads();
+
+  // ---- carries, norms, factors, operand tiles ----
+  float rI0[4], rI1[4];  // reference r_I = Gamma just before block I
+  rI0[0] = rI1[0] = 0.f;
+#pragma unroll
+  for (int b = 1; b < 4; ++b) {
+    rI0[b] = rI0[b - 1] + sBsum[(b - 1) * 128 + c0];
+    rI1[b] = rI1[b - 1] + sBsum[(b - 1) * 128 + c0 + 1];
+  }
+  const float gl0 = rI0[3] + sBsum[3 * 128 + c0];  // gamma_C (log2)
+  const float gl1 = rI1[3] + sBsum[3 * 128 + c0 + 1];
+  const float rb0 = rI0[rg], rb1 = rI1[rg];
+  const bool guard = (sFlag[0] >> rg) & 1;
+  const float erb0 = ex2(rb0), erb1 = ex2(rb1);
+  const float ekg0 = ex2(gl0 - rb0), ekg1 = ex2(gl1 - rb1);
+  if (rg == 0) {
+    float* dout = reinterpret_cast<float*>(out + OFF_D);
+    dout[c0] = ex2(gl0);
+    dout[c0 + 1] = ex2(gl1);
+  }
+  float qh0[16], qh1[16], kh0[16], kh1[16];
+  const uint32_t pan = (uint32_t)(c0 >> 6);  // panel of this channel pair
+  const uint32_t cc = (uint32_t)(c0 & 63);
+  float F0[4], F1[4];  // 2^(r_I - r_b) for the blocks I > rg that see this block's keys
+#pragma unroll
+  for (int I = 0; I < 4; ++I) {
+    F0[I] = (I > rg) ? ex2(rI0[I] - rb0) : 1.f;
+    F1[I] = (I > rg) ? ex2(rI1[I] - rb1) : 1.f;
+  }
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int row = 16 * rg + r;
+    float qn = a.scale, kn = 1.f;
+    if (a.qk_l2norm) {
+      const float sq = sRowsq[(row * 2) * 2 + 0] + sRowsq[(row * 2 + 1) * 2 + 0];
+      const float sk = sRowsq[(row * 2) * 2 + 1] + sRowsq[(row * 2 + 1) * 2 + 1];
+      qn *= rsqrtf(sq + 1e-6f);
+      kn = rsqrtf(sk + 1e-6f);
+    }
+    const float q0 = bf_lo(q2[r]) * qn, q1 = bf_hi(q2[r]) * qn;
+    const float k0 = bf_lo(k2[r]) * kn, k1 = bf_hi(k2[r]) * kn;
+    qh0[r] = q0; qh1[r] = q1; kh0[r] = k0; kh1[r] = k1;
+    const float P0 = ex2(G0[r]), P1 = ex2(G1[r]);     // 2^(Gamma - r_b) <= 1
+    // [Qs;Ks] rows: block rg's queries at 32rg + r, keys at 32rg + 16 + r
+    sts_u32(sm + P_QSKS + pan * 16384, sw128_offset(32 * rg + r, cc), pack_bf16x2(q0 * P0, q1 * P1));
+    sts_u32(sm + P_QSKS + pan * 16384, sw128_offset(32 * rg + 16 + r, cc),
+            pack_bf16x2(k0 * P0, k1 * P1));
+    // Qg (row-major) and X^T (transposed) share 2^Gamma = P 2^r_b
+    sts_u32(out + OFF_QG + pan * 8192, sw128_offset(row, cc),
+            pack_bf16x2(q0 * P0 * erb0, q1 * P1 * erb1));
+    sts_u16(sm + P_XT, sw128_offset(c0, row), k0 * P0 * erb0);
+    sts_u16(sm + P_XT, sw128_offset(c0 + 1, row), k1 * P1 * erb1);
+    if (!guard) {
+      const float E0 = ex2(-G0[r]), E1 = ex2(-G1[r]);  // 2^(r_b - Gamma) <= 2^120
+      const float ke0 = k0 * E0, ke1 = k1 * E1;
+#pragma unroll
+      for (int I = 0; I < 4; ++I) {
+        if (I < rg) continue;
+        sts_u32(sm + P_KA + ka_off(I) + pan * (2048u * (I + 1)), sw128_offset(row, cc),
+                pack_bf16x2(ke0 * F0[I], ke1 * F1[I]));
+      }
+      sts_u16(out + OFF_KGT, sw128_offset(c0, row), ke0 * ekg0);
+      sts_u16(out + OFF_KGT, sw128_offset(c0 + 1, row), ke1 * ekg1);
+    } else {
+      // every exponent below is <= 0; the diagonal block is evaluated exactly further down
+#pragma unroll
+      for (int I = 0; I < 4; ++I) {
+        if (I < rg) continue;
+        const float v0 = (I == rg) ? 0.f : k0 * ex2(rI0[I] - rb0 - G0[r]);
+        const float v1 = (I == rg) ? 0.f : k1 * ex2(rI1[I] - rb1 - G1[r]);
+        sts_u32(sm + P_KA + ka_off(I) + pan * (2048u * (I + 1)), sw128_offset(row, cc),
+                pack_bf16x2(v0, v1));
+      }
+      sts_u16(out + OFF_KGT, sw128_offset(c0, row), k0 * ex2(gl0 - rb0 - G0[r]));
+      sts_u16(out + OFF_KGT, sw128_offset(c0 + 1, row), k1 * ex2(gl1 - rb1 - G1[r]));
+    }
+  }
+  if (guard) {
+    // exact diagonal block: partial sums over this thread's two channels
+    float* dq = sDiag + rg * 512;
+    float* dk = dq + 256;
+    for (int i = 0; i < 16; ++i)
+      for (int j = 0; j <= i; ++j) {
+        const float e0 = ex2(G0[i] - G0[j]), e1 = ex2(G1[i] - G1[j]);
+        atomicAdd(&dq[i * 16 + j], qh0[i] * kh0[j] * e0 + qh1[i] * kh1[j] * e1);
+        atomicAdd(&dk[i * 16 + j], kh0[i] * kh0[j] * e0 + kh1[i] * kh1[j] * e1);
+      }
+  }
+  fence_async_smem();
+  __syncthreads();
+
+  // ---- Aqk / Akk: D_I = [Qs;Ks] Ka_I^T, M=128, N=16(I+1), K=128 ----
+  if (tid == 0) {
+    tc_fence_after();
+#pragma unroll
+    for (int I = 0; I < 4; ++I) {
+      const uint32_t idesc = idesc_bf16(128, 16 * (I + 1));
+      const uint32_t abase = smem_u32(sm + P_QSKS);
+      const uint32_t bbase = smem_u32(sm + P_KA + ka_off(I));
+      const uint32_t bpan = 2048u * (I + 1);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t ad = sdesc_sw128(abase + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(bbase + (ks >> 2) * bpan + (ks & 3) * 32, 16, 1024);
+        mma_bf16(tmem + d_col(I), ad, bd, idesc, ks > 0);
+      }
+    }
+    mma_commit(&bars[0]);
+  }
+  __syncwarp();
+  if (!mbar_wait(&bars[0], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
+  tc_fence_after();
+
+  // ---- epilogue A: warp w owns block w (lanes 0-15 query rows, 16-31 key rows) ----
+  float* sL = reinterpret_cast<float*>(sm + P_KA);  // Akk0 [64][65]; Ka no longer needed
+  float* sX = sL + 64 * SOLVE_LD;                   // (I + Akk0)^-1 [64][65]
+  if (warp < 4) {
+    const int w = warp;
+    const bool isk = lane >= 16;
+    const int i = 16 * w + (lane & 15);
+    const bool gw = (sFlag[0] >> w) & 1;
+    const float bi = sBeta[i];
+    const float* dg = sDiag + w * 512 + (isk ? 256 : 0) + (i - 16 * w) * 16;
+#pragma unroll
+    for (int cc4 = 0; cc4 < 4; ++cc4) {
+      uint32_t r[16];
+      if (cc4 <= w) {
+        tmem_ld16(tmem_addr(tmem, 32 * w, d_col(w) + 16 * cc4), r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) r[x] = 0u;
+      }
+      float vals[16];
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const int j = 16 * cc4 + x;
+        float v = __uint_as_float(r[x]);
+        if (gw && cc4 == w) v = dg[x];
+        const bool keep = isk ? (j < i) : (j <= i);
+        vals[x] = keep ? v : 0.f;
+      }
+      if (!isk) {
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          const int j0 = 16 * cc4 + 8 * hlf;
+          sts_v4(out + OFF_AQK, sw128_offset(i, j0),
+                 pack_bf16x2(vals[8 * hlf + 0], vals[8 * hlf + 1]),
+                 pack_bf16x2(vals[8 * hlf + 2], vals[8 * hlf + 3]),
+                 pack_bf16x2(vals[8 * hlf + 4], vals[8 * hlf + 5]),
+                 pack_bf16x2(vals[8 * hlf + 6], vals[8 * hlf + 7]));
+        }
+      }
+      // Akk0 rows written after the barrier below (sL aliases the Ka operands being read
+      // by nothing now, but keep the order explicit)
+      if (isk) {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) sL[i * SOLVE_LD + 16 * cc4 + x] = bi * vals[x];
+      }
+    }
+  } else {
+    for (int e = tid - 128; e < 64 * SOLVE_LD; e += 128) sX[e] = 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- solve: X = (I + Akk0)^-1, 16x16 blocks ----
+  float* sP = sDiag;  // scratch [3][16][16]
+  if (tid < 64) {
+    const int b = tid >> 4, col = tid & 15, base = 16 * b;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
+#pragma unroll
+    for (int i = 1; i < 16; ++i) {
+      float s = 0.f;
+#pragma unroll
+      for (int m = 0; m < i; ++m) s = fmaf(sL[(base + i) * SOLVE_LD + base + m], x[m], s);
+      x[i] = (i > col) ? -s : x[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sX[(base + i) * SOLVE_LD + base + col] = x[i];
+  }
+  __syncthreads();
+  for (int bi = 1; bi < 4; ++bi) {
+    for (int e = tid; e < bi * 256; e += 256) {
+      const int bj = e >> 8, r = (e >> 4) & 15, cc2 = e & 15;
+      float s = 0.f;
+      for (int m = 16 * bj; m < 16 * bi; ++m)
+        s = fmaf(sL[(16 * bi + r) * SOLVE_LD + m], sX[m * SOLVE_LD + 16 * bj + cc2], s);
+      sP[e] = s;
+    }
+    __syncthreads();
+    for (int e = tid; e < bi * 256; e += 256) {
+      const int bj = e >> 8, r = (e >> 4) & 15, cc2 = e & 15;
+      float s = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        s = fmaf(sX[(16 * bi + r) * SOLVE_LD + 16 * bi + m], sP[bj * 256 + m * 16 + cc2], s);
+      sX[(16 * bi + r) * SOLVE_LD + 16 * bj + cc2] = -s;
+    }
+    __syncthreads();
+  }
+  // T = X Diag(beta), bf16 row-major (also the B operand of the W MMA)
+  {
+    const int i = tid >> 2, j0 = (tid & 3) * 16;
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      float t[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const int j = j0 + 8 * hlf + x;
+        t[x] = (j <= i) ? sX[i * SOLVE_LD + j] * sBeta[j] : 0.f;
+      }
+      sts_v4(out + OFF_T, sw128_offset(i, j0 + 8 * hlf), pack_bf16x2(t[0], t[1]),
+             pack_bf16x2(t[2], t[3]), pack_bf16x2(t[4], t[5]), pack_bf16x2(t[6], t[7]));
+    }
+  }
+  fence_async_smem();
+  __syncthreads();
+
+  // ---- W^T = X^T T^T: M=128 channels, N=64 tokens, K=64 ----
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t idesc = idesc_bf16(128, 64);
+    const uint32_t abase = smem_u32(sm + P_XT), bbase = smem_u32(out + OFF_T);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem + WT_COL, sdesc_sw128(abase + ks * 32, 16, 1024),
+               sdesc_sw128(bbase + ks * 32, 16, 1024), idesc, ks > 0);
+    mma_commit(&bars[0]);
+  }
+  __syncwarp();
+  if (!mbar_wait(&bars[0], 1)) flag_status(a.status, KDA_DEV_TIMEOUT);
+  tc_fence_after();
+  if (warp < 4) {
+    const int kch = 32 * warp + lane;
+    uint8_t* wp = out + OFF_W + (kch >> 6) * 8192;
+#pragma unroll
+    for (int cc4 = 0; cc4 < 4; ++cc4) {
+      uint32_t r[16];
+      tmem_ld16(tmem_addr(tmem, 32 * warp, WT_COL + 16 * cc4), r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int x = 0; x < 16; ++x)
+        sts_u16(wp, sw128_offset(16 * cc4 + x, kch & 63), __uint_as_float(r[x]));
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    uint8_t* dst = reinterpret_cast<uint8_t*>(a.ws) + p.off_inter + ((size_t)c * p.HV + hv) * p.inter_block_bytes;
+    bulk_s2g(dst, out, BLOCK_BYTES);
+    bulk_commit();
+    bulk_wait0();
+  }
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ======================================================================================
+// tc_recur
+// ======================================================================================
+constexpr uint32_t R_RING = 0;                       // 2 packed blocks
+constexpr uint32_t R_VT = 2 * BLOCK_SLOT;            // 2 v tiles [64 tokens x 64 ch]
+constexpr uint32_t R_ST = R_VT + 2 * 8192;           // S^T bf16 [64 v x 128 ch], 2 panels
+constexpr uint32_t R_VN = R_ST + 16384;              // V_new^T bf16 [64 v x 64 tokens]
+constexpr uint32_t R_BAR = R_VN + 8192;              // full[2], mma
+constexpr uint32_t R_TMEM = R_BAR + 32;
+constexpr uint32_t R_END = R_TMEM + 16;
+constexpr uint32_t R_SMEM = R_END + 1024;
+constexpr uint32_t TM_U = 0, TM_O = 64, TM_S = 128;
+
+__global__ void __launch_bounds__(256, 1) tc_recur_kernel(const FwdArgs a,
+                                                          const __grid_constant__ CUtensorMap vmap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const Plan& p = a.plan;
+  const int HV = p.HV;
+  const int vt = (int)(blockIdx.x % 2);
+  const int hv = (int)((blockIdx.x / 2) % HV);
+  const int n = (int)(blockIdx.x / (2u * HV));
+  const int v0 = vt * TC_BV;
+  int64_t bos, eos, cfirst;
+  if (!seq_range(a, n, bos, eos, cfirst)) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + R_BAR);
+  uint64_t* mbar = full + 2;
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + R_TMEM);
+  if (warp == 0) {
+    tmem_alloc(sTmem, 256);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(mbar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  const int64_t nch = (eos - bos + TC_C - 1) / TC_C;
+  const uint8_t* blocks = reinterpret_cast<const uint8_t*>(a.ws) + p.off_inter;
+  const CUtensorMap* vmap_ptr = &vmap;  // generic address of the kernel parameter
+
+  auto issue = [&](int64_t ci, int stage) {
+    const int64_t cg = cfirst + ci;
+    mbar_arrive_expect_tx(&full[stage], BLOCK_BYTES + 8192);
+    bulk_g2s(sm + R_RING + stage * BLOCK_SLOT,
+             blocks + ((size_t)cg * HV + hv) * p.inter_block_bytes, BLOCK_BYTES, &full[stage]);
+    tma_load_3d(sm + R_VT + stage * 8192, vmap_ptr, v0, hv, (int32_t)(bos + ci * TC_C),
+                &full[stage]);
+  };
+
+  // thread -> state row v (lanes 0-15 of each warp; M=64 TMEM layout) and column half hh
+  const int q4 = warp & 3, hh = warp >> 2;
+  const bool active = lane < 16;
+  const int v = 16 * q4 + (lane & 15);
+  const size_t sbase = ((size_t)n * HV + hv) * (size_t)TC_K * TC_V;
+  float S[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j)
+    S[j] = (a.h0 != nullptr && active) ? a.h0[sbase + (size_t)(64 * hh + j) * TC_V + v0 + v] : 0.f;
+  auto store_state = [&]() {
+    if (!active) return;
+    uint8_t* st = sm + R_ST + hh * 8192;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+      sts_v4(st, sw128_offset(v, 8 * ch), pack_bf16x2(S[8 * ch + 0], S[8 * ch + 1]),
+             pack_bf16x2(S[8 * ch + 2], S[8 * ch + 3]), pack_bf16x2(S[8 * ch + 4], S[8 * ch + 5]),
+             pack_bf16x2(S[8 * ch + 6], S[8 * ch + 7]));
+  };
+  store_state();
+  if (tid == 0 && nch > 0) issue(0, 0);
+  fence_async_smem();
+  __syncthreads();
+
+  __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
+  uint32_t mphase = 0;
+  bool ok = true;
+  int64_t issued = nch > 0 ? 1 : 0;  // chunks whose loads were issued
+  for (int64_t ci = 0; ci < nch; ++ci) {
+    const int s = (int)(ci & 1);
+    const int64_t t0 = bos + ci * TC_C;
+    const int L = (int)((eos - t0) < TC_C ? (eos - t0) : TC_C);
+    uint8_t* blk = sm + R_RING + s * BLOCK_SLOT;
+    uint8_t* vtile = sm + R_VT + s * 8192;
+    if (tid == 0 && ci + 1 < nch) issue(ci + 1, s ^ 1);
+    if (ci + 1 < nch) issued = ci + 2;
+    if (!mbar_wait(&full[s], (uint32_t)((ci >> 1) & 1))) {
+      flag_status(a.status, KDA_DEV_TIMEOUT);
+      ok = false;
+    }
+    if (L < TC_C) {  // rows past the chunk's end belong to another sequence or padding
+      for (int e = tid; e < (TC_C - L) * 8; e += 256) {
+        const int row = L + e / 8, ch = e % 8;
+        sts_v4(vtile, row * 128 + ch * 16, 0u, 0u, 0u, 0u);
+      }
+      fence_async_smem();
+      __syncthreads();
+    }
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t vb = smem_u32(vtile), tb = smem_u32(blk + OFF_T);
+      const uint32_t sb = smem_u32(sm + R_ST), wb = smem_u32(blk + OFF_W),
+                     qb = smem_u32(blk + OFF_QG);
+      // U^T = V^T T^T  (A = v tile, MN-major)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + TM_U, sdesc_sw128(vb + ks * 2048, 8192, 1024),
+                 sdesc_sw128(tb + ks * 32, 16, 1024), idesc_bf16(64, 64, true), ks > 0);
+      // V_new^T = U^T - S^T W^T
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(tmem + TM_U, sdesc_sw128(sb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
+                 sdesc_sw128(wb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
+                 idesc_bf16(64, 64, false, false, true), 1);
+      // O^T = S^T Qg^T
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(tmem + TM_O, sdesc_sw128(sb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
+                 sdesc_sw128(qb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), idesc_bf16(64, 64),
+                 ks > 0);
+      mma_commit(mbar);
+    }
+    __syncwarp();
+    if (!mbar_wait(mbar, mphase)) {
+      flag_status(a.status, KDA_DEV_TIMEOUT);
+      ok = false;
+    }
+    mphase ^= 1;
+    tc_fence_after();
+    // epilogue 1: V_new^T -> bf16 operand tile
+    {
+      uint32_t r[32];
+      tmem_ld32(tmem_addr(tmem, 32 * q4, TM_U + 32 * hh), r);
+      tmem_wait_ld();
+      if (active) {
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+          sts_v4(sm + R_VN, sw128_offset(v, 32 * hh + 8 * ch),
+                 pack_bf16x2(__uint_as_float(r[8 * ch + 0]), __uint_as_float(r[8 * ch + 1])),
+                 pack_bf16x2(__uint_as_float(r[8 * ch + 2]), __uint_as_float(r[8 * ch + 3])),
+                 pack_bf16x2(__uint_as_float(r[8 * ch + 4]), __uint_as_float(r[8 * ch + 5])),
+                 pack_bf16x2(__uint_as_float(r[8 * ch + 6]), __uint_as_float(r[8 * ch + 7])));
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    ok = __syncthreads_and(ok);
+    if (tid == 0 && ok) {
+      tc_fence_after();
+      const uint32_t nb = smem_u32(sm + R_VN), ab = smem_u32(blk + OFF_AQK),
+                     kb = smem_u32(blk + OFF_KGT);
+      // O^T += V_new^T Aqk^T
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + TM_O, sdesc_sw128(nb + ks * 32, 16, 1024),
+                 sdesc_sw128(ab + ks * 32, 16, 1024), idesc_bf16(64, 64), 1);
+      // dS^T = V_new^T Kg
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + TM_S, sdesc_sw128(nb + ks * 32, 16, 1024),
+                 sdesc_sw128(kb + ks * 32, 16, 1024), idesc_bf16(64, 128), ks > 0);
+      mma_commit(mbar);
+    }
+    __syncwarp();
+    if (ok && !mbar_wait(mbar, mphase)) {
+      flag_status(a.status, KDA_DEV_TIMEOUT);
+      ok = false;
+    }
+    mphase ^= 1;
+    tc_fence_after();
+    // epilogue 2: S = Diag(e^gamma_C) S + dS, then O
+    {
+      const float* dec = reinterpret_cast<const float*>(blk + OFF_D) + 64 * hh;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t r[16];
+        tmem_ld16(tmem_addr(tmem, 32 * q4, TM_S + 64 * hh + 16 * c4), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          S[16 * c4 + x] = fmaf(dec[16 * c4 + x], S[16 * c4 + x], __uint_as_float(r[x]));
+      }
+      store_state();
+      uint32_t r[32];
+      tmem_ld32(tmem_addr(tmem, 32 * q4, TM_O + 32 * hh), r);
+      tmem_wait_ld();
+      if (active) {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int tt = 32 * hh + x;
+          if (tt < L)
+            go[((t0 + tt) * HV + hv) * (int64_t)TC_V + v0 + v] =
+                __float2bfloat16_rn(__uint_as_float(r[x]));
+        }
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    ok = __syncthreads_and(ok);
+    if (!ok) {
+      // a wait ran out: let the last issued copy land (bounded) before leaving
+      if (tid == 0 && issued > ci + 1) mbar_wait(&full[s ^ 1], (uint32_t)(((ci + 1) >> 1) & 1));
+      break;
+    }
+  }
+  if (a.final_state != nullptr && active && ok) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) a.final_state[sbase + (size_t)(64 * hh + j) * TC_V + v0 + v] = S[j];
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// Driver entry point for tensor-map encoding, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool tc_eligible(const Plan& p, int dtype) {
+  return dtype == KDA_BF16 && p.K == TC_K && p.V == TC_V && p.C == TC_C && p.ntok > 0;
+}
+
+size_t tc_inter_block_bytes() { return BLOCK_BYTES; }
+
+cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s) {
+  const Plan& p = a.plan;
+  if (p.nct == 0) return cudaSuccess;
+  const dim3 grid((unsigned)p.nct, (unsigned)p.HV);
+  cudaError_t e;
+#define KDA_LAUNCH_INTRA(G)                                                                  \
+  e = cudaFuncSetAttribute(tc_intra_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           (int)P_SMEM);                                                     \
+  if (e != cudaSuccess) return e;                                                            \
+  tc_intra_kernel<G><<<grid, 256, P_SMEM, s>>>(a);
+  if (a.gate_mode == KDA_GATE_SAFE) {
+    KDA_LAUNCH_INTRA(KDA_GATE_SAFE)
+  } else if (a.gate_mode == KDA_GATE_PLAIN) {
+    KDA_LAUNCH_INTRA(KDA_GATE_PLAIN)
+  } else {
+    KDA_LAUNCH_INTRA(KDA_GATE_PREGATED)
+  }
+#undef KDA_LAUNCH_INTRA
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_recur(const FwdArgs& a, cudaStream_t s) {
+  const Plan& p = a.plan;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  CUtensorMap vmap;
+  const cuuint64_t dims[3] = {(cuuint64_t)TC_V, (cuuint64_t)p.HV, (cuuint64_t)p.ntok};
+  const cuuint64_t strides[2] = {(cuuint64_t)TC_V * 2, (cuuint64_t)p.HV * TC_V * 2};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(tc_recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)R_SMEM);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((size_t)2 * p.HV * p.N));
+  tc_recur_kernel<<<grid, 256, R_SMEM, s>>>(a, vmap);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -134,3 +134,80 @@ def test_repeat_calls_are_deterministic():
     o1, f1 = run_gpu(inp)
     o2, f2 = run_gpu(inp)
     assert np.array_equal(o1, o2) and np.array_equal(f1, f2)
+
+
+# ---- bf16 tensor-core path (K = V = 128, chunk 64) ---------------------------------------
+
+def tc(**kw):
+    kw.setdefault("K", 128)
+    kw.setdefault("V", 128)
+    return small(**kw)
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 130, 300])
+def test_tc_ragged_lengths(T):
+    check_case(tc(T=T, seed=200 + T))
+
+
+@pytest.mark.parametrize("gate", [kin.GATE_SAFE, kin.GATE_PLAIN, kin.GATE_PREGATED])
+def test_tc_gate_modes(gate):
+    wl = tc(T=200, B=2, gate=gate, seed=300 + gate)
+    inp = kin.make_inputs(wl)
+    if gate == kin.GATE_PREGATED:
+        inp.g[:] = kin.round_to_bf16(-np.abs(inp.g) * 0.5)
+    o, fs = run_gpu(inp)
+    ro, rfs = run_oracle(inp)
+    assert_close(o, ro, "bf16", "o")
+    assert_close(fs, rfs, "bf16", "final_state")
+
+
+def test_tc_plain_gate_exact_diagonal_guard():
+    """A plain gate with exp(A_log) ~ 20 decays a 16-token block far beyond 2^120: the
+    diagonal blocks must come from the exact element-wise evaluation."""
+    wl = tc(T=160, gate=kin.GATE_PLAIN, seed=311)
+    inp = kin.make_inputs(wl)
+    inp.A_log[:] = 3.0
+    o, fs = run_gpu(inp)
+    ro, rfs = run_oracle(inp)
+    assert_close(o, ro, "bf16", "o")
+    assert_close(fs, rfs, "bf16", "final_state")
+
+
+def test_tc_safe_gate_at_lower_bound():
+    """Safe gate saturated at lower_bound = -5: 16 tokens decay by 2^-115 (the largest
+    in-block factor the block references must hold)."""
+    wl = tc(T=192, seed=321)
+    inp = kin.make_inputs(wl)
+    inp.g[:] = kin.round_to_bf16(np.abs(inp.g) + 4.0)
+    o, fs = run_gpu(inp)
+    ro, rfs = run_oracle(inp)
+    assert_close(o, ro, "bf16", "o")
+    assert_close(fs, rfs, "bf16", "final_state")
+
+
+def test_tc_gva_and_no_alog():
+    check_case(tc(T=130, H=2, HV=4, seed=331))
+    check_case(tc(T=90, alog=False, dt=False, seed=332))
+
+
+def test_tc_varlen_with_empty_and_single_token_sequences():
+    wl = tc(T=400, varlen=6, maxlen=120, seed=341)
+    inp = kin.make_inputs(wl)
+    inp.cu_seqlens[:] = np.array([0, 1, 1, 65, 66, 130, 300], dtype=np.int64)
+    o, fs = run_gpu(inp)
+    ro, rfs = run_oracle(inp)
+    assert_close(o, ro, "bf16", "o")
+    assert_close(fs, rfs, "bf16", "final_state")
+    assert np.all(o[:, 300:] == 0)
+
+
+def test_tc_path_is_selected():
+    import kimi_delta_attention_gate_gb300 as kda
+    from kimi_delta_attention_gate_gb300 import _binding as kb
+    import torch
+    q = torch.zeros((1, 64, 2, 128), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros((1, 64, 2, 128), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros((1, 64, 2), dtype=torch.bfloat16, device="cuda")
+    p = kda.make_params(q, q, v, v, b, lower_bound=-5.0, o=v)
+    names = [kb.kda_fwd_stage_name(p, i) for i in range(kb.kda_fwd_num_stages(p))]
+    assert names == ["tc_intra", "tc_recur"]
