@@ -88,6 +88,11 @@ def stage_bytes(name: str, inp: kin.Inputs, p, lib) -> float:
         return float(ntok * (e * (2 * H * K + HV * (K + V + 1))) + 4 * HV * (1 + K) + inter)
     if name == "simt_recur":
         return float(inter + ntok * HV * V * e + state * ((inp.h0 is not None) + 1))
+    tc_block = 66048  # packed per-(chunk, head) block of the tensor-core path
+    if name == "tc_intra":
+        return float(ntok * e * (2 * H * K + HV * (K + 1)) + 4 * HV * (1 + K) + nct * HV * tc_block)
+    if name == "tc_recur":
+        return float(nct * HV * tc_block + 2 * ntok * HV * V * e + state * ((inp.h0 is not None) + 1))
     if name == "chunk_table":
         return float(16 * (inp.N + 1))
     return essential_bytes(inp)
