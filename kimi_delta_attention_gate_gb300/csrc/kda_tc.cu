@@ -9,7 +9,7 @@
 //             sigmoid; Aqk and Akk by tcgen05 MMAs; A = (I + Akk)^-1 by blocked
 //             forward substitution; W = A Diag(beta) (e^Gamma . K) by a tcgen05 MMA;
 //             Qg, Kg^T, e^gamma_C.
-//   tc_recur  one CTA per (sequence, value head, 64-wide V tile), chunks in order.
+//   tc_recur  one CTA per (sequence, value head), chunks in order.
 //             Steps 4-5 in transposed form so that the MMA M dimension is the V tile:
 //               V_new^T = V^T T^T - S^T W^T          (T = A Diag(beta))
 //               O^T     = S^T Qg^T + V_new^T Aqk^T
@@ -40,19 +40,19 @@ using namespace tc;
 constexpr int TC_C = 64;
 constexpr int TC_K = 128;
 constexpr int TC_V = 128;
-constexpr int TC_BV = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kGuardLog2 = 120.0f;
 
 // Packed block (bytes).  All panels 1024-byte aligned within the block.
-constexpr uint32_t OFF_QG = 0;        // Qg   [64 tokens x 128 ch]  2 panels of 64 rows
-constexpr uint32_t OFF_W = 16384;     // W    [64 tokens x 128 ch]  2 panels of 64 rows
-constexpr uint32_t OFF_KGT = 32768;   // Kg^T [128 ch x 64 tokens]  1 panel of 128 rows
-constexpr uint32_t OFF_AQK = 49152;   // Aqk  [64 x 64]             1 panel
-constexpr uint32_t OFF_T = 57344;     // T = A Diag(beta) [64 x 64] 1 panel
-constexpr uint32_t OFF_D = 65536;     // e^gamma_C  fp32 [128]
+//   B1 = [W; -Qg]   [128 rows x 128 ch]: panel p (16 KB) holds channels 64p..64p+63,
+//                   rows 0-63 = W (tokens), rows 64-127 = -Qg (tokens)
+//   B2 = [Kg^T; Aqk] [192 rows x 64 tokens]: rows 0-127 = Kg^T (channels), 128-191 = Aqk
+//   T  = A Diag(beta) [64 x 64];  D = e^gamma_C fp32 [128]
+constexpr uint32_t OFF_B1 = 0;
+constexpr uint32_t OFF_B2 = 32768;
+constexpr uint32_t OFF_T = 57344;
+constexpr uint32_t OFF_D = 65536;
 constexpr uint32_t BLOCK_BYTES = 66048;
-constexpr uint32_t BLOCK_SLOT = 66560;  // 1024-aligned slot in shared memory
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -275,8 +275,8 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
     sts_u32(sm + P_QSKS + pan * 16384, sw128_offset(32 * rg + 16 + r, cc),
             pack_bf16x2(k0 * P0, k1 * P1));
     // Qg (row-major) and X^T (transposed) share 2^Gamma = P 2^r_b
-    sts_u32(out + OFF_QG + pan * 8192, sw128_offset(row, cc),
-            pack_bf16x2(q0 * P0 * erb0, q1 * P1 * erb1));
+    sts_u32(out + OFF_B1 + pan * 16384, sw128_offset(64 + row, cc),
+            pack_bf16x2(-q0 * P0 * erb0, -q1 * P1 * erb1));
     sts_u16(sm + P_XT, sw128_offset(c0, row), k0 * P0 * erb0);
     sts_u16(sm + P_XT, sw128_offset(c0 + 1, row), k1 * P1 * erb1);
     if (!guard) {
@@ -288,8 +288,8 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
         sts_u32(sm + P_KA + ka_off(I) + pan * (2048u * (I + 1)), sw128_offset(row, cc),
                 pack_bf16x2(ke0 * F0[I], ke1 * F1[I]));
       }
-      sts_u16(out + OFF_KGT, sw128_offset(c0, row), ke0 * ekg0);
-      sts_u16(out + OFF_KGT, sw128_offset(c0 + 1, row), ke1 * ekg1);
+      sts_u16(out + OFF_B2, sw128_offset(c0, row), ke0 * ekg0);
+      sts_u16(out + OFF_B2, sw128_offset(c0 + 1, row), ke1 * ekg1);
     } else {
       // every exponent below is <= 0; the diagonal block is evaluated exactly further down
 #pragma unroll
@@ -300,8 +300,8 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
         sts_u32(sm + P_KA + ka_off(I) + pan * (2048u * (I + 1)), sw128_offset(row, cc),
                 pack_bf16x2(v0, v1));
       }
-      sts_u16(out + OFF_KGT, sw128_offset(c0, row), k0 * ex2(gl0 - rb0 - G0[r]));
-      sts_u16(out + OFF_KGT, sw128_offset(c0 + 1, row), k1 * ex2(gl1 - rb1 - G1[r]));
+      sts_u16(out + OFF_B2, sw128_offset(c0, row), k0 * ex2(gl0 - rb0 - G0[r]));
+      sts_u16(out + OFF_B2, sw128_offset(c0 + 1, row), k1 * ex2(gl1 - rb1 - G1[r]));
     }
   }
   if (guard) {
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
 #pragma unroll
         for (int hlf = 0; hlf < 2; ++hlf) {
           const int j0 = 16 * cc4 + 8 * hlf;
-          sts_v4(out + OFF_AQK, sw128_offset(i, j0),
+          sts_v4(out + OFF_B2, sw128_offset(128 + i, j0),
                  pack_bf16x2(vals[8 * hlf + 0], vals[8 * hlf + 1]),
                  pack_bf16x2(vals[8 * hlf + 2], vals[8 * hlf + 3]),
                  pack_bf16x2(vals[8 * hlf + 4], vals[8 * hlf + 5]),
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
   tc_fence_after();
   if (warp < 4) {
     const int kch = 32 * warp + lane;
-    uint8_t* wp = out + OFF_W + (kch >> 6) * 8192;
+    uint8_t* wp = out + OFF_B1 + (kch >> 6) * 16384;
 #pragma unroll
     for (int cc4 = 0; cc4 < 4; ++cc4) {
       uint32_t r[16];
@@ -491,142 +491,238 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
 // ======================================================================================
 // tc_recur
 // ======================================================================================
-constexpr uint32_t R_RING = 0;                       // 2 packed blocks
-constexpr uint32_t R_VT = 2 * BLOCK_SLOT;            // 2 v tiles [64 tokens x 64 ch]
-constexpr uint32_t R_ST = R_VT + 2 * 8192;           // S^T bf16 [64 v x 128 ch], 2 panels
-constexpr uint32_t R_VN = R_ST + 16384;              // V_new^T bf16 [64 v x 64 tokens]
-constexpr uint32_t R_BAR = R_VN + 8192;              // full[2], mma
-constexpr uint32_t R_TMEM = R_BAR + 32;
+// One CTA per (sequence, value head) holds the whole V = 128.  Warps 0-7 are epilogue
+// warps (MMA M = 128: thread v of warp quadrant q owns state row v = 32q + lane; warps
+// q and q+4 split the key channels); warp 8 is the control warp: one thread issues every
+// MMA, bulk / tensor copy and L2 prefetch, and the roles meet on mbarriers.
+// Per chunk, two MMA groups share the tensor pipe:
+//   G1  D1 = V^T T^T (U^T, columns 0-63; issued as soon as the chunk's data lands), then
+//       D1 -= S^T [W; -Qg]^T over N = 128: columns 0-63 become V_new^T, columns 64-127
+//       S^T Qg^T                                                          (12 MMAs)
+//   G2  D2 = V_new^T [Kg^T; Aqk]^T over N = 192: columns 0-127 dS^T, 128-191
+//       V_new^T Aqk^T                                                      (4 MMAs)
+// The epilogue warps turn V_new^T into the G2 operand, update the fp32 state held in
+// registers (S^T = S^T Diag(e^gamma_C) + dS^T) into the next G1 operand, and, while the
+// next G1 runs, drain O^T = D1[:, 64:128] + D2[:, 128:192] through a shared-memory
+// staging tile with coalesced stores (D1 is double-buffered; its output half is cleared
+// with tcgen05.st after the drain).  Packed blocks and v tiles are prefetched into L2
+// four chunks ahead and copied into shared memory one chunk ahead.
+constexpr uint32_t SL_T = 57344;                     // within a slot (same offsets as the block)
+constexpr uint32_t SL_D = 65536;
+constexpr uint32_t SL_V = 66560;                     // v tile [64 tokens x 128 v], 2 MN panels
+constexpr uint32_t SLOT = 82944;
+constexpr uint32_t R_RING = 0;                       // 2 slots
+constexpr uint32_t R_ST = 2 * SLOT;                  // S^T bf16 [128 v x 128 ch], 2 K panels
+constexpr uint32_t R_VN = R_ST + 32768;              // V_new^T bf16 [128 v x 64 tokens]; O staging
+constexpr uint32_t R_BAR = R_VN + 16384;             // full[2], bar_v, bar_s, bar_vn, bar_st
+constexpr uint32_t R_TMEM = R_BAR + 64;
 constexpr uint32_t R_END = R_TMEM + 16;
 constexpr uint32_t R_SMEM = R_END + 1024;
-constexpr uint32_t TM_U = 0, TM_O = 64, TM_S = 128;
+constexpr uint32_t TM_D1 = 0, TM_D2 = 256;           // D1[b] at 128 b; D2 192 columns
+constexpr int kPrefetch = 4;     // chunks whose loads are prefetched into L2 ahead
+constexpr int kRecThreads = 288; // 8 epilogue warps + 1 control warp
+constexpr int kEpiThreads = 256;
 
-__global__ void __launch_bounds__(256, 1) tc_recur_kernel(const FwdArgs a,
-                                                          const __grid_constant__ CUtensorMap vmap) {
+__global__ void __launch_bounds__(kRecThreads, 1)
+    tc_recur_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const Plan& p = a.plan;
   const int HV = p.HV;
-  const int vt = (int)(blockIdx.x % 2);
-  const int hv = (int)((blockIdx.x / 2) % HV);
-  const int n = (int)(blockIdx.x / (2u * HV));
-  const int v0 = vt * TC_BV;
+  const int hv = (int)(blockIdx.x % HV);
+  const int n = (int)(blockIdx.x / HV);
   int64_t bos, eos, cfirst;
   if (!seq_range(a, n, bos, eos, cfirst)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + R_BAR);
-  uint64_t* mbar = full + 2;
+  uint64_t* bar_v = full + 2;
+  uint64_t* bar_s = full + 3;
+  uint64_t* bar_vn = full + 4;
+  uint64_t* bar_st = full + 5;
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + R_TMEM);
-  if (warp == 0) {
-    tmem_alloc(sTmem, 256);
+  if (warp == 8) {
+    tmem_alloc(sTmem, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    mbar_init(mbar, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&full[i], 1);
+    mbar_init(bar_vn, 8);
+    mbar_init(bar_st, 8);
     fence_mbar_init();
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sTmem;
   const int64_t nch = (eos - bos + TC_C - 1) / TC_C;
-  const uint8_t* blocks = reinterpret_cast<const uint8_t*>(a.ws) + p.off_inter;
-  const CUtensorMap* vmap_ptr = &vmap;  // generic address of the kernel parameter
-
-  auto issue = [&](int64_t ci, int stage) {
-    const int64_t cg = cfirst + ci;
-    mbar_arrive_expect_tx(&full[stage], BLOCK_BYTES + 8192);
-    bulk_g2s(sm + R_RING + stage * BLOCK_SLOT,
-             blocks + ((size_t)cg * HV + hv) * p.inter_block_bytes, BLOCK_BYTES, &full[stage]);
-    tma_load_3d(sm + R_VT + stage * 8192, vmap_ptr, v0, hv, (int32_t)(bos + ci * TC_C),
-                &full[stage]);
-  };
-
-  // thread -> state row v (lanes 0-15 of each warp; M=64 TMEM layout) and column half hh
-  const int q4 = warp & 3, hh = warp >> 2;
-  const bool active = lane < 16;
-  const int v = 16 * q4 + (lane & 15);
-  const size_t sbase = ((size_t)n * HV + hv) * (size_t)TC_K * TC_V;
-  float S[64];
-#pragma unroll
-  for (int j = 0; j < 64; ++j)
-    S[j] = (a.h0 != nullptr && active) ? a.h0[sbase + (size_t)(64 * hh + j) * TC_V + v0 + v] : 0.f;
-  auto store_state = [&]() {
-    if (!active) return;
-    uint8_t* st = sm + R_ST + hh * 8192;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-      sts_v4(st, sw128_offset(v, 8 * ch), pack_bf16x2(S[8 * ch + 0], S[8 * ch + 1]),
-             pack_bf16x2(S[8 * ch + 2], S[8 * ch + 3]), pack_bf16x2(S[8 * ch + 4], S[8 * ch + 5]),
-             pack_bf16x2(S[8 * ch + 6], S[8 * ch + 7]));
-  };
-  store_state();
-  if (tid == 0 && nch > 0) issue(0, 0);
-  fence_async_smem();
-  __syncthreads();
-
-  __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
-  uint32_t mphase = 0;
   bool ok = true;
-  int64_t issued = nch > 0 ? 1 : 0;  // chunks whose loads were issued
-  for (int64_t ci = 0; ci < nch; ++ci) {
-    const int s = (int)(ci & 1);
-    const int64_t t0 = bos + ci * TC_C;
-    const int L = (int)((eos - t0) < TC_C ? (eos - t0) : TC_C);
-    uint8_t* blk = sm + R_RING + s * BLOCK_SLOT;
-    uint8_t* vtile = sm + R_VT + s * 8192;
-    if (tid == 0 && ci + 1 < nch) issue(ci + 1, s ^ 1);
-    if (ci + 1 < nch) issued = ci + 2;
-    if (!mbar_wait(&full[s], (uint32_t)((ci >> 1) & 1))) {
-      flag_status(a.status, KDA_DEV_TIMEOUT);
-      ok = false;
-    }
-    if (L < TC_C) {  // rows past the chunk's end belong to another sequence or padding
-      for (int e = tid; e < (TC_C - L) * 8; e += 256) {
-        const int row = L + e / 8, ch = e % 8;
-        sts_v4(vtile, row * 128 + ch * 16, 0u, 0u, 0u, 0u);
+
+  if (warp == 8) {
+    // ---------------------------------- control warp ----------------------------------
+    if (lane == 0) {
+      const uint8_t* blocks = reinterpret_cast<const uint8_t*>(a.ws) + p.off_inter;
+      const CUtensorMap* vmap_ptr = &vmap;  // generic address of the kernel parameter
+      auto issue = [&](int64_t ci, int st) {  // chunk ci -> slot st
+        const int64_t cg = cfirst + ci;
+        uint8_t* dst = sm + R_RING + st * SLOT;
+        const uint8_t* src = blocks + ((size_t)cg * HV + hv) * p.inter_block_bytes;
+        mbar_arrive_expect_tx(&full[st], BLOCK_BYTES + 16384);
+        bulk_g2s(dst, src, 16384, &full[st]);
+        bulk_g2s(dst + 16384, src + 16384, 16384, &full[st]);
+        bulk_g2s(dst + 32768, src + 32768, 16384, &full[st]);
+        bulk_g2s(dst + 49152, src + 49152, BLOCK_BYTES - 49152, &full[st]);
+        tma_load_3d(dst + SL_V, vmap_ptr, 0, hv, (int32_t)(bos + ci * TC_C), &full[st]);
+        tma_load_3d(dst + SL_V + 8192, vmap_ptr, 64, hv, (int32_t)(bos + ci * TC_C), &full[st]);
+      };
+      auto prefetch = [&](int64_t ci) {
+        const int64_t cg = cfirst + ci;
+        bulk_prefetch_l2(blocks + ((size_t)cg * HV + hv) * p.inter_block_bytes, BLOCK_BYTES);
+        tma_prefetch_3d(vmap_ptr, 0, hv, (int32_t)(bos + ci * TC_C));
+        tma_prefetch_3d(vmap_ptr, 64, hv, (int32_t)(bos + ci * TC_C));
+      };
+      // wait for chunk ci's data, clear v rows past the chunk end, issue U^T into D1[ci&1]
+      auto issue_u = [&](int64_t ci) -> bool {
+        const int st = (int)(ci & 1);
+        if (!mbar_wait(&full[st], (uint32_t)((ci >> 1) & 1))) return false;
+        uint8_t* slot = sm + R_RING + st * SLOT;
+        const int64_t t0 = bos + ci * TC_C;
+        const int L = (int)((eos - t0) < TC_C ? (eos - t0) : TC_C);
+        if (L < TC_C) {  // those rows belong to another sequence or to padding
+          for (int e = L * 8; e < TC_C * 8; ++e) {
+            sts_v4(slot + SL_V, (uint32_t)e * 16u, 0u, 0u, 0u, 0u);
+            sts_v4(slot + SL_V + 8192, (uint32_t)e * 16u, 0u, 0u, 0u, 0u);
+          }
+          fence_async_smem();
+        }
+        tc_fence_after();
+        const uint32_t vb = smem_u32(slot + SL_V), tb = smem_u32(slot + SL_T);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + TM_D1 + 128 * (uint32_t)st, sdesc_sw128(vb + ks * 2048, 8192, 1024),
+                   sdesc_sw128(tb + ks * 32, 16, 1024), idesc_bf16(128, 64, true), ks > 0);
+        return true;
+      };
+      if (nch > 0) {
+        issue(0, 0);
+        for (int64_t d = 1; d <= kPrefetch && d < nch; ++d) prefetch(d);
+        if (!issue_u(0)) ok = false;
       }
-      fence_async_smem();
-      __syncthreads();
-    }
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t vb = smem_u32(vtile), tb = smem_u32(blk + OFF_T);
-      const uint32_t sb = smem_u32(sm + R_ST), wb = smem_u32(blk + OFF_W),
-                     qb = smem_u32(blk + OFF_QG);
-      // U^T = V^T T^T  (A = v tile, MN-major)
+      for (int64_t ci = 0; ci < nch && ok; ++ci) {
+        const int s = (int)(ci & 1);
+        uint8_t* slot = sm + R_RING + s * SLOT;
+        // G1: needs S^T of the previous chunk (and the initial clears for ci = 0)
+        if (!mbar_wait(bar_st, (uint32_t)(ci & 1))) { ok = false; break; }
+        tc_fence_after();
+        {
+          const uint32_t sb = smem_u32(sm + R_ST), b1 = smem_u32(slot + OFF_B1);
+          const uint32_t d1 = tmem + TM_D1 + 128 * (uint32_t)s;
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + TM_U, sdesc_sw128(vb + ks * 2048, 8192, 1024),
-                 sdesc_sw128(tb + ks * 32, 16, 1024), idesc_bf16(64, 64, true), ks > 0);
-      // V_new^T = U^T - S^T W^T
+          for (int ks = 0; ks < 8; ++ks)
+            mma_bf16(d1, sdesc_sw128(sb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                     sdesc_sw128(b1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                     idesc_bf16(128, 128, false, false, true), 1);
+          mma_commit(bar_v);
+        }
+        // slot s^1 (chunk ci-1) is free: its MMAs completed before its state update
+        if (ci + 1 < nch) issue(ci + 1, s ^ 1);
+        if (ci + 1 + kPrefetch < nch) prefetch(ci + 1 + kPrefetch);
+        // G2: needs V_new^T of this chunk (and the drain of chunk ci-1, which precedes it)
+        if (!mbar_wait(bar_vn, (uint32_t)(ci & 1))) { ok = false; break; }
+        tc_fence_after();
+        {
+          const uint32_t nb = smem_u32(sm + R_VN), b2 = smem_u32(slot + OFF_B2);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + TM_U, sdesc_sw128(sb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
-                 sdesc_sw128(wb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
-                 idesc_bf16(64, 64, false, false, true), 1);
-      // O^T = S^T Qg^T
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + TM_O, sdesc_sw128(sb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
-                 sdesc_sw128(qb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), idesc_bf16(64, 64),
-                 ks > 0);
-      mma_commit(mbar);
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + TM_D2, sdesc_sw128(nb + ks * 32, 16, 1024),
+                     sdesc_sw128(b2 + ks * 32, 16, 1024), idesc_bf16(128, 192), ks > 0);
+          mma_commit(bar_s);
+        }
+        if (ci + 1 < nch && !issue_u(ci + 1)) { ok = false; break; }
+      }
+      if (!ok) {
+        flag_status(a.status, KDA_DEV_TIMEOUT);
+        for (int st = 0; st < 2; ++st) mbar_wait(&full[st], 0, 100000000ull);
+      }
     }
     __syncwarp();
-    if (!mbar_wait(mbar, mphase)) {
-      flag_status(a.status, KDA_DEV_TIMEOUT);
-      ok = false;
-    }
-    mphase ^= 1;
-    tc_fence_after();
-    // epilogue 1: V_new^T -> bf16 operand tile
-    {
-      uint32_t r[32];
-      tmem_ld32(tmem_addr(tmem, 32 * q4, TM_U + 32 * hh), r);
-      tmem_wait_ld();
-      if (active) {
+  } else {
+    // --------------------------------- epilogue warps ---------------------------------
+    const int q4 = warp & 3, hh = warp >> 2;
+    const int v = 32 * q4 + lane;
+    const uint32_t lane_base = tmem_addr(tmem, 32 * q4, 0);
+    const size_t sbase = ((size_t)n * HV + hv) * (size_t)TC_K * TC_V;
+    float S[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+      S[j] = (a.h0 != nullptr) ? a.h0[sbase + (size_t)(64 * hh + j) * TC_V + v] : 0.f;
+    auto store_state = [&]() {
+      uint8_t* st = sm + R_ST + hh * 16384;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        sts_v4(st, sw128_offset(v, 8 * ch), pack_bf16x2(S[8 * ch + 0], S[8 * ch + 1]),
+               pack_bf16x2(S[8 * ch + 2], S[8 * ch + 3]), pack_bf16x2(S[8 * ch + 4], S[8 * ch + 5]),
+               pack_bf16x2(S[8 * ch + 6], S[8 * ch + 7]));
+    };
+    auto arrive = [&](uint64_t* bar) {  // one arrival per warp, after the warp's writes
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
+    __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
+    // O^T of chunk ci = D1[ci&1][64:128] + D2[128:192]: stage as [token][v] in the VN
+    // buffer, then coalesced 16-byte stores of the chunk's rows; clear D1's output half.
+    auto drain_o = [&](int64_t ci) -> bool {
+      const int64_t t0 = bos + ci * TC_C;
+      const int L = (int)((eos - t0) < TC_C ? (eos - t0) : TC_C);
+      const uint32_t d1 = TM_D1 + 128 * (uint32_t)(ci & 1) + 64 + 32 * hh;
+      uint8_t* stg = sm + R_VN;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r1[16], r2[16];
+        tmem_ld16(lane_base + d1 + 16 * half, r1);
+        tmem_ld16(lane_base + TM_D2 + 128 + 32 * hh + 16 * half, r2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int tt = 32 * hh + 16 * half + x;
+          *reinterpret_cast<__nv_bfloat16*>(stg + tt * 256 + v * 2) =
+              __float2bfloat16_rn(__uint_as_float(r1[x]) + __uint_as_float(r2[x]));
+        }
+      }
+      tmem_st32_zero(lane_base + d1);
+      tmem_wait_st();
+      tc_fence_before();
+      bool good = named_bar_and(1, kEpiThreads, true);
+      {
+        const int row = tid >> 2, c0 = (tid & 3) * 4;
+        if (row < L) {
+          const uint4* srow = reinterpret_cast<const uint4*>(stg + row * 256);
+          uint4* grow = reinterpret_cast<uint4*>(go + ((t0 + row) * HV + hv) * (int64_t)TC_V);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) grow[c0 + c] = srow[c0 + c];
+        }
+      }
+      good = named_bar_and(1, kEpiThreads, good);
+      return good;
+    };
+
+    store_state();
+    tmem_st32_zero(lane_base + TM_D1 + 64 + 32 * hh);
+    tmem_st32_zero(lane_base + TM_D1 + 128 + 64 + 32 * hh);
+    tmem_wait_st();
+    fence_async_smem();
+    tc_fence_before();
+    arrive(bar_st);
+
+    for (int64_t ci = 0; ci < nch; ++ci) {
+      const int s = (int)(ci & 1);
+      uint8_t* slot = sm + R_RING + s * SLOT;
+      if (ci > 0 && !drain_o(ci - 1)) { ok = false; break; }
+      // V_new^T -> bf16 operand of G2
+      bool w = mbar_wait(bar_v, (uint32_t)(ci & 1));
+      tc_fence_after();
+      {
+        uint32_t r[32];
+        tmem_ld32(lane_base + TM_D1 + 128 * (uint32_t)s + 32 * hh, r);
+        tmem_wait_ld();
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
           sts_v4(sm + R_VN, sw128_offset(v, 32 * hh + 8 * ch),
@@ -635,75 +731,47 @@ __global__ void __launch_bounds__(256, 1) tc_recur_kernel(const FwdArgs a,
                  pack_bf16x2(__uint_as_float(r[8 * ch + 4]), __uint_as_float(r[8 * ch + 5])),
                  pack_bf16x2(__uint_as_float(r[8 * ch + 6]), __uint_as_float(r[8 * ch + 7])));
       }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    ok = __syncthreads_and(ok);
-    if (tid == 0 && ok) {
+      fence_async_smem();
+      tc_fence_before();
+      arrive(bar_vn);
+      // S^T = S^T Diag(e^gamma_C) + dS^T -> next G1 operand
+      w = mbar_wait(bar_s, (uint32_t)(ci & 1)) && w;
       tc_fence_after();
-      const uint32_t nb = smem_u32(sm + R_VN), ab = smem_u32(blk + OFF_AQK),
-                     kb = smem_u32(blk + OFF_KGT);
-      // O^T += V_new^T Aqk^T
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + TM_O, sdesc_sw128(nb + ks * 32, 16, 1024),
-                 sdesc_sw128(ab + ks * 32, 16, 1024), idesc_bf16(64, 64), 1);
-      // dS^T = V_new^T Kg
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + TM_S, sdesc_sw128(nb + ks * 32, 16, 1024),
-                 sdesc_sw128(kb + ks * 32, 16, 1024), idesc_bf16(64, 128), ks > 0);
-      mma_commit(mbar);
-    }
-    __syncwarp();
-    if (ok && !mbar_wait(mbar, mphase)) {
-      flag_status(a.status, KDA_DEV_TIMEOUT);
-      ok = false;
-    }
-    mphase ^= 1;
-    tc_fence_after();
-    // epilogue 2: S = Diag(e^gamma_C) S + dS, then O
-    {
-      const float* dec = reinterpret_cast<const float*>(blk + OFF_D) + 64 * hh;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t r[16];
-        tmem_ld16(tmem_addr(tmem, 32 * q4, TM_S + 64 * hh + 16 * c4), r);
+      {
+        uint32_t r[64];
+        tmem_ld16(lane_base + TM_D2 + 64 * hh, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tmem_ld16(lane_base + TM_D2 + 64 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tmem_ld16(lane_base + TM_D2 + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[16]>(r + 32));
+        tmem_ld16(lane_base + TM_D2 + 64 * hh + 48, *reinterpret_cast<uint32_t(*)[16]>(r + 48));
         tmem_wait_ld();
+        const float4* dec = reinterpret_cast<const float4*>(slot + SL_D) + 16 * hh;
 #pragma unroll
-        for (int x = 0; x < 16; ++x)
-          S[16 * c4 + x] = fmaf(dec[16 * c4 + x], S[16 * c4 + x], __uint_as_float(r[x]));
-      }
-      store_state();
-      uint32_t r[32];
-      tmem_ld32(tmem_addr(tmem, 32 * q4, TM_O + 32 * hh), r);
-      tmem_wait_ld();
-      if (active) {
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const int tt = 32 * hh + x;
-          if (tt < L)
-            go[((t0 + tt) * HV + hv) * (int64_t)TC_V + v0 + v] =
-                __float2bfloat16_rn(__uint_as_float(r[x]));
+        for (int x4 = 0; x4 < 16; ++x4) {
+          const float4 d = dec[x4];
+          S[4 * x4 + 0] = fmaf(d.x, S[4 * x4 + 0], __uint_as_float(r[4 * x4 + 0]));
+          S[4 * x4 + 1] = fmaf(d.y, S[4 * x4 + 1], __uint_as_float(r[4 * x4 + 1]));
+          S[4 * x4 + 2] = fmaf(d.z, S[4 * x4 + 2], __uint_as_float(r[4 * x4 + 2]));
+          S[4 * x4 + 3] = fmaf(d.w, S[4 * x4 + 3], __uint_as_float(r[4 * x4 + 3]));
         }
+        store_state();
       }
+      fence_async_smem();
+      tc_fence_before();
+      arrive(bar_st);
+      if (!named_bar_and(1, kEpiThreads, w)) { ok = false; break; }
     }
-    fence_async_smem();
-    tc_fence_before();
-    ok = __syncthreads_and(ok);
-    if (!ok) {
-      // a wait ran out: let the last issued copy land (bounded) before leaving
-      if (tid == 0 && issued > ci + 1) mbar_wait(&full[s ^ 1], (uint32_t)(((ci + 1) >> 1) & 1));
-      break;
+    if (ok && nch > 0) {
+      ok = drain_o(nch - 1);
     }
-  }
-  if (a.final_state != nullptr && active && ok) {
+    if (!ok) flag_status(a.status, KDA_DEV_TIMEOUT);
+    if (a.final_state != nullptr && ok) {
 #pragma unroll
-    for (int j = 0; j < 64; ++j) a.final_state[sbase + (size_t)(64 * hh + j) * TC_V + v0 + v] = S[j];
+      for (int j = 0; j < 64; ++j) a.final_state[sbase + (size_t)(64 * hh + j) * TC_V + v] = S[j];
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 8) tmem_dealloc(tmem, 512);
 }
 
 // Driver entry point for tensor-map encoding, looked up once.
@@ -767,8 +835,8 @@ cudaError_t launch_tc_recur(const FwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(tc_recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)R_SMEM);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((size_t)2 * p.HV * p.N));
-  tc_recur_kernel<<<grid, 256, R_SMEM, s>>>(a, vmap);
+  const dim3 grid((unsigned)((size_t)p.HV * p.N));
+  tc_recur_kernel<<<grid, kRecThreads, R_SMEM, s>>>(a, vmap);
   return cudaGetLastError();
 }
 
