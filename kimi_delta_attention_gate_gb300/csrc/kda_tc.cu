@@ -95,24 +95,25 @@ __device__ __forceinline__ float gate_fast(float x, float a, float lb) {
 // tc_intra
 // ======================================================================================
 constexpr uint32_t P_QSKS = 0;       // [Qs;Ks] A operand: 128 rows x 128 ch, 2 panels x 16 KB
-constexpr uint32_t P_KA = 32768;     // Ka_0..Ka_3 B operands (16/32/48/64 rows x 128 ch); later solve
-constexpr uint32_t P_XT = 73728;     // X^T [128 ch x 64 tokens] A operand of the W MMA
+constexpr uint32_t P_KA = 32768;     // [Ka_0; Ka_1; Ka_2; Ka_3] B operand: 160 rows, 2 panels x 20 KB;
+                                     // after the Aqk/Akk MMA: fp32 solve scratch
+constexpr uint32_t KA_PANEL = 20480;
+constexpr uint32_t P_XT = 73728;     // X^T [128 ch x 64 tokens]: B operand of the W MMA
 constexpr uint32_t P_OUT = 90112;    // packed block
 constexpr uint32_t P_BETA = P_OUT + BLOCK_BYTES;  // fp32 [64]
 constexpr uint32_t P_BSUM = P_BETA + 256;         // fp32 [4][128] block sums of the gate
 constexpr uint32_t P_ROWSQ = P_BSUM + 2048;       // fp32 [64 rows][2 halves][2 (q,k)]
-constexpr uint32_t P_DIAG = P_ROWSQ + 1024;       // fp32 [4][2][16][16] exact diagonal blocks
+constexpr uint32_t P_DIAG = P_ROWSQ + 1024;       // fp32 [4][2][16][16] exact diagonal blocks;
+                                                  // later solve scratch Y [32][32]
 constexpr uint32_t P_DT = P_DIAG + 8192;          // fp32 [128] dt_bias row
 constexpr uint32_t P_FLAG = P_DT + 512;
 constexpr uint32_t P_BAR = P_FLAG + 16;
 constexpr uint32_t P_TMEM = P_BAR + 16;
 constexpr uint32_t P_END = P_TMEM + 16;
 constexpr uint32_t P_SMEM = P_END + 1024;
-// Ka_I (16(I+1) rows, 2 panels) offsets within P_KA: 0, 4096, 12288, 24576
-__host__ __device__ constexpr uint32_t ka_off(int I) { return 1024u * (uint32_t)(I * (I + 1) * 2); }
-// TMEM columns of the Aqk/Akk accumulators D_I (16(I+1) columns each): 0, 32, 64, 128
-__host__ __device__ constexpr uint32_t d_col(int I) { return I < 3 ? 32u * (uint32_t)I : 128u; }
-constexpr uint32_t WT_COL = 192;
+// Ka_I (16(I+1) rows) starts at row 8 I (I+1) of the B operand; its accumulator D_I at the
+// same TMEM column: 0, 16, 48, 96
+__host__ __device__ constexpr uint32_t ka_row(int I) { return 8u * (uint32_t)(I * (I + 1)); }
 constexpr int SOLVE_LD = 65;
 
 template <int GATE>
@@ -147,12 +148,11 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
     fence_mbar_init();
     sFlag[0] = 0;
   }
-  for (int i = tid; i < 4 * 2 * 256; i += 256) sDiag[i] = 0.f;
+  for (int i = tid; i < 4 * 2 * 256; i += 256) sDiag[i] = 0.f;  // exact diagonal blocks
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sTmem;
-  // dt_bias row: one bulk copy, overlapped with the loads below
-  if (tid == 0 && a.dt_bias != nullptr && GATE != KDA_GATE_PREGATED) {
+  if (tid == 0 && a.dt_bias != nullptr && GATE != KDA_GATE_PREGATED) {  // dt_bias row: bulk copy
     mbar_arrive_expect_tx(&bars[1], TC_K * 4);
     bulk_g2s(sDt, a.dt_bias + (size_t)hv * TC_K, TC_K * 4, &bars[1]);
   }
@@ -247,7 +247,6 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
     dout[c0] = ex2(gl0);
     dout[c0 + 1] = ex2(gl1);
   }
-  float qh0[16], qh1[16], kh0[16], kh1[16];
   const uint32_t pan = (uint32_t)(c0 >> 6);  // panel of this channel pair
   const uint32_t cc = (uint32_t)(c0 & 63);
   float F0[4], F1[4];  // 2^(r_I - r_b) for the blocks I > rg that see this block's keys
@@ -256,6 +255,9 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
     F0[I] = (I > rg) ? ex2(rI0[I] - rb0) : 1.f;
     F1[I] = (I > rg) ? ex2(rI1[I] - rb1) : 1.f;
   }
+  // transposed tiles (X^T and Kg^T: row = channel, 16 consecutive tokens per thread) are
+  // packed two tokens per register and written as 16-byte chunks after the loop
+  uint32_t xt0[8], xt1[8], kt0[8], kt1[8];
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = 16 * rg + r;
@@ -268,28 +270,27 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
     }
     const float q0 = bf_lo(q2[r]) * qn, q1 = bf_hi(q2[r]) * qn;
     const float k0 = bf_lo(k2[r]) * kn, k1 = bf_hi(k2[r]) * kn;
-    qh0[r] = q0; qh1[r] = q1; kh0[r] = k0; kh1[r] = k1;
-    const float P0 = ex2(G0[r]), P1 = ex2(G1[r]);     // 2^(Gamma - r_b) <= 1
+    const float P0 = ex2(G0[r]), P1 = ex2(G1[r]);  // 2^(Gamma - r_b) <= 1
     // [Qs;Ks] rows: block rg's queries at 32rg + r, keys at 32rg + 16 + r
     sts_u32(sm + P_QSKS + pan * 16384, sw128_offset(32 * rg + r, cc), pack_bf16x2(q0 * P0, q1 * P1));
     sts_u32(sm + P_QSKS + pan * 16384, sw128_offset(32 * rg + 16 + r, cc),
             pack_bf16x2(k0 * P0, k1 * P1));
-    // Qg (row-major) and X^T (transposed) share 2^Gamma = P 2^r_b
+    // -Qg (rows 64-127 of B1) and X^T share 2^Gamma = P 2^r_b
     sts_u32(out + OFF_B1 + pan * 16384, sw128_offset(64 + row, cc),
             pack_bf16x2(-q0 * P0 * erb0, -q1 * P1 * erb1));
-    sts_u16(sm + P_XT, sw128_offset(c0, row), k0 * P0 * erb0);
-    sts_u16(sm + P_XT, sw128_offset(c0 + 1, row), k1 * P1 * erb1);
+    const float x0 = k0 * P0 * erb0, x1 = k1 * P1 * erb1;
+    float kg0, kg1;
     if (!guard) {
       const float E0 = ex2(-G0[r]), E1 = ex2(-G1[r]);  // 2^(r_b - Gamma) <= 2^120
       const float ke0 = k0 * E0, ke1 = k1 * E1;
 #pragma unroll
       for (int I = 0; I < 4; ++I) {
         if (I < rg) continue;
-        sts_u32(sm + P_KA + ka_off(I) + pan * (2048u * (I + 1)), sw128_offset(row, cc),
+        sts_u32(sm + P_KA + pan * KA_PANEL, sw128_offset(ka_row(I) + row, cc),
                 pack_bf16x2(ke0 * F0[I], ke1 * F1[I]));
       }
-      sts_u16(out + OFF_B2, sw128_offset(c0, row), ke0 * ekg0);
-      sts_u16(out + OFF_B2, sw128_offset(c0 + 1, row), ke1 * ekg1);
+      kg0 = ke0 * ekg0;
+      kg1 = ke1 * ekg1;
     } else {
       // every exponent below is <= 0; the diagonal block is evaluated exactly further down
 #pragma unroll
@@ -297,43 +298,72 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
         if (I < rg) continue;
         const float v0 = (I == rg) ? 0.f : k0 * ex2(rI0[I] - rb0 - G0[r]);
         const float v1 = (I == rg) ? 0.f : k1 * ex2(rI1[I] - rb1 - G1[r]);
-        sts_u32(sm + P_KA + ka_off(I) + pan * (2048u * (I + 1)), sw128_offset(row, cc),
-                pack_bf16x2(v0, v1));
+        sts_u32(sm + P_KA + pan * KA_PANEL, sw128_offset(ka_row(I) + row, cc), pack_bf16x2(v0, v1));
       }
-      sts_u16(out + OFF_B2, sw128_offset(c0, row), k0 * ex2(gl0 - rb0 - G0[r]));
-      sts_u16(out + OFF_B2, sw128_offset(c0 + 1, row), k1 * ex2(gl1 - rb1 - G1[r]));
+      kg0 = k0 * ex2(gl0 - rb0 - G0[r]);
+      kg1 = k1 * ex2(gl1 - rb1 - G1[r]);
+    }
+    if (r & 1) {
+      xt0[r >> 1] = pack_bf16x2(__uint_as_float(xt0[r >> 1]), x0);
+      xt1[r >> 1] = pack_bf16x2(__uint_as_float(xt1[r >> 1]), x1);
+      kt0[r >> 1] = pack_bf16x2(__uint_as_float(kt0[r >> 1]), kg0);
+      kt1[r >> 1] = pack_bf16x2(__uint_as_float(kt1[r >> 1]), kg1);
+    } else {  // hold the even row's value until its odd partner is computed
+      xt0[r >> 1] = __float_as_uint(x0);
+      xt1[r >> 1] = __float_as_uint(x1);
+      kt0[r >> 1] = __float_as_uint(kg0);
+      kt1[r >> 1] = __float_as_uint(kg1);
     }
   }
+#pragma unroll
+  for (int hlf = 0; hlf < 2; ++hlf) {
+    const int tcol = 16 * rg + 8 * hlf;
+    sts_v4(sm + P_XT, sw128_offset(c0, tcol), xt0[4 * hlf], xt0[4 * hlf + 1], xt0[4 * hlf + 2],
+           xt0[4 * hlf + 3]);
+    sts_v4(sm + P_XT, sw128_offset(c0 + 1, tcol), xt1[4 * hlf], xt1[4 * hlf + 1], xt1[4 * hlf + 2],
+           xt1[4 * hlf + 3]);
+    sts_v4(out + OFF_B2, sw128_offset(c0, tcol), kt0[4 * hlf], kt0[4 * hlf + 1], kt0[4 * hlf + 2],
+           kt0[4 * hlf + 3]);
+    sts_v4(out + OFF_B2, sw128_offset(c0 + 1, tcol), kt1[4 * hlf], kt1[4 * hlf + 1],
+           kt1[4 * hlf + 2], kt1[4 * hlf + 3]);
+  }
   if (guard) {
-    // exact diagonal block: partial sums over this thread's two channels
+    // exact diagonal block: partial sums over this thread's two channels (recomputed
+    // normalised q, k; every exponent Gamma_i - Gamma_j <= 0)
+    // (fully unrolled: runtime indices would force q2, k2, G0, G1 into local memory)
     float* dq = sDiag + rg * 512;
     float* dk = dq + 256;
-    for (int i = 0; i < 16; ++i)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int rowi = 16 * rg + i;
+      const float qn = a.qk_l2norm ? a.scale * rsqrtf(sRowsq[(rowi * 2) * 2] + sRowsq[(rowi * 2 + 1) * 2] + 1e-6f)
+                                   : a.scale;
+      const float kni = a.qk_l2norm ? rsqrtf(sRowsq[(rowi * 2) * 2 + 1] + sRowsq[(rowi * 2 + 1) * 2 + 1] + 1e-6f)
+                                    : 1.f;
+#pragma unroll
       for (int j = 0; j <= i; ++j) {
+        const int rowj = 16 * rg + j;
+        const float knj = a.qk_l2norm ? rsqrtf(sRowsq[(rowj * 2) * 2 + 1] + sRowsq[(rowj * 2 + 1) * 2 + 1] + 1e-6f)
+                                      : 1.f;
         const float e0 = ex2(G0[i] - G0[j]), e1 = ex2(G1[i] - G1[j]);
-        atomicAdd(&dq[i * 16 + j], qh0[i] * kh0[j] * e0 + qh1[i] * kh1[j] * e1);
-        atomicAdd(&dk[i * 16 + j], kh0[i] * kh0[j] * e0 + kh1[i] * kh1[j] * e1);
+        const float kj0 = bf_lo(k2[j]) * knj, kj1 = bf_hi(k2[j]) * knj;
+        atomicAdd(&dq[i * 16 + j], (bf_lo(q2[i]) * kj0 * e0 + bf_hi(q2[i]) * kj1 * e1) * qn);
+        atomicAdd(&dk[i * 16 + j], (bf_lo(k2[i]) * kj0 * e0 + bf_hi(k2[i]) * kj1 * e1) * kni);
       }
+    }
   }
   fence_async_smem();
   __syncthreads();
 
-  // ---- Aqk / Akk: D_I = [Qs;Ks] Ka_I^T, M=128, N=16(I+1), K=128 ----
+  // ---- Aqk / Akk in one MMA: D = [Qs;Ks] [Ka_0;..;Ka_3]^T, M=128, N=160, K=128 ----
   if (tid == 0) {
     tc_fence_after();
+    const uint32_t abase = smem_u32(sm + P_QSKS), bbase = smem_u32(sm + P_KA);
 #pragma unroll
-    for (int I = 0; I < 4; ++I) {
-      const uint32_t idesc = idesc_bf16(128, 16 * (I + 1));
-      const uint32_t abase = smem_u32(sm + P_QSKS);
-      const uint32_t bbase = smem_u32(sm + P_KA + ka_off(I));
-      const uint32_t bpan = 2048u * (I + 1);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t ad = sdesc_sw128(abase + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(bbase + (ks >> 2) * bpan + (ks & 3) * 32, 16, 1024);
-        mma_bf16(tmem + d_col(I), ad, bd, idesc, ks > 0);
-      }
-    }
+    for (int ks = 0; ks < 8; ++ks)
+      mma_bf16(tmem, sdesc_sw128(abase + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+               sdesc_sw128(bbase + (ks >> 2) * KA_PANEL + (ks & 3) * 32, 16, 1024),
+               idesc_bf16(128, 160), ks > 0);
     mma_commit(&bars[0]);
   }
   __syncwarp();
@@ -354,7 +384,7 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
     for (int cc4 = 0; cc4 < 4; ++cc4) {
       uint32_t r[16];
       if (cc4 <= w) {
-        tmem_ld16(tmem_addr(tmem, 32 * w, d_col(w) + 16 * cc4), r);
+        tmem_ld16(tmem_addr(tmem, 32 * w, ka_row(w) + 16 * cc4), r);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -379,23 +409,18 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
                  pack_bf16x2(vals[8 * hlf + 4], vals[8 * hlf + 5]),
                  pack_bf16x2(vals[8 * hlf + 6], vals[8 * hlf + 7]));
         }
-      }
-      // Akk0 rows written after the barrier below (sL aliases the Ka operands being read
-      // by nothing now, but keep the order explicit)
-      if (isk) {
+      } else {
 #pragma unroll
         for (int x = 0; x < 16; ++x) sL[i * SOLVE_LD + 16 * cc4 + x] = bi * vals[x];
       }
     }
-  } else {
-    for (int e = tid - 128; e < 64 * SOLVE_LD; e += 128) sX[e] = 0.f;
   }
   tc_fence_before();
   __syncthreads();
 
-  // ---- solve: X = (I + Akk0)^-1, 16x16 blocks ----
-  float* sP = sDiag;  // scratch [3][16][16]
-  if (tid < 64) {
+  // ---- solve X = (I + Akk0)^-1 by recursive halving (16 -> 32 -> 64), fp32 ----
+  float* sY = sDiag;  // scratch
+  if (tid < 64) {     // level 1: the four 16 x 16 diagonal blocks, one column per thread
     const int b = tid >> 4, col = tid & 15, base = 16 * b;
     float x[16];
 #pragma unroll
@@ -411,26 +436,53 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
     for (int i = 0; i < 16; ++i) sX[(base + i) * SOLVE_LD + base + col] = x[i];
   }
   __syncthreads();
-  for (int bi = 1; bi < 4; ++bi) {
-    for (int e = tid; e < bi * 256; e += 256) {
-      const int bj = e >> 8, r = (e >> 4) & 15, cc2 = e & 15;
-      float s = 0.f;
-      for (int m = 16 * bj; m < 16 * bi; ++m)
-        s = fmaf(sL[(16 * bi + r) * SOLVE_LD + m], sX[m * SOLVE_LD + 16 * bj + cc2], s);
-      sP[e] = s;
-    }
-    __syncthreads();
-    for (int e = tid; e < bi * 256; e += 256) {
-      const int bj = e >> 8, r = (e >> 4) & 15, cc2 = e & 15;
+  {  // level 2: X_{2p+1,2p} = -X_{2p+1,2p+1} (L_{2p+1,2p} X_{2p,2p}), p = 0, 1
+    for (int e = tid; e < 512; e += 256) {
+      const int pr = e >> 8, i = (e >> 4) & 15, j = e & 15;
+      const int rb = 32 * pr + 16, cb = 32 * pr;
       float s = 0.f;
 #pragma unroll
       for (int m = 0; m < 16; ++m)
-        s = fmaf(sX[(16 * bi + r) * SOLVE_LD + 16 * bi + m], sP[bj * 256 + m * 16 + cc2], s);
-      sX[(16 * bi + r) * SOLVE_LD + 16 * bj + cc2] = -s;
+        s = fmaf(sL[(rb + i) * SOLVE_LD + cb + m], sX[(cb + m) * SOLVE_LD + cb + j], s);
+      sY[e] = s;
+    }
+    __syncthreads();
+    for (int e = tid; e < 512; e += 256) {
+      const int pr = e >> 8, i = (e >> 4) & 15, j = e & 15;
+      const int rb = 32 * pr + 16, cb = 32 * pr;
+      float s = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        s = fmaf(sX[(rb + i) * SOLVE_LD + rb + m], sY[pr * 256 + m * 16 + j], s);
+      sX[(rb + i) * SOLVE_LD + cb + j] = -s;
     }
     __syncthreads();
   }
-  // T = X Diag(beta), bf16 row-major (also the B operand of the W MMA)
+  {  // level 3: X_{B,A} = -X_BB (L_BA X_AA), A = 0..31, B = 32..63; 2 x 2 tile per thread
+    const int ti = tid >> 4, tj = tid & 15;
+    const int i0 = 2 * ti, j0 = 2 * tj;
+    float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+    for (int m = j0; m < 32; ++m) {  // X_AA is lower triangular: rows m >= j
+      const float l0 = sL[(32 + i0) * SOLVE_LD + m], l1 = sL[(33 + i0) * SOLVE_LD + m];
+      const float xa = sX[m * SOLVE_LD + j0], xb = sX[m * SOLVE_LD + j0 + 1];
+      y00 = fmaf(l0, xa, y00); y01 = fmaf(l0, xb, y01);
+      y10 = fmaf(l1, xa, y10); y11 = fmaf(l1, xb, y11);
+    }
+    sY[i0 * 32 + j0] = y00; sY[i0 * 32 + j0 + 1] = y01;
+    sY[(i0 + 1) * 32 + j0] = y10; sY[(i0 + 1) * 32 + j0 + 1] = y11;
+    __syncthreads();
+    float z00 = 0.f, z01 = 0.f, z10 = 0.f, z11 = 0.f;
+    for (int m = 0; m <= i0 + 1; ++m) {  // X_BB is lower triangular: columns m <= i
+      const float xa = sX[(32 + i0) * SOLVE_LD + 32 + m], xb = sX[(33 + i0) * SOLVE_LD + 32 + m];
+      const float ya = sY[m * 32 + j0], yb = sY[m * 32 + j0 + 1];
+      z00 = fmaf(xa, ya, z00); z01 = fmaf(xa, yb, z01);
+      z10 = fmaf(xb, ya, z10); z11 = fmaf(xb, yb, z11);
+    }
+    sX[(32 + i0) * SOLVE_LD + j0] = -z00; sX[(32 + i0) * SOLVE_LD + j0 + 1] = -z01;
+    sX[(33 + i0) * SOLVE_LD + j0] = -z10; sX[(33 + i0) * SOLVE_LD + j0 + 1] = -z11;
+  }
+  __syncthreads();
+  // T = X Diag(beta), bf16 row-major (A operand of the W MMA and of U = T V downstream)
   {
     const int i = tid >> 2, j0 = (tid & 3) * 16;
 #pragma unroll
@@ -446,33 +498,40 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
     }
   }
   fence_async_smem();
+  tc_fence_before();
   __syncthreads();
 
-  // ---- W^T = X^T T^T: M=128 channels, N=64 tokens, K=64 ----
+  // ---- W = T X: M=64 tokens, N=128 channels, K=64 (row i in TMEM lane 32(i/16)+i%16) ----
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t idesc = idesc_bf16(128, 64);
-    const uint32_t abase = smem_u32(sm + P_XT), bbase = smem_u32(out + OFF_T);
+    const uint32_t abase = smem_u32(out + OFF_T), bbase = smem_u32(sm + P_XT);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      mma_bf16(tmem + WT_COL, sdesc_sw128(abase + ks * 32, 16, 1024),
-               sdesc_sw128(bbase + ks * 32, 16, 1024), idesc, ks > 0);
+      mma_bf16(tmem, sdesc_sw128(abase + ks * 32, 16, 1024), sdesc_sw128(bbase + ks * 32, 16, 1024),
+               idesc_bf16(64, 128), ks > 0);
     mma_commit(&bars[0]);
   }
   __syncwarp();
   if (!mbar_wait(&bars[0], 1)) flag_status(a.status, KDA_DEV_TIMEOUT);
   tc_fence_after();
-  if (warp < 4) {
-    const int kch = 32 * warp + lane;
-    uint8_t* wp = out + OFF_B1 + (kch >> 6) * 16384;
+  {
+    const int q4 = warp & 3, hh = warp >> 2;
+    const int i = 16 * q4 + (lane & 15);
+    uint8_t* wp = out + OFF_B1 + hh * 16384;  // rows 0-63 of panel hh
 #pragma unroll
-    for (int cc4 = 0; cc4 < 4; ++cc4) {
+    for (int c4 = 0; c4 < 4; ++c4) {
       uint32_t r[16];
-      tmem_ld16(tmem_addr(tmem, 32 * warp, WT_COL + 16 * cc4), r);
+      tmem_ld16(tmem_addr(tmem, 32 * q4, 64 * hh + 16 * c4), r);
       tmem_wait_ld();
+      if (lane < 16) {
 #pragma unroll
-      for (int x = 0; x < 16; ++x)
-        sts_u16(wp, sw128_offset(16 * cc4 + x, kch & 63), __uint_as_float(r[x]));
+        for (int hlf = 0; hlf < 2; ++hlf)
+          sts_v4(wp, sw128_offset(i, 16 * c4 + 8 * hlf),
+                 pack_bf16x2(__uint_as_float(r[8 * hlf + 0]), __uint_as_float(r[8 * hlf + 1])),
+                 pack_bf16x2(__uint_as_float(r[8 * hlf + 2]), __uint_as_float(r[8 * hlf + 3])),
+                 pack_bf16x2(__uint_as_float(r[8 * hlf + 4]), __uint_as_float(r[8 * hlf + 5])),
+                 pack_bf16x2(__uint_as_float(r[8 * hlf + 6]), __uint_as_float(r[8 * hlf + 7])));
+      }
     }
   }
   fence_async_smem();
@@ -561,15 +620,13 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     if (lane == 0) {
       const uint8_t* blocks = reinterpret_cast<const uint8_t*>(a.ws) + p.off_inter;
       const CUtensorMap* vmap_ptr = &vmap;  // generic address of the kernel parameter
-      auto issue = [&](int64_t ci, int st) {  // chunk ci -> slot st
+      auto issue = [&](int64_t ci, int st) {  // chunk ci -> slot st: block + 2 v halves
         const int64_t cg = cfirst + ci;
         uint8_t* dst = sm + R_RING + st * SLOT;
         const uint8_t* src = blocks + ((size_t)cg * HV + hv) * p.inter_block_bytes;
         mbar_arrive_expect_tx(&full[st], BLOCK_BYTES + 16384);
-        bulk_g2s(dst, src, 16384, &full[st]);
-        bulk_g2s(dst + 16384, src + 16384, 16384, &full[st]);
-        bulk_g2s(dst + 32768, src + 32768, 16384, &full[st]);
-        bulk_g2s(dst + 49152, src + 49152, BLOCK_BYTES - 49152, &full[st]);
+        bulk_g2s(dst, src, BLOCK_BYTES, &full[st]);  // one large copy: per-SM bulk-copy
+                                                     // throughput grows with copy size
         tma_load_3d(dst + SL_V, vmap_ptr, 0, hv, (int32_t)(bos + ci * TC_C), &full[st]);
         tma_load_3d(dst + SL_V + 8192, vmap_ptr, 64, hv, (int32_t)(bos + ci * TC_C), &full[st]);
       };
