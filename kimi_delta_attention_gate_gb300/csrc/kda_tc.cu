@@ -102,8 +102,8 @@ constexpr uint32_t P_XT = 73728;     // X^T [128 ch x 64 tokens]: B operand of t
 constexpr uint32_t P_OUT = 90112;    // packed block
 constexpr uint32_t P_BETA = P_OUT + BLOCK_BYTES;  // fp32 [64]
 constexpr uint32_t P_BSUM = P_BETA + 256;         // fp32 [4][128] block sums of the gate
-constexpr uint32_t P_ROWSQ = P_BSUM + 2048;       // fp32 [64 rows][2 halves][2 (q,k)]
-constexpr uint32_t P_DIAG = P_ROWSQ + 1024;       // fp32 [4][2][16][16] exact diagonal blocks;
+constexpr uint32_t P_ROWSQ = P_BSUM + 2048;       // fp32 [64 rows][2 halves][2 (q,k)], then norms [64][2]
+constexpr uint32_t P_DIAG = P_ROWSQ + 1536;       // fp32 [4][2][16][16] exact diagonal blocks;
                                                   // later solve scratch Y [32][32]
 constexpr uint32_t P_DT = P_DIAG + 8192;          // fp32 [128] dt_bias row
 constexpr uint32_t P_FLAG = P_DT + 512;
@@ -227,6 +227,18 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
     }
   }
   __syncthreads();
+  float* sNorm = sRowsq + 64 * 4;  // [64 rows][2]: q multiplier (with scale), k multiplier
+  if (tid < 64) {
+    const float* rq = sRowsq + tid * 4;
+    float qn = a.scale, kn = 1.f;
+    if (a.qk_l2norm) {
+      qn *= rsqrtf(rq[0] + rq[2] + 1e-6f);
+      kn = rsqrtf(rq[1] + rq[3] + 1e-6f);
+    }
+    sNorm[2 * tid] = qn;
+    sNorm[2 * tid + 1] = kn;
+  }
+  __syncthreads();
 
   // ---- carries, norms, factors, operand tiles ----
   float rI0[4], rI1[4];  // reference r_I = Gamma just before block I
@@ -261,13 +273,7 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = 16 * rg + r;
-    float qn = a.scale, kn = 1.f;
-    if (a.qk_l2norm) {
-      const float sq = sRowsq[(row * 2) * 2 + 0] + sRowsq[(row * 2 + 1) * 2 + 0];
-      const float sk = sRowsq[(row * 2) * 2 + 1] + sRowsq[(row * 2 + 1) * 2 + 1];
-      qn *= rsqrtf(sq + 1e-6f);
-      kn = rsqrtf(sk + 1e-6f);
-    }
+    const float qn = sNorm[2 * row], kn = sNorm[2 * row + 1];
     const float q0 = bf_lo(q2[r]) * qn, q1 = bf_hi(q2[r]) * qn;
     const float k0 = bf_lo(k2[r]) * kn, k1 = bf_hi(k2[r]) * kn;
     const float P0 = ex2(G0[r]), P1 = ex2(G1[r]);  // 2^(Gamma - r_b) <= 1
@@ -336,15 +342,11 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int rowi = 16 * rg + i;
-      const float qn = a.qk_l2norm ? a.scale * rsqrtf(sRowsq[(rowi * 2) * 2] + sRowsq[(rowi * 2 + 1) * 2] + 1e-6f)
-                                   : a.scale;
-      const float kni = a.qk_l2norm ? rsqrtf(sRowsq[(rowi * 2) * 2 + 1] + sRowsq[(rowi * 2 + 1) * 2 + 1] + 1e-6f)
-                                    : 1.f;
+      const float qn = sNorm[2 * rowi], kni = sNorm[2 * rowi + 1];
 #pragma unroll
       for (int j = 0; j <= i; ++j) {
         const int rowj = 16 * rg + j;
-        const float knj = a.qk_l2norm ? rsqrtf(sRowsq[(rowj * 2) * 2 + 1] + sRowsq[(rowj * 2 + 1) * 2 + 1] + 1e-6f)
-                                      : 1.f;
+        const float knj = sNorm[2 * rowj + 1];
         const float e0 = ex2(G0[i] - G0[j]), e1 = ex2(G1[i] - G1[j]);
         const float kj0 = bf_lo(k2[j]) * knj, kj1 = bf_hi(k2[j]) * knj;
         atomicAdd(&dq[i * 16 + j], (bf_lo(q2[i]) * kj0 * e0 + bf_hi(q2[i]) * kj1 * e1) * qn);
