@@ -216,7 +216,7 @@ def cpu_sample_plan(inp: kin.Inputs, target_s: float, nthreads: int):
     """Pick a bounded oracle sample (all heads of the first sequence, a prefix of its
     tokens) expected to take about target_s seconds; returns (tokens, heads)."""
     wl = inp.wl
-    heads = min(wl.HV, max(1, nthreads)) if wl.H == wl.HV else wl.HV
+    heads = wl.HV
     probe = min(wl.T, 256)
     dt = max(oracle_sample_time(inp, probe, heads, nthreads), 1e-4)
     tokens = int(min(wl.T, max(probe, probe * target_s / dt)))
