@@ -552,10 +552,11 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
 // ======================================================================================
 // tc_recur
 // ======================================================================================
-// One CTA per (sequence, value head) holds the whole V = 128.  Warps 0-7 are epilogue
-// warps (MMA M = 128: thread v of warp quadrant q owns state row v = 32q + lane; warps
-// q and q+4 split the key channels); warp 8 is the control warp: one thread issues every
-// MMA, bulk / tensor copy and L2 prefetch, and the roles meet on mbarriers.
+// One CTA per (sequence, value head) holds the whole V = 128.  Warps 0-15 are epilogue
+// warps (MMA M = 128: thread v = 32q + lane of TMEM lane quadrant q = warp % 4 owns state
+// row v; the four warps of a quadrant split the 128 key channels, 32 each); warp 16 is the
+// control warp: one thread issues every MMA, bulk / tensor copy and L2 prefetch, and the
+// roles meet on mbarriers.
 // Per chunk, two MMA groups share the tensor pipe:
 //   G1  D1 = V^T T^T (U^T, columns 0-63; issued as soon as the chunk's data lands), then
 //       D1 -= S^T [W; -Qg]^T over N = 128: columns 0-63 become V_new^T, columns 64-127
@@ -564,10 +565,10 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
 //       V_new^T Aqk^T                                                      (4 MMAs)
 // The epilogue warps turn V_new^T into the G2 operand, update the fp32 state held in
 // registers (S^T = S^T Diag(e^gamma_C) + dS^T) into the next G1 operand, and, while the
-// next G1 runs, drain O^T = D1[:, 64:128] + D2[:, 128:192] through a shared-memory
-// staging tile with coalesced stores (D1 is double-buffered; its output half is cleared
-// with tcgen05.st after the drain).  Packed blocks and v tiles are prefetched into L2
-// four chunks ahead and copied into shared memory one chunk ahead.
+// next G1 runs, drain O^T = D1[:, 64:128] + D2[:, 128:192] through a shared-memory staging
+// tile written back by one TMA store (D1 is double-buffered; its output half is cleared
+// with tcgen05.st after the drain).  Packed blocks and v tiles are prefetched into L2 four
+// chunks ahead and copied into shared memory one chunk ahead.
 constexpr uint32_t SL_T = 57344;                     // within a slot (same offsets as the block)
 constexpr uint32_t SL_D = 65536;
 constexpr uint32_t SL_V = 66560;                     // v tile [64 tokens x 128 v], 2 MN panels
@@ -581,11 +582,13 @@ constexpr uint32_t R_END = R_TMEM + 16;
 constexpr uint32_t R_SMEM = R_END + 1024;
 constexpr uint32_t TM_D1 = 0, TM_D2 = 256;           // D1[b] at 128 b; D2 192 columns
 constexpr int kPrefetch = 4;     // chunks whose loads are prefetched into L2 ahead
-constexpr int kRecThreads = 288; // 8 epilogue warps + 1 control warp
-constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kRecThreads = kEpiThreads + 32;  // + control warp
 
 __global__ void __launch_bounds__(kRecThreads, 1)
-    tc_recur_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap vmap) {
+    tc_recur_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap vmap,
+                    const __grid_constant__ CUtensorMap omap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const Plan& p = a.plan;
@@ -601,14 +604,14 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   uint64_t* bar_vn = full + 4;
   uint64_t* bar_st = full + 5;
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + R_TMEM);
-  if (warp == 8) {
+  if (warp == kEpiWarps) {
     tmem_alloc(sTmem, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(&full[i], 1);
-    mbar_init(bar_vn, 8);
-    mbar_init(bar_st, 8);
+    mbar_init(bar_vn, kEpiWarps);
+    mbar_init(bar_st, kEpiWarps);
     fence_mbar_init();
   }
   __syncthreads();
@@ -617,7 +620,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   const int64_t nch = (eos - bos + TC_C - 1) / TC_C;
   bool ok = true;
 
-  if (warp == 8) {
+  if (warp == kEpiWarps) {
     // ---------------------------------- control warp ----------------------------------
     if (lane == 0) {
       const uint8_t* blocks = reinterpret_cast<const uint8_t*>(a.ws) + p.off_inter;
@@ -705,58 +708,63 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------- epilogue warps ---------------------------------
-    const int q4 = warp & 3, hh = warp >> 2;
+    const int q4 = warp & 3, part = warp >> 2;  // part: key channels 32 part .. +31
     const int v = 32 * q4 + lane;
     const uint32_t lane_base = tmem_addr(tmem, 32 * q4, 0);
     const size_t sbase = ((size_t)n * HV + hv) * (size_t)TC_K * TC_V;
-    float S[64];
+    float S[32];
 #pragma unroll
-    for (int j = 0; j < 64; ++j)
-      S[j] = (a.h0 != nullptr) ? a.h0[sbase + (size_t)(64 * hh + j) * TC_V + v] : 0.f;
+    for (int j = 0; j < 32; ++j)
+      S[j] = (a.h0 != nullptr) ? a.h0[sbase + (size_t)(32 * part + j) * TC_V + v] : 0.f;
+    uint8_t* st_row = sm + R_ST + (part >> 1) * 16384;  // K panel holding channels 32 part..
+    const int st_col = 32 * (part & 1);
     auto store_state = [&]() {
-      uint8_t* st = sm + R_ST + hh * 16384;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        sts_v4(st, sw128_offset(v, 8 * ch), pack_bf16x2(S[8 * ch + 0], S[8 * ch + 1]),
-               pack_bf16x2(S[8 * ch + 2], S[8 * ch + 3]), pack_bf16x2(S[8 * ch + 4], S[8 * ch + 5]),
-               pack_bf16x2(S[8 * ch + 6], S[8 * ch + 7]));
+      for (int c8 = 0; c8 < 4; ++c8)
+        sts_v4(st_row, sw128_offset(v, st_col + 8 * c8), pack_bf16x2(S[8 * c8 + 0], S[8 * c8 + 1]),
+               pack_bf16x2(S[8 * c8 + 2], S[8 * c8 + 3]), pack_bf16x2(S[8 * c8 + 4], S[8 * c8 + 5]),
+               pack_bf16x2(S[8 * c8 + 6], S[8 * c8 + 7]));
     };
     auto arrive = [&](uint64_t* bar) {  // one arrival per warp, after the warp's writes
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
     };
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
+    const CUtensorMap* omap_ptr = &omap;
     // O^T of chunk ci = D1[ci&1][64:128] + D2[128:192]: stage as [token][v] in the VN
-    // buffer, then coalesced 16-byte stores of the chunk's rows; clear D1's output half.
+    // buffer, write it back (one TMA store for a full chunk, 16-byte stores of the valid
+    // rows otherwise), clear D1's output half.
     auto drain_o = [&](int64_t ci) -> bool {
       const int64_t t0 = bos + ci * TC_C;
       const int L = (int)((eos - t0) < TC_C ? (eos - t0) : TC_C);
-      const uint32_t d1 = TM_D1 + 128 * (uint32_t)(ci & 1) + 64 + 32 * hh;
+      const uint32_t d1 = TM_D1 + 128 * (uint32_t)(ci & 1) + 64 + 16 * part;
       uint8_t* stg = sm + R_VN;
+      uint32_t r1[16], r2[16];
+      tmem_ld16(lane_base + d1, r1);
+      tmem_ld16(lane_base + TM_D2 + 128 + 16 * part, r2);
+      tmem_wait_ld();
+      tmem_st16_zero(lane_base + d1);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r1[16], r2[16];
-        tmem_ld16(lane_base + d1 + 16 * half, r1);
-        tmem_ld16(lane_base + TM_D2 + 128 + 32 * hh + 16 * half, r2);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int tt = 32 * hh + 16 * half + x;
-          *reinterpret_cast<__nv_bfloat16*>(stg + tt * 256 + v * 2) =
-              __float2bfloat16_rn(__uint_as_float(r1[x]) + __uint_as_float(r2[x]));
-        }
+      for (int x = 0; x < 16; ++x) {
+        const int tt = 16 * part + x;
+        *reinterpret_cast<__nv_bfloat16*>(stg + tt * 256 + v * 2) =
+            __float2bfloat16_rn(__uint_as_float(r1[x]) + __uint_as_float(r2[x]));
       }
-      tmem_st32_zero(lane_base + d1);
       tmem_wait_st();
       tc_fence_before();
+      fence_async_smem();
       bool good = named_bar_and(1, kEpiThreads, true);
-      {
-        const int row = tid >> 2, c0 = (tid & 3) * 4;
-        if (row < L) {
-          const uint4* srow = reinterpret_cast<const uint4*>(stg + row * 256);
-          uint4* grow = reinterpret_cast<uint4*>(go + ((t0 + row) * HV + hv) * (int64_t)TC_V);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) grow[c0 + c] = srow[c0 + c];
+      if (L == TC_C) {
+        if (tid == 0) {
+          tma_store_3d(omap_ptr, 0, hv, (int32_t)t0, stg);
+          bulk_commit();
+          bulk_wait_read0();  // the staging buffer is rewritten right after
+        }
+      } else {
+        for (int e = tid; e < L * 16; e += kEpiThreads) {
+          const int row = e >> 4, c16 = e & 15;
+          reinterpret_cast<uint4*>(go + ((t0 + row) * HV + hv) * (int64_t)TC_V)[c16] =
+              reinterpret_cast<const uint4*>(stg + row * 256)[c16];
         }
       }
       good = named_bar_and(1, kEpiThreads, good);
@@ -764,8 +772,8 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     };
 
     store_state();
-    tmem_st32_zero(lane_base + TM_D1 + 64 + 32 * hh);
-    tmem_st32_zero(lane_base + TM_D1 + 128 + 64 + 32 * hh);
+    tmem_st16_zero(lane_base + TM_D1 + 64 + 16 * part);
+    tmem_st16_zero(lane_base + TM_D1 + 128 + 64 + 16 * part);
     tmem_wait_st();
     fence_async_smem();
     tc_fence_before();
@@ -775,42 +783,43 @@ __global__ void __launch_bounds__(kRecThreads, 1)
       const int s = (int)(ci & 1);
       uint8_t* slot = sm + R_RING + s * SLOT;
       if (ci > 0 && !drain_o(ci - 1)) { ok = false; break; }
-      // V_new^T -> bf16 operand of G2
+      // V_new^T -> bf16 operand of G2 (this warp: tokens 16 part .. +15)
       bool w = mbar_wait(bar_v, (uint32_t)(ci & 1));
       tc_fence_after();
       {
-        uint32_t r[32];
-        tmem_ld32(lane_base + TM_D1 + 128 * (uint32_t)s + 32 * hh, r);
+        uint32_t r[16];
+        tmem_ld16(lane_base + TM_D1 + 128 * (uint32_t)s + 16 * part, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-          sts_v4(sm + R_VN, sw128_offset(v, 32 * hh + 8 * ch),
-                 pack_bf16x2(__uint_as_float(r[8 * ch + 0]), __uint_as_float(r[8 * ch + 1])),
-                 pack_bf16x2(__uint_as_float(r[8 * ch + 2]), __uint_as_float(r[8 * ch + 3])),
-                 pack_bf16x2(__uint_as_float(r[8 * ch + 4]), __uint_as_float(r[8 * ch + 5])),
-                 pack_bf16x2(__uint_as_float(r[8 * ch + 6]), __uint_as_float(r[8 * ch + 7])));
+        for (int c8 = 0; c8 < 2; ++c8)
+          sts_v4(sm + R_VN, sw128_offset(v, 16 * part + 8 * c8),
+                 pack_bf16x2(__uint_as_float(r[8 * c8 + 0]), __uint_as_float(r[8 * c8 + 1])),
+                 pack_bf16x2(__uint_as_float(r[8 * c8 + 2]), __uint_as_float(r[8 * c8 + 3])),
+                 pack_bf16x2(__uint_as_float(r[8 * c8 + 4]), __uint_as_float(r[8 * c8 + 5])),
+                 pack_bf16x2(__uint_as_float(r[8 * c8 + 6]), __uint_as_float(r[8 * c8 + 7])));
       }
       fence_async_smem();
       tc_fence_before();
       arrive(bar_vn);
-      // S^T = S^T Diag(e^gamma_C) + dS^T -> next G1 operand
+      // S^T = S^T Diag(e^gamma_C) + dS^T -> next G1 operand (this warp: 32 channels)
       w = mbar_wait(bar_s, (uint32_t)(ci & 1)) && w;
       tc_fence_after();
       {
-        uint32_t r[64];
-        tmem_ld16(lane_base + TM_D2 + 64 * hh, *reinterpret_cast<uint32_t(*)[16]>(r));
-        tmem_ld16(lane_base + TM_D2 + 64 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-        tmem_ld16(lane_base + TM_D2 + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[16]>(r + 32));
-        tmem_ld16(lane_base + TM_D2 + 64 * hh + 48, *reinterpret_cast<uint32_t(*)[16]>(r + 48));
-        tmem_wait_ld();
-        const float4* dec = reinterpret_cast<const float4*>(slot + SL_D) + 16 * hh;
+        const float4* dec = reinterpret_cast<const float4*>(slot + SL_D) + 8 * part;
 #pragma unroll
-        for (int x4 = 0; x4 < 16; ++x4) {
-          const float4 d = dec[x4];
-          S[4 * x4 + 0] = fmaf(d.x, S[4 * x4 + 0], __uint_as_float(r[4 * x4 + 0]));
-          S[4 * x4 + 1] = fmaf(d.y, S[4 * x4 + 1], __uint_as_float(r[4 * x4 + 1]));
-          S[4 * x4 + 2] = fmaf(d.z, S[4 * x4 + 2], __uint_as_float(r[4 * x4 + 2]));
-          S[4 * x4 + 3] = fmaf(d.w, S[4 * x4 + 3], __uint_as_float(r[4 * x4 + 3]));
+        for (int h = 0; h < 2; ++h) {  // two 16-column loads keep the register count low
+          uint32_t r[16];
+          tmem_ld16(lane_base + TM_D2 + 32 * part + 16 * h, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x4 = 0; x4 < 4; ++x4) {
+            const float4 d = dec[4 * h + x4];
+            const int j = 16 * h + 4 * x4;
+            S[j + 0] = fmaf(d.x, S[j + 0], __uint_as_float(r[4 * x4 + 0]));
+            S[j + 1] = fmaf(d.y, S[j + 1], __uint_as_float(r[4 * x4 + 1]));
+            S[j + 2] = fmaf(d.z, S[j + 2], __uint_as_float(r[4 * x4 + 2]));
+            S[j + 3] = fmaf(d.w, S[j + 3], __uint_as_float(r[4 * x4 + 3]));
+          }
         }
         store_state();
       }
@@ -825,12 +834,13 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     if (!ok) flag_status(a.status, KDA_DEV_TIMEOUT);
     if (a.final_state != nullptr && ok) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) a.final_state[sbase + (size_t)(64 * hh + j) * TC_V + v] = S[j];
+      for (int j = 0; j < 32; ++j) a.final_state[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
     }
+    if (tid == 0) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) tmem_dealloc(tmem, 512);
+  if (warp == kEpiWarps) tmem_dealloc(tmem, 512);
 }
 
 // Driver entry point for tensor-map encoding, looked up once.
@@ -882,20 +892,27 @@ cudaError_t launch_tc_recur(const FwdArgs& a, cudaStream_t s) {
   const Plan& p = a.plan;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
-  CUtensorMap vmap;
+  // v tiles: [64 tokens x 64 channels] boxes with 128-byte swizzle (MMA operand)
+  // o tiles: [64 tokens x 128 channels] boxes, plain row-major (output staging)
+  CUtensorMap vmap, omap;
   const cuuint64_t dims[3] = {(cuuint64_t)TC_V, (cuuint64_t)p.HV, (cuuint64_t)p.ntok};
   const cuuint64_t strides[2] = {(cuuint64_t)TC_V * 2, (cuuint64_t)p.HV * TC_V * 2};
-  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t vbox[3] = {64, 1, 64};
+  const cuuint32_t obox[3] = {128, 1, 64};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   vbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  r = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.o, dims, strides, obox, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc_recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)R_SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((size_t)p.HV * p.N));
-  tc_recur_kernel<<<grid, kRecThreads, R_SMEM, s>>>(a, vmap);
+  tc_recur_kernel<<<grid, kRecThreads, R_SMEM, s>>>(a, vmap, omap);
   return cudaGetLastError();
 }
 
