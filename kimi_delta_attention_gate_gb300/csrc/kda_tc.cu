@@ -94,20 +94,25 @@ __device__ __forceinline__ float gate_fast(float x, float a, float lb) {
 // ======================================================================================
 // tc_intra
 // ======================================================================================
-constexpr uint32_t P_QSKS = 0;       // [Qs;Ks] A operand: 128 rows x 128 ch, 2 panels x 16 KB
-constexpr uint32_t P_KA = 32768;     // [Ka_0; Ka_1; Ka_2; Ka_3] B operand: 160 rows, 2 panels x 20 KB;
-                                     // after the Aqk/Akk MMA: fp32 solve scratch
+// One CTA (256 threads, two resident per SM) per (chunk, value head).  The chunk's q, k
+// and g tiles arrive by TMA in the 128-byte-swizzled panel layout of the MMA operands and
+// are transformed in place: q, k -> [Qs; Ks] (A operand of the Aqk/Akk MMA) and g -> X =
+// e^Gamma . K (MN-major B operand of the W MMA).  The packed block goes straight from
+// registers to global memory.
+constexpr uint32_t P_QK = 0;        // 2 K-panels x [64 query rows; 64 key rows], 16 KB each;
+                                    // after the Aqk/Akk MMA: T (A operand of the W MMA)
+constexpr uint32_t P_X = 32768;     // 2 MN-panels x [64 tokens x 64 ch], 8 KB each: g, then X
+constexpr uint32_t P_KA = 49152;    // [Ka_0; Ka_1; Ka_2; Ka_3] B operand: 160 rows, 2 panels x
+                                    // 20 KB; after the Aqk/Akk MMA: fp32 solve scratch
 constexpr uint32_t KA_PANEL = 20480;
-constexpr uint32_t P_XT = 73728;     // X^T [128 ch x 64 tokens]: B operand of the W MMA
-constexpr uint32_t P_OUT = 90112;    // packed block
-constexpr uint32_t P_BETA = P_OUT + BLOCK_BYTES;  // fp32 [64]
+constexpr uint32_t P_DIAG = P_KA + 2 * KA_PANEL;  // fp32 [4][2][16][16] exact diagonal blocks;
+                                                  // later solve scratch Y [32][32]
+constexpr uint32_t P_BETA = P_DIAG + 8192;        // fp32 [64]
 constexpr uint32_t P_BSUM = P_BETA + 256;         // fp32 [4][128] block sums of the gate
 constexpr uint32_t P_ROWSQ = P_BSUM + 2048;       // fp32 [64 rows][2 halves][2 (q,k)], then norms [64][2]
-constexpr uint32_t P_DIAG = P_ROWSQ + 1536;       // fp32 [4][2][16][16] exact diagonal blocks;
-                                                  // later solve scratch Y [32][32]
-constexpr uint32_t P_DT = P_DIAG + 8192;          // fp32 [128] dt_bias row
+constexpr uint32_t P_DT = P_ROWSQ + 1536;         // fp32 [128] dt_bias row
 constexpr uint32_t P_FLAG = P_DT + 512;
-constexpr uint32_t P_BAR = P_FLAG + 16;
+constexpr uint32_t P_BAR = P_FLAG + 16;           // [0] tile loads, [1] MMA completions
 constexpr uint32_t P_TMEM = P_BAR + 16;
 constexpr uint32_t P_END = P_TMEM + 16;
 constexpr uint32_t P_SMEM = P_END + 1024;
@@ -116,8 +121,15 @@ constexpr uint32_t P_SMEM = P_END + 1024;
 __host__ __device__ constexpr uint32_t ka_row(int I) { return 8u * (uint32_t)(I * (I + 1)); }
 constexpr int SOLVE_LD = 65;
 
+__device__ __forceinline__ uint32_t lds_u32(const uint8_t* base, uint32_t off) {
+  return *reinterpret_cast<const uint32_t*>(base + off);
+}
+
 template <int GATE>
-__global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(256, 2)
+    tc_intra_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap qmap,
+                    const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap gmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const Plan& p = a.plan;
@@ -136,45 +148,31 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
   int* sFlag = reinterpret_cast<int*>(sm + P_FLAG);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + P_BAR);
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + P_TMEM);
-  uint8_t* out = sm + P_OUT;
+  uint8_t* blk = reinterpret_cast<uint8_t*>(a.ws) + p.off_inter +
+                 ((size_t)c * p.HV + hv) * p.inter_block_bytes;
+  const bool has_dt = a.dt_bias != nullptr && GATE != KDA_GATE_PREGATED;
 
   if (warp == 0) {
     tmem_alloc(sTmem, 256);
     tmem_relinquish();
   }
-  if (tid == 0) {
+  if (tid == 32) {  // tile loads: q, k -> [q; k] per channel panel, g -> 2 panels, dt_bias row
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
     fence_mbar_init();
     sFlag[0] = 0;
+    const int32_t tt = (int32_t)t0;
+    mbar_arrive_expect_tx(&bars[0], 49152u + (has_dt ? TC_K * 4u : 0u));
+    tma_load_3d(sm + P_QK, &qmap, 0, h, tt, &bars[0]);
+    tma_load_3d(sm + P_QK + 8192, &kmap, 0, h, tt, &bars[0]);
+    tma_load_3d(sm + P_QK + 16384, &qmap, 64, h, tt, &bars[0]);
+    tma_load_3d(sm + P_QK + 24576, &kmap, 64, h, tt, &bars[0]);
+    tma_load_3d(sm + P_X, &gmap, 0, hv, tt, &bars[0]);
+    tma_load_3d(sm + P_X + 8192, &gmap, 64, hv, tt, &bars[0]);
+    if (has_dt) bulk_g2s(sDt, a.dt_bias + (size_t)hv * TC_K, TC_K * 4, &bars[0]);
   }
   for (int i = tid; i < 4 * 2 * 256; i += 256) sDiag[i] = 0.f;  // exact diagonal blocks
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *sTmem;
-  if (tid == 0 && a.dt_bias != nullptr && GATE != KDA_GATE_PREGATED) {  // dt_bias row: bulk copy
-    mbar_arrive_expect_tx(&bars[1], TC_K * 4);
-    bulk_g2s(sDt, a.dt_bias + (size_t)hv * TC_K, TC_K * 4, &bars[1]);
-  }
-
-  // ---- element-wise phase: thread = 16-row block rg x channel pair (c0, c0+1) ----
-  const int rg = tid >> 6, cp = tid & 63, c0 = 2 * cp;
-  const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(a.q);
-  const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(a.k);
-  const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(a.g);
   const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.beta);
-  uint32_t q2[16], k2[16], g2[16];
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int row = 16 * rg + r;
-    q2[r] = k2[r] = g2[r] = 0u;
-    if (row < L) {
-      const int64_t tok = t0 + row;
-      q2[r] = ldg_u32(gq + (tok * p.H + h) * TC_K + c0);
-      k2[r] = ldg_u32(gk + (tok * p.H + h) * TC_K + c0);
-      g2[r] = ldg_u32(gg + (tok * p.HV + hv) * TC_K + c0);
-    }
-  }
   if (tid < TC_C) {
     float b = 0.f;
     if (tid < L) {
@@ -185,9 +183,19 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
   }
   const float lb = a.lower_bound;
   const float aexp = (GATE != KDA_GATE_PREGATED && a.A_log != nullptr) ? expf(a.A_log[hv]) : 1.f;
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  if (!mbar_wait(&bars[0], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
+
+  // ---- element-wise phase: thread = 16-row block rg x channel pair (c0, c0+1) ----
+  const int rg = tid >> 6, cp = tid & 63, c0 = 2 * cp;
+  const uint32_t pan = (uint32_t)(c0 >> 6);  // panel of this channel pair
+  const uint32_t cc = (uint32_t)(c0 & 63);
+  uint8_t* qk_pan = sm + P_QK + pan * 16384;
+  uint8_t* x_pan = sm + P_X + pan * 8192;
   float dt0 = 0.f, dt1 = 0.f;
-  if (a.dt_bias != nullptr && GATE != KDA_GATE_PREGATED) {
-    if (!mbar_wait(&bars[1], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
+  if (has_dt) {
     dt0 = sDt[c0];
     dt1 = sDt[c0 + 1];
   }
@@ -196,10 +204,12 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
   float acc0 = 0.f, acc1 = 0.f, span = 0.f;
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
+    const int row = 16 * rg + r;
     float g0 = 0.f, g1 = 0.f;
-    if (16 * rg + r < L) {
-      g0 = gate_fast<GATE>(bf_lo(g2[r]) + dt0, aexp, lb);
-      g1 = gate_fast<GATE>(bf_hi(g2[r]) + dt1, aexp, lb);
+    if (row < L) {
+      const uint32_t gv = lds_u32(x_pan, sw128_offset(row, cc));
+      g0 = gate_fast<GATE>(bf_lo(gv) + dt0, aexp, lb);
+      g1 = gate_fast<GATE>(bf_hi(gv) + dt1, aexp, lb);
     }
     acc0 = fmaf(g0, kLog2e, acc0);
     acc1 = fmaf(g1, kLog2e, acc1);
@@ -213,15 +223,17 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
   // row sums of squares of q and k (each warp covers 64 channels of its block's rows)
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
-    float sq = bf_lo(q2[r]) * bf_lo(q2[r]) + bf_hi(q2[r]) * bf_hi(q2[r]);
-    float sk = bf_lo(k2[r]) * bf_lo(k2[r]) + bf_hi(k2[r]) * bf_hi(k2[r]);
+    const int row = 16 * rg + r;
+    const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(row, cc)) : 0u;
+    const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(64 + row, cc)) : 0u;
+    float sq = bf_lo(qv) * bf_lo(qv) + bf_hi(qv) * bf_hi(qv);
+    float sk = bf_lo(kv) * bf_lo(kv) + bf_hi(kv) * bf_hi(kv);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       sq += __shfl_xor_sync(0xffffffffu, sq, o);
       sk += __shfl_xor_sync(0xffffffffu, sk, o);
     }
     if (lane == 0) {
-      const int row = 16 * rg + r;
       sRowsq[(row * 2 + (warp & 1)) * 2 + 0] = sq;
       sRowsq[(row * 2 + (warp & 1)) * 2 + 1] = sk;
     }
@@ -240,7 +252,7 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
   }
   __syncthreads();
 
-  // ---- carries, norms, factors, operand tiles ----
+  // ---- carries, factors, operand tiles ----
   float rI0[4], rI1[4];  // reference r_I = Gamma just before block I
   rI0[0] = rI1[0] = 0.f;
 #pragma unroll
@@ -254,37 +266,61 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
   const bool guard = (sFlag[0] >> rg) & 1;
   const float erb0 = ex2(rb0), erb1 = ex2(rb1);
   const float ekg0 = ex2(gl0 - rb0), ekg1 = ex2(gl1 - rb1);
-  if (rg == 0) {
-    float* dout = reinterpret_cast<float*>(out + OFF_D);
-    dout[c0] = ex2(gl0);
-    dout[c0 + 1] = ex2(gl1);
-  }
-  const uint32_t pan = (uint32_t)(c0 >> 6);  // panel of this channel pair
-  const uint32_t cc = (uint32_t)(c0 & 63);
+  if (rg == 0)
+    *reinterpret_cast<float2*>(blk + OFF_D + 4 * c0) = make_float2(ex2(gl0), ex2(gl1));
   float F0[4], F1[4];  // 2^(r_I - r_b) for the blocks I > rg that see this block's keys
 #pragma unroll
   for (int I = 0; I < 4; ++I) {
     F0[I] = (I > rg) ? ex2(rI0[I] - rb0) : 1.f;
     F1[I] = (I > rg) ? ex2(rI1[I] - rb1) : 1.f;
   }
-  // transposed tiles (X^T and Kg^T: row = channel, 16 consecutive tokens per thread) are
-  // packed two tokens per register and written as 16-byte chunks after the loop
-  uint32_t xt0[8], xt1[8], kt0[8], kt1[8];
+  if (guard) {
+    // exact diagonal block from the raw tiles (read before they are overwritten below):
+    // partial sums over this thread's two channels; every exponent Gamma_i - Gamma_j <= 0
+    // (fully unrolled: runtime indices would force G0, G1 into local memory)
+    float* dq = sDiag + rg * 512;
+    float* dk = dq + 256;
+    float kn0[16], kn1[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int rowj = 16 * rg + j;
+      const uint32_t kv = rowj < L ? lds_u32(qk_pan, sw128_offset(64 + rowj, cc)) : 0u;
+      const float knj = sNorm[2 * rowj + 1];
+      kn0[j] = bf_lo(kv) * knj;
+      kn1[j] = bf_hi(kv) * knj;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int rowi = 16 * rg + i;
+      const uint32_t qv = rowi < L ? lds_u32(qk_pan, sw128_offset(rowi, cc)) : 0u;
+      const float qn = sNorm[2 * rowi];
+      const float qi0 = bf_lo(qv) * qn, qi1 = bf_hi(qv) * qn;
+#pragma unroll
+      for (int j = 0; j <= i; ++j) {
+        const float e0 = ex2(G0[i] - G0[j]), e1 = ex2(G1[i] - G1[j]);
+        atomicAdd(&dq[i * 16 + j], qi0 * kn0[j] * e0 + qi1 * kn1[j] * e1);
+        atomicAdd(&dk[i * 16 + j], kn0[i] * kn0[j] * e0 + kn1[i] * kn1[j] * e1);
+      }
+    }
+  }
+  // Kg^T (row = channel, 16 consecutive tokens per thread) is packed two tokens per
+  // register and written as 16-byte pieces after the loop
+  uint32_t kt0[8], kt1[8];
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = 16 * rg + r;
+    const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(row, cc)) : 0u;
+    const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(64 + row, cc)) : 0u;
     const float qn = sNorm[2 * row], kn = sNorm[2 * row + 1];
-    const float q0 = bf_lo(q2[r]) * qn, q1 = bf_hi(q2[r]) * qn;
-    const float k0 = bf_lo(k2[r]) * kn, k1 = bf_hi(k2[r]) * kn;
+    const float q0 = bf_lo(qv) * qn, q1 = bf_hi(qv) * qn;
+    const float k0 = bf_lo(kv) * kn, k1 = bf_hi(kv) * kn;
     const float P0 = ex2(G0[r]), P1 = ex2(G1[r]);  // 2^(Gamma - r_b) <= 1
-    // [Qs;Ks] rows: block rg's queries at 32rg + r, keys at 32rg + 16 + r
-    sts_u32(sm + P_QSKS + pan * 16384, sw128_offset(32 * rg + r, cc), pack_bf16x2(q0 * P0, q1 * P1));
-    sts_u32(sm + P_QSKS + pan * 16384, sw128_offset(32 * rg + 16 + r, cc),
-            pack_bf16x2(k0 * P0, k1 * P1));
-    // -Qg (rows 64-127 of B1) and X^T share 2^Gamma = P 2^r_b
-    sts_u32(out + OFF_B1 + pan * 16384, sw128_offset(64 + row, cc),
+    sts_u32(qk_pan, sw128_offset(row, cc), pack_bf16x2(q0 * P0, q1 * P1));       // Qs
+    sts_u32(qk_pan, sw128_offset(64 + row, cc), pack_bf16x2(k0 * P0, k1 * P1));  // Ks
+    // -Qg (rows 64-127 of B1) and X share 2^Gamma = P 2^r_b
+    sts_u32(blk + OFF_B1 + pan * 16384, sw128_offset(64 + row, cc),
             pack_bf16x2(-q0 * P0 * erb0, -q1 * P1 * erb1));
-    const float x0 = k0 * P0 * erb0, x1 = k1 * P1 * erb1;
+    sts_u32(x_pan, sw128_offset(row, cc), pack_bf16x2(k0 * P0 * erb0, k1 * P1 * erb1));
     float kg0, kg1;
     if (!guard) {
       const float E0 = ex2(-G0[r]), E1 = ex2(-G1[r]);  // 2^(r_b - Gamma) <= 2^120
@@ -298,7 +334,7 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
       kg0 = ke0 * ekg0;
       kg1 = ke1 * ekg1;
     } else {
-      // every exponent below is <= 0; the diagonal block is evaluated exactly further down
+      // every exponent below is <= 0; the diagonal block is evaluated exactly above
 #pragma unroll
       for (int I = 0; I < 4; ++I) {
         if (I < rg) continue;
@@ -310,13 +346,9 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
       kg1 = k1 * ex2(gl1 - rb1 - G1[r]);
     }
     if (r & 1) {
-      xt0[r >> 1] = pack_bf16x2(__uint_as_float(xt0[r >> 1]), x0);
-      xt1[r >> 1] = pack_bf16x2(__uint_as_float(xt1[r >> 1]), x1);
       kt0[r >> 1] = pack_bf16x2(__uint_as_float(kt0[r >> 1]), kg0);
       kt1[r >> 1] = pack_bf16x2(__uint_as_float(kt1[r >> 1]), kg1);
     } else {  // hold the even row's value until its odd partner is computed
-      xt0[r >> 1] = __float_as_uint(x0);
-      xt1[r >> 1] = __float_as_uint(x1);
       kt0[r >> 1] = __float_as_uint(kg0);
       kt1[r >> 1] = __float_as_uint(kg1);
     }
@@ -324,35 +356,10 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
 #pragma unroll
   for (int hlf = 0; hlf < 2; ++hlf) {
     const int tcol = 16 * rg + 8 * hlf;
-    sts_v4(sm + P_XT, sw128_offset(c0, tcol), xt0[4 * hlf], xt0[4 * hlf + 1], xt0[4 * hlf + 2],
-           xt0[4 * hlf + 3]);
-    sts_v4(sm + P_XT, sw128_offset(c0 + 1, tcol), xt1[4 * hlf], xt1[4 * hlf + 1], xt1[4 * hlf + 2],
-           xt1[4 * hlf + 3]);
-    sts_v4(out + OFF_B2, sw128_offset(c0, tcol), kt0[4 * hlf], kt0[4 * hlf + 1], kt0[4 * hlf + 2],
+    sts_v4(blk + OFF_B2, sw128_offset(c0, tcol), kt0[4 * hlf], kt0[4 * hlf + 1], kt0[4 * hlf + 2],
            kt0[4 * hlf + 3]);
-    sts_v4(out + OFF_B2, sw128_offset(c0 + 1, tcol), kt1[4 * hlf], kt1[4 * hlf + 1],
+    sts_v4(blk + OFF_B2, sw128_offset(c0 + 1, tcol), kt1[4 * hlf], kt1[4 * hlf + 1],
            kt1[4 * hlf + 2], kt1[4 * hlf + 3]);
-  }
-  if (guard) {
-    // exact diagonal block: partial sums over this thread's two channels (recomputed
-    // normalised q, k; every exponent Gamma_i - Gamma_j <= 0)
-    // (fully unrolled: runtime indices would force q2, k2, G0, G1 into local memory)
-    float* dq = sDiag + rg * 512;
-    float* dk = dq + 256;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int rowi = 16 * rg + i;
-      const float qn = sNorm[2 * rowi], kni = sNorm[2 * rowi + 1];
-#pragma unroll
-      for (int j = 0; j <= i; ++j) {
-        const int rowj = 16 * rg + j;
-        const float knj = sNorm[2 * rowj + 1];
-        const float e0 = ex2(G0[i] - G0[j]), e1 = ex2(G1[i] - G1[j]);
-        const float kj0 = bf_lo(k2[j]) * knj, kj1 = bf_hi(k2[j]) * knj;
-        atomicAdd(&dq[i * 16 + j], (bf_lo(q2[i]) * kj0 * e0 + bf_hi(q2[i]) * kj1 * e1) * qn);
-        atomicAdd(&dk[i * 16 + j], (bf_lo(k2[i]) * kj0 * e0 + bf_hi(k2[i]) * kj1 * e1) * kni);
-      }
-    }
   }
   fence_async_smem();
   __syncthreads();
@@ -360,67 +367,70 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
   // ---- Aqk / Akk in one MMA: D = [Qs;Ks] [Ka_0;..;Ka_3]^T, M=128, N=160, K=128 ----
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t abase = smem_u32(sm + P_QSKS), bbase = smem_u32(sm + P_KA);
+    const uint32_t abase = smem_u32(sm + P_QK), bbase = smem_u32(sm + P_KA);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
       mma_bf16(tmem, sdesc_sw128(abase + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                sdesc_sw128(bbase + (ks >> 2) * KA_PANEL + (ks & 3) * 32, 16, 1024),
                idesc_bf16(128, 160), ks > 0);
-    mma_commit(&bars[0]);
+    mma_commit(&bars[1]);
   }
   __syncwarp();
-  if (!mbar_wait(&bars[0], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
+  if (!mbar_wait(&bars[1], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
   tc_fence_after();
 
-  // ---- epilogue A: warp w owns block w (lanes 0-15 query rows, 16-31 key rows) ----
-  float* sL = reinterpret_cast<float*>(sm + P_KA);  // Akk0 [64][65]; Ka no longer needed
-  float* sX = sL + 64 * SOLVE_LD;                   // (I + Akk0)^-1 [64][65]
-  if (warp < 4) {
-    const int w = warp;
-    const bool isk = lane >= 16;
-    const int i = 16 * w + (lane & 15);
-    const bool gw = (sFlag[0] >> w) & 1;
+  // ---- epilogue A: TMEM lanes 0-63 hold query rows, 64-127 key rows.  Row i of block I
+  // uses the 16(I+1) columns of D_I; a quadrant's two blocks span 16-column pieces 0-2
+  // (blocks 0, 1) or 3-9 (blocks 2, 3), shared by the quadrant's two warps ----
+  float* sL = reinterpret_cast<float*>(sm + P_KA);  // beta Akk0 [64][65]; Ka no longer needed
+  float* sX = sL + 64 * SOLVE_LD;                   // (I + beta Akk0)^-1 [64][65]
+  {
+    const int qd = warp & 3, hh = warp >> 2;
+    const bool isk = qd >= 2;
+    const int i = 32 * (qd & 1) + lane;
+    const int I = i >> 4;
+    const bool gw = (sFlag[0] >> I) & 1;
     const float bi = sBeta[i];
-    const float* dg = sDiag + w * 512 + (isk ? 256 : 0) + (i - 16 * w) * 16;
-#pragma unroll
-    for (int cc4 = 0; cc4 < 4; ++cc4) {
+    const float* dg = sDiag + I * 512 + (isk ? 256 : 0) + (i - 16 * I) * 16;
+    const int pc0 = (qd & 1) ? 3 : 0, pc1 = (qd & 1) ? 10 : 3;
+    for (int pc = pc0 + hh; pc < pc1; pc += 2) {
+      const int bI = pc == 0 ? 0 : (pc < 3 ? 1 : (pc < 6 ? 2 : 3));
+      const int jb = 16 * pc - (int)ka_row(bI);  // first key index of the piece
       uint32_t r[16];
-      if (cc4 <= w) {
-        tmem_ld16(tmem_addr(tmem, 32 * w, ka_row(w) + 16 * cc4), r);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int x = 0; x < 16; ++x) r[x] = 0u;
-      }
+      tmem_ld16(tmem_addr(tmem, 32 * qd, 16 * pc), r);
+      tmem_wait_ld();
+      if (I != bI) continue;
+      const bool diag = gw && jb == 16 * I;
       float vals[16];
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
-        const int j = 16 * cc4 + x;
-        float v = __uint_as_float(r[x]);
-        if (gw && cc4 == w) v = dg[x];
+        const int j = jb + x;
+        const float v = diag ? dg[x] : __uint_as_float(r[x]);
         const bool keep = isk ? (j < i) : (j <= i);
         vals[x] = keep ? v : 0.f;
       }
       if (!isk) {
 #pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          const int j0 = 16 * cc4 + 8 * hlf;
-          sts_v4(out + OFF_B2, sw128_offset(128 + i, j0),
+        for (int hlf = 0; hlf < 2; ++hlf)
+          sts_v4(blk + OFF_B2, sw128_offset(128 + i, jb + 8 * hlf),
                  pack_bf16x2(vals[8 * hlf + 0], vals[8 * hlf + 1]),
                  pack_bf16x2(vals[8 * hlf + 2], vals[8 * hlf + 3]),
                  pack_bf16x2(vals[8 * hlf + 4], vals[8 * hlf + 5]),
                  pack_bf16x2(vals[8 * hlf + 6], vals[8 * hlf + 7]));
-        }
       } else {
 #pragma unroll
-        for (int x = 0; x < 16; ++x) sL[i * SOLVE_LD + 16 * cc4 + x] = bi * vals[x];
+        for (int x = 0; x < 16; ++x) sL[i * SOLVE_LD + jb + x] = bi * vals[x];
       }
+    }
+    if (!isk && hh == 0) {  // Aqk columns past the row's block are zero
+      for (int j0 = 16 * (I + 1); j0 < TC_C; j0 += 8)
+        sts_v4(blk + OFF_B2, sw128_offset(128 + i, j0), 0u, 0u, 0u, 0u);
     }
   }
   tc_fence_before();
   __syncthreads();
 
-  // ---- solve X = (I + Akk0)^-1 by recursive halving (16 -> 32 -> 64), fp32 ----
+  // ---- solve X = (I + beta Akk0)^-1 by recursive halving (16 -> 32 -> 64), fp32 ----
   float* sY = sDiag;  // scratch
   if (tid < 64) {     // level 1: the four 16 x 16 diagonal blocks, one column per thread
     const int b = tid >> 4, col = tid & 15, base = 16 * b;
@@ -484,7 +494,7 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
     sX[(33 + i0) * SOLVE_LD + j0] = -z10; sX[(33 + i0) * SOLVE_LD + j0 + 1] = -z11;
   }
   __syncthreads();
-  // T = X Diag(beta), bf16 row-major (A operand of the W MMA and of U = T V downstream)
+  // T = X Diag(beta), bf16: A operand of the W MMA (over the dead [Qs; Ks] tile) and block
   {
     const int i = tid >> 2, j0 = (tid & 3) * 16;
 #pragma unroll
@@ -495,31 +505,36 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
         const int j = j0 + 8 * hlf + x;
         t[x] = (j <= i) ? sX[i * SOLVE_LD + j] * sBeta[j] : 0.f;
       }
-      sts_v4(out + OFF_T, sw128_offset(i, j0 + 8 * hlf), pack_bf16x2(t[0], t[1]),
-             pack_bf16x2(t[2], t[3]), pack_bf16x2(t[4], t[5]), pack_bf16x2(t[6], t[7]));
+      const uint32_t w0 = pack_bf16x2(t[0], t[1]), w1 = pack_bf16x2(t[2], t[3]);
+      const uint32_t w2 = pack_bf16x2(t[4], t[5]), w3 = pack_bf16x2(t[6], t[7]);
+      const uint32_t off = sw128_offset(i, j0 + 8 * hlf);
+      sts_v4(sm + P_QK, off, w0, w1, w2, w3);
+      sts_v4(blk + OFF_T, off, w0, w1, w2, w3);
     }
   }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
 
-  // ---- W = T X: M=64 tokens, N=128 channels, K=64 (row i in TMEM lane 32(i/16)+i%16) ----
+  // ---- W = T X: M=64 tokens, N=128 channels, K=64 (X MN-major; row i of W in TMEM
+  // lane 32(i/16)+i%16) ----
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t abase = smem_u32(out + OFF_T), bbase = smem_u32(sm + P_XT);
+    const uint32_t abase = smem_u32(sm + P_QK), bbase = smem_u32(sm + P_X);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      mma_bf16(tmem, sdesc_sw128(abase + ks * 32, 16, 1024), sdesc_sw128(bbase + ks * 32, 16, 1024),
-               idesc_bf16(64, 128), ks > 0);
-    mma_commit(&bars[0]);
+      mma_bf16(tmem, sdesc_sw128(abase + ks * 32, 16, 1024),
+               sdesc_sw128(bbase + ks * 2048, 8192, 1024), idesc_bf16(64, 128, false, true),
+               ks > 0);
+    mma_commit(&bars[1]);
   }
   __syncwarp();
-  if (!mbar_wait(&bars[0], 1)) flag_status(a.status, KDA_DEV_TIMEOUT);
+  if (!mbar_wait(&bars[1], 1)) flag_status(a.status, KDA_DEV_TIMEOUT);
   tc_fence_after();
   {
     const int q4 = warp & 3, hh = warp >> 2;
     const int i = 16 * q4 + (lane & 15);
-    uint8_t* wp = out + OFF_B1 + hh * 16384;  // rows 0-63 of panel hh
+    uint8_t* wp = blk + OFF_B1 + hh * 16384;  // rows 0-63 of panel hh
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
       uint32_t r[16];
@@ -536,15 +551,7 @@ __global__ void __launch_bounds__(256, 1) tc_intra_kernel(const FwdArgs a) {
       }
     }
   }
-  fence_async_smem();
   tc_fence_before();
-  __syncthreads();
-  if (tid == 0) {
-    uint8_t* dst = reinterpret_cast<uint8_t*>(a.ws) + p.off_inter + ((size_t)c * p.HV + hv) * p.inter_block_bytes;
-    bulk_s2g(dst, out, BLOCK_BYTES);
-    bulk_commit();
-    bulk_wait0();
-  }
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
@@ -870,13 +877,35 @@ size_t tc_inter_block_bytes() { return BLOCK_BYTES; }
 cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s) {
   const Plan& p = a.plan;
   if (p.nct == 0) return cudaSuccess;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // q, k, g tiles: [64 tokens x 64 channels] boxes with 128-byte swizzle (MMA operands)
+  CUtensorMap qmap, kmap, gmap;
+  const cuuint64_t qdims[3] = {(cuuint64_t)TC_K, (cuuint64_t)p.H, (cuuint64_t)p.ntok};
+  const cuuint64_t qstr[2] = {(cuuint64_t)TC_K * 2, (cuuint64_t)p.H * TC_K * 2};
+  const cuuint64_t gdims[3] = {(cuuint64_t)TC_K, (cuuint64_t)p.HV, (cuuint64_t)p.ntok};
+  const cuuint64_t gstr[2] = {(cuuint64_t)TC_K * 2, (cuuint64_t)p.HV * TC_K * 2};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), qdims, qstr,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  r = enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k), qdims, qstr, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  r = enc(&gmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.g), gdims, gstr, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)p.nct, (unsigned)p.HV);
   cudaError_t e;
 #define KDA_LAUNCH_INTRA(G)                                                                  \
   e = cudaFuncSetAttribute(tc_intra_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                            (int)P_SMEM);                                                     \
   if (e != cudaSuccess) return e;                                                            \
-  tc_intra_kernel<G><<<grid, 256, P_SMEM, s>>>(a);
+  tc_intra_kernel<G><<<grid, 256, P_SMEM, s>>>(a, qmap, kmap, gmap);
   if (a.gate_mode == KDA_GATE_SAFE) {
     KDA_LAUNCH_INTRA(KDA_GATE_SAFE)
   } else if (a.gate_mode == KDA_GATE_PLAIN) {
