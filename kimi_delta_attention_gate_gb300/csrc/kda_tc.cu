@@ -77,9 +77,15 @@ __device__ __forceinline__ void sts_v4(uint8_t* base, uint32_t off, uint32_t a, 
                                        uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4*>(base + off) = make_uint4(a, b, c, d);
 }
-// sigmoid through ex2 / rcp: absolute error ~1e-7, far below bf16 resolution
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// sigmoid through ex2 / rcp (hardware approximations): absolute error ~1e-7, far below
+// bf16 resolution
 __device__ __forceinline__ float sigmoid_fast(float x) {
-  return __frcp_rn(1.0f + ex2(-x * kLog2e));
+  return rcp_approx(1.0f + ex2(-x * kLog2e));
 }
 __device__ __forceinline__ float softplus_fast(float x) {
   return x > 20.0f ? x : log1pf(ex2(x * kLog2e));
@@ -172,15 +178,11 @@ __global__ void __launch_bounds__(256, 2)
     if (has_dt) bulk_g2s(sDt, a.dt_bias + (size_t)hv * TC_K, TC_K * 4, &bars[0]);
   }
   for (int i = tid; i < 4 * 2 * 256; i += 256) sDiag[i] = 0.f;  // exact diagonal blocks
+  // beta is read here and published to shared memory only after the tile wait, so that
+  // its load latency overlaps the TMA loads
   const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.beta);
-  if (tid < TC_C) {
-    float b = 0.f;
-    if (tid < L) {
-      b = __bfloat162float(gb[(t0 + tid) * p.HV + hv]);
-      if (a.beta_sigmoid) b = sigmoid_fast(b);
-    }
-    sBeta[tid] = b;
-  }
+  __nv_bfloat16 beta_raw = __float2bfloat16_rn(0.f);
+  if (tid < L && tid < TC_C) beta_raw = gb[(t0 + tid) * p.HV + hv];
   const float lb = a.lower_bound;
   const float aexp = (GATE != KDA_GATE_PREGATED && a.A_log != nullptr) ? expf(a.A_log[hv]) : 1.f;
   __syncthreads();
@@ -220,22 +222,42 @@ __global__ void __launch_bounds__(256, 2)
   sBsum[rg * 128 + c0] = acc0;
   sBsum[rg * 128 + c0 + 1] = acc1;
   if (span > kGuardLog2) atomicOr(sFlag, 1 << rg);
-  // row sums of squares of q and k (each warp covers 64 channels of its block's rows)
+  if (tid < TC_C) {
+    float b = __bfloat162float(beta_raw);
+    if (a.beta_sigmoid && tid < L) b = sigmoid_fast(b);
+    sBeta[tid] = b;
+  }
+  // row sums of squares of q and k over the warp's 64 channels: a butterfly that halves
+  // the rows each lane carries at every step (16 shuffles per tile instead of 80); at the
+  // end lanes 2m and 2m+1 hold the sum of row rsel(m)
+  {
+    float sq[16], sk[16];
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int row = 16 * rg + r;
-    const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(row, cc)) : 0u;
-    const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(64 + row, cc)) : 0u;
-    float sq = bf_lo(qv) * bf_lo(qv) + bf_hi(qv) * bf_hi(qv);
-    float sk = bf_lo(kv) * bf_lo(kv) + bf_hi(kv) * bf_hi(kv);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    for (int r = 0; r < 16; ++r) {
+      const int row = 16 * rg + r;
+      const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(row, cc)) : 0u;
+      const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(64 + row, cc)) : 0u;
+      sq[r] = bf_lo(qv) * bf_lo(qv) + bf_hi(qv) * bf_hi(qv);
+      sk[r] = bf_lo(kv) * bf_lo(kv) + bf_hi(kv) * bf_hi(kv);
     }
-    if (lane == 0) {
-      sRowsq[(row * 2 + (warp & 1)) * 2 + 0] = sq;
-      sRowsq[(row * 2 + (warp & 1)) * 2 + 1] = sk;
+#pragma unroll
+    for (int hw = 8; hw >= 1; hw >>= 1) {  // keep rows [hw, 2hw) if the lane bit is set
+      const bool up = (lane & (2 * hw)) != 0;
+#pragma unroll
+      for (int x = 0; x < hw; ++x) {
+        const float qs = up ? sq[x] : sq[x + hw], ks = up ? sk[x] : sk[x + hw];
+        const float qk_ = up ? sq[x + hw] : sq[x], kk_ = up ? sk[x + hw] : sk[x];
+        sq[x] = qk_ + __shfl_xor_sync(0xffffffffu, qs, 2 * hw);
+        sk[x] = kk_ + __shfl_xor_sync(0xffffffffu, ks, 2 * hw);
+      }
+    }
+    sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 1);
+    sk[0] += __shfl_xor_sync(0xffffffffu, sk[0], 1);
+    if ((lane & 1) == 0) {
+      const int row = 16 * rg + ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 +
+                      ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+      sRowsq[(row * 2 + (warp & 1)) * 2 + 0] = sq[0];
+      sRowsq[(row * 2 + (warp & 1)) * 2 + 1] = sk[0];
     }
   }
   __syncthreads();
@@ -432,20 +454,28 @@ __global__ void __launch_bounds__(256, 2)
 
   // ---- solve X = (I + beta Akk0)^-1 by recursive halving (16 -> 32 -> 64), fp32 ----
   float* sY = sDiag;  // scratch
-  if (tid < 64) {     // level 1: the four 16 x 16 diagonal blocks, one column per thread
+  if (tid < 64) {     // level 1: the four 16 x 16 diagonal blocks, one column per thread,
+                      // right-looking so that each step adds one FMA to the dependent chain
     const int b = tid >> 4, col = tid & 15, base = 16 * b;
-    float x[16];
+    float x[16], sacc[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
+    for (int i = 0; i < 16; ++i) sacc[i] = 0.f;
 #pragma unroll
-    for (int i = 1; i < 16; ++i) {
-      float s = 0.f;
+    for (int m = 0; m < 16; ++m) {
+      x[m] = (m == col) ? 1.f : ((m > col) ? -sacc[m] : 0.f);
 #pragma unroll
-      for (int m = 0; m < i; ++m) s = fmaf(sL[(base + i) * SOLVE_LD + base + m], x[m], s);
-      x[i] = (i > col) ? -s : x[i];
+      for (int i = m + 1; i < 16; ++i)
+        sacc[i] = fmaf(sL[(base + i) * SOLVE_LD + base + m], x[m], sacc[i]);
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) sX[(base + i) * SOLVE_LD + base + col] = x[i];
+  } else if (tid < 128) {  // the upper-right 16 x 16 of each 32 x 32 diagonal block is zero
+    const int e = tid - 64;  // 64 threads x 8 entries
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const int f = 8 * e + x, pr = f >> 8, i = (f >> 4) & 15, j = f & 15;
+      sX[(32 * pr + i) * SOLVE_LD + 32 * pr + 16 + j] = 0.f;
+    }
   }
   __syncthreads();
   {  // level 2: X_{2p+1,2p} = -X_{2p+1,2p+1} (L_{2p+1,2p} X_{2p,2p}), p = 0, 1
@@ -471,10 +501,12 @@ __global__ void __launch_bounds__(256, 2)
     __syncthreads();
   }
   {  // level 3: X_{B,A} = -X_BB (L_BA X_AA), A = 0..31, B = 32..63; 2 x 2 tile per thread
+     // (full-length unrolled sums: the zero upper blocks of X_AA, X_BB mask themselves)
     const int ti = tid >> 4, tj = tid & 15;
     const int i0 = 2 * ti, j0 = 2 * tj;
     float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-    for (int m = j0; m < 32; ++m) {  // X_AA is lower triangular: rows m >= j
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
       const float l0 = sL[(32 + i0) * SOLVE_LD + m], l1 = sL[(33 + i0) * SOLVE_LD + m];
       const float xa = sX[m * SOLVE_LD + j0], xb = sX[m * SOLVE_LD + j0 + 1];
       y00 = fmaf(l0, xa, y00); y01 = fmaf(l0, xb, y01);
@@ -484,7 +516,8 @@ __global__ void __launch_bounds__(256, 2)
     sY[(i0 + 1) * 32 + j0] = y10; sY[(i0 + 1) * 32 + j0 + 1] = y11;
     __syncthreads();
     float z00 = 0.f, z01 = 0.f, z10 = 0.f, z11 = 0.f;
-    for (int m = 0; m <= i0 + 1; ++m) {  // X_BB is lower triangular: columns m <= i
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
       const float xa = sX[(32 + i0) * SOLVE_LD + 32 + m], xb = sX[(33 + i0) * SOLVE_LD + 32 + m];
       const float ya = sY[m * 32 + j0], yb = sY[m * 32 + j0 + 1];
       z00 = fmaf(xa, ya, z00); z01 = fmaf(xa, yb, z01);
