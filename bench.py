@@ -349,11 +349,15 @@ def main():
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
-    def step(evs=None):
+    n_launch = kb.kda_fwd_num_launches(p)
+
+    def step():  # one forward pass through the C ABI (the pipelined schedule, if any)
+        kb.raise_for(kb.kda_fwd(p, sh))
+
+    def stage_step(evs):  # the same pass stage by stage, an event after every kernel
         for i in range(nst):
             kb.raise_for(kb.kda_fwd_stage(p, sh, i))
-            if evs is not None:
-                evs[i].record(stream)
+            evs[i].record(stream)
 
     sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else local_rank)
     sampler.start()
@@ -364,23 +368,32 @@ def main():
     if status != 0:
         raise RuntimeError(f"device status {status:#x} after warm-up")
 
-    # Timed region: K steps, events after every stage on the launching stream.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(args.steps)]
+    # Timed region: K forward passes on the launching stream, CUDA events around them.
     start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     start.record(stream)
     for s_ in range(args.steps):
-        step(evs[s_])
-    barrier_ev = evs[-1][-1]
+        step()
+    stop.record(stream)
     torch.cuda.synchronize()
     barrier()
     t_wall1 = time.time()
     clocks = sampler.stop(t_wall0, t_wall1)
-    total_ms = start.elapsed_time(barrier_ev)
+    total_ms = start.elapsed_time(stop)
+    # Per-kernel durations (roofline of the dominant kernel): the same K passes stage by
+    # stage, each kernel alone on the stream between two events.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(args.steps)]
+    s0 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s0.record(stream)
+    for s_ in range(args.steps):
+        stage_step(evs[s_])
+    torch.cuda.synchronize()
     stage_ms = np.zeros(nst)
-    prev = start
+    prev = s0
     for s_ in range(args.steps):
         for i in range(nst):
             stage_ms[i] += prev.elapsed_time(evs[s_][i])
@@ -461,7 +474,7 @@ def main():
             "stages": {n: float(t) for n, t in zip(names, stage_ms)},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
-            "gpu_launches": int(nst * args.steps), "clocks": clocks,
+            "gpu_launches": int(n_launch * args.steps), "clocks": clocks,
             "kernel_source_sha": kernel_source_hash()}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -111,19 +111,34 @@ kda_status kda_fwd_check(const kda_fwd_params* p);
 /* The forward pass, enqueued on `stream` (a cudaStream_t; NULL = legacy default
    stream).  Asynchronous: returns once the kernels are enqueued.  Writes o and,
    if non-NULL, final_state.  Rows of o that no sequence covers (varlen padding)
-   are left untouched.  Returns KDA_ERR_CUDA if a launch fails. */
+   are left untouched.  Returns KDA_ERR_CUDA if a launch fails.
+   When few (sequence, value head) recurrences would leave most SMs idle (bf16
+   tensor-core path, N * HV <= 96, at least 128 chunks), the chunk range is cut
+   into up to 16 segments: the intra-chunk kernel of segment k+1 runs on `stream`
+   while the recurrence of segment k runs on a library-owned high-priority stream
+   of the current device, the fp32 state carried between segments in the
+   workspace.  The work is still ordered after everything enqueued on `stream`
+   before the call and before everything enqueued after it (event fork / join,
+   valid under stream capture); the results are bit-identical to the stages run
+   one after another.  kda_fwd_num_launches gives the kernel count. */
 kda_status kda_fwd(const kda_fwd_params* p, void* stream);
 
 /* Number of kernel launches one kda_fwd call makes for these parameters (0 if
    they are invalid).  Host only; makes no CUDA call. */
+int32_t kda_fwd_num_launches(const kda_fwd_params* p);
+
+/* Number of stages of the forward pass for these parameters (0 if they are
+   invalid): chunk table (varlen only), intra-chunk kernel, recurrence kernel.
+   Host only; makes no CUDA call. */
 int32_t kda_fwd_num_stages(const kda_fwd_params* p);
 
 /* Name of stage `stage` (0 <= stage < kda_fwd_num_stages), "" if out of range. */
 const char* kda_fwd_stage_name(const kda_fwd_params* p, int32_t stage);
 
-/* Enqueue only stage `stage` of kda_fwd on `stream`.  Calling every stage in
-   order on one stream is exactly kda_fwd; the split exists so that a caller can
-   put timing events between the kernels.  Same checks and errors as kda_fwd. */
+/* Enqueue only stage `stage` of kda_fwd on `stream`, as one launch over the whole
+   chunk range.  Calling every stage in order on one stream computes exactly what
+   kda_fwd computes (bit-identical); the split exists so that a caller can put
+   timing events between the kernels.  Same checks and errors as kda_fwd. */
 kda_status kda_fwd_stage(const kda_fwd_params* p, void* stream, int32_t stage);
 
 /* Size of the static device scratch that kda_fwd_noalloc uses: 32 MiB. */

@@ -32,7 +32,8 @@ KDA_DEV_BAD_SEQLENS = 0x1
 KDA_DEV_TIMEOUT = 0x2
 
 # Every symbol the header declares.
-EXPORTED = ("kda_fwd_workspace_size", "kda_fwd_check", "kda_fwd", "kda_fwd_num_stages",
+EXPORTED = ("kda_fwd_workspace_size", "kda_fwd_check", "kda_fwd", "kda_fwd_num_launches",
+            "kda_fwd_num_stages",
             "kda_fwd_stage_name", "kda_fwd_stage", "kda_get_device_status", "kda_status_string",
             "kda_last_error", "kda_abi_version", "kda_fwd_noalloc")
 
@@ -88,6 +89,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kda_fwd.argtypes = [P, ctypes.c_void_p]
             lib.kda_fwd_noalloc.restype = ctypes.c_int
             lib.kda_fwd_noalloc.argtypes = [P, ctypes.c_void_p]
+            lib.kda_fwd_num_launches.restype = ctypes.c_int32
+            lib.kda_fwd_num_launches.argtypes = [P]
             lib.kda_fwd_num_stages.restype = ctypes.c_int32
             lib.kda_fwd_num_stages.argtypes = [P]
             lib.kda_fwd_stage_name.restype = ctypes.c_char_p
@@ -120,6 +123,10 @@ def kda_fwd(p: kda_fwd_params, stream: int = 0) -> int:
 
 def kda_fwd_noalloc(p: kda_fwd_params, stream: int = 0) -> int:
     return int(load().kda_fwd_noalloc(ctypes.byref(p), ctypes.c_void_p(stream)))
+
+
+def kda_fwd_num_launches(p: kda_fwd_params) -> int:
+    return int(load().kda_fwd_num_launches(ctypes.byref(p)))
 
 
 def kda_fwd_num_stages(p: kda_fwd_params) -> int:

@@ -39,6 +39,12 @@ bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(pt
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Pipelined schedule limits: segment only when at most this many (sequence, value head)
+// recurrences run (each takes one SM), with at least kSegChunks chunks per segment.
+constexpr int64_t kSegMaxRecurrences = 96;
+constexpr int64_t kSegChunks = 64;
+constexpr int kMaxSegments = 16;
+
 // Every check that needs no workspace and no CUDA call.
 kda_status check_args(const kda_fwd_params* p) {
   if (p == nullptr) return fail(KDA_ERR_INVALID_ARG, "params is NULL");
@@ -135,8 +141,87 @@ Plan make_plan(const kda_fwd_params* p) {
   pl.inter_block_bytes =
       pl.tensor_core ? tc_inter_block_bytes() : simt_inter_block_bytes(pl.C, pl.K, pl.V);
   off += pl.inter_block_bytes * (size_t)pl.nct * (size_t)pl.HV;
+  // Pipelined schedule: when few (sequence, head) recurrences leave most SMs idle during
+  // the recurrence, the chunk range is cut into segments so that the intra-chunk kernel of
+  // segment k+1 runs beside the recurrence of segment k.
+  pl.nseg = 1;
+  pl.off_state = 0;
+  if (pl.tensor_core && (int64_t)pl.N * pl.HV <= kSegMaxRecurrences) {
+    int64_t ns = pl.nct / kSegChunks;
+    pl.nseg = (int)(ns < 1 ? 1 : (ns > kMaxSegments ? kMaxSegments : ns));
+  }
+  if (pl.nseg > 1) {
+    off = round_up(off, 256);
+    pl.off_state = off;
+    off += sizeof(float) * (size_t)pl.N * pl.HV * pl.K * pl.V;
+  }
   pl.total_bytes = off;
   return pl;
+}
+
+// Internal high-priority stream and events of the pipelined schedule, one set per device.
+struct PipeCtx {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t rs = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t seg[kMaxSegments] = {};
+};
+PipeCtx g_pipe[64];
+
+PipeCtx* pipe_ctx() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  PipeCtx& c = g_pipe[dev];
+  std::lock_guard<std::mutex> lk(c.mu);
+  if (!c.ready) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithPriority(&c.rs, cudaStreamNonBlocking, greatest) != cudaSuccess)
+      return nullptr;
+    if (cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+    for (int i = 0; i < kMaxSegments; ++i)
+      if (cudaEventCreateWithFlags(&c.seg[i], cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    c.ready = true;
+  }
+  return &c;
+}
+
+// Segments k = 0..nseg-1: intra(k) on the caller's stream, recur(k) on the internal
+// high-priority stream after intra(k) and recur(k-1); the caller's stream then waits for
+// the last recurrence.  Stream order alone carries every dependency (no kernel waits on
+// another), so the schedule is also valid under stream capture.
+cudaError_t launch_pipelined(const FwdArgs& a, cudaStream_t s, const char** what) {
+  const Plan& pl = a.plan;
+  PipeCtx* cx = pipe_ctx();
+  *what = "pipeline setup";
+  if (cx == nullptr) return cudaErrorInitializationError;
+  std::lock_guard<std::mutex> lk(cx->mu);
+  cudaError_t e;
+  if (pl.varlen) {
+    *what = "chunk_table";
+    if ((e = launch_chunk_table(a, s)) != cudaSuccess) return e;
+  }
+  *what = "pipeline fork";
+  if ((e = cudaEventRecord(cx->fork, s)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(cx->rs, cx->fork, 0)) != cudaSuccess) return e;
+  for (int k = 0; k < pl.nseg; ++k) {
+    FwdArgs ak = a;
+    ak.c_begin = pl.nct * k / pl.nseg;
+    ak.c_end = pl.nct * (k + 1) / pl.nseg;
+    *what = "tc_intra";
+    if ((e = launch_tc_intra(ak, s)) != cudaSuccess) return e;
+    *what = "pipeline event";
+    if ((e = cudaEventRecord(cx->seg[k], s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(cx->rs, cx->seg[k], 0)) != cudaSuccess) return e;
+    *what = "tc_recur";
+    if ((e = launch_tc_recur(ak, cx->rs)) != cudaSuccess) return e;
+  }
+  *what = "pipeline join";
+  if ((e = cudaEventRecord(cx->join, cx->rs)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(s, cx->join, 0);
 }
 
 std::mutex g_status_mu;
@@ -196,6 +281,8 @@ kda_status prepare(const kda_fwd_params* p, FwdArgs& a) {
   a.o = p->o; a.final_state = p->final_state;
   a.ws = static_cast<char*>(p->workspace);
   a.status = status;
+  a.c_begin = 0;
+  a.c_end = pl.nct;
   return KDA_OK;
 }
 
@@ -242,6 +329,13 @@ kda_status kda_fwd(const kda_fwd_params* p, void* stream) {
   FwdArgs a;
   kda_status s = prepare(p, a);
   if (s != KDA_OK) return s;
+  if (a.plan.nseg > 1) {
+    const char* what = "";
+    cudaError_t e = launch_pipelined(a, static_cast<cudaStream_t>(stream), &what);
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "%s failed: %s", what, cudaGetErrorString(e));
+    t_last_error.clear();
+    return KDA_OK;
+  }
   Stage st[kMaxStages];
   const int n = stages_for(a.plan, st);
   for (int i = 0; i < n; ++i) {
@@ -251,6 +345,14 @@ kda_status kda_fwd(const kda_fwd_params* p, void* stream) {
   }
   t_last_error.clear();
   return KDA_OK;
+}
+
+int32_t kda_fwd_num_launches(const kda_fwd_params* p) {
+  if (check_args(p) != KDA_OK) return 0;
+  const Plan pl = make_plan(p);
+  if (pl.nseg > 1) return (pl.varlen ? 1 : 0) + 2 * pl.nseg;
+  Stage st[kMaxStages];
+  return stages_for(pl, st);
 }
 
 int32_t kda_fwd_num_stages(const kda_fwd_params* p) {

@@ -24,6 +24,8 @@ struct Plan {
   size_t off_inter;         // per chunk-head intermediates
   size_t inter_block_bytes; // bytes per (chunk, value head)
   bool tensor_core;         // bf16 tensor-core kernels (else the fp32 CUDA-core kernels)
+  int nseg;                 // chunk-range segments of the pipelined tensor-core schedule
+  size_t off_state;         // fp32 [N][HV][K][V] states carried between segments (nseg > 1)
   size_t total_bytes;
 };
 
@@ -45,6 +47,7 @@ struct FwdArgs {
   float* final_state;
   char* ws;                 // workspace base
   unsigned int* status;     // device status word
+  int64_t c_begin, c_end;   // global chunk range of this launch (tensor-core kernels)
 };
 
 // ---------------------------------------------------------------------------------------

@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(256, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const Plan& p = a.plan;
-  const int64_t c = blockIdx.x;
+  const int64_t c = a.c_begin + blockIdx.x;
   const int hv = blockIdx.y;
   const int h = hv / p.G;
   int n, L;
@@ -637,6 +637,22 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   const int n = (int)(blockIdx.x / HV);
   int64_t bos, eos, cfirst;
   if (!seq_range(a, n, bos, eos, cfirst)) return;
+  // the part of the sequence inside this launch's chunk range [c_begin, c_end)
+  const int64_t nch_seq = (eos - bos + TC_C - 1) / TC_C;
+  const int64_t lo = cfirst > a.c_begin ? cfirst : a.c_begin;
+  const int64_t hi = cfirst + nch_seq < a.c_end ? cfirst + nch_seq : a.c_end;
+  bool mine = lo < hi;
+  if (nch_seq == 0)  // an empty sequence: one launch passes its initial state through
+    mine = (a.c_begin <= cfirst && cfirst < a.c_end) || (cfirst == a.c_end && a.c_end == p.nct);
+  if (!mine) return;
+  const bool seq_start = nch_seq == 0 || lo == cfirst;
+  const bool seq_end = nch_seq == 0 || hi == cfirst + nch_seq;
+  const int64_t nch = nch_seq == 0 ? 0 : hi - lo;
+  if (nch_seq > 0) {
+    bos += (lo - cfirst) * TC_C;
+    cfirst = lo;
+  }
+  float* carry = reinterpret_cast<float*>(a.ws + p.off_state);  // states between segments
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + R_BAR);
   uint64_t* bar_v = full + 2;
@@ -657,7 +673,6 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sTmem;
-  const int64_t nch = (eos - bos + TC_C - 1) / TC_C;
   bool ok = true;
 
   if (warp == kEpiWarps) {
@@ -755,7 +770,8 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     float S[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      S[j] = (a.h0 != nullptr) ? a.h0[sbase + (size_t)(32 * part + j) * TC_V + v] : 0.f;
+      S[j] = !seq_start ? carry[sbase + (size_t)(32 * part + j) * TC_V + v]
+             : (a.h0 != nullptr) ? a.h0[sbase + (size_t)(32 * part + j) * TC_V + v] : 0.f;
     uint8_t* st_row = sm + R_ST + (part >> 1) * 16384;  // K panel holding channels 32 part..
     const int st_col = 32 * (part & 1);
     auto store_state = [&]() {
@@ -872,9 +888,10 @@ __global__ void __launch_bounds__(kRecThreads, 1)
       ok = drain_o(nch - 1);
     }
     if (!ok) flag_status(a.status, KDA_DEV_TIMEOUT);
-    if (a.final_state != nullptr && ok) {
+    float* sout = seq_end ? a.final_state : carry;
+    if (sout != nullptr && ok) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) a.final_state[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
+      for (int j = 0; j < 32; ++j) sout[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
     }
     if (tid == 0) bulk_wait0();
   }
@@ -909,7 +926,7 @@ size_t tc_inter_block_bytes() { return BLOCK_BYTES; }
 
 cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s) {
   const Plan& p = a.plan;
-  if (p.nct == 0) return cudaSuccess;
+  if (a.c_end <= a.c_begin) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   // q, k, g tiles: [64 tokens x 64 channels] boxes with 128-byte swizzle (MMA operands)
@@ -932,7 +949,7 @@ cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s) {
           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)p.nct, (unsigned)p.HV);
+  const dim3 grid((unsigned)(a.c_end - a.c_begin), (unsigned)p.HV);
   cudaError_t e;
 #define KDA_LAUNCH_INTRA(G)                                                                  \
   e = cudaFuncSetAttribute(tc_intra_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, \

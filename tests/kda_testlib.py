@@ -90,3 +90,29 @@ def assert_close(got, ref, dtype: str, what: str):
     if tol["max_abs"] is not None:
         assert mx <= tol["max_abs"], f"{what}: max-abs {mx:.3e} > {tol['max_abs']:.0e}"
     return rel, mx
+
+
+def run_gpu_stages(inp: kin.Inputs):
+    """The CUDA path on ``inp`` through the per-stage entry point: every stage is one
+    launch over the whole chunk range, in order, on the current stream."""
+    import torch
+    import kimi_delta_attention_gate_gb300 as kda
+    from kimi_delta_attention_gate_gb300 import _binding as kb
+    wl = inp.wl
+    q, k, v, g, b = (to_device(x, wl.dtype) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    cu = None if inp.cu_seqlens is None else torch.from_numpy(inp.cu_seqlens).cuda()
+    cu_cpu = None if inp.cu_seqlens is None else torch.from_numpy(inp.cu_seqlens)
+    o = torch.zeros((wl.B, wl.T, wl.HV, wl.V), dtype=v.dtype, device="cuda")
+    fs = torch.empty((inp.N, wl.HV, wl.K, wl.V), dtype=torch.float32, device="cuda")
+    p = kda.make_params(q, k, v, g, b, A_log=f32_device(inp.A_log), dt_bias=f32_device(inp.dt_bias),
+                        scale=inp.scale, initial_state=f32_device(inp.h0), final_state=fs, o=o,
+                        cu_seqlens=cu, cu_seqlens_cpu=cu_cpu, chunk_size=wl.chunk_size,
+                        **gate_kwargs(wl))
+    ws = torch.empty(max(kb.kda_fwd_workspace_size(p), 1), dtype=torch.uint8, device="cuda")
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    sh = torch.cuda.current_stream().cuda_stream
+    for i in range(kb.kda_fwd_num_stages(p)):
+        kb.raise_for(kb.kda_fwd_stage(p, sh, i))
+    torch.cuda.synchronize()
+    assert kb.kda_get_device_status(sh) == 0
+    return o.float().cpu().double().numpy(), fs.cpu().double().numpy()

@@ -211,3 +211,36 @@ def test_tc_path_is_selected():
     p = kda.make_params(q, q, v, v, b, lower_bound=-5.0, o=v)
     names = [kb.kda_fwd_stage_name(p, i) for i in range(kb.kda_fwd_num_stages(p))]
     assert names == ["tc_intra", "tc_recur"]
+
+
+# ---- pipelined schedule: segments of the chunk range on two streams ---------------------------
+
+def check_pipelined(inp):
+    from kda_testlib import run_gpu_stages
+    o, fs = run_gpu(inp)
+    ro, rfs = run_oracle(inp)
+    assert_close(o, ro, "bf16", "o")
+    assert_close(fs, rfs, "bf16", "final_state")
+    # the carried fp32 state makes the segmented schedule bit-identical to one launch per stage
+    so, sfs = run_gpu_stages(inp)
+    assert np.array_equal(o, so) and np.array_equal(fs, sfs)
+
+
+@pytest.mark.parametrize("gate", [kin.GATE_SAFE, kin.GATE_PLAIN])
+def test_tc_pipelined_one_long_sequence(gate):
+    """129 chunks of one sequence: two segments, the state carried between them."""
+    check_pipelined(kin.make_inputs(tc(T=64 * 128 + 37, gate=gate, seed=400 + gate)))
+
+
+def test_tc_pipelined_batch_boundary_inside_a_sequence():
+    """B=3 x 44 chunks: the segment boundary (chunk 66) falls inside the second sequence."""
+    check_pipelined(kin.make_inputs(tc(B=3, T=64 * 43 + 10, seed=405)))
+
+
+def test_tc_pipelined_varlen_with_empty_sequences():
+    """Varlen with an empty sequence in the middle and one at the end; the boundary (chunk
+    67) falls inside the third sequence."""
+    wl = tc(T=8537, varlen=5, maxlen=4600, seed=410)
+    inp = kin.make_inputs(wl)
+    inp.cu_seqlens[:] = np.array([0, 4000, 4000, 8500, 8537, 8537], dtype=np.int64)
+    check_pipelined(inp)
