@@ -14,7 +14,7 @@
 //               V_new^T = V^T T^T - S^T W^T          (T = A Diag(beta))
 //               O^T     = S^T Qg^T + V_new^T Aqk^T
 //               S^T     = S^T Diag(e^gamma_C) + V_new^T Kg
-//             S^T stays in registers in fp32 and is rounded to bf16 only as an MMA
+//             S^T stays in tensor memory in fp32 and is rounded to bf16 only as an MMA
 //             operand.
 //
 // Exponent range (FLA-KDA engineering notes, section 3): the decay inside a chunk
@@ -44,9 +44,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kGuardLog2 = 120.0f;
 
 // Packed block (bytes).  All panels 1024-byte aligned within the block.
-//   B1 = [W; -Qg]   [128 rows x 128 ch]: panel p (16 KB) holds channels 64p..64p+63,
-//                   rows 0-63 = W (tokens), rows 64-127 = -Qg (tokens)
-//   B2 = [Kg^T; Aqk] [192 rows x 64 tokens]: rows 0-127 = Kg^T (channels), 128-191 = Aqk
+//   B1 = [-W; Qg]   [128 rows x 128 ch]: panel p (16 KB) holds channels 64p..64p+63,
+//                   rows 0-63 = -W (tokens), rows 64-127 = Qg (tokens)
+//   B2 = [Aqk; Kg^T] [192 rows x 64 tokens]: rows 0-63 = Aqk, 64-191 = Kg^T (channels)
 //   T  = A Diag(beta) [64 x 64];  D = e^gamma_C fp32 [128]
 constexpr uint32_t OFF_B1 = 0;
 constexpr uint32_t OFF_B2 = 32768;
@@ -339,9 +339,9 @@ __global__ void __launch_bounds__(256, 2)
     const float P0 = ex2(G0[r]), P1 = ex2(G1[r]);  // 2^(Gamma - r_b) <= 1
     sts_u32(qk_pan, sw128_offset(row, cc), pack_bf16x2(q0 * P0, q1 * P1));       // Qs
     sts_u32(qk_pan, sw128_offset(64 + row, cc), pack_bf16x2(k0 * P0, k1 * P1));  // Ks
-    // -Qg (rows 64-127 of B1) and X share 2^Gamma = P 2^r_b
+    // Qg (rows 64-127 of B1) and X share 2^Gamma = P 2^r_b
     sts_u32(blk + OFF_B1 + pan * 16384, sw128_offset(64 + row, cc),
-            pack_bf16x2(-q0 * P0 * erb0, -q1 * P1 * erb1));
+            pack_bf16x2(q0 * P0 * erb0, q1 * P1 * erb1));
     sts_u32(x_pan, sw128_offset(row, cc), pack_bf16x2(k0 * P0 * erb0, k1 * P1 * erb1));
     float kg0, kg1;
     if (!guard) {
@@ -378,9 +378,9 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
   for (int hlf = 0; hlf < 2; ++hlf) {
     const int tcol = 16 * rg + 8 * hlf;
-    sts_v4(blk + OFF_B2, sw128_offset(c0, tcol), kt0[4 * hlf], kt0[4 * hlf + 1], kt0[4 * hlf + 2],
-           kt0[4 * hlf + 3]);
-    sts_v4(blk + OFF_B2, sw128_offset(c0 + 1, tcol), kt1[4 * hlf], kt1[4 * hlf + 1],
+    sts_v4(blk + OFF_B2, sw128_offset(64 + c0, tcol), kt0[4 * hlf], kt0[4 * hlf + 1],
+           kt0[4 * hlf + 2], kt0[4 * hlf + 3]);
+    sts_v4(blk + OFF_B2, sw128_offset(65 + c0, tcol), kt1[4 * hlf], kt1[4 * hlf + 1],
            kt1[4 * hlf + 2], kt1[4 * hlf + 3]);
   }
   fence_async_smem();
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(256, 2)
       if (!isk) {
 #pragma unroll
         for (int hlf = 0; hlf < 2; ++hlf)
-          sts_v4(blk + OFF_B2, sw128_offset(128 + i, jb + 8 * hlf),
+          sts_v4(blk + OFF_B2, sw128_offset(i, jb + 8 * hlf),
                  pack_bf16x2(vals[8 * hlf + 0], vals[8 * hlf + 1]),
                  pack_bf16x2(vals[8 * hlf + 2], vals[8 * hlf + 3]),
                  pack_bf16x2(vals[8 * hlf + 4], vals[8 * hlf + 5]),
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(256, 2)
     }
     if (!isk && hh == 0) {  // Aqk columns past the row's block are zero
       for (int j0 = 16 * (I + 1); j0 < TC_C; j0 += 8)
-        sts_v4(blk + OFF_B2, sw128_offset(128 + i, j0), 0u, 0u, 0u, 0u);
+        sts_v4(blk + OFF_B2, sw128_offset(i, j0), 0u, 0u, 0u, 0u);
     }
   }
   tc_fence_before();
@@ -576,11 +576,11 @@ __global__ void __launch_bounds__(256, 2)
       if (lane < 16) {
 #pragma unroll
         for (int hlf = 0; hlf < 2; ++hlf)
-          sts_v4(wp, sw128_offset(i, 16 * c4 + 8 * hlf),
-                 pack_bf16x2(__uint_as_float(r[8 * hlf + 0]), __uint_as_float(r[8 * hlf + 1])),
-                 pack_bf16x2(__uint_as_float(r[8 * hlf + 2]), __uint_as_float(r[8 * hlf + 3])),
-                 pack_bf16x2(__uint_as_float(r[8 * hlf + 4]), __uint_as_float(r[8 * hlf + 5])),
-                 pack_bf16x2(__uint_as_float(r[8 * hlf + 6]), __uint_as_float(r[8 * hlf + 7])));
+          sts_v4(wp, sw128_offset(i, 16 * c4 + 8 * hlf),  // -W (rows 0-63 of B1)
+                 pack_bf16x2(-__uint_as_float(r[8 * hlf + 0]), -__uint_as_float(r[8 * hlf + 1])),
+                 pack_bf16x2(-__uint_as_float(r[8 * hlf + 2]), -__uint_as_float(r[8 * hlf + 3])),
+                 pack_bf16x2(-__uint_as_float(r[8 * hlf + 4]), -__uint_as_float(r[8 * hlf + 5])),
+                 pack_bf16x2(-__uint_as_float(r[8 * hlf + 6]), -__uint_as_float(r[8 * hlf + 7])));
       }
     }
   }
@@ -593,34 +593,40 @@ __global__ void __launch_bounds__(256, 2)
 // tc_recur
 // ======================================================================================
 // One CTA per (sequence, value head) holds the whole V = 128.  Warps 0-15 are epilogue
-// warps (MMA M = 128: thread v = 32q + lane of TMEM lane quadrant q = warp % 4 owns state
-// row v; the four warps of a quadrant split the 128 key channels, 32 each); warp 16 is the
-// control warp: one thread issues every MMA, bulk / tensor copy and L2 prefetch, and the
-// roles meet on mbarriers.
-// Per chunk, two MMA groups share the tensor pipe:
-//   G1  D1 = V^T T^T (U^T, columns 0-63; issued as soon as the chunk's data lands), then
-//       D1 -= S^T [W; -Qg]^T over N = 128: columns 0-63 become V_new^T, columns 64-127
-//       S^T Qg^T                                                          (12 MMAs)
-//   G2  D2 = V_new^T [Kg^T; Aqk]^T over N = 192: columns 0-127 dS^T, 128-191
-//       V_new^T Aqk^T                                                      (4 MMAs)
-// The epilogue warps turn V_new^T into the G2 operand, update the fp32 state held in
-// registers (S^T = S^T Diag(e^gamma_C) + dS^T) into the next G1 operand, and, while the
-// next G1 runs, drain O^T = D1[:, 64:128] + D2[:, 128:192] through a shared-memory staging
-// tile written back by one TMA store (D1 is double-buffered; its output half is cleared
-// with tcgen05.st after the drain).  Packed blocks and v tiles are prefetched into L2 four
-// chunks ahead and copied into shared memory one chunk ahead.
+// warps (thread v = 32q + lane of TMEM lane quadrant q = warp % 4 owns row v of every
+// transposed tile; the four warps of a quadrant split its columns); warp 16 is the control
+// warp: one thread issues every MMA, bulk / tensor copy and L2 prefetch, and the roles meet
+// on mbarriers.  The fp32 state S^T lives in tensor memory as an MMA accumulator; the bf16
+// copies of S^T and V_new^T that serve as A operands are written to tensor memory too, so
+// no operand goes through shared memory except the packed block and the v tile.
+// An MMA instruction (M = 128, K = 16) costs at least ~94 cycles whatever N up to 128
+// (~107 at N = 192, measured), so the chunk's products are merged into as few
+// instructions as the tensor-memory layout [V_new^T | O^T | S^T] (64 + 64 + 128 columns)
+// allows.  Per chunk (M = 128 rows of v in every MMA):
+//   U      V_new^T = V^T T^T                       A = v tile (smem)  4 MMAs, N = 64
+//   G1+O1  [V_new^T | O^T] += S^T [-W; Qg]^T       A = S^T (TMEM)     8 MMAs, N = 128
+//   G2+O2  [O^T | S^T] += V_new^T [Aqk; Kg^T]^T    A = V_new^T (TMEM) 4 MMAs, N = 192
+// where O^T was cleared and S^T scaled to S^T Diag(e^gamma_C) by the epilogue beforehand.
+// G1+O1 -> G2+O2 -> G1+O1 is the dependent chain; U runs in its shadow.  O^T is drained
+// through a shared-memory staging tile written back by one TMA store.  Packed blocks and
+// v tiles are prefetched into L2 four chunks ahead and copied into shared memory one chunk
+// ahead.
 constexpr uint32_t SL_T = 57344;                     // within a slot (same offsets as the block)
 constexpr uint32_t SL_D = 65536;
 constexpr uint32_t SL_V = 66560;                     // v tile [64 tokens x 128 v], 2 MN panels
 constexpr uint32_t SLOT = 82944;
 constexpr uint32_t R_RING = 0;                       // 2 slots
-constexpr uint32_t R_ST = 2 * SLOT;                  // S^T bf16 [128 v x 128 ch], 2 K panels
-constexpr uint32_t R_VN = R_ST + 32768;              // V_new^T bf16 [128 v x 64 tokens]; O staging
-constexpr uint32_t R_BAR = R_VN + 16384;             // full[2], bar_v, bar_s, bar_vn, bar_st
+constexpr uint32_t R_STG = 2 * SLOT;                 // O staging [64 tokens x 128 v] bf16
+constexpr uint32_t R_BAR = R_STG + 16384;            // full[2], bar_v, bar_s, bar_vn, bar_st
 constexpr uint32_t R_TMEM = R_BAR + 64;
 constexpr uint32_t R_END = R_TMEM + 16;
 constexpr uint32_t R_SMEM = R_END + 1024;
-constexpr uint32_t TM_D1 = 0, TM_D2 = 256;           // D1[b] at 128 b; D2 192 columns
+// tensor-memory columns
+constexpr uint32_t TM_VN = 0;    // V_new^T fp32 [128 v x 64 tokens]
+constexpr uint32_t TM_O = 64;    // O^T fp32 [128 v x 64 tokens]
+constexpr uint32_t TM_S = 128;   // S^T fp32 [128 v x 128 ch]
+constexpr uint32_t TM_SA = 256;  // S^T bf16 pairs (A operand), 64 columns
+constexpr uint32_t TM_VA = 320;  // V_new^T bf16 pairs (A operand), 32 columns
 constexpr int kPrefetch = 4;     // chunks whose loads are prefetched into L2 ahead
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
@@ -655,10 +661,10 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   float* carry = reinterpret_cast<float*>(a.ws + p.off_state);  // states between segments
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + R_BAR);
-  uint64_t* bar_v = full + 2;
-  uint64_t* bar_s = full + 3;
-  uint64_t* bar_vn = full + 4;
-  uint64_t* bar_st = full + 5;
+  uint64_t* bar_v = full + 2;   // G1+O1 done: V_new^T complete
+  uint64_t* bar_s = full + 3;   // G2+O2 done: O^T and the next chunk's S^T complete
+  uint64_t* bar_vn = full + 4;  // epilogue: bf16 V_new^T written
+  uint64_t* bar_st = full + 5;  // epilogue: O^T read and cleared, bf16 S^T written
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + R_TMEM);
   if (warp == kEpiWarps) {
     tmem_alloc(sTmem, 512);
@@ -696,7 +702,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
         tma_prefetch_3d(vmap_ptr, 0, hv, (int32_t)(bos + ci * TC_C));
         tma_prefetch_3d(vmap_ptr, 64, hv, (int32_t)(bos + ci * TC_C));
       };
-      // wait for chunk ci's data, clear v rows past the chunk end, issue U^T into D1[ci&1]
+      // wait for chunk ci's data, clear v rows past the chunk end, issue U^T into TM_VN
       auto issue_u = [&](int64_t ci) -> bool {
         const int st = (int)(ci & 1);
         if (!mbar_wait(&full[st], (uint32_t)((ci >> 1) & 1))) return false;
@@ -714,7 +720,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
         const uint32_t vb = smem_u32(slot + SL_V), tb = smem_u32(slot + SL_T);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem + TM_D1 + 128 * (uint32_t)st, sdesc_sw128(vb + ks * 2048, 8192, 1024),
+          mma_bf16(tmem + TM_VN, sdesc_sw128(vb + ks * 2048, 8192, 1024),
                    sdesc_sw128(tb + ks * 32, 16, 1024), idesc_bf16(128, 64, true), ks > 0);
         return true;
       };
@@ -726,33 +732,27 @@ __global__ void __launch_bounds__(kRecThreads, 1)
       for (int64_t ci = 0; ci < nch && ok; ++ci) {
         const int s = (int)(ci & 1);
         uint8_t* slot = sm + R_RING + s * SLOT;
-        // G1: needs S^T of the previous chunk (and the initial clears for ci = 0)
+        const uint32_t b1 = smem_u32(slot + OFF_B1), b2 = smem_u32(slot + OFF_B2);
+        // G1+O1 need the bf16 S^T of this chunk and a cleared O^T
         if (!mbar_wait(bar_st, (uint32_t)(ci & 1))) { ok = false; break; }
         tc_fence_after();
-        {
-          const uint32_t sb = smem_u32(sm + R_ST), b1 = smem_u32(slot + OFF_B1);
-          const uint32_t d1 = tmem + TM_D1 + 128 * (uint32_t)s;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_bf16(d1, sdesc_sw128(sb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                     sdesc_sw128(b1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                     idesc_bf16(128, 128, false, false, true), 1);
-          mma_commit(bar_v);
-        }
-        // slot s^1 (chunk ci-1) is free: its MMAs completed before its state update
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16_ts(tmem + TM_VN, tmem + TM_SA + 8 * ks,
+                      sdesc_sw128(b1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                      idesc_bf16(128, 128), 1);
+        mma_commit(bar_v);
+        // slot s^1 (chunk ci-1) is free: G2+O2 of chunk ci-1 completed before bar_st
         if (ci + 1 < nch) issue(ci + 1, s ^ 1);
         if (ci + 1 + kPrefetch < nch) prefetch(ci + 1 + kPrefetch);
-        // G2: needs V_new^T of this chunk (and the drain of chunk ci-1, which precedes it)
+        // G2+O2 need the bf16 V_new^T of this chunk
         if (!mbar_wait(bar_vn, (uint32_t)(ci & 1))) { ok = false; break; }
         tc_fence_after();
-        {
-          const uint32_t nb = smem_u32(sm + R_VN), b2 = smem_u32(slot + OFF_B2);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + TM_D2, sdesc_sw128(nb + ks * 32, 16, 1024),
-                     sdesc_sw128(b2 + ks * 32, 16, 1024), idesc_bf16(128, 192), ks > 0);
-          mma_commit(bar_s);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16_ts(tmem + TM_O, tmem + TM_VA + 8 * ks, sdesc_sw128(b2 + ks * 32, 16, 1024),
+                      idesc_bf16(128, 192), 1);
+        mma_commit(bar_s);
         if (ci + 1 < nch && !issue_u(ci + 1)) { ok = false; break; }
       }
       if (!ok) {
@@ -763,58 +763,57 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------- epilogue warps ---------------------------------
-    const int q4 = warp & 3, part = warp >> 2;  // part: key channels 32 part .. +31
+    const int q4 = warp & 3, part = warp >> 2;  // part: S^T columns 32 part..; tokens 16 part..
     const int v = 32 * q4 + lane;
     const uint32_t lane_base = tmem_addr(tmem, 32 * q4, 0);
     const size_t sbase = ((size_t)n * HV + hv) * (size_t)TC_K * TC_V;
-    float S[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      S[j] = !seq_start ? carry[sbase + (size_t)(32 * part + j) * TC_V + v]
-             : (a.h0 != nullptr) ? a.h0[sbase + (size_t)(32 * part + j) * TC_V + v] : 0.f;
-    uint8_t* st_row = sm + R_ST + (part >> 1) * 16384;  // K panel holding channels 32 part..
-    const int st_col = 32 * (part & 1);
-    auto store_state = [&]() {
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8)
-        sts_v4(st_row, sw128_offset(v, st_col + 8 * c8), pack_bf16x2(S[8 * c8 + 0], S[8 * c8 + 1]),
-               pack_bf16x2(S[8 * c8 + 2], S[8 * c8 + 3]), pack_bf16x2(S[8 * c8 + 4], S[8 * c8 + 5]),
-               pack_bf16x2(S[8 * c8 + 6], S[8 * c8 + 7]));
-    };
+    float* sout = seq_end ? a.final_state : carry;
     auto arrive = [&](uint64_t* bar) {  // one arrival per warp, after the warp's writes
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
     };
-    __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
-    const CUtensorMap* omap_ptr = &omap;
-    // O^T of chunk ci = D1[ci&1][64:128] + D2[128:192]: stage as [token][v] in the VN
-    // buffer, write it back (one TMA store for a full chunk, 16-byte stores of the valid
-    // rows otherwise), clear D1's output half.
-    auto drain_o = [&](int64_t ci) -> bool {
-      const int64_t t0 = bos + ci * TC_C;
-      const int L = (int)((eos - t0) < TC_C ? (eos - t0) : TC_C);
-      const uint32_t d1 = TM_D1 + 128 * (uint32_t)(ci & 1) + 64 + 16 * part;
-      uint8_t* stg = sm + R_VN;
-      uint32_t r1[16], r2[16];
-      tmem_ld16(lane_base + d1, r1);
-      tmem_ld16(lane_base + TM_D2 + 128 + 16 * part, r2);
-      tmem_wait_ld();
-      tmem_st16_zero(lane_base + d1);
+    auto slot_of = [&](int64_t ci) { return sm + R_RING + (int)(ci & 1) * SLOT; };
+    // bf16 copy of 32 state columns into the A operand; then S^T Diag(e^gamma_C) of chunk
+    // ci (waiting for that chunk's data) back into the accumulator
+    auto publish_state = [&](float (&S)[32], int64_t ci) -> bool {
+      uint32_t pk[16];
 #pragma unroll
-      for (int x = 0; x < 16; ++x) {
-        const int tt = 16 * part + x;
-        *reinterpret_cast<__nv_bfloat16*>(stg + tt * 256 + v * 2) =
-            __float2bfloat16_rn(__uint_as_float(r1[x]) + __uint_as_float(r2[x]));
-      }
+      for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
+      tmem_st16(lane_base + TM_SA + 16 * part, pk);
       tmem_wait_st();
       tc_fence_before();
+      arrive(bar_st);
+      if (ci >= nch) return true;
+      const bool w = mbar_wait(&full[ci & 1], (uint32_t)((ci >> 1) & 1));
+      const float4* dec = reinterpret_cast<const float4*>(slot_of(ci) + SL_D) + 8 * part;
+      uint32_t sc[32];
+#pragma unroll
+      for (int x4 = 0; x4 < 8; ++x4) {
+        const float4 d = dec[x4];
+        sc[4 * x4 + 0] = __float_as_uint(S[4 * x4 + 0] * d.x);
+        sc[4 * x4 + 1] = __float_as_uint(S[4 * x4 + 1] * d.y);
+        sc[4 * x4 + 2] = __float_as_uint(S[4 * x4 + 2] * d.z);
+        sc[4 * x4 + 3] = __float_as_uint(S[4 * x4 + 3] * d.w);
+      }
+      tmem_st32(lane_base + TM_S + 32 * part, sc);
+      tmem_wait_st();
+      return w;
+    };
+    __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
+    const CUtensorMap* omap_ptr = &omap;
+    // O^T of chunk ci (already in the staging tile as [token][v]): one TMA store for a
+    // full chunk, 16-byte stores of the valid rows otherwise
+    auto store_o = [&](int64_t ci, bool good) -> bool {
+      const int64_t t0 = bos + ci * TC_C;
+      const int L = (int)((eos - t0) < TC_C ? (eos - t0) : TC_C);
+      uint8_t* stg = sm + R_STG;
       fence_async_smem();
-      bool good = named_bar_and(1, kEpiThreads, true);
+      good = named_bar_and(1, kEpiThreads, good);
       if (L == TC_C) {
         if (tid == 0) {
           tma_store_3d(omap_ptr, 0, hv, (int32_t)t0, stg);
           bulk_commit();
-          bulk_wait_read0();  // the staging buffer is rewritten right after
+          bulk_wait_read0();  // the staging tile is rewritten for the next chunk
         }
       } else {
         for (int e = tid; e < L * 16; e += kEpiThreads) {
@@ -823,76 +822,75 @@ __global__ void __launch_bounds__(kRecThreads, 1)
               reinterpret_cast<const uint4*>(stg + row * 256)[c16];
         }
       }
-      good = named_bar_and(1, kEpiThreads, good);
-      return good;
+      return named_bar_and(1, kEpiThreads, good);
     };
 
-    store_state();
-    tmem_st16_zero(lane_base + TM_D1 + 64 + 16 * part);
-    tmem_st16_zero(lane_base + TM_D1 + 128 + 64 + 16 * part);
-    tmem_wait_st();
-    fence_async_smem();
-    tc_fence_before();
-    arrive(bar_st);
+    {  // initial state -> bf16 A operand and the accumulator (scaled for chunk 0); O^T = 0
+      float S[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const size_t idx = sbase + (size_t)(32 * part + j) * TC_V + v;
+        S[j] = !seq_start ? carry[idx] : (a.h0 != nullptr) ? a.h0[idx] : 0.f;
+      }
+      if (nch == 0 && sout != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sout[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
+      }
+      tmem_st16_zero(lane_base + TM_O + 16 * part);
+      if (!publish_state(S, 0)) ok = false;
+    }
 
     for (int64_t ci = 0; ci < nch; ++ci) {
-      const int s = (int)(ci & 1);
-      uint8_t* slot = sm + R_RING + s * SLOT;
-      if (ci > 0 && !drain_o(ci - 1)) { ok = false; break; }
-      // V_new^T -> bf16 operand of G2 (this warp: tokens 16 part .. +15)
+      // V_new^T -> bf16 A operand of G2+O2 (this warp: tokens 16 part .. +15)
       bool w = mbar_wait(bar_v, (uint32_t)(ci & 1));
       tc_fence_after();
       {
-        uint32_t r[16];
-        tmem_ld16(lane_base + TM_D1 + 128 * (uint32_t)s + 16 * part, r);
+        uint32_t r[16], pk[8];
+        tmem_ld16(lane_base + TM_VN + 16 * part, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int c8 = 0; c8 < 2; ++c8)
-          sts_v4(sm + R_VN, sw128_offset(v, 16 * part + 8 * c8),
-                 pack_bf16x2(__uint_as_float(r[8 * c8 + 0]), __uint_as_float(r[8 * c8 + 1])),
-                 pack_bf16x2(__uint_as_float(r[8 * c8 + 2]), __uint_as_float(r[8 * c8 + 3])),
-                 pack_bf16x2(__uint_as_float(r[8 * c8 + 4]), __uint_as_float(r[8 * c8 + 5])),
-                 pack_bf16x2(__uint_as_float(r[8 * c8 + 6]), __uint_as_float(r[8 * c8 + 7])));
+        for (int j = 0; j < 8; ++j)
+          pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+        tmem_st8(lane_base + TM_VA + 8 * part, pk);
+        tmem_wait_st();
       }
-      fence_async_smem();
       tc_fence_before();
       arrive(bar_vn);
-      // S^T = S^T Diag(e^gamma_C) + dS^T -> next G1 operand (this warp: 32 channels)
+      // O^T of chunk ci -> staging tile (then cleared); S^T of chunk ci+1 -> bf16 copy for
+      // G1+O1 and rescaled accumulator for G2+O2
       w = mbar_wait(bar_s, (uint32_t)(ci & 1)) && w;
       tc_fence_after();
       {
-        const float4* dec = reinterpret_cast<const float4*>(slot + SL_D) + 8 * part;
+        uint32_t r[16];
+        tmem_ld16(lane_base + TM_O + 16 * part, r);
+        tmem_wait_ld();
+        tmem_st16_zero(lane_base + TM_O + 16 * part);
+        uint8_t* stg = sm + R_STG;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {  // two 16-column loads keep the register count low
-          uint32_t r[16];
-          tmem_ld16(lane_base + TM_D2 + 32 * part + 16 * h, r);
-          tmem_wait_ld();
+        for (int x = 0; x < 16; ++x)
+          *reinterpret_cast<__nv_bfloat16*>(stg + (16 * part + x) * 256 + v * 2) =
+              __float2bfloat16_rn(__uint_as_float(r[x]));
+        float S[32];
+        tmem_ld16(lane_base + TM_S + 32 * part, r);
+        tmem_wait_ld();
 #pragma unroll
-          for (int x4 = 0; x4 < 4; ++x4) {
-            const float4 d = dec[4 * h + x4];
-            const int j = 16 * h + 4 * x4;
-            S[j + 0] = fmaf(d.x, S[j + 0], __uint_as_float(r[4 * x4 + 0]));
-            S[j + 1] = fmaf(d.y, S[j + 1], __uint_as_float(r[4 * x4 + 1]));
-            S[j + 2] = fmaf(d.z, S[j + 2], __uint_as_float(r[4 * x4 + 2]));
-            S[j + 3] = fmaf(d.w, S[j + 3], __uint_as_float(r[4 * x4 + 3]));
-          }
+        for (int j = 0; j < 16; ++j) S[j] = __uint_as_float(r[j]);
+        tmem_ld16(lane_base + TM_S + 32 * part + 16, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) S[16 + j] = __uint_as_float(r[j]);
+        if (ci + 1 == nch && sout != nullptr) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sout[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
         }
-        store_state();
+        if (ci + 1 < nch)
+          w = publish_state(S, ci + 1) && w;
+        else
+          tmem_wait_st();
       }
-      fence_async_smem();
-      tc_fence_before();
-      arrive(bar_st);
-      if (!named_bar_and(1, kEpiThreads, w)) { ok = false; break; }
-    }
-    if (ok && nch > 0) {
-      ok = drain_o(nch - 1);
+      if (!store_o(ci, w)) { ok = false; break; }
     }
     if (!ok) flag_status(a.status, KDA_DEV_TIMEOUT);
-    float* sout = seq_end ? a.final_state : carry;
-    if (sout != nullptr && ok) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) sout[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
-    }
     if (tid == 0) bulk_wait0();
   }
   tc_fence_before();

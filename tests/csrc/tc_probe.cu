@@ -11,7 +11,7 @@
 using namespace kda::tc;
 
 struct ProbeArgs {
-  int M, N, K, a_mn, b_mn, neg_a;
+  int M, N, K, a_mn, b_mn, neg_a, a_tmem;  // a_tmem: A read from tensor memory
   const uint16_t* A;  // logical [M][K]
   const uint16_t* B;  // logical [N][K]
   float* out;         // [128][N]
@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(ProbeArgs a) {
   }
   fence_async_smem();
   if (warp == 0) {
-    tmem_alloc(&tbase, 256);
+    tmem_alloc(&tbase, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -53,6 +53,22 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(ProbeArgs a) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tbase;
+  if (a.a_tmem) {  // row m of A -> lane m, columns 256 + k/2 (bf16 pairs, lower k low)
+    const int m = 32 * warp + lane;
+    for (int k0 = 0; k0 < a.K; k0 += 16) {
+      uint32_t r[8];
+      for (int j = 0; j < 8; ++j) {
+        const int k = k0 + 2 * j;
+        const uint32_t lo = m < a.M ? a.A[m * a.K + k] : 0u, hi = m < a.M ? a.A[m * a.K + k + 1] : 0u;
+        r[j] = lo | (hi << 16);
+      }
+      tmem_st8(tmem_addr(tmem, 32 * warp, 256 + k0 / 2), r);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   if (tid == 0) {
     const uint32_t idesc = idesc_bf16(a.M, a.N, a.a_mn, a.b_mn, a.neg_a);
     for (int ks = 0; ks < a.K / 16; ++ks) {
@@ -65,7 +81,10 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(ProbeArgs a) {
         bd = sdesc_sw128(smem_u32(sB) + (ks / 4) * (a.N * 128) + (ks % 4) * 32, 16, 1024);
       else
         bd = sdesc_sw128(smem_u32(sB) + ks * 2048, a.K * 128, 1024);
-      mma_bf16(tmem, ad, bd, idesc, ks > 0);
+      if (a.a_tmem)
+        mma_bf16_ts(tmem, tmem + 256 + ks * 8, bd, idesc, ks > 0);
+      else
+        mma_bf16(tmem, ad, bd, idesc, ks > 0);
     }
     mma_commit(&bar);
   }
@@ -84,12 +103,14 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(ProbeArgs a) {
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-extern "C" int tc_probe_run(int M, int N, int K, int a_mn, int b_mn, int neg_a, const uint16_t* hA,
-                            const uint16_t* hB, float* hOut) {
-  if (M > 128 || N > 256 || K > 128 || K % 16 || (a_mn && M % 64) || (b_mn && N % 64)) return -1;
+extern "C" int tc_probe_run(int M, int N, int K, int a_mn, int b_mn, int neg_a, int a_tmem,
+                            const uint16_t* hA, const uint16_t* hB, float* hOut) {
+  if (M > 128 || N > 256 || K > 128 || K % 16 || (a_mn && M % 64) || (b_mn && N % 64) ||
+      (a_tmem && (M != 128 || a_mn)))
+    return -1;
   uint16_t *dA, *dB;
   float* dO;
   int* dE;
@@ -101,7 +122,7 @@ extern "C" int tc_probe_run(int M, int N, int K, int a_mn, int b_mn, int neg_a, 
   cudaMemcpy(dB, hB, N * K * 2, cudaMemcpyHostToDevice);
   cudaMemset(dO, 0, 128 * N * 4);
   cudaMemset(dE, 0, 4);
-  ProbeArgs a{M, N, K, a_mn, b_mn, neg_a, dA, dB, dO, dE};
+  ProbeArgs a{M, N, K, a_mn, b_mn, neg_a, a_tmem, dA, dB, dO, dE};
   const int smem = 1024 + 32768 + 65536;
   cudaFuncSetAttribute(tc_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   tc_probe_kernel<<<1, 128, smem>>>(a);

@@ -34,12 +34,12 @@ def bf16_bits(x):
     return (np.ascontiguousarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
 
 
-def run(lib, M, N, K, a_mn=0, b_mn=0, neg_a=0, seed=0):
+def run(lib, M, N, K, a_mn=0, b_mn=0, neg_a=0, seed=0, a_tmem=0):
     r = np.random.default_rng(seed)
     A = r.integers(-4, 5, size=(M, K)).astype(np.float32) / 4
     B = r.integers(-4, 5, size=(N, K)).astype(np.float32) / 4
     out = np.zeros((128, N), np.float32)
-    rc = lib.tc_probe_run(M, N, K, a_mn, b_mn, neg_a,
+    rc = lib.tc_probe_run(M, N, K, a_mn, b_mn, neg_a, a_tmem,
                           bf16_bits(A).ctypes.data_as(ctypes.c_void_p),
                           bf16_bits(B).ctypes.data_as(ctypes.c_void_p),
                           out.ctypes.data_as(ctypes.c_void_p))
@@ -72,3 +72,11 @@ def test_m64_lane_layout(probe):
     lanes = np.array([32 * (r // 16) + r % 16 for r in range(64)])
     found = {r: [int(l) for l in range(128) if np.array_equal(out[l], ref[r])] for r in range(64)}
     assert np.array_equal(out[lanes], ref), f"row -> lanes holding it: {found}"
+
+
+@pytest.mark.parametrize("N,K,b_mn", [(64, 128, 0), (128, 64, 0), (192, 64, 0), (128, 128, 1)])
+def test_a_from_tensor_memory(probe, N, K, b_mn):
+    """A in TMEM (row m in lane m, bf16 pairs along the columns, lower K index in the low
+    half), B from shared memory."""
+    out, ref = run(probe, 128, N, K, b_mn=b_mn, a_tmem=1, seed=7 + N + K)
+    assert np.array_equal(out, ref)
