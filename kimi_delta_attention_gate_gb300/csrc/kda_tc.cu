@@ -131,6 +131,33 @@ __device__ __forceinline__ uint32_t lds_u32(const uint8_t* base, uint32_t off) {
   return *reinterpret_cast<const uint32_t*>(base + off);
 }
 
+// Exact diagonal 16 x 16 block of Aqk and Akk0 for row block rg (every exponent
+// Gamma_i - Gamma_j <= 0): partial sums over this thread's two channels, from the raw
+// q / k tiles (read before they are transformed in place) and the gate cumsums gs[0..15],
+// gs[16..31] of the two channels; out of line so that it costs the common path no
+// instruction-cache space.
+__device__ __noinline__ void guard_diagonal(const uint8_t* qk_pan, uint32_t cc, int rg, int L,
+                                            const float* gs, const float* sNorm, float* dq) {
+  float* dk = dq + 256;
+  for (int i = 0; i < 16; ++i) {
+    const int rowi = 16 * rg + i;
+    const uint32_t qv = rowi < L ? lds_u32(qk_pan, sw128_offset(rowi, cc)) : 0u;
+    const uint32_t kiv = rowi < L ? lds_u32(qk_pan, sw128_offset(64 + rowi, cc)) : 0u;
+    const float qn = sNorm[2 * rowi], kni = sNorm[2 * rowi + 1];
+    const float qi0 = bf_lo(qv) * qn, qi1 = bf_hi(qv) * qn;
+    const float ki0 = bf_lo(kiv) * kni, ki1 = bf_hi(kiv) * kni;
+    for (int j = 0; j <= i; ++j) {
+      const int rowj = 16 * rg + j;
+      const uint32_t kv = rowj < L ? lds_u32(qk_pan, sw128_offset(64 + rowj, cc)) : 0u;
+      const float knj = sNorm[2 * rowj + 1];
+      const float kj0 = bf_lo(kv) * knj, kj1 = bf_hi(kv) * knj;
+      const float e0 = ex2(gs[i] - gs[j]), e1 = ex2(gs[16 + i] - gs[16 + j]);
+      atomicAdd(&dq[i * 16 + j], qi0 * kj0 * e0 + qi1 * kj1 * e1);
+      atomicAdd(&dk[i * 16 + j], ki0 * kj0 * e0 + ki1 * kj1 * e1);
+    }
+  }
+}
+
 template <int GATE>
 __global__ void __launch_bounds__(256, 2)
     tc_intra_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap qmap,
@@ -296,34 +323,17 @@ __global__ void __launch_bounds__(256, 2)
     F0[I] = (I > rg) ? ex2(rI0[I] - rb0) : 1.f;
     F1[I] = (I > rg) ? ex2(rI1[I] - rb1) : 1.f;
   }
-  if (guard) {
-    // exact diagonal block from the raw tiles (read before they are overwritten below):
-    // partial sums over this thread's two channels; every exponent Gamma_i - Gamma_j <= 0
-    // (fully unrolled: runtime indices would force G0, G1 into local memory)
-    float* dq = sDiag + rg * 512;
-    float* dk = dq + 256;
-    float kn0[16], kn1[16];
+  if (sFlag[0] != 0) {  // some block needs its diagonal entries evaluated exactly
+    // the thread's gate cumsums go to a scratch row in the (not yet written) Ka tile, so
+    // that the rarely taken evaluation can run as compact loops out of line
+    float* gs = reinterpret_cast<float*>(sm + P_KA) + tid * 33;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int rowj = 16 * rg + j;
-      const uint32_t kv = rowj < L ? lds_u32(qk_pan, sw128_offset(64 + rowj, cc)) : 0u;
-      const float knj = sNorm[2 * rowj + 1];
-      kn0[j] = bf_lo(kv) * knj;
-      kn1[j] = bf_hi(kv) * knj;
+    for (int r = 0; r < 16; ++r) {
+      gs[r] = G0[r];
+      gs[16 + r] = G1[r];
     }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int rowi = 16 * rg + i;
-      const uint32_t qv = rowi < L ? lds_u32(qk_pan, sw128_offset(rowi, cc)) : 0u;
-      const float qn = sNorm[2 * rowi];
-      const float qi0 = bf_lo(qv) * qn, qi1 = bf_hi(qv) * qn;
-#pragma unroll
-      for (int j = 0; j <= i; ++j) {
-        const float e0 = ex2(G0[i] - G0[j]), e1 = ex2(G1[i] - G1[j]);
-        atomicAdd(&dq[i * 16 + j], qi0 * kn0[j] * e0 + qi1 * kn1[j] * e1);
-        atomicAdd(&dk[i * 16 + j], kn0[i] * kn0[j] * e0 + kn1[i] * kn1[j] * e1);
-      }
-    }
+    if (guard) guard_diagonal(qk_pan, cc, rg, L, gs, sNorm, sDiag + rg * 512);
+    __syncthreads();
   }
   // Kg^T (row = channel, 16 consecutive tokens per thread) is packed two tokens per
   // register and written as 16-byte pieces after the loop
@@ -501,11 +511,12 @@ __global__ void __launch_bounds__(256, 2)
     __syncthreads();
   }
   {  // level 3: X_{B,A} = -X_BB (L_BA X_AA), A = 0..31, B = 32..63; 2 x 2 tile per thread
-     // (full-length unrolled sums: the zero upper blocks of X_AA, X_BB mask themselves)
+     // (full-length sums: the zero upper blocks of X_AA, X_BB mask themselves; loops
+     // kept rolled, since instruction-cache space is scarcer than issue slots here)
     const int ti = tid >> 4, tj = tid & 15;
     const int i0 = 2 * ti, j0 = 2 * tj;
     float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-#pragma unroll
+#pragma unroll 2
     for (int m = 0; m < 32; ++m) {
       const float l0 = sL[(32 + i0) * SOLVE_LD + m], l1 = sL[(33 + i0) * SOLVE_LD + m];
       const float xa = sX[m * SOLVE_LD + j0], xb = sX[m * SOLVE_LD + j0 + 1];
@@ -516,7 +527,7 @@ __global__ void __launch_bounds__(256, 2)
     sY[(i0 + 1) * 32 + j0] = y10; sY[(i0 + 1) * 32 + j0 + 1] = y11;
     __syncthreads();
     float z00 = 0.f, z01 = 0.f, z10 = 0.f, z11 = 0.f;
-#pragma unroll
+#pragma unroll 2
     for (int m = 0; m < 32; ++m) {
       const float xa = sX[(32 + i0) * SOLVE_LD + 32 + m], xb = sX[(33 + i0) * SOLVE_LD + 32 + m];
       const float ya = sY[m * 32 + j0], yb = sY[m * 32 + j0 + 1];
