@@ -510,32 +510,94 @@ __global__ void __launch_bounds__(256, 2)
     }
     __syncthreads();
   }
-  {  // level 3: X_{B,A} = -X_BB (L_BA X_AA), A = 0..31, B = 32..63; 2 x 2 tile per thread
-     // (full-length sums: the zero upper blocks of X_AA, X_BB mask themselves; loops
-     // kept rolled, since instruction-cache space is scarcer than issue slots here)
-    const int ti = tid >> 4, tj = tid & 15;
-    const int i0 = 2 * ti, j0 = 2 * tj;
-    float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-#pragma unroll 2
-    for (int m = 0; m < 32; ++m) {
-      const float l0 = sL[(32 + i0) * SOLVE_LD + m], l1 = sL[(33 + i0) * SOLVE_LD + m];
-      const float xa = sX[m * SOLVE_LD + j0], xb = sX[m * SOLVE_LD + j0 + 1];
-      y00 = fmaf(l0, xa, y00); y01 = fmaf(l0, xb, y01);
-      y10 = fmaf(l1, xa, y10); y11 = fmaf(l1, xb, y11);
+  // level 3: X_{B,A} = -X_BB (L_BA X_AA), A = rows / columns 0..31, B = 32..63, as two
+  // tcgen05 MMA rounds (M = 64 with rows 32..63 kept, N = 32, K = 32).  Each fp32 operand is
+  // split into bf16 hi + lo parts and a b ~ a_hi b_hi + a_hi b_lo + a_lo b_hi is accumulated
+  // in fp32 (relative error ~2^-16, far below the bf16 rounding of T).  Operand tiles live in
+  // the dead [Qs; Ks] tile: A hi / lo (K-major, 64 rows) and B hi / lo (MN-major, 32 rows).
+  {
+    uint8_t* tA = sm + P_QK;          // [2][64 rows x 128 B]: hi, lo
+    uint8_t* tB = sm + P_QK + 16384;  // [2][32 rows x 128 B]: hi, lo
+    const uint32_t la = tmem + 0, lb = tmem + 32;  // accumulators of rounds 1 and 2
+    // 4 consecutive fp32 values -> hi / lo bf16 quads at byte offset `off` of two tiles
+    auto put4 = [&](uint8_t* hi_tile, uint32_t tile_bytes, uint32_t off, const float* v) {
+      const uint32_t h0 = pack_bf16x2(v[0], v[1]), h1 = pack_bf16x2(v[2], v[3]);
+      const uint32_t l0 = pack_bf16x2(v[0] - bf_lo(h0), v[1] - bf_hi(h0));
+      const uint32_t l1 = pack_bf16x2(v[2] - bf_lo(h1), v[3] - bf_hi(h1));
+      *reinterpret_cast<uint2*>(hi_tile + off) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(hi_tile + tile_bytes + off) = make_uint2(l0, l1);
+    };
+    auto issue_round = [&](uint32_t acc) {  // 2 K steps x 3 hi / lo products
+      tc_fence_after();
+      const uint32_t ab = smem_u32(tA), bb = smem_u32(tB);
+      int n = 0;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+          const uint32_t ao = (t == 2) ? 8192u : 0u, bo = (t == 1) ? 4096u : 0u;
+          mma_bf16(acc, sdesc_sw128(ab + ao + ks * 32, 16, 1024),
+                   sdesc_sw128(bb + bo + ks * 2048, 4096, 1024),
+                   idesc_bf16(64, 32, false, true), n++ > 0);
+        }
+      mma_commit(&bars[1]);
+    };
+    // D rows 32..63 sit in lanes 0-15 of quadrants 2, 3 (M = 64 layout); warp halves split
+    // the 32 columns
+    const bool epi = (warp & 2) && lane < 16;
+    const int er = 16 * ((warp & 3) - 2) + lane;  // row - 32
+    const int ec = 16 * (warp >> 2);              // first column
+    {  // round 1 operands: A = L[32..63][0..31], B = X_AA
+      const int i = tid >> 3, m0 = (tid & 7) * 4;
+      float v[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) v[x] = sL[(32 + i) * SOLVE_LD + m0 + x];
+      put4(tA, 8192, sw128_offset(32 + i, m0), v);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) v[x] = sX[i * SOLVE_LD + m0 + x];
+      put4(tB, 4096, sw128_offset(i, m0), v);
     }
-    sY[i0 * 32 + j0] = y00; sY[i0 * 32 + j0 + 1] = y01;
-    sY[(i0 + 1) * 32 + j0] = y10; sY[(i0 + 1) * 32 + j0 + 1] = y11;
+    fence_async_smem();
     __syncthreads();
-    float z00 = 0.f, z01 = 0.f, z10 = 0.f, z11 = 0.f;
-#pragma unroll 2
-    for (int m = 0; m < 32; ++m) {
-      const float xa = sX[(32 + i0) * SOLVE_LD + 32 + m], xb = sX[(33 + i0) * SOLVE_LD + 32 + m];
-      const float ya = sY[m * 32 + j0], yb = sY[m * 32 + j0 + 1];
-      z00 = fmaf(xa, ya, z00); z01 = fmaf(xa, yb, z01);
-      z10 = fmaf(xb, ya, z10); z11 = fmaf(xb, yb, z11);
+    if (tid == 0) issue_round(la);
+    __syncwarp();
+    if (!mbar_wait(&bars[1], 1)) flag_status(a.status, KDA_DEV_TIMEOUT);
+    tc_fence_after();
+    {  // round 2 operands: B = Y = L_BA X_AA (from TMEM), A = X[32..63][32..63]
+      uint32_t r[16];
+      tmem_ld16(tmem_addr(la, 32 * (warp & 3), ec), r);
+      tmem_wait_ld();
+      if (epi) {
+#pragma unroll
+        for (int x = 0; x < 16; x += 4) {
+          const float v[4] = {__uint_as_float(r[x]), __uint_as_float(r[x + 1]),
+                              __uint_as_float(r[x + 2]), __uint_as_float(r[x + 3])};
+          put4(tB, 4096, sw128_offset(er, ec + x), v);
+        }
+      }
+      const int i = tid >> 3, m0 = (tid & 7) * 4;
+      float v[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) v[x] = sX[(32 + i) * SOLVE_LD + 32 + m0 + x];
+      put4(tA, 8192, sw128_offset(32 + i, m0), v);
     }
-    sX[(32 + i0) * SOLVE_LD + j0] = -z00; sX[(32 + i0) * SOLVE_LD + j0 + 1] = -z01;
-    sX[(33 + i0) * SOLVE_LD + j0] = -z10; sX[(33 + i0) * SOLVE_LD + j0 + 1] = -z11;
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) issue_round(lb);
+    __syncwarp();
+    if (!mbar_wait(&bars[1], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
+    tc_fence_after();
+    {  // X_BA = -(X_BB Y)
+      uint32_t r[16];
+      tmem_ld16(tmem_addr(lb, 32 * (warp & 3), ec), r);
+      tmem_wait_ld();
+      if (epi) {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) sX[(32 + er) * SOLVE_LD + ec + x] = -__uint_as_float(r[x]);
+      }
+    }
+    tc_fence_before();
   }
   __syncthreads();
   // T = X Diag(beta), bf16: A operand of the W MMA (over the dead [Qs; Ks] tile) and block

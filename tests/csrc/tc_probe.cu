@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(ProbeArgs a) {
 
 extern "C" int tc_probe_run(int M, int N, int K, int a_mn, int b_mn, int neg_a, int a_tmem,
                             const uint16_t* hA, const uint16_t* hB, float* hOut) {
-  if (M > 128 || N > 256 || K > 128 || K % 16 || (a_mn && M % 64) || (b_mn && N % 64) ||
+  if (M > 128 || N > 256 || K > 128 || K % 16 || (a_mn && M % 64) || (b_mn && N % 64 && N != 32) ||
       (a_tmem && (M != 128 || a_mn)))
     return -1;
   uint16_t *dA, *dB;

@@ -80,3 +80,12 @@ def test_a_from_tensor_memory(probe, N, K, b_mn):
     half), B from shared memory."""
     out, ref = run(probe, 128, N, K, b_mn=b_mn, a_tmem=1, seed=7 + N + K)
     assert np.array_equal(out, ref)
+
+
+@pytest.mark.parametrize("b_mn", [0, 1])
+def test_m64_n32_k32(probe, b_mn):
+    """The small solve products: M = 64, N = 32, K = 32 (two K steps of a 64-wide tile), B
+    K-major or MN-major (half of one 64-element panel)."""
+    out, ref = run(probe, 64, 32, 32, b_mn=b_mn, seed=9 + b_mn)
+    lanes = np.array([32 * (r // 16) + r % 16 for r in range(64)])
+    assert np.array_equal(out[lanes], ref)
