@@ -105,7 +105,9 @@ __device__ __forceinline__ float gate_fast(float x, float a, float lb) {
 // are transformed in place: q, k -> [Qs; Ks] (A operand of the Aqk/Akk MMA) and g -> X =
 // e^Gamma . K (MN-major B operand of the W MMA).  The packed block goes straight from
 // registers to global memory.
-constexpr uint32_t P_QK = 0;        // 2 K-panels x [64 query rows; 64 key rows], 16 KB each;
+constexpr uint32_t P_QK = 0;        // 2 K-panels x 128 rows, 16 KB each: row block b holds the
+                                    // queries of tokens 16b..16b+15 in rows 32b..32b+15 and
+                                    // their keys in rows 32b+16..32b+31;
                                     // after the Aqk/Akk MMA: T (A operand of the W MMA)
 constexpr uint32_t P_X = 32768;     // 2 MN-panels x [64 tokens x 64 ch], 8 KB each: g, then X
 constexpr uint32_t P_KA = 49152;    // [Ka_0; Ka_1; Ka_2; Ka_3] B operand: 160 rows, 2 panels x
@@ -125,6 +127,9 @@ constexpr uint32_t P_SMEM = P_END + 1024;
 // Ka_I (16(I+1) rows) starts at row 8 I (I+1) of the B operand; its accumulator D_I at the
 // same TMEM column: 0, 16, 48, 96
 __host__ __device__ constexpr uint32_t ka_row(int I) { return 8u * (uint32_t)(I * (I + 1)); }
+// Rows of token t's query and key in the [Qs; Ks] operand (one TMEM lane quadrant per block)
+__host__ __device__ constexpr uint32_t q_row(int t) { return 32u * (uint32_t)(t >> 4) + (uint32_t)(t & 15); }
+__host__ __device__ constexpr uint32_t k_row(int t) { return q_row(t) + 16u; }
 constexpr int SOLVE_LD = 65;
 
 __device__ __forceinline__ uint32_t lds_u32(const uint8_t* base, uint32_t off) {
@@ -141,14 +146,14 @@ __device__ __noinline__ void guard_diagonal(const uint8_t* qk_pan, uint32_t cc, 
   float* dk = dq + 256;
   for (int i = 0; i < 16; ++i) {
     const int rowi = 16 * rg + i;
-    const uint32_t qv = rowi < L ? lds_u32(qk_pan, sw128_offset(rowi, cc)) : 0u;
-    const uint32_t kiv = rowi < L ? lds_u32(qk_pan, sw128_offset(64 + rowi, cc)) : 0u;
+    const uint32_t qv = rowi < L ? lds_u32(qk_pan, sw128_offset(q_row(rowi), cc)) : 0u;
+    const uint32_t kiv = rowi < L ? lds_u32(qk_pan, sw128_offset(k_row(rowi), cc)) : 0u;
     const float qn = sNorm[2 * rowi], kni = sNorm[2 * rowi + 1];
     const float qi0 = bf_lo(qv) * qn, qi1 = bf_hi(qv) * qn;
     const float ki0 = bf_lo(kiv) * kni, ki1 = bf_hi(kiv) * kni;
     for (int j = 0; j <= i; ++j) {
       const int rowj = 16 * rg + j;
-      const uint32_t kv = rowj < L ? lds_u32(qk_pan, sw128_offset(64 + rowj, cc)) : 0u;
+      const uint32_t kv = rowj < L ? lds_u32(qk_pan, sw128_offset(k_row(rowj), cc)) : 0u;
       const float knj = sNorm[2 * rowj + 1];
       const float kj0 = bf_lo(kv) * knj, kj1 = bf_hi(kv) * knj;
       const float e0 = ex2(gs[i] - gs[j]), e1 = ex2(gs[16 + i] - gs[16 + j]);
@@ -189,17 +194,21 @@ __global__ void __launch_bounds__(256, 2)
     tmem_alloc(sTmem, 256);
     tmem_relinquish();
   }
-  if (tid == 32) {  // tile loads: q, k -> [q; k] per channel panel, g -> 2 panels, dt_bias row
+  if (tid == 32) {  // tile loads: q, k -> [Qs; Ks] row blocks, g -> 2 panels, dt_bias row
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
     fence_mbar_init();
     sFlag[0] = 0;
     const int32_t tt = (int32_t)t0;
     mbar_arrive_expect_tx(&bars[0], 49152u + (has_dt ? TC_K * 4u : 0u));
-    tma_load_3d(sm + P_QK, &qmap, 0, h, tt, &bars[0]);
-    tma_load_3d(sm + P_QK + 8192, &kmap, 0, h, tt, &bars[0]);
-    tma_load_3d(sm + P_QK + 16384, &qmap, 64, h, tt, &bars[0]);
-    tma_load_3d(sm + P_QK + 24576, &kmap, 64, h, tt, &bars[0]);
+#pragma unroll
+    for (int pn = 0; pn < 2; ++pn)  // 16-token boxes: queries and keys of each row block
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        uint8_t* dst = sm + P_QK + pn * 16384 + b * 4096;
+        tma_load_3d(dst, &qmap, 64 * pn, h, tt + 16 * b, &bars[0]);
+        tma_load_3d(dst + 2048, &kmap, 64 * pn, h, tt + 16 * b, &bars[0]);
+      }
     tma_load_3d(sm + P_X, &gmap, 0, hv, tt, &bars[0]);
     tma_load_3d(sm + P_X + 8192, &gmap, 64, hv, tt, &bars[0]);
     if (has_dt) bulk_g2s(sDt, a.dt_bias + (size_t)hv * TC_K, TC_K * 4, &bars[0]);
@@ -262,8 +271,8 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int row = 16 * rg + r;
-      const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(row, cc)) : 0u;
-      const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(64 + row, cc)) : 0u;
+      const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(q_row(row), cc)) : 0u;
+      const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(k_row(row), cc)) : 0u;
       sq[r] = bf_lo(qv) * bf_lo(qv) + bf_hi(qv) * bf_hi(qv);
       sk[r] = bf_lo(kv) * bf_lo(kv) + bf_hi(kv) * bf_hi(kv);
     }
@@ -341,14 +350,14 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = 16 * rg + r;
-    const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(row, cc)) : 0u;
-    const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(64 + row, cc)) : 0u;
+    const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(q_row(row), cc)) : 0u;
+    const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(k_row(row), cc)) : 0u;
     const float qn = sNorm[2 * row], kn = sNorm[2 * row + 1];
     const float q0 = bf_lo(qv) * qn, q1 = bf_hi(qv) * qn;
     const float k0 = bf_lo(kv) * kn, k1 = bf_hi(kv) * kn;
     const float P0 = ex2(G0[r]), P1 = ex2(G1[r]);  // 2^(Gamma - r_b) <= 1
-    sts_u32(qk_pan, sw128_offset(row, cc), pack_bf16x2(q0 * P0, q1 * P1));       // Qs
-    sts_u32(qk_pan, sw128_offset(64 + row, cc), pack_bf16x2(k0 * P0, k1 * P1));  // Ks
+    sts_u32(qk_pan, sw128_offset(q_row(row), cc), pack_bf16x2(q0 * P0, q1 * P1));  // Qs
+    sts_u32(qk_pan, sw128_offset(k_row(row), cc), pack_bf16x2(k0 * P0, k1 * P1));  // Ks
     // Qg (rows 64-127 of B1) and X share 2^Gamma = P 2^r_b
     sts_u32(blk + OFF_B1 + pan * 16384, sw128_offset(64 + row, cc),
             pack_bf16x2(q0 * P0 * erb0, q1 * P1 * erb1));
@@ -411,28 +420,24 @@ __global__ void __launch_bounds__(256, 2)
   if (!mbar_wait(&bars[1], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
   tc_fence_after();
 
-  // ---- epilogue A: TMEM lanes 0-63 hold query rows, 64-127 key rows.  Row i of block I
-  // uses the 16(I+1) columns of D_I; a quadrant's two blocks span 16-column pieces 0-2
-  // (blocks 0, 1) or 3-9 (blocks 2, 3), shared by the quadrant's two warps ----
+  // ---- epilogue A: TMEM lane quadrant b holds row block b: queries in lanes 0-15, keys
+  // in lanes 16-31.  Row i of block b uses the 16(b+1) columns of D_b, in 16-column pieces
+  // shared by the quadrant's two warps ----
   float* sL = reinterpret_cast<float*>(sm + P_KA);  // beta Akk0 [64][65]; Ka no longer needed
   float* sX = sL + 64 * SOLVE_LD;                   // (I + beta Akk0)^-1 [64][65]
   {
-    const int qd = warp & 3, hh = warp >> 2;
-    const bool isk = qd >= 2;
-    const int i = 32 * (qd & 1) + lane;
-    const int I = i >> 4;
-    const bool gw = (sFlag[0] >> I) & 1;
+    const int bq = warp & 3, hh = warp >> 2;
+    const bool isk = lane >= 16;
+    const int i = 16 * bq + (lane & 15);
+    const bool diag_exact = (sFlag[0] >> bq) & 1;
     const float bi = sBeta[i];
-    const float* dg = sDiag + I * 512 + (isk ? 256 : 0) + (i - 16 * I) * 16;
-    const int pc0 = (qd & 1) ? 3 : 0, pc1 = (qd & 1) ? 10 : 3;
-    for (int pc = pc0 + hh; pc < pc1; pc += 2) {
-      const int bI = pc == 0 ? 0 : (pc < 3 ? 1 : (pc < 6 ? 2 : 3));
-      const int jb = 16 * pc - (int)ka_row(bI);  // first key index of the piece
+    const float* dg = sDiag + bq * 512 + (isk ? 256 : 0) + (lane & 15) * 16;
+    for (int pc = hh; pc <= bq; pc += 2) {
+      const int jb = 16 * pc;  // first key index of the piece
       uint32_t r[16];
-      tmem_ld16(tmem_addr(tmem, 32 * qd, 16 * pc), r);
+      tmem_ld16(tmem_addr(tmem, 32 * bq, ka_row(bq) + jb), r);
       tmem_wait_ld();
-      if (I != bI) continue;
-      const bool diag = gw && jb == 16 * I;
+      const bool diag = diag_exact && pc == bq;
       float vals[16];
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
@@ -455,7 +460,7 @@ __global__ void __launch_bounds__(256, 2)
       }
     }
     if (!isk && hh == 0) {  // Aqk columns past the row's block are zero
-      for (int j0 = 16 * (I + 1); j0 < TC_C; j0 += 8)
+      for (int j0 = 16 * (bq + 1); j0 < TC_C; j0 += 8)
         sts_v4(blk + OFF_B2, sw128_offset(i, j0), 0u, 0u, 0u, 0u);
     }
   }
@@ -1000,19 +1005,21 @@ cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s) {
   if (a.c_end <= a.c_begin) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
-  // q, k, g tiles: [64 tokens x 64 channels] boxes with 128-byte swizzle (MMA operands)
+  // q, k tiles: [16 tokens x 64 channels] boxes, g tiles: [64 tokens x 64 channels] boxes,
+  // all with 128-byte swizzle (MMA operand layout)
   CUtensorMap qmap, kmap, gmap;
   const cuuint64_t qdims[3] = {(cuuint64_t)TC_K, (cuuint64_t)p.H, (cuuint64_t)p.ntok};
   const cuuint64_t qstr[2] = {(cuuint64_t)TC_K * 2, (cuuint64_t)p.H * TC_K * 2};
   const cuuint64_t gdims[3] = {(cuuint64_t)TC_K, (cuuint64_t)p.HV, (cuuint64_t)p.ntok};
   const cuuint64_t gstr[2] = {(cuuint64_t)TC_K * 2, (cuuint64_t)p.HV * TC_K * 2};
   const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t box16[3] = {64, 1, 16};  // q / k: one 16-token row block per box
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), qdims, qstr,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   box16, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  r = enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k), qdims, qstr, box,
+  r = enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k), qdims, qstr, box16,
           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
