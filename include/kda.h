@@ -113,8 +113,8 @@ kda_status kda_fwd_check(const kda_fwd_params* p);
    if non-NULL, final_state.  Rows of o that no sequence covers (varlen padding)
    are left untouched.  Returns KDA_ERR_CUDA if a launch fails.
    When few (sequence, value head) recurrences would leave most SMs idle (bf16
-   tensor-core path, N * HV <= 96, at least 128 chunks), the chunk range is cut
-   into up to 16 segments: the intra-chunk kernel of segment k+1 runs on `stream`
+   tensor-core path, N * HV <= 96, at least 256 chunks), the chunk range is cut
+   into up to 8 segments: the intra-chunk kernel of segment k+1 runs on `stream`
    while the recurrence of segment k runs on a library-owned high-priority stream
    of the current device, the fp32 state carried between segments in the
    workspace.  The work is still ordered after everything enqueued on `stream`

@@ -40,10 +40,28 @@ bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(pt
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Pipelined schedule limits: segment only when at most this many (sequence, value head)
-// recurrences run (each takes one SM), with at least kSegChunks chunks per segment.
+// recurrences run (each takes one SM), with about kSegChunks chunks per segment (each
+// segment costs a few microseconds of launch and pipeline start-up; 8 segments of 128
+// chunks measured best for 1024 chunks).
 constexpr int64_t kSegMaxRecurrences = 96;
-constexpr int64_t kSegChunks = 64;
-constexpr int kMaxSegments = 16;
+constexpr int64_t kSegChunks = 128;
+constexpr int kMaxSegments = 8;
+
+// Chunk boundary k (0..nseg) of the segments: weights 1, 2, 4, ..., 4, 2, 1 so that the
+// first intra-chunk segment (which runs alone) and the last recurrence segment (which
+// also runs alone) are short.
+int64_t seg_bound(int64_t nct, int nseg, int k) {
+  auto weight = [nseg](int j) {
+    const int e = j < nseg - 1 - j ? j : nseg - 1 - j;  // distance to the nearer end
+    return e == 0 ? 1 : (e == 1 ? 2 : 4);
+  };
+  int64_t tot = 0, part = 0;
+  for (int j = 0; j < nseg; ++j) {
+    tot += weight(j);
+    if (j < k) part += weight(j);
+  }
+  return nct * part / tot;
+}
 
 // Every check that needs no workspace and no CUDA call.
 kda_status check_args(const kda_fwd_params* p) {
@@ -209,8 +227,8 @@ cudaError_t launch_pipelined(const FwdArgs& a, cudaStream_t s, const char** what
   if ((e = cudaStreamWaitEvent(cx->rs, cx->fork, 0)) != cudaSuccess) return e;
   for (int k = 0; k < pl.nseg; ++k) {
     FwdArgs ak = a;
-    ak.c_begin = pl.nct * k / pl.nseg;
-    ak.c_end = pl.nct * (k + 1) / pl.nseg;
+    ak.c_begin = seg_bound(pl.nct, pl.nseg, k);
+    ak.c_end = seg_bound(pl.nct, pl.nseg, k + 1);
     *what = "tc_intra";
     if ((e = launch_tc_intra(ak, s)) != cudaSuccess) return e;
     *what = "pipeline event";

@@ -228,19 +228,24 @@ def check_pipelined(inp):
 
 @pytest.mark.parametrize("gate", [kin.GATE_SAFE, kin.GATE_PLAIN])
 def test_tc_pipelined_one_long_sequence(gate):
-    """129 chunks of one sequence: two segments, the state carried between them."""
-    check_pipelined(kin.make_inputs(tc(T=64 * 128 + 37, gate=gate, seed=400 + gate)))
+    """257 chunks of one sequence: two segments, the state carried between them."""
+    check_pipelined(kin.make_inputs(tc(T=64 * 256 + 37, gate=gate, seed=400 + gate)))
+
+
+def test_tc_pipelined_ramped_segments():
+    """640 chunks: five segments of uneven (ramped) length."""
+    check_pipelined(kin.make_inputs(tc(T=64 * 640, H=1, HV=1, seed=402)))
 
 
 def test_tc_pipelined_batch_boundary_inside_a_sequence():
-    """B=3 x 44 chunks: the segment boundary (chunk 66) falls inside the second sequence."""
-    check_pipelined(kin.make_inputs(tc(B=3, T=64 * 43 + 10, seed=405)))
+    """B=3 x 91 chunks: the segment boundary (chunk 136) falls inside the second sequence."""
+    check_pipelined(kin.make_inputs(tc(B=3, T=64 * 90 + 10, seed=405)))
 
 
 def test_tc_pipelined_varlen_with_empty_sequences():
     """Varlen with an empty sequence in the middle and one at the end; the boundary (chunk
-    67) falls inside the third sequence."""
-    wl = tc(T=8537, varlen=5, maxlen=4600, seed=410)
+    133) falls inside the third sequence."""
+    wl = tc(T=17037, varlen=5, maxlen=9100, seed=410)
     inp = kin.make_inputs(wl)
-    inp.cu_seqlens[:] = np.array([0, 4000, 4000, 8500, 8537, 8537], dtype=np.int64)
+    inp.cu_seqlens[:] = np.array([0, 8000, 8000, 17000, 17037, 17037], dtype=np.int64)
     check_pipelined(inp)
