@@ -694,8 +694,8 @@ constexpr uint32_t SL_D = 65536;
 constexpr uint32_t SL_V = 66560;                     // v tile [64 tokens x 128 v], 2 MN panels
 constexpr uint32_t SLOT = 82944;
 constexpr uint32_t R_RING = 0;                       // 2 slots
-constexpr uint32_t R_STG = 2 * SLOT;                 // O staging [64 tokens x 128 v] bf16
-constexpr uint32_t R_BAR = R_STG + 16384;            // full[2], bar_v, bar_s, bar_vn, bar_st
+constexpr uint32_t R_STG = 2 * SLOT;                 // O staging [2][64 tokens x 128 v] bf16
+constexpr uint32_t R_BAR = R_STG + 32768;            // full[2], bar_v, bar_s, bar_vn, bar_st
 constexpr uint32_t R_TMEM = R_BAR + 64;
 constexpr uint32_t R_END = R_TMEM + 16;
 constexpr uint32_t R_SMEM = R_END + 1024;
@@ -705,6 +705,9 @@ constexpr uint32_t TM_O = 64;    // O^T fp32 [128 v x 64 tokens]
 constexpr uint32_t TM_S = 128;   // S^T fp32 [128 v x 128 ch]
 constexpr uint32_t TM_SA = 256;  // S^T bf16 pairs (A operand), 64 columns
 constexpr uint32_t TM_VA = 320;  // V_new^T bf16 pairs (A operand), 32 columns
+#ifndef USE_TMA_STORE
+#define USE_TMA_STORE 1
+#endif
 constexpr int kPrefetch = 4;     // chunks whose loads are prefetched into L2 ahead
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
@@ -802,9 +805,12 @@ __global__ void __launch_bounds__(kRecThreads, 1)
                    sdesc_sw128(tb + ks * 32, 16, 1024), idesc_bf16(128, 64, true), ks > 0);
         return true;
       };
+      // Slot s holds chunks s, s+2, ...: chunk ci+2 is copied in as soon as G2+O2 of chunk ci
+      // (the last reader of the slot) completes, a whole chunk before U of chunk ci+2 needs it
       if (nch > 0) {
         issue(0, 0);
-        for (int64_t d = 1; d <= kPrefetch && d < nch; ++d) prefetch(d);
+        if (nch > 1) issue(1, 1);
+        for (int64_t d = 2; d < 2 + kPrefetch && d < nch; ++d) prefetch(d);
         if (!issue_u(0)) ok = false;
       }
       for (int64_t ci = 0; ci < nch && ok; ++ci) {
@@ -820,9 +826,6 @@ __global__ void __launch_bounds__(kRecThreads, 1)
                       sdesc_sw128(b1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                       idesc_bf16(128, 128), 1);
         mma_commit(bar_v);
-        // slot s^1 (chunk ci-1) is free: G2+O2 of chunk ci-1 completed before bar_st
-        if (ci + 1 < nch) issue(ci + 1, s ^ 1);
-        if (ci + 1 + kPrefetch < nch) prefetch(ci + 1 + kPrefetch);
         // G2+O2 need the bf16 V_new^T of this chunk
         if (!mbar_wait(bar_vn, (uint32_t)(ci & 1))) { ok = false; break; }
         tc_fence_after();
@@ -832,6 +835,11 @@ __global__ void __launch_bounds__(kRecThreads, 1)
                       idesc_bf16(128, 192), 1);
         mma_commit(bar_s);
         if (ci + 1 < nch && !issue_u(ci + 1)) { ok = false; break; }
+        if (ci + 2 < nch) {
+          if (!mbar_wait(bar_s, (uint32_t)(ci & 1))) { ok = false; break; }
+          issue(ci + 2, s);
+          if (ci + 2 + kPrefetch < nch) prefetch(ci + 2 + kPrefetch);
+        }
       }
       if (!ok) {
         flag_status(a.status, KDA_DEV_TIMEOUT);
@@ -851,9 +859,8 @@ __global__ void __launch_bounds__(kRecThreads, 1)
       if (lane == 0) mbar_arrive(bar);
     };
     auto slot_of = [&](int64_t ci) { return sm + R_RING + (int)(ci & 1) * SLOT; };
-    // bf16 copy of 32 state columns into the A operand; then S^T Diag(e^gamma_C) of chunk
-    // ci (waiting for that chunk's data) back into the accumulator
-    auto publish_state = [&](float (&S)[32], int64_t ci) -> bool {
+    // bf16 copy of 32 state columns into the A operand of G1+O1; releases G1+O1
+    auto publish_state = [&](const float (&S)[32]) {
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
@@ -861,37 +868,49 @@ __global__ void __launch_bounds__(kRecThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       arrive(bar_st);
-      if (ci >= nch) return true;
+    };
+    // S^T Diag(e^gamma_C) of chunk ci into the accumulator (before G2+O2 of chunk ci)
+    auto rescale_state = [&](const float (&S)[32], int64_t ci) -> bool {
       const bool w = mbar_wait(&full[ci & 1], (uint32_t)((ci >> 1) & 1));
       const float4* dec = reinterpret_cast<const float4*>(slot_of(ci) + SL_D) + 8 * part;
-      uint32_t sc[32];
 #pragma unroll
-      for (int x4 = 0; x4 < 8; ++x4) {
-        const float4 d = dec[x4];
-        sc[4 * x4 + 0] = __float_as_uint(S[4 * x4 + 0] * d.x);
-        sc[4 * x4 + 1] = __float_as_uint(S[4 * x4 + 1] * d.y);
-        sc[4 * x4 + 2] = __float_as_uint(S[4 * x4 + 2] * d.z);
-        sc[4 * x4 + 3] = __float_as_uint(S[4 * x4 + 3] * d.w);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sc[16];
+#pragma unroll
+        for (int x4 = 0; x4 < 4; ++x4) {
+          const float4 d = dec[4 * h + x4];
+          const int j = 16 * h + 4 * x4;
+          sc[4 * x4 + 0] = __float_as_uint(S[j + 0] * d.x);
+          sc[4 * x4 + 1] = __float_as_uint(S[j + 1] * d.y);
+          sc[4 * x4 + 2] = __float_as_uint(S[j + 2] * d.z);
+          sc[4 * x4 + 3] = __float_as_uint(S[j + 3] * d.w);
+        }
+        tmem_st16(lane_base + TM_S + 32 * part + 16 * h, sc);
       }
-      tmem_st32(lane_base + TM_S + 32 * part, sc);
       tmem_wait_st();
       return w;
     };
     __nv_bfloat16* go = static_cast<__nv_bfloat16*>(a.o);
     const CUtensorMap* omap_ptr = &omap;
-    // O^T of chunk ci (already in the staging tile as [token][v]): one TMA store for a
-    // full chunk, 16-byte stores of the valid rows otherwise
-    auto store_o = [&](int64_t ci, bool good) -> bool {
+    // O of chunk ci (this thread: 16 tokens of column v) through staging tile ci & 1: one TMA
+    // store for a full chunk, 16-byte stores of the valid rows otherwise.  The tile was last
+    // read by the store of chunk ci-2, which the first barrier confirms.
+    auto store_o = [&](int64_t ci, const uint32_t (&ro)[16], bool good) -> bool {
       const int64_t t0 = bos + ci * TC_C;
       const int L = (int)((eos - t0) < TC_C ? (eos - t0) : TC_C);
-      uint8_t* stg = sm + R_STG;
+      uint8_t* stg = sm + R_STG + (uint32_t)(ci & 1) * 16384u;
+      if (tid == 0) bulk_wait_read1();
+      good = named_bar_and(1, kEpiThreads, good);
+#pragma unroll
+      for (int x = 0; x < 16; ++x)
+        *reinterpret_cast<__nv_bfloat16*>(stg + (16 * part + x) * 256 + v * 2) =
+            __float2bfloat16_rn(__uint_as_float(ro[x]));
       fence_async_smem();
       good = named_bar_and(1, kEpiThreads, good);
-      if (L == TC_C) {
+      if (USE_TMA_STORE && L == TC_C) {
         if (tid == 0) {
           tma_store_3d(omap_ptr, 0, hv, (int32_t)t0, stg);
           bulk_commit();
-          bulk_wait_read0();  // the staging tile is rewritten for the next chunk
         }
       } else {
         for (int e = tid; e < L * 16; e += kEpiThreads) {
@@ -900,7 +919,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
               reinterpret_cast<const uint4*>(stg + row * 256)[c16];
         }
       }
-      return named_bar_and(1, kEpiThreads, good);
+      return good;
     };
 
     {  // initial state -> bf16 A operand and the accumulator (scaled for chunk 0); O^T = 0
@@ -915,7 +934,8 @@ __global__ void __launch_bounds__(kRecThreads, 1)
         for (int j = 0; j < 32; ++j) sout[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
       }
       tmem_st16_zero(lane_base + TM_O + 16 * part);
-      if (!publish_state(S, 0)) ok = false;
+      publish_state(S);
+      if (nch > 0 && !rescale_state(S, 0)) ok = false;
     }
 
     for (int64_t ci = 0; ci < nch; ++ci) {
@@ -934,39 +954,36 @@ __global__ void __launch_bounds__(kRecThreads, 1)
       }
       tc_fence_before();
       arrive(bar_vn);
-      // O^T of chunk ci -> staging tile (then cleared); S^T of chunk ci+1 -> bf16 copy for
-      // G1+O1 and rescaled accumulator for G2+O2
+      // S^T of chunk ci+1 and O^T of chunk ci in one tensor-memory round trip; O^T cleared,
+      // then G1+O1 of chunk ci+1 released before the output and the rescale are handled
       w = mbar_wait(bar_s, (uint32_t)(ci & 1)) && w;
       tc_fence_after();
+      uint32_t ro[16];
       {
-        uint32_t r[16];
-        tmem_ld16(lane_base + TM_O + 16 * part, r);
+        uint32_t r0[16], r1[16];
+        tmem_ld16(lane_base + TM_S + 32 * part, r0);
+        tmem_ld16(lane_base + TM_S + 32 * part + 16, r1);
+        tmem_ld16(lane_base + TM_O + 16 * part, ro);
         tmem_wait_ld();
         tmem_st16_zero(lane_base + TM_O + 16 * part);
-        uint8_t* stg = sm + R_STG;
-#pragma unroll
-        for (int x = 0; x < 16; ++x)
-          *reinterpret_cast<__nv_bfloat16*>(stg + (16 * part + x) * 256 + v * 2) =
-              __float2bfloat16_rn(__uint_as_float(r[x]));
         float S[32];
-        tmem_ld16(lane_base + TM_S + 32 * part, r);
-        tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) S[j] = __uint_as_float(r[j]);
-        tmem_ld16(lane_base + TM_S + 32 * part + 16, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) S[16 + j] = __uint_as_float(r[j]);
-        if (ci + 1 == nch && sout != nullptr) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) sout[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
+        for (int j = 0; j < 16; ++j) {
+          S[j] = __uint_as_float(r0[j]);
+          S[16 + j] = __uint_as_float(r1[j]);
         }
-        if (ci + 1 < nch)
-          w = publish_state(S, ci + 1) && w;
-        else
+        if (ci + 1 < nch) {
+          publish_state(S);
+          w = rescale_state(S, ci + 1) && w;
+        } else {
           tmem_wait_st();
+          if (sout != nullptr) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sout[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
+          }
+        }
       }
-      if (!store_o(ci, w)) { ok = false; break; }
+      if (!store_o(ci, ro, w)) { ok = false; break; }
     }
     if (!ok) flag_status(a.status, KDA_DEV_TIMEOUT);
     if (tid == 0) bulk_wait0();
