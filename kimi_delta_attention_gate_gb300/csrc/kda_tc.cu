@@ -90,6 +90,36 @@ __device__ __forceinline__ float sigmoid_fast(float x) {
 __device__ __forceinline__ float softplus_fast(float x) {
   return x > 20.0f ? x : log1pf(ex2(x * kLog2e));
 }
+// Packed fp32 pair arithmetic (one instruction for both channels of a pair; each half is
+// rounded exactly as the scalar operation would be)
+__device__ __forceinline__ uint64_t u64_of(float2 v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_of(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(u64_of(a)), "l"(u64_of(b)));
+  return f2_of(r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(u64_of(a)), "l"(u64_of(b)));
+  return f2_of(r);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(u64_of(a)), "l"(u64_of(b)), "l"(u64_of(c)));
+  return f2_of(r);
+}
+__device__ __forceinline__ float2 bf_pair(uint32_t v) { return make_float2(bf_lo(v), bf_hi(v)); }
+__device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16x2(v.x, v.y); }
+
 template <int GATE>
 __device__ __forceinline__ float gate_fast(float x, float a, float lb) {
   if (GATE == KDA_GATE_PLAIN) return -a * softplus_fast(x);
@@ -243,14 +273,22 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = 16 * rg + r;
-    float g0 = 0.f, g1 = 0.f;
+    float2 gp = make_float2(0.f, 0.f);
     if (row < L) {
       const uint32_t gv = lds_u32(x_pan, sw128_offset(row, cc));
-      g0 = gate_fast<GATE>(bf_lo(gv) + dt0, aexp, lb);
-      g1 = gate_fast<GATE>(bf_hi(gv) + dt1, aexp, lb);
+      if (GATE == KDA_GATE_SAFE) {  // lb sigmoid(a x) on the channel pair
+        const float2 y = mul2(add2(bf_pair(gv), make_float2(dt0, dt1)), make_float2(aexp, aexp));
+        const float2 z = mul2(y, make_float2(-kLog2e, -kLog2e));
+        const float2 d = add2(make_float2(ex2(z.x), ex2(z.y)), make_float2(1.f, 1.f));
+        gp = mul2(make_float2(rcp_approx(d.x), rcp_approx(d.y)), make_float2(lb, lb));
+      } else {
+        gp.x = gate_fast<GATE>(bf_lo(gv) + dt0, aexp, lb);
+        gp.y = gate_fast<GATE>(bf_hi(gv) + dt1, aexp, lb);
+      }
     }
-    acc0 = fmaf(g0, kLog2e, acc0);
-    acc1 = fmaf(g1, kLog2e, acc1);
+    const float2 acc = fma2(gp, make_float2(kLog2e, kLog2e), make_float2(acc0, acc1));
+    acc0 = acc.x;
+    acc1 = acc.y;
     G0[r] = acc0;
     G1[r] = acc1;
     span = fmaxf(span, fmaxf(fabsf(acc0), fabsf(acc1)));
@@ -326,12 +364,11 @@ __global__ void __launch_bounds__(256, 2)
   const float ekg0 = ex2(gl0 - rb0), ekg1 = ex2(gl1 - rb1);
   if (rg == 0)
     *reinterpret_cast<float2*>(blk + OFF_D + 4 * c0) = make_float2(ex2(gl0), ex2(gl1));
-  float F0[4], F1[4];  // 2^(r_I - r_b) for the blocks I > rg that see this block's keys
+  float2 F[4];  // 2^(r_I - r_b) for the blocks I > rg that see this block's keys
 #pragma unroll
-  for (int I = 0; I < 4; ++I) {
-    F0[I] = (I > rg) ? ex2(rI0[I] - rb0) : 1.f;
-    F1[I] = (I > rg) ? ex2(rI1[I] - rb1) : 1.f;
-  }
+  for (int I = 0; I < 4; ++I)
+    F[I] = (I > rg) ? make_float2(ex2(rI0[I] - rb0), ex2(rI1[I] - rb1)) : make_float2(1.f, 1.f);
+  const float2 erb = make_float2(erb0, erb1), ekg = make_float2(ekg0, ekg1);
   if (sFlag[0] != 0) {  // some block needs its diagonal entries evaluated exactly
     // the thread's gate cumsums go to a scratch row in the (not yet written) Ka tile, so
     // that the rarely taken evaluation can run as compact loops out of line
@@ -352,28 +389,30 @@ __global__ void __launch_bounds__(256, 2)
     const int row = 16 * rg + r;
     const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(q_row(row), cc)) : 0u;
     const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(k_row(row), cc)) : 0u;
-    const float qn = sNorm[2 * row], kn = sNorm[2 * row + 1];
-    const float q0 = bf_lo(qv) * qn, q1 = bf_hi(qv) * qn;
-    const float k0 = bf_lo(kv) * kn, k1 = bf_hi(kv) * kn;
-    const float P0 = ex2(G0[r]), P1 = ex2(G1[r]);  // 2^(Gamma - r_b) <= 1
-    sts_u32(qk_pan, sw128_offset(q_row(row), cc), pack_bf16x2(q0 * P0, q1 * P1));  // Qs
-    sts_u32(qk_pan, sw128_offset(k_row(row), cc), pack_bf16x2(k0 * P0, k1 * P1));  // Ks
+    const float2 nrm = *reinterpret_cast<const float2*>(sNorm + 2 * row);  // (qn, kn)
+    const float2 qf = mul2(bf_pair(qv), make_float2(nrm.x, nrm.x));
+    const float2 kf = mul2(bf_pair(kv), make_float2(nrm.y, nrm.y));
+    const float k0 = kf.x, k1 = kf.y;
+    const float2 P = make_float2(ex2(G0[r]), ex2(G1[r]));  // 2^(Gamma - r_b) <= 1
+    const float2 qs = mul2(qf, P), ks = mul2(kf, P);
+    sts_u32(qk_pan, sw128_offset(q_row(row), cc), pack2(qs));  // Qs
+    sts_u32(qk_pan, sw128_offset(k_row(row), cc), pack2(ks));  // Ks
     // Qg (rows 64-127 of B1) and X share 2^Gamma = P 2^r_b
-    sts_u32(blk + OFF_B1 + pan * 16384, sw128_offset(64 + row, cc),
-            pack_bf16x2(q0 * P0 * erb0, q1 * P1 * erb1));
-    sts_u32(x_pan, sw128_offset(row, cc), pack_bf16x2(k0 * P0 * erb0, k1 * P1 * erb1));
+    sts_u32(blk + OFF_B1 + pan * 16384, sw128_offset(64 + row, cc), pack2(mul2(qs, erb)));
+    sts_u32(x_pan, sw128_offset(row, cc), pack2(mul2(ks, erb)));
     float kg0, kg1;
     if (!guard) {
-      const float E0 = ex2(-G0[r]), E1 = ex2(-G1[r]);  // 2^(r_b - Gamma) <= 2^120
-      const float ke0 = k0 * E0, ke1 = k1 * E1;
+      const float2 E = make_float2(ex2(-G0[r]), ex2(-G1[r]));  // 2^(r_b - Gamma) <= 2^120
+      const float2 ke = mul2(kf, E);
 #pragma unroll
       for (int I = 0; I < 4; ++I) {
         if (I < rg) continue;
         sts_u32(sm + P_KA + pan * KA_PANEL, sw128_offset(ka_row(I) + row, cc),
-                pack_bf16x2(ke0 * F0[I], ke1 * F1[I]));
+                pack2(I == rg ? ke : mul2(ke, F[I])));
       }
-      kg0 = ke0 * ekg0;
-      kg1 = ke1 * ekg1;
+      const float2 kg = mul2(ke, ekg);
+      kg0 = kg.x;
+      kg1 = kg.y;
     } else {
       // every exponent below is <= 0; the diagonal block is evaluated exactly above
 #pragma unroll
