@@ -256,6 +256,30 @@ def run_reference(args, wl):
     return 0
 
 
+# ---------------------------------------------------------------------------------------
+# replicas over ranks (one process per GPU; no exchange on the data path)
+# ---------------------------------------------------------------------------------------
+
+def replica_inputs(wl: kin.Workload, rank: int) -> kin.Inputs:
+    """Rank `rank`'s own seeded copy of the workload (same shapes, different values)."""
+    return kin.make_inputs(wl, seed=wl.seed + 1000 * rank)
+
+
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The slowest rank's figure (a time), identical on every rank."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's step time."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
 def config_of(inp: kin.Inputs, args):
     wl = inp.wl
     return {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "HV": wl.HV, "K": wl.K,
@@ -316,7 +340,7 @@ def main():
     kb.load()
 
     # Inputs: each rank its own replica (seed offset by rank), uploaded once.
-    inp = kin.make_inputs(wl, seed=wl.seed + 1000 * rank)
+    inp = replica_inputs(wl, rank)
     dev = torch.device("cuda", local_rank)
 
     def up(x, dtype):
@@ -399,13 +423,9 @@ def main():
             stage_ms[i] += prev.elapsed_time(evs[s_][i])
             prev = evs[s_][i]
     stage_ms /= args.steps
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
-    tokens_all = inp.n_tokens * world
-    value = tokens_all / (ms_per_step / 1e3)
+    value = job_throughput(inp.n_tokens, world, ms_per_step)
     status = kb.kda_get_device_status(sh)
     if status != 0:
         raise RuntimeError(f"device status {status:#x} after the timed region")
@@ -441,11 +461,8 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = tokens_all / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_value = job_throughput(inp.n_tokens, world, e2e_ms)
 
     # Roofline of the dominant kernel.
     peaks, peak_kind = load_peaks()
