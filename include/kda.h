@@ -28,9 +28,10 @@
  *   beta      [B, T, HV]         in_dtype (logits if beta_sigmoid, else the value)
  *   A_log     [HV]               fp32
  *   dt_bias   [HV * K]           fp32 (same memory as [HV, K])
- *   h0        [N, HV, K, V]      fp32 (state stored d_k x d_v, forward step 4 of the reading notes)
+ *   h0        [N, HV, K, V]      fp32 (state stored d_k x d_v, forward step 4 of the reading notes;
+ *                                [N, HV, V, K] with state_v_first)
  *   o         [B, T, HV, V]      in_dtype
- *   final_state [N, HV, K, V]    fp32
+ *   final_state [N, HV, K, V]    fp32 (layout as h0)
  *   cu_seqlens [N + 1]           int64; with it B must be 1 and sequence n spans tokens
  *                                [cu[n], cu[n+1]) of the flattened batch (varlen, section 2.2)
  *
@@ -81,6 +82,12 @@ typedef struct kda_fwd_params {
   int32_t qk_l2norm;         /* 1: q, k are L2-normalised in-kernel over K (section 2.2) */
   int32_t beta_sigmoid;      /* 1: beta holds logits, the kernel applies sigmoid (section 2.2) */
   int32_t N;                 /* number of sequences: B, or len(cu_seqlens) - 1 */
+  int32_t allow_neg_eigval;  /* 1: beta = 2 sigmoid(logit) in [0, 2), so that the transition
+                                I - beta k k^T may have a negative eigenvalue; needs
+                                beta_sigmoid ("Reading Notes: Implementation Notes for KDA in
+                                FLA", section 2.1) */
+  int32_t state_v_first;     /* 1: h0 and final_state are stored [N, HV, V, K] (the state
+                                transposed; section 2.2 of the same notes) */
   const void* q;
   const void* k;
   const void* v;
@@ -179,7 +186,7 @@ const char* kda_last_error(void);
 /* ABI version of this header (incremented on incompatible changes). */
 int32_t kda_abi_version(void);
 
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

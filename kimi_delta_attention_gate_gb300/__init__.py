@@ -44,8 +44,12 @@ def make_params(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None,
                 initial_state=None, final_state=None, o=None, cu_seqlens=None,
                 cu_seqlens_cpu=None, chunk_size: int = 64, use_gate_in_kernel: bool = True,
                 safe_gate: Optional[bool] = None, use_qk_l2norm_in_kernel: bool = True,
-                use_beta_sigmoid_in_kernel: bool = True, workspace=None) -> kda_fwd_params:
-    """Fill a ``kda_fwd_params`` from tensors (no checks beyond shapes; the C layer checks)."""
+                use_beta_sigmoid_in_kernel: bool = True, allow_neg_eigval: bool = False,
+                transpose_state_layout: bool = False, workspace=None) -> kda_fwd_params:
+    """Fill a ``kda_fwd_params`` from tensors (no checks beyond shapes; the C layer checks).
+
+    ``allow_neg_eigval``: beta = 2 sigmoid(logit) in [0, 2).  ``transpose_state_layout``
+    (the notes' ``state_v_first``): initial / final states are [N, HV, V, K]."""
     import torch
     if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or g.dim() != 4 or beta.dim() != 3:
         raise ValueError("expected q,k [B,T,H,K], v [B,T,HV,V], g [B,T,HV,K], beta [B,T,HV]")
@@ -71,8 +75,9 @@ def make_params(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None,
     if dt_bias is not None and dt_bias.numel() != HV * K:
         raise ValueError("dt_bias must be [HV*K] (or [HV, K])")
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
-    if initial_state is not None and tuple(initial_state.shape) != (N, HV, K, V):
-        raise ValueError("initial_state must be [N,HV,K,V] float32")
+    st_shape = (N, HV, V, K) if transpose_state_layout else (N, HV, K, V)
+    if initial_state is not None and tuple(initial_state.shape) != st_shape:
+        raise ValueError(f"initial_state must be {list(st_shape)} float32")
     p = kda_fwd_params()
     p.B, p.T, p.H, p.HV, p.K, p.V = B, T, H, HV, K, V
     p.chunk_size = int(chunk_size)
@@ -83,6 +88,8 @@ def make_params(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None,
     p.qk_l2norm = int(bool(use_qk_l2norm_in_kernel))
     p.beta_sigmoid = int(bool(use_beta_sigmoid_in_kernel))
     p.N = N
+    p.allow_neg_eigval = int(bool(allow_neg_eigval))
+    p.state_v_first = int(bool(transpose_state_layout))
     p.q, p.k, p.v, p.g, p.beta = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
     p.A_log, p.dt_bias, p.h0 = _ptr(A_log), _ptr(dt_bias), _ptr(initial_state)
     p.cu_seqlens = _ptr(cu_seqlens)
@@ -101,12 +108,13 @@ def kda_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None, sca
             initial_state=None, output_final_state: bool = True, cu_seqlens=None,
             cu_seqlens_cpu=None, chunk_size: int = 64, use_gate_in_kernel: bool = True,
             safe_gate: Optional[bool] = None, use_qk_l2norm_in_kernel: bool = True,
-            use_beta_sigmoid_in_kernel: bool = True, workspace=None, o=None, final_state=None,
+            use_beta_sigmoid_in_kernel: bool = True, allow_neg_eigval: bool = False,
+            transpose_state_layout: bool = False, workspace=None, o=None, final_state=None,
             stream=None) -> Tuple["torch.Tensor", Optional["torch.Tensor"]]:
     """Chunk-parallel KDA forward on the current CUDA device.  Returns (o, final_state).
 
-    o has v's dtype and shape [B,T,HV,V]; final_state is fp32 [N,HV,K,V] (None if
-    ``output_final_state`` is False).  With ``cu_seqlens`` (int64 [N+1], B == 1),
+    o has v's dtype and shape [B,T,HV,V]; final_state is fp32 [N,HV,K,V] ([N,HV,V,K] with
+    ``transpose_state_layout``; None if ``output_final_state`` is False).  With ``cu_seqlens`` (int64 [N+1], B == 1),
     rows of o outside every sequence are zero.  Asynchronous on ``stream``
     (default: the current PyTorch stream).
     """
@@ -124,13 +132,16 @@ def kda_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None, sca
         padded = cu_seqlens is not None and int(cu_seqlens_cpu[-1]) < B * T
         o = (torch.zeros if padded else torch.empty)((B, T, HV, V), dtype=v.dtype, device=v.device)
     if final_state is None and output_final_state:
-        final_state = torch.empty((N, HV, K, V), dtype=torch.float32, device=v.device)
+        st_shape = (N, HV, V, K) if transpose_state_layout else (N, HV, K, V)
+        final_state = torch.empty(st_shape, dtype=torch.float32, device=v.device)
     p = make_params(q, k, v, g, beta, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound,
                     scale=scale, initial_state=initial_state, final_state=final_state, o=o,
                     cu_seqlens=cu_seqlens, cu_seqlens_cpu=cu_seqlens_cpu, chunk_size=chunk_size,
                     use_gate_in_kernel=use_gate_in_kernel, safe_gate=safe_gate,
                     use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel,
-                    use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel)
+                    use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
+                    allow_neg_eigval=allow_neg_eigval,
+                    transpose_state_layout=transpose_state_layout)
     _binding.raise_for(_binding.kda_fwd_check(p))
     need = _binding.kda_fwd_workspace_size(p)
     if workspace is None:

@@ -51,6 +51,7 @@ class kda_fwd_params(ctypes.Structure):
         ("gate_mode", ctypes.c_int32), ("lower_bound", ctypes.c_float),
         ("scale", ctypes.c_float), ("qk_l2norm", ctypes.c_int32),
         ("beta_sigmoid", ctypes.c_int32), ("N", ctypes.c_int32),
+        ("allow_neg_eigval", ctypes.c_int32), ("state_v_first", ctypes.c_int32),
         ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
         ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("A_log", ctypes.c_void_p),
         ("dt_bias", ctypes.c_void_p), ("h0", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),

@@ -97,8 +97,13 @@ kda_status check_args(const kda_fwd_params* p) {
       return fail(KDA_ERR_INVALID_ARG, "unknown gate_mode %d", p->gate_mode);
   }
   if (!isfinite(p->scale)) return fail(KDA_ERR_INVALID_ARG, "scale must be finite");
-  if ((p->qk_l2norm != 0 && p->qk_l2norm != 1) || (p->beta_sigmoid != 0 && p->beta_sigmoid != 1))
-    return fail(KDA_ERR_INVALID_ARG, "qk_l2norm and beta_sigmoid must be 0 or 1");
+  if ((p->qk_l2norm != 0 && p->qk_l2norm != 1) || (p->beta_sigmoid != 0 && p->beta_sigmoid != 1) ||
+      (p->allow_neg_eigval != 0 && p->allow_neg_eigval != 1) ||
+      (p->state_v_first != 0 && p->state_v_first != 1))
+    return fail(KDA_ERR_INVALID_ARG,
+                "qk_l2norm, beta_sigmoid, allow_neg_eigval and state_v_first must be 0 or 1");
+  if (p->allow_neg_eigval && !p->beta_sigmoid)  // reading notes section 2.1
+    return fail(KDA_ERR_INVALID_ARG, "allow_neg_eigval needs beta_sigmoid (beta = 2 sigmoid(logit))");
   // sequences
   if (p->cu_seqlens != nullptr) {
     if (p->B != 1) return fail(KDA_ERR_SHAPE, "cu_seqlens requires B == 1 (got B=%d)", p->B);
@@ -293,6 +298,7 @@ kda_status prepare(const kda_fwd_params* p, FwdArgs& a) {
   a.plan = pl;
   a.dtype = p->in_dtype; a.gate_mode = p->gate_mode;
   a.qk_l2norm = p->qk_l2norm; a.beta_sigmoid = p->beta_sigmoid;
+  a.allow_neg_eigval = p->allow_neg_eigval; a.state_v_first = p->state_v_first;
   a.lower_bound = p->lower_bound; a.scale = p->scale;
   a.q = p->q; a.k = p->k; a.v = p->v; a.g = p->g; a.beta = p->beta;
   a.A_log = p->A_log; a.dt_bias = p->dt_bias; a.h0 = p->h0; a.cu_seqlens = p->cu_seqlens;

@@ -32,7 +32,7 @@ struct Plan {
 // Arguments every kernel of the forward pass receives (by value).
 struct FwdArgs {
   Plan plan;
-  int dtype, gate_mode, qk_l2norm, beta_sigmoid;
+  int dtype, gate_mode, qk_l2norm, beta_sigmoid, allow_neg_eigval, state_v_first;
   float lower_bound, scale;
   const void* q;
   const void* k;

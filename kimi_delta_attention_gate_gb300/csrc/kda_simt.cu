@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kIntraThreads) simt_intra_kernel(const FwdArgs
     float b = 0.f;
     if (i < L) {
       b = to_f32(gb[(t0 + i) * HV + hv]);
-      if (a.beta_sigmoid) b = sigmoid_exact(b);
+      if (a.beta_sigmoid) b = (a.allow_neg_eigval ? 2.f : 1.f) * sigmoid_exact(b);
     }
     sB[i] = b;
   }
@@ -222,8 +222,10 @@ __global__ void __launch_bounds__(kRecThreads) simt_recur_kernel(const FwdArgs a
   Tin* go = static_cast<Tin*>(a.o);
   const size_t state_base = ((size_t)n * HV + hv) * (size_t)K * V;
 
-  for (int kk = warp; kk < K; kk += kRecWarps)
-    sS[kk * kBV + lane] = (a.h0 != nullptr && cv) ? a.h0[state_base + (size_t)kk * V + col] : 0.f;
+  for (int kk = warp; kk < K; kk += kRecWarps) {
+    const size_t si = a.state_v_first ? (size_t)col * K + kk : (size_t)kk * V + col;
+    sS[kk * kBV + lane] = (a.h0 != nullptr && cv) ? a.h0[state_base + si] : 0.f;
+  }
   __syncthreads();
 
   const int64_t nch = (eos - bos + C - 1) / C;
@@ -273,7 +275,8 @@ __global__ void __launch_bounds__(kRecThreads) simt_recur_kernel(const FwdArgs a
   }
   if (a.final_state != nullptr && cv)
     for (int kk = warp; kk < K; kk += kRecWarps)
-      a.final_state[state_base + (size_t)kk * V + col] = sS[kk * kBV + lane];
+      a.final_state[state_base + (a.state_v_first ? (size_t)col * K + kk : (size_t)kk * V + col)] =
+          sS[kk * kBV + lane];
 }
 
 // Varlen: chunk offsets cs[n] = sum_{m<n} ceil(len_m / C), one block.

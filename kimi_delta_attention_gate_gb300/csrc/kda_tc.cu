@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(256, 2)
   if (span > kGuardLog2) atomicOr(sFlag, 1 << rg);
   if (tid < TC_C) {
     float b = __bfloat162float(beta_raw);
-    if (a.beta_sigmoid && tid < L) b = sigmoid_fast(b);
+    if (a.beta_sigmoid && tid < L) b = (a.allow_neg_eigval ? 2.f : 1.f) * sigmoid_fast(b);
     sBeta[tid] = b;
   }
   // row sums of squares of q and k over the warp's 64 channels: a butterfly that halves
@@ -893,6 +893,12 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     const uint32_t lane_base = tmem_addr(tmem, 32 * q4, 0);
     const size_t sbase = ((size_t)n * HV + hv) * (size_t)TC_K * TC_V;
     float* sout = seq_end ? a.final_state : carry;
+    // state element (channel 32 part + j, column v): [K][V] in the carry buffer, [K][V] or
+    // [V][K] (state_v_first) in h0 / final_state
+    auto sidx = [&](int j, bool external) -> size_t {
+      return sbase + ((external && a.state_v_first) ? (size_t)v * TC_K + 32 * part + j
+                                                      : (size_t)(32 * part + j) * TC_V + v);
+    };
     auto arrive = [&](uint64_t* bar) {  // one arrival per warp, after the warp's writes
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
@@ -964,13 +970,11 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     {  // initial state -> bf16 A operand and the accumulator (scaled for chunk 0); O^T = 0
       float S[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const size_t idx = sbase + (size_t)(32 * part + j) * TC_V + v;
-        S[j] = !seq_start ? carry[idx] : (a.h0 != nullptr) ? a.h0[idx] : 0.f;
-      }
+      for (int j = 0; j < 32; ++j)
+        S[j] = !seq_start ? carry[sidx(j, false)] : (a.h0 != nullptr) ? a.h0[sidx(j, true)] : 0.f;
       if (nch == 0 && sout != nullptr) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sout[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
+        for (int j = 0; j < 32; ++j) sout[sidx(j, seq_end)] = S[j];
       }
       tmem_st16_zero(lane_base + TM_O + 16 * part);
       publish_state(S);
@@ -1018,7 +1022,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
           tmem_wait_st();
           if (sout != nullptr) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sout[sbase + (size_t)(32 * part + j) * TC_V + v] = S[j];
+            for (int j = 0; j < 32; ++j) sout[sidx(j, seq_end)] = S[j];
           }
         }
       }

@@ -159,16 +159,26 @@ def _segments(B, T, cu_seqlens):
 
 def fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, gate_mode=GATE_SAFE, lower_bound=None,
         scale=None, qk_l2norm=True, beta_sigmoid=True, initial_state=None, cu_seqlens=None,
-        l2_eps=L2_EPS, nthreads=0):
+        allow_neg_eigval=False, transpose_state_layout=False, l2_eps=L2_EPS, nthreads=0):
     """Token-recurrent KDA forward in fp64 (C).  Returns (o [B,T,HV,V], final_state [N,HV,K,V]).
 
     The recurrence S_t = Diag(a_t) S - b_t k_t (k_t^T Diag(a_t) S) + b_t k_t v_t^T,
     o_t = scale S_t^T q_t, with a_t = exp(g'_t).  With ``cu_seqlens`` the batch
     is flattened to B = 1 and sequence n spans tokens [cu[n], cu[n+1]) ([notes]
     section 2.2, varlen example); rows no sequence covers come back as 0.
+    ``allow_neg_eigval`` ([notes] section 2.1): beta = 2 sigmoid(logit), which needs
+    ``beta_sigmoid``.  ``transpose_state_layout`` ([notes] section 2.2, state_v_first):
+    initial and final states are [N,HV,V,K], the transpose of the K x V state.
     """
     lib = _load()
     q = _f64(q); k = _f64(k); v = _f64(v); g = _f64(g); beta = _f64(beta)
+    if allow_neg_eigval:
+        if not beta_sigmoid:
+            raise ValueError("allow_neg_eigval needs beta_sigmoid")
+        beta = 2.0 * sigmoid_np(beta)          # the C routine then takes beta as given
+        beta_sigmoid = False
+    if transpose_state_layout and initial_state is not None:
+        initial_state = np.swapaxes(np.asarray(initial_state), -1, -2)
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
     cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int64)
@@ -186,6 +196,8 @@ def fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, gate_mode=GATE_SAFE, lowe
                       N, _dptr(o), _dptr(fs), int(nthreads))
     if rc != 0:
         raise ValueError("oracle: inconsistent arguments")
+    if transpose_state_layout:
+        fs = np.ascontiguousarray(np.swapaxes(fs, -1, -2))
     return o, fs
 
 

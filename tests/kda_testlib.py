@@ -35,8 +35,9 @@ def gate_kwargs(wl: kin.Workload):
     return dict(use_gate_in_kernel=True)
 
 
-def run_gpu(inp: kin.Inputs, chunk_size=None, stream=None, workspace=None):
-    """The CUDA path on ``inp``; returns (o, final_state) as float64 numpy arrays."""
+def run_gpu(inp: kin.Inputs, chunk_size=None, stream=None, workspace=None, **opts):
+    """The CUDA path on ``inp``; returns (o, final_state) as float64 numpy arrays.  ``opts``:
+    allow_neg_eigval, transpose_state_layout (inp.h0 then already in that layout)."""
     import torch
     import kimi_delta_attention_gate_gb300 as kda
     wl = inp.wl
@@ -48,15 +49,15 @@ def run_gpu(inp: kin.Inputs, chunk_size=None, stream=None, workspace=None):
                         scale=inp.scale, initial_state=f32_device(inp.h0), output_final_state=True,
                         cu_seqlens=cu, cu_seqlens_cpu=cu_cpu,
                         chunk_size=chunk_size or wl.chunk_size, stream=stream, workspace=workspace,
-                        **gate_kwargs(wl))
+                        **gate_kwargs(wl), **opts)
     torch.cuda.synchronize()
     status = kda.kda_get_device_status(0)
     assert status == 0, f"device status {status:#x}"
     return o.float().cpu().double().numpy(), fs.cpu().double().numpy()
 
 
-def run_oracle(inp: kin.Inputs, heads=None, nthreads=0):
-    """The oracle on ``inp`` (optionally only the value heads ``heads``)."""
+def run_oracle(inp: kin.Inputs, heads=None, nthreads=0, **opts):
+    """The oracle on ``inp`` (optionally only the value heads ``heads``); ``opts`` as run_gpu."""
     wl = inp.wl
     q, k, v, g, b = inp.q, inp.k, inp.v, inp.g, inp.beta
     A_log, dt, h0 = inp.A_log, inp.dt_bias, inp.h0
@@ -72,7 +73,7 @@ def run_oracle(inp: kin.Inputs, heads=None, nthreads=0):
     lb = wl.lower_bound if wl.gate == kin.GATE_SAFE else None
     return oracle.fwd(q, k, v, g, b, A_log=A_log, dt_bias=dt, gate_mode=wl.gate, lower_bound=lb,
                       scale=inp.scale, qk_l2norm=True, beta_sigmoid=True, initial_state=h0,
-                      cu_seqlens=inp.cu_seqlens, nthreads=nthreads)
+                      cu_seqlens=inp.cu_seqlens, nthreads=nthreads, **opts)
 
 
 def errors(got: np.ndarray, ref: np.ndarray):

@@ -34,7 +34,7 @@ def test_header_declares_what_binding_expects():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert kb.kda_abi_version() == 1
+    assert kb.kda_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -44,10 +44,10 @@ def test_status_strings(lib):
 
 
 def test_struct_layout_matches_header():
-    # int32 x 9, float x 2, int32 x 3 -> 56 bytes, then 13 pointers and a size_t
-    assert kb.kda_fwd_params.q.offset == 56
-    assert kb.kda_fwd_params.workspace_bytes.offset == 56 + 13 * 8
-    assert ctypes.sizeof(kb.kda_fwd_params) == 56 + 14 * 8
+    # int32 x 9, float x 2, int32 x 5 -> 64 bytes, then 13 pointers and a size_t
+    assert kb.kda_fwd_params.q.offset == 64
+    assert kb.kda_fwd_params.workspace_bytes.offset == 64 + 13 * 8
+    assert ctypes.sizeof(kb.kda_fwd_params) == 64 + 14 * 8
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced by the checks
@@ -101,6 +101,9 @@ def test_valid_params_pass_and_have_workspace(lib):
     (dict(qk_l2norm=2), kb.KDA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), kb.KDA_ERR_INVALID_ARG),
     (dict(B=0), kb.KDA_ERR_SHAPE),
+    (dict(allow_neg_eigval=1, beta_sigmoid=0), kb.KDA_ERR_INVALID_ARG),   # needs beta sigmoid
+    (dict(allow_neg_eigval=2), kb.KDA_ERR_INVALID_ARG),
+    (dict(state_v_first=3), kb.KDA_ERR_INVALID_ARG),
 ])
 def test_rule_rejections(lib, over, status):
     p = valid_params(**over)

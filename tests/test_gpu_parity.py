@@ -249,3 +249,31 @@ def test_tc_pipelined_varlen_with_empty_sequences():
     inp = kin.make_inputs(wl)
     inp.cu_seqlens[:] = np.array([0, 8000, 8000, 17000, 17037, 17037], dtype=np.int64)
     check_pipelined(inp)
+
+
+
+# ---- allow_neg_eigval and the transposed ([V, K]) state layout ---------------------------------
+
+@pytest.mark.parametrize("dtype,K", [("bf16", 128), ("f32", 64)])
+def test_allow_neg_eigval(dtype, K):
+    """beta = 2 sigmoid(logit) in [0, 2) on both paths (bf16 tensor-core, fp32 CUDA-core)."""
+    inp = kin.make_inputs(small(T=150, K=K, V=K, dtype=dtype, seed=500 + K))
+    o, fs = run_gpu(inp, allow_neg_eigval=True)
+    ro, rfs = run_oracle(inp, allow_neg_eigval=True)
+    assert_close(o, ro, dtype, "o")
+    assert_close(fs, rfs, dtype, "final_state")
+
+
+@pytest.mark.parametrize("dtype,K,T", [("bf16", 128, 150), ("f32", 64, 150),
+                                       ("bf16", 128, 64 * 256 + 37)])
+def test_transposed_state_layout(dtype, K, T):
+    """Initial and final states as [N, HV, V, K]; the last case runs the pipelined schedule,
+    whose carried state between segments stays internal."""
+    wl = small(T=T, K=K, V=K, dtype=dtype, seed=510 + K + T)
+    inp = kin.make_inputs(wl)
+    inp.h0 = np.ascontiguousarray(np.swapaxes(inp.h0, -1, -2))
+    o, fs = run_gpu(inp, transpose_state_layout=True)
+    ro, rfs = run_oracle(inp, transpose_state_layout=True)
+    assert fs.shape == (1, wl.HV, wl.V, wl.K)
+    assert_close(o, ro, dtype, "o")
+    assert_close(fs, rfs, dtype, "final_state")

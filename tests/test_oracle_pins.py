@@ -321,3 +321,52 @@ def test_empty_sequence_keeps_state():
     o, fs = oracle.fwd(**d, **kw)
     assert o.shape == (1, 0, 1, 3)
     assert np.array_equal(fs, kw["initial_state"])
+
+
+# ---- allow_neg_eigval and the transposed state layout ------------------------------------
+
+def test_neg_eigval_beta_near_two_is_a_householder_reflection():
+    """With beta = 2 sigmoid(b) -> 2 (b = 40), no decay (pre-gated g = 0), v = 0 and a unit
+    key, each token applies I - 2 k k^T to the state: a reflection.  One token negates the
+    state's component along k; the same token twice restores the initial state."""
+    rng = np.random.default_rng(17)
+    K = V = 8
+    kvec = rng.standard_normal(K)
+    kvec /= np.sqrt(np.sum(kvec ** 2))                # a unit key (no in-kernel norm below)
+    k = np.tile(kvec, (1, 2, 1, 1))                   # [1, 2, 1, K]: the same key twice
+    q = rng.standard_normal((1, 2, 1, K))
+    v = np.zeros((1, 2, 1, V))
+    g = np.zeros((1, 2, 1, K))
+    beta = np.full((1, 2, 1), 40.0)
+    h0 = rng.standard_normal((1, 1, K, V))
+    kw = dict(gate_mode=GATE_PREGATED, qk_l2norm=False, beta_sigmoid=True, allow_neg_eigval=True,
+              initial_state=h0)
+    _, fs2 = oracle.fwd(q, k, v, g, beta, **kw)
+    assert np.allclose(fs2, h0, rtol=0, atol=1e-12)
+    _, fs1 = oracle.fwd(q[:, :1], k[:, :1], v[:, :1], g[:, :1], beta[:, :1], **kw)
+    assert np.allclose(kvec @ fs1[0, 0], -(kvec @ h0[0, 0]), rtol=0, atol=1e-12)
+    # the part of the state orthogonal to k is untouched
+    perp = h0[0, 0] - np.outer(kvec, kvec @ h0[0, 0])
+    assert np.allclose(fs1[0, 0] - np.outer(kvec, kvec @ fs1[0, 0]), perp, rtol=0, atol=1e-12)
+
+
+def test_neg_eigval_needs_beta_sigmoid():
+    with pytest.raises(ValueError):
+        oracle.fwd(np.zeros((1, 1, 1, 4)), np.zeros((1, 1, 1, 4)), np.zeros((1, 1, 1, 4)),
+                   np.zeros((1, 1, 1, 4)), np.zeros((1, 1, 1)), gate_mode=GATE_PREGATED,
+                   beta_sigmoid=False, allow_neg_eigval=True)
+
+
+def test_transposed_state_layout_is_the_transpose():
+    """state_v_first stores the K x V state as V x K, both ways."""
+    rng = np.random.default_rng(23)
+    B, T, H, K, V = 1, 9, 1, 6, 5
+    d = dict(q=rng.standard_normal((B, T, H, K)), k=rng.standard_normal((B, T, H, K)),
+             v=rng.standard_normal((B, T, H, V)), g=-np.abs(rng.standard_normal((B, T, H, K))),
+             beta=rng.standard_normal((B, T, H)))
+    h0 = rng.standard_normal((1, 1, K, V))
+    o, fs = oracle.fwd(**d, gate_mode=GATE_PREGATED, initial_state=h0)
+    oT, fsT = oracle.fwd(**d, gate_mode=GATE_PREGATED, initial_state=np.swapaxes(h0, -1, -2),
+                         transpose_state_layout=True)
+    assert fsT.shape == (1, 1, V, K)
+    assert np.array_equal(oT, o) and np.array_equal(fsT, np.swapaxes(fs, -1, -2))
