@@ -280,6 +280,51 @@ def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
     return tokens_per_rank * world / (ms_per_step / 1e3)
 
 
+def measure_decode(kb, kda, dev, steps, warmup, peak_gbs):
+    """One decode step through kda_fused_recurrent_fwd (256 sequences x 1 token, 32 heads,
+    K = V = 128, bf16): tokens/s and the HBM roofline of its state traffic (read h0 and
+    write final_state, fp32, plus the token's q, k, v, g, beta, o)."""
+    import torch
+    inp = kin.make_inputs(kin.WORKLOADS["decode_bf16"])
+    wl = inp.wl
+
+    def up(x, dtype):
+        if dtype == "bf16":
+            return torch.from_numpy(kin.to_bf16_bits(x).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
+
+    q, k, v, g, b = (up(x, "bf16") for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    A_log, dt_bias, h0 = (up(x, "f32") for x in (inp.A_log, inp.dt_bias, inp.h0))
+    o = torch.empty_like(v)
+    fs = torch.empty_like(h0)
+    p = kda.make_params(q, k, v, g, b, A_log=A_log, dt_bias=dt_bias, lower_bound=wl.lower_bound,
+                        scale=inp.scale, initial_state=h0, final_state=fs, o=o)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    for _ in range(max(warmup, 3)):
+        kb.raise_for(kb.kda_fused_recurrent_fwd(p, sh))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        kb.raise_for(kb.kda_fused_recurrent_fwd(p, sh))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if kb.kda_get_device_status(sh) != 0:
+        raise RuntimeError("device status flagged in the decode measurement")
+    ms = e0.elapsed_time(e1) / steps
+    ntok = wl.B * wl.T
+    state = 2 * wl.B * wl.HV * wl.K * wl.V * 4
+    per_tok = 2 * (2 * wl.H * wl.K + wl.HV * (2 * wl.V + wl.K + 1))   # q, k, v, g, beta, o
+    nbytes = state + ntok * per_tok + 4 * wl.HV * (1 + wl.K)
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {"workload": "decode_bf16 (B=256 sequences x 1 token, H=HV=32, K=V=128)",
+            "entry": "kda_fused_recurrent_fwd", "value": ntok / (ms / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
+                         "frac": achieved / peak_gbs, "bytes_per_launch": float(nbytes)}}
+
+
 def config_of(inp: kin.Inputs, args):
     wl = inp.wl
     return {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "HV": wl.HV, "K": wl.K,
@@ -494,6 +539,8 @@ def main():
             "gpu_launches": int(n_launch * args.steps), "clocks": clocks,
             "kernel_source_sha": kernel_source_hash()}
 
+    if rank == 0 and world == 1:
+        line["decode"] = measure_decode(kb, kda, dev, args.steps, args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

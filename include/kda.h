@@ -100,6 +100,11 @@ typedef struct kda_fwd_params {
   const int64_t* cu_seqlens_host; /* host copy of cu_seqlens, required with it */
   void* o;                   /* output */
   float* final_state;        /* output, optional (NULL = not written) */
+  float* h_out;              /* output, optional: the state before every chunk
+                                ("return_intermediate_states", reading notes section 2.2),
+                                [nct, HV, K, V] fp32 ([nct, HV, V, K] with state_v_first), chunk c
+                                of sequence n at index (chunks of sequences 0..n-1) + c;
+                                nct from kda_fwd_num_chunks */
   void* workspace;
   size_t workspace_bytes;
 } kda_fwd_params;
@@ -133,6 +138,21 @@ kda_status kda_fwd(const kda_fwd_params* p, void* stream);
 /* Number of kernel launches one kda_fwd call makes for these parameters (0 if
    they are invalid).  Host only; makes no CUDA call. */
 int32_t kda_fwd_num_launches(const kda_fwd_params* p);
+
+/* The same forward pass as a token recurrence (decode and short prefill;
+   "Reading Notes: Implementation Notes for KDA in FLA", section 1,
+   fused_recurrent_kda): per token alpha = exp(g'), S <- Diag(alpha) S,
+   S <- S + beta k (v - S^T k)^T, o = scale S^T q, the state read from h0 (or 0)
+   and written to final_state.  Same parameters, checks, layouts and outputs as
+   kda_fwd, except: chunk_size and the workspace are not used (no workspace is
+   needed), and h_out must be NULL.  fp32 arithmetic on every dtype.  One CTA per
+   (sequence, value head, 32 columns of V), tokens in order.  Asynchronous on
+   `stream`. */
+kda_status kda_fused_recurrent_fwd(const kda_fwd_params* p, void* stream);
+
+/* Number of chunks over all sequences, the first dimension of h_out (0 if the
+   parameters are invalid).  Host only; makes no CUDA call. */
+int64_t kda_fwd_num_chunks(const kda_fwd_params* p);
 
 /* Number of stages of the forward pass for these parameters (0 if they are
    invalid): chunk table (varlen only), intra-chunk kernel, recurrence kernel.

@@ -45,7 +45,7 @@ def make_params(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None,
                 cu_seqlens_cpu=None, chunk_size: int = 64, use_gate_in_kernel: bool = True,
                 safe_gate: Optional[bool] = None, use_qk_l2norm_in_kernel: bool = True,
                 use_beta_sigmoid_in_kernel: bool = True, allow_neg_eigval: bool = False,
-                transpose_state_layout: bool = False, workspace=None) -> kda_fwd_params:
+                transpose_state_layout: bool = False, h_out=None, workspace=None) -> kda_fwd_params:
     """Fill a ``kda_fwd_params`` from tensors (no checks beyond shapes; the C layer checks).
 
     ``allow_neg_eigval``: beta = 2 sigmoid(logit) in [0, 2).  ``transpose_state_layout``
@@ -94,7 +94,7 @@ def make_params(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None,
     p.A_log, p.dt_bias, p.h0 = _ptr(A_log), _ptr(dt_bias), _ptr(initial_state)
     p.cu_seqlens = _ptr(cu_seqlens)
     p.cu_seqlens_host = _ptr(cu_seqlens_cpu)
-    p.o, p.final_state = _ptr(o), _ptr(final_state)
+    p.o, p.final_state, p.h_out = _ptr(o), _ptr(final_state), _ptr(h_out)
     if workspace is not None:
         p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     return p
@@ -109,12 +109,15 @@ def kda_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None, sca
             cu_seqlens_cpu=None, chunk_size: int = 64, use_gate_in_kernel: bool = True,
             safe_gate: Optional[bool] = None, use_qk_l2norm_in_kernel: bool = True,
             use_beta_sigmoid_in_kernel: bool = True, allow_neg_eigval: bool = False,
-            transpose_state_layout: bool = False, workspace=None, o=None, final_state=None,
-            stream=None) -> Tuple["torch.Tensor", Optional["torch.Tensor"]]:
+            transpose_state_layout: bool = False, return_intermediate_states: bool = False,
+            workspace=None, o=None, final_state=None, stream=None):
     """Chunk-parallel KDA forward on the current CUDA device.  Returns (o, final_state).
 
     o has v's dtype and shape [B,T,HV,V]; final_state is fp32 [N,HV,K,V] ([N,HV,V,K] with
-    ``transpose_state_layout``; None if ``output_final_state`` is False).  With ``cu_seqlens`` (int64 [N+1], B == 1),
+    ``transpose_state_layout``; None if ``output_final_state`` is False).  With
+    ``return_intermediate_states`` a third result: the state before every chunk, fp32
+    [nct, HV, K, V] (transposed like final_state), chunks of sequence n after those of
+    sequences 0..n-1.  With ``cu_seqlens`` (int64 [N+1], B == 1),
     rows of o outside every sequence are zero.  Asynchronous on ``stream``
     (default: the current PyTorch stream).
     """
@@ -143,6 +146,12 @@ def kda_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None, sca
                     allow_neg_eigval=allow_neg_eigval,
                     transpose_state_layout=transpose_state_layout)
     _binding.raise_for(_binding.kda_fwd_check(p))
+    h_out = None
+    if return_intermediate_states:
+        nct = _binding.kda_fwd_num_chunks(p)
+        hs_shape = (nct, HV, V, K) if transpose_state_layout else (nct, HV, K, V)
+        h_out = torch.empty(hs_shape, dtype=torch.float32, device=v.device)
+        p.h_out = _ptr(h_out)
     need = _binding.kda_fwd_workspace_size(p)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=v.device)
@@ -151,4 +160,46 @@ def kda_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None, sca
         stream = torch.cuda.current_stream(v.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     _binding.raise_for(_binding.kda_fwd(p, handle))
+    if return_intermediate_states:
+        return o, final_state, h_out
+    return o, final_state
+
+
+def kda_fused_recurrent_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None,
+                            scale=None, initial_state=None, output_final_state: bool = True,
+                            cu_seqlens=None, cu_seqlens_cpu=None, use_gate_in_kernel: bool = True,
+                            safe_gate: Optional[bool] = None, use_qk_l2norm_in_kernel: bool = True,
+                            use_beta_sigmoid_in_kernel: bool = True, allow_neg_eigval: bool = False,
+                            transpose_state_layout: bool = False, o=None, final_state=None,
+                            stream=None):
+    """The same forward pass as a token recurrence (decode / short prefill).  Returns
+    (o, final_state) exactly as ``kda_fwd``; no workspace, no chunking."""
+    import torch
+    if not q.is_cuda:
+        raise ValueError("kda_fused_recurrent_fwd runs on CUDA tensors only")
+    if cu_seqlens is not None and cu_seqlens_cpu is None:
+        cu_seqlens_cpu = cu_seqlens.to("cpu")
+    if cu_seqlens_cpu is not None:
+        cu_seqlens_cpu = cu_seqlens_cpu.to(torch.int64).contiguous()
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        padded = cu_seqlens is not None and int(cu_seqlens_cpu[-1]) < B * T
+        o = (torch.zeros if padded else torch.empty)((B, T, HV, V), dtype=v.dtype, device=v.device)
+    if final_state is None and output_final_state:
+        st_shape = (N, HV, V, K) if transpose_state_layout else (N, HV, K, V)
+        final_state = torch.empty(st_shape, dtype=torch.float32, device=v.device)
+    p = make_params(q, k, v, g, beta, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound,
+                    scale=scale, initial_state=initial_state, final_state=final_state, o=o,
+                    cu_seqlens=cu_seqlens, cu_seqlens_cpu=cu_seqlens_cpu,
+                    use_gate_in_kernel=use_gate_in_kernel, safe_gate=safe_gate,
+                    use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel,
+                    use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
+                    allow_neg_eigval=allow_neg_eigval,
+                    transpose_state_layout=transpose_state_layout)
+    if stream is None:
+        stream = torch.cuda.current_stream(v.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _binding.raise_for(_binding.kda_fused_recurrent_fwd(p, handle))
     return o, final_state

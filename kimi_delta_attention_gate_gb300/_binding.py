@@ -33,6 +33,7 @@ KDA_DEV_TIMEOUT = 0x2
 
 # Every symbol the header declares.
 EXPORTED = ("kda_fwd_workspace_size", "kda_fwd_check", "kda_fwd", "kda_fwd_num_launches",
+            "kda_fwd_num_chunks", "kda_fused_recurrent_fwd",
             "kda_fwd_num_stages",
             "kda_fwd_stage_name", "kda_fwd_stage", "kda_get_device_status", "kda_status_string",
             "kda_last_error", "kda_abi_version", "kda_fwd_noalloc")
@@ -56,7 +57,7 @@ class kda_fwd_params(ctypes.Structure):
         ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("A_log", ctypes.c_void_p),
         ("dt_bias", ctypes.c_void_p), ("h0", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
         ("cu_seqlens_host", ctypes.c_void_p), ("o", ctypes.c_void_p),
-        ("final_state", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+        ("final_state", ctypes.c_void_p), ("h_out", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
     ]
 
@@ -92,6 +93,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kda_fwd_noalloc.argtypes = [P, ctypes.c_void_p]
             lib.kda_fwd_num_launches.restype = ctypes.c_int32
             lib.kda_fwd_num_launches.argtypes = [P]
+            lib.kda_fwd_num_chunks.restype = ctypes.c_int64
+            lib.kda_fwd_num_chunks.argtypes = [P]
+            lib.kda_fused_recurrent_fwd.restype = ctypes.c_int
+            lib.kda_fused_recurrent_fwd.argtypes = [P, ctypes.c_void_p]
             lib.kda_fwd_num_stages.restype = ctypes.c_int32
             lib.kda_fwd_num_stages.argtypes = [P]
             lib.kda_fwd_stage_name.restype = ctypes.c_char_p
@@ -124,6 +129,14 @@ def kda_fwd(p: kda_fwd_params, stream: int = 0) -> int:
 
 def kda_fwd_noalloc(p: kda_fwd_params, stream: int = 0) -> int:
     return int(load().kda_fwd_noalloc(ctypes.byref(p), ctypes.c_void_p(stream)))
+
+
+def kda_fused_recurrent_fwd(p: kda_fwd_params, stream: int) -> int:
+    return int(load().kda_fused_recurrent_fwd(ctypes.byref(p), ctypes.c_void_p(stream)))
+
+
+def kda_fwd_num_chunks(p: kda_fwd_params) -> int:
+    return int(load().kda_fwd_num_chunks(ctypes.byref(p)))
 
 
 def kda_fwd_num_launches(p: kda_fwd_params) -> int:

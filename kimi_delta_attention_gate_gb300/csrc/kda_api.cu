@@ -130,6 +130,7 @@ kda_status check_args(const kda_fwd_params* p) {
       {p->beta, "beta", any_tokens},  {p->o, "o", any_tokens},
       {p->A_log, "A_log", false},     {p->dt_bias, "dt_bias", false},
       {p->h0, "h0", false},           {p->final_state, "final_state", false},
+      {p->h_out, "h_out", false},
   };
   for (auto& e : ptrs) {
     if (e.required && e.ptr == nullptr) return fail(KDA_ERR_INVALID_ARG, "%s is NULL", e.name);
@@ -302,7 +303,7 @@ kda_status prepare(const kda_fwd_params* p, FwdArgs& a) {
   a.lower_bound = p->lower_bound; a.scale = p->scale;
   a.q = p->q; a.k = p->k; a.v = p->v; a.g = p->g; a.beta = p->beta;
   a.A_log = p->A_log; a.dt_bias = p->dt_bias; a.h0 = p->h0; a.cu_seqlens = p->cu_seqlens;
-  a.o = p->o; a.final_state = p->final_state;
+  a.o = p->o; a.final_state = p->final_state; a.h_out = p->h_out;
   a.ws = static_cast<char*>(p->workspace);
   a.status = status;
   a.c_begin = 0;
@@ -377,6 +378,37 @@ int32_t kda_fwd_num_launches(const kda_fwd_params* p) {
   if (pl.nseg > 1) return (pl.varlen ? 1 : 0) + 2 * pl.nseg;
   Stage st[kMaxStages];
   return stages_for(pl, st);
+}
+
+kda_status kda_fused_recurrent_fwd(const kda_fwd_params* p, void* stream) {
+  if (p == nullptr) return fail(KDA_ERR_INVALID_ARG, "params is NULL");
+  kda_fwd_params c = *p;
+  c.chunk_size = 64;  // not used by the token recurrence; every other rule applies
+  kda_status s = check_args(&c);
+  if (s != KDA_OK) return s;
+  if (p->h_out != nullptr)
+    return fail(KDA_ERR_INVALID_ARG, "h_out (per-chunk states) is an output of kda_fwd only");
+  unsigned int* status = device_status_ptr();
+  if (status == nullptr) return fail(KDA_ERR_CUDA, "no CUDA device / status word unavailable");
+  FwdArgs a{};
+  a.plan = make_plan(&c);
+  a.dtype = p->in_dtype; a.gate_mode = p->gate_mode;
+  a.qk_l2norm = p->qk_l2norm; a.beta_sigmoid = p->beta_sigmoid;
+  a.allow_neg_eigval = p->allow_neg_eigval; a.state_v_first = p->state_v_first;
+  a.lower_bound = p->lower_bound; a.scale = p->scale;
+  a.q = p->q; a.k = p->k; a.v = p->v; a.g = p->g; a.beta = p->beta;
+  a.A_log = p->A_log; a.dt_bias = p->dt_bias; a.h0 = p->h0; a.cu_seqlens = p->cu_seqlens;
+  a.o = p->o; a.final_state = p->final_state;
+  a.status = status;
+  cudaError_t e = launch_recurrent(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "recurrent launch failed: %s", cudaGetErrorString(e));
+  t_last_error.clear();
+  return KDA_OK;
+}
+
+int64_t kda_fwd_num_chunks(const kda_fwd_params* p) {
+  if (check_args(p) != KDA_OK) return 0;
+  return make_plan(p).nct;
 }
 
 int32_t kda_fwd_num_stages(const kda_fwd_params* p) {

@@ -45,6 +45,7 @@ struct FwdArgs {
   const int64_t* cu_seqlens;
   void* o;
   float* final_state;
+  float* h_out;             // per-chunk states (optional)
   char* ws;                 // workspace base
   unsigned int* status;     // device status word
   int64_t c_begin, c_end;   // global chunk range of this launch (tensor-core kernels)
@@ -145,6 +146,10 @@ cudaError_t launch_chunk_table(const FwdArgs& a, cudaStream_t s);
 size_t simt_inter_block_bytes(int C, int K, int V);
 cudaError_t launch_simt_intra(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_simt_recur(const FwdArgs& a, cudaStream_t s);
+
+// token-recurrent forward (decode / short prefill)
+size_t recurrent_smem_bytes(int K);
+cudaError_t launch_recurrent(const FwdArgs& a, cudaStream_t s);
 
 // bf16 tensor-core path (K = V = 128, chunk 64)
 bool tc_eligible(const Plan& p, int dtype);

@@ -1,0 +1,176 @@
+// Token-recurrent KDA forward: the method's recurrence taken one token at a time, with the
+// state read from memory at the start and written back at the end.  This is the decode /
+// short-prefill counterpart of the chunk path ("Reading Notes: Implementation Notes for
+// KDA in FLA", section 1: fused_recurrent_kda next to chunk_kda), for one or a few tokens
+// per sequence where the chunk form has nothing to amortise.
+//
+// Per token t of a sequence, for value head hv (q/k head hv / G):
+//   alpha = exp(g'_t)                          g' the activated gate (section 2)
+//   S <- Diag(alpha) S ;  p = S^T k ;  S <- S + beta k (v - p)^T ;  o_t = scale S^T q
+// with q, k L2-normalised over K and beta = sigmoid(logit) (x2 with allow_neg_eigval) when
+// the flags ask for it.  One CTA per (sequence, value head, 32 columns of V); 8 warps split
+// the K rows of the 32-column state tile, which stays in shared memory in fp32.
+
+#include "kda_internal.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTile = 32;  // V columns per CTA
+
+__device__ __forceinline__ float warp_sum_all(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads) recurrent_kernel(const FwdArgs a) {
+  extern __shared__ float smem[];
+  const Plan& p = a.plan;
+  const int K = p.K, V = p.V, HV = p.HV, H = p.H;
+  const int nvt = (V + kTile - 1) / kTile;
+  float* sS = smem;                       // [K][kTile] state tile
+  float* sQ = sS + (size_t)K * kTile;     // [K] normalised, scaled query
+  float* sK = sQ + K;                     // [K] normalised key
+  float* sA = sK + K;                     // [K] decay alpha
+  float* sRed = sA + K;                   // [kWarps][kTile] cross-warp partial sums
+  float* sMisc = sRed + kWarps * kTile;   // [2 * kWarps] norm partials, [2] beta / flags
+
+  const int vt = (int)(blockIdx.x % nvt);
+  const int hv = (int)((blockIdx.x / nvt) % HV);
+  const int n = (int)(blockIdx.x / ((unsigned)nvt * HV));
+  const int h = hv / p.G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int col = vt * kTile + lane;
+  const bool cv = col < V;
+  int64_t bos, eos;  // token range of sequence n
+  if (p.varlen) {
+    bos = a.cu_seqlens[n];
+    eos = a.cu_seqlens[n + 1];
+  } else {
+    bos = (int64_t)n * p.T;
+    eos = bos + p.T;
+  }
+  if (bos < 0 || eos < bos || eos > p.ntok) {
+    if (tid == 0) flag_status(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const Tin* gq = static_cast<const Tin*>(a.q);
+  const Tin* gk = static_cast<const Tin*>(a.k);
+  const Tin* gv = static_cast<const Tin*>(a.v);
+  const Tin* gg = static_cast<const Tin*>(a.g);
+  const Tin* gb = static_cast<const Tin*>(a.beta);
+  Tin* go = static_cast<Tin*>(a.o);
+  const size_t state_base = ((size_t)n * HV + hv) * (size_t)K * V;
+  auto sidx = [&](int kk) {
+    return state_base + (a.state_v_first ? (size_t)col * K + kk : (size_t)kk * V + col);
+  };
+  for (int kk = warp; kk < K; kk += kWarps)
+    sS[kk * kTile + lane] = (a.h0 != nullptr && cv) ? a.h0[sidx(kk)] : 0.f;
+  const float a_exp = (a.gate_mode != KDA_GATE_PREGATED && a.A_log != nullptr) ? expf(a.A_log[hv]) : 1.f;
+
+  for (int64_t t = bos; t < eos; ++t) {
+    // per-token vectors over K (thread i < K holds element i)
+    float qi = 0.f, ki = 0.f;
+    if (tid < K) {
+      qi = to_f32(gq[(t * H + h) * (int64_t)K + tid]);
+      ki = to_f32(gk[(t * H + h) * (int64_t)K + tid]);
+      const float gi = to_f32(gg[(t * HV + hv) * (int64_t)K + tid]);
+      const float dt = (a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED)
+                           ? a.dt_bias[(size_t)hv * K + tid] : 0.f;
+      sA[tid] = expf(gate_exact(a.gate_mode, gi, a_exp, dt, a.lower_bound));
+    }
+    if (a.qk_l2norm) {
+      const float sq = warp_sum_all(qi * qi), sk = warp_sum_all(ki * ki);
+      if (lane == 0) {
+        sMisc[warp] = sq;
+        sMisc[kWarps + warp] = sk;
+      }
+    }
+    if (tid == 0) {
+      float b = to_f32(gb[t * HV + hv]);
+      if (a.beta_sigmoid) b = (a.allow_neg_eigval ? 2.f : 1.f) * sigmoid_exact(b);
+      sMisc[2 * kWarps] = b;
+    }
+    __syncthreads();
+    if (tid < K) {
+      float qn = a.scale, kn = 1.f;
+      if (a.qk_l2norm) {
+        float sq = 0.f, sk = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+          sq += sMisc[w];
+          sk += sMisc[kWarps + w];
+        }
+        qn *= rsqrtf(sq + 1e-6f);
+        kn = rsqrtf(sk + 1e-6f);
+      }
+      sQ[tid] = qi * qn;
+      sK[tid] = ki * kn;
+    }
+    __syncthreads();
+    // S <- Diag(alpha) S and this warp's part of p = S^T k
+    float pacc = 0.f;
+    for (int kk = warp; kk < K; kk += kWarps) {
+      const float s = sS[kk * kTile + lane] * sA[kk];
+      sS[kk * kTile + lane] = s;
+      pacc = fmaf(s, sK[kk], pacc);
+    }
+    sRed[warp * kTile + lane] = pacc;
+    __syncthreads();
+    float pv = 0.f;
+    for (int w = 0; w < kWarps; ++w) pv += sRed[w * kTile + lane];
+    const float vv = cv ? to_f32(gv[(t * HV + hv) * (int64_t)V + col]) : 0.f;
+    const float u = sMisc[2 * kWarps] * (vv - pv);
+    __syncthreads();  // sRed is rewritten below
+    // S <- S + k u^T and this warp's part of o = scale S^T q (scale folded into sQ)
+    float oacc = 0.f;
+    for (int kk = warp; kk < K; kk += kWarps) {
+      const float s = fmaf(sK[kk], u, sS[kk * kTile + lane]);
+      sS[kk * kTile + lane] = s;
+      oacc = fmaf(s, sQ[kk], oacc);
+    }
+    sRed[warp * kTile + lane] = oacc;
+    __syncthreads();
+    if (warp == 0 && cv) {
+      float o = 0.f;
+      for (int w = 0; w < kWarps; ++w) o += sRed[w * kTile + lane];
+      go[(t * HV + hv) * (int64_t)V + col] = from_f32<Tin>(o);
+    }
+    __syncthreads();  // the next token rewrites sQ, sK, sA, sRed
+  }
+  if (a.final_state != nullptr && cv)
+    for (int kk = warp; kk < K; kk += kWarps) a.final_state[sidx(kk)] = sS[kk * kTile + lane];
+}
+
+}  // namespace
+
+size_t recurrent_smem_bytes(int K) {
+  return sizeof(float) * ((size_t)K * kTile + 3 * (size_t)K + kWarps * kTile + 2 * kWarps + 2);
+}
+
+cudaError_t launch_recurrent(const FwdArgs& a, cudaStream_t s) {
+  const Plan& p = a.plan;
+  const int nvt = (p.V + kTile - 1) / kTile;
+  const size_t blocks = (size_t)p.N * p.HV * nvt;
+  if (blocks == 0) return cudaSuccess;
+  const size_t smem = recurrent_smem_bytes(p.K);
+  cudaError_t e;
+  if (a.dtype == KDA_BF16) {
+    e = cudaFuncSetAttribute(recurrent_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    recurrent_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, smem, s>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(recurrent_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    recurrent_kernel<float><<<(unsigned)blocks, kThreads, smem, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kda

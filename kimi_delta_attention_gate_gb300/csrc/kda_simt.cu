@@ -233,6 +233,11 @@ __global__ void __launch_bounds__(kRecThreads) simt_recur_kernel(const FwdArgs a
     const int64_t t0 = bos + ci * C;
     const int L = (int)((eos - t0) < C ? (eos - t0) : C);
     InterView in(a, cfirst + ci, hv);
+    if (a.h_out != nullptr && cv) {  // the state before this chunk
+      float* hc = a.h_out + ((size_t)(cfirst + ci) * HV + hv) * (size_t)K * V;
+      for (int kk = warp; kk < K; kk += kRecWarps)
+        hc[a.state_v_first ? (size_t)col * K + kk : (size_t)kk * V + col] = sS[kk * kBV + lane];
+    }
     float preg[64 / kRecWarps];
     // Step 4, first half and step 5, first half: both read S_{t-1}.
 #pragma unroll

@@ -752,6 +752,7 @@ constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kRecThreads = kEpiThreads + 32;  // + control warp
 
+template <bool SAVE_STATES>  // SAVE_STATES: write the state before every chunk to h_out
 __global__ void __launch_bounds__(kRecThreads, 1)
     tc_recur_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap vmap,
                     const __grid_constant__ CUtensorMap omap) {
@@ -895,15 +896,23 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     float* sout = seq_end ? a.final_state : carry;
     // state element (channel 32 part + j, column v): [K][V] in the carry buffer, [K][V] or
     // [V][K] (state_v_first) in h0 / final_state
-    auto sidx = [&](int j, bool external) -> size_t {
-      return sbase + ((external && a.state_v_first) ? (size_t)v * TC_K + 32 * part + j
-                                                      : (size_t)(32 * part + j) * TC_V + v);
+    auto sloc = [&](int j, bool external) -> size_t {  // offset within one K x V state
+      return (external && a.state_v_first) ? (size_t)v * TC_K + 32 * part + j
+                                           : (size_t)(32 * part + j) * TC_V + v;
     };
+    auto sidx = [&](int j, bool external) -> size_t { return sbase + sloc(j, external); };
     auto arrive = [&](uint64_t* bar) {  // one arrival per warp, after the warp's writes
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
     };
     auto slot_of = [&](int64_t ci) { return sm + R_RING + (int)(ci & 1) * SLOT; };
+    // the state before chunk ci, when the caller asked for the per-chunk states
+    auto save_chunk_state = [&](const float (&S)[32], int64_t ci) {
+      if (!SAVE_STATES) return;
+      float* hc = a.h_out + ((size_t)(cfirst + ci) * HV + hv) * (size_t)TC_K * TC_V;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) hc[sloc(j, true)] = S[j];
+    };
     // bf16 copy of 32 state columns into the A operand of G1+O1; releases G1+O1
     auto publish_state = [&](const float (&S)[32]) {
       uint32_t pk[16];
@@ -977,6 +986,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
         for (int j = 0; j < 32; ++j) sout[sidx(j, seq_end)] = S[j];
       }
       tmem_st16_zero(lane_base + TM_O + 16 * part);
+      if (nch > 0) save_chunk_state(S, 0);
       publish_state(S);
       if (nch > 0 && !rescale_state(S, 0)) ok = false;
     }
@@ -1016,6 +1026,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
           S[16 + j] = __uint_as_float(r1[j]);
         }
         if (ci + 1 < nch) {
+          save_chunk_state(S, ci + 1);
           publish_state(S);
           w = rescale_state(S, ci + 1) && w;
         } else {
@@ -1125,11 +1136,11 @@ cudaError_t launch_tc_recur(const FwdArgs& a, cudaStream_t s) {
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc_recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)R_SMEM);
-  if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((size_t)p.HV * p.N));
-  tc_recur_kernel<<<grid, kRecThreads, R_SMEM, s>>>(a, vmap, omap);
+  auto kern = a.h_out != nullptr ? tc_recur_kernel<true> : tc_recur_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)R_SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kRecThreads, R_SMEM, s>>>(a, vmap, omap);
   return cudaGetLastError();
 }
 

@@ -71,6 +71,10 @@ WORKLOADS = {
                             varlen_n=8, varlen_max_len=8191, seed=1004),
     "long_bf16": Workload("long_bf16", B=1, T=65536, H=32, HV=32, K=128, V=128, chunk_size=64,
                           dtype="bf16", gate=GATE_SAFE, lower_bound=-5.0, seed=1005),
+    # decode step of the token-recurrent entry point: 256 sequences of one token each
+    "decode_bf16": Workload("decode_bf16", B=256, T=1, H=32, HV=32, K=128, V=128, chunk_size=64,
+                            dtype="bf16", gate=GATE_SAFE, lower_bound=-5.0, h0_std=0.1,
+                            seed=1006),
 }
 
 

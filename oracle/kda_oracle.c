@@ -93,6 +93,9 @@ void kdao_gate(int mode, int64_t ntok, int HV, int K, const double* g, const dou
  *   o     [B*T, HV, V]  (rows that no sequence covers are set to 0)
  *   final_state [N, HV, K, V] or NULL
  *   nthreads <= 0: OpenMP default.
+ *   h_out (nullable): the state before every chunk of chunk_size tokens of every
+ *   sequence ("return_intermediate_states", reading notes section 2.2), [nct][HV][K][V]
+ *   with sequence n's chunks numbered after those of sequences 0..n-1.
  * Returns 0, or -1 on inconsistent arguments.
  */
 int kdao_fwd(int B, int T, int H, int HV, int K, int V,
@@ -101,7 +104,8 @@ int kdao_fwd(int B, int T, int H, int HV, int K, int V,
              int gate_mode, double lower_bound, double scale,
              int qk_l2norm, int beta_sigmoid, double l2_eps,
              const double* h0, const int64_t* cu_seqlens, int N,
-             double* o, double* final_state, int nthreads) {
+             double* o, double* final_state, int nthreads, int chunk_size, double* h_out) {
+  if (h_out != NULL && chunk_size <= 0) return -1;
   if (H <= 0 || HV <= 0 || HV % H != 0 || K <= 0 || V <= 0 || B <= 0 || T < 0) return -1;
   if (cu_seqlens != NULL && B != 1) return -1;
   if (cu_seqlens == NULL && N != B) return -1;
@@ -144,8 +148,18 @@ int kdao_fwd(int B, int T, int H, int HV, int K, int V,
         memcpy(S, h0 + ((int64_t)n * HV + hv) * (int64_t)K * V, sizeof(double) * (size_t)K * V);
       else
         memset(S, 0, sizeof(double) * (size_t)K * V);
+      int64_t cfirst = 0; /* global index of sequence n's first chunk */
+      if (h_out) {
+        for (int m = 0; m < n; ++m) {
+          const int64_t len = cu_seqlens ? cu_seqlens[m + 1] - cu_seqlens[m] : (int64_t)T;
+          cfirst += (len + chunk_size - 1) / chunk_size;
+        }
+      }
 
       for (int64_t t = bos; t < eos; ++t) {
+        if (h_out && (t - bos) % chunk_size == 0)
+          memcpy(h_out + ((cfirst + (t - bos) / chunk_size) * HV + hv) * (int64_t)K * V, S,
+                 sizeof(double) * (size_t)K * V);
         const double* qt = q + (t * H + h) * (int64_t)K;
         const double* kt = k + (t * H + h) * (int64_t)K;
         const double* vt = v + (t * HV + hv) * (int64_t)V;

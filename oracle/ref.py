@@ -60,7 +60,7 @@ def _load():
             ci, cd = ctypes.c_int, ctypes.c_double
             lib.kdao_fwd.restype = ci
             lib.kdao_fwd.argtypes = [ci, ci, ci, ci, ci, ci, d, d, d, d, d, d, d, ci, cd, cd,
-                                     ci, ci, cd, d, i64, ci, d, d, ci]
+                                     ci, ci, cd, d, i64, ci, d, d, ci, ci, d]
             lib.kdao_gate.restype = None
             lib.kdao_gate.argtypes = [ci, ctypes.c_int64, ci, ci, d, d, d, cd, d]
             lib.kdao_max_threads.restype = ci
@@ -159,7 +159,8 @@ def _segments(B, T, cu_seqlens):
 
 def fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, gate_mode=GATE_SAFE, lower_bound=None,
         scale=None, qk_l2norm=True, beta_sigmoid=True, initial_state=None, cu_seqlens=None,
-        allow_neg_eigval=False, transpose_state_layout=False, l2_eps=L2_EPS, nthreads=0):
+        allow_neg_eigval=False, transpose_state_layout=False, return_intermediate_states=False,
+        chunk_size=64, l2_eps=L2_EPS, nthreads=0):
     """Token-recurrent KDA forward in fp64 (C).  Returns (o [B,T,HV,V], final_state [N,HV,K,V]).
 
     The recurrence S_t = Diag(a_t) S - b_t k_t (k_t^T Diag(a_t) S) + b_t k_t v_t^T,
@@ -169,6 +170,9 @@ def fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, gate_mode=GATE_SAFE, lowe
     ``allow_neg_eigval`` ([notes] section 2.1): beta = 2 sigmoid(logit), which needs
     ``beta_sigmoid``.  ``transpose_state_layout`` ([notes] section 2.2, state_v_first):
     initial and final states are [N,HV,V,K], the transpose of the K x V state.
+    ``return_intermediate_states`` ([notes] section 2.2): a third result, the state before
+    every chunk of ``chunk_size`` tokens, [nct,HV,K,V] (chunks of sequence n after those of
+    sequences 0..n-1; transposed like the other states).
     """
     lib = _load()
     q = _f64(q); k = _f64(k); v = _f64(v); g = _f64(g); beta = _f64(beta)
@@ -189,15 +193,24 @@ def fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, gate_mode=GATE_SAFE, lowe
     A_log = _f64(A_log); dt_bias = _f64(dt_bias); h0 = _f64(initial_state)
     o = np.zeros((B, T, HV, V), dtype=np.float64)
     fs = np.zeros((N, HV, K, V), dtype=np.float64)
+    hs = None
+    if return_intermediate_states:
+        lens = ([T] * B) if cu is None else np.diff(cu).tolist()
+        nct = int(sum((ln + chunk_size - 1) // chunk_size for ln in lens))
+        hs = np.zeros((nct, HV, K, V), dtype=np.float64)
     rc = lib.kdao_fwd(B, T, H, HV, K, V, _dptr(q), _dptr(k), _dptr(v), _dptr(g), _dptr(beta),
                       _dptr(A_log), _dptr(dt_bias), int(gate_mode), lb, float(scale),
                       int(bool(qk_l2norm)), int(bool(beta_sigmoid)), float(l2_eps), _dptr(h0),
                       None if cu is None else cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
-                      N, _dptr(o), _dptr(fs), int(nthreads))
+                      N, _dptr(o), _dptr(fs), int(nthreads), int(chunk_size), _dptr(hs))
     if rc != 0:
         raise ValueError("oracle: inconsistent arguments")
     if transpose_state_layout:
         fs = np.ascontiguousarray(np.swapaxes(fs, -1, -2))
+        if hs is not None:
+            hs = np.ascontiguousarray(np.swapaxes(hs, -1, -2))
+    if return_intermediate_states:
+        return o, fs, hs
     return o, fs
 
 

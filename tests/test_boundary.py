@@ -44,10 +44,10 @@ def test_status_strings(lib):
 
 
 def test_struct_layout_matches_header():
-    # int32 x 9, float x 2, int32 x 5 -> 64 bytes, then 13 pointers and a size_t
+    # int32 x 9, float x 2, int32 x 5 -> 64 bytes, then 14 pointers and a size_t
     assert kb.kda_fwd_params.q.offset == 64
-    assert kb.kda_fwd_params.workspace_bytes.offset == 64 + 13 * 8
-    assert ctypes.sizeof(kb.kda_fwd_params) == 64 + 14 * 8
+    assert kb.kda_fwd_params.workspace_bytes.offset == 64 + 14 * 8
+    assert ctypes.sizeof(kb.kda_fwd_params) == 64 + 15 * 8
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced by the checks
@@ -97,6 +97,7 @@ def test_valid_params_pass_and_have_workspace(lib):
     (dict(o=0), kb.KDA_ERR_INVALID_ARG),
     (dict(k=FAKE + 4), kb.KDA_ERR_INVALID_ARG),                              # misaligned
     (dict(dt_bias=FAKE + 8), kb.KDA_ERR_INVALID_ARG),
+    (dict(h_out=FAKE + 4), kb.KDA_ERR_INVALID_ARG),
     (dict(N=3), kb.KDA_ERR_SHAPE),                                           # N == B without varlen
     (dict(qk_l2norm=2), kb.KDA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), kb.KDA_ERR_INVALID_ARG),
@@ -140,6 +141,13 @@ def test_varlen_rules(lib):
     p, keep = cu_params([0, 5, 64, 100])
     p.cu_seqlens_host = None
     assert check(p) == kb.KDA_ERR_INVALID_ARG                                 # host copy needed
+
+
+def test_num_chunks(lib):
+    assert kb.kda_fwd_num_chunks(valid_params()) == 2 * 2            # B = 2, T = 100, chunk 64
+    p, keep = cu_params([0, 5, 64, 64, 200])                          # 1 + 1 + 0 + 3
+    assert kb.kda_fwd_num_chunks(p) == 5
+    assert kb.kda_fwd_num_chunks(valid_params(K=300)) == 0            # invalid parameters
 
 
 def test_workspace_grows_with_chunks(lib):

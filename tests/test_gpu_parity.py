@@ -277,3 +277,32 @@ def test_transposed_state_layout(dtype, K, T):
     assert fs.shape == (1, wl.HV, wl.V, wl.K)
     assert_close(o, ro, dtype, "o")
     assert_close(fs, rfs, dtype, "final_state")
+
+
+
+# ---- per-chunk states (return_intermediate_states) -------------------------------------------
+
+@pytest.mark.parametrize("dtype,K,T,transposed", [("bf16", 128, 300, False), ("f32", 64, 200, False),
+                                                  ("bf16", 128, 64 * 256 + 37, False),
+                                                  ("bf16", 128, 150, True)])
+def test_intermediate_states(dtype, K, T, transposed):
+    """The state before every chunk, on both paths; the third case runs the pipelined schedule
+    (segments in the middle of the sequence), the last the transposed layout."""
+    import torch
+    import kimi_delta_attention_gate_gb300 as kda
+    from kda_testlib import f32_device, gate_kwargs, to_device
+    wl = small(T=T, K=K, V=K, dtype=dtype, seed=520 + K + T)
+    inp = kin.make_inputs(wl)
+    if transposed:
+        inp.h0 = np.ascontiguousarray(np.swapaxes(inp.h0, -1, -2))
+    q, k, v, g, b = (to_device(x, dtype) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    o, fs, hs = kda.kda_fwd(q, k, v, g, b, A_log=f32_device(inp.A_log),
+                            dt_bias=f32_device(inp.dt_bias), scale=inp.scale,
+                            initial_state=f32_device(inp.h0), return_intermediate_states=True,
+                            transpose_state_layout=transposed, **gate_kwargs(wl))
+    torch.cuda.synchronize()
+    ro, rfs, rhs = run_oracle(inp, return_intermediate_states=True, chunk_size=64,
+                              transpose_state_layout=transposed)
+    assert hs.shape == rhs.shape == ((T + 63) // 64, wl.HV) + rfs.shape[2:]
+    assert_close(hs.cpu().double().numpy(), rhs, dtype, "intermediate states")
+    assert_close(o.float().cpu().double().numpy(), ro, dtype, "o")

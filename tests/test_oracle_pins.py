@@ -370,3 +370,30 @@ def test_transposed_state_layout_is_the_transpose():
                          transpose_state_layout=True)
     assert fsT.shape == (1, 1, V, K)
     assert np.array_equal(oT, o) and np.array_equal(fsT, np.swapaxes(fs, -1, -2))
+
+
+
+def test_intermediate_states_are_the_prefix_final_states():
+    """return_intermediate_states: entry c of sequence n is the state after the first c
+    chunks of that sequence, i.e. the final state of the same recurrence run on that prefix;
+    chunks of later sequences follow those of earlier ones; an empty sequence has none."""
+    rng = np.random.default_rng(29)
+    H, K, V, C = 1, 6, 5, 4
+    cu = np.array([0, 10, 10, 17], dtype=np.int64)   # lengths 10, 0, 7 -> 3 + 0 + 2 chunks
+    T = int(cu[-1])
+    d = dict(q=rng.standard_normal((1, T, H, K)), k=rng.standard_normal((1, T, H, K)),
+             v=rng.standard_normal((1, T, H, V)), g=-np.abs(rng.standard_normal((1, T, H, K))),
+             beta=rng.standard_normal((1, T, H)))
+    h0 = rng.standard_normal((3, H, K, V))
+    kw = dict(gate_mode=GATE_PREGATED, initial_state=h0)
+    o, fs, hs = oracle.fwd(**d, **kw, cu_seqlens=cu, return_intermediate_states=True, chunk_size=C)
+    assert hs.shape == (5, H, K, V)
+    order = [(0, 0), (0, 1), (0, 2), (2, 0), (2, 1)]  # (sequence, chunk) of each entry
+    for idx, (n, c) in enumerate(order):
+        bos = int(cu[n])
+        if c == 0:
+            assert np.array_equal(hs[idx], h0[n])
+            continue
+        pre = {key: val[:, bos:bos + c * C] for key, val in d.items()}
+        _, fpre = oracle.fwd(**pre, gate_mode=GATE_PREGATED, initial_state=h0[n:n + 1])
+        assert np.allclose(hs[idx], fpre[0], rtol=1e-13, atol=1e-13)
