@@ -70,9 +70,6 @@ __device__ __forceinline__ uint32_t ldg_u32(const void* p) {
 __device__ __forceinline__ void sts_u32(uint8_t* base, uint32_t off, uint32_t v) {
   *reinterpret_cast<uint32_t*>(base + off) = v;
 }
-__device__ __forceinline__ void sts_u16(uint8_t* base, uint32_t off, float v) {
-  *reinterpret_cast<__nv_bfloat16*>(base + off) = __float2bfloat16_rn(v);
-}
 __device__ __forceinline__ void sts_v4(uint8_t* base, uint32_t off, uint32_t a, uint32_t b,
                                        uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4*>(base + off) = make_uint4(a, b, c, d);
@@ -744,9 +741,6 @@ constexpr uint32_t TM_O = 64;    // O^T fp32 [128 v x 64 tokens]
 constexpr uint32_t TM_S = 128;   // S^T fp32 [128 v x 128 ch]
 constexpr uint32_t TM_SA = 256;  // S^T bf16 pairs (A operand), 64 columns
 constexpr uint32_t TM_VA = 320;  // V_new^T bf16 pairs (A operand), 32 columns
-#ifndef USE_TMA_STORE
-#define USE_TMA_STORE 1
-#endif
 constexpr int kPrefetch = 4;     // chunks whose loads are prefetched into L2 ahead
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
@@ -961,7 +955,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
             __float2bfloat16_rn(__uint_as_float(ro[x]));
       fence_async_smem();
       good = named_bar_and(1, kEpiThreads, good);
-      if (USE_TMA_STORE && L == TC_C) {
+      if (L == TC_C) {
         if (tid == 0) {
           tma_store_3d(omap_ptr, 0, hv, (int32_t)t0, stg);
           bulk_commit();
