@@ -475,17 +475,31 @@ def main():
     if status != 0:
         raise RuntimeError(f"device status {status:#x} after the timed region")
 
-    # End to end through the public API: pinned host inputs -> device -> kda_fwd -> host.
+    # End to end through the public API on host buffers: kda_fwd_host copies every input in
+    # from pinned host memory (the token rows segment by segment, overlapping the kernels) and
+    # o / final_state back out.  For context the same pass as three serial phases (copy in,
+    # kda_fwd, copy out) is timed too.
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 10))
-    pin = lambda t: t.cpu().pin_memory()
+    pin = lambda t: None if t is None else t.cpu().pin_memory()
     hq, hk, hv_, hg, hb = (pin(x) for x in (q, k, v, g, b))
+    hA, hdt, hh0 = (pin(x) for x in (A_log, dt_bias, h0))
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hfs = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
-    dq, dk, dv, dg, db = (torch.empty_like(x) for x in (q, k, v, g, b))
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv_, hg, hb))
+    host_in = [x for x in (hq, hk, hv_, hg, hb, hA, hdt, hh0, cu_cpu) if x is not None]
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = ho.numel() * ho.element_size() + hfs.numel() * hfs.element_size()
+    hp = kda.make_params(hq, hk, hv_, hg, hb, A_log=hA, dt_bias=hdt, scale=inp.scale,
+                         initial_state=hh0, final_state=hfs, o=ho, cu_seqlens=cu_cpu,
+                         cu_seqlens_cpu=cu_cpu, chunk_size=wl.chunk_size, **gate)
+    hp.cu_seqlens = None
+    arena = torch.empty(kb.kda_fwd_host_arena_size(hp), dtype=torch.uint8, device=dev)
 
     def e2e_step():
+        kb.raise_for(kb.kda_fwd_host(hp, arena.data_ptr(), arena.numel(), sh))
+
+    dq, dk, dv, dg, db = (torch.empty_like(x) for x in (q, k, v, g, b))
+
+    def serial_step():
         for d, h in ((dq, hq), (dk, hk), (dv, hv_), (dg, hg), (db, hb)):
             d.copy_(h, non_blocking=True)
         oo, ff = kda.kda_fwd(dq, dk, dv, dg, db, A_log=A_log, dt_bias=dt_bias, scale=inp.scale,
@@ -495,18 +509,24 @@ def main():
         ho.copy_(oo, non_blocking=True)
         hfs.copy_(ff, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    def time_steps(fn):
+        fn()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+
+    serial_ms = time_steps(serial_step)
+    e2e_ms = time_steps(e2e_step)
+    status = kb.kda_get_device_status(sh)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} after the end-to-end passes")
     e2e_value = job_throughput(inp.n_tokens, world, e2e_ms)
 
     # Roofline of the dominant kernel.
@@ -535,7 +555,8 @@ def main():
             "config": config_of(inp, args), "roofline": roofline, "path_roofline": path,
             "stages": {n: float(t) for n, t in zip(names, stage_ms)},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+                    "entry": "kda_fwd_host", "serial_copy_run_copy_ms": serial_ms},
             "gpu_launches": int(n_launch * args.steps), "clocks": clocks,
             "kernel_source_sha": kernel_source_hash()}
 

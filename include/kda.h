@@ -139,6 +139,26 @@ kda_status kda_fwd(const kda_fwd_params* p, void* stream);
    they are invalid).  Host only; makes no CUDA call. */
 int32_t kda_fwd_num_launches(const kda_fwd_params* p);
 
+/* Bytes of device arena kda_fwd_host needs for these parameters (0 if they are
+   invalid): device copies of every tensor plus the pass's workspace.  Host only;
+   makes no CUDA call. */
+size_t kda_fwd_host_arena_size(const kda_fwd_params* p);
+
+/* kda_fwd on HOST buffers: q, k, v, g, beta, A_log, dt_bias, h0 and
+   cu_seqlens_host are read from host memory, o, final_state and h_out written to
+   host memory (the device field cu_seqlens and workspace / workspace_bytes are
+   ignored; varlen is selected by cu_seqlens_host).  Everything runs in `arena`
+   (device memory the caller owns, kda_fwd_host_arena_size bytes, 256-byte
+   aligned).  With the pipelined schedule the input rows of segment k+1 are copied
+   in while segment k computes and the output rows of each segment are copied out
+   as soon as its recurrence finishes, on library-owned copy streams; page-locked
+   (pinned) host memory lets these copies run asynchronously.  Ordered on `stream`
+   like kda_fwd; the host buffers must stay valid, and o / final_state / h_out may
+   be read, only once `stream` has passed this call.  Rows of o that no sequence
+   covers are left untouched.  The source pages have no counterpart to this entry
+   point: it is the end-to-end path of a caller whose tensors live in host memory. */
+kda_status kda_fwd_host(const kda_fwd_params* p, void* arena, size_t arena_bytes, void* stream);
+
 /* The same forward pass as a token recurrence (decode and short prefill;
    "Reading Notes: Implementation Notes for KDA in FLA", section 1,
    fused_recurrent_kda): per token alpha = exp(g'), S <- Diag(alpha) S,

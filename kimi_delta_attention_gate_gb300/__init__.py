@@ -21,8 +21,8 @@ from ._binding import (KDA_BF16, KDA_F32, KDA_GATE_PLAIN, KDA_GATE_PREGATED, KDA
                        KdaError, kda_abi_version, kda_fwd_params, kda_get_device_status,
                        kda_last_error, kda_status_string)
 
-__all__ = ["kda_fwd", "kda_fwd_workspace_size", "make_params", "KdaError", "kda_get_device_status",
-           "kda_last_error", "kda_status_string", "kda_abi_version", "KDA_GATE_SAFE",
+__all__ = ["kda_fwd", "kda_fwd_host", "kda_fused_recurrent_fwd", "kda_fwd_workspace_size",
+           "make_params", "KdaError", "kda_get_device_status", "kda_last_error", "kda_status_string", "kda_abi_version", "KDA_GATE_SAFE",
            "KDA_GATE_PLAIN", "KDA_GATE_PREGATED", "KDA_BF16", "KDA_F32"]
 
 
@@ -202,4 +202,42 @@ def kda_fused_recurrent_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower
         stream = torch.cuda.current_stream(v.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     _binding.raise_for(_binding.kda_fused_recurrent_fwd(p, handle))
+    return o, final_state
+
+
+def kda_fwd_host(q, k, v, g, beta, *, o, final_state=None, A_log=None, dt_bias=None,
+                 lower_bound=None, scale=None, initial_state=None, cu_seqlens=None,
+                 chunk_size: int = 64, use_gate_in_kernel: bool = True,
+                 safe_gate: Optional[bool] = None, use_qk_l2norm_in_kernel: bool = True,
+                 use_beta_sigmoid_in_kernel: bool = True, allow_neg_eigval: bool = False,
+                 transpose_state_layout: bool = False, h_out=None, arena=None, stream=None):
+    """The forward pass on host (CPU) tensors; pinned memory makes the copies overlap the
+    kernels.  ``o`` (and ``final_state`` / ``h_out`` if given) are host tensors the result is
+    written to; ``cu_seqlens`` is a host int64 tensor.  ``arena`` (device uint8 tensor of at
+    least ``kda_fwd_host_arena_size`` bytes) is allocated when not given.  Asynchronous on
+    ``stream``: synchronise it before reading the outputs."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("o", o)):
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+    cu_cpu = None if cu_seqlens is None else cu_seqlens.to(torch.int64).contiguous()
+    p = make_params(q, k, v, g, beta, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound,
+                    scale=scale, initial_state=initial_state, final_state=final_state, o=o,
+                    cu_seqlens=cu_cpu, cu_seqlens_cpu=cu_cpu, chunk_size=chunk_size,
+                    use_gate_in_kernel=use_gate_in_kernel, safe_gate=safe_gate,
+                    use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel,
+                    use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
+                    allow_neg_eigval=allow_neg_eigval,
+                    transpose_state_layout=transpose_state_layout, h_out=h_out)
+    p.cu_seqlens = None  # the host entry reads cu_seqlens_host only
+    need = _binding.kda_fwd_host_arena_size(p)
+    if need == 0:
+        _binding.raise_for(_binding.kda_fwd_check(p))
+    if arena is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        arena = torch.empty(need, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(arena.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _binding.raise_for(_binding.kda_fwd_host(p, _ptr(arena), arena.numel(), handle))
     return o, final_state

@@ -33,7 +33,8 @@ KDA_DEV_TIMEOUT = 0x2
 
 # Every symbol the header declares.
 EXPORTED = ("kda_fwd_workspace_size", "kda_fwd_check", "kda_fwd", "kda_fwd_num_launches",
-            "kda_fwd_num_chunks", "kda_fused_recurrent_fwd",
+            "kda_fwd_num_chunks", "kda_fused_recurrent_fwd", "kda_fwd_host_arena_size",
+            "kda_fwd_host",
             "kda_fwd_num_stages",
             "kda_fwd_stage_name", "kda_fwd_stage", "kda_get_device_status", "kda_status_string",
             "kda_last_error", "kda_abi_version", "kda_fwd_noalloc")
@@ -97,6 +98,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kda_fwd_num_chunks.argtypes = [P]
             lib.kda_fused_recurrent_fwd.restype = ctypes.c_int
             lib.kda_fused_recurrent_fwd.argtypes = [P, ctypes.c_void_p]
+            lib.kda_fwd_host_arena_size.restype = ctypes.c_size_t
+            lib.kda_fwd_host_arena_size.argtypes = [P]
+            lib.kda_fwd_host.restype = ctypes.c_int
+            lib.kda_fwd_host.argtypes = [P, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
             lib.kda_fwd_num_stages.restype = ctypes.c_int32
             lib.kda_fwd_num_stages.argtypes = [P]
             lib.kda_fwd_stage_name.restype = ctypes.c_char_p
@@ -129,6 +134,15 @@ def kda_fwd(p: kda_fwd_params, stream: int = 0) -> int:
 
 def kda_fwd_noalloc(p: kda_fwd_params, stream: int = 0) -> int:
     return int(load().kda_fwd_noalloc(ctypes.byref(p), ctypes.c_void_p(stream)))
+
+
+def kda_fwd_host_arena_size(p: kda_fwd_params) -> int:
+    return int(load().kda_fwd_host_arena_size(ctypes.byref(p)))
+
+
+def kda_fwd_host(p: kda_fwd_params, arena: int, arena_bytes: int, stream: int) -> int:
+    return int(load().kda_fwd_host(ctypes.byref(p), ctypes.c_void_p(arena), ctypes.c_size_t(arena_bytes),
+                                   ctypes.c_void_p(stream)))
 
 
 def kda_fused_recurrent_fwd(p: kda_fwd_params, stream: int) -> int:

@@ -12,7 +12,9 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 #include <string>
 
 #include "kda_internal.cuh"
@@ -190,6 +192,10 @@ struct PipeCtx {
   cudaStream_t rs = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   cudaEvent_t seg[kMaxSegments] = {};
+  // host-buffer entry: copy-in and copy-out streams and their events
+  cudaStream_t cin = nullptr, cout = nullptr;
+  cudaEvent_t ein[kMaxSegments] = {}, eout[kMaxSegments] = {};
+  cudaEvent_t hfork = nullptr, hdone = nullptr;
 };
 PipeCtx g_pipe[64];
 
@@ -207,22 +213,36 @@ PipeCtx* pipe_ctx() {
         cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming) != cudaSuccess)
       return nullptr;
     for (int i = 0; i < kMaxSegments; ++i)
-      if (cudaEventCreateWithFlags(&c.seg[i], cudaEventDisableTiming) != cudaSuccess) return nullptr;
+      if (cudaEventCreateWithFlags(&c.seg[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&c.ein[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&c.eout[i], cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+    if (cudaStreamCreateWithFlags(&c.cin, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&c.cout, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c.hfork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c.hdone, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
     c.ready = true;
   }
   return &c;
 }
 
+// Work a caller adds around each segment of the pipelined schedule (host-buffer entry:
+// wait for the segment's input copies before its intra-chunk kernel, copy its output out
+// after its recurrence).  Called with the pipeline context locked.
+struct SegHooks {
+  virtual cudaError_t before_intra(PipeCtx& cx, int k, int64_t cb, int64_t ce) = 0;
+  virtual cudaError_t after_recur(PipeCtx& cx, int k, int64_t cb, int64_t ce) = 0;
+  virtual ~SegHooks() = default;
+};
+
 // Segments k = 0..nseg-1: intra(k) on the caller's stream, recur(k) on the internal
 // high-priority stream after intra(k) and recur(k-1); the caller's stream then waits for
 // the last recurrence.  Stream order alone carries every dependency (no kernel waits on
 // another), so the schedule is also valid under stream capture.
-cudaError_t launch_pipelined(const FwdArgs& a, cudaStream_t s, const char** what) {
+cudaError_t launch_pipelined_locked(PipeCtx* cx, const FwdArgs& a, cudaStream_t s,
+                                    const char** what, SegHooks* hooks) {
   const Plan& pl = a.plan;
-  PipeCtx* cx = pipe_ctx();
-  *what = "pipeline setup";
-  if (cx == nullptr) return cudaErrorInitializationError;
-  std::lock_guard<std::mutex> lk(cx->mu);
   cudaError_t e;
   if (pl.varlen) {
     *what = "chunk_table";
@@ -235,6 +255,8 @@ cudaError_t launch_pipelined(const FwdArgs& a, cudaStream_t s, const char** what
     FwdArgs ak = a;
     ak.c_begin = seg_bound(pl.nct, pl.nseg, k);
     ak.c_end = seg_bound(pl.nct, pl.nseg, k + 1);
+    *what = "input copies";
+    if (hooks && (e = hooks->before_intra(*cx, k, ak.c_begin, ak.c_end)) != cudaSuccess) return e;
     *what = "tc_intra";
     if ((e = launch_tc_intra(ak, s)) != cudaSuccess) return e;
     *what = "pipeline event";
@@ -242,10 +264,20 @@ cudaError_t launch_pipelined(const FwdArgs& a, cudaStream_t s, const char** what
     if ((e = cudaStreamWaitEvent(cx->rs, cx->seg[k], 0)) != cudaSuccess) return e;
     *what = "tc_recur";
     if ((e = launch_tc_recur(ak, cx->rs)) != cudaSuccess) return e;
+    *what = "output copies";
+    if (hooks && (e = hooks->after_recur(*cx, k, ak.c_begin, ak.c_end)) != cudaSuccess) return e;
   }
   *what = "pipeline join";
   if ((e = cudaEventRecord(cx->join, cx->rs)) != cudaSuccess) return e;
   return cudaStreamWaitEvent(s, cx->join, 0);
+}
+
+cudaError_t launch_pipelined(const FwdArgs& a, cudaStream_t s, const char** what) {
+  PipeCtx* cx = pipe_ctx();
+  *what = "pipeline setup";
+  if (cx == nullptr) return cudaErrorInitializationError;
+  std::lock_guard<std::mutex> lk(cx->mu);
+  return launch_pipelined_locked(cx, a, s, what, nullptr);
 }
 
 std::mutex g_status_mu;
@@ -310,6 +342,130 @@ kda_status prepare(const kda_fwd_params* p, FwdArgs& a) {
   a.c_end = pl.nct;
   return KDA_OK;
 }
+
+// ---- host-buffer entry ------------------------------------------------------------------
+// Device arena of kda_fwd_host: the device copy of every tensor, then the pass's workspace.
+struct HostArena {
+  size_t q, k, v, g, beta, o, h0, fs, hout, alog, dt, cu, ws;
+};
+
+HostArena host_arena(const kda_fwd_params* p, int64_t nct) {
+  HostArena A{};
+  const size_t e = p->in_dtype == KDA_BF16 ? 2 : 4;
+  const size_t ntok = (size_t)p->B * p->T;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  };
+  const size_t st = (size_t)p->N * p->HV * p->K * p->V * sizeof(float);
+  A.q = take(ntok * p->H * p->K * e);
+  A.k = take(ntok * p->H * p->K * e);
+  A.v = take(ntok * p->HV * p->V * e);
+  A.g = take(ntok * p->HV * p->K * e);
+  A.beta = take(ntok * p->HV * e);
+  A.o = take(ntok * p->HV * p->V * e);
+  A.h0 = take(p->h0 ? st : 0);
+  A.fs = take(p->final_state ? st : 0);
+  A.hout = take(p->h_out ? (size_t)nct * p->HV * p->K * p->V * sizeof(float) : 0);
+  A.alog = take(p->A_log ? (size_t)p->HV * sizeof(float) : 0);
+  A.dt = take(p->dt_bias ? (size_t)p->HV * p->K * sizeof(float) : 0);
+  A.cu = take(p->cu_seqlens_host ? (size_t)(p->N + 1) * sizeof(int64_t) : 0);
+  A.ws = off;
+  return A;
+}
+
+// The kda_fwd parameters that run the pass inside the arena at `base`.
+kda_fwd_params arena_params(const kda_fwd_params* hp, const HostArena& A, char* base) {
+  kda_fwd_params d = *hp;
+  d.q = base + A.q; d.k = base + A.k; d.v = base + A.v; d.g = base + A.g;
+  d.beta = base + A.beta; d.o = base + A.o;
+  d.h0 = hp->h0 ? reinterpret_cast<const float*>(base + A.h0) : nullptr;
+  d.final_state = hp->final_state ? reinterpret_cast<float*>(base + A.fs) : nullptr;
+  d.h_out = hp->h_out ? reinterpret_cast<float*>(base + A.hout) : nullptr;
+  d.A_log = hp->A_log ? reinterpret_cast<const float*>(base + A.alog) : nullptr;
+  d.dt_bias = hp->dt_bias ? reinterpret_cast<const float*>(base + A.dt) : nullptr;
+  d.cu_seqlens = hp->cu_seqlens_host ? reinterpret_cast<const int64_t*>(base + A.cu) : nullptr;
+  d.workspace = base + A.ws;
+  d.workspace_bytes = 0;
+  return d;
+}
+
+// Checks of the host parameters; fills the arena layout and the arena-relative params
+// (at a stand-in base when `base` is NULL) and returns the arena size through `bytes`.
+kda_status host_plan(const kda_fwd_params* hp, char* base, HostArena& A, kda_fwd_params& dp,
+                     size_t& bytes) {
+  if (hp == nullptr) return fail(KDA_ERR_INVALID_ARG, "params is NULL");
+  const struct { const void* ptr; const char* name; } need[] = {
+      {hp->q, "q"}, {hp->k, "k"}, {hp->v, "v"}, {hp->g, "g"}, {hp->beta, "beta"}, {hp->o, "o"}};
+  for (auto& e : need)
+    if (e.ptr == nullptr) return fail(KDA_ERR_INVALID_ARG, "%s is NULL", e.name);
+  kda_fwd_params probe = *hp;  // the device-side rules, checked on a stand-in arena
+  char* stand_in = reinterpret_cast<char*>(uintptr_t(1) << 20);
+  HostArena A0 = host_arena(hp, 0);
+  probe = arena_params(hp, A0, stand_in);
+  kda_status s = check_args(&probe);
+  if (s != KDA_OK) return s;
+  const Plan pl = make_plan(&probe);
+  A = host_arena(hp, pl.nct);
+  dp = arena_params(hp, A, base ? base : stand_in);
+  dp.workspace_bytes = pl.total_bytes;
+  bytes = A.ws + pl.total_bytes;
+  return KDA_OK;
+}
+
+// First token of global chunk c (c == nct: one past the last token of the last sequence).
+int64_t chunk_token(const Plan& pl, const kda_fwd_params* hp, const std::vector<int64_t>& cfirst,
+                    int64_t c) {
+  if (!pl.varlen) {
+    const int64_t n = c / pl.nc_per_seq, ci = c - n * pl.nc_per_seq;
+    return n * pl.T + ci * pl.C;
+  }
+  if (c >= pl.nct) return hp->cu_seqlens_host[pl.N];
+  int n = (int)(std::upper_bound(cfirst.begin(), cfirst.end(), c) - cfirst.begin()) - 1;
+  return hp->cu_seqlens_host[n] + (c - cfirst[n]) * pl.C;
+}
+
+// Copies in, per segment, the token rows of q, k, v, g, beta on the copy-in stream; the
+// segment's intra-chunk kernel waits for them; its output rows go out on the copy-out
+// stream after its recurrence.
+struct HostCopies : SegHooks {
+  const kda_fwd_params* hp;
+  const kda_fwd_params* dp;
+  const Plan* pl;
+  std::vector<int64_t> cfirst;
+  cudaStream_t s;
+  size_t e;
+  cudaError_t rows_in(cudaStream_t st, int64_t tb, int64_t te) {
+    const struct { void* dst; const void* src; size_t row; } t[] = {
+        {const_cast<void*>(dp->q), hp->q, (size_t)pl->H * pl->K * e},
+        {const_cast<void*>(dp->k), hp->k, (size_t)pl->H * pl->K * e},
+        {const_cast<void*>(dp->v), hp->v, (size_t)pl->HV * pl->V * e},
+        {const_cast<void*>(dp->g), hp->g, (size_t)pl->HV * pl->K * e},
+        {const_cast<void*>(dp->beta), hp->beta, (size_t)pl->HV * e}};
+    for (auto& x : t) {
+      cudaError_t r = cudaMemcpyAsync(static_cast<char*>(x.dst) + tb * x.row,
+                                      static_cast<const char*>(x.src) + tb * x.row,
+                                      (te - tb) * x.row, cudaMemcpyHostToDevice, st);
+      if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
+  }
+  cudaError_t before_intra(PipeCtx& cx, int k, int64_t, int64_t) override {
+    return cudaStreamWaitEvent(s, cx.ein[k], 0);
+  }
+  cudaError_t after_recur(PipeCtx& cx, int k, int64_t cb, int64_t ce) override {
+    cudaError_t r;
+    if ((r = cudaEventRecord(cx.eout[k], cx.rs)) != cudaSuccess) return r;
+    if ((r = cudaStreamWaitEvent(cx.cout, cx.eout[k], 0)) != cudaSuccess) return r;
+    const int64_t tb = chunk_token(*pl, hp, cfirst, cb), te = chunk_token(*pl, hp, cfirst, ce);
+    const size_t row = (size_t)pl->HV * pl->V * e;
+    return cudaMemcpyAsync(static_cast<char*>(hp->o) + tb * row,
+                           static_cast<const char*>(dp->o) + tb * row, (te - tb) * row,
+                           cudaMemcpyDeviceToHost, cx.cout);
+  }
+};
 
 }  // namespace
 
@@ -378,6 +534,101 @@ int32_t kda_fwd_num_launches(const kda_fwd_params* p) {
   if (pl.nseg > 1) return (pl.varlen ? 1 : 0) + 2 * pl.nseg;
   Stage st[kMaxStages];
   return stages_for(pl, st);
+}
+
+size_t kda_fwd_host_arena_size(const kda_fwd_params* p) {
+  HostArena A;
+  kda_fwd_params dp;
+  size_t bytes = 0;
+  return host_plan(p, nullptr, A, dp, bytes) == KDA_OK ? bytes : 0;
+}
+
+kda_status kda_fwd_host(const kda_fwd_params* p, void* arena, size_t arena_bytes, void* stream) {
+  HostArena A;
+  kda_fwd_params dp;
+  size_t need = 0;
+  kda_status st = host_plan(p, static_cast<char*>(arena), A, dp, need);
+  if (st != KDA_OK) return st;
+  if (arena == nullptr || arena_bytes < need)
+    return fail(KDA_ERR_WORKSPACE, "arena needs %zu bytes (got %zu%s)", need, arena_bytes,
+                arena ? "" : ", NULL");
+  if (!aligned(arena, 256)) return fail(KDA_ERR_WORKSPACE, "arena must be 256-byte aligned");
+  FwdArgs a;
+  st = prepare(&dp, a);
+  if (st != KDA_OK) return st;
+  const Plan& pl = a.plan;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t e = p->in_dtype == KDA_BF16 ? 2 : 4;
+  const size_t sbytes = (size_t)pl.N * pl.HV * pl.K * pl.V * sizeof(float);
+  const char* what = "parameter copies";
+  auto h2d = [&](const void* dst, const void* src, size_t n, cudaStream_t on) {
+    return n == 0 || src == nullptr
+               ? cudaSuccess
+               : cudaMemcpyAsync(const_cast<void*>(dst), src, n, cudaMemcpyHostToDevice, on);
+  };
+  auto d2h = [&](void* dst, const void* src, size_t n, cudaStream_t on) {
+    return n == 0 || dst == nullptr ? cudaSuccess
+                                    : cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, on);
+  };
+  cudaError_t r = cudaSuccess;
+  auto chk = [&](cudaError_t x) {
+    if (r == cudaSuccess) r = x;
+    return r == cudaSuccess;
+  };
+  chk(h2d(dp.A_log, p->A_log, p->A_log ? (size_t)pl.HV * sizeof(float) : 0, s));
+  chk(h2d(dp.dt_bias, p->dt_bias, p->dt_bias ? (size_t)pl.HV * pl.K * sizeof(float) : 0, s));
+  chk(h2d(dp.h0, p->h0, p->h0 ? sbytes : 0, s));
+  chk(h2d(dp.cu_seqlens, p->cu_seqlens_host,
+          p->cu_seqlens_host ? (size_t)(pl.N + 1) * sizeof(int64_t) : 0, s));
+  const size_t hbytes = (size_t)pl.nct * pl.HV * pl.K * pl.V * sizeof(float);
+  if (r == cudaSuccess && pl.nseg > 1) {
+    PipeCtx* cx = pipe_ctx();
+    if (cx == nullptr) return fail(KDA_ERR_CUDA, "pipeline setup failed");
+    std::lock_guard<std::mutex> lk(cx->mu);
+    HostCopies hc;
+    hc.hp = p; hc.dp = &dp; hc.pl = &pl; hc.s = s; hc.e = e;
+    if (pl.varlen) {
+      hc.cfirst.resize(pl.N + 1);
+      hc.cfirst[0] = 0;
+      for (int n = 0; n < pl.N; ++n)
+        hc.cfirst[n + 1] = hc.cfirst[n] +
+            (p->cu_seqlens_host[n + 1] - p->cu_seqlens_host[n] + pl.C - 1) / pl.C;
+    }
+    what = "input copies";
+    chk(cudaEventRecord(cx->hfork, s)) && chk(cudaStreamWaitEvent(cx->cin, cx->hfork, 0)) &&
+        chk(cudaStreamWaitEvent(cx->cout, cx->hfork, 0));
+    for (int k = 0; k < pl.nseg && r == cudaSuccess; ++k) {
+      const int64_t tb = chunk_token(pl, p, hc.cfirst, seg_bound(pl.nct, pl.nseg, k));
+      const int64_t te = chunk_token(pl, p, hc.cfirst, seg_bound(pl.nct, pl.nseg, k + 1));
+      chk(hc.rows_in(cx->cin, tb, te)) && chk(cudaEventRecord(cx->ein[k], cx->cin));
+    }
+    if (r == cudaSuccess) r = launch_pipelined_locked(cx, a, s, &what, &hc);
+    what = "output copies";
+    chk(d2h(p->final_state, dp.final_state, p->final_state ? sbytes : 0, cx->cout));
+    chk(d2h(p->h_out, dp.h_out, p->h_out ? hbytes : 0, cx->cout));
+    chk(cudaEventRecord(cx->hdone, cx->cout)) && chk(cudaStreamWaitEvent(s, cx->hdone, 0));
+  } else if (r == cudaSuccess) {
+    HostCopies hc;
+    hc.hp = p; hc.dp = &dp; hc.pl = &pl; hc.s = s; hc.e = e;
+    // rows past the last sequence are neither read nor written
+    const int64_t tend = pl.varlen ? p->cu_seqlens_host[pl.N] : pl.ntok;
+    what = "input copies";
+    if (chk(hc.rows_in(s, 0, tend))) {
+      Stage stg[kMaxStages];
+      const int n = stages_for(pl, stg);
+      for (int i = 0; i < n && r == cudaSuccess; ++i) {
+        what = stg[i].name;
+        chk(stg[i].launch(a, s));
+      }
+    }
+    what = "output copies";
+    chk(d2h(p->o, dp.o, (size_t)tend * pl.HV * pl.V * e, s));
+    chk(d2h(p->final_state, dp.final_state, p->final_state ? sbytes : 0, s));
+    chk(d2h(p->h_out, dp.h_out, p->h_out ? hbytes : 0, s));
+  }
+  if (r != cudaSuccess) return fail(KDA_ERR_CUDA, "%s failed: %s", what, cudaGetErrorString(r));
+  t_last_error.clear();
+  return KDA_OK;
 }
 
 kda_status kda_fused_recurrent_fwd(const kda_fwd_params* p, void* stream) {

@@ -117,3 +117,44 @@ def run_gpu_stages(inp: kin.Inputs):
     torch.cuda.synchronize()
     assert kb.kda_get_device_status(sh) == 0
     return o.float().cpu().double().numpy(), fs.cpu().double().numpy()
+
+
+def to_pinned(x: np.ndarray, dtype: str):
+    """``x`` as a page-locked host tensor in the path's input type."""
+    import torch
+    if dtype == "bf16":
+        t = torch.from_numpy(kin.to_bf16_bits(x).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(x, np.float32))
+    return t.pin_memory()
+
+
+def run_gpu_host(inp: kin.Inputs, sentinel=7.0, h_out_chunks=0, **opts):
+    """The host-buffer entry point on ``inp``: every tensor in pinned host memory, the device
+    arena pre-filled with NaN bits.  Host o starts at ``sentinel`` so rows no sequence covers
+    can be checked untouched.  Returns (o, final_state[, h_out]) as float64 numpy arrays."""
+    import torch
+    import kimi_delta_attention_gate_gb300 as kda
+    wl = inp.wl
+    q, k, v, g, b = (to_pinned(x, wl.dtype) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    pin32 = (lambda x: None if x is None else
+             torch.from_numpy(np.ascontiguousarray(x, np.float32)).pin_memory())
+    o = torch.full((wl.B, wl.T, wl.HV, wl.V), sentinel, dtype=v.dtype).pin_memory()
+    st = (wl.V, wl.K) if opts.get("transpose_state_layout") else (wl.K, wl.V)
+    fs = torch.zeros((inp.N, wl.HV) + st, dtype=torch.float32).pin_memory()
+    hs = (torch.zeros((h_out_chunks, wl.HV) + st, dtype=torch.float32).pin_memory()
+          if h_out_chunks else None)
+    cu = None if inp.cu_seqlens is None else torch.from_numpy(inp.cu_seqlens)
+    kw = dict(A_log=pin32(inp.A_log), dt_bias=pin32(inp.dt_bias), scale=inp.scale,
+              initial_state=pin32(inp.h0), cu_seqlens=cu, chunk_size=wl.chunk_size,
+              **gate_kwargs(wl), **opts)
+    from kimi_delta_attention_gate_gb300 import _binding as kb
+    p = kda.make_params(q, k, v, g, b, o=o, final_state=fs, h_out=hs, cu_seqlens_cpu=cu, **kw)
+    need = kb.kda_fwd_host_arena_size(p)
+    assert need > 0, kb.kda_last_error()
+    arena = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    kda.kda_fwd_host(q, k, v, g, b, o=o, final_state=fs, h_out=hs, arena=arena, **kw)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status(0) == 0
+    out = (o.float().double().numpy(), fs.double().numpy())
+    return out + ((hs.double().numpy(),) if hs is not None else ())

@@ -205,3 +205,23 @@ def test_launch_counts_of_the_pipelined_schedule(lib):
     # varlen adds the chunk-table launch
     p, keep = cu_params([0, 64 * 400, 64 * 600], T=64 * 600, H=4, HV=4, V=128)
     assert kb.kda_fwd_num_launches(p) == 1 + 2 * 4
+
+
+def test_host_entry_arena_size_and_rejections(lib):
+    p = valid_params()
+    # device copies of q, k, v, g, beta and o (each 256-byte aligned), then the workspace
+    copies = 2 * 102400 + 102400 + 204800 + 1792 + 102400
+    assert kb.kda_fwd_host_arena_size(p) == copies + kb.kda_fwd_workspace_size(p)
+    fs = valid_params(final_state=FAKE)
+    assert kb.kda_fwd_host_arena_size(fs) == kb.kda_fwd_host_arena_size(p) + 2 * 4 * 128 * 64 * 4
+    assert kb.kda_fwd_host_arena_size(valid_params(K=300)) == 0
+    need = kb.kda_fwd_host_arena_size(p)
+    # arena checks come before any CUDA call
+    assert kb.kda_fwd_host(p, 0, need, 0) == kb.KDA_ERR_WORKSPACE
+    assert kb.kda_fwd_host(p, FAKE, need - 1, 0) == kb.KDA_ERR_WORKSPACE
+    assert kb.kda_fwd_host(p, FAKE + 16, need, 0) == kb.KDA_ERR_WORKSPACE
+    assert kb.kda_fwd_host(valid_params(q=None), FAKE, need, 0) == kb.KDA_ERR_INVALID_ARG
+    # varlen on the host entry is selected by cu_seqlens_host alone
+    cu = (ctypes.c_int64 * 3)(0, 150, 200)
+    v = valid_params(B=1, T=200, N=2, cu_seqlens_host=ctypes.addressof(cu))
+    assert kb.kda_fwd_host_arena_size(v) > 0
