@@ -54,8 +54,11 @@ constexpr uint32_t OFF_T = 57344;
 constexpr uint32_t OFF_D = 65536;
 constexpr uint32_t BLOCK_BYTES = 66048;
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+// First 1024-byte-aligned byte of the dynamic shared memory.  The offset is added to the
+// shared array itself, not to an integer copy of its address, so that every access made
+// through the result compiles to a 32-bit shared-memory access rather than a generic one.
+__device__ __forceinline__ uint8_t* align1024(uint8_t* smem) {
+  return smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
 }
 __device__ __forceinline__ float ex2(float x) {
   float y;
