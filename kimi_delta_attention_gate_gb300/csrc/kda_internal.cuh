@@ -89,7 +89,7 @@ __device__ __forceinline__ bool locate_chunk(const FwdArgs& a, int64_t c, int& n
   const Plan& p = a.plan;
   int64_t bos, eos, ci;
   if (!p.varlen) {
-    n = (int)(c / p.nc_per_seq);
+    n = (int)((uint32_t)c / (uint32_t)p.nc_per_seq);  // chunk indexes fit in 32 bits
     ci = c - (int64_t)n * p.nc_per_seq;
     bos = (int64_t)n * p.T;
     eos = bos + p.T;

@@ -255,6 +255,16 @@ __global__ void __launch_bounds__(256, 2)
   tc_fence_after();
   const uint32_t tmem = *sTmem;
   if (!mbar_wait(&bars[0], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
+  if (L < TC_C) {  // a short chunk: its q, k and g rows past L (the next sequence's tokens or
+                   // the copy's fill) become zero, so that no later load needs a row mask
+    for (int e = tid; e < (TC_C - L) * 48; e += 256) {
+      const int t = L + e / 48, x = e % 48, pn = x / 24, w = x % 24, rk = w >> 3, ch = w & 7;
+      const uint32_t row = rk == 0 ? q_row(t) : (rk == 1 ? k_row(t) : (uint32_t)t);
+      uint8_t* base = rk < 2 ? sm + P_QK + pn * 16384 : sm + P_X + pn * 8192;
+      sts_v4(base, row * 128 + ch * 16, 0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+  }
 
   // ---- element-wise phase: thread = 16-row block rg x channel pair (c0, c0+1) ----
   const int rg = tid >> 6, cp = tid & 63, c0 = 2 * cp;
@@ -270,6 +280,7 @@ __global__ void __launch_bounds__(256, 2)
   // gate + in-block cumsum (log2 units); G <= 0 for every non-positive gate
   float G0[16], G1[16];
   float acc0 = 0.f, acc1 = 0.f, span = 0.f;
+  const float zsc = -kLog2e * aexp;  // safe gate: 2^(zsc (g + dt)) = e^(-aexp (g + dt))
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = 16 * rg + r;
@@ -277,8 +288,7 @@ __global__ void __launch_bounds__(256, 2)
     if (row < L) {
       const uint32_t gv = lds_u32(x_pan, sw128_offset(row, cc));
       if (GATE == KDA_GATE_SAFE) {  // lb sigmoid(a x) on the channel pair
-        const float2 y = mul2(add2(bf_pair(gv), make_float2(dt0, dt1)), make_float2(aexp, aexp));
-        const float2 z = mul2(y, make_float2(-kLog2e, -kLog2e));
+        const float2 z = mul2(add2(bf_pair(gv), make_float2(dt0, dt1)), make_float2(zsc, zsc));
         const float2 d = add2(make_float2(ex2(z.x), ex2(z.y)), make_float2(1.f, 1.f));
         gp = mul2(make_float2(rcp_approx(d.x), rcp_approx(d.y)), make_float2(lb, lb));
       } else {
@@ -291,8 +301,10 @@ __global__ void __launch_bounds__(256, 2)
     acc1 = acc.y;
     G0[r] = acc0;
     G1[r] = acc1;
-    span = fmaxf(span, fmaxf(fabsf(acc0), fabsf(acc1)));
+    // a gate that is never positive makes the cumsum monotone: its last value is the span
+    if (GATE == KDA_GATE_PREGATED) span = fmaxf(span, fmaxf(fabsf(acc0), fabsf(acc1)));
   }
+  if (GATE != KDA_GATE_PREGATED) span = fmaxf(fabsf(acc0), fabsf(acc1));
   sBsum[rg * 128 + c0] = acc0;
   sBsum[rg * 128 + c0 + 1] = acc1;
   if (span > kGuardLog2) atomicOr(sFlag, 1 << rg);
@@ -309,8 +321,8 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int row = 16 * rg + r;
-      const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(q_row(row), cc)) : 0u;
-      const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(k_row(row), cc)) : 0u;
+      const uint32_t qv = lds_u32(qk_pan, sw128_offset(q_row(row), cc));
+      const uint32_t kv = lds_u32(qk_pan, sw128_offset(k_row(row), cc));
       sq[r] = bf_lo(qv) * bf_lo(qv) + bf_hi(qv) * bf_hi(qv);
       sk[r] = bf_lo(kv) * bf_lo(kv) + bf_hi(kv) * bf_hi(kv);
     }
@@ -387,8 +399,8 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = 16 * rg + r;
-    const uint32_t qv = row < L ? lds_u32(qk_pan, sw128_offset(q_row(row), cc)) : 0u;
-    const uint32_t kv = row < L ? lds_u32(qk_pan, sw128_offset(k_row(row), cc)) : 0u;
+    const uint32_t qv = lds_u32(qk_pan, sw128_offset(q_row(row), cc));
+    const uint32_t kv = lds_u32(qk_pan, sw128_offset(k_row(row), cc));
     const float2 nrm = *reinterpret_cast<const float2*>(sNorm + 2 * row);  // (qn, kn)
     const float2 qf = mul2(bf_pair(qv), make_float2(nrm.x, nrm.x));
     const float2 kf = mul2(bf_pair(kv), make_float2(nrm.y, nrm.y));
@@ -408,7 +420,7 @@ __global__ void __launch_bounds__(256, 2)
       for (int I = 0; I < 4; ++I) {
         if (I < rg) continue;
         sts_u32(sm + P_KA + pan * KA_PANEL, sw128_offset(ka_row(I) + row, cc),
-                pack2(I == rg ? ke : mul2(ke, F[I])));
+                pack2(mul2(ke, F[I])));  // F[rg] = 1 exactly
       }
       const float2 kg = mul2(ke, ekg);
       kg0 = kg.x;
@@ -476,14 +488,17 @@ __global__ void __launch_bounds__(256, 2)
       uint32_t r[16];
       tmem_ld16(tmem_addr(tmem, 32 * bq, ka_row(bq) + jb), r);
       tmem_wait_ld();
-      const bool diag = diag_exact && pc == bq;
       float vals[16];
 #pragma unroll
-      for (int x = 0; x < 16; ++x) {
-        const int j = jb + x;
-        const float v = diag ? dg[x] : __uint_as_float(r[x]);
-        const bool keep = isk ? (j < i) : (j <= i);
-        vals[x] = keep ? v : 0.f;
+      for (int x = 0; x < 16; ++x) vals[x] = __uint_as_float(r[x]);
+      if (pc == bq) {  // the diagonal piece (warp-uniform): exact entries, lower triangle
+        if (diag_exact) {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) vals[x] = dg[x];
+        }
+        const int li = lane & 15;
+#pragma unroll
+        for (int x = 0; x < 16; ++x) vals[x] = (isk ? (x < li) : (x <= li)) ? vals[x] : 0.f;
       }
       if (!isk) {
 #pragma unroll
@@ -650,10 +665,13 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {
       float t[8];
+      const float4 b0 = *reinterpret_cast<const float4*>(sBeta + j0 + 8 * hlf);
+      const float4 b1 = *reinterpret_cast<const float4*>(sBeta + j0 + 8 * hlf + 4);
+      const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
       for (int x = 0; x < 8; ++x) {
         const int j = j0 + 8 * hlf + x;
-        t[x] = (j <= i) ? sX[i * SOLVE_LD + j] * sBeta[j] : 0.f;
+        t[x] = (j <= i) ? sX[i * SOLVE_LD + j] * bj[x] : 0.f;
       }
       const uint32_t w0 = pack_bf16x2(t[0], t[1]), w1 = pack_bf16x2(t[2], t[3]);
       const uint32_t w2 = pack_bf16x2(t[4], t[5]), w3 = pack_bf16x2(t[6], t[7]);
