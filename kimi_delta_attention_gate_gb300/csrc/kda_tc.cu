@@ -729,9 +729,10 @@ __global__ void __launch_bounds__(256, 2)
 // ======================================================================================
 // One CTA per (sequence, value head) holds the whole V = 128.  Warps 0-15 are epilogue
 // warps (thread v = 32q + lane of TMEM lane quadrant q = warp % 4 owns row v of every
-// transposed tile; the four warps of a quadrant split its columns); warp 16 is the control
-// warp: one thread issues every MMA, bulk / tensor copy and L2 prefetch, and the roles meet
-// on mbarriers.  The fp32 state S^T lives in tensor memory as an MMA accumulator; the bf16
+// transposed tile; the four warps of a quadrant split its columns); in warp 16 one thread
+// issues every MMA, in warp 17 one thread every bulk / tensor copy and L2 prefetch (issuing
+// a chunk's copies takes ~1,000 cycles, which must not delay the next MMA), and the roles
+// meet on mbarriers.  The fp32 state S^T lives in tensor memory as an MMA accumulator; the bf16
 // copies of S^T and V_new^T that serve as A operands are written to tensor memory too, so
 // no operand goes through shared memory except the packed block and the v tile.
 // An MMA instruction (M = 128, K = 16) costs at least ~94 cycles whatever N up to 128
@@ -752,7 +753,7 @@ constexpr uint32_t SL_V = 66560;                     // v tile [64 tokens x 128 
 constexpr uint32_t SLOT = 82944;
 constexpr uint32_t R_RING = 0;                       // 2 slots
 constexpr uint32_t R_STG = 2 * SLOT;                 // O staging [2][64 tokens x 128 v] bf16
-constexpr uint32_t R_BAR = R_STG + 32768;            // full[2], bar_v, bar_s, bar_vn, bar_st
+constexpr uint32_t R_BAR = R_STG + 32768;  // full[2], bar_v, bar_s, bar_vn, bar_st, freed[2]
 constexpr uint32_t R_TMEM = R_BAR + 64;
 constexpr uint32_t R_END = R_TMEM + 16;
 constexpr uint32_t R_SMEM = R_END + 1024;
@@ -765,7 +766,8 @@ constexpr uint32_t TM_VA = 320;  // V_new^T bf16 pairs (A operand), 32 columns
 constexpr int kPrefetch = 4;     // chunks whose loads are prefetched into L2 ahead
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kRecThreads = kEpiThreads + 32;  // + control warp
+constexpr int kMmaWarp = kEpiWarps, kCopyWarp = kEpiWarps + 1;
+constexpr int kRecThreads = kEpiThreads + 64;  // + MMA warp + copy warp
 
 template <bool SAVE_STATES>  // SAVE_STATES: write the state before every chunk to h_out
 __global__ void __launch_bounds__(kRecThreads, 1)
@@ -801,13 +803,16 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   uint64_t* bar_s = full + 3;   // G2+O2 done: O^T and the next chunk's S^T complete
   uint64_t* bar_vn = full + 4;  // epilogue: bf16 V_new^T written
   uint64_t* bar_st = full + 5;  // epilogue: O^T read and cleared, bf16 S^T written
+  uint64_t* freed = full + 6;   // [2]: G2+O2 of the slot's chunk done, the slot may be refilled
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + R_TMEM);
-  if (warp == kEpiWarps) {
+  if (warp == kMmaWarp) {
     tmem_alloc(sTmem, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(&full[i], 1);
+    mbar_init(&freed[0], 1);
+    mbar_init(&freed[1], 1);
     mbar_init(bar_vn, kEpiWarps);
     mbar_init(bar_st, kEpiWarps);
     fence_mbar_init();
@@ -817,10 +822,10 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   const uint32_t tmem = *sTmem;
   bool ok = true;
 
-  if (warp == kEpiWarps) {
-    // ---------------------------------- control warp ----------------------------------
+  const uint8_t* blocks = reinterpret_cast<const uint8_t*>(a.ws) + p.off_inter;
+  if (warp == kCopyWarp) {
+    // ----------------------------------- copy warp ------------------------------------
     if (lane == 0) {
-      const uint8_t* blocks = reinterpret_cast<const uint8_t*>(a.ws) + p.off_inter;
       const CUtensorMap* vmap_ptr = &vmap;  // generic address of the kernel parameter
       auto issue = [&](int64_t ci, int st) {  // chunk ci -> slot st: block + 2 v halves
         const int64_t cg = cfirst + ci;
@@ -838,6 +843,38 @@ __global__ void __launch_bounds__(kRecThreads, 1)
         tma_prefetch_3d(vmap_ptr, 0, hv, (int32_t)(bos + ci * TC_C));
         tma_prefetch_3d(vmap_ptr, 64, hv, (int32_t)(bos + ci * TC_C));
       };
+      // Slot s holds chunks s, s+2, ...: chunk ci+2 is copied in as soon as G2+O2 of chunk ci
+      // (the last reader of the slot) completes, a whole chunk before U of chunk ci+2 needs it.
+      // freed[s] completes once per chunk of slot s and chunk ci+2 cannot complete before this
+      // thread has seen chunk ci's phase, so the parity waits never fall two phases behind.
+      int64_t issued = 0;
+      if (nch > 0) {
+        issue(0, 0);
+        issued = 1;
+        if (nch > 1) {
+          issue(1, 1);
+          issued = 2;
+        }
+        for (int64_t d = 2; d < 2 + kPrefetch && d < nch; ++d) prefetch(d);
+      }
+      for (int64_t ci = 0; ci + 2 < nch; ++ci) {
+        const int s = (int)(ci & 1);
+        if (!mbar_wait(&freed[s], (uint32_t)((ci >> 1) & 1))) { ok = false; break; }
+        issue(ci + 2, s);
+        issued = ci + 3;
+        if (ci + 2 + kPrefetch < nch) prefetch(ci + 2 + kPrefetch);
+      }
+      if (!ok) {
+        flag_status(a.status, KDA_DEV_TIMEOUT);
+        // the copies in flight must land before the CTA's shared memory is released
+        for (int64_t c = issued > 2 ? issued - 2 : 0; c < issued; ++c)
+          mbar_wait(&full[c & 1], (uint32_t)((c >> 1) & 1), 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------ MMA warp ------------------------------------
+    if (lane == 0) {
       // wait for chunk ci's data, clear v rows past the chunk end, issue U^T into TM_VN
       auto issue_u = [&](int64_t ci) -> bool {
         const int st = (int)(ci & 1);
@@ -860,14 +897,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
                    sdesc_sw128(tb + ks * 32, 16, 1024), idesc_bf16(128, 64, true), ks > 0);
         return true;
       };
-      // Slot s holds chunks s, s+2, ...: chunk ci+2 is copied in as soon as G2+O2 of chunk ci
-      // (the last reader of the slot) completes, a whole chunk before U of chunk ci+2 needs it
-      if (nch > 0) {
-        issue(0, 0);
-        if (nch > 1) issue(1, 1);
-        for (int64_t d = 2; d < 2 + kPrefetch && d < nch; ++d) prefetch(d);
-        if (!issue_u(0)) ok = false;
-      }
+      if (nch > 0 && !issue_u(0)) ok = false;
       for (int64_t ci = 0; ci < nch && ok; ++ci) {
         const int s = (int)(ci & 1);
         uint8_t* slot = sm + R_RING + s * SLOT;
@@ -889,17 +919,10 @@ __global__ void __launch_bounds__(kRecThreads, 1)
           mma_bf16_ts(tmem + TM_O, tmem + TM_VA + 8 * ks, sdesc_sw128(b2 + ks * 32, 16, 1024),
                       idesc_bf16(128, 192), 1);
         mma_commit(bar_s);
+        mma_commit(&freed[s]);  // the slot's last reader
         if (ci + 1 < nch && !issue_u(ci + 1)) { ok = false; break; }
-        if (ci + 2 < nch) {
-          if (!mbar_wait(bar_s, (uint32_t)(ci & 1))) { ok = false; break; }
-          issue(ci + 2, s);
-          if (ci + 2 + kPrefetch < nch) prefetch(ci + 2 + kPrefetch);
-        }
       }
-      if (!ok) {
-        flag_status(a.status, KDA_DEV_TIMEOUT);
-        for (int st = 0; st < 2; ++st) mbar_wait(&full[st], 0, 100000000ull);
-      }
+      if (!ok) flag_status(a.status, KDA_DEV_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -1059,7 +1082,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kEpiWarps) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 // Driver entry point for tensor-map encoding, looked up once.
