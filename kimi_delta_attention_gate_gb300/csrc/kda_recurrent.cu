@@ -8,8 +8,15 @@
 //   alpha = exp(g'_t)                          g' the activated gate (section 2)
 //   S <- Diag(alpha) S ;  p = S^T k ;  S <- S + beta k (v - p)^T ;  o_t = scale S^T q
 // with q, k L2-normalised over K and beta = sigmoid(logit) (x2 with allow_neg_eigval) when
-// the flags ask for it.  One CTA per (sequence, value head, 32 columns of V); 8 warps split
-// the K rows of the 32-column state tile, which stays in shared memory in fp32.
+// the flags ask for it.
+//
+// Two kernels.  For K <= 128 (recurrent_reg_kernel) the state lives in registers: one CTA per
+// (sequence, value head, 64 columns of V), each column held by 4 adjacent lanes that own its K
+// rows r = 4j + sub (32 fp32 values each), so that every reduction over K is two shuffles and
+// a token costs one block barrier; for decode the kernel is a stream of state
+// reads and writes.  For larger K (recurrent_kernel) one CTA per (sequence, value head, 32
+// columns of V); 8 warps split the K rows of the 32-column state tile, which stays in shared
+// memory in fp32.
 
 #include "kda_internal.cuh"
 
@@ -146,6 +153,134 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const FwdArgs a) {
     for (int kk = warp; kk < K; kk += kWarps) a.final_state[sidx(kk)] = sS[kk * kTile + lane];
 }
 
+constexpr int kColLanes = 4;                   // lanes per V column
+constexpr int kRegRows = 32;                   // K rows per lane (K <= kColLanes * kRegRows)
+constexpr int kRegCols = kThreads / kColLanes;  // V columns per CTA
+
+// FIXED: K = V = 128 and the [K][V] state layout, so that every state row offset is a
+// compile-time immediate (few address registers: three CTAs per SM keep more state reads in
+// flight); otherwise K, V and the layout are read from the arguments.
+template <typename Tin, bool FIXED>
+__global__ void __launch_bounds__(kThreads, FIXED ? 3 : 2) recurrent_reg_kernel(const FwdArgs a) {
+  __shared__ float sQ[kColLanes * kRegRows], sK[kColLanes * kRegRows];  // raw q, k
+  __shared__ float sA[kColLanes * kRegRows];                            // decay
+  __shared__ float sPart[2][kWarps];                                       // sums of squares
+  __shared__ float sBeta;
+  const Plan& p = a.plan;
+  const int K = FIXED ? 128 : p.K, V = FIXED ? 128 : p.V, HV = p.HV, H = p.H;
+  const bool v_first = FIXED ? false : (bool)a.state_v_first;
+  const int nvt = (V + kRegCols - 1) / kRegCols;
+  const int vt = (int)(blockIdx.x % nvt);
+  const int hv = (int)((blockIdx.x / nvt) % HV);
+  const int n = (int)(blockIdx.x / ((unsigned)nvt * HV));
+  const int h = hv / p.G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sub = lane & (kColLanes - 1);  // rows kColLanes j + sub
+  const int col = vt * kRegCols + warp * (32 / kColLanes) + lane / kColLanes;
+  const bool cv = col < V;
+  int64_t bos, eos;
+  if (p.varlen) {
+    bos = a.cu_seqlens[n];
+    eos = a.cu_seqlens[n + 1];
+  } else {
+    bos = (int64_t)n * p.T;
+    eos = bos + p.T;
+  }
+  if (bos < 0 || eos < bos || eos > p.ntok) {
+    if (tid == 0) flag_status(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const Tin* gq = static_cast<const Tin*>(a.q);
+  const Tin* gk = static_cast<const Tin*>(a.k);
+  const Tin* gv = static_cast<const Tin*>(a.v);
+  const Tin* gg = static_cast<const Tin*>(a.g);
+  const Tin* gb = static_cast<const Tin*>(a.beta);
+  Tin* go = static_cast<Tin*>(a.o);
+  const size_t state_base = ((size_t)n * HV + hv) * (size_t)K * V;
+  auto sidx = [&](int r) {
+    return state_base + (v_first ? (size_t)col * K + r : (size_t)r * V + col);
+  };
+  float S[kRegRows];
+#pragma unroll
+  for (int j = 0; j < kRegRows; ++j) {
+    const int r = kColLanes * j + sub;
+    S[j] = (a.h0 != nullptr && cv && r < K) ? a.h0[sidx(r)] : 0.f;
+  }
+  const float a_exp = (a.gate_mode != KDA_GATE_PREGATED && a.A_log != nullptr) ? expf(a.A_log[hv]) : 1.f;
+
+  for (int64_t t = bos; t < eos; ++t) {
+    // the token's q, k, decay and beta (thread r < K holds row r; rows past K stay 0)
+    float qi = 0.f, ki = 0.f, ai = 1.f;
+    if (tid < K) {
+      qi = to_f32(gq[(t * H + h) * (int64_t)K + tid]);
+      ki = to_f32(gk[(t * H + h) * (int64_t)K + tid]);
+      const float gi = to_f32(gg[(t * HV + hv) * (int64_t)K + tid]);
+      const float dt = (a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED)
+                           ? a.dt_bias[(size_t)hv * K + tid] : 0.f;
+      ai = expf(gate_exact(a.gate_mode, gi, a_exp, dt, a.lower_bound));
+    }
+    if (tid < kColLanes * kRegRows) {
+      sQ[tid] = qi;
+      sK[tid] = ki;
+      sA[tid] = ai;
+    }
+    const float vv = cv ? to_f32(gv[(t * HV + hv) * (int64_t)V + col]) : 0.f;
+    if (a.qk_l2norm) {
+      const float sq = warp_sum_all(qi * qi), sk = warp_sum_all(ki * ki);
+      if (lane == 0) {
+        sPart[0][warp] = sq;
+        sPart[1][warp] = sk;
+      }
+    }
+    if (tid == 0) {
+      float b = to_f32(gb[t * HV + hv]);
+      if (a.beta_sigmoid) b = (a.allow_neg_eigval ? 2.f : 1.f) * sigmoid_exact(b);
+      sBeta = b;
+    }
+    __syncthreads();
+    float qn = a.scale, kn = 1.f;
+    if (a.qk_l2norm) {
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        sq += sPart[0][w];
+        sk += sPart[1][w];
+      }
+      qn *= rsqrtf(sq + 1e-6f);
+      kn = rsqrtf(sk + 1e-6f);
+    }
+    // S <- Diag(alpha) S and this lane's part of S^T k
+    float pp = 0.f;
+#pragma unroll
+    for (int j = 0; j < kRegRows; ++j) {
+      const int r = kColLanes * j + sub;
+      S[j] *= sA[r];
+      pp = fmaf(S[j], sK[r], pp);
+    }
+    pp += __shfl_xor_sync(0xffffffffu, pp, 1);
+    pp += __shfl_xor_sync(0xffffffffu, pp, 2);
+    const float ku = kn * (sBeta * (vv - kn * pp));  // S <- S + k_hat u^T, k_hat = kn k
+    float oo = 0.f;
+#pragma unroll
+    for (int j = 0; j < kRegRows; ++j) {
+      const int r = kColLanes * j + sub;
+      S[j] = fmaf(sK[r], ku, S[j]);
+      oo = fmaf(S[j], sQ[r], oo);
+    }
+    oo += __shfl_xor_sync(0xffffffffu, oo, 1);
+    oo += __shfl_xor_sync(0xffffffffu, oo, 2);
+    if (sub == 0 && cv) go[(t * HV + hv) * (int64_t)V + col] = from_f32<Tin>(qn * oo);
+    __syncthreads();  // the next token rewrites the shared vectors
+  }
+  if (a.final_state != nullptr && cv) {
+#pragma unroll
+    for (int j = 0; j < kRegRows; ++j) {
+      const int r = kColLanes * j + sub;
+      if (r < K) a.final_state[sidx(r)] = S[j];
+    }
+  }
+}
+
 }  // namespace
 
 size_t recurrent_smem_bytes(int K) {
@@ -154,6 +289,24 @@ size_t recurrent_smem_bytes(int K) {
 
 cudaError_t launch_recurrent(const FwdArgs& a, cudaStream_t s) {
   const Plan& p = a.plan;
+  if (p.K <= kColLanes * kRegRows) {  // state in registers
+    const int nvr = (p.V + kRegCols - 1) / kRegCols;
+    const size_t blocks = (size_t)p.N * p.HV * nvr;
+    if (blocks == 0) return cudaSuccess;
+    const bool fixed = p.K == 128 && p.V == 128 && !a.state_v_first;
+    if (a.dtype == KDA_BF16) {
+      if (fixed)
+        recurrent_reg_kernel<__nv_bfloat16, true><<<(unsigned)blocks, kThreads, 0, s>>>(a);
+      else
+        recurrent_reg_kernel<__nv_bfloat16, false><<<(unsigned)blocks, kThreads, 0, s>>>(a);
+    } else {
+      if (fixed)
+        recurrent_reg_kernel<float, true><<<(unsigned)blocks, kThreads, 0, s>>>(a);
+      else
+        recurrent_reg_kernel<float, false><<<(unsigned)blocks, kThreads, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+  }
   const int nvt = (p.V + kTile - 1) / kTile;
   const size_t blocks = (size_t)p.N * p.HV * nvt;
   if (blocks == 0) return cudaSuccess;
