@@ -150,8 +150,8 @@ constexpr uint32_t P_BSUM = P_BETA + 256;         // fp32 [4][128] block sums of
 constexpr uint32_t P_ROWSQ = P_BSUM + 2048;       // fp32 [64 rows][2 halves][2 (q,k)], then norms [64][2]
 constexpr uint32_t P_DT = P_ROWSQ + 1536;         // fp32 [128] dt_bias row
 constexpr uint32_t P_FLAG = P_DT + 512;
-constexpr uint32_t P_BAR = P_FLAG + 16;           // [0] tile loads, [1] MMA completions
-constexpr uint32_t P_TMEM = P_BAR + 16;
+constexpr uint32_t P_BAR = P_FLAG + 16;  // [0] g + dt_bias loads, [1] MMA completions, [2] q, k loads
+constexpr uint32_t P_TMEM = P_BAR + 32;
 constexpr uint32_t P_END = P_TMEM + 16;
 constexpr uint32_t P_SMEM = P_END + 1024;
 // Ka_I (16(I+1) rows) starts at row 8 I (I+1) of the B operand; its accumulator D_I at the
@@ -224,24 +224,27 @@ __global__ void __launch_bounds__(256, 2)
     tmem_alloc(sTmem, 256);
     tmem_relinquish();
   }
-  if (tid == 32) {  // tile loads: q, k -> [Qs; Ks] row blocks, g -> 2 panels, dt_bias row
+  if (tid == 32) {  // tile loads: g -> 2 panels and the dt_bias row first (the gate phase
+                    // needs only them), then q, k -> [Qs; Ks] row blocks on their own barrier
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
+    mbar_init(&bars[2], 1);
     fence_mbar_init();
     sFlag[0] = 0;
     const int32_t tt = (int32_t)t0;
-    mbar_arrive_expect_tx(&bars[0], 49152u + (has_dt ? TC_K * 4u : 0u));
+    mbar_arrive_expect_tx(&bars[0], 16384u + (has_dt ? TC_K * 4u : 0u));
+    tma_load_3d(sm + P_X, &gmap, 0, hv, tt, &bars[0]);
+    tma_load_3d(sm + P_X + 8192, &gmap, 64, hv, tt, &bars[0]);
+    if (has_dt) bulk_g2s(sDt, a.dt_bias + (size_t)hv * TC_K, TC_K * 4, &bars[0]);
+    mbar_arrive_expect_tx(&bars[2], 32768u);
 #pragma unroll
     for (int pn = 0; pn < 2; ++pn)  // 16-token boxes: queries and keys of each row block
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         uint8_t* dst = sm + P_QK + pn * 16384 + b * 4096;
-        tma_load_3d(dst, &qmap, 64 * pn, h, tt + 16 * b, &bars[0]);
-        tma_load_3d(dst + 2048, &kmap, 64 * pn, h, tt + 16 * b, &bars[0]);
+        tma_load_3d(dst, &qmap, 64 * pn, h, tt + 16 * b, &bars[2]);
+        tma_load_3d(dst + 2048, &kmap, 64 * pn, h, tt + 16 * b, &bars[2]);
       }
-    tma_load_3d(sm + P_X, &gmap, 0, hv, tt, &bars[0]);
-    tma_load_3d(sm + P_X + 8192, &gmap, 64, hv, tt, &bars[0]);
-    if (has_dt) bulk_g2s(sDt, a.dt_bias + (size_t)hv * TC_K, TC_K * 4, &bars[0]);
   }
   for (int i = tid; i < 4 * 2 * 256; i += 256) sDiag[i] = 0.f;  // exact diagonal blocks
   // beta is read here and published to shared memory only after the tile wait, so that
@@ -255,13 +258,12 @@ __global__ void __launch_bounds__(256, 2)
   tc_fence_after();
   const uint32_t tmem = *sTmem;
   if (!mbar_wait(&bars[0], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
-  if (L < TC_C) {  // a short chunk: its q, k and g rows past L (the next sequence's tokens or
-                   // the copy's fill) become zero, so that no later load needs a row mask
-    for (int e = tid; e < (TC_C - L) * 48; e += 256) {
-      const int t = L + e / 48, x = e % 48, pn = x / 24, w = x % 24, rk = w >> 3, ch = w & 7;
-      const uint32_t row = rk == 0 ? q_row(t) : (rk == 1 ? k_row(t) : (uint32_t)t);
-      uint8_t* base = rk < 2 ? sm + P_QK + pn * 16384 : sm + P_X + pn * 8192;
-      sts_v4(base, row * 128 + ch * 16, 0u, 0u, 0u, 0u);
+  // A short chunk: its q, k and g rows past L (the next sequence's tokens or the copy's fill)
+  // become zero once, so that no later load needs a row mask.
+  if (L < TC_C) {
+    for (int e = tid; e < (TC_C - L) * 16; e += 256) {  // g: 2 panels x 8 pieces per token
+      const int t = L + (e >> 4), pn = (e >> 3) & 1, ch = e & 7;
+      sts_v4(sm + P_X + pn * 8192, (uint32_t)t * 128 + ch * 16, 0u, 0u, 0u, 0u);
     }
     __syncthreads();
   }
@@ -312,6 +314,14 @@ __global__ void __launch_bounds__(256, 2)
     float b = __bfloat162float(beta_raw);
     if (a.beta_sigmoid && tid < L) b = (a.allow_neg_eigval ? 2.f : 1.f) * sigmoid_fast(b);
     sBeta[tid] = b;
+  }
+  if (!mbar_wait(&bars[2], 0)) flag_status(a.status, KDA_DEV_TIMEOUT);
+  if (L < TC_C) {  // q, k: 2 panels x (query row, key row) x 8 pieces per token
+    for (int e = tid; e < (TC_C - L) * 32; e += 256) {
+      const int t = L + (e >> 5), pn = (e >> 4) & 1, rk = (e >> 3) & 1, ch = e & 7;
+      sts_v4(sm + P_QK + pn * 16384, (rk ? k_row(t) : q_row(t)) * 128 + ch * 16, 0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
   }
   // row sums of squares of q and k over the warp's 64 channels: a butterfly that halves
   // the rows each lane carries at every step (16 shuffles per tile instead of 80); at the
