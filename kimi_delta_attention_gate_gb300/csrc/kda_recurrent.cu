@@ -157,18 +157,15 @@ constexpr int kColLanes = 4;                   // lanes per V column
 constexpr int kRegRows = 32;                   // K rows per lane (K <= kColLanes * kRegRows)
 constexpr int kRegCols = kThreads / kColLanes;  // V columns per CTA
 
-// FIXED: K = V = 128 and the [K][V] state layout, so that every state row offset is a
-// compile-time immediate (few address registers: three CTAs per SM keep more state reads in
-// flight); otherwise K, V and the layout are read from the arguments.
-template <typename Tin, bool FIXED>
-__global__ void __launch_bounds__(kThreads, FIXED ? 3 : 2) recurrent_reg_kernel(const FwdArgs a) {
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads, 2) recurrent_reg_kernel(const FwdArgs a) {
   __shared__ float sQ[kColLanes * kRegRows], sK[kColLanes * kRegRows];  // raw q, k
   __shared__ float sA[kColLanes * kRegRows];                            // decay
   __shared__ float sPart[2][kWarps];                                       // sums of squares
   __shared__ float sBeta;
   const Plan& p = a.plan;
-  const int K = FIXED ? 128 : p.K, V = FIXED ? 128 : p.V, HV = p.HV, H = p.H;
-  const bool v_first = FIXED ? false : (bool)a.state_v_first;
+  const int K = p.K, V = p.V, HV = p.HV, H = p.H;
+  const bool v_first = a.state_v_first;
   const int nvt = (V + kRegCols - 1) / kRegCols;
   const int vt = (int)(blockIdx.x % nvt);
   const int hv = (int)((blockIdx.x / nvt) % HV);
@@ -281,6 +278,142 @@ __global__ void __launch_bounds__(kThreads, FIXED ? 3 : 2) recurrent_reg_kernel(
   }
 }
 
+// K = V = 128 with the [K][V] state layout (the decode shape): one CTA per (sequence, value
+// head).  Warp w holds columns 16w..16w+15; lane = 4 x row lane rl + column group cg owns
+// columns 16w + 4cg .. +3 of rows 8j + rl (j < 16), so that every state access moves 16 bytes
+// and a warp instruction covers 8 rows x 64 contiguous bytes; reductions over K are three
+// shuffles (lane bits 2-4) per column.
+constexpr int kVecRows = 16;  // rows per lane
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads, 2) recurrent_k128_kernel(const FwdArgs a) {
+  constexpr int K = 128, V = 128;
+  __shared__ float sQ[K], sK[K], sA[K];
+  __shared__ float sPart[2][kWarps];
+  __shared__ float sBeta;
+  const Plan& p = a.plan;
+  const int HV = p.HV, H = p.H;
+  const int hv = (int)(blockIdx.x % HV);
+  const int n = (int)(blockIdx.x / HV);
+  const int h = hv / p.G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rl = lane >> 2, c0 = 16 * warp + 4 * (lane & 3);
+  int64_t bos, eos;
+  if (p.varlen) {
+    bos = a.cu_seqlens[n];
+    eos = a.cu_seqlens[n + 1];
+  } else {
+    bos = (int64_t)n * p.T;
+    eos = bos + p.T;
+  }
+  if (bos < 0 || eos < bos || eos > p.ntok) {
+    if (tid == 0) flag_status(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const Tin* gq = static_cast<const Tin*>(a.q);
+  const Tin* gk = static_cast<const Tin*>(a.k);
+  const Tin* gv = static_cast<const Tin*>(a.v);
+  const Tin* gg = static_cast<const Tin*>(a.g);
+  const Tin* gb = static_cast<const Tin*>(a.beta);
+  Tin* go = static_cast<Tin*>(a.o);
+  const size_t state_base = ((size_t)n * HV + hv) * (size_t)K * V + (size_t)rl * V + c0;
+  float4 S[kVecRows];  // rows 8j + rl, columns c0..c0+3
+#pragma unroll
+  for (int j = 0; j < kVecRows; ++j)
+    S[j] = a.h0 != nullptr
+               ? *reinterpret_cast<const float4*>(a.h0 + state_base + (size_t)8 * j * V)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float a_exp = (a.gate_mode != KDA_GATE_PREGATED && a.A_log != nullptr) ? expf(a.A_log[hv]) : 1.f;
+
+  for (int64_t t = bos; t < eos; ++t) {
+    float qi = 0.f, ki = 0.f;
+    if (tid < K) {
+      qi = to_f32(gq[(t * H + h) * (int64_t)K + tid]);
+      ki = to_f32(gk[(t * H + h) * (int64_t)K + tid]);
+      const float gi = to_f32(gg[(t * HV + hv) * (int64_t)K + tid]);
+      const float dt = (a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED)
+                           ? a.dt_bias[(size_t)hv * K + tid] : 0.f;
+      sQ[tid] = qi;
+      sK[tid] = ki;
+      sA[tid] = expf(gate_exact(a.gate_mode, gi, a_exp, dt, a.lower_bound));
+    }
+    float vv[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) vv[x] = to_f32(gv[(t * HV + hv) * (int64_t)V + c0 + x]);
+    if (a.qk_l2norm) {
+      const float sq = warp_sum_all(qi * qi), sk = warp_sum_all(ki * ki);
+      if (lane == 0) {
+        sPart[0][warp] = sq;
+        sPart[1][warp] = sk;
+      }
+    }
+    if (tid == 0) {
+      float b = to_f32(gb[t * HV + hv]);
+      if (a.beta_sigmoid) b = (a.allow_neg_eigval ? 2.f : 1.f) * sigmoid_exact(b);
+      sBeta = b;
+    }
+    __syncthreads();
+    float qn = a.scale, kn = 1.f;
+    if (a.qk_l2norm) {
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        sq += sPart[0][w];
+        sk += sPart[1][w];
+      }
+      qn *= rsqrtf(sq + 1e-6f);
+      kn = rsqrtf(sk + 1e-6f);
+    }
+    // S <- Diag(alpha) S and S^T k over this lane's rows, then over the 8 row lanes
+    float pp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < kVecRows; ++j) {
+      const int r = 8 * j + rl;
+      const float al = sA[r], kr = sK[r];
+      S[j].x *= al; S[j].y *= al; S[j].z *= al; S[j].w *= al;
+      pp[0] = fmaf(S[j].x, kr, pp[0]);
+      pp[1] = fmaf(S[j].y, kr, pp[1]);
+      pp[2] = fmaf(S[j].z, kr, pp[2]);
+      pp[3] = fmaf(S[j].w, kr, pp[3]);
+    }
+    float ku[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) pp[x] += __shfl_xor_sync(0xffffffffu, pp[x], o);
+      ku[x] = kn * (sBeta * (vv[x] - kn * pp[x]));  // S <- S + k_hat u^T, k_hat = kn k
+    }
+    float oo[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < kVecRows; ++j) {
+      const int r = 8 * j + rl;
+      const float kr = sK[r], qr = sQ[r];
+      S[j].x = fmaf(kr, ku[0], S[j].x);
+      S[j].y = fmaf(kr, ku[1], S[j].y);
+      S[j].z = fmaf(kr, ku[2], S[j].z);
+      S[j].w = fmaf(kr, ku[3], S[j].w);
+      oo[0] = fmaf(S[j].x, qr, oo[0]);
+      oo[1] = fmaf(S[j].y, qr, oo[1]);
+      oo[2] = fmaf(S[j].z, qr, oo[2]);
+      oo[3] = fmaf(S[j].w, qr, oo[3]);
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) oo[x] += __shfl_xor_sync(0xffffffffu, oo[x], o);
+    }
+    if (rl == 0) {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) go[(t * HV + hv) * (int64_t)V + c0 + x] = from_f32<Tin>(qn * oo[x]);
+    }
+    __syncthreads();  // the next token rewrites the shared vectors
+  }
+  if (a.final_state != nullptr) {
+#pragma unroll
+    for (int j = 0; j < kVecRows; ++j)
+      *reinterpret_cast<float4*>(a.final_state + state_base + (size_t)8 * j * V) = S[j];
+  }
+}
+
 }  // namespace
 
 size_t recurrent_smem_bytes(int K) {
@@ -293,18 +426,18 @@ cudaError_t launch_recurrent(const FwdArgs& a, cudaStream_t s) {
     const int nvr = (p.V + kRegCols - 1) / kRegCols;
     const size_t blocks = (size_t)p.N * p.HV * nvr;
     if (blocks == 0) return cudaSuccess;
-    const bool fixed = p.K == 128 && p.V == 128 && !a.state_v_first;
-    if (a.dtype == KDA_BF16) {
-      if (fixed)
-        recurrent_reg_kernel<__nv_bfloat16, true><<<(unsigned)blocks, kThreads, 0, s>>>(a);
+    if (p.K == 128 && p.V == 128 && !a.state_v_first) {  // 16-byte state accesses
+      const unsigned nb = (unsigned)((size_t)p.N * p.HV);
+      if (a.dtype == KDA_BF16)
+        recurrent_k128_kernel<__nv_bfloat16><<<nb, kThreads, 0, s>>>(a);
       else
-        recurrent_reg_kernel<__nv_bfloat16, false><<<(unsigned)blocks, kThreads, 0, s>>>(a);
-    } else {
-      if (fixed)
-        recurrent_reg_kernel<float, true><<<(unsigned)blocks, kThreads, 0, s>>>(a);
-      else
-        recurrent_reg_kernel<float, false><<<(unsigned)blocks, kThreads, 0, s>>>(a);
+        recurrent_k128_kernel<float><<<nb, kThreads, 0, s>>>(a);
+      return cudaGetLastError();
     }
+    if (a.dtype == KDA_BF16)
+      recurrent_reg_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, s>>>(a);
+    else
+      recurrent_reg_kernel<float><<<(unsigned)blocks, kThreads, 0, s>>>(a);
     return cudaGetLastError();
   }
   const int nvt = (p.V + kTile - 1) / kTile;
