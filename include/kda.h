@@ -165,9 +165,10 @@ kda_status kda_fwd_host(const kda_fwd_params* p, void* arena, size_t arena_bytes
    S <- S + beta k (v - S^T k)^T, o = scale S^T q, the state read from h0 (or 0)
    and written to final_state.  Same parameters, checks, layouts and outputs as
    kda_fwd, except: chunk_size and the workspace are not used (no workspace is
-   needed), and h_out must be NULL.  fp32 arithmetic on every dtype.  One CTA per
-   (sequence, value head, 32 columns of V), tokens in order.  Asynchronous on
-   `stream`. */
+   needed), and h_out must be NULL.  fp32 arithmetic on every dtype.  Each CTA
+   owns one (sequence, value head) and a range of V columns (all 128 of them for
+   K = V = 128), processes the tokens in order and keeps the state in registers
+   (K <= 128) or shared memory (K > 128).  Asynchronous on `stream`. */
 kda_status kda_fused_recurrent_fwd(const kda_fwd_params* p, void* stream);
 
 /* Number of chunks over all sequences, the first dimension of h_out (0 if the
