@@ -306,3 +306,43 @@ def test_intermediate_states(dtype, K, T, transposed):
     assert hs.shape == rhs.shape == ((T + 63) // 64, wl.HV) + rfs.shape[2:]
     assert_close(hs.cpu().double().numpy(), rhs, dtype, "intermediate states")
     assert_close(o.float().cpu().double().numpy(), ro, dtype, "o")
+
+
+# ---- CUDA graph capture -------------------------------------------------------------------------
+
+def test_pipelined_schedule_replays_from_a_cuda_graph():
+    """The pipelined schedule (internal streams joined back by events) captures into a CUDA
+    graph; replays with new inputs copied into the captured buffers give bit for bit what direct
+    calls give."""
+    import torch
+    import kimi_delta_attention_gate_gb300 as kda
+    from kda_testlib import f32_device, gate_kwargs, to_device
+    wl = tc(T=64 * 256 + 37, seed=700)
+    inps = [kin.make_inputs(wl), kin.make_inputs(tc(T=64 * 256 + 37, seed=701))]
+    dev = [tuple(to_device(x, "bf16") for x in (i.q, i.k, i.v, i.g, i.beta)) for i in inps]
+    q, k, v, g, b = (x.clone() for x in dev[0])
+    A, dt, h0 = f32_device(inps[0].A_log), f32_device(inps[0].dt_bias), f32_device(inps[0].h0)
+    o = torch.empty_like(v)
+    fs = torch.empty(h0.shape, dtype=torch.float32, device="cuda")
+    p = kda.make_params(q, k, v, g, b, A_log=A, dt_bias=dt, scale=inps[0].scale, initial_state=h0,
+                        final_state=fs, o=o, **gate_kwargs(wl))
+    ws = torch.empty(kda.kda_fwd_workspace_size(p), dtype=torch.uint8, device="cuda")
+    call = dict(A_log=A, dt_bias=dt, scale=inps[0].scale, initial_state=h0, workspace=ws, o=o,
+                final_state=fs, **gate_kwargs(wl))
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        kda.kda_fwd(q, k, v, g, b, **call)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        kda.kda_fwd(q, k, v, g, b, **call)
+    for src in dev:
+        for dst, x in zip((q, k, v, g, b), src):
+            dst.copy_(x)
+        graph.replay()
+        torch.cuda.synchronize()
+        go, gfs = o.clone(), fs.clone()
+        ro, rfs = kda.kda_fwd(*src, **{**call, "o": None, "final_state": None})
+        torch.cuda.synchronize()
+        assert torch.equal(go, ro) and torch.equal(gfs, rfs)
+    assert kda.kda_get_device_status(0) == 0
