@@ -146,9 +146,9 @@ constexpr uint32_t KA_PANEL = 20480;
 constexpr uint32_t P_DIAG = P_KA + 2 * KA_PANEL;  // fp32 [4][2][16][16] exact diagonal blocks;
                                                   // later solve scratch Y [32][32]
 constexpr uint32_t P_BETA = P_DIAG + 8192;        // fp32 [64]
-constexpr uint32_t P_BSUM = P_BETA + 256;         // fp32 [4][128] block sums of the gate
-constexpr uint32_t P_ROWSQ = P_BSUM + 2048;       // fp32 [64 rows][2 halves][2 (q,k)], then norms [64][2]
-constexpr uint32_t P_DT = P_ROWSQ + 1536;         // fp32 [128] dt_bias row
+constexpr uint32_t P_BSUM = P_BETA + 256;         // fp32 [8][128] half-block sums of the gate
+constexpr uint32_t P_NORM = P_BSUM + 4096;        // fp32 [64 rows][2]: q (with scale), k multipliers
+constexpr uint32_t P_DT = P_NORM + 512;           // fp32 [128] dt_bias row
 constexpr uint32_t P_FLAG = P_DT + 512;
 constexpr uint32_t P_BAR = P_FLAG + 16;  // [0] g + dt_bias loads, [1] MMA completions, [2] q, k loads
 constexpr uint32_t P_TMEM = P_BAR + 32;
@@ -162,6 +162,12 @@ __host__ __device__ constexpr uint32_t q_row(int t) { return 32u * (uint32_t)(t 
 __host__ __device__ constexpr uint32_t k_row(int t) { return q_row(t) + 16u; }
 constexpr int SOLVE_LD = 65;
 
+__device__ __forceinline__ uint2 lds_u64(const uint8_t* base, uint32_t off) {
+  return *reinterpret_cast<const uint2*>(base + off);
+}
+__device__ __forceinline__ void sts_u64(uint8_t* base, uint32_t off, uint32_t a, uint32_t b) {
+  *reinterpret_cast<uint2*>(base + off) = make_uint2(a, b);
+}
 __device__ __forceinline__ uint32_t lds_u32(const uint8_t* base, uint32_t off) {
   return *reinterpret_cast<const uint32_t*>(base + off);
 }
@@ -210,7 +216,7 @@ __global__ void __launch_bounds__(256, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float* sBeta = reinterpret_cast<float*>(sm + P_BETA);
   float* sBsum = reinterpret_cast<float*>(sm + P_BSUM);
-  float* sRowsq = reinterpret_cast<float*>(sm + P_ROWSQ);
+  float* sNorm = reinterpret_cast<float*>(sm + P_NORM);
   float* sDiag = reinterpret_cast<float*>(sm + P_DIAG);
   float* sDt = reinterpret_cast<float*>(sm + P_DT);
   int* sFlag = reinterpret_cast<int*>(sm + P_FLAG);
@@ -268,48 +274,60 @@ __global__ void __launch_bounds__(256, 2)
     __syncthreads();
   }
 
-  // ---- element-wise phase: thread = 16-row block rg x channel pair (c0, c0+1) ----
-  const int rg = tid >> 6, cp = tid & 63, c0 = 2 * cp;
-  const uint32_t pan = (uint32_t)(c0 >> 6);  // panel of this channel pair
+  // ---- element-wise phases: thread = 8-row half block hb (of 16-row block rg) x channels
+  // c0..c0+3 (pairs A = c0, c0+1 and B = c0+2, c0+3); warp hb holds all 128 channels of its
+  // rows, so that row norms reduce inside the warp ----
+  const int hb = tid >> 5, rg = hb >> 1, c0 = 4 * lane;
+  const uint32_t pan = (uint32_t)(c0 >> 6);  // panel of these channels
   const uint32_t cc = (uint32_t)(c0 & 63);
   uint8_t* qk_pan = sm + P_QK + pan * 16384;
   uint8_t* x_pan = sm + P_X + pan * 8192;
-  float dt0 = 0.f, dt1 = 0.f;
+  float2 dtA = make_float2(0.f, 0.f), dtB = make_float2(0.f, 0.f);
   if (has_dt) {
-    dt0 = sDt[c0];
-    dt1 = sDt[c0 + 1];
+    const float4 d4 = *reinterpret_cast<const float4*>(sDt + c0);
+    dtA = make_float2(d4.x, d4.y);
+    dtB = make_float2(d4.z, d4.w);
   }
-  // gate + in-block cumsum (log2 units); G <= 0 for every non-positive gate
-  float G0[16], G1[16];
-  float acc0 = 0.f, acc1 = 0.f, span = 0.f;
+  // gate + in-half-block cumsum (log2 units); G <= 0 for every non-positive gate
+  float2 GA[8], GB[8];
+  float2 accA = make_float2(0.f, 0.f), accB = make_float2(0.f, 0.f);
+  float span = 0.f;
   const float zsc = -kLog2e * aexp;  // safe gate: 2^(zsc (g + dt)) = e^(-aexp (g + dt))
+  const float2 zsc2 = make_float2(zsc, zsc), lb2 = make_float2(lb, lb);
+  const float2 one2 = make_float2(1.f, 1.f), l2e2 = make_float2(kLog2e, kLog2e);
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int row = 16 * rg + r;
-    float2 gp = make_float2(0.f, 0.f);
+  for (int r = 0; r < 8; ++r) {
+    const int row = 8 * hb + r;
+    float2 gpA = make_float2(0.f, 0.f), gpB = make_float2(0.f, 0.f);
     if (row < L) {
-      const uint32_t gv = lds_u32(x_pan, sw128_offset(row, cc));
-      if (GATE == KDA_GATE_SAFE) {  // lb sigmoid(a x) on the channel pair
-        const float2 z = mul2(add2(bf_pair(gv), make_float2(dt0, dt1)), make_float2(zsc, zsc));
-        const float2 d = add2(make_float2(ex2(z.x), ex2(z.y)), make_float2(1.f, 1.f));
-        gp = mul2(make_float2(rcp_approx(d.x), rcp_approx(d.y)), make_float2(lb, lb));
+      const uint2 gv = lds_u64(x_pan, sw128_offset(row, cc));
+      if (GATE == KDA_GATE_SAFE) {  // lb sigmoid(a x) on the two channel pairs
+        const float2 zA = mul2(add2(bf_pair(gv.x), dtA), zsc2);
+        const float2 zB = mul2(add2(bf_pair(gv.y), dtB), zsc2);
+        const float2 dA = add2(make_float2(ex2(zA.x), ex2(zA.y)), one2);
+        const float2 dB = add2(make_float2(ex2(zB.x), ex2(zB.y)), one2);
+        gpA = mul2(make_float2(rcp_approx(dA.x), rcp_approx(dA.y)), lb2);
+        gpB = mul2(make_float2(rcp_approx(dB.x), rcp_approx(dB.y)), lb2);
       } else {
-        gp.x = gate_fast<GATE>(bf_lo(gv) + dt0, aexp, lb);
-        gp.y = gate_fast<GATE>(bf_hi(gv) + dt1, aexp, lb);
+        gpA.x = gate_fast<GATE>(bf_lo(gv.x) + dtA.x, aexp, lb);
+        gpA.y = gate_fast<GATE>(bf_hi(gv.x) + dtA.y, aexp, lb);
+        gpB.x = gate_fast<GATE>(bf_lo(gv.y) + dtB.x, aexp, lb);
+        gpB.y = gate_fast<GATE>(bf_hi(gv.y) + dtB.y, aexp, lb);
       }
     }
-    const float2 acc = fma2(gp, make_float2(kLog2e, kLog2e), make_float2(acc0, acc1));
-    acc0 = acc.x;
-    acc1 = acc.y;
-    G0[r] = acc0;
-    G1[r] = acc1;
-    // a gate that is never positive makes the cumsum monotone: its last value is the span
-    if (GATE == KDA_GATE_PREGATED) span = fmaxf(span, fmaxf(fabsf(acc0), fabsf(acc1)));
+    accA = fma2(gpA, l2e2, accA);
+    accB = fma2(gpB, l2e2, accB);
+    GA[r] = accA;
+    GB[r] = accB;
+    if (GATE == KDA_GATE_PREGATED)
+      span = fmaxf(span, fmaxf(fmaxf(fabsf(accA.x), fabsf(accA.y)), fmaxf(fabsf(accB.x), fabsf(accB.y))));
   }
-  if (GATE != KDA_GATE_PREGATED) span = fmaxf(fabsf(acc0), fabsf(acc1));
-  sBsum[rg * 128 + c0] = acc0;
-  sBsum[rg * 128 + c0 + 1] = acc1;
-  if (span > kGuardLog2) atomicOr(sFlag, 1 << rg);
+  // a gate that is never positive makes the cumsum monotone: its last value is the span
+  if (GATE != KDA_GATE_PREGATED)
+    span = fmaxf(fmaxf(fabsf(accA.x), fabsf(accA.y)), fmaxf(fabsf(accB.x), fabsf(accB.y)));
+  *reinterpret_cast<float4*>(sBsum + hb * 128 + c0) = make_float4(accA.x, accA.y, accB.x, accB.y);
+  // both halves within 2^60 keep the block's in-block decay within 2^120
+  if (span > 0.5f * kGuardLog2) atomicOr(sFlag, 1 << rg);
   if (tid < TC_C) {
     float b = __bfloat162float(beta_raw);
     if (a.beta_sigmoid && tid < L) b = (a.allow_neg_eigval ? 2.f : 1.f) * sigmoid_fast(b);
@@ -323,146 +341,167 @@ __global__ void __launch_bounds__(256, 2)
     }
     __syncthreads();
   }
-  // row sums of squares of q and k over the warp's 64 channels: a butterfly that halves
-  // the rows each lane carries at every step (16 shuffles per tile instead of 80); at the
-  // end lanes 2m and 2m+1 hold the sum of row rsel(m)
+  // row sums of squares of q and k over all 128 channels inside the warp: a butterfly that
+  // halves the rows each lane carries (lane bits 16, 8, 4), then sums over lane bits 2 and 1;
+  // lane 4m ends with row 8 hb + m and publishes its multipliers
   {
-    float sq[16], sk[16];
+    float sq[8], sk[8];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const int row = 16 * rg + r;
-      const uint32_t qv = lds_u32(qk_pan, sw128_offset(q_row(row), cc));
-      const uint32_t kv = lds_u32(qk_pan, sw128_offset(k_row(row), cc));
-      sq[r] = bf_lo(qv) * bf_lo(qv) + bf_hi(qv) * bf_hi(qv);
-      sk[r] = bf_lo(kv) * bf_lo(kv) + bf_hi(kv) * bf_hi(kv);
+    for (int r = 0; r < 8; ++r) {
+      const int row = 8 * hb + r;
+      const uint2 qv = lds_u64(qk_pan, sw128_offset(q_row(row), cc));
+      const uint2 kv = lds_u64(qk_pan, sw128_offset(k_row(row), cc));
+      const float2 qa = bf_pair(qv.x), qb = bf_pair(qv.y), ka = bf_pair(kv.x), kb = bf_pair(kv.y);
+      sq[r] = fmaf(qa.x, qa.x, fmaf(qa.y, qa.y, fmaf(qb.x, qb.x, qb.y * qb.y)));
+      sk[r] = fmaf(ka.x, ka.x, fmaf(ka.y, ka.y, fmaf(kb.x, kb.x, kb.y * kb.y)));
     }
 #pragma unroll
-    for (int hw = 8; hw >= 1; hw >>= 1) {  // keep rows [hw, 2hw) if the lane bit is set
-      const bool up = (lane & (2 * hw)) != 0;
+    for (int hw = 4; hw >= 1; hw >>= 1) {  // keep rows [hw, 2hw) if the lane bit is set
+      const bool up = (lane & (4 * hw)) != 0;
 #pragma unroll
       for (int x = 0; x < hw; ++x) {
         const float qs = up ? sq[x] : sq[x + hw], ks = up ? sk[x] : sk[x + hw];
         const float qk_ = up ? sq[x + hw] : sq[x], kk_ = up ? sk[x + hw] : sk[x];
-        sq[x] = qk_ + __shfl_xor_sync(0xffffffffu, qs, 2 * hw);
-        sk[x] = kk_ + __shfl_xor_sync(0xffffffffu, ks, 2 * hw);
+        sq[x] = qk_ + __shfl_xor_sync(0xffffffffu, qs, 4 * hw);
+        sk[x] = kk_ + __shfl_xor_sync(0xffffffffu, ks, 4 * hw);
       }
     }
-    sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 1);
-    sk[0] += __shfl_xor_sync(0xffffffffu, sk[0], 1);
-    if ((lane & 1) == 0) {
-      const int row = 16 * rg + ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 +
-                      ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-      sRowsq[(row * 2 + (warp & 1)) * 2 + 0] = sq[0];
-      sRowsq[(row * 2 + (warp & 1)) * 2 + 1] = sk[0];
+#pragma unroll
+    for (int o = 2; o >= 1; o >>= 1) {
+      sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], o);
+      sk[0] += __shfl_xor_sync(0xffffffffu, sk[0], o);
+    }
+    if ((lane & 3) == 0) {
+      const int row = 8 * hb + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+      float qn = a.scale, kn = 1.f;
+      if (a.qk_l2norm) {
+        qn *= rsqrtf(sq[0] + 1e-6f);
+        kn = rsqrtf(sk[0] + 1e-6f);
+      }
+      *reinterpret_cast<float2*>(sNorm + 2 * row) = make_float2(qn, kn);
     }
   }
-  __syncthreads();
-  float* sNorm = sRowsq + 64 * 4;  // [64 rows][2]: q multiplier (with scale), k multiplier
-  if (tid < 64) {
-    const float* rq = sRowsq + tid * 4;
-    float qn = a.scale, kn = 1.f;
-    if (a.qk_l2norm) {
-      qn *= rsqrtf(rq[0] + rq[2] + 1e-6f);
-      kn = rsqrtf(rq[1] + rq[3] + 1e-6f);
-    }
-    sNorm[2 * tid] = qn;
-    sNorm[2 * tid + 1] = kn;
-  }
-  __syncthreads();
+  __syncthreads();  // half-block sums, exact-diagonal flags, row multipliers
 
   // ---- carries, factors, operand tiles ----
-  float rI0[4], rI1[4];  // reference r_I = Gamma just before block I
-  rI0[0] = rI1[0] = 0.f;
+  // block references r_I = Gamma just before block I and gamma_C, summed from the half-block
+  // sums; G made relative to the start of block rg
+  float4 rI[4], gl;
+  {
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f), cy = run;
 #pragma unroll
-  for (int b = 1; b < 4; ++b) {
-    rI0[b] = rI0[b - 1] + sBsum[(b - 1) * 128 + c0];
-    rI1[b] = rI1[b - 1] + sBsum[(b - 1) * 128 + c0 + 1];
-  }
-  const float gl0 = rI0[3] + sBsum[3 * 128 + c0];  // gamma_C (log2)
-  const float gl1 = rI1[3] + sBsum[3 * 128 + c0 + 1];
-  const float rb0 = rI0[rg], rb1 = rI1[rg];
-  const bool guard = (sFlag[0] >> rg) & 1;
-  const float erb0 = ex2(rb0), erb1 = ex2(rb1);
-  const float ekg0 = ex2(gl0 - rb0), ekg1 = ex2(gl1 - rb1);
-  if (rg == 0)
-    *reinterpret_cast<float2*>(blk + OFF_D + 4 * c0) = make_float2(ex2(gl0), ex2(gl1));
-  float2 F[4];  // 2^(r_I - r_b) for the blocks I > rg that see this block's keys
-#pragma unroll
-  for (int I = 0; I < 4; ++I)
-    F[I] = (I > rg) ? make_float2(ex2(rI0[I] - rb0), ex2(rI1[I] - rb1)) : make_float2(1.f, 1.f);
-  const float2 erb = make_float2(erb0, erb1), ekg = make_float2(ekg0, ekg1);
-  if (sFlag[0] != 0) {  // some block needs its diagonal entries evaluated exactly
-    // the thread's gate cumsums go to a scratch row in the (not yet written) Ka tile, so
-    // that the rarely taken evaluation can run as compact loops out of line
-    float* gs = reinterpret_cast<float*>(sm + P_KA) + tid * 33;
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      gs[r] = G0[r];
-      gs[16 + r] = G1[r];
+    for (int x = 0; x < 8; ++x) {
+      if ((x & 1) == 0) rI[x >> 1] = run;
+      const float4 h4 = *reinterpret_cast<const float4*>(sBsum + x * 128 + c0);
+      if (x == hb - 1 && (hb & 1)) cy = h4;
+      run = make_float4(run.x + h4.x, run.y + h4.y, run.z + h4.z, run.w + h4.w);
     }
-    if (guard) guard_diagonal(qk_pan, cc, rg, L, gs, sNorm, sDiag + rg * 512);
+    gl = run;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      GA[r] = add2(GA[r], make_float2(cy.x, cy.y));
+      GB[r] = add2(GB[r], make_float2(cy.z, cy.w));
+    }
+  }
+  // r_b by selects (a run-time index would move rI to local memory)
+  const float4 rb = rg == 0 ? rI[0] : (rg == 1 ? rI[1] : (rg == 2 ? rI[2] : rI[3]));
+  const bool guard = (sFlag[0] >> rg) & 1;
+  const float2 erbA = make_float2(ex2(rb.x), ex2(rb.y)), erbB = make_float2(ex2(rb.z), ex2(rb.w));
+  const float2 ekgA = make_float2(ex2(gl.x - rb.x), ex2(gl.y - rb.y));
+  const float2 ekgB = make_float2(ex2(gl.z - rb.z), ex2(gl.w - rb.w));
+  if (hb == 0)
+    *reinterpret_cast<float4*>(blk + OFF_D + 4 * c0) =
+        make_float4(ex2(gl.x), ex2(gl.y), ex2(gl.z), ex2(gl.w));
+  float2 FA[4], FB[4];  // 2^(r_I - r_b) for the blocks I > rg that see this block's keys
+#pragma unroll
+  for (int I = 0; I < 4; ++I) {
+    FA[I] = (I > rg) ? make_float2(ex2(rI[I].x - rb.x), ex2(rI[I].y - rb.y)) : one2;
+    FB[I] = (I > rg) ? make_float2(ex2(rI[I].z - rb.z), ex2(rI[I].w - rb.w)) : one2;
+  }
+  if (sFlag[0] != 0) {  // some block needs its diagonal entries evaluated exactly
+    // the gate cumsums of (block, channel pair) go to a scratch row in the (not yet written)
+    // Ka tile; then thread (block tid / 64, pair tid % 64) evaluates its 16 x 16 partial sums
+    // out of line
+    const int p0 = 2 * lane;  // pairs p0 (A) and p0 + 1 (B) of this thread
+    float* gsA = reinterpret_cast<float*>(sm + P_KA) + (rg * 64 + p0) * 33;
+    float* gsB = gsA + 33;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int ri = 8 * (hb & 1) + r;
+      gsA[ri] = GA[r].x;
+      gsA[16 + ri] = GA[r].y;
+      gsB[ri] = GB[r].x;
+      gsB[16 + ri] = GB[r].y;
+    }
+    __syncthreads();
+    const int grg = tid >> 6, gp = tid & 63;
+    if ((sFlag[0] >> grg) & 1)
+      guard_diagonal(sm + P_QK + (uint32_t)((2 * gp) >> 6) * 16384, (uint32_t)((2 * gp) & 63), grg,
+                     L, reinterpret_cast<float*>(sm + P_KA) + (grg * 64 + gp) * 33, sNorm,
+                     sDiag + grg * 512);
     __syncthreads();
   }
-  // Kg^T (row = channel, 16 consecutive tokens per thread) is packed two tokens per
-  // register and written as 16-byte pieces after the loop
-  uint32_t kt0[8], kt1[8];
+  // Kg^T (row = channel, 8 consecutive tokens per thread) is packed two tokens per register
+  // and written as one 16-byte piece per channel after the loop
+  uint32_t kt[4][4];
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int row = 16 * rg + r;
-    const uint32_t qv = lds_u32(qk_pan, sw128_offset(q_row(row), cc));
-    const uint32_t kv = lds_u32(qk_pan, sw128_offset(k_row(row), cc));
+  for (int r = 0; r < 8; ++r) {
+    const int row = 8 * hb + r;
+    const uint32_t oq = sw128_offset(q_row(row), cc), ok = sw128_offset(k_row(row), cc);
+    const uint2 qv = lds_u64(qk_pan, oq), kv = lds_u64(qk_pan, ok);
     const float2 nrm = *reinterpret_cast<const float2*>(sNorm + 2 * row);  // (qn, kn)
-    const float2 qf = mul2(bf_pair(qv), make_float2(nrm.x, nrm.x));
-    const float2 kf = mul2(bf_pair(kv), make_float2(nrm.y, nrm.y));
-    const float k0 = kf.x, k1 = kf.y;
-    const float2 P = make_float2(ex2(G0[r]), ex2(G1[r]));  // 2^(Gamma - r_b) <= 1
-    const float2 qs = mul2(qf, P), ks = mul2(kf, P);
-    sts_u32(qk_pan, sw128_offset(q_row(row), cc), pack2(qs));  // Qs
-    sts_u32(qk_pan, sw128_offset(k_row(row), cc), pack2(ks));  // Ks
+    const float2 qn2 = make_float2(nrm.x, nrm.x), kn2 = make_float2(nrm.y, nrm.y);
+    const float2 kfA = mul2(bf_pair(kv.x), kn2), kfB = mul2(bf_pair(kv.y), kn2);
+    const float2 PA = make_float2(ex2(GA[r].x), ex2(GA[r].y));  // 2^(Gamma - r_b) <= 1
+    const float2 PB = make_float2(ex2(GB[r].x), ex2(GB[r].y));
+    const float2 qsA = mul2(mul2(bf_pair(qv.x), qn2), PA), qsB = mul2(mul2(bf_pair(qv.y), qn2), PB);
+    const float2 ksA = mul2(kfA, PA), ksB = mul2(kfB, PB);
+    sts_u64(qk_pan, oq, pack2(qsA), pack2(qsB));  // Qs
+    sts_u64(qk_pan, ok, pack2(ksA), pack2(ksB));  // Ks
     // Qg (rows 64-127 of B1) and X share 2^Gamma = P 2^r_b
-    sts_u32(blk + OFF_B1 + pan * 16384, sw128_offset(64 + row, cc), pack2(mul2(qs, erb)));
-    sts_u32(x_pan, sw128_offset(row, cc), pack2(mul2(ks, erb)));
-    float kg0, kg1;
+    sts_u64(blk + OFF_B1 + pan * 16384, sw128_offset(64 + row, cc), pack2(mul2(qsA, erbA)),
+            pack2(mul2(qsB, erbB)));
+    sts_u64(x_pan, sw128_offset(row, cc), pack2(mul2(ksA, erbA)), pack2(mul2(ksB, erbB)));
+    float2 kgA, kgB;
     if (!guard) {
-      const float2 E = make_float2(ex2(-G0[r]), ex2(-G1[r]));  // 2^(r_b - Gamma) <= 2^120
-      const float2 ke = mul2(kf, E);
+      // 2^(r_b - Gamma) <= 2^120
+      const float2 keA = mul2(kfA, make_float2(ex2(-GA[r].x), ex2(-GA[r].y)));
+      const float2 keB = mul2(kfB, make_float2(ex2(-GB[r].x), ex2(-GB[r].y)));
 #pragma unroll
       for (int I = 0; I < 4; ++I) {
         if (I < rg) continue;
-        sts_u32(sm + P_KA + pan * KA_PANEL, sw128_offset(ka_row(I) + row, cc),
-                pack2(mul2(ke, F[I])));  // F[rg] = 1 exactly
+        sts_u64(sm + P_KA + pan * KA_PANEL, sw128_offset(ka_row(I) + row, cc),
+                pack2(mul2(keA, FA[I])), pack2(mul2(keB, FB[I])));  // F[rg] = 1 exactly
       }
-      const float2 kg = mul2(ke, ekg);
-      kg0 = kg.x;
-      kg1 = kg.y;
+      kgA = mul2(keA, ekgA);
+      kgB = mul2(keB, ekgB);
     } else {
       // every exponent below is <= 0; the diagonal block is evaluated exactly above
 #pragma unroll
       for (int I = 0; I < 4; ++I) {
         if (I < rg) continue;
-        const float v0 = (I == rg) ? 0.f : k0 * ex2(rI0[I] - rb0 - G0[r]);
-        const float v1 = (I == rg) ? 0.f : k1 * ex2(rI1[I] - rb1 - G1[r]);
-        sts_u32(sm + P_KA + pan * KA_PANEL, sw128_offset(ka_row(I) + row, cc), pack_bf16x2(v0, v1));
+        float2 vA = make_float2(0.f, 0.f), vB = vA;
+        if (I > rg) {
+          vA = make_float2(kfA.x * ex2(rI[I].x - rb.x - GA[r].x), kfA.y * ex2(rI[I].y - rb.y - GA[r].y));
+          vB = make_float2(kfB.x * ex2(rI[I].z - rb.z - GB[r].x), kfB.y * ex2(rI[I].w - rb.w - GB[r].y));
+        }
+        sts_u64(sm + P_KA + pan * KA_PANEL, sw128_offset(ka_row(I) + row, cc), pack2(vA), pack2(vB));
       }
-      kg0 = k0 * ex2(gl0 - rb0 - G0[r]);
-      kg1 = k1 * ex2(gl1 - rb1 - G1[r]);
+      kgA = make_float2(kfA.x * ex2(gl.x - rb.x - GA[r].x), kfA.y * ex2(gl.y - rb.y - GA[r].y));
+      kgB = make_float2(kfB.x * ex2(gl.z - rb.z - GB[r].x), kfB.y * ex2(gl.w - rb.w - GB[r].y));
     }
-    if (r & 1) {
-      kt0[r >> 1] = pack_bf16x2(__uint_as_float(kt0[r >> 1]), kg0);
-      kt1[r >> 1] = pack_bf16x2(__uint_as_float(kt1[r >> 1]), kg1);
-    } else {  // hold the even row's value until its odd partner is computed
-      kt0[r >> 1] = __float_as_uint(kg0);
-      kt1[r >> 1] = __float_as_uint(kg1);
+    const float kg[4] = {kgA.x, kgA.y, kgB.x, kgB.y};
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      if (r & 1)
+        kt[x][r >> 1] = pack_bf16x2(__uint_as_float(kt[x][r >> 1]), kg[x]);
+      else  // hold the even row's value until its odd partner is computed
+        kt[x][r >> 1] = __float_as_uint(kg[x]);
     }
   }
 #pragma unroll
-  for (int hlf = 0; hlf < 2; ++hlf) {
-    const int tcol = 16 * rg + 8 * hlf;
-    sts_v4(blk + OFF_B2, sw128_offset(64 + c0, tcol), kt0[4 * hlf], kt0[4 * hlf + 1],
-           kt0[4 * hlf + 2], kt0[4 * hlf + 3]);
-    sts_v4(blk + OFF_B2, sw128_offset(65 + c0, tcol), kt1[4 * hlf], kt1[4 * hlf + 1],
-           kt1[4 * hlf + 2], kt1[4 * hlf + 3]);
-  }
+  for (int x = 0; x < 4; ++x)
+    sts_v4(blk + OFF_B2, sw128_offset(64 + c0 + x, 8 * hb), kt[x][0], kt[x][1], kt[x][2], kt[x][3]);
   fence_async_smem();
   __syncthreads();
 
