@@ -23,9 +23,10 @@
 // before the block: the query side q_i 2^(Gamma_i - r_I) <= 1 and the key side
 // k_j 2^(r_I - Gamma_j), which is <= 1 for earlier blocks and at most 2^115 inside the
 // block at lower_bound = -5 (16 tokens x 5 nat), within the fp32/bf16 exponent range.
-// A block whose in-block decay exceeds 2^120 (possible only for the plain or
-// pre-gated gate) takes its diagonal 16 x 16 entries from an exact element-wise
-// evaluation instead.
+// A block whose in-block decay could exceed 2^120 (tested as either 8-row half exceeding
+// 2^60, which never happens for the safe gate at lower_bound = -5: 8 tokens x 5 nat is
+// 2^57.7; possible for the plain or pre-gated gate) takes its diagonal 16 x 16 entries
+// from an exact element-wise evaluation instead.
 #include <cudaTypedefs.h>
 #include <stdio.h>
 
