@@ -125,7 +125,7 @@ def profiled_traffic(stage: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -140,7 +140,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -166,7 +166,8 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             rows.append((ts, parts))
-        inside = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25] or rows
+        inside = [r for r in rows if t0 <= r[0] <= t1] or \
+            [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         sm, smax, power = [], [], []
@@ -232,7 +233,10 @@ def run_reference(args, wl):
     oracle.build()
     inp = kin.make_inputs(wl)
     nthreads = oracle.max_threads()
-    tokens, heads = cpu_sample_plan(inp, 4.0, nthreads)
+    # each step a bounded sample, sized so that the warm-up and timed steps together take
+    # about two minutes of host time (at most 4 s a step)
+    per_step = min(4.0, 120.0 / max(1, args.steps + args.warmup))
+    tokens, heads = cpu_sample_plan(inp, per_step, nthreads)
     for _ in range(args.warmup):
         oracle_sample_time(inp, tokens, heads, nthreads)
     times = [oracle_sample_time(inp, tokens, heads, nthreads) for _ in range(args.steps)]
@@ -343,7 +347,7 @@ def config_of(inp: kin.Inputs, args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_bf16", choices=sorted(kin.WORKLOADS))
