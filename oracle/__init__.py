@@ -13,9 +13,12 @@ Contents
                           in "KDA reading notes: Implementation Notes for KDA in
                           FLA", written out with a dense solve (cross-check).
   * ``transition_np``  -- brute force: explicit K x K transition matrices.
+  * ``backward.bwd``   -- fp64 gradients of the forward (PyTorch autograd over the
+                          token recurrence), the reference for a backward pass.
 
-Every function is pinned by ``tests/test_oracle_pins.py`` against things the
-pages and the mathematics fix (closed forms, special cases, identities).
+Every function is pinned by ``tests/test_oracle_pins.py`` (``backward`` by
+``tests/test_oracle_backward.py``) against things the pages and the mathematics
+fix (closed forms, special cases, identities, finite differences of ``fwd``).
 """
 from .ref import (GATE_PLAIN, GATE_PREGATED, GATE_SAFE, L2_EPS, build, chunk_np, fwd, gate_c, gate_np,
                   l2norm_np, lib_path, max_threads, recurrent_np, sigmoid_np, softplus_np,

@@ -1,0 +1,118 @@
+"""Pins for the oracle's reference gradients (oracle/backward.py), all on the CPU.
+
+None compares the autograd restatement with itself: its forward is checked against the C
+oracle, its gradients against central finite differences of the C oracle's forward (independent
+code), against closed-form derivatives of one-token cases, and against linearity in the incoming
+gradient."""
+import numpy as np
+import pytest
+
+pytest.importorskip("torch")
+
+import oracle
+from oracle import GATE_PLAIN, GATE_PREGATED, GATE_SAFE
+from oracle import backward as ob
+
+
+def case(seed, B=2, T=5, H=1, HV=2, K=4, V=3, gate=GATE_SAFE):
+    r = np.random.default_rng(seed)
+    d = dict(q=r.standard_normal((B, T, H, K)), k=r.standard_normal((B, T, H, K)),
+             v=r.standard_normal((B, T, HV, V)), g=r.standard_normal((B, T, HV, K)),
+             beta=r.standard_normal((B, T, HV)), initial_state=0.3 * r.standard_normal((B, HV, K, V)),
+             dt_bias=0.5 * r.standard_normal(HV * K))
+    if gate == GATE_PREGATED:
+        d["g"] = -np.abs(d["g"]) * 0.5
+        d.pop("dt_bias")
+        opts = dict(gate_mode=GATE_PREGATED)
+    elif gate == GATE_PLAIN:
+        d["A_log"] = r.uniform(-1.0, 0.5, HV)
+        opts = dict(gate_mode=GATE_PLAIN)
+    else:
+        d["A_log"] = r.uniform(-0.5, 0.5, HV)
+        opts = dict(gate_mode=GATE_SAFE, lower_bound=-5.0)
+    do = r.standard_normal((B, T, HV, V))
+    dfinal = r.standard_normal((B, HV, K, V))
+    return d, opts, do, dfinal
+
+
+def c_loss(d, opts, do, dfinal, **extra):
+    o, fs = oracle.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], A_log=d.get("A_log"),
+                       dt_bias=d.get("dt_bias"), initial_state=d.get("initial_state"),
+                       **opts, **extra)
+    return float(np.sum(o * do) + np.sum(fs * dfinal))
+
+
+def grads(d, opts, do, dfinal, **extra):
+    return ob.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], do, dfinal, A_log=d.get("A_log"),
+                  dt_bias=d.get("dt_bias"), initial_state=d.get("initial_state"), **opts, **extra)
+
+
+NAMES = {"q": "dq", "k": "dk", "v": "dv", "g": "dg", "beta": "dbeta", "A_log": "dA_log",
+         "dt_bias": "ddt_bias", "initial_state": "dh0"}
+
+
+def test_forward_matches_the_c_oracle():
+    d, opts, do, dfinal = case(1)
+    r = grads(d, opts, do, dfinal)
+    o, fs = oracle.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], A_log=d["A_log"],
+                       dt_bias=d["dt_bias"], initial_state=d["initial_state"], **opts)
+    assert np.allclose(r["o"], o, rtol=0, atol=1e-12)
+    assert np.allclose(r["final_state"], fs, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("gate", [GATE_SAFE, GATE_PLAIN, GATE_PREGATED])
+@pytest.mark.parametrize("neg", [False, True])
+def test_directional_derivatives_match_finite_differences_of_the_c_oracle(gate, neg):
+    """<grad, delta> against (L(x + eps delta) - L(x - eps delta)) / (2 eps), L evaluated by
+    the C oracle, for a random direction in every input."""
+    extra = dict(allow_neg_eigval=True) if neg else {}
+    d, opts, do, dfinal = case(10 + gate + 3 * neg, gate=gate)
+    r = grads(d, opts, do, dfinal, **extra)
+    rng = np.random.default_rng(99)
+    eps = 1e-6
+    for name, key in NAMES.items():
+        if name not in d:
+            assert r[key] is None
+            continue
+        delta = rng.standard_normal(np.shape(d[name]))
+        plus = dict(d); plus[name] = d[name] + eps * delta
+        minus = dict(d); minus[name] = d[name] - eps * delta
+        fd = (c_loss(plus, opts, do, dfinal, **extra) - c_loss(minus, opts, do, dfinal, **extra)) / (2 * eps)
+        an = float(np.sum(r[key] * delta))
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_one_token_closed_forms():
+    """One token, K = V = 1, no norms, beta taken as given, pre-gated decay g:
+    o = s q (a S0 + b k (v - k a S0)), a = e^g."""
+    q, k, v, g, b, S0, s = 0.7, -1.3, 0.4, -0.35, 0.6, 0.9, 0.8
+    a = np.exp(g)
+    r = ob.bwd(np.full((1, 1, 1, 1), q), np.full((1, 1, 1, 1), k), np.full((1, 1, 1, 1), v),
+               np.full((1, 1, 1, 1), g), np.full((1, 1, 1), b), np.ones((1, 1, 1, 1)), None,
+               gate_mode=GATE_PREGATED, scale=s, qk_l2norm=False, beta_sigmoid=False,
+               initial_state=np.full((1, 1, 1, 1), S0))
+    expect = {"dv": s * q * b * k,
+              "dq": s * (a * S0 + b * k * (v - k * a * S0)),
+              "dbeta": s * q * k * (v - k * a * S0),
+              "dk": s * q * b * (v - 2 * k * a * S0),
+              "dg": s * q * a * S0 * (1 - b * k * k),
+              "dh0": s * q * a * (1 - b * k * k)}
+    for key, val in expect.items():
+        assert np.isclose(float(r[key].ravel()[0]), val, rtol=1e-13, atol=1e-15), key
+
+
+def test_gradients_are_linear_in_the_incoming_gradient():
+    d, opts, do1, df1 = case(21)
+    _, _, do2, df2 = case(22)
+    r1, r2 = grads(d, opts, do1, df1), grads(d, opts, do2, df2)
+    r12 = grads(d, opts, do1 + 2.0 * do2, df1 + 2.0 * df2)
+    for key in NAMES.values():
+        assert np.allclose(r12[key], r1[key] + 2.0 * r2[key], rtol=1e-12, atol=1e-12), key
+
+
+def test_final_state_gradient_alone_leaves_q_untouched():
+    """The final state does not depend on q: with do = 0 the gradient of q is exactly zero."""
+    d, opts, do, dfinal = case(31)
+    r = grads(d, opts, np.zeros_like(do), dfinal)
+    assert np.all(r["dq"] == 0)
+    assert np.any(r["dk"] != 0)
