@@ -532,6 +532,24 @@ def main():
     if status != 0:
         raise RuntimeError(f"device status {status:#x} after the end-to-end passes")
     e2e_value = job_throughput(inp.n_tokens, world, e2e_ms)
+    # The host link's own rates (one 512 MiB pinned copy each way): the step's bytes at these
+    # rates, the two directions overlapping, are the floor of the end-to-end time.
+    link_buf = torch.empty(1 << 29, dtype=torch.uint8).pin_memory()
+    link_dev = torch.empty(1 << 29, dtype=torch.uint8, device=dev)
+    link = {}
+    for name, fn in (("h2d", lambda: link_dev.copy_(link_buf, non_blocking=True)),
+                     ("d2h", lambda: link_buf.copy_(link_dev, non_blocking=True))):
+        fn()
+        torch.cuda.synchronize()
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(stream)
+        for _ in range(3):
+            fn()
+        l1.record(stream)
+        torch.cuda.synchronize()
+        link[name] = 3 * link_buf.numel() / (l0.elapsed_time(l1) / 1e3) / 1e9
+    del link_buf, link_dev
+    link_floor_ms = 1e3 * max(h2d / (link["h2d"] * 1e9), d2h / (link["d2h"] * 1e9))
 
     # Roofline of the dominant kernel.
     peaks, peak_kind = load_peaks()
@@ -560,7 +578,9 @@ def main():
             "stages": {n: float(t) for n, t in zip(names, stage_ms)},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
-                    "entry": "kda_fwd_host", "serial_copy_run_copy_ms": serial_ms},
+                    "entry": "kda_fwd_host", "serial_copy_run_copy_ms": serial_ms,
+                    "link_h2d_gbs": link["h2d"], "link_d2h_gbs": link["d2h"],
+                    "link_floor_ms": link_floor_ms},
             "gpu_launches": int(n_launch * args.steps), "clocks": clocks,
             "kernel_source_sha": kernel_source_hash()}
 
