@@ -14,7 +14,9 @@ Contents
                           FLA", written out with a dense solve (cross-check).
   * ``transition_np``  -- brute force: explicit K x K transition matrices.
   * ``backward.bwd``   -- fp64 gradients of the forward (PyTorch autograd over the
-                          token recurrence), the reference for a backward pass.
+                          token recurrence), the reference for a backward pass;
+                          ``backward.chunk_bwd_np`` the same gradients derived by hand
+                          through the chunk form.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` (``backward`` by
 ``tests/test_oracle_backward.py``) against things the pages and the mathematics

@@ -11,6 +11,10 @@ steps as ``ref.recurrent_np``) in PyTorch fp64 on the CPU and lets autograd diff
 It is only as correct as that restatement and autograd; the pins in tests/test_oracle_backward.py
 tie it to things outside it: central finite differences of the C oracle's forward, closed-form
 derivatives of one-token cases, and linearity in the incoming gradient.
+
+``chunk_bwd_np`` is the second form: the gradients derived by hand through the chunk form, stage
+by stage as a chunked backward computes them (the intermediates a GPU backward can be checked
+against one by one); it is pinned to ``bwd``.
 """
 from __future__ import annotations
 
@@ -106,4 +110,152 @@ def bwd(q, k, v, g, beta, do, dfinal=None, *, A_log=None, dt_bias=None, gate_mod
         out["d" + name] = None
     for (name, x), gr in zip(present, grads):
         out["d" + name] = (torch.zeros_like(x) if gr is None else gr).detach().numpy()
+    return out
+
+
+# ----------------------------------------------------------------------------------------------
+# The chunked backward, written out by hand
+# ----------------------------------------------------------------------------------------------
+
+def _l2norm_bwd(x, dxh, eps):
+    """x_hat = x / sqrt(|x|^2 + eps) over the last axis: the gradient with respect to x."""
+    n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+    return dxh / n - x * np.sum(x * dxh, axis=-1, keepdims=True) / n ** 3
+
+
+def chunk_bwd_np(q, k, v, g, beta, do, dfinal=None, *, chunk_size=64, A_log=None, dt_bias=None,
+                 gate_mode=GATE_SAFE, lower_bound=None, scale=None, qk_l2norm=True,
+                 beta_sigmoid=True, allow_neg_eigval=False, initial_state=None,
+                 l2_eps=L2_EPS) -> dict:
+    """The same gradients as ``bwd``, derived by hand through the chunk form ([reading] forward
+    pass steps 1-5; its backward-propagation section runs the same derivative as recompute
+    U, W, Qg and the states; dU and dAqk from O; the reverse cross-chunk recurrence of dS; the WY
+    gradients; the intra-chunk terms; a reverse cumsum for the gate), NumPy fp64, dense.
+
+    Per chunk, with S the state before it and dS' the gradient of the state after it:
+      dV_new = Aqk^T dO + Kg dS'        dAqk = (dO V_new^T) . M       dQg = dO S^T
+      dS = Qg^T dO - W^T dV_new + Diag(e^gamma_C) dS'
+      dKg = V_new dS'^T                 d gamma_C += e^gamma_C . rowsum(S . dS')
+      dU = dV_new, dW = -dV_new S^T, dA = dU (beta V)^T + dW (beta K~)^T
+      d(beta V) = A^T dU, d(beta K~) = A^T dW, dAkk0 = -(A^T dA A^T) . M_-1
+    then through Aqk_ij = sum_k Q_ik K_jk e^(Gamma_ik - Gamma_jk) (and the same for Akk0's
+    K K term), K~ = e^Gamma . K, Qg = e^Gamma . Q, Kg = e^(gamma_C - Gamma) . K, and
+    Gamma = cumsum(g') (a reverse cumsum).  Returns the dict ``bwd`` returns (no varlen)."""
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    g = np.asarray(g, np.float64); beta = np.asarray(beta, np.float64)
+    do = np.asarray(do, np.float64)
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    G = HV // H
+    if scale is None:
+        scale = K ** -0.5
+    from .ref import gate_np, sigmoid_np, softplus_np
+    qh = q / np.sqrt(np.sum(q * q, -1, keepdims=True) + l2_eps) if qk_l2norm else q
+    kh = k / np.sqrt(np.sum(k * k, -1, keepdims=True) + l2_eps) if qk_l2norm else k
+    gp = gate_np(g, gate_mode, A_log, dt_bias, lower_bound)
+    cb = 2.0 if (beta_sigmoid and allow_neg_eigval) else 1.0
+    bb = cb * sigmoid_np(beta) if beta_sigmoid else beta
+    dqh = np.zeros_like(qh); dkh = np.zeros_like(kh); dv = np.zeros_like(v)
+    dgp = np.zeros_like(gp); dbb = np.zeros_like(bb)
+    o = np.zeros((B, T, HV, V)); fs = np.zeros((B, HV, K, V)); dh0 = np.zeros((B, HV, K, V))
+    C = int(chunk_size)
+    for n in range(B):
+        for hv in range(HV):
+            h = hv // G
+            S = np.zeros((K, V)) if initial_state is None else np.array(initial_state[n, hv], np.float64)
+            chunks, states = [], []
+            for cs in range(0, T, C):  # forward: the state before every chunk
+                ce = min(cs + C, T)
+                L = ce - cs
+                Q = scale * qh[n, cs:ce, h]
+                Kc = kh[n, cs:ce, h]
+                Vc = v[n, cs:ce, hv]
+                bc = bb[n, cs:ce, hv]
+                Gam = np.cumsum(gp[n, cs:ce, hv], axis=0)
+                gC = Gam[L - 1]
+                lower = np.tril(np.ones((L, L), bool))
+                strict = np.tril(np.ones((L, L), bool), -1)
+                D = Gam[:, None, :] - Gam[None, :, :]
+                E = np.where(lower[:, :, None], np.exp(np.where(lower[:, :, None], D, 0.0)), 0.0)
+                Aqk = np.einsum("ik,jk,ijk->ij", Q, Kc, E)
+                P = np.where(strict, np.einsum("ik,jk,ijk->ij", Kc, Kc, E), 0.0)
+                A = np.linalg.inv(np.eye(L) + bc[:, None] * P)
+                Kt = np.exp(Gam) * Kc
+                BV, BK = bc[:, None] * Vc, bc[:, None] * Kt
+                U, W = A @ BV, A @ BK
+                Qg = np.exp(Gam) * Q
+                Kg = np.exp(gC[None, :] - Gam) * Kc
+                Vnew = U - W @ S
+                o[n, cs:ce, hv] = Qg @ S + Aqk @ Vnew
+                states.append(S)
+                chunks.append((cs, ce, Q, Kc, Vc, bc, Gam, gC, lower, strict, E, Aqk, P, A, Kt,
+                               BV, BK, Qg, Kg, Vnew))
+                S = np.exp(gC)[:, None] * S + Kg.T @ Vnew
+            fs[n, hv] = S
+            dS = np.zeros((K, V)) if dfinal is None else np.array(dfinal[n, hv], np.float64)
+            for (cs, ce, Q, Kc, Vc, bc, Gam, gC, lower, strict, E, Aqk, P, A, Kt, BV, BK, Qg, Kg,
+                 Vnew), S in zip(reversed(chunks), reversed(states)):
+                dO = do[n, cs:ce, hv]
+                dVnew = Aqk.T @ dO + Kg @ dS
+                dAqk = np.where(lower, dO @ Vnew.T, 0.0)
+                dQg = dO @ S.T
+                dKg = Vnew @ dS.T
+                dgC = np.exp(gC) * np.sum(S * dS, axis=1)
+                dS_prev = Qg.T @ dO - (A @ BK).T @ dVnew + np.exp(gC)[:, None] * dS
+                dW = -dVnew @ S.T
+                dA = dVnew @ BV.T + dW @ BK.T
+                dBV, dBK = A.T @ dVnew, A.T @ dW
+                dv[n, cs:ce, hv] += bc[:, None] * dBV
+                db = np.sum(dBV * Vc, axis=1) + np.sum(dBK * Kt, axis=1)
+                dKt = bc[:, None] * dBK
+                dAkk0 = np.where(strict, -(A.T @ dA @ A.T), 0.0)
+                db += np.sum(dAkk0 * P, axis=1)
+                dP = bc[:, None] * dAkk0
+                dbb[n, cs:ce, hv] += db
+                # the e^(Gamma_i - Gamma_j) kernels: rows i, columns j
+                tq = np.einsum("ij,ik,jk,ijk->ijk", dAqk, Q, Kc, E)
+                tk = np.einsum("ij,ik,jk,ijk->ijk", dP, Kc, Kc, E)
+                dQ = dQg * np.exp(Gam) + np.einsum("ij,jk,ijk->ik", dAqk, Kc, E)
+                dK = (np.einsum("ij,ik,ijk->jk", dAqk, Q, E) + np.einsum("ij,jk,ijk->ik", dP, Kc, E)
+                      + np.einsum("ij,ik,ijk->jk", dP, Kc, E)
+                      + dKt * np.exp(Gam) + dKg * np.exp(gC[None, :] - Gam))
+                dGam = (dQg * Qg + dKt * Kt - dKg * Kg
+                        + tq.sum(1) - tq.sum(0) + tk.sum(1) - tk.sum(0))
+                dgC = dgC + np.sum(dKg * Kg, axis=0)
+                dGam[-1] += dgC
+                dgp[n, cs:ce, hv] += np.cumsum(dGam[::-1], axis=0)[::-1]  # Gamma = cumsum(g')
+                dqh[n, cs:ce, h] += scale * dQ
+                dkh[n, cs:ce, h] += dK
+                dS = dS_prev
+            dh0[n, hv] = dS
+    out = {"o": o, "final_state": fs}
+    out["dq"] = _l2norm_bwd(q, dqh, l2_eps) if qk_l2norm else dqh
+    out["dk"] = _l2norm_bwd(k, dkh, l2_eps) if qk_l2norm else dkh
+    out["dv"] = dv
+    if beta_sigmoid:
+        sg = sigmoid_np(beta)
+        out["dbeta"] = dbb * cb * sg * (1.0 - sg)
+    else:
+        out["dbeta"] = dbb
+    # the gate activation ([notes] section 2)
+    out["dA_log"] = out["ddt_bias"] = None
+    if gate_mode == GATE_PREGATED:
+        out["dg"] = dgp
+    else:
+        x = g + (0.0 if dt_bias is None else np.asarray(dt_bias, np.float64).reshape(HV, K))
+        if gate_mode == GATE_PLAIN:
+            a = np.exp(np.asarray(A_log, np.float64)).reshape(HV, 1)
+            dx = dgp * (-a) * sigmoid_np(x)
+            out["dA_log"] = np.sum(dgp * (-a) * softplus_np(x), axis=(0, 1, 3))
+        else:
+            a = 1.0 if A_log is None else np.exp(np.asarray(A_log, np.float64)).reshape(HV, 1)
+            sg = sigmoid_np(a * x)
+            ds = dgp * float(lower_bound) * sg * (1.0 - sg)
+            dx = ds * a
+            if A_log is not None:
+                out["dA_log"] = np.sum(ds * a * x, axis=(0, 1, 3))
+        out["dg"] = dx
+        if dt_bias is not None:
+            out["ddt_bias"] = np.sum(dx, axis=(0, 1)).reshape(np.shape(dt_bias))
+    out["dh0"] = dh0 if initial_state is not None else None
     return out

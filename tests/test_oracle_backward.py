@@ -116,3 +116,32 @@ def test_final_state_gradient_alone_leaves_q_untouched():
     r = grads(d, opts, np.zeros_like(do), dfinal)
     assert np.all(r["dq"] == 0)
     assert np.any(r["dk"] != 0)
+
+
+@pytest.mark.parametrize("gate", [GATE_SAFE, GATE_PLAIN, GATE_PREGATED])
+@pytest.mark.parametrize("C,T", [(4, 13), (5, 5), (16, 11)])
+def test_chunked_backward_matches_autograd(gate, C, T):
+    """The hand-derived chunked backward (chunks of C tokens, a ragged last chunk) against the
+    autograd reference, which is itself pinned to finite differences of the C oracle."""
+    d, opts, do, dfinal = case(40 + gate + C, T=T, gate=gate)
+    ref = grads(d, opts, do, dfinal)
+    got = ob.chunk_bwd_np(d["q"], d["k"], d["v"], d["g"], d["beta"], do, dfinal, chunk_size=C,
+                          A_log=d.get("A_log"), dt_bias=d.get("dt_bias"),
+                          initial_state=d.get("initial_state"), **opts)
+    for key in ["o", "final_state"] + list(NAMES.values()):
+        if ref[key] is None:
+            assert got[key] is None, key
+            continue
+        assert np.allclose(got[key], ref[key], rtol=1e-9, atol=1e-10), key
+
+
+def test_chunked_backward_options():
+    """No norms, beta taken as given; and beta = 2 sigmoid(logit)."""
+    d, opts, do, dfinal = case(51, T=9)
+    for extra in (dict(qk_l2norm=False, beta_sigmoid=False), dict(allow_neg_eigval=True)):
+        ref = grads(d, opts, do, dfinal, **extra)
+        got = ob.chunk_bwd_np(d["q"], d["k"], d["v"], d["g"], d["beta"], do, dfinal, chunk_size=4,
+                              A_log=d["A_log"], dt_bias=d["dt_bias"],
+                              initial_state=d["initial_state"], **opts, **extra)
+        for key in NAMES.values():
+            assert np.allclose(got[key], ref[key], rtol=1e-9, atol=1e-10), (extra, key)
