@@ -80,15 +80,70 @@ def recurrent_t(q, k, v, g, beta, *, A_log=None, dt_bias=None, gate_mode=GATE_SA
     return torch.stack(outs), torch.stack(finals)
 
 
+def _split_varlen(cu_seqlens, arrays):
+    """[1, total, ...] arrays -> per-sequence [1, len, ...] views (cu_seqlens, [notes] section
+    2.2 varlen example)."""
+    cu = np.asarray(cu_seqlens, np.int64)
+    return [[None if a is None else a[:, cu[n]:cu[n + 1]] for a in arrays] for n in range(len(cu) - 1)]
+
+
+def _varlen(fn, q, k, v, g, beta, do, dfinal, cu_seqlens, initial_state, transpose, kw) -> dict:
+    """Run ``fn`` per sequence of a varlen batch and assemble the results: token gradients in
+    the flattened layout (rows no sequence covers get 0), per-sequence states stacked, the
+    shared A_log / dt_bias gradients summed."""
+    tok = np.asarray(q).shape[1]
+    outs = []
+    for n, (qn, kn, vn, gn, bn, don) in enumerate(
+            _split_varlen(cu_seqlens, [np.asarray(q), np.asarray(k), np.asarray(v), np.asarray(g),
+                                       np.asarray(beta), np.asarray(do)])):
+        h0n = None if initial_state is None else np.asarray(initial_state)[n:n + 1]
+        dfn = None if dfinal is None else np.asarray(dfinal)[n:n + 1]
+        outs.append(fn(qn, kn, vn, gn, bn, don, dfn, initial_state=h0n,
+                       transpose_state_layout=transpose, **kw))
+    cu = np.asarray(cu_seqlens, np.int64)
+    res = {}
+    for key, tokwise in (("o", True), ("dq", True), ("dk", True), ("dv", True), ("dg", True),
+                         ("dbeta", True), ("final_state", False), ("dh0", False),
+                         ("dA_log", None), ("ddt_bias", None)):
+        parts = [r[key] for r in outs]
+        if parts[0] is None:
+            res[key] = None
+        elif tokwise:
+            full = np.zeros((1, tok) + parts[0].shape[2:])
+            for n, part in enumerate(parts):
+                full[:, cu[n]:cu[n + 1]] = part
+            res[key] = full
+        elif tokwise is False:
+            res[key] = np.concatenate(parts, axis=0)
+        else:
+            res[key] = np.sum(parts, axis=0)
+    return res
+
+
 def bwd(q, k, v, g, beta, do, dfinal=None, *, A_log=None, dt_bias=None, gate_mode=GATE_SAFE,
         lower_bound=None, scale=None, qk_l2norm=True, beta_sigmoid=True, allow_neg_eigval=False,
-        initial_state=None, l2_eps=L2_EPS) -> dict:
+        initial_state=None, cu_seqlens=None, transpose_state_layout=False, l2_eps=L2_EPS) -> dict:
     """Gradients of <do, o> + <dfinal, final_state> with respect to every input, in fp64.
 
-    Inputs as for ``ref.recurrent_np`` without varlen (B sequences of T tokens); do has o's
-    shape [B,T,HV,V], dfinal the final state's [B,HV,K,V] (None: zero).  Returns a dict with
-    o, final_state and dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dh0 (None for absent inputs),
-    as float64 NumPy arrays."""
+    Inputs as for ``ref.recurrent_np``: B sequences of T tokens, or with ``cu_seqlens`` a
+    varlen batch flattened to B = 1; do has o's shape [B,T,HV,V], dfinal the final state's
+    [N,HV,K,V] (None: zero).  ``transpose_state_layout``: initial / final states (and their
+    gradients) are [N,HV,V,K].  Returns a dict with o, final_state and dq, dk, dv, dg, dbeta,
+    dA_log, ddt_bias, dh0 (None for absent inputs), as float64 NumPy arrays."""
+    if cu_seqlens is not None:
+        kw = dict(A_log=A_log, dt_bias=dt_bias, gate_mode=gate_mode, lower_bound=lower_bound,
+                  scale=scale, qk_l2norm=qk_l2norm, beta_sigmoid=beta_sigmoid,
+                  allow_neg_eigval=allow_neg_eigval, l2_eps=l2_eps)
+        return _varlen(bwd, q, k, v, g, beta, do, dfinal, cu_seqlens, initial_state,
+                       transpose_state_layout, kw)
+    if transpose_state_layout:
+        sw = lambda x: None if x is None else np.swapaxes(np.asarray(x), -1, -2)
+        r = bwd(q, k, v, g, beta, do, sw(dfinal), A_log=A_log, dt_bias=dt_bias,
+                gate_mode=gate_mode, lower_bound=lower_bound, scale=scale, qk_l2norm=qk_l2norm,
+                beta_sigmoid=beta_sigmoid, allow_neg_eigval=allow_neg_eigval,
+                initial_state=sw(initial_state), l2_eps=l2_eps)
+        r["final_state"], r["dh0"] = sw(r["final_state"]), sw(r["dh0"])
+        return r
     import torch
     leaves = {"q": _t(q), "k": _t(k), "v": _t(v), "g": _t(g), "beta": _t(beta),
               "A_log": _t(A_log), "dt_bias": _t(dt_bias), "h0": _t(initial_state)}
@@ -125,8 +180,8 @@ def _l2norm_bwd(x, dxh, eps):
 
 def chunk_bwd_np(q, k, v, g, beta, do, dfinal=None, *, chunk_size=64, A_log=None, dt_bias=None,
                  gate_mode=GATE_SAFE, lower_bound=None, scale=None, qk_l2norm=True,
-                 beta_sigmoid=True, allow_neg_eigval=False, initial_state=None,
-                 l2_eps=L2_EPS) -> dict:
+                 beta_sigmoid=True, allow_neg_eigval=False, initial_state=None, cu_seqlens=None,
+                 transpose_state_layout=False, l2_eps=L2_EPS) -> dict:
     """The same gradients as ``bwd``, derived by hand through the chunk form ([reading] forward
     pass steps 1-5; its backward-propagation section runs the same derivative as recompute
     U, W, Qg and the states; dU and dAqk from O; the reverse cross-chunk recurrence of dS; the WY
@@ -140,7 +195,22 @@ def chunk_bwd_np(q, k, v, g, beta, do, dfinal=None, *, chunk_size=64, A_log=None
       d(beta V) = A^T dU, d(beta K~) = A^T dW, dAkk0 = -(A^T dA A^T) . M_-1
     then through Aqk_ij = sum_k Q_ik K_jk e^(Gamma_ik - Gamma_jk) (and the same for Akk0's
     K K term), K~ = e^Gamma . K, Qg = e^Gamma . Q, Kg = e^(gamma_C - Gamma) . K, and
-    Gamma = cumsum(g') (a reverse cumsum).  Returns the dict ``bwd`` returns (no varlen)."""
+    Gamma = cumsum(g') (a reverse cumsum).  Arguments and result as for ``bwd``."""
+    if cu_seqlens is not None:
+        kw = dict(chunk_size=chunk_size, A_log=A_log, dt_bias=dt_bias, gate_mode=gate_mode,
+                  lower_bound=lower_bound, scale=scale, qk_l2norm=qk_l2norm,
+                  beta_sigmoid=beta_sigmoid, allow_neg_eigval=allow_neg_eigval, l2_eps=l2_eps)
+        return _varlen(chunk_bwd_np, q, k, v, g, beta, do, dfinal, cu_seqlens, initial_state,
+                       transpose_state_layout, kw)
+    if transpose_state_layout:
+        sw = lambda x: None if x is None else np.swapaxes(np.asarray(x), -1, -2)
+        r = chunk_bwd_np(q, k, v, g, beta, do, sw(dfinal), chunk_size=chunk_size, A_log=A_log,
+                         dt_bias=dt_bias, gate_mode=gate_mode, lower_bound=lower_bound,
+                         scale=scale, qk_l2norm=qk_l2norm, beta_sigmoid=beta_sigmoid,
+                         allow_neg_eigval=allow_neg_eigval, initial_state=sw(initial_state),
+                         l2_eps=l2_eps)
+        r["final_state"], r["dh0"] = sw(r["final_state"]), sw(r["dh0"])
+        return r
     q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
     g = np.asarray(g, np.float64); beta = np.asarray(beta, np.float64)
     do = np.asarray(do, np.float64)

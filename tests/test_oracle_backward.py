@@ -145,3 +145,51 @@ def test_chunked_backward_options():
                               initial_state=d["initial_state"], **opts, **extra)
         for key in NAMES.values():
             assert np.allclose(got[key], ref[key], rtol=1e-9, atol=1e-10), (extra, key)
+
+
+def test_varlen_gradients_pin_to_the_c_oracle_and_match_the_chunked_form():
+    """A varlen batch (an empty sequence included): finite differences of the C oracle's varlen
+    forward pin the autograd form, and the chunked form agrees with it."""
+    r = np.random.default_rng(61)
+    tot, H, HV, K, V = 14, 1, 2, 4, 3
+    cu = np.array([0, 5, 5, 11, 14], np.int64)
+    N = len(cu) - 1
+    d = dict(q=r.standard_normal((1, tot, H, K)), k=r.standard_normal((1, tot, H, K)),
+             v=r.standard_normal((1, tot, HV, V)), g=r.standard_normal((1, tot, HV, K)),
+             beta=r.standard_normal((1, tot, HV)), initial_state=0.3 * r.standard_normal((N, HV, K, V)),
+             dt_bias=0.5 * r.standard_normal(HV * K), A_log=r.uniform(-0.5, 0.5, HV))
+    opts = dict(gate_mode=GATE_SAFE, lower_bound=-5.0)
+    do, dfinal = r.standard_normal((1, tot, HV, V)), r.standard_normal((N, HV, K, V))
+    ref = grads(d, opts, do, dfinal, cu_seqlens=cu)
+    got = ob.chunk_bwd_np(d["q"], d["k"], d["v"], d["g"], d["beta"], do, dfinal, chunk_size=4,
+                          A_log=d["A_log"], dt_bias=d["dt_bias"], initial_state=d["initial_state"],
+                          cu_seqlens=cu, **opts)
+    for key in NAMES.values():
+        assert np.allclose(got[key], ref[key], rtol=1e-9, atol=1e-10), key
+    rng = np.random.default_rng(62)
+    eps = 1e-6
+    for name, key in NAMES.items():
+        delta = rng.standard_normal(np.shape(d[name]))
+        plus = dict(d); plus[name] = d[name] + eps * delta
+        minus = dict(d); minus[name] = d[name] - eps * delta
+        fd = (c_loss(plus, opts, do, dfinal, cu_seqlens=cu)
+              - c_loss(minus, opts, do, dfinal, cu_seqlens=cu)) / (2 * eps)
+        an = float(np.sum(ref[key] * delta))
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_transposed_state_layout_is_the_transpose():
+    d, opts, do, dfinal = case(71, T=6)
+    ref = grads(d, opts, do, dfinal)
+    sw = lambda x: np.ascontiguousarray(np.swapaxes(x, -1, -2))
+    dt = dict(d); dt["initial_state"] = sw(d["initial_state"])
+    for fn in (lambda **kw: grads(dt, opts, do, sw(dfinal), **kw),
+               lambda **kw: ob.chunk_bwd_np(dt["q"], dt["k"], dt["v"], dt["g"], dt["beta"], do,
+                                            sw(dfinal), chunk_size=4, A_log=dt["A_log"],
+                                            dt_bias=dt["dt_bias"], initial_state=dt["initial_state"],
+                                            **opts, **kw)):
+        got = fn(transpose_state_layout=True)
+        assert np.allclose(got["dh0"], sw(ref["dh0"]), rtol=1e-9, atol=1e-10)
+        assert np.allclose(got["final_state"], sw(ref["final_state"]), rtol=1e-9, atol=1e-10)
+        for key in ("dq", "dk", "dv", "dg", "dbeta"):
+            assert np.allclose(got[key], ref[key], rtol=1e-9, atol=1e-10), key
