@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(256, 2)
   {
     uint8_t* tA = sm + P_QK;          // [2][64 rows x 128 B]: hi, lo
     uint8_t* tB = sm + P_QK + 16384;  // [2][32 rows x 128 B]: hi, lo
-    const uint32_t la = tmem + 0, lb = tmem + 32;  // accumulators of rounds 1 and 2
+    const uint32_t la = tmem + 0, lb = tmem + 32;  // first / second MMA round accumulators
     // 4 consecutive fp32 values -> hi / lo bf16 quads at byte offset `off` of two tiles
     auto put4 = [&](uint8_t* hi_tile, uint32_t tile_bytes, uint32_t off, const float* v) {
       const uint32_t h0 = pack_bf16x2(v[0], v[1]), h1 = pack_bf16x2(v[2], v[3]);
@@ -656,7 +656,7 @@ __global__ void __launch_bounds__(256, 2)
     const bool epi = (warp & 2) && lane < 16;
     const int er = 16 * ((warp & 3) - 2) + lane;  // row - 32
     const int ec = 16 * (warp >> 2);              // first column
-    {  // round 1 operands: A = L[32..63][0..31], B = X_AA
+    {  // first MMA round's operands: A = L[32..63][0..31], B = X_AA
       const int i = tid >> 3, m0 = (tid & 7) * 4;
       float v[4];
 #pragma unroll
@@ -672,7 +672,7 @@ __global__ void __launch_bounds__(256, 2)
     __syncwarp();
     if (!mbar_wait(&bars[1], 1)) flag_status(a.status, KDA_DEV_TIMEOUT);
     tc_fence_after();
-    {  // round 2 operands: B = Y = L_BA X_AA (from TMEM), A = X[32..63][32..63]
+    {  // second MMA round's operands: B = Y = L_BA X_AA (from TMEM), A = X[32..63][32..63]
       uint32_t r[16];
       tmem_ld16(tmem_addr(la, 32 * (warp & 3), ec), r);
       tmem_wait_ld();
