@@ -110,11 +110,42 @@ def _code_only(text: str) -> str:
     return "\n".join(line.rstrip() for line in text.split("\n"))
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources' code (comments excluded): ncu counters committed under
-    profiles/ are used only while it matches the hash recorded with them."""
+# Translation unit of each kernel the bench names: ncu counters depend on that unit's code only.
+KERNEL_TU = {"tc_intra": "kda_tc.cu", "tc_recur": "kda_tc.cu", "recurrent_k128": "kda_recurrent.cu",
+             "simt_intra": "kda_simt.cu", "simt_recur": "kda_simt.cu", "chunk_table": "kda_simt.cu"}
+_INCLUDE = re.compile(r'^\s*#\s*include\s*"([^"]+)"', re.M)
+
+
+def tu_files(root: str):
+    """The project files one translation unit compiles: `root` (a file of csrc/) and every
+    header it includes from csrc/ or include/, recursively."""
+    csrc = os.path.join(ROOT, "kimi_delta_attention_gate_gb300", "csrc")
+    dirs = (csrc, os.path.join(ROOT, "include"))
+    seen, todo = [], [os.path.join(csrc, root)]
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.append(f)
+        for inc in _INCLUDE.findall(open(f, encoding="utf-8").read()):
+            for d in dirs:
+                cand = os.path.join(d, inc)
+                if os.path.exists(cand):
+                    todo.append(cand)
+                    break
+    return sorted(seen)
+
+
+def kernel_source_hash(tu: str = None) -> str:
+    """Hash of the code (comments excluded) of one kernel's translation unit, or of every
+    csrc/ file when `tu` is None: ncu counters committed under profiles/ are used only while
+    it matches the hash recorded with them."""
+    if tu is None:
+        files = sorted(glob.glob(os.path.join(ROOT, "kimi_delta_attention_gate_gb300", "csrc", "*")))
+    else:
+        files = tu_files(tu)
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "kimi_delta_attention_gate_gb300", "csrc", "*"))):
+    for f in files:
         h.update(os.path.basename(f).encode() + b"\0")
         h.update(_code_only(open(f, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
@@ -131,7 +162,8 @@ def profiled_traffic(stage: str, workload: str):
         if ":" in line:
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    if fields.get("kernel_source_sha", "").split(" ")[0] != kernel_source_hash():
+    tu = KERNEL_TU.get(stage)
+    if tu is None or fields.get("kernel_source_sha", "").split(" ")[0] != kernel_source_hash(tu):
         return None
     try:
         return float(fields["dram_bytes_per_launch"])
