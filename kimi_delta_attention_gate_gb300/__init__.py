@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) chunk-parallel Kimi Delta Attention forward pass.
+"""GB300 (sm_103a) chunk-parallel Kimi Delta Attention: forward pass and its backward.
 
 ``kda_fwd`` takes PyTorch CUDA tensors, allocates the outputs and the
 workspace with PyTorch, fills the C parameter block and calls the C ABI
@@ -18,10 +18,10 @@ from typing import Optional, Tuple
 
 from . import _binding
 from ._binding import (KDA_BF16, KDA_F32, KDA_GATE_PLAIN, KDA_GATE_PREGATED, KDA_GATE_SAFE,
-                       KdaError, kda_abi_version, kda_fwd_params, kda_get_device_status,
-                       kda_last_error, kda_status_string)
+                       KdaError, kda_abi_version, kda_bwd_params, kda_fwd_params,
+                       kda_get_device_status, kda_last_error, kda_status_string)
 
-__all__ = ["kda_fwd", "kda_fwd_host", "kda_fused_recurrent_fwd", "kda_fwd_workspace_size",
+__all__ = ["kda_fwd", "kda_bwd", "kda_fwd_host", "kda_fused_recurrent_fwd", "kda_fwd_workspace_size",
            "make_params", "KdaError", "kda_get_device_status", "kda_last_error", "kda_status_string", "kda_abi_version", "KDA_GATE_SAFE",
            "KDA_GATE_PLAIN", "KDA_GATE_PREGATED", "KDA_BF16", "KDA_F32"]
 
@@ -241,3 +241,65 @@ def kda_fwd_host(q, k, v, g, beta, *, o, final_state=None, A_log=None, dt_bias=N
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     _binding.raise_for(_binding.kda_fwd_host(p, _ptr(arena), arena.numel(), handle))
     return o, final_state
+
+
+def kda_bwd(q, k, v, g, beta, do, *, dht=None, A_log=None, dt_bias=None, lower_bound=None,
+            scale=None, initial_state=None, cu_seqlens=None, cu_seqlens_cpu=None,
+            chunk_size: int = 64, use_gate_in_kernel: bool = True, safe_gate: Optional[bool] = None,
+            use_qk_l2norm_in_kernel: bool = True, use_beta_sigmoid_in_kernel: bool = True,
+            allow_neg_eigval: bool = False, transpose_state_layout: bool = False,
+            return_dh0: bool = True, workspace=None, stream=None):
+    """Backward pass of ``kda_fwd`` (same inputs and keyword arguments) for the incoming
+    gradients ``do`` (o's shape and dtype) and ``dht`` (final_state's shape, fp32; None = 0).
+
+    Returns (dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dh0), fp32 tensors shaped like q, k, v,
+    g, beta, A_log, dt_bias and the initial state; dA_log / ddt_bias are None when A_log /
+    dt_bias are absent or the gate is not in-kernel, dh0 None unless ``return_dh0``.  dg is the
+    gradient with respect to g as passed (the raw gate input).  Asynchronous on ``stream``."""
+    import torch
+    if not q.is_cuda:
+        raise ValueError("kda_bwd runs on CUDA tensors only")
+    if cu_seqlens is not None and cu_seqlens_cpu is None:
+        cu_seqlens_cpu = cu_seqlens.to("cpu")
+    if cu_seqlens_cpu is not None:
+        cu_seqlens_cpu = cu_seqlens_cpu.to(torch.int64).contiguous()
+    if tuple(do.shape) != tuple(v.shape) or do.dtype != v.dtype or not do.is_contiguous():
+        raise ValueError("do must be contiguous with o's shape and dtype")
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    st_shape = (N, HV, V, K) if transpose_state_layout else (N, HV, K, V)
+    if dht is not None and (tuple(dht.shape) != st_shape or dht.dtype != torch.float32
+                            or not dht.is_contiguous()):
+        raise ValueError(f"dht must be contiguous float32 {list(st_shape)}")
+    f = make_params(q, k, v, g, beta, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound,
+                    scale=scale, initial_state=initial_state, cu_seqlens=cu_seqlens,
+                    cu_seqlens_cpu=cu_seqlens_cpu, chunk_size=chunk_size,
+                    use_gate_in_kernel=use_gate_in_kernel, safe_gate=safe_gate,
+                    use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel,
+                    use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
+                    allow_neg_eigval=allow_neg_eigval,
+                    transpose_state_layout=transpose_state_layout)
+    dev = v.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk = torch.empty(q.shape, **f32), torch.empty(k.shape, **f32)
+    dv, dg, dbeta = torch.empty(v.shape, **f32), torch.empty(g.shape, **f32), torch.empty(beta.shape, **f32)
+    in_gate = f.gate_mode != KDA_GATE_PREGATED
+    dA_log = torch.empty((HV,), **f32) if (A_log is not None and in_gate) else None
+    ddt_bias = torch.empty(tuple(dt_bias.shape), **f32) if (dt_bias is not None and in_gate) else None
+    dh0 = torch.empty(st_shape, **f32) if return_dh0 else None
+    p = kda_bwd_params()
+    p.fwd = f
+    p.d_o, p.d_final_state = _ptr(do), _ptr(dht)
+    p.dq, p.dk, p.dv, p.dg, p.dbeta = _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta)
+    p.dA_log, p.ddt_bias, p.dh0 = _ptr(dA_log), _ptr(ddt_bias), _ptr(dh0)
+    _binding.raise_for(_binding.kda_bwd_check(p))
+    need = _binding.kda_bwd_workspace_size(p)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel()
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _binding.raise_for(_binding.kda_bwd(p, handle))
+    return dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dh0

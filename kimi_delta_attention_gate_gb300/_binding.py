@@ -1,4 +1,5 @@
-"""ctypes view of the C ABI in ``include/kda.h`` (argument marshalling only).
+"""ctypes view of the C ABI in ``include/kda.h`` and ``include/kda_bwd.h`` (argument
+marshalling only).
 
 Loading fails loudly when the CUDA library has not been built: there is no
 fallback of any kind.
@@ -37,7 +38,8 @@ EXPORTED = ("kda_fwd_workspace_size", "kda_fwd_check", "kda_fwd", "kda_fwd_num_l
             "kda_fwd_host",
             "kda_fwd_num_stages",
             "kda_fwd_stage_name", "kda_fwd_stage", "kda_get_device_status", "kda_status_string",
-            "kda_last_error", "kda_abi_version", "kda_fwd_noalloc")
+            "kda_last_error", "kda_abi_version", "kda_fwd_noalloc",
+            "kda_bwd_check", "kda_bwd_workspace_size", "kda_bwd_num_launches", "kda_bwd")
 
 # Size of the static device scratch behind kda_fwd_noalloc (KDA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -59,6 +61,18 @@ class kda_fwd_params(ctypes.Structure):
         ("dt_bias", ctypes.c_void_p), ("h0", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
         ("cu_seqlens_host", ctypes.c_void_p), ("o", ctypes.c_void_p),
         ("final_state", ctypes.c_void_p), ("h_out", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class kda_bwd_params(ctypes.Structure):
+    """Mirror of ``struct kda_bwd_params`` (include/kda_bwd.h)."""
+
+    _fields_ = [
+        ("fwd", kda_fwd_params), ("d_o", ctypes.c_void_p), ("d_final_state", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("dg", ctypes.c_void_p), ("dbeta", ctypes.c_void_p), ("dA_log", ctypes.c_void_p),
+        ("ddt_bias", ctypes.c_void_p), ("dh0", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
     ]
 
@@ -116,6 +130,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kda_last_error.argtypes = []
             lib.kda_abi_version.restype = ctypes.c_int32
             lib.kda_abi_version.argtypes = []
+            PB = ctypes.POINTER(kda_bwd_params)
+            lib.kda_bwd_check.restype = ctypes.c_int
+            lib.kda_bwd_check.argtypes = [PB]
+            lib.kda_bwd_workspace_size.restype = ctypes.c_size_t
+            lib.kda_bwd_workspace_size.argtypes = [PB]
+            lib.kda_bwd_num_launches.restype = ctypes.c_int32
+            lib.kda_bwd_num_launches.argtypes = [PB]
+            lib.kda_bwd.restype = ctypes.c_int
+            lib.kda_bwd.argtypes = [PB, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -183,6 +206,22 @@ def kda_last_error() -> str:
 
 def kda_abi_version() -> int:
     return int(load().kda_abi_version())
+
+
+def kda_bwd_check(p: kda_bwd_params) -> int:
+    return int(load().kda_bwd_check(ctypes.byref(p)))
+
+
+def kda_bwd_workspace_size(p: kda_bwd_params) -> int:
+    return int(load().kda_bwd_workspace_size(ctypes.byref(p)))
+
+
+def kda_bwd_num_launches(p: kda_bwd_params) -> int:
+    return int(load().kda_bwd_num_launches(ctypes.byref(p)))
+
+
+def kda_bwd(p: kda_bwd_params, stream: int = 0) -> int:
+    return int(load().kda_bwd(ctypes.byref(p), ctypes.c_void_p(stream)))
 
 
 def raise_for(status: int) -> None:

@@ -474,6 +474,10 @@ struct HostCopies : SegHooks {
 
 void set_last_error(const char* msg) { t_last_error = msg; }
 
+// The device status word of the current device (NULL without a device): the backward pass
+// (kda_bwd.cu) flags into the same word that kda_get_device_status reads.
+unsigned int* device_status_word() { return device_status_ptr(); }
+
 }  // namespace kda
 
 using namespace kda;

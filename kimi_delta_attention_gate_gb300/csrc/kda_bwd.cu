@@ -1,0 +1,221 @@
+// GPU kernels and C entry points of the KDA backward pass (include/kda_bwd.h).  The stage
+// bodies live in kda_bwd.cuh; here each phase is one thread's share of the work followed
+// by a block barrier.
+
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "kda_bwd.cuh"
+#include "kda_internal.cuh"
+
+namespace kda {
+
+unsigned int* device_status_word();  // kda_api.cu
+
+namespace bwd {
+namespace {
+
+struct GpuExec {
+  template <class F>
+  __device__ __forceinline__ void phase(F&& f) {
+    f((int)threadIdx.x, (int)blockDim.x);
+    __syncthreads();
+  }
+  __device__ __forceinline__ void atomic_add(float* p, float x) { atomicAdd(p, x); }
+  __device__ __forceinline__ void flag(unsigned int* s, unsigned int bits) { atomicOr(s, bits); }
+};
+
+__global__ void __launch_bounds__(kThreads) prep_kernel(const Args a) {
+  GpuExec ex;
+  prep_body(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y);
+}
+
+__global__ void __launch_bounds__(kThreads) states_kernel(const Args a) {
+  extern __shared__ float smem[];
+  GpuExec ex;
+  states_body(ex, a, (int64_t)blockIdx.x, smem);
+}
+
+__global__ void __launch_bounds__(kThreads) dstate_kernel(const Args a) {
+  extern __shared__ float smem[];
+  GpuExec ex;
+  dstate_body(ex, a, (int64_t)blockIdx.x, smem);
+}
+
+__global__ void __launch_bounds__(kThreads) grads_kernel(const Args a) {
+  extern __shared__ float smem[];
+  GpuExec ex;
+  grads_body(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);
+}
+
+thread_local char t_msg[512];
+
+kda_status fail(kda_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof t_msg, fmt, ap);
+  va_end(ap);
+  set_last_error(t_msg);
+  return s;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// The forward parameters the backward is checked against: d_o takes the place of o.
+kda_fwd_params fwd_view(const kda_bwd_params* p) {
+  kda_fwd_params f = p->fwd;
+  f.o = const_cast<void*>(p->d_o);
+  f.final_state = nullptr;
+  f.h_out = nullptr;
+  f.workspace = nullptr;
+  f.workspace_bytes = 0;
+  return f;
+}
+
+kda_status check(const kda_bwd_params* p) {
+  if (p == nullptr) return fail(KDA_ERR_INVALID_ARG, "params is NULL");
+  const kda_fwd_params f = fwd_view(p);
+  kda_status s = kda_fwd_check(&f);
+  if (s != KDA_OK) return s;  // the forward's message stays
+  const bool tokens = (int64_t)f.B * f.T > 0;
+  struct { const void* ptr; const char* name; bool required; } ptrs[] = {
+      {p->dq, "dq", tokens},         {p->dk, "dk", tokens},
+      {p->dv, "dv", tokens},         {p->dg, "dg", tokens},
+      {p->dbeta, "dbeta", tokens},   {p->d_final_state, "d_final_state", false},
+      {p->dA_log, "dA_log", false},  {p->ddt_bias, "ddt_bias", false},
+      {p->dh0, "dh0", false},
+  };
+  for (auto& e : ptrs) {
+    if (e.required && e.ptr == nullptr) return fail(KDA_ERR_INVALID_ARG, "%s is NULL", e.name);
+    if (e.ptr != nullptr && !aligned16(e.ptr))
+      return fail(KDA_ERR_INVALID_ARG, "%s must be 16-byte aligned", e.name);
+  }
+  if (p->dA_log != nullptr && (f.A_log == nullptr || f.gate_mode == KDA_GATE_PREGATED))
+    return fail(KDA_ERR_INVALID_ARG, "dA_log needs A_log and an in-kernel gate (plain or safe)");
+  if (p->ddt_bias != nullptr && (f.dt_bias == nullptr || f.gate_mode == KDA_GATE_PREGATED))
+    return fail(KDA_ERR_INVALID_ARG, "ddt_bias needs dt_bias and an in-kernel gate (plain or safe)");
+  return KDA_OK;
+}
+
+Args make_args(const kda_bwd_params* p, const Plan& pl, unsigned int* status) {
+  const kda_fwd_params& f = p->fwd;
+  Args a;
+  memset(&a, 0, sizeof a);
+  a.p = pl;
+  a.dtype = f.in_dtype; a.gate_mode = f.gate_mode; a.qk_l2norm = f.qk_l2norm;
+  a.beta_sigmoid = f.beta_sigmoid; a.allow_neg_eigval = f.allow_neg_eigval;
+  a.state_v_first = f.state_v_first; a.lower_bound = f.lower_bound; a.scale = f.scale;
+  a.q = f.q; a.k = f.k; a.v = f.v; a.g = f.g; a.beta = f.beta; a.d_o = p->d_o;
+  a.A_log = f.A_log; a.dt_bias = f.dt_bias; a.h0 = f.h0; a.d_final_state = p->d_final_state;
+  a.cu_seqlens = f.cu_seqlens;
+  a.dq = p->dq; a.dk = p->dk; a.dv = p->dv; a.dg = p->dg; a.dbeta = p->dbeta;
+  a.dA_log = p->dA_log; a.ddt_bias = p->ddt_bias; a.dh0 = p->dh0;
+  a.ws = static_cast<char*>(p->workspace);
+  a.status = status;
+  return a;
+}
+
+}  // namespace
+}  // namespace bwd
+}  // namespace kda
+
+using kda::set_last_error;
+namespace B = kda::bwd;
+
+extern "C" {
+
+kda_status kda_bwd_check(const kda_bwd_params* p) {
+  kda_status s = B::check(p);
+  if (s == KDA_OK) set_last_error("");
+  return s;
+}
+
+size_t kda_bwd_workspace_size(const kda_bwd_params* p) {
+  if (B::check(p) != KDA_OK) return 0;
+  const kda_fwd_params f = B::fwd_view(p);
+  return B::make_plan(&f).total_bytes;
+}
+
+int32_t kda_bwd_num_launches(const kda_bwd_params* p) {
+  if (B::check(p) != KDA_OK) return 0;
+  const kda_fwd_params f = B::fwd_view(p);
+  const B::Plan pl = B::make_plan(&f);
+  int n = pl.varlen ? 1 : 0;
+  if (pl.nct > 0) n += 2;               // prep, grads
+  if (B::state_blocks(pl) > 0) n += 2;  // states, dstate
+  return n;
+}
+
+kda_status kda_bwd(const kda_bwd_params* p, void* stream) {
+  kda_status s = B::check(p);
+  if (s != KDA_OK) return s;
+  const kda_fwd_params f = B::fwd_view(p);
+  const B::Plan pl = B::make_plan(&f);
+  if (p->workspace == nullptr || p->workspace_bytes < pl.total_bytes)
+    return B::fail(KDA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu%s)", pl.total_bytes,
+                p->workspace_bytes, p->workspace ? "" : ", NULL");
+  if ((reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0)
+    return B::fail(KDA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  unsigned int* status = kda::device_status_word();
+  if (status == nullptr) return B::fail(KDA_ERR_CUDA, "no CUDA device / status word unavailable");
+  const B::Args a = B::make_args(p, pl, status);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const char* what = "output zeroing";
+  cudaError_t e = cudaSuccess;
+  auto chk = [&](cudaError_t x) {
+    if (e == cudaSuccess) e = x;
+    return e == cudaSuccess;
+  };
+  auto zero = [&](void* ptr, size_t bytes) {
+    return ptr == nullptr || bytes == 0 ? cudaSuccess : cudaMemsetAsync(ptr, 0, bytes, st);
+  };
+  const size_t ntok = (size_t)pl.ntok;
+  chk(zero(a.dq, ntok * pl.H * pl.K * sizeof(float)));
+  chk(zero(a.dk, ntok * pl.H * pl.K * sizeof(float)));
+  chk(zero(a.dv, ntok * pl.HV * pl.V * sizeof(float)));
+  chk(zero(a.dg, ntok * pl.HV * pl.K * sizeof(float)));
+  chk(zero(a.dbeta, ntok * pl.HV * sizeof(float)));
+  chk(zero(a.dA_log, (size_t)pl.HV * sizeof(float)));
+  chk(zero(a.ddt_bias, (size_t)pl.HV * pl.K * sizeof(float)));
+  if (e == cudaSuccess && pl.varlen) {
+    what = "chunk_table";
+    kda::FwdArgs t{};  // the forward's chunk-table kernel, writing into this workspace
+    t.plan.N = pl.N; t.plan.C = pl.C; t.plan.nct = pl.nct; t.plan.ntok = pl.ntok;
+    t.plan.varlen = true; t.plan.off_chunk_table = pl.off_table;
+    t.cu_seqlens = a.cu_seqlens; t.ws = a.ws; t.status = status;
+    chk(kda::launch_chunk_table(t, st));
+  }
+  if (e == cudaSuccess && pl.nct > 0) {
+    what = "bwd_prep";
+    B::prep_kernel<<<dim3((unsigned)pl.nct, (unsigned)pl.HV), B::kThreads, 0, st>>>(a);
+    chk(cudaGetLastError());
+  }
+  if (e == cudaSuccess && B::state_blocks(pl) > 0) {
+    what = "bwd_states";
+    const size_t sm = B::states_smem(pl);
+    if (chk(cudaFuncSetAttribute(B::states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm))) {
+      B::states_kernel<<<(unsigned)B::state_blocks(pl), B::kThreads, sm, st>>>(a);
+      chk(cudaGetLastError());
+    }
+    what = "bwd_dstate";
+    const size_t sd = B::dstate_smem(pl);
+    if (e == cudaSuccess &&
+        chk(cudaFuncSetAttribute(B::dstate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd))) {
+      B::dstate_kernel<<<(unsigned)B::state_blocks(pl), B::kThreads, sd, st>>>(a);
+      chk(cudaGetLastError());
+    }
+  }
+  if (e == cudaSuccess && pl.nct > 0) {
+    what = "bwd_grads";
+    const size_t sg = B::grads_smem(pl);
+    if (chk(cudaFuncSetAttribute(B::grads_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg))) {
+      B::grads_kernel<<<dim3((unsigned)pl.nct, (unsigned)pl.HV), B::kThreads, sg, st>>>(a);
+      chk(cudaGetLastError());
+    }
+  }
+  if (e != cudaSuccess) return B::fail(KDA_ERR_CUDA, "%s failed: %s", what, cudaGetErrorString(e));
+  set_last_error("");
+  return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,836 @@
+// Backward pass of the chunk-parallel KDA forward: fp32 CUDA-core stage bodies, written once
+// for the GPU kernels (kda_bwd.cu) and for a host build that the tests run under
+// AddressSanitizer.
+//
+// The stages follow the backward-propagation section of "Reading Notes: Implementation
+// Notes for KDA in FLA" (chunk_kda_bwd), with C the chunk size, Gamma the chunk-local cumsum
+// of the log decay g', gamma_C its last row, Q = scale * q / |q|, K = k / |k|:
+//   prep    per (chunk, value head): g', Gamma, Q, K, beta, Aqk (lower), the strictly lower
+//           P_ij = sum_k K_ik K_jk e^(Gamma_ik - Gamma_jk), e^gamma_C, Qg = e^Gamma Q,
+//           Kg = e^(gamma_C - Gamma) K, and W = A Diag(beta) e^Gamma K, U = A Diag(beta) V
+//           with A = (I + Diag(beta) P)^-1 by forward substitution (the recompute, step 1)
+//   states  per (sequence, value head, 32-column V tile), chunks in order: the state S
+//           before every chunk and V_new = U - W S (the recompute of the states, step 2)
+//   dstate  per (sequence, value head, V tile), chunks in reverse, with dS' the gradient of
+//           the state after a chunk: dV_new = Aqk^T dO + Kg dS' and
+//           dS = Qg^T dO - W^T dV_new + Diag(e^gamma_C) dS' (steps 3-4)
+//   grads   per (chunk, value head): dAqk = (dO V_new^T) masked lower, dQg = dO S^T,
+//           dW = -dV_new S^T, dKg = V_new dS'^T; X = A^T dV_new and Y = A^T dW by back
+//           substitution; dv = beta X, dbeta from X, Y and dAkk = -(A^T dA A^T) masked
+//           strictly lower with A^T dA = X (beta V)^T + Y (beta e^Gamma K)^T; the
+//           e^(Gamma_i - Gamma_j) terms of Aqk and P; the reverse cumsum of dGamma; the
+//           backward of the gate activation, of the L2 norm and of the beta sigmoid
+//           (steps 5-7).
+// Every exponent is Gamma_i - Gamma_j with i >= j, Gamma_i, or gamma_C - Gamma_i: never
+// positive while the log decay is non-positive, as in the forward's CUDA-core path.
+//
+// Execution model.  A stage body is a sequence of phases separated by block-wide barriers.
+// Inside a phase each thread takes the elements tid, tid + nthr, ... of the phase's work
+// ranges and keeps nothing across a barrier except in memory; control flow outside the
+// phases is the same for every thread.  On the GPU a phase is one thread's share followed
+// by __syncthreads(); the host build runs every thread's share of a phase, in a shuffled
+// thread order, before the next phase, so that the host tests run the index arithmetic,
+// barriers and work split of the GPU kernels.
+#pragma once
+
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kda_bwd.h"
+
+#if defined(__CUDACC__)
+#define KDA_HD __host__ __device__ __forceinline__
+#define KDA_BODY __device__ __forceinline__
+#else
+#define KDA_HD inline
+#define KDA_BODY inline
+#endif
+
+namespace kda {
+namespace bwd {
+
+constexpr int kThreads = 256;  // threads per block of every stage
+constexpr int kBV = 32;        // V columns per block of the two state stages
+constexpr float kL2Eps = 1e-6f;
+
+// Float offsets of one (chunk, value head) block of the workspace.
+struct Block {
+  size_t gam, qn, kn, qg, kg, w, y, dq, dk, dgam, dkg;  // [C][K]
+  size_t u, vn, dvn, x;                                  // [C][V]
+  size_t aqk, p;                                         // [C][C]
+  size_t beta, decay;                                    // [C], [K]
+  size_t floats;                                         // a multiple of 64 (256 bytes)
+};
+
+KDA_HD Block block_layout(int C, int K, int V) {
+  const size_t ck = (size_t)C * K, cv = (size_t)C * V, cc = (size_t)C * C;
+  Block b;
+  size_t o = 0;
+  b.gam = o; o += ck;   // Gamma
+  b.qn = o; o += ck;    // Q
+  b.kn = o; o += ck;    // K
+  b.qg = o; o += ck;    // Qg
+  b.kg = o; o += ck;    // Kg
+  b.w = o; o += ck;     // W
+  b.y = o; o += ck;     // dW, then Y = A^T dW
+  b.dq = o; o += ck;    // gradient of Q
+  b.dk = o; o += ck;    // gradient of K
+  b.dgam = o; o += ck;  // gradient of Gamma
+  b.dkg = o; o += ck;   // dKg * Kg (the gamma_C part of the Kg gradient)
+  b.u = o; o += cv;     // U
+  b.vn = o; o += cv;    // V_new
+  b.dvn = o; o += cv;   // dV_new
+  b.x = o; o += cv;     // X = A^T dV_new
+  b.aqk = o; o += cc;   // Aqk
+  b.p = o; o += cc;     // P (strictly lower, without beta)
+  b.beta = o; o += C;
+  b.decay = o; o += K;  // e^gamma_C
+  b.floats = (o + 63) / 64 * 64;
+  return b;
+}
+
+// Resolved sizes and workspace layout of one backward call.
+struct Plan {
+  int B, T, H, HV, K, V, C, N, G;
+  int64_t ntok, nct;
+  int nc_per_seq, varlen;
+  size_t off_table;   // int64 [N + 1] chunk offsets (varlen only)
+  size_t off_blocks;  // [nct][HV] blocks
+  size_t off_h;       // fp32 [nct][HV][K][V]: the state before every chunk
+  size_t off_dh;      // fp32 [nct][HV][K][V]: the gradient of the state after every chunk
+  size_t total_bytes;
+  Block blk;
+};
+
+inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Plan of a checked parameter set (host only).
+inline Plan make_plan(const kda_fwd_params* f) {
+  Plan p;
+  memset(&p, 0, sizeof p);
+  p.B = f->B; p.T = f->T; p.H = f->H; p.HV = f->HV; p.K = f->K; p.V = f->V;
+  p.C = f->chunk_size; p.N = f->N; p.G = f->HV / f->H;
+  p.ntok = (int64_t)f->B * f->T;
+  p.varlen = f->cu_seqlens != nullptr || f->cu_seqlens_host != nullptr;
+  p.nc_per_seq = (f->T + p.C - 1) / p.C;
+  if (p.varlen) {
+    int64_t nct = 0;
+    for (int n = 0; n < f->N; ++n)
+      nct += (f->cu_seqlens_host[n + 1] - f->cu_seqlens_host[n] + p.C - 1) / p.C;
+    p.nct = nct;
+  } else {
+    p.nct = (int64_t)f->B * p.nc_per_seq;
+  }
+  p.blk = block_layout(p.C, p.K, p.V);
+  size_t off = 256;
+  p.off_table = off;
+  if (p.varlen) off += round256(sizeof(int64_t) * (size_t)(p.N + 1));
+  p.off_blocks = off;
+  off += round256(sizeof(float) * p.blk.floats * (size_t)p.nct * p.HV);
+  const size_t states = sizeof(float) * (size_t)p.nct * p.HV * p.K * p.V;
+  p.off_h = off;
+  off += round256(states);
+  p.off_dh = off;
+  off += round256(states);
+  p.total_bytes = off;
+  return p;
+}
+
+// Arguments of every stage (passed by value to the kernels).
+struct Args {
+  Plan p;
+  int dtype, gate_mode, qk_l2norm, beta_sigmoid, allow_neg_eigval, state_v_first;
+  float lower_bound, scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* g;
+  const void* beta;
+  const void* d_o;
+  const float* A_log;
+  const float* dt_bias;
+  const float* h0;
+  const float* d_final_state;
+  const int64_t* cu_seqlens;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dg;
+  float* dbeta;
+  float* dA_log;
+  float* ddt_bias;
+  float* dh0;
+  char* ws;
+  unsigned int* status;
+};
+
+// Grid sizes (blocks) of the stages.
+inline int64_t chunk_blocks(const Plan& p) { return p.nct * p.HV; }
+inline int64_t state_blocks(const Plan& p) {
+  return (int64_t)p.N * p.HV * ((p.V + kBV - 1) / kBV);
+}
+// Dynamic shared memory (bytes) of the stages.
+inline size_t states_smem(const Plan& p) { return sizeof(float) * (size_t)(p.K + p.C) * kBV; }
+inline size_t dstate_smem(const Plan& p) { return sizeof(float) * (size_t)(p.K + 2 * p.C) * kBV; }
+inline size_t grads_smem(const Plan& p) {
+  return sizeof(float) * (4 * (size_t)p.C * p.C + 2 * (size_t)p.C + kThreads);
+}
+
+// ---- element helpers ------------------------------------------------------------------
+
+KDA_HD float bits_to_f32(uint32_t u) {
+#if defined(__CUDA_ARCH__)
+  return __uint_as_float(u);
+#else
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+#endif
+}
+
+// Element i of an input tensor (bf16 widens exactly to fp32).
+KDA_HD float ld_in(const void* base, int dtype, size_t i) {
+  return dtype == KDA_F32 ? static_cast<const float*>(base)[i]
+                          : bits_to_f32((uint32_t) static_cast<const uint16_t*>(base)[i] << 16);
+}
+
+KDA_HD float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+// The sigmoid's derivative s(x) (1 - s(x)), as s(x) s(-x): no cancellation once s(x) rounds
+// to 1 (|x| beyond about 17 in fp32).
+KDA_HD float dsigmoid_f(float x) { return sigmoid_f(x) * sigmoid_f(-x); }
+// log(1 + e^x); above 20 the correction log1p(e^-x) < 2.1e-9 is below fp32 resolution of x.
+KDA_HD float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
+
+// The activated log decay of one element ("FLA-KDA engineering notes", section 2), with
+// x = g + dt_bias and `a` = exp(A_log) (1 without A_log in the safe gate).
+KDA_HD float gate_f(int mode, float graw, float a, float dt, float lb) {
+  const float x = graw + dt;
+  if (mode == KDA_GATE_PLAIN) return -a * softplus_f(x);
+  if (mode == KDA_GATE_SAFE) return lb * sigmoid_f(a * x);
+  return graw;
+}
+
+KDA_HD float* block_ptr(const Args& a, int64_t c, int hv) {
+  return reinterpret_cast<float*>(a.ws + a.p.off_blocks) +
+         ((size_t)c * a.p.HV + hv) * a.p.blk.floats;
+}
+
+KDA_HD float* state_ptr(const Args& a, size_t off, int64_t c, int hv) {
+  return reinterpret_cast<float*>(a.ws + off) + ((size_t)c * a.p.HV + hv) * (size_t)a.p.K * a.p.V;
+}
+
+// Sequence n, first token t0 and length L of global chunk c; false if the device-side chunk
+// table disagrees with the plan.
+KDA_HD bool locate(const Args& a, int64_t c, int& n, int64_t& t0, int& L) {
+  const Plan& p = a.p;
+  int64_t bos, eos, ci;
+  if (!p.varlen) {
+    n = (int)(c / p.nc_per_seq);
+    ci = c - (int64_t)n * p.nc_per_seq;
+    bos = (int64_t)n * p.T;
+    eos = bos + p.T;
+  } else {
+    const int64_t* cs = reinterpret_cast<const int64_t*>(a.ws + p.off_table);
+    int lo = 0, hi = p.N;  // n with cs[n] <= c < cs[n + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cs[mid] <= c) lo = mid; else hi = mid;
+    }
+    n = lo;
+    ci = c - cs[n];
+    bos = a.cu_seqlens[n];
+    eos = a.cu_seqlens[n + 1];
+  }
+  t0 = bos + ci * p.C;
+  const int64_t len = eos - t0;
+  if (ci < 0 || t0 < 0 || len <= 0 || eos > p.ntok) return false;
+  L = (int)(len < p.C ? len : p.C);
+  return true;
+}
+
+// Token range and first global chunk of sequence n; false if inconsistent.
+KDA_HD bool seq_range(const Args& a, int n, int64_t& bos, int64_t& eos, int64_t& cfirst) {
+  const Plan& p = a.p;
+  if (!p.varlen) {
+    bos = (int64_t)n * p.T;
+    eos = bos + p.T;
+    cfirst = (int64_t)n * p.nc_per_seq;
+    return true;
+  }
+  bos = a.cu_seqlens[n];
+  eos = a.cu_seqlens[n + 1];
+  cfirst = reinterpret_cast<const int64_t*>(a.ws + p.off_table)[n];
+  return bos >= 0 && eos >= bos && eos <= p.ntok && cfirst >= 0 &&
+         cfirst + (eos - bos + p.C - 1) / p.C <= p.nct;
+}
+
+// ---- prep: per (chunk c, value head hv) ------------------------------------------------
+
+template <class Exec>
+KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv) {
+  const Plan& p = a.p;
+  const int C = p.C, K = p.K, V = p.V, H = p.H, HV = p.HV, h = hv / p.G;
+  int n, L;
+  int64_t t0;
+  if (!locate(a, c, n, t0, L)) {
+    ex.flag(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  float* blk = block_ptr(a, c, hv);
+  const Block& b = p.blk;
+  float* Gam = blk + b.gam;
+  float* Qn = blk + b.qn;
+  float* Kn = blk + b.kn;
+  float* Qg = blk + b.qg;
+  float* Kg = blk + b.kg;
+  float* W = blk + b.w;
+  float* U = blk + b.u;
+  float* Aqk = blk + b.aqk;
+  float* P = blk + b.p;
+  float* Be = blk + b.beta;
+  float* Dc = blk + b.decay;
+  const bool has_alog = a.A_log != nullptr && a.gate_mode != KDA_GATE_PREGATED;
+  const float a_exp = has_alog ? expf(a.A_log[hv]) : 1.0f;
+
+  // gate activation, q and k rows, beta; rows i >= L are zero
+  ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < C * K; e += nthr) {
+      const int i = e / K, kk = e - (e / K) * K;
+      float gv = 0.f, qv = 0.f, kv = 0.f;
+      if (i < L) {
+        const size_t tok = (size_t)(t0 + i);
+        const float dt = (a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED)
+                             ? a.dt_bias[(size_t)hv * K + kk] : 0.f;
+        gv = gate_f(a.gate_mode, ld_in(a.g, a.dtype, (tok * HV + hv) * K + kk), a_exp, dt,
+                    a.lower_bound);
+        qv = ld_in(a.q, a.dtype, (tok * H + h) * K + kk);
+        kv = ld_in(a.k, a.dtype, (tok * H + h) * K + kk);
+      }
+      Gam[e] = gv;
+      Qn[e] = qv;
+      Kn[e] = kv;
+    }
+    for (int i = tid; i < C; i += nthr) {
+      float bv = 0.f;
+      if (i < L) {
+        bv = ld_in(a.beta, a.dtype, (size_t)(t0 + i) * HV + hv);
+        if (a.beta_sigmoid) bv = (a.allow_neg_eigval ? 2.f : 1.f) * sigmoid_f(bv);
+      }
+      Be[i] = bv;
+    }
+  });
+  // chunk-local cumsum (one thread per channel); L2 norm and scale of the rows (one thread
+  // per row of q or k)
+  ex.phase([&](int tid, int nthr) {
+    for (int kk = tid; kk < K; kk += nthr) {
+      float acc = 0.f;
+      for (int i = 0; i < L; ++i) {
+        acc += Gam[(size_t)i * K + kk];
+        Gam[(size_t)i * K + kk] = acc;
+      }
+    }
+    for (int r = tid; r < 2 * C; r += nthr) {
+      const int i = r < C ? r : r - C;
+      if (i >= L) continue;
+      float* row = (r < C ? Qn : Kn) + (size_t)i * K;
+      float mul = 1.f;
+      if (a.qk_l2norm) {
+        float ss = 0.f;
+        for (int kk = 0; kk < K; ++kk) ss = fmaf(row[kk], row[kk], ss);
+        mul = 1.0f / sqrtf(ss + kL2Eps);
+      }
+      if (r < C) mul *= a.scale;
+      for (int kk = 0; kk < K; ++kk) row[kk] *= mul;
+    }
+  });
+  // Aqk (j <= i) and P (j < i); e^gamma_C; Qg, Kg; the right-hand sides of W and U
+  ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < C * C; e += nthr) {
+      const int i = e / C, j = e - (e / C) * C;
+      float sq = 0.f, sk = 0.f;
+      if (i < L && j <= i) {
+        const float* gi = Gam + (size_t)i * K;
+        const float* gj = Gam + (size_t)j * K;
+        const float* qi = Qn + (size_t)i * K;
+        const float* ki = Kn + (size_t)i * K;
+        const float* kj = Kn + (size_t)j * K;
+        for (int kk = 0; kk < K; ++kk) {
+          const float kd = kj[kk] * expf(gi[kk] - gj[kk]);
+          sq = fmaf(qi[kk], kd, sq);
+          sk = fmaf(ki[kk], kd, sk);
+        }
+      }
+      Aqk[e] = sq;
+      P[e] = j < i ? sk : 0.f;
+    }
+    for (int kk = tid; kk < K; kk += nthr) Dc[kk] = expf(Gam[(size_t)(L - 1) * K + kk]);
+    for (int e = tid; e < C * K; e += nthr) {
+      const int i = e / K, kk = e - (e / K) * K;
+      float qg = 0.f, kg = 0.f, w = 0.f;
+      if (i < L) {
+        const float gi = Gam[e], eg = expf(gi);
+        qg = Qn[e] * eg;
+        kg = Kn[e] * expf(Gam[(size_t)(L - 1) * K + kk] - gi);
+        w = Be[i] * eg * Kn[e];
+      }
+      Qg[e] = qg;
+      Kg[e] = kg;
+      W[e] = w;
+    }
+    for (int e = tid; e < C * V; e += nthr) {
+      const int i = e / V, cc = e - (e / V) * V;
+      U[e] = i < L ? Be[i] * ld_in(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + cc) : 0.f;
+    }
+  });
+  // W and U: forward substitution with (I + Diag(beta) P), one thread per column
+  ex.phase([&](int tid, int nthr) {
+    for (int col = tid; col < K + V; col += nthr) {
+      float* X = col < K ? W + col : U + (col - K);
+      const size_t ld = col < K ? (size_t)K : (size_t)V;
+      for (int i = 1; i < L; ++i) {
+        float x = X[i * ld];
+        const float bi = Be[i];
+        const float* pr = P + (size_t)i * C;
+        for (int j = 0; j < i; ++j) x = fmaf(-bi * pr[j], X[j * ld], x);
+        X[i * ld] = x;
+      }
+    }
+  });
+}
+
+// ---- states: per (sequence, value head, V tile), chunks in order ------------------------
+
+template <class Exec>
+KDA_BODY void states_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
+  const Plan& p = a.p;
+  const int C = p.C, K = p.K, V = p.V, HV = p.HV;
+  const int nvt = (V + kBV - 1) / kBV;
+  const int vt = (int)(bid % nvt);
+  const int hv = (int)((bid / nvt) % HV);
+  const int n = (int)(bid / ((int64_t)nvt * HV));
+  int64_t bos, eos, cfirst;
+  if (!seq_range(a, n, bos, eos, cfirst)) {
+    ex.flag(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const Block& b = p.blk;
+  float* sS = smem;                     // [K][kBV] the state tile
+  float* sVn = smem + (size_t)K * kBV;  // [C][kBV] V_new tile
+  const int c0 = vt * kBV;
+  const int nc = V - c0 < kBV ? V - c0 : kBV;  // columns of this tile
+  const size_t sbase = ((size_t)n * HV + hv) * (size_t)K * V;
+  ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < K * kBV; e += nthr) {
+      const int kk = e / kBV, cl = e - (e / kBV) * kBV;
+      float s = 0.f;
+      if (cl < nc && a.h0 != nullptr)
+        s = a.h0[sbase + (a.state_v_first ? (size_t)(c0 + cl) * K + kk : (size_t)kk * V + c0 + cl)];
+      sS[e] = s;
+    }
+  });
+  const int64_t nch = (eos - bos + C - 1) / C;
+  for (int64_t ci = 0; ci < nch; ++ci) {
+    const int64_t c = cfirst + ci;
+    const int64_t rem = eos - (bos + ci * C);
+    const int L = (int)(rem < C ? rem : C);
+    const float* blk = block_ptr(a, c, hv);
+    const float* W = blk + b.w;
+    const float* U = blk + b.u;
+    const float* Kg = blk + b.kg;
+    const float* Dc = blk + b.decay;
+    float* Vn = block_ptr(a, c, hv) + b.vn;
+    float* hS = state_ptr(a, p.off_h, c, hv);
+    // the state before this chunk; V_new = U - W S
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < K * kBV; e += nthr) {
+        const int kk = e / kBV, cl = e - (e / kBV) * kBV;
+        if (cl < nc) hS[(size_t)kk * V + c0 + cl] = sS[e];
+      }
+      for (int e = tid; e < C * kBV; e += nthr) {
+        const int i = e / kBV, cl = e - (e / kBV) * kBV;
+        float vn = 0.f;
+        if (i < L && cl < nc) {
+          vn = U[(size_t)i * V + c0 + cl];
+          const float* wr = W + (size_t)i * K;
+          for (int kk = 0; kk < K; ++kk) vn = fmaf(-wr[kk], sS[kk * kBV + cl], vn);
+        }
+        sVn[e] = vn;
+        if (cl < nc) Vn[(size_t)i * V + c0 + cl] = vn;
+      }
+    });
+    // S <- Diag(e^gamma_C) S + Kg^T V_new
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < K * kBV; e += nthr) {
+        const int kk = e / kBV, cl = e - (e / kBV) * kBV;
+        float s = sS[e] * Dc[kk];
+        for (int i = 0; i < L; ++i) s = fmaf(Kg[(size_t)i * K + kk], sVn[i * kBV + cl], s);
+        sS[e] = s;
+      }
+    });
+  }
+}
+
+// ---- dstate: per (sequence, value head, V tile), chunks in reverse -----------------------
+
+template <class Exec>
+KDA_BODY void dstate_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
+  const Plan& p = a.p;
+  const int C = p.C, K = p.K, V = p.V, HV = p.HV;
+  const int nvt = (V + kBV - 1) / kBV;
+  const int vt = (int)(bid % nvt);
+  const int hv = (int)((bid / nvt) % HV);
+  const int n = (int)(bid / ((int64_t)nvt * HV));
+  int64_t bos, eos, cfirst;
+  if (!seq_range(a, n, bos, eos, cfirst)) {
+    ex.flag(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const Block& b = p.blk;
+  float* sD = smem;                       // [K][kBV] gradient of the state after the chunk
+  float* sDv = sD + (size_t)K * kBV;      // [C][kBV] dV_new
+  float* sDo = sDv + (size_t)C * kBV;     // [C][kBV] dO
+  const int c0 = vt * kBV;
+  const int nc = V - c0 < kBV ? V - c0 : kBV;
+  const size_t sbase = ((size_t)n * HV + hv) * (size_t)K * V;
+  ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < K * kBV; e += nthr) {
+      const int kk = e / kBV, cl = e - (e / kBV) * kBV;
+      float d = 0.f;
+      if (cl < nc && a.d_final_state != nullptr)
+        d = a.d_final_state[sbase + (a.state_v_first ? (size_t)(c0 + cl) * K + kk
+                                                     : (size_t)kk * V + c0 + cl)];
+      sD[e] = d;
+    }
+  });
+  const int64_t nch = (eos - bos + C - 1) / C;
+  for (int64_t ci = nch - 1; ci >= 0; --ci) {
+    const int64_t c = cfirst + ci;
+    const int64_t t0 = bos + ci * C;
+    const int64_t rem = eos - t0;
+    const int L = (int)(rem < C ? rem : C);
+    const float* blk = block_ptr(a, c, hv);
+    const float* Aqk = blk + b.aqk;
+    const float* Kg = blk + b.kg;
+    const float* Qg = blk + b.qg;
+    const float* W = blk + b.w;
+    const float* Dc = blk + b.decay;
+    float* dVn = block_ptr(a, c, hv) + b.dvn;
+    float* hD = state_ptr(a, p.off_dh, c, hv);
+    // dS' of this chunk; the dO tile
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < K * kBV; e += nthr) {
+        const int kk = e / kBV, cl = e - (e / kBV) * kBV;
+        if (cl < nc) hD[(size_t)kk * V + c0 + cl] = sD[e];
+      }
+      for (int e = tid; e < C * kBV; e += nthr) {
+        const int i = e / kBV, cl = e - (e / kBV) * kBV;
+        sDo[e] = (i < L && cl < nc)
+                     ? ld_in(a.d_o, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + c0 + cl) : 0.f;
+      }
+    });
+    // dV_new = Aqk^T dO + Kg dS'
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < C * kBV; e += nthr) {
+        const int i = e / kBV, cl = e - (e / kBV) * kBV;
+        float d = 0.f;
+        if (i < L && cl < nc) {
+          for (int j = i; j < L; ++j) d = fmaf(Aqk[(size_t)j * C + i], sDo[j * kBV + cl], d);
+          const float* kr = Kg + (size_t)i * K;
+          for (int kk = 0; kk < K; ++kk) d = fmaf(kr[kk], sD[kk * kBV + cl], d);
+        }
+        sDv[e] = d;
+        if (cl < nc) dVn[(size_t)i * V + c0 + cl] = d;
+      }
+    });
+    // dS = Qg^T dO - W^T dV_new + Diag(e^gamma_C) dS'
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < K * kBV; e += nthr) {
+        const int kk = e / kBV, cl = e - (e / kBV) * kBV;
+        float d = sD[e] * Dc[kk];
+        for (int i = 0; i < L; ++i) {
+          d = fmaf(Qg[(size_t)i * K + kk], sDo[i * kBV + cl], d);
+          d = fmaf(-W[(size_t)i * K + kk], sDv[i * kBV + cl], d);
+        }
+        sD[e] = d;
+      }
+    });
+  }
+  if (a.dh0 != nullptr) {
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < K * kBV; e += nthr) {
+        const int kk = e / kBV, cl = e - (e / kBV) * kBV;
+        if (cl < nc)
+          a.dh0[sbase + (a.state_v_first ? (size_t)(c0 + cl) * K + kk : (size_t)kk * V + c0 + cl)] =
+              sD[e];
+      }
+    });
+  }
+}
+
+// ---- grads: per (chunk c, value head hv) -----------------------------------------------
+
+template <class Exec>
+KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem) {
+  const Plan& p = a.p;
+  const int C = p.C, K = p.K, V = p.V, H = p.H, HV = p.HV, h = hv / p.G;
+  int n, L;
+  int64_t t0;
+  if (!locate(a, c, n, t0, L)) {
+    ex.flag(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const Block& b = p.blk;
+  float* blk = block_ptr(a, c, hv);
+  const float* Gam = blk + b.gam;
+  const float* Qn = blk + b.qn;
+  const float* Kn = blk + b.kn;
+  const float* Qg = blk + b.qg;
+  const float* Kg = blk + b.kg;
+  const float* Vn = blk + b.vn;
+  const float* dVn = blk + b.dvn;
+  const float* Aqk = blk + b.aqk;
+  const float* P = blk + b.p;
+  const float* Be = blk + b.beta;
+  const float* Dc = blk + b.decay;
+  float* Y = blk + b.y;
+  float* X = blk + b.x;
+  float* dQ = blk + b.dq;
+  float* dK = blk + b.dk;
+  float* dGam = blk + b.dgam;
+  float* dKG = blk + b.dkg;
+  const float* S = state_ptr(a, p.off_h, c, hv);
+  const float* dSp = state_ptr(a, p.off_dh, c, hv);
+  float* sAk = smem;                          // [C][C] beta_i P_ij
+  float* sdA = sAk + (size_t)C * C;           // [C][C] dAqk
+  float* sZ = sdA + (size_t)C * C;            // [C][C] A^T dA, then A^T dA A^T, then dP
+  float* sAq = sZ + (size_t)C * C;            // [C][C] Aqk
+  float* sB = sAq + (size_t)C * C;            // [C] beta
+  float* sDB = sB + C;                        // [C] gradient of beta (the value)
+  float* sRed = sDB + C;                      // [kThreads] partial sums of dA_log
+  const bool has_alog = a.A_log != nullptr && a.gate_mode != KDA_GATE_PREGATED;
+  const float a_exp = has_alog ? expf(a.A_log[hv]) : 1.0f;
+  auto dO = [&](int i, int v) {
+    return ld_in(a.d_o, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + v);
+  };
+  auto vin = [&](int i, int v) { return ld_in(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + v); };
+
+  // the chunk's C x C matrices; dAqk = (dO V_new^T) masked lower
+  ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < C * C; e += nthr) {
+      const int i = e / C, j = e - (e / C) * C;
+      sAk[e] = Be[i] * P[e];
+      sAq[e] = Aqk[e];
+      float d = 0.f;
+      if (i < L && j <= i)
+        for (int v = 0; v < V; ++v) d = fmaf(dO(i, v), Vn[(size_t)j * V + v], d);
+      sdA[e] = d;
+    }
+    for (int i = tid; i < C; i += nthr) sB[i] = Be[i];
+  });
+  // dQg = dO S^T, dW = -dV_new S^T, dKg = V_new dS'^T and their direct terms
+  ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < C * K; e += nthr) {
+      const int i = e / K, kk = e - (e / K) * K;
+      float y = 0.f, dq = 0.f, dk = 0.f, dg = 0.f, dkg_kg = 0.f;
+      if (i < L) {
+        const float* sr = S + (size_t)kk * V;
+        const float* dr = dSp + (size_t)kk * V;
+        const float* vr = Vn + (size_t)i * V;
+        const float* dvr = dVn + (size_t)i * V;
+        float dqg = 0.f, dw = 0.f, dkg = 0.f;
+        for (int v = 0; v < V; ++v) {
+          dqg = fmaf(dO(i, v), sr[v], dqg);
+          dw = fmaf(-dvr[v], sr[v], dw);
+          dkg = fmaf(vr[v], dr[v], dkg);
+        }
+        const float gi = Gam[e];
+        y = dw;
+        dq = dqg * expf(gi);
+        dk = dkg * expf(Gam[(size_t)(L - 1) * K + kk] - gi);
+        dkg_kg = dkg * Kg[e];
+        dg = dqg * Qg[e] - dkg_kg;
+      }
+      Y[e] = y;
+      dQ[e] = dq;
+      dK[e] = dk;
+      dGam[e] = dg;
+      dKG[e] = dkg_kg;
+    }
+  });
+  // X = A^T dV_new, Y = A^T dW: back substitution with (I + Diag(beta) P)^T, one thread per
+  // column
+  ex.phase([&](int tid, int nthr) {
+    for (int col = tid; col < V + K; col += nthr) {
+      float* Xc = col < V ? X + col : Y + (col - V);
+      const size_t ld = col < V ? (size_t)V : (size_t)K;
+      if (col < V)
+        for (int i = 0; i < C; ++i) Xc[i * ld] = i < L ? dVn[(size_t)i * V + col] : 0.f;
+      for (int i = L - 2; i >= 0; --i) {
+        float x = Xc[i * ld];
+        for (int j = i + 1; j < L; ++j) x = fmaf(-sAk[(size_t)j * C + i], Xc[j * ld], x);
+        Xc[i * ld] = x;
+      }
+    }
+  });
+  // dv; the WY part of dbeta; the e^Gamma K part of dK and dGamma; A^T dA (strictly lower)
+  ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < C * V; e += nthr) {
+      const int i = e / V, v = e - (e / V) * V;
+      if (i < L) a.dv[((size_t)(t0 + i) * HV + hv) * V + v] = sB[i] * X[e];
+    }
+    for (int i = tid; i < C; i += nthr) {
+      float db = 0.f;
+      if (i < L) {
+        for (int v = 0; v < V; ++v) db = fmaf(X[(size_t)i * V + v], vin(i, v), db);
+        for (int kk = 0; kk < K; ++kk) {
+          const size_t e = (size_t)i * K + kk;
+          db = fmaf(Y[e], expf(Gam[e]) * Kn[e], db);
+        }
+      }
+      sDB[i] = db;
+    }
+    for (int e = tid; e < C * K; e += nthr) {
+      const int i = e / K;
+      if (i < L) {
+        const float eg = expf(Gam[e]);
+        const float t = sB[i] * Y[e];
+        dK[e] += t * eg;
+        dGam[e] += t * eg * Kn[e];
+      }
+    }
+    for (int e = tid; e < C * C; e += nthr) {
+      const int i = e / C, j = e - (e / C) * C;
+      float z = 0.f;
+      if (i < L && j < i) {
+        for (int v = 0; v < V; ++v) z = fmaf(X[(size_t)i * V + v], vin(j, v), z);
+        float zk = 0.f;
+        for (int kk = 0; kk < K; ++kk)
+          zk = fmaf(Y[(size_t)i * K + kk], expf(Gam[(size_t)j * K + kk]) * Kn[(size_t)j * K + kk], zk);
+        z = sB[j] * (z + zk);
+      }
+      sZ[e] = z;
+    }
+  });
+  // dAkk = -(A^T dA A^T) masked strictly lower (row r of A^T dA A^T is A applied to row r of
+  // A^T dA: forward substitution, one thread per row); dP = beta dAkk; dbeta += rowsum(dAkk P)
+  ex.phase([&](int tid, int nthr) {
+    for (int r = tid; r < L; r += nthr) {
+      float* z = sZ + (size_t)r * C;
+      for (int i = 1; i < r; ++i) {
+        float x = z[i];
+        for (int j = 0; j < i; ++j) x = fmaf(-sAk[(size_t)i * C + j], z[j], x);
+        z[i] = x;
+      }
+      float db = 0.f;
+      for (int i = 0; i < r; ++i) {
+        const float d = -z[i];
+        db = fmaf(d, P[(size_t)r * C + i], db);
+        z[i] = sB[r] * d;
+      }
+      sDB[r] += db;
+    }
+  });
+  // the e^(Gamma_i - Gamma_j) terms of Aqk and P, one thread per (row r, channel k): r as
+  // the row index i (dQ, dK) and as the column index j (dK)
+  ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < C * K; e += nthr) {
+      const int r = e / K, kk = e - (e / K) * K;
+      if (r >= L) continue;
+      const float gr = Gam[e];
+      float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
+      for (int j = 0; j <= r; ++j) {
+        const float kd = Kn[(size_t)j * K + kk] * expf(gr - Gam[(size_t)j * K + kk]);
+        s1 = fmaf(sdA[(size_t)r * C + j], kd, s1);
+        if (j < r) s2 = fmaf(sZ[(size_t)r * C + j], kd, s2);
+      }
+      for (int i = r; i < L; ++i) {
+        const float ed = expf(Gam[(size_t)i * K + kk] - gr);
+        s3 = fmaf(sdA[(size_t)i * C + r], Qn[(size_t)i * K + kk] * ed, s3);
+        if (i > r) s4 = fmaf(sZ[(size_t)i * C + r], Kn[(size_t)i * K + kk] * ed, s4);
+      }
+      dQ[e] += s1;
+      dK[e] += s2 + s3 + s4;
+      dGam[e] += Qn[e] * s1 + Kn[e] * (s2 - s3 - s4);
+    }
+  });
+  // reverse cumsum of dGamma (plus the gamma_C terms on the last row) and the gate backward,
+  // one thread per channel
+  ex.phase([&](int tid, int nthr) {
+    float alog_part = 0.f;
+    for (int kk = tid; kk < K; kk += nthr) {
+      float dgc = 0.f;
+      const float* sr = S + (size_t)kk * V;
+      const float* dr = dSp + (size_t)kk * V;
+      for (int v = 0; v < V; ++v) dgc = fmaf(sr[v], dr[v], dgc);
+      dgc *= Dc[kk];
+      for (int i = 0; i < L; ++i) dgc += dKG[(size_t)i * K + kk];
+      const float dt = (a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED)
+                           ? a.dt_bias[(size_t)hv * K + kk] : 0.f;
+      float run = dgc, dt_part = 0.f;
+      for (int i = L - 1; i >= 0; --i) {
+        run += dGam[(size_t)i * K + kk];
+        const size_t gi = ((size_t)(t0 + i) * HV + hv) * K + kk;
+        float dx = run;
+        if (a.gate_mode == KDA_GATE_PLAIN) {
+          const float x = ld_in(a.g, a.dtype, gi) + dt;
+          dx = run * (-a_exp) * sigmoid_f(x);
+          alog_part = fmaf(run * (-a_exp), softplus_f(x), alog_part);
+        } else if (a.gate_mode == KDA_GATE_SAFE) {
+          const float x = ld_in(a.g, a.dtype, gi) + dt;
+          const float ds = run * a.lower_bound * dsigmoid_f(a_exp * x);
+          dx = ds * a_exp;
+          alog_part = fmaf(ds * a_exp, x, alog_part);
+        }
+        a.dg[gi] = dx;
+        dt_part += dx;
+      }
+      if (a.ddt_bias != nullptr) ex.atomic_add(a.ddt_bias + (size_t)hv * K + kk, dt_part);
+    }
+    sRed[tid] = alog_part;
+  });
+  // dA_log; the L2-norm backward of q and k (one thread per row); dbeta
+  ex.phase([&](int tid, int nthr) {
+    if (tid == 0 && a.dA_log != nullptr && has_alog) {
+      float s = 0.f;
+      for (int t = 0; t < nthr; ++t) s += sRed[t];
+      ex.atomic_add(a.dA_log + hv, s);
+    }
+    for (int r = tid; r < 2 * C; r += nthr) {
+      const int i = r < C ? r : r - C;
+      if (i >= L) continue;
+      const float* dx = (r < C ? dQ : dK) + (size_t)i * K;
+      const float mul = r < C ? a.scale : 1.f;  // Q = scale * q / |q|
+      const void* src = r < C ? a.q : a.k;
+      float* dst = (r < C ? a.dq : a.dk) + ((size_t)(t0 + i) * H + h) * K;
+      const size_t row = ((size_t)(t0 + i) * H + h) * K;
+      float inv = 1.f, dot = 0.f;
+      if (a.qk_l2norm) {
+        float ss = 0.f;
+        for (int kk = 0; kk < K; ++kk) {
+          const float x = ld_in(src, a.dtype, row + kk);
+          ss = fmaf(x, x, ss);
+        }
+        inv = 1.0f / sqrtf(ss + kL2Eps);
+        for (int kk = 0; kk < K; ++kk) dot = fmaf(ld_in(src, a.dtype, row + kk) * inv, mul * dx[kk], dot);
+      }
+      for (int kk = 0; kk < K; ++kk) {
+        const float d = mul * dx[kk];
+        const float val = a.qk_l2norm ? (d - ld_in(src, a.dtype, row + kk) * inv * dot) * inv : d;
+        if (p.G == 1) dst[kk] = val; else ex.atomic_add(dst + kk, val);
+      }
+    }
+    for (int i = tid; i < L; i += nthr) {
+      float db = sDB[i];
+      if (a.beta_sigmoid) {
+        db *= (a.allow_neg_eigval ? 2.f : 1.f) *
+              dsigmoid_f(ld_in(a.beta, a.dtype, (size_t)(t0 + i) * HV + hv));
+      }
+      a.dbeta[(size_t)(t0 + i) * HV + hv] = db;
+    }
+  });
+}
+
+}  // namespace bwd
+}  // namespace kda

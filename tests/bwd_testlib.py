@@ -1,0 +1,157 @@
+"""Helpers of the backward tests: seeded upstream gradients, the oracle's gradients of the
+same inputs, the host emulation of the backward stage bodies, and the comparison."""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+
+import numpy as np
+
+from kimi_delta_attention_gate_gb300 import inputs as kin
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+EMU_SRC = os.path.join(ROOT, "tests", "emulation", "kda_bwd_emu.cpp")
+GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias", "dh0")
+
+# rel-L2 bounds of each gradient against the fp64 oracle.  The kernels compute in fp32 from
+# inputs that are exact in fp32 (bf16 widens exactly), so only fp32 rounding separates them.
+# Most gradients are short chains of dot products over K, V and the chunk (relative error a
+# few 1e-7 measured on the emulation); 1e-4, the fp32 forward's bound, leaves a wide margin.
+# The gate gradients pass through a cancellation that the method itself contains: dGamma is a
+# row sum minus a column sum of the same e^(Gamma_i - Gamma_j) terms, then summed in reverse
+# over the chunk, and dA_log / ddt_bias sum dg over the tokens.  With the safe gate near its
+# bound this costs about two decimal digits (measured: dg 3e-5, dA_log 1e-4, ddt_bias 2.4e-4);
+# those three get 1e-3.
+REL_L2 = 1e-4
+REL_L2_GATE = 1e-3
+GATE_GRADS = ("dg", "dA_log", "ddt_bias")
+
+
+def upstream(inp: kin.Inputs, seed: int, state_v_first: bool = False):
+    """Seeded gradients of o ([B,T,HV,V], in the input dtype's values) and of final_state
+    ([N,HV,K,V] fp32, or [N,HV,V,K])."""
+    wl = inp.wl
+    rng = np.random.default_rng(seed)
+    d_o = rng.standard_normal((wl.B, wl.T, wl.HV, wl.V), dtype=np.float32)
+    if wl.dtype == "bf16":
+        kin.round_to_bf16(d_o)
+    dfs = rng.standard_normal((inp.N, wl.HV, wl.K, wl.V), dtype=np.float32)
+    if state_v_first:
+        dfs = np.ascontiguousarray(np.swapaxes(dfs, -1, -2))
+    return d_o, dfs
+
+
+def oracle_grads(inp: kin.Inputs, d_o, dfs, *, allow_neg_eigval=False, state_v_first=False,
+                 chunk_form=False) -> dict:
+    """The oracle's gradients (fp64) for the inputs of ``inp`` (h0 and dfs in the layout that
+    ``state_v_first`` names): the autograd form, or with ``chunk_form`` the chunked form."""
+    from oracle import backward as ob
+    wl = inp.wl
+    lb = wl.lower_bound if wl.gate == kin.GATE_SAFE else None
+    fn = ob.chunk_bwd_np if chunk_form else ob.bwd
+    extra = dict(chunk_size=wl.chunk_size) if chunk_form else {}
+    f64 = lambda x: None if x is None else np.asarray(x, np.float64)
+    return fn(f64(inp.q), f64(inp.k), f64(inp.v), f64(inp.g), f64(inp.beta), f64(d_o), f64(dfs),
+              A_log=f64(inp.A_log), dt_bias=f64(inp.dt_bias), gate_mode=wl.gate, lower_bound=lb,
+              scale=inp.scale, qk_l2norm=True, beta_sigmoid=True, allow_neg_eigval=allow_neg_eigval,
+              initial_state=f64(inp.h0), cu_seqlens=inp.cu_seqlens,
+              transpose_state_layout=state_v_first, **extra)
+
+
+def build_emulator(out_dir: str) -> str:
+    """Compile the host emulation of the backward stage bodies with AddressSanitizer and
+    UndefinedBehaviorSanitizer; returns the executable's path."""
+    gxx = shutil.which("g++")
+    if gxx is None:
+        raise RuntimeError("g++ not found")
+    exe = os.path.join(out_dir, "kda_bwd_emu")
+    cmd = [gxx, "-std=c++17", "-O1", "-g", "-fsanitize=address,undefined", "-fno-omit-frame-pointer",
+           "-fno-sanitize-recover=all", "-Wall", "-Wextra", "-Werror",
+           "-I", os.path.join(ROOT, "include"),
+           "-I", os.path.join(ROOT, "kimi_delta_attention_gate_gb300", "csrc"), EMU_SRC, "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"emulator build failed:\n{r.stdout}\n{r.stderr}")
+    return exe
+
+
+def _raw(x: np.ndarray, dtype: str) -> bytes:
+    if dtype == "bf16":
+        return kin.to_bf16_bits(x).tobytes()
+    return np.ascontiguousarray(x, np.float32).tobytes()
+
+
+def run_emulator(exe: str, workdir: str, inp: kin.Inputs, d_o, dfs, *, seed=0,
+                 allow_neg_eigval=False, state_v_first=False, want=GRADS) -> dict:
+    """The backward stage bodies on the host: returns {gradient name: fp64 array} (the
+    optional ones only when requested and defined) and the device status bits."""
+    wl = inp.wl
+    os.makedirs(workdir, exist_ok=True)
+    has = dict(A_log=inp.A_log is not None, dt_bias=inp.dt_bias is not None, h0=inp.h0 is not None,
+               cu_seqlens=inp.cu_seqlens is not None, d_final_state=dfs is not None)
+    in_gate = wl.gate != kin.GATE_PREGATED
+    spec = dict(B=wl.B, T=wl.T, H=wl.H, HV=wl.HV, K=wl.K, V=wl.V, chunk_size=wl.chunk_size,
+                in_dtype=0 if wl.dtype == "bf16" else 1, gate_mode=wl.gate,
+                lower_bound=wl.lower_bound if wl.gate == kin.GATE_SAFE else 0.0,
+                scale=repr(float(np.float32(inp.scale))), qk_l2norm=1, beta_sigmoid=1,
+                N=inp.N, allow_neg_eigval=int(allow_neg_eigval), state_v_first=int(state_v_first),
+                seed=seed, **{f"has_{k}": int(v) for k, v in has.items()},
+                want_dA_log=int("dA_log" in want and has["A_log"] and in_gate),
+                want_ddt_bias=int("ddt_bias" in want and has["dt_bias"] and in_gate),
+                want_dh0=int("dh0" in want))
+    with open(os.path.join(workdir, "spec.txt"), "w") as f:
+        for key, val in spec.items():
+            f.write(f"{key} {val}\n")
+    files = dict(q=_raw(inp.q, wl.dtype), k=_raw(inp.k, wl.dtype), v=_raw(inp.v, wl.dtype),
+                 g=_raw(inp.g, wl.dtype), beta=_raw(inp.beta, wl.dtype), d_o=_raw(d_o, wl.dtype))
+    if has["A_log"]:
+        files["A_log"] = _raw(inp.A_log, "f32")
+    if has["dt_bias"]:
+        files["dt_bias"] = _raw(inp.dt_bias, "f32")
+    if has["h0"]:
+        files["h0"] = _raw(inp.h0, "f32")
+    if has["cu_seqlens"]:
+        files["cu_seqlens"] = np.ascontiguousarray(inp.cu_seqlens, np.int64).tobytes()
+    if has["d_final_state"]:
+        files["d_final_state"] = _raw(dfs, "f32")
+    for name, data in files.items():
+        with open(os.path.join(workdir, name + ".bin"), "wb") as f:
+            f.write(data)
+    env = dict(os.environ, ASAN_OPTIONS="detect_leaks=0:abort_on_error=0",
+               UBSAN_OPTIONS="print_stacktrace=1")
+    r = subprocess.run([exe, workdir], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        raise AssertionError(f"emulator failed ({r.returncode}):\n{r.stdout}\n{r.stderr[-4000:]}")
+    shapes = dict(dq=inp.q.shape, dk=inp.k.shape, dv=inp.v.shape, dg=inp.g.shape,
+                  dbeta=inp.beta.shape, dA_log=(wl.HV,), ddt_bias=(wl.HV * wl.K,),
+                  dh0=(inp.N, wl.HV, wl.V, wl.K) if state_v_first else (inp.N, wl.HV, wl.K, wl.V))
+    out = {}
+    for name in GRADS:
+        path = os.path.join(workdir, f"out_{name}.bin")
+        if os.path.exists(path):
+            out[name] = np.fromfile(path, np.float32).reshape(shapes[name]).astype(np.float64)
+    with open(os.path.join(workdir, "out_status.txt")) as f:
+        out["status"] = int(f.read().split()[0])
+    return out
+
+
+def rel_l2(got, ref) -> float:
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
+def assert_grads_close(got: dict, ref: dict, names=GRADS):
+    """Every gradient in ``names`` that ``ref`` defines is present in ``got``, finite, and
+    within its rel-L2 bound; returns the errors."""
+    errs = {}
+    for name in names:
+        if ref.get(name) is None:
+            continue
+        assert name in got, f"{name} missing"
+        g = got[name]
+        assert g.shape == ref[name].shape, (name, g.shape, ref[name].shape)
+        assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+        errs[name] = rel_l2(g, ref[name])
+        tol = REL_L2_GATE if name in GATE_GRADS else REL_L2
+        assert errs[name] <= tol, f"{name}: rel-L2 {errs[name]:.3e} > {tol:.0e}"
+    return errs

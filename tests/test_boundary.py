@@ -12,7 +12,8 @@ from kimi_delta_attention_gate_gb300 import _binding as kb
 from kimi_delta_attention_gate_gb300 import build as kbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "kda.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -22,7 +23,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
 
@@ -43,11 +44,19 @@ def test_status_strings(lib):
     assert kb.kda_status_string(0) == "ok"
 
 
+def test_every_header_is_covered():
+    assert [os.path.basename(h) for h in HEADERS] == ["kda.h", "kda_bwd.h"]
+
+
 def test_struct_layout_matches_header():
     # int32 x 9, float x 2, int32 x 5 -> 64 bytes, then 14 pointers and a size_t
     assert kb.kda_fwd_params.q.offset == 64
     assert kb.kda_fwd_params.workspace_bytes.offset == 64 + 14 * 8
     assert ctypes.sizeof(kb.kda_fwd_params) == 64 + 15 * 8
+    # the forward block, then 11 pointers and a size_t
+    assert kb.kda_bwd_params.d_o.offset == ctypes.sizeof(kb.kda_fwd_params)
+    assert kb.kda_bwd_params.workspace_bytes.offset == 184 + 11 * 8
+    assert ctypes.sizeof(kb.kda_bwd_params) == 184 + 12 * 8
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced by the checks
