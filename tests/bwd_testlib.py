@@ -28,6 +28,29 @@ REL_L2_GATE = 1e-3
 GATE_GRADS = ("dg", "dA_log", "ddt_bias")
 
 
+def workload(name="bwd", B=2, T=150, H=1, HV=2, K=32, V=16, C=64, dtype="f32",
+             gate=kin.GATE_SAFE, seed=7, **kw) -> kin.Workload:
+    """A small workload for the backward tests (every gate mode with its usual inputs)."""
+    lb = -5.0 if gate == kin.GATE_SAFE else None
+    kw.setdefault("h0_std", 0.3)
+    if gate == kin.GATE_PLAIN:
+        kw.setdefault("a_log_mean", -1.0)
+        kw.setdefault("a_log_std", 0.5)
+    if gate == kin.GATE_PREGATED:
+        kw.setdefault("has_a_log", False)
+        kw.setdefault("has_dt_bias", False)
+    return kin.Workload(name, B=B, T=T, H=H, HV=HV, K=K, V=V, chunk_size=C, dtype=dtype, gate=gate,
+                        lower_bound=lb, seed=seed, **kw)
+
+
+def pregate(inp: kin.Inputs) -> kin.Inputs:
+    """A log decay in (-1, 0] for the pre-gated mode (g is used as it is)."""
+    inp.g = -np.abs(inp.g) * np.float32(0.5)
+    if inp.wl.dtype == "bf16":
+        kin.round_to_bf16(inp.g)
+    return inp
+
+
 def upstream(inp: kin.Inputs, seed: int, state_v_first: bool = False):
     """Seeded gradients of o ([B,T,HV,V], in the input dtype's values) and of final_state
     ([N,HV,K,V] fp32, or [N,HV,V,K])."""
@@ -155,3 +178,23 @@ def assert_grads_close(got: dict, ref: dict, names=GRADS):
         tol = REL_L2_GATE if name in GATE_GRADS else REL_L2
         assert errs[name] <= tol, f"{name}: rel-L2 {errs[name]:.3e} > {tol:.0e}"
     return errs
+
+
+def run_gpu_bwd(inp: kin.Inputs, d_o, dfs, *, allow_neg_eigval=False, state_v_first=False) -> dict:
+    """kda_bwd (the C ABI through the package's wrapper) on the GPU: {gradient: fp64 array}."""
+    import torch
+    import kimi_delta_attention_gate_gb300 as kda
+    from kda_testlib import f32_device, gate_kwargs, to_device
+    wl = inp.wl
+    q, k, v, g, b, do = (to_device(x, wl.dtype) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta, d_o))
+    cu = None if inp.cu_seqlens is None else torch.from_numpy(inp.cu_seqlens).cuda()
+    cu_cpu = None if inp.cu_seqlens is None else torch.from_numpy(inp.cu_seqlens)
+    res = kda.kda_bwd(q, k, v, g, b, do, dht=f32_device(dfs), A_log=f32_device(inp.A_log),
+                      dt_bias=f32_device(inp.dt_bias), scale=inp.scale,
+                      initial_state=f32_device(inp.h0), cu_seqlens=cu, cu_seqlens_cpu=cu_cpu,
+                      chunk_size=wl.chunk_size, allow_neg_eigval=allow_neg_eigval,
+                      transpose_state_layout=state_v_first, **gate_kwargs(wl))
+    torch.cuda.synchronize()
+    status = kda.kda_get_device_status(0)
+    assert status == 0, f"device status {status:#x}"
+    return {n: t.cpu().double().numpy() for n, t in zip(GRADS, res) if t is not None}

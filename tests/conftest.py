@@ -12,7 +12,14 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
 
 
+# GPU test files that run after all the others (in this order): the backward pass is
+# checked once the forward's tests have all run.
+LAST = ("test_gpu_backward.py",)
+
+
 def pytest_collection_modifyitems(config, items):
+    rank = {name: i + 1 for i, name in enumerate(LAST)}
+    items.sort(key=lambda it: rank.get(os.path.basename(it.nodeid.split("::")[0]), 0))  # stable
     # Run GPU tests only where a GPU exists; on a CPU-only machine they are skipped
     # (the CPU suite is selected with -m "not gpu" anyway).
     try:

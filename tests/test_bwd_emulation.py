@@ -19,26 +19,8 @@ def emu(tmp_path_factory):
     return bt.build_emulator(str(tmp_path_factory.mktemp("bwd_emu")))
 
 
-def wl_(name="bwd", B=2, T=150, H=1, HV=2, K=32, V=16, C=64, dtype="f32", gate=kin.GATE_SAFE,
-        seed=7, **kw):
-    lb = -5.0 if gate == kin.GATE_SAFE else None
-    kw.setdefault("h0_std", 0.3)
-    if gate == kin.GATE_PLAIN:
-        kw.setdefault("a_log_mean", -1.0)
-        kw.setdefault("a_log_std", 0.5)
-    if gate == kin.GATE_PREGATED:
-        kw.setdefault("has_a_log", False)
-        kw.setdefault("has_dt_bias", False)
-    return kin.Workload(name, B=B, T=T, H=H, HV=HV, K=K, V=V, chunk_size=C, dtype=dtype, gate=gate,
-                        lower_bound=lb, seed=seed, **kw)
-
-
-def pregate(inp):
-    """A log decay in (-1, 0] for the pre-gated mode (g is used as it is)."""
-    inp.g = -np.abs(inp.g) * np.float32(0.5)
-    if inp.wl.dtype == "bf16":
-        kin.round_to_bf16(inp.g)
-    return inp
+wl_ = bt.workload
+pregate = bt.pregate
 
 
 def check(emu, tmp_path, inp, *, seed=0, chunk_form=False, up_seed=11, **opts):

@@ -5,7 +5,7 @@ to give the library a workspace).  kda_fwd_noalloc serves them from a static
 device array inside the library.  This test calls it through the C ABI twice in
 a row, on different inputs, and checks each result against kda_fwd (which runs
 with a caller-provided workspace) within the tolerance the parity tests use.
-It sits in a file of its own that pytest collects last."""
+It sits in a file of its own, collected after the other forward tests."""
 import numpy as np
 import pytest
 
