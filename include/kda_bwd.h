@@ -84,6 +84,19 @@ size_t kda_bwd_workspace_size(const kda_bwd_params* p);
    the outputs (cudaMemsetAsync) is not counted.  Host only. */
 int32_t kda_bwd_num_launches(const kda_bwd_params* p);
 
+/* Number of stages of kda_bwd for these parameters (0 if they are invalid): the zeroing of
+   the outputs, then the kernels kda_bwd_num_launches counts.  Host only. */
+int32_t kda_bwd_num_stages(const kda_bwd_params* p);
+
+/* Name of stage `stage` ("zero_outputs", "chunk_table", "bwd_prep", "bwd_states",
+   "bwd_dstate", "bwd_grads"); "" if out of range or the parameters are invalid. */
+const char* kda_bwd_stage_name(const kda_bwd_params* p, int32_t stage);
+
+/* Enqueue only stage `stage` of kda_bwd on `stream`.  Calling every stage in order on one
+   stream computes exactly what kda_bwd computes; the split exists so that a caller can put
+   timing events between the kernels.  Same checks and errors as kda_bwd. */
+kda_status kda_bwd_stage(const kda_bwd_params* p, void* stream, int32_t stage);
+
 /* The backward pass, enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
    Asynchronous: returns once the work is enqueued.  Returns KDA_ERR_CUDA if a launch
    fails; kda_get_device_status reports inconsistent device-side cu_seqlens as for kda_fwd. */

@@ -39,7 +39,8 @@ EXPORTED = ("kda_fwd_workspace_size", "kda_fwd_check", "kda_fwd", "kda_fwd_num_l
             "kda_fwd_num_stages",
             "kda_fwd_stage_name", "kda_fwd_stage", "kda_get_device_status", "kda_status_string",
             "kda_last_error", "kda_abi_version", "kda_fwd_noalloc",
-            "kda_bwd_check", "kda_bwd_workspace_size", "kda_bwd_num_launches", "kda_bwd")
+            "kda_bwd_check", "kda_bwd_workspace_size", "kda_bwd_num_launches", "kda_bwd",
+            "kda_bwd_num_stages", "kda_bwd_stage_name", "kda_bwd_stage")
 
 # Size of the static device scratch behind kda_fwd_noalloc (KDA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -139,6 +140,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kda_bwd_num_launches.argtypes = [PB]
             lib.kda_bwd.restype = ctypes.c_int
             lib.kda_bwd.argtypes = [PB, ctypes.c_void_p]
+            lib.kda_bwd_num_stages.restype = ctypes.c_int32
+            lib.kda_bwd_num_stages.argtypes = [PB]
+            lib.kda_bwd_stage_name.restype = ctypes.c_char_p
+            lib.kda_bwd_stage_name.argtypes = [PB, ctypes.c_int32]
+            lib.kda_bwd_stage.restype = ctypes.c_int
+            lib.kda_bwd_stage.argtypes = [PB, ctypes.c_void_p, ctypes.c_int32]
             _lib = lib
     return _lib
 
@@ -222,6 +229,18 @@ def kda_bwd_num_launches(p: kda_bwd_params) -> int:
 
 def kda_bwd(p: kda_bwd_params, stream: int = 0) -> int:
     return int(load().kda_bwd(ctypes.byref(p), ctypes.c_void_p(stream)))
+
+
+def kda_bwd_num_stages(p: kda_bwd_params) -> int:
+    return int(load().kda_bwd_num_stages(ctypes.byref(p)))
+
+
+def kda_bwd_stage_name(p: kda_bwd_params, stage: int) -> str:
+    return load().kda_bwd_stage_name(ctypes.byref(p), int(stage)).decode()
+
+
+def kda_bwd_stage(p: kda_bwd_params, stream: int, stage: int) -> int:
+    return int(load().kda_bwd_stage(ctypes.byref(p), ctypes.c_void_p(stream), int(stage)))
 
 
 def raise_for(status: int) -> None:

@@ -115,6 +115,97 @@ Args make_args(const kda_bwd_params* p, const Plan& pl, unsigned int* status) {
   return a;
 }
 
+cudaError_t run_zero(const Args& a, cudaStream_t st) {
+  const Plan& pl = a.p;
+  auto zero = [&](void* ptr, size_t bytes) {
+    return ptr == nullptr || bytes == 0 ? cudaSuccess : cudaMemsetAsync(ptr, 0, bytes, st);
+  };
+  const size_t ntok = (size_t)pl.ntok;
+  const struct { void* ptr; size_t bytes; } outs[] = {
+      {a.dq, ntok * pl.H * pl.K * sizeof(float)},     {a.dk, ntok * pl.H * pl.K * sizeof(float)},
+      {a.dv, ntok * pl.HV * pl.V * sizeof(float)},    {a.dg, ntok * pl.HV * pl.K * sizeof(float)},
+      {a.dbeta, ntok * pl.HV * sizeof(float)},        {a.dA_log, (size_t)pl.HV * sizeof(float)},
+      {a.ddt_bias, (size_t)pl.HV * pl.K * sizeof(float)},
+  };
+  for (auto& o : outs) {
+    cudaError_t e = zero(o.ptr, o.bytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t run_chunk_table(const Args& a, cudaStream_t st) {
+  const Plan& pl = a.p;
+  FwdArgs t{};  // the forward's chunk-table kernel, writing into this workspace
+  t.plan.N = pl.N; t.plan.C = pl.C; t.plan.nct = pl.nct; t.plan.ntok = pl.ntok;
+  t.plan.varlen = true; t.plan.off_chunk_table = pl.off_table;
+  t.cu_seqlens = a.cu_seqlens; t.ws = a.ws; t.status = a.status;
+  return launch_chunk_table(t, st);
+}
+
+cudaError_t run_prep(const Args& a, cudaStream_t st) {
+  prep_kernel<<<dim3((unsigned)a.p.nct, (unsigned)a.p.HV), kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <class Kernel>
+cudaError_t launch_smem(Kernel kernel, dim3 grid, size_t smem, const Args& a, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t run_states(const Args& a, cudaStream_t st) {
+  return launch_smem(states_kernel, dim3((unsigned)state_blocks(a.p)), states_smem(a.p), a, st);
+}
+
+cudaError_t run_dstate(const Args& a, cudaStream_t st) {
+  return launch_smem(dstate_kernel, dim3((unsigned)state_blocks(a.p)), dstate_smem(a.p), a, st);
+}
+
+cudaError_t run_grads(const Args& a, cudaStream_t st) {
+  return launch_smem(grads_kernel, dim3((unsigned)a.p.nct, (unsigned)a.p.HV), grads_smem(a.p), a, st);
+}
+
+struct Stage {
+  const char* name;
+  cudaError_t (*run)(const Args&, cudaStream_t);
+};
+constexpr int kMaxStages = 6;
+
+// The stages of one backward call, in order: the zeroing of the outputs (cudaMemsetAsync,
+// no kernel of this library), then the kernels.
+int stages_for(const Plan& pl, Stage* out) {
+  int n = 0;
+  out[n++] = {"zero_outputs", run_zero};
+  if (pl.varlen) out[n++] = {"chunk_table", run_chunk_table};
+  if (pl.nct > 0) out[n++] = {"bwd_prep", run_prep};
+  if (state_blocks(pl) > 0) {
+    out[n++] = {"bwd_states", run_states};
+    out[n++] = {"bwd_dstate", run_dstate};
+  }
+  if (pl.nct > 0) out[n++] = {"bwd_grads", run_grads};
+  return n;
+}
+
+// Checks (host), plan, workspace and the device status word; fills the kernel arguments.
+kda_status prepare(const kda_bwd_params* p, Args& a) {
+  kda_status s = check(p);
+  if (s != KDA_OK) return s;
+  const kda_fwd_params f = fwd_view(p);
+  const Plan pl = make_plan(&f);
+  if (p->workspace == nullptr || p->workspace_bytes < pl.total_bytes)
+    return fail(KDA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu%s)", pl.total_bytes,
+                p->workspace_bytes, p->workspace ? "" : ", NULL");
+  if ((reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0)
+    return fail(KDA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  unsigned int* status = device_status_word();
+  if (status == nullptr) return fail(KDA_ERR_CUDA, "no CUDA device / status word unavailable");
+  a = make_args(p, pl, status);
+  return KDA_OK;
+}
+
 }  // namespace
 }  // namespace bwd
 }  // namespace kda
@@ -139,81 +230,51 @@ size_t kda_bwd_workspace_size(const kda_bwd_params* p) {
 int32_t kda_bwd_num_launches(const kda_bwd_params* p) {
   if (B::check(p) != KDA_OK) return 0;
   const kda_fwd_params f = B::fwd_view(p);
-  const B::Plan pl = B::make_plan(&f);
-  int n = pl.varlen ? 1 : 0;
-  if (pl.nct > 0) n += 2;               // prep, grads
-  if (B::state_blocks(pl) > 0) n += 2;  // states, dstate
-  return n;
+  B::Stage st[B::kMaxStages];
+  return B::stages_for(B::make_plan(&f), st) - 1;  // every stage but the zeroing
+}
+
+int32_t kda_bwd_num_stages(const kda_bwd_params* p) {
+  if (B::check(p) != KDA_OK) return 0;
+  const kda_fwd_params f = B::fwd_view(p);
+  B::Stage st[B::kMaxStages];
+  return B::stages_for(B::make_plan(&f), st);
+}
+
+const char* kda_bwd_stage_name(const kda_bwd_params* p, int32_t stage) {
+  if (B::check(p) != KDA_OK) return "";
+  const kda_fwd_params f = B::fwd_view(p);
+  B::Stage st[B::kMaxStages];
+  const int n = B::stages_for(B::make_plan(&f), st);
+  return (stage >= 0 && stage < n) ? st[stage].name : "";
+}
+
+kda_status kda_bwd_stage(const kda_bwd_params* p, void* stream, int32_t stage) {
+  B::Args a;
+  kda_status s = B::prepare(p, a);
+  if (s != KDA_OK) return s;
+  B::Stage st[B::kMaxStages];
+  const int n = B::stages_for(a.p, st);
+  if (stage < 0 || stage >= n)
+    return B::fail(KDA_ERR_INVALID_ARG, "stage %d out of range [0,%d)", stage, n);
+  cudaError_t e = st[stage].run(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return B::fail(KDA_ERR_CUDA, "%s failed: %s", st[stage].name, cudaGetErrorString(e));
+  set_last_error("");
+  return KDA_OK;
 }
 
 kda_status kda_bwd(const kda_bwd_params* p, void* stream) {
-  kda_status s = B::check(p);
+  B::Args a;
+  kda_status s = B::prepare(p, a);
   if (s != KDA_OK) return s;
-  const kda_fwd_params f = B::fwd_view(p);
-  const B::Plan pl = B::make_plan(&f);
-  if (p->workspace == nullptr || p->workspace_bytes < pl.total_bytes)
-    return B::fail(KDA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu%s)", pl.total_bytes,
-                p->workspace_bytes, p->workspace ? "" : ", NULL");
-  if ((reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0)
-    return B::fail(KDA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  unsigned int* status = kda::device_status_word();
-  if (status == nullptr) return B::fail(KDA_ERR_CUDA, "no CUDA device / status word unavailable");
-  const B::Args a = B::make_args(p, pl, status);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const char* what = "output zeroing";
-  cudaError_t e = cudaSuccess;
-  auto chk = [&](cudaError_t x) {
-    if (e == cudaSuccess) e = x;
-    return e == cudaSuccess;
-  };
-  auto zero = [&](void* ptr, size_t bytes) {
-    return ptr == nullptr || bytes == 0 ? cudaSuccess : cudaMemsetAsync(ptr, 0, bytes, st);
-  };
-  const size_t ntok = (size_t)pl.ntok;
-  chk(zero(a.dq, ntok * pl.H * pl.K * sizeof(float)));
-  chk(zero(a.dk, ntok * pl.H * pl.K * sizeof(float)));
-  chk(zero(a.dv, ntok * pl.HV * pl.V * sizeof(float)));
-  chk(zero(a.dg, ntok * pl.HV * pl.K * sizeof(float)));
-  chk(zero(a.dbeta, ntok * pl.HV * sizeof(float)));
-  chk(zero(a.dA_log, (size_t)pl.HV * sizeof(float)));
-  chk(zero(a.ddt_bias, (size_t)pl.HV * pl.K * sizeof(float)));
-  if (e == cudaSuccess && pl.varlen) {
-    what = "chunk_table";
-    kda::FwdArgs t{};  // the forward's chunk-table kernel, writing into this workspace
-    t.plan.N = pl.N; t.plan.C = pl.C; t.plan.nct = pl.nct; t.plan.ntok = pl.ntok;
-    t.plan.varlen = true; t.plan.off_chunk_table = pl.off_table;
-    t.cu_seqlens = a.cu_seqlens; t.ws = a.ws; t.status = status;
-    chk(kda::launch_chunk_table(t, st));
+  B::Stage st[B::kMaxStages];
+  const int n = B::stages_for(a.p, st);
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = st[i].run(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+      return B::fail(KDA_ERR_CUDA, "%s failed: %s", st[i].name, cudaGetErrorString(e));
   }
-  if (e == cudaSuccess && pl.nct > 0) {
-    what = "bwd_prep";
-    B::prep_kernel<<<dim3((unsigned)pl.nct, (unsigned)pl.HV), B::kThreads, 0, st>>>(a);
-    chk(cudaGetLastError());
-  }
-  if (e == cudaSuccess && B::state_blocks(pl) > 0) {
-    what = "bwd_states";
-    const size_t sm = B::states_smem(pl);
-    if (chk(cudaFuncSetAttribute(B::states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm))) {
-      B::states_kernel<<<(unsigned)B::state_blocks(pl), B::kThreads, sm, st>>>(a);
-      chk(cudaGetLastError());
-    }
-    what = "bwd_dstate";
-    const size_t sd = B::dstate_smem(pl);
-    if (e == cudaSuccess &&
-        chk(cudaFuncSetAttribute(B::dstate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd))) {
-      B::dstate_kernel<<<(unsigned)B::state_blocks(pl), B::kThreads, sd, st>>>(a);
-      chk(cudaGetLastError());
-    }
-  }
-  if (e == cudaSuccess && pl.nct > 0) {
-    what = "bwd_grads";
-    const size_t sg = B::grads_smem(pl);
-    if (chk(cudaFuncSetAttribute(B::grads_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg))) {
-      B::grads_kernel<<<dim3((unsigned)pl.nct, (unsigned)pl.HV), B::kThreads, sg, st>>>(a);
-      chk(cudaGetLastError());
-    }
-  }
-  if (e != cudaSuccess) return B::fail(KDA_ERR_CUDA, "%s failed: %s", what, cudaGetErrorString(e));
   set_last_error("");
   return KDA_OK;
 }

@@ -136,3 +136,23 @@ def test_without_gpu_reports_cuda_error(lib):
     p.workspace = FAKE
     p.workspace_bytes = kb.kda_bwd_workspace_size(p)
     assert kb.kda_bwd(p, 0) == kb.KDA_ERR_CUDA
+
+
+def test_stage_lists(lib):
+    names = lambda p: [kb.kda_bwd_stage_name(p, i) for i in range(kb.kda_bwd_num_stages(p))]
+    assert names(params()) == ["zero_outputs", "bwd_prep", "bwd_states", "bwd_dstate", "bwd_grads"]
+    cu = (ctypes.c_int64 * 4)(0, 5, 64, 200)
+    p = params(fwd_B=1, fwd_T=200, fwd_N=3, fwd_cu_seqlens=FAKE)
+    p.fwd.cu_seqlens_host = ctypes.addressof(cu)
+    assert names(p) == ["zero_outputs", "chunk_table", "bwd_prep", "bwd_states", "bwd_dstate",
+                        "bwd_grads"]
+    assert kb.kda_bwd_num_launches(p) == kb.kda_bwd_num_stages(p) - 1
+    assert kb.kda_bwd_stage_name(params(), 5) == "" and kb.kda_bwd_stage_name(params(), -1) == ""
+    assert kb.kda_bwd_num_stages(params(dq=0)) == 0
+
+
+def test_stage_rejects_small_workspace_before_cuda(lib):
+    p = params()
+    p.workspace = FAKE
+    p.workspace_bytes = 16
+    assert kb.kda_bwd_stage(p, 0, 1) == kb.KDA_ERR_WORKSPACE

@@ -78,3 +78,44 @@ def test_equal_heads_are_bit_reproducible():
     b = bt.run_gpu_bwd(inp, d_o, dfs)
     for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
         assert np.array_equal(a[name], b[name]), name
+
+
+def test_stages_one_by_one_give_the_whole_pass():
+    """kda_bwd_stage over every stage in order equals kda_bwd (the bench times it that way)."""
+    import torch
+    import kimi_delta_attention_gate_gb300 as kda
+    from kimi_delta_attention_gate_gb300 import _binding as kb
+    from kda_testlib import f32_device, gate_kwargs, to_device
+    inp = kin.make_inputs(bt.workload(H=2, HV=2, T=150, seed=52, varlen_n=3, varlen_max_len=60,
+                                      B=1))
+    wl = inp.wl
+    d_o, dfs = bt.upstream(inp, 6)
+    whole = bt.run_gpu_bwd(inp, d_o, dfs)
+    q, k, v, g, b, do = (to_device(x, wl.dtype) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta, d_o))
+    cu_cpu = torch.from_numpy(inp.cu_seqlens)
+    f = kda.make_params(q, k, v, g, b, A_log=f32_device(inp.A_log), dt_bias=f32_device(inp.dt_bias),
+                        scale=inp.scale, initial_state=f32_device(inp.h0), cu_seqlens=cu_cpu.cuda(),
+                        cu_seqlens_cpu=cu_cpu, chunk_size=wl.chunk_size, **gate_kwargs(wl))
+    outs = {n: torch.full(s, float("nan"), dtype=torch.float32, device="cuda") for n, s in
+            (("dq", q.shape), ("dk", k.shape), ("dv", v.shape), ("dg", g.shape),
+             ("dbeta", b.shape), ("dA_log", (wl.HV,)), ("ddt_bias", (wl.HV * wl.K,)),
+             ("dh0", tuple(inp.h0.shape)))}
+    dht = f32_device(dfs)
+    p = kb.kda_bwd_params()
+    p.fwd = f
+    p.d_o, p.d_final_state = do.data_ptr(), dht.data_ptr()
+    for n, t in outs.items():
+        setattr(p, n, t.data_ptr())
+    ws = torch.empty(kb.kda_bwd_workspace_size(p), dtype=torch.uint8, device="cuda")
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    sh = torch.cuda.current_stream().cuda_stream
+    nst = kb.kda_bwd_num_stages(p)
+    assert [kb.kda_bwd_stage_name(p, i) for i in range(nst)][:2] == ["zero_outputs", "chunk_table"]
+    for i in range(nst):
+        kb.raise_for(kb.kda_bwd_stage(p, sh, i))
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status(0) == 0
+    for n in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        assert np.array_equal(outs[n].cpu().double().numpy(), whole[n]), n
+    for n in ("dA_log", "ddt_bias"):
+        assert bt.rel_l2(outs[n].cpu().double().numpy(), whole[n]) < 1e-6, n
