@@ -376,6 +376,133 @@ def measure_decode(kb, kda, dev, steps, warmup, peak_gbs):
                          "frac": achieved / peak_gbs, "bytes_per_launch": float(nbytes)}}
 
 
+# fp32 CUDA-core peak of one GB300: 152 SMs x 128 fp32 lanes x 2 flops (a fused multiply-add)
+# per cycle at the maximum SM clock of 2070 MHz.
+N_SM, FP32_LANES_PER_SM, MAX_SM_MHZ = 152, 128, 2070
+
+
+def fp32_alu_peak_tflops(sm_mhz: float = MAX_SM_MHZ) -> float:
+    return N_SM * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+def bwd_stage_flops(stage: str, C: int, K: int, V: int, nct: int, HV: int) -> float:
+    """Algorithmic flops of one launch of a backward kernel over nct chunks x HV value heads
+    (every chunk full; a fused multiply-add counts 2, an exponential 0): the dot products and
+    triangular substitutions each kernel's stage computes."""
+    per = {
+        # Aqk and P over j <= i (2 FMA + 1 mul per channel); W, U forward substitution
+        "bwd_prep": 5 * K * C * (C + 1) / 2 + 3 * (K + V) * C * (C - 1) / 2,
+        # V_new = U - W S and S <- e^gamma S + Kg^T V_new
+        "bwd_states": 4 * C * K * V,
+        # dV_new = Kg dS' + Aqk^T dO (lower triangle); dS = Qg^T dO - W^T dV_new + ...
+        "bwd_dstate": 2 * C * K * V + C * (C + 1) * V + 4 * C * K * V,
+        # dAqk; dQg, dW, dKg; X, Y back substitution; A^T dA (strictly lower); the
+        # e^(Gamma_i - Gamma_j) sums over rows and columns
+        "bwd_grads": (V * C * (C + 1) + 6 * C * K * V + (K + V) * C * (C - 1)
+                      + C * (C - 1) / 2 * (2 * V + 3 * K) + 5.5 * K * C * (C + 1)),
+    }.get(stage, 0.0)
+    return float(per) * nct * HV
+
+
+def measure_backward(kb, kda, dev, stream, inp, t, gate, steps):
+    """The backward pass (kda_bwd) on the bench's workload with seeded incoming gradients:
+    tokens/s, each kernel's time (the same passes stage by stage, an event after every
+    kernel), and the fp32 CUDA-core roofline of the dominant kernel."""
+    import torch
+    wl = inp.wl
+    rng = np.random.default_rng(wl.seed + 7)
+    d_o = rng.standard_normal((wl.B, wl.T, wl.HV, wl.V), dtype=np.float32)
+    if wl.dtype == "bf16":
+        kin.round_to_bf16(d_o)
+        d_o = torch.from_numpy(kin.to_bf16_bits(d_o).view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        d_o = torch.from_numpy(d_o).to(dev)
+    st_shape = (inp.N, wl.HV, wl.K, wl.V)
+    dht = torch.from_numpy(rng.standard_normal(st_shape, dtype=np.float32)).to(dev)
+    f = kda.make_params(t["q"], t["k"], t["v"], t["g"], t["b"], A_log=t["A_log"],
+                        dt_bias=t["dt_bias"], scale=inp.scale, initial_state=t["h0"],
+                        cu_seqlens=t["cu"], cu_seqlens_cpu=t["cu_cpu"], chunk_size=wl.chunk_size,
+                        **gate)
+    f32 = dict(dtype=torch.float32, device=dev)
+    outs = {"dq": torch.empty(t["q"].shape, **f32), "dk": torch.empty(t["k"].shape, **f32),
+            "dv": torch.empty(t["v"].shape, **f32), "dg": torch.empty(t["g"].shape, **f32),
+            "dbeta": torch.empty(t["b"].shape, **f32), "dh0": torch.empty(st_shape, **f32)}
+    in_gate = wl.gate != kin.GATE_PREGATED
+    if t["A_log"] is not None and in_gate:
+        outs["dA_log"] = torch.empty((wl.HV,), **f32)
+    if t["dt_bias"] is not None and in_gate:
+        outs["ddt_bias"] = torch.empty(tuple(t["dt_bias"].shape), **f32)
+    p = kb.kda_bwd_params()
+    p.fwd = f
+    p.d_o, p.d_final_state = d_o.data_ptr(), dht.data_ptr()
+    for name, x in outs.items():
+        setattr(p, name, x.data_ptr())
+    kb.raise_for(kb.kda_bwd_check(p))
+    ws = torch.empty(kb.kda_bwd_workspace_size(p), dtype=torch.uint8, device=dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    sh = stream.cuda_stream
+    nst = kb.kda_bwd_num_stages(p)
+    names = [kb.kda_bwd_stage_name(p, i) for i in range(nst)]
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    whole = lambda: kb.raise_for(kb.kda_bwd(p, sh))
+    first_ms = timed(whole, 1)                      # warm-up (and the size of a step)
+    n = steps if first_ms < 2000 else 1
+    ms = timed(whole, n)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(n)]
+    s0 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s0.record(stream)
+    for s_ in range(n):
+        for i in range(nst):
+            kb.raise_for(kb.kda_bwd_stage(p, sh, i))
+            evs[s_][i].record(stream)
+    torch.cuda.synchronize()
+    stage_ms = np.zeros(nst)
+    prev = s0
+    for s_ in range(n):
+        for i in range(nst):
+            stage_ms[i] += prev.elapsed_time(evs[s_][i])
+            prev = evs[s_][i]
+    stage_ms /= n
+    status = kb.kda_get_device_status(sh)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} in the backward measurement")
+    C = wl.chunk_size
+    if inp.cu_seqlens is None:
+        nct = wl.B * ((wl.T + C - 1) // C)
+    else:
+        nct = int(np.sum((np.diff(inp.cu_seqlens) + C - 1) // C))
+    flops = {nm: bwd_stage_flops(nm, wl.chunk_size, wl.K, wl.V, nct, wl.HV) for nm in names}
+    kern = [i for i, nm in enumerate(names) if flops[nm] > 0]
+    dom = max(kern, key=lambda i: stage_ms[i])
+    peak = fp32_alu_peak_tflops()
+    achieved = flops[names[dom]] / (stage_ms[dom] / 1e3) / 1e12
+    total_flops = sum(flops.values())
+    return {"workload": f"{wl.name} (the forward's workload), incoming gradients N(0, 1) seeded",
+            "entry": "kda_bwd", "arithmetic": "fp32 CUDA cores (bf16 inputs widened exactly)",
+            "value": inp.n_tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "steps": n, "gpu_launches_per_step": int(kb.kda_bwd_num_launches(p)),
+            "workspace_bytes": int(ws.numel()),
+            "stages": {nm: float(x) for nm, x in zip(names, stage_ms)},
+            "flops_per_step": total_flops,
+            "tflops": total_flops / (ms / 1e3) / 1e12,
+            "roofline": {"kernel": names[dom], "bound": "alu", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",
+                         "flops_per_launch": flops[names[dom]],
+                         "ms_per_launch": float(stage_ms[dom]), "traffic": None}}
+
+
 def config_of(inp: kin.Inputs, args):
     wl = inp.wl
     return {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "HV": wl.HV, "K": wl.K,
@@ -401,6 +528,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bwd-steps", type=int, default=3,
+                    help="timed passes of the backward measurement (0: skip it)")
     ap.add_argument("--T", type=int, default=None,
                     help="override the workload's sequence length (small profiling captures)")
     args = ap.parse_args()
@@ -633,6 +762,16 @@ def main():
 
     if rank == 0 and world == 1:
         line["decode"] = measure_decode(kb, kda, dev, args.steps, args.warmup, peak)
+    if rank == 0 and world == 1 and args.bwd_steps > 0:
+        # Last on the GPU, and on its own: a failure here leaves the forward's figures as
+        # they are.
+        try:
+            tens = dict(q=q, k=k, v=v, g=g, b=b, A_log=A_log, dt_bias=dt_bias, h0=h0, cu=cu,
+                        cu_cpu=cu_cpu)
+            line["backward"] = measure_backward(kb, kda, dev, stream, inp, tens, gate,
+                                                args.bwd_steps)
+        except Exception as exc:  # noqa: BLE001
+            line["backward"] = {"error": f"{type(exc).__name__}: {exc}"[:400]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
