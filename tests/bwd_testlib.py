@@ -66,20 +66,51 @@ def upstream(inp: kin.Inputs, seed: int, state_v_first: bool = False):
 
 
 def oracle_grads(inp: kin.Inputs, d_o, dfs, *, allow_neg_eigval=False, state_v_first=False,
-                 chunk_form=False) -> dict:
+                 chunk_form=False, heads=None) -> dict:
     """The oracle's gradients (fp64) for the inputs of ``inp`` (h0 and dfs in the layout that
-    ``state_v_first`` names): the autograd form, or with ``chunk_form`` the chunked form."""
+    ``state_v_first`` names): the autograd form, or with ``chunk_form`` the chunked form.
+    ``heads``: only these value heads (whole groups only when HV > H), the gradients of
+    the other heads left out."""
     from oracle import backward as ob
     wl = inp.wl
     lb = wl.lower_bound if wl.gate == kin.GATE_SAFE else None
     fn = ob.chunk_bwd_np if chunk_form else ob.bwd
     extra = dict(chunk_size=wl.chunk_size) if chunk_form else {}
     f64 = lambda x: None if x is None else np.asarray(x, np.float64)
-    return fn(f64(inp.q), f64(inp.k), f64(inp.v), f64(inp.g), f64(inp.beta), f64(d_o), f64(dfs),
-              A_log=f64(inp.A_log), dt_bias=f64(inp.dt_bias), gate_mode=wl.gate, lower_bound=lb,
+    q, k, v, g, b, A_log, dt, h0 = (inp.q, inp.k, inp.v, inp.g, inp.beta, inp.A_log, inp.dt_bias,
+                                    inp.h0)
+    if heads is not None:
+        heads = np.asarray(heads)
+        assert wl.G == 1, "sample heads with HV == H only"
+        q, k = q[:, :, heads], k[:, :, heads]
+        v, g, b, d_o = v[:, :, heads], g[:, :, heads], b[:, :, heads], d_o[:, :, heads]
+        A_log = None if A_log is None else A_log[heads]
+        dt = None if dt is None else dt.reshape(wl.HV, wl.K)[heads].reshape(-1)
+        h0 = None if h0 is None else h0[:, heads]
+        dfs = None if dfs is None else dfs[:, heads]
+    return fn(f64(q), f64(k), f64(v), f64(g), f64(b), f64(d_o), f64(dfs),
+              A_log=f64(A_log), dt_bias=f64(dt), gate_mode=wl.gate, lower_bound=lb,
               scale=inp.scale, qk_l2norm=True, beta_sigmoid=True, allow_neg_eigval=allow_neg_eigval,
-              initial_state=f64(inp.h0), cu_seqlens=inp.cu_seqlens,
+              initial_state=f64(h0), cu_seqlens=inp.cu_seqlens,
               transpose_state_layout=state_v_first, **extra)
+
+
+def take_heads(got: dict, heads, wl: kin.Workload) -> dict:
+    """The gradients of value heads ``heads`` (HV == H) out of a full set."""
+    heads = np.asarray(heads)
+    out = {}
+    for name, x in got.items():
+        if name in ("dq", "dk", "dv", "dg"):
+            out[name] = x[:, :, heads]
+        elif name == "dbeta":
+            out[name] = x[:, :, heads]
+        elif name == "dA_log":
+            out[name] = x[heads]
+        elif name == "ddt_bias":
+            out[name] = x.reshape(wl.HV, wl.K)[heads].reshape(-1)
+        elif name == "dh0":
+            out[name] = x[:, heads]
+    return out
 
 
 def build_emulator(out_dir: str) -> str:

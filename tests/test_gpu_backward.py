@@ -70,6 +70,17 @@ def test_safe_gate_at_its_bound():
     check(inp)
 
 
+def test_long_workload_sampled_head():
+    """The backward at the bench's full size (long_bf16: one sequence of 65,536 tokens, 32
+    heads, K = V = 128) in one launch; head 13's gradients against the chunked oracle over
+    the whole sequence (about half a minute of fp64 NumPy)."""
+    inp = kin.make_inputs(kin.WORKLOADS["long_bf16"])
+    d_o, dfs = bt.upstream(inp, 13)
+    got = bt.take_heads(bt.run_gpu_bwd(inp, d_o, dfs), [13], inp.wl)
+    ref = bt.oracle_grads(inp, d_o, dfs, chunk_form=True, heads=[13])
+    bt.assert_grads_close(got, ref)
+
+
 def test_equal_heads_are_bit_reproducible():
     """With HV == H only dA_log and ddt_bias are summed by atomics."""
     inp = kin.make_inputs(bt.workload(H=2, HV=2, T=130, seed=49))
