@@ -62,6 +62,13 @@ def test_full_head_dimensions(emu, tmp_path):
     check(emu, tmp_path, inp, chunk_form=True)
 
 
+def test_largest_head_dimensions(emu, tmp_path):
+    """K = 256 (the largest the checks allow) and V = 200 (six full V tiles and a partial one),
+    chunk 32, over three chunks."""
+    inp = kin.make_inputs(wl_(B=1, T=70, H=1, HV=1, K=256, V=200, C=32, seed=53, h0_std=0.05))
+    check(emu, tmp_path, inp, chunk_form=True)
+
+
 def test_varlen_with_empty_sequences_and_padding(emu, tmp_path):
     inp = kin.make_inputs(wl_(B=1, T=200, seed=44, varlen_n=5, varlen_max_len=60))
     inp.cu_seqlens[:] = np.array([0, 70, 70, 71, 135, 190], dtype=np.int64)  # 10 padding rows
