@@ -211,8 +211,10 @@ def assert_grads_close(got: dict, ref: dict, names=GRADS):
     return errs
 
 
-def run_gpu_bwd(inp: kin.Inputs, d_o, dfs, *, allow_neg_eigval=False, state_v_first=False) -> dict:
-    """kda_bwd (the C ABI through the package's wrapper) on the GPU: {gradient: fp64 array}."""
+def run_gpu_bwd(inp: kin.Inputs, d_o, dfs, *, allow_neg_eigval=False, state_v_first=False,
+                heads=None) -> dict:
+    """kda_bwd (the C ABI through the package's wrapper) on the GPU: {gradient: fp64 array};
+    with ``heads`` (HV == H) only those value heads' gradients are copied back."""
     import torch
     import kimi_delta_attention_gate_gb300 as kda
     from kda_testlib import f32_device, gate_kwargs, to_device
@@ -228,4 +230,19 @@ def run_gpu_bwd(inp: kin.Inputs, d_o, dfs, *, allow_neg_eigval=False, state_v_fi
     torch.cuda.synchronize()
     status = kda.kda_get_device_status(0)
     assert status == 0, f"device status {status:#x}"
-    return {n: t.cpu().double().numpy() for n, t in zip(GRADS, res) if t is not None}
+    out = {}
+    for name, t in zip(GRADS, res):
+        if t is None:
+            continue
+        if heads is not None:
+            idx = torch.as_tensor(np.asarray(heads), device=t.device)
+            if name == "ddt_bias":
+                t = t.reshape(wl.HV, wl.K).index_select(0, idx).reshape(-1)
+            elif name == "dA_log":
+                t = t.index_select(0, idx)
+            elif name == "dh0":
+                t = t.index_select(1, idx)
+            else:
+                t = t.index_select(2, idx)
+        out[name] = t.cpu().double().numpy()
+    return out
