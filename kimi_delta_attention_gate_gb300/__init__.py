@@ -14,7 +14,7 @@ entry): ``use_gate_in_kernel`` selects the in-kernel gate, and with it
 """
 from __future__ import annotations
 
-from typing import Optional, Tuple
+from typing import Optional
 
 from . import _binding
 from ._binding import (KDA_BF16, KDA_F32, KDA_GATE_PLAIN, KDA_GATE_PREGATED, KDA_GATE_SAFE,

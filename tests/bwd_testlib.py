@@ -95,24 +95,6 @@ def oracle_grads(inp: kin.Inputs, d_o, dfs, *, allow_neg_eigval=False, state_v_f
               transpose_state_layout=state_v_first, **extra)
 
 
-def take_heads(got: dict, heads, wl: kin.Workload) -> dict:
-    """The gradients of value heads ``heads`` (HV == H) out of a full set."""
-    heads = np.asarray(heads)
-    out = {}
-    for name, x in got.items():
-        if name in ("dq", "dk", "dv", "dg"):
-            out[name] = x[:, :, heads]
-        elif name == "dbeta":
-            out[name] = x[:, :, heads]
-        elif name == "dA_log":
-            out[name] = x[heads]
-        elif name == "ddt_bias":
-            out[name] = x.reshape(wl.HV, wl.K)[heads].reshape(-1)
-        elif name == "dh0":
-            out[name] = x[:, heads]
-    return out
-
-
 def build_emulator(out_dir: str) -> str:
     """Compile the host emulation of the backward stage bodies with AddressSanitizer and
     UndefinedBehaviorSanitizer; returns the executable's path."""
