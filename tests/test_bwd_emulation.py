@@ -148,3 +148,40 @@ def test_a_planted_error_in_the_oracle_is_caught(emu, tmp_path, monkeypatch):
     monkeypatch.setattr(ob, "bwd", planted_dv)
     with pytest.raises(AssertionError, match="dv"):
         check(emu, tmp_path, kin.make_inputs(wl_(seed=51)))
+
+
+def test_no_decay(emu, tmp_path):
+    """Pre-gated log decay 0 (alpha = 1): Gamma = 0, every exponential is 1."""
+    inp = kin.make_inputs(wl_(gate=kin.GATE_PREGATED, seed=54))
+    inp.g[:] = 0.0
+    check(emu, tmp_path, inp)
+
+
+def test_beta_near_zero(emu, tmp_path):
+    """beta logits of -30: beta ~ 1e-13, the state is barely written."""
+    inp = kin.make_inputs(wl_(seed=55))
+    inp.beta[:] = np.float32(-30.0)
+    check(emu, tmp_path, inp)
+
+
+def test_zero_query_and_key_rows(emu, tmp_path):
+    """All-zero q and k rows: the L2 norm sits at its epsilon (|x| = 0 < sqrt(1e-6))."""
+    inp = kin.make_inputs(wl_(seed=56))
+    inp.q[:, 5] = 0.0
+    inp.k[:, 70] = 0.0
+    check(emu, tmp_path, inp)
+
+
+def test_zero_incoming_gradients_give_zero(emu, tmp_path):
+    inp = kin.make_inputs(wl_(seed=57))
+    d_o, dfs = bt.upstream(inp, 1)
+    d_o[:] = 0.0
+    dfs[:] = 0.0
+    got = bt.run_emulator(emu, str(tmp_path / "z"), inp, d_o, dfs)
+    for name in bt.GRADS:
+        assert np.all(got[name] == 0), name
+
+
+def test_single_token_sequences(emu, tmp_path):
+    """B = 3 sequences of one token (one one-row chunk each)."""
+    check(emu, tmp_path, kin.make_inputs(wl_(B=3, T=1, seed=58)))
