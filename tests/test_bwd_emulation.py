@@ -185,3 +185,11 @@ def test_zero_incoming_gradients_give_zero(emu, tmp_path):
 def test_single_token_sequences(emu, tmp_path):
     """B = 3 sequences of one token (one one-row chunk each)."""
     check(emu, tmp_path, kin.make_inputs(wl_(B=3, T=1, seed=58)))
+
+
+@pytest.mark.parametrize("seed", range(100, 116))
+def test_random_shapes(emu, tmp_path, seed):
+    """Seeded random configurations: batch, length (ragged tails), grouped heads, K, V
+    (partial value tiles), chunk size, gate mode, dtype, varlen, optional inputs, options."""
+    inp, opts = bt.random_case(seed)
+    check(emu, tmp_path, inp, chunk_form=True, **opts)

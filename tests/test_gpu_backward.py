@@ -130,3 +130,10 @@ def test_stages_one_by_one_give_the_whole_pass():
         assert np.array_equal(outs[n].cpu().double().numpy(), whole[n]), n
     for n in ("dA_log", "ddt_bias"):
         assert bt.rel_l2(outs[n].cpu().double().numpy(), whole[n]) < 1e-6, n
+
+
+@pytest.mark.parametrize("seed", range(100, 108))
+def test_random_shapes(seed):
+    """Seeded random configurations (the first half of the host emulation's sweep)."""
+    inp, opts = bt.random_case(seed)
+    check(inp, chunk_form=True, **opts)
