@@ -75,25 +75,17 @@ def dense_flops(inp: kin.Inputs) -> float:
     return float(inp.n_tokens * wl.HV * (2 * C * (3 * K + 2 * V) + 6 * K * V))
 
 
-def stage_bytes(name: str, inp: kin.Inputs, p, lib) -> float:
-    """Algorithmic bytes of one launch of the named stage."""
+def own_bytes(name: str, inp: kin.Inputs) -> float:
+    """Method bytes one launch of the named stage owns: the inputs it is the first to read
+    and the outputs it writes, intermediates excluded (they sum to essential_bytes)."""
     wl = inp.wl
     e = elem(wl.dtype)
     ntok = inp.n_tokens
-    C, K, V, H, HV = wl.chunk_size, wl.K, wl.V, wl.H, wl.HV
-    lens = np.diff(inp.cu_seqlens) if inp.cu_seqlens is not None else np.full(wl.B, wl.T)
-    nct = int(np.sum((lens + C - 1) // C))
-    inter = nct * HV * (4 * (C * (3 * K + V + C) + K))
-    state = inp.N * HV * K * V * 4
-    if name == "simt_intra":
-        return float(ntok * (e * (2 * H * K + HV * (K + V + 1))) + 4 * HV * (1 + K) + inter)
-    if name == "simt_recur":
-        return float(inter + ntok * HV * V * e + state * ((inp.h0 is not None) + 1))
-    tc_block = 66048  # packed per-(chunk, head) block of the tensor-core path
-    if name == "tc_intra":
-        return float(ntok * e * (2 * H * K + HV * (K + 1)) + 4 * HV * (1 + K) + nct * HV * tc_block)
-    if name == "tc_recur":
-        return float(nct * HV * tc_block + 2 * ntok * HV * V * e + state * ((inp.h0 is not None) + 1))
+    state = inp.N * wl.HV * wl.K * wl.V * 4 * ((inp.h0 is not None) + 1)
+    if name in ("tc_intra", "simt_intra"):
+        return float(ntok * e * (2 * wl.H * wl.K + wl.HV * (wl.K + 1)) + 4 * wl.HV * (1 + wl.K))
+    if name in ("tc_recur", "simt_recur"):
+        return float(ntok * e * 2 * wl.HV * wl.V + state)
     if name == "chunk_table":
         return float(16 * (inp.N + 1))
     return essential_bytes(inp)
@@ -727,31 +719,41 @@ def main():
     del link_buf, link_dev
     link_floor_ms = 1e3 * max(h2d / (link["h2d"] * 1e9), d2h / (link["d2h"] * 1e9))
 
-    # Roofline of the dominant kernel.
+    # Roofline of the step by the method's byte model: q, k, v, g, beta read once, o written
+    # once, plus the states and the gate parameters (intermediates are not counted), over the
+    # device time of one step; the step is HBM-bound (arithmetic intensity below the ridge).
     peaks, peak_kind = load_peaks()
-    dom = int(np.argmax(stage_ms))
-    dom_bytes = stage_bytes(names[dom], inp, p, kb)
-    achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
     peak = float(peaks["hbm_gbs"])
-    roofline = {"kernel": names[dom], "bound": "hbm", "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
-                "bytes_per_launch": dom_bytes, "ms_per_launch": float(stage_ms[dom]),
-                "traffic": profiled_traffic(names[dom], wl.name)}
     ess = essential_bytes(inp)
     flops = dense_flops(inp)
     t_roof = max(ess / (peak * 1e9), flops / (float(peaks["bf16_tflops"]) * 1e12))
-    path = {"essential_bytes": ess, "dense_flops": flops,
-            "achieved_gbs": ess / (ms_per_step / 1e3) / 1e9,
-            "tflops": flops / (ms_per_step / 1e3) / 1e12,
-            "roofline_ms": 1e3 * t_roof,
-            "frac": (1e3 * t_roof) / ms_per_step}
+    stage_traffic = [profiled_traffic(n, wl.name) for n in names]
+    roofline = {"kernel": "kda_fwd step (all kernels)", "bound": "hbm",
+                "achieved": ess / (ms_per_step / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                "frac": ess / (ms_per_step / 1e3) / 1e9 / peak, "peak_source": peak_kind,
+                "bytes_per_step": ess, "ms_per_step": ms_per_step,
+                "traffic": (None if any(t is None for t in stage_traffic)
+                            else float(sum(stage_traffic))),
+                "dense_flops": flops, "tflops": flops / (ms_per_step / 1e3) / 1e12,
+                "roofline_ms": 1e3 * t_roof, "frac_of_roofline_time": (1e3 * t_roof) / ms_per_step}
+    # Each kernel against the method bytes it owns (the inputs it reads and outputs it
+    # writes, intermediates excluded), timed alone stage by stage; "traffic" is its DRAM bytes
+    # per launch from the committed ncu summary (null once its code changed), and
+    # "traffic_over_own_bytes" the waste ratio.
+    stages = {}
+    for i, n in enumerate(names):
+        own = own_bytes(n, inp)
+        ach = own / (stage_ms[i] / 1e3) / 1e9
+        stages[n] = {"ms": float(stage_ms[i]), "own_bytes": own, "achieved_gbs": ach,
+                     "frac": ach / peak, "traffic": stage_traffic[i],
+                     "traffic_over_own_bytes": (None if stage_traffic[i] is None or own <= 0
+                                                else stage_traffic[i] / own)}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic (seeded PCG64, shapes and distributions of the workload)",
-            "config": config_of(inp, args), "roofline": roofline, "path_roofline": path,
-            "stages": {n: float(t) for n, t in zip(names, stage_ms)},
+            "config": config_of(inp, args), "roofline": roofline, "stages": stages,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
                     "entry": "kda_fwd_host", "serial_copy_run_copy_ms": serial_ms,

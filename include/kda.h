@@ -84,10 +84,10 @@ typedef struct kda_fwd_params {
   int32_t N;                 /* number of sequences: B, or len(cu_seqlens) - 1 */
   int32_t allow_neg_eigval;  /* 1: beta = 2 sigmoid(logit) in [0, 2), so that the transition
                                 I - beta k k^T may have a negative eigenvalue; needs
-                                beta_sigmoid ("Reading Notes: Implementation Notes for KDA in
-                                FLA", section 2.1) */
+                                beta_sigmoid ("FLA-KDA engineering notes", section 2.1) */
   int32_t state_v_first;     /* 1: h0 and final_state are stored [N, HV, V, K] (the state
-                                transposed; section 2.2 of the same notes) */
+                                transposed; "FLA-KDA engineering notes", section 2.2,
+                                transpose_state_layout) */
   const void* q;
   const void* k;
   const void* v;
@@ -101,7 +101,8 @@ typedef struct kda_fwd_params {
   void* o;                   /* output */
   float* final_state;        /* output, optional (NULL = not written) */
   float* h_out;              /* output, optional: the state before every chunk
-                                ("return_intermediate_states", reading notes section 2.2),
+                                ("return_intermediate_states", "FLA-KDA engineering notes"
+                                section 2.2),
                                 [nct, HV, K, V] fp32 ([nct, HV, V, K] with state_v_first), chunk c
                                 of sequence n at index (chunks of sequences 0..n-1) + c;
                                 nct from kda_fwd_num_chunks */
@@ -122,8 +123,9 @@ kda_status kda_fwd_check(const kda_fwd_params* p);
 
 /* The forward pass, enqueued on `stream` (a cudaStream_t; NULL = legacy default
    stream).  Asynchronous: returns once the kernels are enqueued.  Writes o and,
-   if non-NULL, final_state.  Rows of o that no sequence covers (varlen padding)
-   are left untouched.  Returns KDA_ERR_CUDA if a launch fails.
+   if non-NULL, final_state.  Rows of o that no sequence covers (varlen padding:
+   tokens cu_seqlens[N] .. B*T - 1) are set to zero, as the token recurrence
+   defines them.  Returns KDA_ERR_CUDA if a launch fails.
    When few (sequence, value head) recurrences would leave most SMs idle (bf16
    tensor-core path, N * HV <= 96, at least 256 chunks), the chunk range is cut
    into up to 8 segments: the intra-chunk kernel of segment k+1 runs on `stream`
@@ -155,13 +157,13 @@ size_t kda_fwd_host_arena_size(const kda_fwd_params* p);
    (pinned) host memory lets these copies run asynchronously.  Ordered on `stream`
    like kda_fwd; the host buffers must stay valid, and o / final_state / h_out may
    be read, only once `stream` has passed this call.  Rows of o that no sequence
-   covers are left untouched.  The source pages have no counterpart to this entry
+   covers are set to zero (copied out from the arena like the others).  The
+   source pages have no counterpart to this entry
    point: it is the end-to-end path of a caller whose tensors live in host memory. */
 kda_status kda_fwd_host(const kda_fwd_params* p, void* arena, size_t arena_bytes, void* stream);
 
 /* The same forward pass as a token recurrence (decode and short prefill;
-   "Reading Notes: Implementation Notes for KDA in FLA", section 1,
-   fused_recurrent_kda): per token alpha = exp(g'), S <- Diag(alpha) S,
+   "FLA-KDA engineering notes", section 1, fused_recurrent_kda): per token alpha = exp(g'), S <- Diag(alpha) S,
    S <- S + beta k (v - S^T k)^T, o = scale S^T q, the state read from h0 (or 0)
    and written to final_state.  Same parameters, checks, layouts and outputs as
    kda_fwd, except: chunk_size and the workspace are not used (no workspace is
@@ -206,7 +208,9 @@ kda_status kda_fwd_stage(const kda_fwd_params* p, void* stream, int32_t stage);
      rejected with KDA_ERR_WORKSPACE and a message giving both sizes.
    - The first call on each device looks up the array's device address
      (cudaGetSymbolAddress) with that device current; make that first call
-     before any stream capture.
+     before any stream capture.  That lookup is its only set-up: the stages run
+     one after another on `stream` (bit-identical to kda_fwd), so this entry
+     point creates none of the library's internal streams or events.
    - All calls share the one array and it keeps the last call's contents.
      Nothing in it needs to start at zero: every call writes each scratch
      element it later reads.  Calls whose kernels overlap on the GPU (on

@@ -30,6 +30,20 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else int(t.data_ptr())
 
 
+def _int64_seqlens(cu_seqlens, cu_seqlens_cpu):
+    """int64 copies of the sequence offsets (FLA callers often hold them as int32) and a host
+    copy when only the device tensor is given; the caller keeps the returned tensors alive
+    while its launches are in flight (they are bound in the parameter block)."""
+    import torch
+    if cu_seqlens is not None:
+        cu_seqlens = cu_seqlens.to(torch.int64).contiguous()
+        if cu_seqlens_cpu is None:
+            cu_seqlens_cpu = cu_seqlens.to("cpu")
+    if cu_seqlens_cpu is not None:
+        cu_seqlens_cpu = cu_seqlens_cpu.to(torch.int64).contiguous()
+    return cu_seqlens, cu_seqlens_cpu
+
+
 def _gate_mode(use_gate_in_kernel: bool, safe_gate: Optional[bool], lower_bound) -> int:
     if not use_gate_in_kernel:
         return KDA_GATE_PREGATED
@@ -46,7 +60,14 @@ def make_params(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None,
                 safe_gate: Optional[bool] = None, use_qk_l2norm_in_kernel: bool = True,
                 use_beta_sigmoid_in_kernel: bool = True, allow_neg_eigval: bool = False,
                 transpose_state_layout: bool = False, h_out=None, workspace=None) -> kda_fwd_params:
-    """Fill a ``kda_fwd_params`` from tensors (no checks beyond shapes; the C layer checks).
+    """Fill a ``kda_fwd_params`` from tensors (no checks beyond shapes and dtypes; the C
+    layer checks the rest).
+
+    The struct holds raw addresses, so the returned object also keeps a reference to every
+    tensor it points at (attribute ``_keep``): the memory stays valid for as long as the
+    parameter block is alive, even when the caller passed temporaries.  ``cu_seqlens`` and
+    ``cu_seqlens_cpu`` must be int64 (the C ABI reads 8-byte offsets); an int32 tensor is
+    rejected rather than read as int64.
 
     ``allow_neg_eigval``: beta = 2 sigmoid(logit) in [0, 2).  ``transpose_state_layout``
     (the notes' ``state_v_first``): initial / final states are [N, HV, V, K]."""
@@ -74,6 +95,9 @@ def make_params(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None,
         raise ValueError("A_log must be [HV]")
     if dt_bias is not None and dt_bias.numel() != HV * K:
         raise ValueError("dt_bias must be [HV*K] (or [HV, K])")
+    for name, t in (("cu_seqlens", cu_seqlens), ("cu_seqlens_cpu", cu_seqlens_cpu)):
+        if t is not None and (t.dtype != torch.int64 or t.dim() != 1 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 1-D int64 tensor (got {t.dtype})")
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
     st_shape = (N, HV, V, K) if transpose_state_layout else (N, HV, K, V)
     if initial_state is not None and tuple(initial_state.shape) != st_shape:
@@ -97,6 +121,8 @@ def make_params(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None,
     p.o, p.final_state, p.h_out = _ptr(o), _ptr(final_state), _ptr(h_out)
     if workspace is not None:
         p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    p._keep = tuple(t for t in (q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens,
+                                cu_seqlens_cpu, o, final_state, h_out, workspace) if t is not None)
     return p
 
 
@@ -124,16 +150,12 @@ def kda_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower_bound=None, sca
     import torch
     if not q.is_cuda:
         raise ValueError("kda_fwd runs on CUDA tensors only")
-    if cu_seqlens is not None and cu_seqlens_cpu is None:
-        cu_seqlens_cpu = cu_seqlens.to("cpu")
-    if cu_seqlens_cpu is not None:
-        cu_seqlens_cpu = cu_seqlens_cpu.to(torch.int64).contiguous()
+    cu_seqlens, cu_seqlens_cpu = _int64_seqlens(cu_seqlens, cu_seqlens_cpu)
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
-    if o is None:
-        padded = cu_seqlens is not None and int(cu_seqlens_cpu[-1]) < B * T
-        o = (torch.zeros if padded else torch.empty)((B, T, HV, V), dtype=v.dtype, device=v.device)
+    if o is None:  # rows past the last sequence are zeroed by the library itself
+        o = torch.empty((B, T, HV, V), dtype=v.dtype, device=v.device)
     if final_state is None and output_final_state:
         st_shape = (N, HV, V, K) if transpose_state_layout else (N, HV, K, V)
         final_state = torch.empty(st_shape, dtype=torch.float32, device=v.device)
@@ -177,16 +199,12 @@ def kda_fused_recurrent_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, lower
     import torch
     if not q.is_cuda:
         raise ValueError("kda_fused_recurrent_fwd runs on CUDA tensors only")
-    if cu_seqlens is not None and cu_seqlens_cpu is None:
-        cu_seqlens_cpu = cu_seqlens.to("cpu")
-    if cu_seqlens_cpu is not None:
-        cu_seqlens_cpu = cu_seqlens_cpu.to(torch.int64).contiguous()
+    cu_seqlens, cu_seqlens_cpu = _int64_seqlens(cu_seqlens, cu_seqlens_cpu)
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
-    if o is None:
-        padded = cu_seqlens is not None and int(cu_seqlens_cpu[-1]) < B * T
-        o = (torch.zeros if padded else torch.empty)((B, T, HV, V), dtype=v.dtype, device=v.device)
+    if o is None:  # rows past the last sequence are zeroed by the library itself
+        o = torch.empty((B, T, HV, V), dtype=v.dtype, device=v.device)
     if final_state is None and output_final_state:
         st_shape = (N, HV, V, K) if transpose_state_layout else (N, HV, K, V)
         final_state = torch.empty(st_shape, dtype=torch.float32, device=v.device)
@@ -259,10 +277,7 @@ def kda_bwd(q, k, v, g, beta, do, *, dht=None, A_log=None, dt_bias=None, lower_b
     import torch
     if not q.is_cuda:
         raise ValueError("kda_bwd runs on CUDA tensors only")
-    if cu_seqlens is not None and cu_seqlens_cpu is None:
-        cu_seqlens_cpu = cu_seqlens.to("cpu")
-    if cu_seqlens_cpu is not None:
-        cu_seqlens_cpu = cu_seqlens_cpu.to(torch.int64).contiguous()
+    cu_seqlens, cu_seqlens_cpu = _int64_seqlens(cu_seqlens, cu_seqlens_cpu)
     if tuple(do.shape) != tuple(v.shape) or do.dtype != v.dtype or not do.is_contiguous():
         raise ValueError("do must be contiguous with o's shape and dtype")
     B, T, H, K = q.shape

@@ -151,6 +151,7 @@ Plan make_plan(const kda_fwd_params* p) {
   pl.C = p->chunk_size; pl.N = p->N; pl.G = p->HV / p->H;
   pl.ntok = (int64_t)p->B * p->T;
   pl.varlen = p->cu_seqlens != nullptr;
+  pl.tok_end = pl.varlen ? p->cu_seqlens_host[p->N] : pl.ntok;
   pl.nc_per_seq = (p->T + pl.C - 1) / pl.C;
   if (pl.varlen) {
     int64_t nct = 0;
@@ -588,6 +589,15 @@ kda_status kda_fwd_host(const kda_fwd_params* p, void* arena, size_t arena_bytes
   chk(h2d(dp.cu_seqlens, p->cu_seqlens_host,
           p->cu_seqlens_host ? (size_t)(pl.N + 1) * sizeof(int64_t) : 0, s));
   const size_t hbytes = (size_t)pl.nct * pl.HV * pl.K * pl.V * sizeof(float);
+  if (pl.tok_end < pl.ntok) {  // rows no sequence covers: zero, like the oracle
+    const size_t row = (size_t)pl.HV * pl.V * e;
+    what = "zeroing uncovered rows";
+    chk(cudaMemsetAsync(static_cast<char*>(dp.o) + pl.tok_end * row, 0,
+                        (size_t)(pl.ntok - pl.tok_end) * row, s)) &&
+        chk(d2h(static_cast<char*>(p->o) + pl.tok_end * row,
+                static_cast<const char*>(dp.o) + pl.tok_end * row,
+                (size_t)(pl.ntok - pl.tok_end) * row, s));
+  }
   if (r == cudaSuccess && pl.nseg > 1) {
     PipeCtx* cx = pipe_ctx();
     if (cx == nullptr) return fail(KDA_ERR_CUDA, "pipeline setup failed");
@@ -658,7 +668,8 @@ kda_status kda_fused_recurrent_fwd(const kda_fwd_params* p, void* stream) {
   a.A_log = p->A_log; a.dt_bias = p->dt_bias; a.h0 = p->h0; a.cu_seqlens = p->cu_seqlens;
   a.o = p->o; a.final_state = p->final_state;
   a.status = status;
-  cudaError_t e = launch_recurrent(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = zero_uncovered_rows(a, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = launch_recurrent(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "recurrent launch failed: %s", cudaGetErrorString(e));
   t_last_error.clear();
   return KDA_OK;

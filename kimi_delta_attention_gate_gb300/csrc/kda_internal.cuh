@@ -17,6 +17,8 @@ constexpr int kMaxV = 256;
 struct Plan {
   int B, T, H, HV, K, V, C, N, G;
   int64_t ntok;             // B * T (flattened token axis)
+  int64_t tok_end;          // one past the last token any sequence covers (cu_seqlens[N] with
+                            // varlen, else ntok); rows [tok_end, ntok) of o are set to zero
   int64_t nct;              // total chunks over all sequences
   int nc_per_seq;           // chunks per sequence when there is no cu_seqlens
   bool varlen;
@@ -142,6 +144,8 @@ __device__ __forceinline__ bool seq_range(const FwdArgs& a, int n, int64_t& bos,
 // Sets the message kda_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
 
+// Sets rows [tok_end, ntok) of o to zero (cudaMemsetAsync; no-op without such rows).
+cudaError_t zero_uncovered_rows(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_table(const FwdArgs& a, cudaStream_t s);
 size_t simt_inter_block_bytes(int C, int K, int V);
 cudaError_t launch_simt_intra(const FwdArgs& a, cudaStream_t s);

@@ -66,10 +66,18 @@ extern "C" kda_status kda_fwd_noalloc(const kda_fwd_params* p, void* stream) {
   }
   void* ptr = scratch_address();
   if (ptr == nullptr) return KDA_ERR_CUDA;
-  // Same pass as kda_fwd; only the workspace is replaced.  Every scratch element a
-  // kernel reads is written earlier in the same call, so nothing needs clearing.
+  // Same pass as kda_fwd, with the workspace replaced, run stage after stage on the
+  // caller's stream (bit-identical to kda_fwd's schedule).  Running the stages in series
+  // keeps this entry point free of the library's internal streams and events, so that its
+  // only first-use set-up is the address lookup above.  Every scratch element a kernel reads
+  // is written earlier in the same call, so nothing needs clearing.
   kda_fwd_params q = *p;
   q.workspace = ptr;
   q.workspace_bytes = KDA_NOALLOC_SCRATCH_BYTES;
-  return kda_fwd(&q, stream);
+  const int32_t nst = kda_fwd_num_stages(&q);
+  for (int32_t i = 0; i < nst; ++i) {
+    s = kda_fwd_stage(&q, stream, i);
+    if (s != KDA_OK) return s;
+  }
+  return KDA_OK;
 }

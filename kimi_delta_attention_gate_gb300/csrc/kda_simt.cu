@@ -340,7 +340,19 @@ size_t simt_inter_block_bytes(int C, int K, int V) {
   return (f * sizeof(float) + 255) / 256 * 256;
 }
 
+cudaError_t zero_uncovered_rows(const FwdArgs& a, cudaStream_t s) {
+  const Plan& p = a.plan;
+  if (p.tok_end >= p.ntok) return cudaSuccess;
+  const size_t row = (size_t)p.HV * p.V * (a.dtype == KDA_BF16 ? 2 : 4);
+  return cudaMemsetAsync(static_cast<char*>(a.o) + (size_t)p.tok_end * row, 0,
+                         (size_t)(p.ntok - p.tok_end) * row, s);
+}
+
+// The varlen chunk table, and the rows of o past the last sequence set to zero (the
+// first stage of every varlen schedule).
 cudaError_t launch_chunk_table(const FwdArgs& a, cudaStream_t s) {
+  cudaError_t e = zero_uncovered_rows(a, s);
+  if (e != cudaSuccess) return e;
   chunk_table_kernel<<<1, 1024, 0, s>>>(a);
   return cudaGetLastError();
 }

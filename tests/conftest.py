@@ -13,8 +13,9 @@ def pytest_configure(config):
 
 
 # GPU test files that run after all the others (in this order): the backward pass is
-# checked once the forward's tests have all run.
-LAST = ("test_gpu_backward.py",)
+# checked once the forward's tests have all run, and the allocation-free entry point last
+# of all, so that a run stopping at its first failure has run every other test by then.
+LAST = ("test_gpu_backward.py", "test_zz_no_alloc.py")
 
 
 def pytest_collection_modifyitems(config, items):

@@ -103,12 +103,13 @@ def run_gpu_stages(inp: kin.Inputs):
     q, k, v, g, b = (to_device(x, wl.dtype) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
     cu = None if inp.cu_seqlens is None else torch.from_numpy(inp.cu_seqlens).cuda()
     cu_cpu = None if inp.cu_seqlens is None else torch.from_numpy(inp.cu_seqlens)
-    o = torch.zeros((wl.B, wl.T, wl.HV, wl.V), dtype=v.dtype, device="cuda")
+    # o starts as NaN: every row, padding included, must be written by the stages
+    o = torch.full((wl.B, wl.T, wl.HV, wl.V), float("nan"), dtype=v.dtype, device="cuda")
     fs = torch.empty((inp.N, wl.HV, wl.K, wl.V), dtype=torch.float32, device="cuda")
-    p = kda.make_params(q, k, v, g, b, A_log=f32_device(inp.A_log), dt_bias=f32_device(inp.dt_bias),
-                        scale=inp.scale, initial_state=f32_device(inp.h0), final_state=fs, o=o,
-                        cu_seqlens=cu, cu_seqlens_cpu=cu_cpu, chunk_size=wl.chunk_size,
-                        **gate_kwargs(wl))
+    A_log, dt_bias, h0 = f32_device(inp.A_log), f32_device(inp.dt_bias), f32_device(inp.h0)
+    p = kda.make_params(q, k, v, g, b, A_log=A_log, dt_bias=dt_bias, scale=inp.scale,
+                        initial_state=h0, final_state=fs, o=o, cu_seqlens=cu,
+                        cu_seqlens_cpu=cu_cpu, chunk_size=wl.chunk_size, **gate_kwargs(wl))
     ws = torch.empty(max(kb.kda_fwd_workspace_size(p), 1), dtype=torch.uint8, device="cuda")
     p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
     sh = torch.cuda.current_stream().cuda_stream
@@ -131,8 +132,9 @@ def to_pinned(x: np.ndarray, dtype: str):
 
 def run_gpu_host(inp: kin.Inputs, sentinel=7.0, h_out_chunks=0, **opts):
     """The host-buffer entry point on ``inp``: every tensor in pinned host memory, the device
-    arena pre-filled with NaN bits.  Host o starts at ``sentinel`` so rows no sequence covers
-    can be checked untouched.  Returns (o, final_state[, h_out]) as float64 numpy arrays."""
+    arena pre-filled with NaN bits.  Host o starts at ``sentinel`` so that rows no sequence
+    covers can be checked set to zero.  Returns (o, final_state[, h_out]) as float64 numpy
+    arrays."""
     import torch
     import kimi_delta_attention_gate_gb300 as kda
     wl = inp.wl

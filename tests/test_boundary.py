@@ -234,3 +234,48 @@ def test_host_entry_arena_size_and_rejections(lib):
     cu = (ctypes.c_int64 * 3)(0, 150, 200)
     v = valid_params(B=1, T=200, N=2, cu_seqlens_host=ctypes.addressof(cu))
     assert kb.kda_fwd_host_arena_size(v) > 0
+
+
+def test_make_params_rejects_int32_seqlens():
+    """The C ABI reads 8-byte offsets: an int32 cu_seqlens (FLA's usual type) must not be read
+    as int64.  make_params refuses it; the kda_fwd wrapper converts before calling it."""
+    import torch
+    import kimi_delta_attention_gate_gb300 as kda
+    q = torch.zeros((1, 16, 1, 8))
+    v = torch.zeros((1, 16, 1, 8))
+    b = torch.zeros((1, 16, 1))
+    for bad in (dict(cu_seqlens=torch.tensor([0, 5, 16], dtype=torch.int32),
+                     cu_seqlens_cpu=torch.tensor([0, 5, 16], dtype=torch.int64)),
+                dict(cu_seqlens=torch.tensor([0, 5, 16], dtype=torch.int64),
+                     cu_seqlens_cpu=torch.tensor([0, 5, 16], dtype=torch.int32))):
+        with pytest.raises(ValueError, match="int64"):
+            kda.make_params(q, q, v, v, b, lower_bound=-5.0, o=v, **bad)
+    from kimi_delta_attention_gate_gb300 import _int64_seqlens
+    cu, cu_cpu = _int64_seqlens(torch.tensor([0, 5, 16], dtype=torch.int32), None)
+    assert cu.dtype == torch.int64 and cu_cpu.dtype == torch.int64
+    assert cu_cpu.tolist() == [0, 5, 16]
+
+
+def test_make_params_keeps_its_tensors_alive():
+    """The parameter block holds raw addresses; it also holds the tensors behind them, so that
+    temporaries passed by the caller cannot be freed (and their memory reused) before launch."""
+    import gc
+    import weakref
+    import torch
+    import kimi_delta_attention_gate_gb300 as kda
+    q = torch.zeros((1, 16, 1, 8))
+    v = torch.zeros((1, 16, 1, 8))
+    b = torch.zeros((1, 16, 1))
+    h0 = torch.ones((1, 1, 8, 8))
+    ref = weakref.ref(h0)
+    p = kda.make_params(q, q, v, v, b, lower_bound=-5.0, o=v, initial_state=h0,
+                        cu_seqlens=torch.tensor([0, 16], dtype=torch.int64),
+                        cu_seqlens_cpu=torch.tensor([0, 16], dtype=torch.int64))
+    addr = p.h0
+    del h0
+    gc.collect()
+    assert ref() is not None and ref().data_ptr() == addr
+    assert any(t.data_ptr() == p.cu_seqlens for t in p._keep)
+    del p
+    gc.collect()
+    assert ref() is None

@@ -104,9 +104,12 @@ def test_stages_one_by_one_give_the_whole_pass():
     whole = bt.run_gpu_bwd(inp, d_o, dfs)
     q, k, v, g, b, do = (to_device(x, wl.dtype) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta, d_o))
     cu_cpu = torch.from_numpy(inp.cu_seqlens)
-    f = kda.make_params(q, k, v, g, b, A_log=f32_device(inp.A_log), dt_bias=f32_device(inp.dt_bias),
-                        scale=inp.scale, initial_state=f32_device(inp.h0), cu_seqlens=cu_cpu.cuda(),
-                        cu_seqlens_cpu=cu_cpu, chunk_size=wl.chunk_size, **gate_kwargs(wl))
+    # every device tensor the parameter blocks point at stays bound until the launches ran
+    cu_dev = cu_cpu.cuda()
+    A_log, dt_bias, h0 = f32_device(inp.A_log), f32_device(inp.dt_bias), f32_device(inp.h0)
+    f = kda.make_params(q, k, v, g, b, A_log=A_log, dt_bias=dt_bias, scale=inp.scale,
+                        initial_state=h0, cu_seqlens=cu_dev, cu_seqlens_cpu=cu_cpu,
+                        chunk_size=wl.chunk_size, **gate_kwargs(wl))
     outs = {n: torch.full(s, float("nan"), dtype=torch.float32, device="cuda") for n, s in
             (("dq", q.shape), ("dk", k.shape), ("dv", v.shape), ("dg", g.shape),
              ("dbeta", b.shape), ("dA_log", (wl.HV,)), ("ddt_bias", (wl.HV * wl.K,)),

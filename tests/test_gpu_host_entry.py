@@ -1,6 +1,6 @@
 """GPU tests of the host-buffer entry point kda_fwd_host: on pinned host tensors it must give
 bit for bit what kda_fwd gives on device tensors (same kernels, same schedule), whatever the
-device arena held before, and leave host rows of o outside every sequence untouched."""
+device arena held before, and set host rows of o outside every sequence to zero."""
 import numpy as np
 import pytest
 
@@ -30,9 +30,9 @@ def same_as_device(inp, **opts):
     o, fs = run_gpu_host(inp, **opts)[:2]
     ro, rfs = run_gpu(inp, **opts)
     covered = inp.wl.T if inp.cu_seqlens is None else int(inp.cu_seqlens[-1])
-    assert np.array_equal(o[:, :covered], ro[:, :covered]), "o differs from kda_fwd"
+    assert np.array_equal(o, ro), "o differs from kda_fwd"
     assert np.array_equal(fs, rfs), "final_state differs from kda_fwd"
-    assert np.all(o[:, covered:] == 7.0), "rows outside every sequence were written"
+    assert np.all(o[:, covered:] == 0.0), "rows outside every sequence are not zero"
     return o, fs
 
 
@@ -51,7 +51,7 @@ def test_host_entry_pipelined_batch_five_segments():
 
 
 def test_host_entry_pipelined_varlen_with_tail_rows():
-    """Varlen with empty sequences; 63 rows past the last sequence stay untouched."""
+    """Varlen with empty sequences; 63 rows past the last sequence come back as zeros."""
     inp = kin.make_inputs(wl_(B=1, T=17100, H=2, HV=2, dtype="bf16", varlen_n=5,
                               varlen_max_len=9100, seed=602))
     inp.cu_seqlens[:] = np.array([0, 8000, 8000, 17000, 17037, 17037], dtype=np.int64)

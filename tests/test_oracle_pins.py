@@ -316,6 +316,83 @@ def test_l2norm_eps_below_tolerance():
     assert rel(o1, o0) < 1e-6 and rel(f1, f0) < 1e-6
 
 
+# --------------------------------------------------------------------------------------
+# In-kernel L2 norm of q and k (use_qk_l2norm_in_kernel, "FLA-KDA engineering notes" 2.2)
+# --------------------------------------------------------------------------------------
+
+def _row_scaled(d, seed, lo=0.01, hi=100.0):
+    """q and k with every (batch, token, head) row multiplied by its own positive constant."""
+    r = np.random.default_rng(seed)
+    out = dict(d)
+    for name in ("q", "k"):
+        c = np.exp(r.uniform(np.log(lo), np.log(hi), d[name].shape[:3]))[..., None]
+        out[name] = d[name] * c
+    return out
+
+
+@pytest.mark.parametrize("gate", [GATE_SAFE, GATE_PLAIN])
+def test_l2norm_output_is_invariant_to_row_scaling(gate):
+    """x / ||x|| over K does not see a positive factor on a row: o and final_state are the
+    same when every q and k row (each token and head its own factor, 1e-2 .. 1e2) is
+    scaled.  Exact with epsilon 0; with the default epsilon to within its own size."""
+    d, kw = make_case(141, B=2, T=30, H=2, HV=4, K=8, V=5, gate=gate)
+    ds = _row_scaled(d, 142)
+    o0, f0 = oracle.fwd(**d, **kw, l2_eps=0.0)
+    o1, f1 = oracle.fwd(**ds, **kw, l2_eps=0.0)
+    assert rel(o1, o0) < 1e-12 and rel(f1, f0) < 1e-12
+    ds = _row_scaled(d, 143, lo=1.0, hi=10.0)
+    o2, f2 = oracle.fwd(**ds, **kw)
+    assert rel(o2, o0) < 1e-6 and rel(f2, f0) < 1e-6
+
+
+def test_l2norm_three_four_five():
+    """With K = 2 the key (3, 4) normalises to (0.6, 0.8) and the query (0, -2) to (0, -1):
+    the normalising call equals the call given those unit vectors with the norm switched off."""
+    r = np.random.default_rng(144)
+    T = 3
+    q = np.array([[0.0, -2.0], [5.0, 12.0], [-8.0, 6.0]]).reshape(1, T, 1, 2)
+    k = np.array([[3.0, 4.0], [-0.3, 0.4], [1.0, 0.0]]).reshape(1, T, 1, 2)
+    qu = np.array([[0.0, -1.0], [5 / 13, 12 / 13], [-0.8, 0.6]]).reshape(1, T, 1, 2)
+    ku = np.array([[0.6, 0.8], [-0.6, 0.8], [1.0, 0.0]]).reshape(1, T, 1, 2)
+    v = r.standard_normal((1, T, 1, 3))
+    g = r.standard_normal((1, T, 1, 2))
+    beta = r.standard_normal((1, T, 1))
+    kw = dict(gate_mode=GATE_SAFE, A_log=np.zeros(1), lower_bound=-3.0,
+              initial_state=r.standard_normal((1, 1, 2, 3)), scale=0.7)
+    o_n, f_n = oracle.fwd(q, k, v, g, beta, qk_l2norm=True, l2_eps=0.0, **kw)
+    o_u, f_u = oracle.fwd(qu, ku, v, g, beta, qk_l2norm=False, **kw)
+    assert np.max(np.abs(o_n - o_u)) < 1e-12 and np.max(np.abs(f_n - f_u)) < 1e-12
+    # the default epsilon (1e-6 inside the square root) moves a row of squared norm s by a
+    # relative 1e-6 / (2 s) at most: 2e-6 for the shortest row here (s = 0.25)
+    o_e, f_e = oracle.fwd(q, k, v, g, beta, qk_l2norm=True, **kw)
+    assert rel(o_e, o_u) < 5e-6 and rel(f_e, f_u) < 5e-6
+
+
+@pytest.mark.parametrize("mistake", ["no_sqrt", "norm_over_tokens", "norm_over_heads"])
+def test_l2norm_pins_catch_a_planted_mistake(mistake):
+    """The two pins above reject plausible wrong norms.  The mistake is planted on the CPU:
+    q and k are normalised by the wrong formula here and passed with the norm switched off,
+    which is what an oracle with that mistake would compute."""
+    def wrong(x):
+        if mistake == "no_sqrt":
+            return x / np.sum(x * x, axis=-1, keepdims=True)
+        axis = 1 if mistake == "norm_over_tokens" else 2
+        return x / np.sqrt(np.sum(x * x, axis=axis, keepdims=True))
+    d, kw = make_case(145, B=1, T=12, H=2, HV=2, K=4, V=3)
+    ds = _row_scaled(d, 146)
+    def mutant(dd):
+        ee = dict(dd, q=wrong(dd["q"]), k=wrong(dd["k"]))
+        return oracle.fwd(**ee, **kw, qk_l2norm=False)
+    o0, _ = mutant(d)
+    o1, _ = mutant(ds)
+    assert rel(o1, o0) > 1e-3      # the invariance pin fails for the mutant
+    q = np.array([0.0, -2.0, 3.0, 4.0]).reshape(1, 1, 2, 2)
+    unit = np.array([0.0, -1.0, 0.6, 0.8]).reshape(1, 1, 2, 2)
+    if mistake != "norm_over_heads":   # a per-row check does not see the head axis
+        with np.errstate(invalid="ignore", divide="ignore"):
+            assert not np.allclose(wrong(q), unit, atol=1e-3)
+
+
 def test_empty_sequence_keeps_state():
     d, kw = make_case(111, B=1, T=0, H=1, HV=1, K=4, V=3)
     o, fs = oracle.fwd(**d, **kw)
