@@ -1,5 +1,5 @@
-"""ctypes view of the C ABI in ``include/kda.h`` and ``include/kda_bwd.h`` (argument
-marshalling only).
+"""ctypes view of the C ABI in ``include/kda.h``, ``include/kda_bwd.h`` and
+``include/kda_cp.h`` (argument marshalling only).
 
 Loading fails loudly when the CUDA library has not been built: there is no
 fallback of any kind.
@@ -40,7 +40,8 @@ EXPORTED = ("kda_fwd_workspace_size", "kda_fwd_check", "kda_fwd", "kda_fwd_num_l
             "kda_fwd_stage_name", "kda_fwd_stage", "kda_get_device_status", "kda_status_string",
             "kda_last_error", "kda_abi_version", "kda_fwd_noalloc",
             "kda_bwd_check", "kda_bwd_workspace_size", "kda_bwd_num_launches", "kda_bwd",
-            "kda_bwd_num_stages", "kda_bwd_stage_name", "kda_bwd_stage")
+            "kda_bwd_num_stages", "kda_bwd_stage_name", "kda_bwd_stage",
+            "kda_state_affine_apply")
 
 # Size of the static device scratch behind kda_fwd_noalloc (KDA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -146,6 +147,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kda_bwd_stage_name.argtypes = [PB, ctypes.c_int32]
             lib.kda_bwd_stage.restype = ctypes.c_int
             lib.kda_bwd_stage.argtypes = [PB, ctypes.c_void_p, ctypes.c_int32]
+            lib.kda_state_affine_apply.restype = ctypes.c_int
+            lib.kda_state_affine_apply.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -241,6 +246,14 @@ def kda_bwd_stage_name(p: kda_bwd_params, stage: int) -> str:
 
 def kda_bwd_stage(p: kda_bwd_params, stream: int, stage: int) -> int:
     return int(load().kda_bwd_stage(ctypes.byref(p), ctypes.c_void_p(stream), int(stage)))
+
+
+def kda_state_affine_apply(P: int, R: int, S_in, S_out: int, nmaps: int, K: int, V: int,
+                           state_v_first: int, stream: int = 0) -> int:
+    return int(load().kda_state_affine_apply(ctypes.c_void_p(P), ctypes.c_void_p(R),
+                                             ctypes.c_void_p(S_in), ctypes.c_void_p(S_out),
+                                             int(nmaps), int(K), int(V), int(state_v_first),
+                                             ctypes.c_void_p(stream)))
 
 
 def raise_for(status: int) -> None:

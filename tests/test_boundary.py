@@ -45,7 +45,7 @@ def test_status_strings(lib):
 
 
 def test_every_header_is_covered():
-    assert [os.path.basename(h) for h in HEADERS] == ["kda.h", "kda_bwd.h"]
+    assert [os.path.basename(h) for h in HEADERS] == ["kda.h", "kda_bwd.h", "kda_cp.h"]
 
 
 def test_struct_layout_matches_header():
