@@ -30,7 +30,7 @@ def test_affine_apply_matches_numpy(K, V, v_first, with_s):
     from kimi_delta_attention_gate_gb300 import cp
     r = np.random.default_rng(K + V)
     n = 7
-    P = r.standard_normal((n, K, K)).astype(np.float32) / np.sqrt(K)
+    P = (r.standard_normal((n, K, K)) / np.sqrt(K)).astype(np.float32)
     st = (n, V, K) if v_first else (n, K, V)
     R = r.standard_normal(st).astype(np.float32)
     S = r.standard_normal(st).astype(np.float32) if with_s else None
