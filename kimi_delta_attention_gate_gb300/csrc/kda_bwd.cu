@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kThreads) dstate_kernel(const Args a) {
   dstate_body(ex, a, (int64_t)blockIdx.x, smem);
 }
 
-__global__ void __launch_bounds__(kThreads) grads_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, 2) grads_kernel(const Args a) {
   extern __shared__ float smem[];
   GpuExec ex;
   grads_body(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);

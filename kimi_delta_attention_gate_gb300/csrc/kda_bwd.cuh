@@ -172,10 +172,19 @@ inline int64_t state_blocks(const Plan& p) {
   return (int64_t)p.N * p.HV * ((p.V + kBV - 1) / kBV);
 }
 // Dynamic shared memory (bytes) of the stages.
-inline size_t states_smem(const Plan& p) { return sizeof(float) * (size_t)(p.K + p.C) * kBV; }
-inline size_t dstate_smem(const Plan& p) { return sizeof(float) * (size_t)(p.K + 2 * p.C) * kBV; }
+inline size_t states_smem(const Plan& p) {
+  const size_t K4 = (size_t)((p.K + 3) & ~3), C = (size_t)p.C;
+  return sizeof(float) * (K4 * kBV + 2 * C * kBV + C * (K4 + 4) + C * K4 + K4);
+}
+KDA_HD bool dstate_stages_qw(int C, int K);
+inline size_t dstate_smem(const Plan& p) {
+  const size_t K4 = (size_t)((p.K + 3) & ~3), C = (size_t)p.C;
+  const size_t base = K4 * kBV + 2 * C * kBV + C * (C + 4) + C * (K4 + 4) + K4;
+  return sizeof(float) * (base + (dstate_stages_qw(p.C, p.K) ? 2 * C * K4 : 0));
+}
 inline size_t grads_smem(const Plan& p) {
-  return sizeof(float) * (4 * (size_t)p.C * p.C + 2 * (size_t)p.C + kThreads);
+  return sizeof(float) * (2 * (size_t)p.C * p.C + (size_t)p.C * (p.C + 1) + 2 * (size_t)p.C +
+                          kThreads + 4);
 }
 
 // ---- element helpers ------------------------------------------------------------------
@@ -401,11 +410,40 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv) {
 }
 
 // ---- states: per (sequence, value head, V tile), chunks in order ------------------------
+//
+// Per chunk, W, Kg and the U tile are staged in shared memory once; V_new = U - W S is then
+// computed in 2 x 4 register blocks (two rows, i and i + C/2, of four adjacent columns) and
+// S <- Diag(e^gamma_C) S + Kg^T V_new in 4 x 4 blocks (four channels of four columns), every
+// operand read as 16 bytes from shared memory.  K is padded to K4 (a multiple of 4) with zero
+// rows, and W's rows are K4 + 4 floats apart so that the rows a warp reads fall in different
+// banks.
+
+struct F4 { float x, y, z, w; };
+// four consecutive floats from a 16-byte aligned address (a 16-byte shared load on the GPU)
+KDA_HD F4 ld4(const float* p) {
+#if defined(__CUDA_ARCH__)
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  return {v.x, v.y, v.z, v.w};
+#else
+  return {p[0], p[1], p[2], p[3]};
+#endif
+}
+KDA_HD void st4(float* p, const float (&v)[4]) {
+#if defined(__CUDA_ARCH__)
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+#else
+  p[0] = v[0]; p[1] = v[1]; p[2] = v[2]; p[3] = v[3];
+#endif
+}
+KDA_HD float f4at(const F4& v, int i) { return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w)); }
+
+KDA_HD int pad4(int x) { return (x + 3) & ~3; }
 
 template <class Exec>
 KDA_BODY void states_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
   const Plan& p = a.p;
   const int C = p.C, K = p.K, V = p.V, HV = p.HV;
+  const int K4 = pad4(K), ldw = K4 + 4, half = C / 2;
   const int nvt = (V + kBV - 1) / kBV;
   const int vt = (int)(bid % nvt);
   const int hv = (int)((bid / nvt) % HV);
@@ -416,16 +454,20 @@ KDA_BODY void states_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
     return;
   }
   const Block& b = p.blk;
-  float* sS = smem;                     // [K][kBV] the state tile
-  float* sVn = smem + (size_t)K * kBV;  // [C][kBV] V_new tile
+  float* sS = smem;                          // [K4][kBV] the state tile
+  float* sVn = sS + (size_t)K4 * kBV;        // [C][kBV] V_new tile
+  float* sW = sVn + (size_t)C * kBV;         // [C][ldw] W
+  float* sKg = sW + (size_t)C * ldw;         // [C][K4] Kg
+  float* sU = sKg + (size_t)C * K4;          // [C][kBV] U tile
+  float* sD = sU + (size_t)C * kBV;          // [K4] e^gamma_C
   const int c0 = vt * kBV;
   const int nc = V - c0 < kBV ? V - c0 : kBV;  // columns of this tile
   const size_t sbase = ((size_t)n * HV + hv) * (size_t)K * V;
   ex.phase([&](int tid, int nthr) {
-    for (int e = tid; e < K * kBV; e += nthr) {
+    for (int e = tid; e < K4 * kBV; e += nthr) {
       const int kk = e / kBV, cl = e - (e / kBV) * kBV;
       float s = 0.f;
-      if (cl < nc && a.h0 != nullptr)
+      if (kk < K && cl < nc && a.h0 != nullptr)
         s = a.h0[sbase + (a.state_v_first ? (size_t)(c0 + cl) * K + kk : (size_t)kk * V + c0 + cl)];
       sS[e] = s;
     }
@@ -442,42 +484,94 @@ KDA_BODY void states_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
     const float* Dc = blk + b.decay;
     float* Vn = block_ptr(a, c, hv) + b.vn;
     float* hS = state_ptr(a, p.off_h, c, hv);
-    // the state before this chunk; V_new = U - W S
+    // stage W, Kg, U, e^gamma_C; the state before this chunk goes out
     ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < C * K4; e += nthr) {
+        const int i = e / K4, kk = e - (e / K4) * K4;
+        const bool in = i < L && kk < K;
+        sW[(size_t)i * ldw + kk] = in ? W[(size_t)i * K + kk] : 0.f;
+        sKg[e] = in ? Kg[(size_t)i * K + kk] : 0.f;
+      }
+      for (int e = tid; e < C * kBV; e += nthr) {
+        const int i = e / kBV, cl = e - (e / kBV) * kBV;
+        sU[e] = (i < L && cl < nc) ? U[(size_t)i * V + c0 + cl] : 0.f;
+      }
+      for (int kk = tid; kk < K4; kk += nthr) sD[kk] = kk < K ? Dc[kk] : 0.f;
       for (int e = tid; e < K * kBV; e += nthr) {
         const int kk = e / kBV, cl = e - (e / kBV) * kBV;
         if (cl < nc) hS[(size_t)kk * V + c0 + cl] = sS[e];
       }
-      for (int e = tid; e < C * kBV; e += nthr) {
-        const int i = e / kBV, cl = e - (e / kBV) * kBV;
-        float vn = 0.f;
-        if (i < L && cl < nc) {
-          vn = U[(size_t)i * V + c0 + cl];
-          const float* wr = W + (size_t)i * K;
-          for (int kk = 0; kk < K; ++kk) vn = fmaf(-wr[kk], sS[kk * kBV + cl], vn);
+    });
+    // V_new = U - W S: rows i and i + C/2, columns 4 g .. 4 g + 3
+    ex.phase([&](int tid, int nthr) {
+      for (int u = tid; u < half * (kBV / 4); u += nthr) {
+        const int i0 = u / (kBV / 4), g = u - (u / (kBV / 4)) * (kBV / 4), i1 = i0 + half;
+        float acc[2][4];
+        {
+          const F4 u0 = ld4(sU + (size_t)i0 * kBV + 4 * g), u1 = ld4(sU + (size_t)i1 * kBV + 4 * g);
+          for (int x = 0; x < 4; ++x) { acc[0][x] = f4at(u0, x); acc[1][x] = f4at(u1, x); }
         }
-        sVn[e] = vn;
-        if (cl < nc) Vn[(size_t)i * V + c0 + cl] = vn;
+        for (int kk = 0; kk < K4; kk += 4) {
+          const F4 w0 = ld4(sW + (size_t)i0 * ldw + kk), w1 = ld4(sW + (size_t)i1 * ldw + kk);
+          for (int y = 0; y < 4; ++y) {
+            const F4 s = ld4(sS + (size_t)(kk + y) * kBV + 4 * g);
+            const float a0 = f4at(w0, y), a1 = f4at(w1, y);
+            for (int x = 0; x < 4; ++x) {
+              acc[0][x] = fmaf(-a0, f4at(s, x), acc[0][x]);
+              acc[1][x] = fmaf(-a1, f4at(s, x), acc[1][x]);
+            }
+          }
+        }
+        st4(sVn + (size_t)i0 * kBV + 4 * g, acc[0]);
+        st4(sVn + (size_t)i1 * kBV + 4 * g, acc[1]);
+        for (int r = 0; r < 2; ++r) {
+          const int i = r == 0 ? i0 : i1;
+          for (int x = 0; x < 4; ++x)
+            if (4 * g + x < nc) Vn[(size_t)i * V + c0 + 4 * g + x] = acc[r][x];
+        }
       }
     });
-    // S <- Diag(e^gamma_C) S + Kg^T V_new
+    // S <- Diag(e^gamma_C) S + Kg^T V_new: channels 4 q .. 4 q + 3, columns 4 g .. 4 g + 3
     ex.phase([&](int tid, int nthr) {
-      for (int e = tid; e < K * kBV; e += nthr) {
-        const int kk = e / kBV, cl = e - (e / kBV) * kBV;
-        float s = sS[e] * Dc[kk];
-        for (int i = 0; i < L; ++i) s = fmaf(Kg[(size_t)i * K + kk], sVn[i * kBV + cl], s);
-        sS[e] = s;
+      for (int u = tid; u < (K4 / 4) * (kBV / 4); u += nthr) {
+        const int q4 = u / (kBV / 4), g = u - (u / (kBV / 4)) * (kBV / 4);
+        float acc[4][4];
+        for (int y = 0; y < 4; ++y) {
+          const F4 s = ld4(sS + (size_t)(4 * q4 + y) * kBV + 4 * g);
+          const float d = sD[4 * q4 + y];
+          for (int x = 0; x < 4; ++x) acc[y][x] = f4at(s, x) * d;
+        }
+        for (int i = 0; i < L; ++i) {
+          const F4 kg = ld4(sKg + (size_t)i * K4 + 4 * q4), vn = ld4(sVn + (size_t)i * kBV + 4 * g);
+          for (int y = 0; y < 4; ++y)
+            for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(f4at(kg, y), f4at(vn, x), acc[y][x]);
+        }
+        for (int y = 0; y < 4; ++y) st4(sS + (size_t)(4 * q4 + y) * kBV + 4 * g, acc[y]);
       }
     });
   }
 }
 
 // ---- dstate: per (sequence, value head, V tile), chunks in reverse -----------------------
+//
+// Per chunk, Aqk (transposed), Kg, Qg, W and the dO tile are staged in shared memory once (Qg
+// and W are read from the workspace directly when K is too large for all of them to fit);
+// dV_new = Aqk^T dO + Kg dS' is computed in 2 x 4 register blocks and
+// dS = Diag(e^gamma_C) dS' + Qg^T dO - W^T dV_new in 4 x 4 blocks.
+
+// Whether dstate stages Qg and W in shared memory (everything fits in 200 KB).
+KDA_HD bool dstate_stages_qw(int C, int K) {
+  const size_t K4 = (size_t)pad4(K);
+  const size_t base = K4 * kBV + 2 * (size_t)C * kBV + (size_t)C * (C + 4) + (size_t)C * (K4 + 4) + K4;
+  return sizeof(float) * (base + 2 * (size_t)C * K4) <= 200u * 1024u;
+}
 
 template <class Exec>
 KDA_BODY void dstate_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
   const Plan& p = a.p;
   const int C = p.C, K = p.K, V = p.V, HV = p.HV;
+  const int K4 = pad4(K), ldk = K4 + 4, lda = C + 4, half = C / 2;
+  const bool stage_qw = dstate_stages_qw(C, K);
   const int nvt = (V + kBV - 1) / kBV;
   const int vt = (int)(bid % nvt);
   const int hv = (int)((bid / nvt) % HV);
@@ -488,17 +582,22 @@ KDA_BODY void dstate_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
     return;
   }
   const Block& b = p.blk;
-  float* sD = smem;                       // [K][kBV] gradient of the state after the chunk
-  float* sDv = sD + (size_t)K * kBV;      // [C][kBV] dV_new
-  float* sDo = sDv + (size_t)C * kBV;     // [C][kBV] dO
+  float* sD = smem;                          // [K4][kBV] gradient of the state after the chunk
+  float* sDv = sD + (size_t)K4 * kBV;        // [C][kBV] dV_new
+  float* sDo = sDv + (size_t)C * kBV;        // [C][kBV] dO
+  float* sAt = sDo + (size_t)C * kBV;        // [C][lda] Aqk^T
+  float* sKg = sAt + (size_t)C * lda;        // [C][ldk] Kg
+  float* sDc = sKg + (size_t)C * ldk;        // [K4] e^gamma_C
+  float* sQg = sDc + K4;                     // [C][K4] Qg (if staged)
+  float* sW = sQg + (size_t)C * K4;          // [C][K4] W (if staged)
   const int c0 = vt * kBV;
   const int nc = V - c0 < kBV ? V - c0 : kBV;
   const size_t sbase = ((size_t)n * HV + hv) * (size_t)K * V;
   ex.phase([&](int tid, int nthr) {
-    for (int e = tid; e < K * kBV; e += nthr) {
+    for (int e = tid; e < K4 * kBV; e += nthr) {
       const int kk = e / kBV, cl = e - (e / kBV) * kBV;
       float d = 0.f;
-      if (cl < nc && a.d_final_state != nullptr)
+      if (kk < K && cl < nc && a.d_final_state != nullptr)
         d = a.d_final_state[sbase + (a.state_v_first ? (size_t)(c0 + cl) * K + kk
                                                      : (size_t)kk * V + c0 + cl)];
       sD[e] = d;
@@ -518,7 +617,7 @@ KDA_BODY void dstate_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
     const float* Dc = blk + b.decay;
     float* dVn = block_ptr(a, c, hv) + b.dvn;
     float* hD = state_ptr(a, p.off_dh, c, hv);
-    // dS' of this chunk; the dO tile
+    // dS' of this chunk goes out; stage the dO tile, Aqk^T, Kg (Qg, W) and e^gamma_C
     ex.phase([&](int tid, int nthr) {
       for (int e = tid; e < K * kBV; e += nthr) {
         const int kk = e / kBV, cl = e - (e / kBV) * kBV;
@@ -529,31 +628,82 @@ KDA_BODY void dstate_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
         sDo[e] = (i < L && cl < nc)
                      ? ld_in(a.d_o, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + c0 + cl) : 0.f;
       }
-    });
-    // dV_new = Aqk^T dO + Kg dS'
-    ex.phase([&](int tid, int nthr) {
-      for (int e = tid; e < C * kBV; e += nthr) {
-        const int i = e / kBV, cl = e - (e / kBV) * kBV;
-        float d = 0.f;
-        if (i < L && cl < nc) {
-          for (int j = i; j < L; ++j) d = fmaf(Aqk[(size_t)j * C + i], sDo[j * kBV + cl], d);
-          const float* kr = Kg + (size_t)i * K;
-          for (int kk = 0; kk < K; ++kk) d = fmaf(kr[kk], sD[kk * kBV + cl], d);
+      for (int e = tid; e < C * C; e += nthr) {  // e = j C + i: Aqk[j][i] -> At[i][j]
+        const int j = e / C, i = e - (e / C) * C;
+        sAt[(size_t)i * lda + j] = (i < L && j < L && j >= i) ? Aqk[e] : 0.f;
+      }
+      for (int e = tid; e < C * K4; e += nthr) {
+        const int i = e / K4, kk = e - (e / K4) * K4;
+        const bool in = i < L && kk < K;
+        sKg[(size_t)i * ldk + kk] = in ? Kg[(size_t)i * K + kk] : 0.f;
+        if (stage_qw) {
+          sQg[e] = in ? Qg[(size_t)i * K + kk] : 0.f;
+          sW[e] = in ? W[(size_t)i * K + kk] : 0.f;
         }
-        sDv[e] = d;
-        if (cl < nc) dVn[(size_t)i * V + c0 + cl] = d;
+      }
+      for (int kk = tid; kk < K4; kk += nthr) sDc[kk] = kk < K ? Dc[kk] : 0.f;
+    });
+    // dV_new = Aqk^T dO + Kg dS': rows i and i + C/2, columns 4 g .. 4 g + 3
+    ex.phase([&](int tid, int nthr) {
+      for (int u = tid; u < half * (kBV / 4); u += nthr) {
+        const int i0 = u / (kBV / 4), g = u - (u / (kBV / 4)) * (kBV / 4), i1 = i0 + half;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int j = i0; j < L; ++j) {  // At[i][j] is zero for j < i
+          const F4 d = ld4(sDo + (size_t)j * kBV + 4 * g);
+          const float a0 = sAt[(size_t)i0 * lda + j], a1 = sAt[(size_t)i1 * lda + j];
+          for (int x = 0; x < 4; ++x) {
+            acc[0][x] = fmaf(a0, f4at(d, x), acc[0][x]);
+            acc[1][x] = fmaf(a1, f4at(d, x), acc[1][x]);
+          }
+        }
+        for (int kk = 0; kk < K4; kk += 4) {
+          const F4 k0 = ld4(sKg + (size_t)i0 * ldk + kk), k1 = ld4(sKg + (size_t)i1 * ldk + kk);
+          for (int y = 0; y < 4; ++y) {
+            const F4 s = ld4(sD + (size_t)(kk + y) * kBV + 4 * g);
+            const float a0 = f4at(k0, y), a1 = f4at(k1, y);
+            for (int x = 0; x < 4; ++x) {
+              acc[0][x] = fmaf(a0, f4at(s, x), acc[0][x]);
+              acc[1][x] = fmaf(a1, f4at(s, x), acc[1][x]);
+            }
+          }
+        }
+        st4(sDv + (size_t)i0 * kBV + 4 * g, acc[0]);
+        st4(sDv + (size_t)i1 * kBV + 4 * g, acc[1]);
+        for (int r = 0; r < 2; ++r) {
+          const int i = r == 0 ? i0 : i1;
+          for (int x = 0; x < 4; ++x)
+            if (4 * g + x < nc) dVn[(size_t)i * V + c0 + 4 * g + x] = acc[r][x];
+        }
       }
     });
-    // dS = Qg^T dO - W^T dV_new + Diag(e^gamma_C) dS'
+    // dS = Diag(e^gamma_C) dS' + Qg^T dO - W^T dV_new: channels 4 q .. 4 q + 3, columns 4 g ..
     ex.phase([&](int tid, int nthr) {
-      for (int e = tid; e < K * kBV; e += nthr) {
-        const int kk = e / kBV, cl = e - (e / kBV) * kBV;
-        float d = sD[e] * Dc[kk];
-        for (int i = 0; i < L; ++i) {
-          d = fmaf(Qg[(size_t)i * K + kk], sDo[i * kBV + cl], d);
-          d = fmaf(-W[(size_t)i * K + kk], sDv[i * kBV + cl], d);
+      for (int u = tid; u < (K4 / 4) * (kBV / 4); u += nthr) {
+        const int q4 = u / (kBV / 4), g = u - (u / (kBV / 4)) * (kBV / 4);
+        float acc[4][4];
+        for (int y = 0; y < 4; ++y) {
+          const F4 s = ld4(sD + (size_t)(4 * q4 + y) * kBV + 4 * g);
+          const float d = sDc[4 * q4 + y];
+          for (int x = 0; x < 4; ++x) acc[y][x] = f4at(s, x) * d;
         }
-        sD[e] = d;
+        for (int i = 0; i < L; ++i) {
+          float qg[4], w[4];
+          if (stage_qw) {
+            const F4 q = ld4(sQg + (size_t)i * K4 + 4 * q4), ww = ld4(sW + (size_t)i * K4 + 4 * q4);
+            for (int y = 0; y < 4; ++y) { qg[y] = f4at(q, y); w[y] = f4at(ww, y); }
+          } else {
+            for (int y = 0; y < 4; ++y) {
+              const int kk = 4 * q4 + y;
+              qg[y] = kk < K ? Qg[(size_t)i * K + kk] : 0.f;
+              w[y] = kk < K ? W[(size_t)i * K + kk] : 0.f;
+            }
+          }
+          const F4 o = ld4(sDo + (size_t)i * kBV + 4 * g), dv = ld4(sDv + (size_t)i * kBV + 4 * g);
+          for (int y = 0; y < 4; ++y)
+            for (int x = 0; x < 4; ++x)
+              acc[y][x] = fmaf(qg[y], f4at(o, x), fmaf(-w[y], f4at(dv, x), acc[y][x]));
+        }
+        for (int y = 0; y < 4; ++y) st4(sD + (size_t)(4 * q4 + y) * kBV + 4 * g, acc[y]);
       }
     });
   }
@@ -570,6 +720,48 @@ KDA_BODY void dstate_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
 }
 
 // ---- grads: per (chunk c, value head hv) -----------------------------------------------
+//
+// The chunk's dense products (dAqk = dO V_new^T, dQg = dO S^T, dW = -dV_new S^T,
+// dKg = V_new dS'^T, A^T dA = X (beta V)^T + Y (beta e^Gamma K)^T) run in 4 x 4 register
+// blocks over 16-byte loads.  The e^(Gamma_i - Gamma_j)-weighted sums of the Aqk and P
+// gradients take every exponent from a per-16-row-block reference rho (Gamma at the block's
+// middle row): e^(Gamma_r - Gamma_j) = e^(Gamma_r - rho_R) e^(rho_R - Gamma_j), so that one
+// exponential serves a whole block instead of one per (row, channel, j) -- unless some
+// exponent could leave [-inf, 60] (an in-block decay beyond 60 nat on either side of the
+// middle row), in which case the chunk evaluates every e^(Gamma_i - Gamma_j) directly.
+
+// Four consecutive elements off..off+3 of a row (fp32 workspace or an input tensor), zero
+// past `len`; `vec`: the row length is a multiple of 4, so that the four are one aligned
+// 16-byte (fp32) or 8-byte (bf16) load.
+KDA_HD F4 ld4w(const float* row, int off, int len, bool vec) {
+  if (vec) {
+#if defined(__CUDA_ARCH__)
+    const float4 v = __ldg(reinterpret_cast<const float4*>(row + off));
+    return {v.x, v.y, v.z, v.w};
+#else
+    return {row[off], row[off + 1], row[off + 2], row[off + 3]};
+#endif
+  }
+  return {off < len ? row[off] : 0.f, off + 1 < len ? row[off + 1] : 0.f,
+          off + 2 < len ? row[off + 2] : 0.f, off + 3 < len ? row[off + 3] : 0.f};
+}
+KDA_HD F4 ld4i(const void* base, int dtype, size_t row, int off, int len, bool vec) {
+  if (vec) {
+    if (dtype == KDA_F32) return ld4w(static_cast<const float*>(base) + row, off, len, true);
+#if defined(__CUDA_ARCH__)
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + row + off));
+    return {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+            __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
+#endif
+  }
+  return {off < len ? ld_in(base, dtype, row + off) : 0.f,
+          off + 1 < len ? ld_in(base, dtype, row + off + 1) : 0.f,
+          off + 2 < len ? ld_in(base, dtype, row + off + 2) : 0.f,
+          off + 3 < len ? ld_in(base, dtype, row + off + 3) : 0.f};
+}
+KDA_HD float dot4(const F4& a, const F4& b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
 
 template <class Exec>
 KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem) {
@@ -590,7 +782,6 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   const float* Kg = blk + b.kg;
   const float* Vn = blk + b.vn;
   const float* dVn = blk + b.dvn;
-  const float* Aqk = blk + b.aqk;
   const float* P = blk + b.p;
   const float* Be = blk + b.beta;
   const float* Dc = blk + b.decay;
@@ -600,63 +791,104 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   float* dK = blk + b.dk;
   float* dGam = blk + b.dgam;
   float* dKG = blk + b.dkg;
+  float* EK = blk + b.w;   // e^Gamma K (the W slot: W is not needed any more)
+  float* QF = blk + b.qg;  // Q e^(Gamma - rho), K e^(Gamma - rho) once Qg, Kg are consumed
+  float* KF = blk + b.kg;
   const float* S = state_ptr(a, p.off_h, c, hv);
   const float* dSp = state_ptr(a, p.off_dh, c, hv);
+  const int ldz = C + 1;                      // padded rows: the row-per-thread substitution
   float* sAk = smem;                          // [C][C] beta_i P_ij
   float* sdA = sAk + (size_t)C * C;           // [C][C] dAqk
-  float* sZ = sdA + (size_t)C * C;            // [C][C] A^T dA, then A^T dA A^T, then dP
-  float* sAq = sZ + (size_t)C * C;            // [C][C] Aqk
-  float* sB = sAq + (size_t)C * C;            // [C] beta
+  float* sZ = sdA + (size_t)C * C;            // [C][ldz] A^T dA, then A^T dA A^T, then dP
+  float* sB = sZ + (size_t)C * ldz;           // [C] beta
   float* sDB = sB + C;                        // [C] gradient of beta (the value)
   float* sRed = sDB + C;                      // [kThreads] partial sums of dA_log
+  float* sFlag = sRed + kThreads;             // [4] > 0: some block exponent out of range
   const bool has_alog = a.A_log != nullptr && a.gate_mode != KDA_GATE_PREGATED;
   const float a_exp = has_alog ? expf(a.A_log[hv]) : 1.0f;
-  auto dO = [&](int i, int v) {
-    return ld_in(a.d_o, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + v);
-  };
+  const int V4 = pad4(V), K4 = pad4(K), CB = C / 4;
+  const bool vecV = (V & 3) == 0, vecK = (K & 3) == 0;
   auto vin = [&](int i, int v) { return ld_in(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + v); };
+  // rows of the inputs dO and v (only rows < L exist)
+  auto in_row = [&](int i) { return ((size_t)(t0 + i) * HV + hv) * V; };
 
-  // the chunk's C x C matrices; dAqk = (dO V_new^T) masked lower
+  // beta P, beta; dAqk = (dO V_new^T) masked lower, in 4 x 4 blocks
   ex.phase([&](int tid, int nthr) {
     for (int e = tid; e < C * C; e += nthr) {
-      const int i = e / C, j = e - (e / C) * C;
+      const int i = e / C;
       sAk[e] = Be[i] * P[e];
-      sAq[e] = Aqk[e];
-      float d = 0.f;
-      if (i < L && j <= i)
-        for (int v = 0; v < V; ++v) d = fmaf(dO(i, v), Vn[(size_t)j * V + v], d);
-      sdA[e] = d;
     }
     for (int i = tid; i < C; i += nthr) sB[i] = Be[i];
-  });
-  // dQg = dO S^T, dW = -dV_new S^T, dKg = V_new dS'^T and their direct terms
-  ex.phase([&](int tid, int nthr) {
-    for (int e = tid; e < C * K; e += nthr) {
-      const int i = e / K, kk = e - (e / K) * K;
-      float y = 0.f, dq = 0.f, dk = 0.f, dg = 0.f, dkg_kg = 0.f;
-      if (i < L) {
-        const float* sr = S + (size_t)kk * V;
-        const float* dr = dSp + (size_t)kk * V;
-        const float* vr = Vn + (size_t)i * V;
-        const float* dvr = dVn + (size_t)i * V;
-        float dqg = 0.f, dw = 0.f, dkg = 0.f;
-        for (int v = 0; v < V; ++v) {
-          dqg = fmaf(dO(i, v), sr[v], dqg);
-          dw = fmaf(-dvr[v], sr[v], dw);
-          dkg = fmaf(vr[v], dr[v], dkg);
+    if (tid == 0) sFlag[0] = 0.f;
+    for (int u = tid; u < CB * CB; u += nthr) {
+      const int ib = u / CB, jb = u - (u / CB) * CB;
+      float acc[4][4] = {};
+      if (jb <= ib && 4 * ib < L) {
+        for (int v = 0; v < V4; v += 4) {
+          F4 o[4], w[4];
+          for (int y = 0; y < 4; ++y) {
+            const int i = 4 * ib + y, j = 4 * jb + y;
+            o[y] = i < L ? ld4i(a.d_o, a.dtype, in_row(i), v, V, vecV) : F4{0.f, 0.f, 0.f, 0.f};
+            w[y] = ld4w(Vn + (size_t)j * V, v, V, vecV);
+          }
+          for (int y = 0; y < 4; ++y)
+            for (int x = 0; x < 4; ++x) acc[y][x] += dot4(o[y], w[x]);
         }
-        const float gi = Gam[e];
-        y = dw;
-        dq = dqg * expf(gi);
-        dk = dkg * expf(Gam[(size_t)(L - 1) * K + kk] - gi);
-        dkg_kg = dkg * Kg[e];
-        dg = dqg * Qg[e] - dkg_kg;
       }
-      Y[e] = y;
-      dQ[e] = dq;
-      dK[e] = dk;
-      dGam[e] = dg;
-      dKG[e] = dkg_kg;
+      for (int y = 0; y < 4; ++y)
+        for (int x = 0; x < 4; ++x) {
+          const int i = 4 * ib + y, j = 4 * jb + x;
+          sdA[(size_t)i * C + j] = (i < L && j <= i) ? acc[y][x] : 0.f;
+        }
+    }
+  });
+  // dQg = dO S^T, dW = -dV_new S^T, dKg = V_new dS'^T in 4 x 4 blocks (rows i, channels k),
+  // and their direct terms; e^Gamma K for the A^T dA product
+  ex.phase([&](int tid, int nthr) {
+    for (int u = tid; u < CB * (K4 / 4); u += nthr) {
+      const int ib = u / (K4 / 4), kb = u - (u / (K4 / 4)) * (K4 / 4);
+      float aq[4][4] = {}, aw[4][4] = {}, ak[4][4] = {};
+      if (4 * ib < L) {
+        for (int v = 0; v < V4; v += 4) {
+          F4 o[4], dv[4], vn[4], s[4], ds[4];
+          for (int y = 0; y < 4; ++y) {
+            const int i = 4 * ib + y, kk = 4 * kb + y;
+            o[y] = i < L ? ld4i(a.d_o, a.dtype, in_row(i), v, V, vecV) : F4{0.f, 0.f, 0.f, 0.f};
+            dv[y] = ld4w(dVn + (size_t)i * V, v, V, vecV);
+            vn[y] = ld4w(Vn + (size_t)i * V, v, V, vecV);
+            s[y] = kk < K ? ld4w(S + (size_t)kk * V, v, V, vecV) : F4{0.f, 0.f, 0.f, 0.f};
+            ds[y] = kk < K ? ld4w(dSp + (size_t)kk * V, v, V, vecV) : F4{0.f, 0.f, 0.f, 0.f};
+          }
+          for (int y = 0; y < 4; ++y)
+            for (int x = 0; x < 4; ++x) {
+              aq[y][x] += dot4(o[y], s[x]);
+              aw[y][x] -= dot4(dv[y], s[x]);
+              ak[y][x] += dot4(vn[y], ds[x]);
+            }
+        }
+      }
+      for (int y = 0; y < 4; ++y)
+        for (int x = 0; x < 4; ++x) {
+          const int i = 4 * ib + y, kk = 4 * kb + x;
+          if (kk >= K) continue;
+          const size_t e = (size_t)i * K + kk;
+          float yv = 0.f, dq = 0.f, dk = 0.f, dg = 0.f, dkg_kg = 0.f, ekv = 0.f;
+          if (i < L) {
+            const float gi = Gam[e], eg = expf(gi);
+            yv = aw[y][x];
+            dq = aq[y][x] * eg;
+            dk = ak[y][x] * expf(Gam[(size_t)(L - 1) * K + kk] - gi);
+            dkg_kg = ak[y][x] * Kg[e];
+            dg = aq[y][x] * Qg[e] - dkg_kg;
+            ekv = eg * Kn[e];
+          }
+          Y[e] = yv;
+          dQ[e] = dq;
+          dK[e] = dk;
+          dGam[e] = dg;
+          dKG[e] = dkg_kg;
+          EK[e] = ekv;
+        }
     }
   });
   // X = A^T dV_new, Y = A^T dW: back substitution with (I + Diag(beta) P)^T, one thread per
@@ -675,6 +907,7 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     }
   });
   // dv; the WY part of dbeta; the e^Gamma K part of dK and dGamma; A^T dA (strictly lower)
+  // in 4 x 4 blocks
   ex.phase([&](int tid, int nthr) {
     for (int e = tid; e < C * V; e += nthr) {
       const int i = e / V, v = e - (e / V) * V;
@@ -686,7 +919,7 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
         for (int v = 0; v < V; ++v) db = fmaf(X[(size_t)i * V + v], vin(i, v), db);
         for (int kk = 0; kk < K; ++kk) {
           const size_t e = (size_t)i * K + kk;
-          db = fmaf(Y[e], expf(Gam[e]) * Kn[e], db);
+          db = fmaf(Y[e], EK[e], db);
         }
       }
       sDB[i] = db;
@@ -694,30 +927,47 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     for (int e = tid; e < C * K; e += nthr) {
       const int i = e / K;
       if (i < L) {
-        const float eg = expf(Gam[e]);
         const float t = sB[i] * Y[e];
-        dK[e] += t * eg;
-        dGam[e] += t * eg * Kn[e];
+        dK[e] += t * expf(Gam[e]);
+        dGam[e] += t * EK[e];
       }
     }
-    for (int e = tid; e < C * C; e += nthr) {
-      const int i = e / C, j = e - (e / C) * C;
-      float z = 0.f;
-      if (i < L && j < i) {
-        for (int v = 0; v < V; ++v) z = fmaf(X[(size_t)i * V + v], vin(j, v), z);
-        float zk = 0.f;
-        for (int kk = 0; kk < K; ++kk)
-          zk = fmaf(Y[(size_t)i * K + kk], expf(Gam[(size_t)j * K + kk]) * Kn[(size_t)j * K + kk], zk);
-        z = sB[j] * (z + zk);
+    for (int u = tid; u < CB * CB; u += nthr) {
+      const int ib = u / CB, jb = u - (u / CB) * CB;
+      float acc[4][4] = {};
+      if (jb <= ib && 4 * ib < L) {
+        for (int v = 0; v < V4; v += 4) {
+          F4 xr[4], vr[4];
+          for (int y = 0; y < 4; ++y) {
+            const int i = 4 * ib + y, j = 4 * jb + y;
+            xr[y] = ld4w(X + (size_t)i * V, v, V, vecV);
+            vr[y] = j < L ? ld4i(a.v, a.dtype, in_row(j), v, V, vecV) : F4{0.f, 0.f, 0.f, 0.f};
+          }
+          for (int y = 0; y < 4; ++y)
+            for (int x = 0; x < 4; ++x) acc[y][x] += dot4(xr[y], vr[x]);
+        }
+        for (int kk = 0; kk < K4; kk += 4) {
+          F4 yr[4], er[4];
+          for (int y = 0; y < 4; ++y) {
+            yr[y] = ld4w(Y + (size_t)(4 * ib + y) * K, kk, K, vecK);
+            er[y] = ld4w(EK + (size_t)(4 * jb + y) * K, kk, K, vecK);
+          }
+          for (int y = 0; y < 4; ++y)
+            for (int x = 0; x < 4; ++x) acc[y][x] += dot4(yr[y], er[x]);
+        }
       }
-      sZ[e] = z;
+      for (int y = 0; y < 4; ++y)
+        for (int x = 0; x < 4; ++x) {
+          const int i = 4 * ib + y, j = 4 * jb + x;
+          sZ[(size_t)i * ldz + j] = (i < L && j < i) ? sB[j] * acc[y][x] : 0.f;
+        }
     }
   });
   // dAkk = -(A^T dA A^T) masked strictly lower (row r of A^T dA A^T is A applied to row r of
   // A^T dA: forward substitution, one thread per row); dP = beta dAkk; dbeta += rowsum(dAkk P)
   ex.phase([&](int tid, int nthr) {
     for (int r = tid; r < L; r += nthr) {
-      float* z = sZ + (size_t)r * C;
+      float* z = sZ + (size_t)r * ldz;
       for (int i = 1; i < r; ++i) {
         float x = z[i];
         for (int j = 0; j < i; ++j) x = fmaf(-sAk[(size_t)i * C + j], z[j], x);
@@ -732,29 +982,126 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
       sDB[r] += db;
     }
   });
-  // the e^(Gamma_i - Gamma_j) terms of Aqk and P, one thread per (row r, channel k): r as
-  // the row index i (dQ, dK) and as the column index j (dK)
+  // block references rho (Gamma at each 16-row block's middle row), Q and K scaled by
+  // e^(Gamma - rho), and the range check of every exponent the blocked sums use
   ex.phase([&](int tid, int nthr) {
     for (int e = tid; e < C * K; e += nthr) {
-      const int r = e / K, kk = e - (e / K) * K;
-      if (r >= L) continue;
-      const float gr = Gam[e];
-      float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
-      for (int j = 0; j <= r; ++j) {
-        const float kd = Kn[(size_t)j * K + kk] * expf(gr - Gam[(size_t)j * K + kk]);
-        s1 = fmaf(sdA[(size_t)r * C + j], kd, s1);
-        if (j < r) s2 = fmaf(sZ[(size_t)r * C + j], kd, s2);
+      const int i = e / K, kk = e - (e / K) * K;
+      float qf = 0.f, kf = 0.f;
+      if (i < L) {
+        const int B = i >> 4;
+        const int mid = (16 * B + 7) < L - 1 ? 16 * B + 7 : L - 1;
+        const float gi = Gam[e], rho = Gam[(size_t)mid * K + kk];
+        bool bad = gi - rho > 60.f;
+        // rho_R - Gamma_i for every block R whose rows see row i (R >= B)
+        for (int R = B; 16 * R < L; ++R) {
+          const int mr = (16 * R + 7) < L - 1 ? 16 * R + 7 : L - 1;
+          bad = bad || Gam[(size_t)mr * K + kk] - gi > 60.f;
+        }
+        if (bad) ex.atomic_add(sFlag, 1.f);
+        const float f = expf(gi - rho);
+        qf = Qn[e] * f;
+        kf = Kn[e] * f;
       }
-      for (int i = r; i < L; ++i) {
-        const float ed = expf(Gam[(size_t)i * K + kk] - gr);
-        s3 = fmaf(sdA[(size_t)i * C + r], Qn[(size_t)i * K + kk] * ed, s3);
-        if (i > r) s4 = fmaf(sZ[(size_t)i * C + r], Kn[(size_t)i * K + kk] * ed, s4);
-      }
-      dQ[e] += s1;
-      dK[e] += s2 + s3 + s4;
-      dGam[e] += Qn[e] * s1 + Kn[e] * (s2 - s3 - s4);
+      QF[e] = qf;
+      KF[e] = kf;
     }
   });
+  if (sFlag[0] == 0.f) {
+    // the e^(Gamma_i - Gamma_j) terms of Aqk and P, one thread per (16-row block R, channel
+    // k), for the rows r of block R:
+    //   s1 = sum_{j<=r} dAqk[r][j] K_j e^(G_r - G_j)   s2 = sum_{j<r} dP[r][j] K_j e^(G_r - G_j)
+    //   s3 = sum_{i>=r} dAqk[i][r] Q_i e^(G_i - G_r)   s4 = sum_{i>r} dP[i][r] K_i e^(G_i - G_r)
+    // with e^(G_r - G_j) = e^(G_r - rho_R) e^(rho_R - G_j) and e^(G_i - G_r) =
+    // e^(G_i - rho_I) e^(rho_I - G_r) (I the block of i)
+    ex.phase([&](int tid, int nthr) {
+      const int NB = (L + 15) >> 4;
+      for (int u = tid; u < NB * K; u += nthr) {
+        const int R = u / K, kk = u - (u / K) * K;
+        const int r0 = 16 * R;
+        const int mid = (r0 + 7) < L - 1 ? r0 + 7 : L - 1;
+        const float rho = Gam[(size_t)mid * K + kk];
+        float s1[16], s2[16];
+        for (int x = 0; x < 16; ++x) { s1[x] = 0.f; s2[x] = 0.f; }
+        const int jend = (r0 + 16 < L ? r0 + 16 : L);
+        for (int j = 0; j < jend; ++j) {
+          const float ke = Kn[(size_t)j * K + kk] * expf(rho - Gam[(size_t)j * K + kk]);
+          const float* da = sdA + (size_t)r0 * C + j;
+          const float* dz = sZ + (size_t)r0 * ldz + j;
+          for (int x = 0; x < 16; ++x) {  // rows r = r0 + x; sdA, sZ are zero above the diagonal
+            s1[x] = fmaf(da[(size_t)x * C], ke, s1[x]);
+            s2[x] = fmaf(dz[(size_t)x * ldz], ke, s2[x]);
+          }
+        }
+        for (int x = 0; x < 16; ++x) {  // the (r, k) elements belong to this unit alone
+          const int r = r0 + x;
+          if (r >= L) break;
+          const size_t e = (size_t)r * K + kk;
+          const float f = expf(Gam[e] - rho);
+          const float a1 = s1[x] * f, a2 = s2[x] * f;
+          dQ[e] += a1;
+          dK[e] += a2;
+          dGam[e] += Qn[e] * a1 + Kn[e] * a2;
+        }
+        float s3[16], s4[16];
+        for (int x = 0; x < 16; ++x) { s3[x] = 0.f; s4[x] = 0.f; }
+        for (int I = R; I < NB; ++I) {
+          const int i0 = 16 * I;
+          const int mi = (i0 + 7) < L - 1 ? i0 + 7 : L - 1;
+          const float rhoI = Gam[(size_t)mi * K + kk];
+          float qf[16], kf[16];
+          for (int y = 0; y < 16; ++y) {
+            const bool in = i0 + y < L;
+            qf[y] = in ? QF[(size_t)(i0 + y) * K + kk] : 0.f;
+            kf[y] = in ? KF[(size_t)(i0 + y) * K + kk] : 0.f;
+          }
+          for (int x = 0; x < 16; ++x) {
+            const int r = r0 + x;
+            if (r >= L) break;
+            float t3 = 0.f, t4 = 0.f;
+            for (int y = 0; y < 16; ++y) {  // sdA[i][r] = 0 for i < r, sZ[i][r] = 0 for i <= r
+              t3 = fmaf(sdA[(size_t)(i0 + y) * C + r], qf[y], t3);
+              t4 = fmaf(sZ[(size_t)(i0 + y) * ldz + r], kf[y], t4);
+            }
+            const float e = expf(rhoI - Gam[(size_t)r * K + kk]);
+            s3[x] = fmaf(e, t3, s3[x]);
+            s4[x] = fmaf(e, t4, s4[x]);
+          }
+        }
+        for (int x = 0; x < 16; ++x) {
+          const int r = r0 + x;
+          if (r >= L) break;
+          const size_t e = (size_t)r * K + kk;
+          dK[e] += s3[x] + s4[x];
+          dGam[e] -= Kn[e] * (s3[x] + s4[x]);
+        }
+      }
+    });
+  } else {
+    // exact fallback: every e^(Gamma_i - Gamma_j) evaluated directly, one thread per (row
+    // r, channel k): r as the row index i (dQ, dK) and as the column index j (dK)
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < C * K; e += nthr) {
+        const int r = e / K, kk = e - (e / K) * K;
+        if (r >= L) continue;
+        const float gr = Gam[e];
+        float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
+        for (int j = 0; j <= r; ++j) {
+          const float kd = Kn[(size_t)j * K + kk] * expf(gr - Gam[(size_t)j * K + kk]);
+          s1 = fmaf(sdA[(size_t)r * C + j], kd, s1);
+          if (j < r) s2 = fmaf(sZ[(size_t)r * ldz + j], kd, s2);
+        }
+        for (int i = r; i < L; ++i) {
+          const float ed = expf(Gam[(size_t)i * K + kk] - gr);
+          s3 = fmaf(sdA[(size_t)i * C + r], Qn[(size_t)i * K + kk] * ed, s3);
+          if (i > r) s4 = fmaf(sZ[(size_t)i * ldz + r], Kn[(size_t)i * K + kk] * ed, s4);
+        }
+        dQ[e] += s1;
+        dK[e] += s2 + s3 + s4;
+        dGam[e] += Qn[e] * s1 + Kn[e] * (s2 - s3 - s4);
+      }
+    });
+  }
   // reverse cumsum of dGamma (plus the gamma_C terms on the last row) and the gate backward,
   // one thread per channel
   ex.phase([&](int tid, int nthr) {

@@ -953,7 +953,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
         uint8_t* slot = sm + R_RING + s * SLOT;
         const uint32_t b1 = smem_u32(slot + OFF_B1), b2 = smem_u32(slot + OFF_B2);
         // G1+O1 need the bf16 S^T of this chunk and a cleared O^T
-        if (!mbar_wait(bar_st, (uint32_t)(ci & 1))) { ok = false; break; }
+        if (!mbar_wait_spin(bar_st, (uint32_t)(ci & 1))) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
@@ -962,7 +962,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
                       idesc_bf16(128, 128), 1);
         mma_commit(bar_v);
         // G2+O2 need the bf16 V_new^T of this chunk
-        if (!mbar_wait(bar_vn, (uint32_t)(ci & 1))) { ok = false; break; }
+        if (!mbar_wait_spin(bar_vn, (uint32_t)(ci & 1))) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)

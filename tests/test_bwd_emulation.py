@@ -193,3 +193,16 @@ def test_random_shapes(emu, tmp_path, seed):
     (partial value tiles), chunk size, gate mode, dtype, varlen, optional inputs, options."""
     inp, opts = bt.random_case(seed)
     check(emu, tmp_path, inp, chunk_form=True, **opts)
+
+
+@pytest.mark.parametrize("C", [32, 64])
+def test_steep_decay_takes_the_exact_exponent_path(emu, tmp_path, C):
+    """A pre-gated log decay of -9 to -15 per element: within a 16-row block Gamma drops by
+    more than 60 nat on one side of the middle row, so the gradient kernel evaluates every
+    e^(Gamma_i - Gamma_j) directly instead of through block references; a milder chunk in the
+    same batch (the first sequence) keeps the blocked path.  Both against the oracle."""
+    inp = kin.make_inputs(wl_(B=2, T=100, C=C, gate=kin.GATE_PREGATED, seed=60 + C))
+    r = np.random.default_rng(61 + C)
+    inp.g[1] = -r.uniform(9.0, 15.0, size=inp.g[1].shape).astype(np.float32)
+    inp.g[0] = -np.abs(inp.g[0]) * np.float32(0.5)
+    check(emu, tmp_path, inp)
