@@ -23,11 +23,23 @@ struct GpuExec {
   }
   __device__ __forceinline__ void atomic_add(float* p, float x) { atomicAdd(p, x); }
   __device__ __forceinline__ void flag(unsigned int* s, unsigned int bits) { atomicOr(s, bits); }
+  // 16 bytes global -> shared without a round trip through registers (both 16-byte aligned);
+  // complete once copy_wait() has returned and the phase's barrier has passed
+  __device__ __forceinline__ void copy16(float* dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+  }
+  __device__ __forceinline__ void copy_wait() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  }
 };
 
 __global__ void __launch_bounds__(kThreads) prep_kernel(const Args a) {
+  extern __shared__ float smem[];
   GpuExec ex;
-  prep_body(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y);
+  prep_body(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);
 }
 
 __global__ void __launch_bounds__(kThreads) states_kernel(const Args a) {
@@ -143,17 +155,16 @@ cudaError_t run_chunk_table(const Args& a, cudaStream_t st) {
   return launch_chunk_table(t, st);
 }
 
-cudaError_t run_prep(const Args& a, cudaStream_t st) {
-  prep_kernel<<<dim3((unsigned)a.p.nct, (unsigned)a.p.HV), kThreads, 0, st>>>(a);
-  return cudaGetLastError();
-}
-
 template <class Kernel>
 cudaError_t launch_smem(Kernel kernel, dim3 grid, size_t smem, const Args& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t run_prep(const Args& a, cudaStream_t st) {
+  return launch_smem(prep_kernel, dim3((unsigned)a.p.nct, (unsigned)a.p.HV), prep_smem(a.p), a, st);
 }
 
 cudaError_t run_states(const Args& a, cudaStream_t st) {

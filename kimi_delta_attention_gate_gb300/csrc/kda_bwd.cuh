@@ -43,9 +43,13 @@
 #if defined(__CUDACC__)
 #define KDA_HD __host__ __device__ __forceinline__
 #define KDA_BODY __device__ __forceinline__
+#define KDA_UNROLL _Pragma("unroll")
+#define KDA_UNROLL4 _Pragma("unroll 4")
 #else
 #define KDA_HD inline
 #define KDA_BODY inline
+#define KDA_UNROLL
+#define KDA_UNROLL4
 #endif
 
 namespace kda {
@@ -172,6 +176,9 @@ inline int64_t state_blocks(const Plan& p) {
   return (int64_t)p.N * p.HV * ((p.V + kBV - 1) / kBV);
 }
 // Dynamic shared memory (bytes) of the stages.
+inline size_t prep_smem(const Plan& p) {
+  return sizeof(float) * ((size_t)p.C * p.C + (size_t)p.C * (p.K + p.V) + 4);
+}
 inline size_t states_smem(const Plan& p) {
   const size_t K4 = (size_t)((p.K + 3) & ~3), C = (size_t)p.C;
   return sizeof(float) * (K4 * kBV + 2 * C * kBV + C * (K4 + 4) + C * K4 + K4);
@@ -182,9 +189,20 @@ inline size_t dstate_smem(const Plan& p) {
   const size_t base = K4 * kBV + 2 * C * kBV + C * (C + 4) + C * (K4 + 4) + K4;
   return sizeof(float) * (base + (dstate_stages_qw(p.C, p.K) ? 2 * C * K4 : 0));
 }
+// floats of the gradient stage's staging / scratch region: the back substitution's column
+// half, the 32-column slices of the products, the row-norm partials
+inline size_t grads_scratch(const Plan& p) {
+  const size_t C = (size_t)p.C, K4 = (size_t)((p.K + 3) & ~3);
+  size_t s = C * ((p.V + p.K + 1) / 2);
+  s = s > (2 * K4 + 3 * C) * 20 ? s : (2 * K4 + 3 * C) * 20;  // 16-column product slices
+  s = s > 2 * C * 36 ? s : 2 * C * 36;                          // 32-column A^T dA slices
+  s = s > 16 * C ? s : 16 * C;
+  s = s > C * (C + 4) ? s : C * (C + 4);                        // dP transposed
+  return s;
+}
 inline size_t grads_smem(const Plan& p) {
-  return sizeof(float) * (2 * (size_t)p.C * p.C + (size_t)p.C * (p.C + 1) + 2 * (size_t)p.C +
-                          kThreads + 4);
+  return sizeof(float) * ((size_t)p.C * p.C + (size_t)p.C * (p.C + 4) + (size_t)p.C * (p.C + 1) + 2 * (size_t)p.C +
+                          kThreads + 4 + (size_t)((p.K + 3) & ~3) + grads_scratch(p));
 }
 
 // ---- element helpers ------------------------------------------------------------------
@@ -275,10 +293,66 @@ KDA_HD bool seq_range(const Args& a, int n, int64_t& bos, int64_t& eos, int64_t&
          cfirst + (eos - bos + p.C - 1) / p.C <= p.nct;
 }
 
+// ---- small vector helpers (16-byte loads on the GPU, plain element accesses on the host) ---
+
+struct F4 { float x, y, z, w; };
+// four consecutive floats from a 16-byte aligned address (a 16-byte shared load on the GPU)
+KDA_HD F4 ld4(const float* p) {
+#if defined(__CUDA_ARCH__)
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  return {v.x, v.y, v.z, v.w};
+#else
+  return {p[0], p[1], p[2], p[3]};
+#endif
+}
+KDA_HD void st4(float* p, const float (&v)[4]) {
+#if defined(__CUDA_ARCH__)
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+#else
+  p[0] = v[0]; p[1] = v[1]; p[2] = v[2]; p[3] = v[3];
+#endif
+}
+KDA_HD float f4at(const F4& v, int i) { return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w)); }
+
+KDA_HD int pad4(int x) { return (x + 3) & ~3; }
+
+// Four consecutive elements off..off+3 of a row (fp32 workspace or an input tensor), zero
+// past `len`; `vec`: the row length is a multiple of 4, so that the four are one aligned
+// 16-byte (fp32) or 8-byte (bf16) load.
+KDA_HD F4 ld4w(const float* row, int off, int len, bool vec) {
+  if (vec) {
+#if defined(__CUDA_ARCH__)
+    const float4 v = __ldg(reinterpret_cast<const float4*>(row + off));
+    return {v.x, v.y, v.z, v.w};
+#else
+    return {row[off], row[off + 1], row[off + 2], row[off + 3]};
+#endif
+  }
+  return {off < len ? row[off] : 0.f, off + 1 < len ? row[off + 1] : 0.f,
+          off + 2 < len ? row[off + 2] : 0.f, off + 3 < len ? row[off + 3] : 0.f};
+}
+KDA_HD F4 ld4i(const void* base, int dtype, size_t row, int off, int len, bool vec) {
+  if (vec) {
+    if (dtype == KDA_F32) return ld4w(static_cast<const float*>(base) + row, off, len, true);
+#if defined(__CUDA_ARCH__)
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + row + off));
+    return {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+            __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
+#endif
+  }
+  return {off < len ? ld_in(base, dtype, row + off) : 0.f,
+          off + 1 < len ? ld_in(base, dtype, row + off + 1) : 0.f,
+          off + 2 < len ? ld_in(base, dtype, row + off + 2) : 0.f,
+          off + 3 < len ? ld_in(base, dtype, row + off + 3) : 0.f};
+}
+KDA_HD float dot4(const F4& a, const F4& b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
 // ---- prep: per (chunk c, value head hv) ------------------------------------------------
 
 template <class Exec>
-KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv) {
+KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem) {
   const Plan& p = a.p;
   const int C = p.C, K = p.K, V = p.V, H = p.H, HV = p.HV, h = hv / p.G;
   int n, L;
@@ -302,9 +376,12 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv) {
   float* Dc = blk + b.decay;
   const bool has_alog = a.A_log != nullptr && a.gate_mode != KDA_GATE_PREGATED;
   const float a_exp = has_alog ? expf(a.A_log[hv]) : 1.0f;
+  float* sFlag = smem + (size_t)C * C + (size_t)C * (K + V);  // > 0: an exponent out of range
 
   // gate activation, q and k rows, beta; rows i >= L are zero
   ex.phase([&](int tid, int nthr) {
+    if (tid == 0) sFlag[0] = 0.f;
+    KDA_UNROLL4
     for (int e = tid; e < C * K; e += nthr) {
       const int i = e / K, kk = e - (e / K) * K;
       float gv = 0.f, qv = 0.f, kv = 0.f;
@@ -335,6 +412,7 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv) {
   ex.phase([&](int tid, int nthr) {
     for (int kk = tid; kk < K; kk += nthr) {
       float acc = 0.f;
+      KDA_UNROLL4
       for (int i = 0; i < L; ++i) {
         acc += Gam[(size_t)i * K + kk];
         Gam[(size_t)i * K + kk] = acc;
@@ -346,65 +424,161 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv) {
       float* row = (r < C ? Qn : Kn) + (size_t)i * K;
       float mul = 1.f;
       if (a.qk_l2norm) {
-        float ss = 0.f;
-        for (int kk = 0; kk < K; ++kk) ss = fmaf(row[kk], row[kk], ss);
-        mul = 1.0f / sqrtf(ss + kL2Eps);
+        float ss = 0.f, ss2 = 0.f;
+        int kk = 0;
+        KDA_UNROLL4
+        for (; kk + 1 < K; kk += 2) {
+          ss = fmaf(row[kk], row[kk], ss);
+          ss2 = fmaf(row[kk + 1], row[kk + 1], ss2);
+        }
+        if (kk < K) ss = fmaf(row[kk], row[kk], ss);
+        mul = 1.0f / sqrtf((ss + ss2) + kL2Eps);
       }
       if (r < C) mul *= a.scale;
+      KDA_UNROLL4
       for (int kk = 0; kk < K; ++kk) row[kk] *= mul;
     }
   });
-  // Aqk (j <= i) and P (j < i); e^gamma_C; Qg, Kg; the right-hand sides of W and U
+  // e^gamma_C; Qg, Kg; the right-hand sides of W and U; the block-referenced operands of Aqk
+  // and P: QF = Q e^(Gamma - rho), KF = K e^(Gamma - rho) (rho: Gamma at the middle row of the
+  // row's 16-row block) and, for every block I, the stacked key rows KI_I[j] = K_j
+  // e^(rho_I - Gamma_j), j < 16 (I + 1), so that Aqk[i][j] = QF_i . KI_I[j] needs no
+  // exponential; any exponent beyond 60 sends the chunk to the direct evaluation
+  float* QFp = blk + b.y;             // [C][K] in the (here unused) gradient slots
+  float* KFp = QFp + (size_t)C * K;   // [C][K]
+  float* KIp = KFp + (size_t)C * K;   // [16 NB (NB + 1) / 2][K]
+  const int NB = (L + 15) >> 4;
+  auto mid_row = [&](int B) { return (16 * B + 7) < L - 1 ? 16 * B + 7 : L - 1; };
   ex.phase([&](int tid, int nthr) {
-    for (int e = tid; e < C * C; e += nthr) {
-      const int i = e / C, j = e - (e / C) * C;
-      float sq = 0.f, sk = 0.f;
-      if (i < L && j <= i) {
-        const float* gi = Gam + (size_t)i * K;
-        const float* gj = Gam + (size_t)j * K;
-        const float* qi = Qn + (size_t)i * K;
-        const float* ki = Kn + (size_t)i * K;
-        const float* kj = Kn + (size_t)j * K;
-        for (int kk = 0; kk < K; ++kk) {
-          const float kd = kj[kk] * expf(gi[kk] - gj[kk]);
-          sq = fmaf(qi[kk], kd, sq);
-          sk = fmaf(ki[kk], kd, sk);
-        }
-      }
-      Aqk[e] = sq;
-      P[e] = j < i ? sk : 0.f;
-    }
     for (int kk = tid; kk < K; kk += nthr) Dc[kk] = expf(Gam[(size_t)(L - 1) * K + kk]);
+    KDA_UNROLL4
     for (int e = tid; e < C * K; e += nthr) {
       const int i = e / K, kk = e - (e / K) * K;
-      float qg = 0.f, kg = 0.f, w = 0.f;
+      float qg = 0.f, kg = 0.f, w = 0.f, qf = 0.f, kf = 0.f;
       if (i < L) {
         const float gi = Gam[e], eg = expf(gi);
         qg = Qn[e] * eg;
         kg = Kn[e] * expf(Gam[(size_t)(L - 1) * K + kk] - gi);
         w = Be[i] * eg * Kn[e];
+        const float rel = gi - Gam[(size_t)mid_row(i >> 4) * K + kk];
+        if (rel > 60.f) ex.atomic_add(sFlag, 1.f);
+        const float f = expf(rel);
+        qf = Qn[e] * f;
+        kf = Kn[e] * f;
       }
       Qg[e] = qg;
       Kg[e] = kg;
       W[e] = w;
+      QFp[e] = qf;
+      KFp[e] = kf;
     }
+    KDA_UNROLL4
     for (int e = tid; e < C * V; e += nthr) {
       const int i = e / V, cc = e - (e / V) * V;
       U[e] = i < L ? Be[i] * ld_in(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + cc) : 0.f;
     }
-  });
-  // W and U: forward substitution with (I + Diag(beta) P), one thread per column
-  ex.phase([&](int tid, int nthr) {
-    for (int col = tid; col < K + V; col += nthr) {
-      float* X = col < K ? W + col : U + (col - K);
-      const size_t ld = col < K ? (size_t)K : (size_t)V;
-      for (int i = 1; i < L; ++i) {
-        float x = X[i * ld];
-        const float bi = Be[i];
-        const float* pr = P + (size_t)i * C;
-        for (int j = 0; j < i; ++j) x = fmaf(-bi * pr[j], X[j * ld], x);
-        X[i * ld] = x;
+    KDA_UNROLL4
+    for (int e = tid; e < 8 * NB * (NB + 1) * K; e += nthr) {  // stacked rows of KI
+      const int row = e / K, kk = e - (e / K) * K;
+      // block I's rows start at 8 I (I + 1): 0, 16, 48, 96
+      const int I = row >= 96 ? 3 : (row >= 48 ? 2 : (row >= 16 ? 1 : 0));
+      const int j = row - 8 * I * (I + 1);
+      float v = 0.f;
+      if (j < L) {
+        const float ex_ = Gam[(size_t)mid_row(I) * K + kk] - Gam[(size_t)j * K + kk];
+        if (ex_ > 60.f) ex.atomic_add(sFlag, 1.f);
+        v = Kn[(size_t)j * K + kk] * expf(ex_);
       }
+      KIp[e] = v;
+    }
+  });
+  const int CB = C / 4;
+  const bool vecK = (K & 3) == 0;
+  if (sFlag[0] == 0.f) {
+    // Aqk (j <= i) and P (j < i) in 4 x 4 blocks: rows i of one 16-row block I, keys j
+    ex.phase([&](int tid, int nthr) {
+      for (int u = tid; u < CB * CB; u += nthr) {
+        const int ib = u / CB, jb = u - (u / CB) * CB;
+        float aq[4][4] = {}, ak[4][4] = {};
+        if (jb <= ib && 4 * ib < L) {
+          const int I = (4 * ib) >> 4;
+          const float* KI = KIp + (size_t)(8 * I * (I + 1)) * K;
+          for (int kk = 0; kk < pad4(K); kk += 4) {
+            F4 qf[4], kf[4], kj[4];
+            for (int y = 0; y < 4; ++y) {
+              qf[y] = ld4w(QFp + (size_t)(4 * ib + y) * K, kk, K, vecK);
+              kf[y] = ld4w(KFp + (size_t)(4 * ib + y) * K, kk, K, vecK);
+              kj[y] = ld4w(KI + (size_t)(4 * jb + y) * K, kk, K, vecK);
+            }
+            for (int y = 0; y < 4; ++y)
+              for (int x = 0; x < 4; ++x) {
+                aq[y][x] += dot4(qf[y], kj[x]);
+                ak[y][x] += dot4(kf[y], kj[x]);
+              }
+          }
+        }
+        for (int y = 0; y < 4; ++y)
+          for (int x = 0; x < 4; ++x) {
+            const int i = 4 * ib + y, j = 4 * jb + x;
+            const size_t e = (size_t)i * C + j;
+            Aqk[e] = (i < L && j <= i) ? aq[y][x] : 0.f;
+            P[e] = (i < L && j < i) ? ak[y][x] : 0.f;
+          }
+      }
+    });
+  } else {
+    // exact path: every e^(Gamma_i - Gamma_j) evaluated directly
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < C * C; e += nthr) {
+        const int i = e / C, j = e - (e / C) * C;
+        float sq = 0.f, sk = 0.f;
+        if (i < L && j <= i) {
+          const float* gi = Gam + (size_t)i * K;
+          const float* gj = Gam + (size_t)j * K;
+          const float* qi = Qn + (size_t)i * K;
+          const float* ki = Kn + (size_t)i * K;
+          const float* kj = Kn + (size_t)j * K;
+          for (int kk = 0; kk < K; ++kk) {
+            const float kd = kj[kk] * expf(gi[kk] - gj[kk]);
+            sq = fmaf(qi[kk], kd, sq);
+            sk = fmaf(ki[kk], kd, sk);
+          }
+        }
+        Aqk[e] = sq;
+        P[e] = j < i ? sk : 0.f;
+      }
+    });
+  }
+  // W and U: forward substitution with (I + Diag(beta) P) on shared-memory columns (one
+  // thread per column; the row of beta P is read by every thread at once)
+  float* sP = smem;                   // [C][C] beta_i P_ij
+  float* sX = sP + (size_t)C * C;     // [C][K + V] the right-hand sides, then the solutions
+  const int ncol = K + V;
+  ex.phase([&](int tid, int nthr) {
+    KDA_UNROLL4
+    for (int e = tid; e < C * C; e += nthr) sP[e] = Be[e / C] * P[e];
+    KDA_UNROLL4
+    for (int e = tid; e < C * ncol; e += nthr) {
+      const int i = e / ncol, col = e - (e / ncol) * ncol;
+      sX[e] = col < K ? W[(size_t)i * K + col] : U[(size_t)i * V + col - K];
+    }
+  });
+  ex.phase([&](int tid, int nthr) {
+    for (int col = tid; col < ncol; col += nthr) {
+      for (int i = 1; i < L; ++i) {
+        float x = sX[(size_t)i * ncol + col];
+        const float* pr = sP + (size_t)i * C;
+        for (int j = 0; j < i; ++j) x = fmaf(-pr[j], sX[(size_t)j * ncol + col], x);
+        sX[(size_t)i * ncol + col] = x;
+      }
+    }
+  });
+  ex.phase([&](int tid, int nthr) {
+    KDA_UNROLL4
+    for (int e = tid; e < C * ncol; e += nthr) {
+      const int i = e / ncol, col = e - (e / ncol) * ncol;
+      if (col < K) W[(size_t)i * K + col] = sX[e];
+      else U[(size_t)i * V + col - K] = sX[e];
     }
   });
 }
@@ -418,26 +592,6 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv) {
 // rows, and W's rows are K4 + 4 floats apart so that the rows a warp reads fall in different
 // banks.
 
-struct F4 { float x, y, z, w; };
-// four consecutive floats from a 16-byte aligned address (a 16-byte shared load on the GPU)
-KDA_HD F4 ld4(const float* p) {
-#if defined(__CUDA_ARCH__)
-  const float4 v = *reinterpret_cast<const float4*>(p);
-  return {v.x, v.y, v.z, v.w};
-#else
-  return {p[0], p[1], p[2], p[3]};
-#endif
-}
-KDA_HD void st4(float* p, const float (&v)[4]) {
-#if defined(__CUDA_ARCH__)
-  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-#else
-  p[0] = v[0]; p[1] = v[1]; p[2] = v[2]; p[3] = v[3];
-#endif
-}
-KDA_HD float f4at(const F4& v, int i) { return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w)); }
-
-KDA_HD int pad4(int x) { return (x + 3) & ~3; }
 
 template <class Exec>
 KDA_BODY void states_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
@@ -484,23 +638,41 @@ KDA_BODY void states_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
     const float* Dc = blk + b.decay;
     float* Vn = block_ptr(a, c, hv) + b.vn;
     float* hS = state_ptr(a, p.off_h, c, hv);
-    // stage W, Kg, U, e^gamma_C; the state before this chunk goes out
+    // stage W, Kg, U, e^gamma_C (16-byte asynchronous copies where the rows allow them; the
+    // rows past L of the workspace blocks are zero); the state before this chunk goes out
     ex.phase([&](int tid, int nthr) {
-      for (int e = tid; e < C * K4; e += nthr) {
-        const int i = e / K4, kk = e - (e / K4) * K4;
-        const bool in = i < L && kk < K;
-        sW[(size_t)i * ldw + kk] = in ? W[(size_t)i * K + kk] : 0.f;
-        sKg[e] = in ? Kg[(size_t)i * K + kk] : 0.f;
+      if ((K & 3) == 0) {
+        const int q = K4 / 4;
+        for (int e = tid; e < C * q; e += nthr) {
+          const int i = e / q, k4 = 4 * (e - (e / q) * q);
+          ex.copy16(sW + (size_t)i * ldw + k4, W + (size_t)i * K + k4);
+          ex.copy16(sKg + (size_t)i * K4 + k4, Kg + (size_t)i * K + k4);
+        }
+        for (int e = tid; e < q; e += nthr) ex.copy16(sD + 4 * e, Dc + 4 * e);
+      } else {
+        for (int e = tid; e < C * K4; e += nthr) {
+          const int i = e / K4, kk = e - (e / K4) * K4;
+          sW[(size_t)i * ldw + kk] = kk < K ? W[(size_t)i * K + kk] : 0.f;
+          sKg[e] = kk < K ? Kg[(size_t)i * K + kk] : 0.f;
+        }
+        for (int kk = tid; kk < K4; kk += nthr) sD[kk] = kk < K ? Dc[kk] : 0.f;
       }
-      for (int e = tid; e < C * kBV; e += nthr) {
-        const int i = e / kBV, cl = e - (e / kBV) * kBV;
-        sU[e] = (i < L && cl < nc) ? U[(size_t)i * V + c0 + cl] : 0.f;
+      if ((V & 3) == 0 && nc == kBV) {
+        for (int e = tid; e < C * (kBV / 4); e += nthr) {
+          const int i = e / (kBV / 4), x4 = 4 * (e - (e / (kBV / 4)) * (kBV / 4));
+          ex.copy16(sU + (size_t)i * kBV + x4, U + (size_t)i * V + c0 + x4);
+        }
+      } else {
+        for (int e = tid; e < C * kBV; e += nthr) {
+          const int i = e / kBV, cl = e - (e / kBV) * kBV;
+          sU[e] = cl < nc ? U[(size_t)i * V + c0 + cl] : 0.f;
+        }
       }
-      for (int kk = tid; kk < K4; kk += nthr) sD[kk] = kk < K ? Dc[kk] : 0.f;
       for (int e = tid; e < K * kBV; e += nthr) {
         const int kk = e / kBV, cl = e - (e / kBV) * kBV;
         if (cl < nc) hS[(size_t)kk * V + c0 + cl] = sS[e];
       }
+      ex.copy_wait();
     });
     // V_new = U - W S: rows i and i + C/2, columns 4 g .. 4 g + 3
     ex.phase([&](int tid, int nthr) {
@@ -554,7 +726,7 @@ KDA_BODY void states_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
 
 // ---- dstate: per (sequence, value head, V tile), chunks in reverse -----------------------
 //
-// Per chunk, Aqk (transposed), Kg, Qg, W and the dO tile are staged in shared memory once (Qg
+// Per chunk, Aqk, Kg, Qg, W and the dO tile are staged in shared memory once (Qg
 // and W are read from the workspace directly when K is too large for all of them to fit);
 // dV_new = Aqk^T dO + Kg dS' is computed in 2 x 4 register blocks and
 // dS = Diag(e^gamma_C) dS' + Qg^T dO - W^T dV_new in 4 x 4 blocks.
@@ -585,7 +757,7 @@ KDA_BODY void dstate_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
   float* sD = smem;                          // [K4][kBV] gradient of the state after the chunk
   float* sDv = sD + (size_t)K4 * kBV;        // [C][kBV] dV_new
   float* sDo = sDv + (size_t)C * kBV;        // [C][kBV] dO
-  float* sAt = sDo + (size_t)C * kBV;        // [C][lda] Aqk^T
+  float* sAt = sDo + (size_t)C * kBV;        // [C][lda] Aqk (row j, column i)
   float* sKg = sAt + (size_t)C * lda;        // [C][ldk] Kg
   float* sDc = sKg + (size_t)C * ldk;        // [K4] e^gamma_C
   float* sQg = sDc + K4;                     // [C][K4] Qg (if staged)
@@ -628,29 +800,44 @@ KDA_BODY void dstate_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
         sDo[e] = (i < L && cl < nc)
                      ? ld_in(a.d_o, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + c0 + cl) : 0.f;
       }
-      for (int e = tid; e < C * C; e += nthr) {  // e = j C + i: Aqk[j][i] -> At[i][j]
-        const int j = e / C, i = e - (e / C) * C;
-        sAt[(size_t)i * lda + j] = (i < L && j < L && j >= i) ? Aqk[e] : 0.f;
+      // Aqk row-major (row j, column i; zero above the diagonal and past L in the workspace)
+      for (int e = tid; e < C * (C / 4); e += nthr) {
+        const int j = e / (C / 4), i4 = 4 * (e - (e / (C / 4)) * (C / 4));
+        ex.copy16(sAt + (size_t)j * lda + i4, Aqk + (size_t)j * C + i4);
       }
-      for (int e = tid; e < C * K4; e += nthr) {
-        const int i = e / K4, kk = e - (e / K4) * K4;
-        const bool in = i < L && kk < K;
-        sKg[(size_t)i * ldk + kk] = in ? Kg[(size_t)i * K + kk] : 0.f;
-        if (stage_qw) {
-          sQg[e] = in ? Qg[(size_t)i * K + kk] : 0.f;
-          sW[e] = in ? W[(size_t)i * K + kk] : 0.f;
+      if ((K & 3) == 0) {
+        const int q = K4 / 4;
+        for (int e = tid; e < C * q; e += nthr) {
+          const int i = e / q, k4 = 4 * (e - (e / q) * q);
+          ex.copy16(sKg + (size_t)i * ldk + k4, Kg + (size_t)i * K + k4);
+          if (stage_qw) {
+            ex.copy16(sQg + (size_t)i * K4 + k4, Qg + (size_t)i * K + k4);
+            ex.copy16(sW + (size_t)i * K4 + k4, W + (size_t)i * K + k4);
+          }
         }
+        for (int e = tid; e < q; e += nthr) ex.copy16(sDc + 4 * e, Dc + 4 * e);
+      } else {
+        for (int e = tid; e < C * K4; e += nthr) {
+          const int i = e / K4, kk = e - (e / K4) * K4;
+          const bool in = kk < K;
+          sKg[(size_t)i * ldk + kk] = in ? Kg[(size_t)i * K + kk] : 0.f;
+          if (stage_qw) {
+            sQg[e] = in ? Qg[(size_t)i * K + kk] : 0.f;
+            sW[e] = in ? W[(size_t)i * K + kk] : 0.f;
+          }
+        }
+        for (int kk = tid; kk < K4; kk += nthr) sDc[kk] = kk < K ? Dc[kk] : 0.f;
       }
-      for (int kk = tid; kk < K4; kk += nthr) sDc[kk] = kk < K ? Dc[kk] : 0.f;
+      ex.copy_wait();
     });
     // dV_new = Aqk^T dO + Kg dS': rows i and i + C/2, columns 4 g .. 4 g + 3
     ex.phase([&](int tid, int nthr) {
       for (int u = tid; u < half * (kBV / 4); u += nthr) {
         const int i0 = u / (kBV / 4), g = u - (u / (kBV / 4)) * (kBV / 4), i1 = i0 + half;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (int j = i0; j < L; ++j) {  // At[i][j] is zero for j < i
+        for (int j = i0; j < L; ++j) {  // Aqk[j][i] is zero for j < i
           const F4 d = ld4(sDo + (size_t)j * kBV + 4 * g);
-          const float a0 = sAt[(size_t)i0 * lda + j], a1 = sAt[(size_t)i1 * lda + j];
+          const float a0 = sAt[(size_t)j * lda + i0], a1 = sAt[(size_t)j * lda + i1];
           for (int x = 0; x < 4; ++x) {
             acc[0][x] = fmaf(a0, f4at(d, x), acc[0][x]);
             acc[1][x] = fmaf(a1, f4at(d, x), acc[1][x]);
@@ -730,38 +917,6 @@ KDA_BODY void dstate_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
 // exponent could leave [-inf, 60] (an in-block decay beyond 60 nat on either side of the
 // middle row), in which case the chunk evaluates every e^(Gamma_i - Gamma_j) directly.
 
-// Four consecutive elements off..off+3 of a row (fp32 workspace or an input tensor), zero
-// past `len`; `vec`: the row length is a multiple of 4, so that the four are one aligned
-// 16-byte (fp32) or 8-byte (bf16) load.
-KDA_HD F4 ld4w(const float* row, int off, int len, bool vec) {
-  if (vec) {
-#if defined(__CUDA_ARCH__)
-    const float4 v = __ldg(reinterpret_cast<const float4*>(row + off));
-    return {v.x, v.y, v.z, v.w};
-#else
-    return {row[off], row[off + 1], row[off + 2], row[off + 3]};
-#endif
-  }
-  return {off < len ? row[off] : 0.f, off + 1 < len ? row[off + 1] : 0.f,
-          off + 2 < len ? row[off + 2] : 0.f, off + 3 < len ? row[off + 3] : 0.f};
-}
-KDA_HD F4 ld4i(const void* base, int dtype, size_t row, int off, int len, bool vec) {
-  if (vec) {
-    if (dtype == KDA_F32) return ld4w(static_cast<const float*>(base) + row, off, len, true);
-#if defined(__CUDA_ARCH__)
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + row + off));
-    return {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-            __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
-#endif
-  }
-  return {off < len ? ld_in(base, dtype, row + off) : 0.f,
-          off + 1 < len ? ld_in(base, dtype, row + off + 1) : 0.f,
-          off + 2 < len ? ld_in(base, dtype, row + off + 2) : 0.f,
-          off + 3 < len ? ld_in(base, dtype, row + off + 3) : 0.f};
-}
-KDA_HD float dot4(const F4& a, const F4& b) {
-  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
-}
 
 template <class Exec>
 KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem) {
@@ -797,133 +952,231 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   const float* S = state_ptr(a, p.off_h, c, hv);
   const float* dSp = state_ptr(a, p.off_dh, c, hv);
   const int ldz = C + 1;                      // padded rows: the row-per-thread substitution
+  const int lda = C + 4;                      // rows of the transposed tiles (16-byte aligned)
   float* sAk = smem;                          // [C][C] beta_i P_ij
-  float* sdA = sAk + (size_t)C * C;           // [C][C] dAqk
-  float* sZ = sdA + (size_t)C * C;            // [C][ldz] A^T dA, then A^T dA A^T, then dP
+  float* sdAt = sAk + (size_t)C * C;          // [C][lda] dAqk transposed: sdAt[j][i] = dAqk[i][j]
+  float* sZ = sdAt + (size_t)C * lda;         // [C][ldz] A^T dA, then A^T dA A^T, then dP
   float* sB = sZ + (size_t)C * ldz;           // [C] beta
   float* sDB = sB + C;                        // [C] gradient of beta (the value)
   float* sRed = sDB + C;                      // [kThreads] partial sums of dA_log
   float* sFlag = sRed + kThreads;             // [4] > 0: some block exponent out of range
+  float* sDgc = sFlag + 4;                    // [K4] diagonal of S dS'^T
+  float* sT = sDgc + pad4(K);                 // staging / scratch (grads_scratch floats)
+  float* sXY = sT;                            // [C][(V + K + 1) / 2] back substitution columns
+  float* sZt = sT;                            // [C][lda] dP transposed (the scratch is free then)
+  const int ncol = V + K, half_cols = (ncol + 1) / 2;
   const bool has_alog = a.A_log != nullptr && a.gate_mode != KDA_GATE_PREGATED;
   const float a_exp = has_alog ? expf(a.A_log[hv]) : 1.0f;
-  const int V4 = pad4(V), K4 = pad4(K), CB = C / 4;
+  const int K4 = pad4(K), CB = C / 4;
   const bool vecV = (V & 3) == 0, vecK = (K & 3) == 0;
-  auto vin = [&](int i, int v) { return ld_in(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + v); };
   // rows of the inputs dO and v (only rows < L exist)
   auto in_row = [&](int i) { return ((size_t)(t0 + i) * HV + hv) * V; };
 
-  // beta P, beta; dAqk = (dO V_new^T) masked lower, in 4 x 4 blocks
+  // beta P, beta; the accumulators of the tiled products start at zero
   ex.phase([&](int tid, int nthr) {
     for (int e = tid; e < C * C; e += nthr) {
-      const int i = e / C;
+      const int i = e / C, j = e - (e / C) * C;
       sAk[e] = Be[i] * P[e];
+      sdAt[(size_t)i * lda + j] = 0.f;
     }
     for (int i = tid; i < C; i += nthr) sB[i] = Be[i];
+    for (int kk = tid; kk < K4; kk += nthr) sDgc[kk] = 0.f;
     if (tid == 0) sFlag[0] = 0.f;
-    for (int u = tid; u < CB * CB; u += nthr) {
-      const int ib = u / CB, jb = u - (u / CB) * CB;
-      float acc[4][4] = {};
-      if (jb <= ib && 4 * ib < L) {
-        for (int v = 0; v < V4; v += 4) {
-          F4 o[4], w[4];
-          for (int y = 0; y < 4; ++y) {
-            const int i = 4 * ib + y, j = 4 * jb + y;
-            o[y] = i < L ? ld4i(a.d_o, a.dtype, in_row(i), v, V, vecV) : F4{0.f, 0.f, 0.f, 0.f};
-            w[y] = ld4w(Vn + (size_t)j * V, v, V, vecV);
-          }
-          for (int y = 0; y < 4; ++y)
-            for (int x = 0; x < 4; ++x) acc[y][x] += dot4(o[y], w[x]);
+  });
+  // The products over v in 32-column slices staged in shared memory (16-byte asynchronous
+  // copies where the rows allow them): dAqk = dO V_new^T (into sdAt), dQg = dO S^T,
+  // dW = -dV_new S^T, dKg = V_new dS'^T (partial sums in the dQ, Y, dK slots of the block,
+  // read back and added per slice) and the diagonal of S dS'^T (gamma_C's gradient, sDgc)
+  // 16-column slices; rows are 20 floats (five 16-byte units) apart and a warp's lanes take
+  // consecutive rows, so that the lanes' 16-byte loads fall in distinct banks
+  constexpr int SW = 16, SL = 20;
+  float* sS = sT;                             // [K4][SL] S slice
+  float* sDs = sS + (size_t)K4 * SL;          // [K4][SL] dS' slice
+  float* sDv = sDs + (size_t)K4 * SL;         // [C][SL] dV_new slice
+  float* sVn = sDv + (size_t)C * SL;          // [C][SL] V_new slice
+  float* sDo = sVn + (size_t)C * SL;          // [C][SL] dO slice
+  const int nvt = (V + SW - 1) / SW;
+  for (int t = 0; t < nvt; ++t) {
+    const int v0 = SW * t, w = V - v0 < SW ? V - v0 : SW;
+    const bool async = vecV && w == SW;
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < (2 * K4 + 2 * C) * (SW / 4); e += nthr) {  // 4-column pieces
+        const int row = e / (SW / 4), c4 = 4 * (e - (e / (SW / 4)) * (SW / 4));
+        const float* src;
+        float* dst;
+        if (row < K4) { src = row < K ? S + (size_t)row * V : nullptr; dst = sS + (size_t)row * SL; }
+        else if (row < 2 * K4) {
+          const int k = row - K4;
+          src = k < K ? dSp + (size_t)k * V : nullptr;
+          dst = sDs + (size_t)k * SL;
+        } else if (row < 2 * K4 + C) {
+          const int i = row - 2 * K4;
+          src = dVn + (size_t)i * V;
+          dst = sDv + (size_t)i * SL;
+        } else {
+          const int i = row - 2 * K4 - C;
+          src = Vn + (size_t)i * V;
+          dst = sVn + (size_t)i * SL;
+        }
+        if (src == nullptr) {
+          const float z[4] = {0.f, 0.f, 0.f, 0.f};
+          st4(dst + c4, z);
+        } else if (async) {
+          ex.copy16(dst + c4, src + v0 + c4);
+        } else {
+          const F4 x = ld4w(src, v0 + c4, V, false);
+          const float y[4] = {x.x, x.y, x.z, x.w};
+          st4(dst + c4, y);
         }
       }
-      for (int y = 0; y < 4; ++y)
-        for (int x = 0; x < 4; ++x) {
-          const int i = 4 * ib + y, j = 4 * jb + x;
-          sdA[(size_t)i * C + j] = (i < L && j <= i) ? acc[y][x] : 0.f;
-        }
-    }
-  });
-  // dQg = dO S^T, dW = -dV_new S^T, dKg = V_new dS'^T in 4 x 4 blocks (rows i, channels k),
-  // and their direct terms; e^Gamma K for the A^T dA product
-  ex.phase([&](int tid, int nthr) {
-    for (int u = tid; u < CB * (K4 / 4); u += nthr) {
-      const int ib = u / (K4 / 4), kb = u - (u / (K4 / 4)) * (K4 / 4);
-      float aq[4][4] = {}, aw[4][4] = {}, ak[4][4] = {};
-      if (4 * ib < L) {
-        for (int v = 0; v < V4; v += 4) {
-          F4 o[4], dv[4], vn[4], s[4], ds[4];
+      for (int e = tid; e < C * (SW / 4); e += nthr) {
+        const int i = e / (SW / 4), c4 = 4 * (e - (e / (SW / 4)) * (SW / 4));
+        const F4 x = i < L ? ld4i(a.d_o, a.dtype, in_row(i), v0 + c4, V, async)
+                           : F4{0.f, 0.f, 0.f, 0.f};
+        const float y[4] = {x.x, x.y, x.z, x.w};
+        st4(sDo + (size_t)i * SL + c4, y);
+      }
+      ex.copy_wait();
+    });
+    ex.phase([&](int tid, int nthr) {
+      // unit (ib, kb): rows 4 ib .. 4 ib + 3, channels kb + nkb x (x = 0..3)
+      const int nkb = K4 / 4;
+      for (int u = tid; u < CB * nkb; u += nthr) {
+        const int ib = u / nkb, kb = u - (u / nkb) * nkb;
+        float aq[4][4], aw[4][4], ak[4][4];
+        for (int y = 0; y < 4; ++y)
+          for (int x = 0; x < 4; ++x) {
+            const int i = 4 * ib + y, kk = kb + nkb * x;
+            const bool rd = t > 0 && kk < K;
+            const size_t e = (size_t)i * K + kk;
+            aq[y][x] = rd ? dQ[e] : 0.f;
+            aw[y][x] = rd ? Y[e] : 0.f;
+            ak[y][x] = rd ? dK[e] : 0.f;
+          }
+        for (int c = 0; c < SW; c += 4) {  // dQg and dW (both against S)
+          F4 o[4], dv[4], s[4];
           for (int y = 0; y < 4; ++y) {
-            const int i = 4 * ib + y, kk = 4 * kb + y;
-            o[y] = i < L ? ld4i(a.d_o, a.dtype, in_row(i), v, V, vecV) : F4{0.f, 0.f, 0.f, 0.f};
-            dv[y] = ld4w(dVn + (size_t)i * V, v, V, vecV);
-            vn[y] = ld4w(Vn + (size_t)i * V, v, V, vecV);
-            s[y] = kk < K ? ld4w(S + (size_t)kk * V, v, V, vecV) : F4{0.f, 0.f, 0.f, 0.f};
-            ds[y] = kk < K ? ld4w(dSp + (size_t)kk * V, v, V, vecV) : F4{0.f, 0.f, 0.f, 0.f};
+            o[y] = ld4(sDo + (size_t)(4 * ib + y) * SL + c);
+            dv[y] = ld4(sDv + (size_t)(4 * ib + y) * SL + c);
+            s[y] = ld4(sS + (size_t)(kb + nkb * y) * SL + c);
           }
           for (int y = 0; y < 4; ++y)
             for (int x = 0; x < 4; ++x) {
               aq[y][x] += dot4(o[y], s[x]);
               aw[y][x] -= dot4(dv[y], s[x]);
-              ak[y][x] += dot4(vn[y], ds[x]);
             }
         }
-      }
-      for (int y = 0; y < 4; ++y)
-        for (int x = 0; x < 4; ++x) {
-          const int i = 4 * ib + y, kk = 4 * kb + x;
-          if (kk >= K) continue;
-          const size_t e = (size_t)i * K + kk;
-          float yv = 0.f, dq = 0.f, dk = 0.f, dg = 0.f, dkg_kg = 0.f, ekv = 0.f;
-          if (i < L) {
-            const float gi = Gam[e], eg = expf(gi);
-            yv = aw[y][x];
-            dq = aq[y][x] * eg;
-            dk = ak[y][x] * expf(Gam[(size_t)(L - 1) * K + kk] - gi);
-            dkg_kg = ak[y][x] * Kg[e];
-            dg = aq[y][x] * Qg[e] - dkg_kg;
-            ekv = eg * Kn[e];
+        for (int c = 0; c < SW; c += 4) {  // dKg
+          F4 vn[4], ds[4];
+          for (int y = 0; y < 4; ++y) {
+            vn[y] = ld4(sVn + (size_t)(4 * ib + y) * SL + c);
+            ds[y] = ld4(sDs + (size_t)(kb + nkb * y) * SL + c);
           }
-          Y[e] = yv;
-          dQ[e] = dq;
-          dK[e] = dk;
-          dGam[e] = dg;
-          dKG[e] = dkg_kg;
-          EK[e] = ekv;
+          for (int y = 0; y < 4; ++y)
+            for (int x = 0; x < 4; ++x) ak[y][x] += dot4(vn[y], ds[x]);
         }
-    }
-  });
-  // X = A^T dV_new, Y = A^T dW: back substitution with (I + Diag(beta) P)^T, one thread per
-  // column
-  ex.phase([&](int tid, int nthr) {
-    for (int col = tid; col < V + K; col += nthr) {
-      float* Xc = col < V ? X + col : Y + (col - V);
-      const size_t ld = col < V ? (size_t)V : (size_t)K;
-      if (col < V)
-        for (int i = 0; i < C; ++i) Xc[i * ld] = i < L ? dVn[(size_t)i * V + col] : 0.f;
-      for (int i = L - 2; i >= 0; --i) {
-        float x = Xc[i * ld];
-        for (int j = i + 1; j < L; ++j) x = fmaf(-sAk[(size_t)j * C + i], Xc[j * ld], x);
-        Xc[i * ld] = x;
+        for (int y = 0; y < 4; ++y)
+          for (int x = 0; x < 4; ++x) {
+            const int i = 4 * ib + y, kk = kb + nkb * x;
+            if (kk >= K) continue;
+            const size_t e = (size_t)i * K + kk;
+            dQ[e] = aq[y][x];
+            Y[e] = aw[y][x];
+            dK[e] = ak[y][x];
+          }
       }
+      for (int u = tid; u < CB * CB; u += nthr) {  // dAqk: rows 4 ib .., keys jb + CB x
+        const int ib = u / CB, jb = u - (u / CB) * CB;
+        float acc[4][4];
+        for (int y = 0; y < 4; ++y)
+          for (int x = 0; x < 4; ++x) acc[y][x] = sdAt[(size_t)(jb + CB * x) * lda + 4 * ib + y];
+        for (int c = 0; c < SW; c += 4) {
+          F4 o[4], vn[4];
+          for (int y = 0; y < 4; ++y) {
+            o[y] = ld4(sDo + (size_t)(4 * ib + y) * SL + c);
+            vn[y] = ld4(sVn + (size_t)(jb + CB * y) * SL + c);
+          }
+          for (int y = 0; y < 4; ++y)
+            for (int x = 0; x < 4; ++x) acc[y][x] += dot4(o[y], vn[x]);
+        }
+        for (int y = 0; y < 4; ++y)
+          for (int x = 0; x < 4; ++x) {
+            const int i = 4 * ib + y, j = jb + CB * x;
+            sdAt[(size_t)j * lda + i] = (i < L && j <= i) ? acc[y][x] : 0.f;
+          }
+      }
+      for (int kk = tid; kk < K; kk += nthr) {  // diagonal of S dS'^T
+        float d = 0.f;
+        for (int c = 0; c < SW; c += 4) d += dot4(ld4(sS + (size_t)kk * SL + c), ld4(sDs + (size_t)kk * SL + c));
+        sDgc[kk] += d;
+      }
+    });
+  }
+  // the direct terms of dQg, dW, dKg; e^Gamma K for the A^T dA product
+  ex.phase([&](int tid, int nthr) {
+    KDA_UNROLL4
+    for (int e = tid; e < C * K; e += nthr) {
+      const int i = e / K, kk = e - (e / K) * K;
+      float dq = 0.f, dk = 0.f, dg = 0.f, dkg_kg = 0.f, ekv = 0.f, yv = 0.f;
+      if (i < L) {
+        const float gi = Gam[e], eg = expf(gi), dqg = dQ[e], dkg = dK[e];
+        yv = Y[e];
+        dq = dqg * eg;
+        dk = dkg * expf(Gam[(size_t)(L - 1) * K + kk] - gi);
+        dkg_kg = dkg * Kg[e];
+        dg = dqg * Qg[e] - dkg_kg;
+        ekv = eg * Kn[e];
+      }
+      Y[e] = yv;
+      dQ[e] = dq;
+      dK[e] = dk;
+      dGam[e] = dg;
+      dKG[e] = dkg_kg;
+      EK[e] = ekv;
     }
   });
-  // dv; the WY part of dbeta; the e^Gamma K part of dK and dGamma; A^T dA (strictly lower)
-  // in 4 x 4 blocks
+  // X = A^T dV_new, Y = A^T dW: back substitution with (I + Diag(beta) P)^T on shared-memory
+  // columns, in two halves of the V + K columns (one thread per column, two accumulators so
+  // that the dot products' dependent chains are half as long; the column of beta P is read by
+  // every thread at once)
+  for (int part = 0; part < 2; ++part) {
+    const int cbeg = part == 0 ? 0 : half_cols, cnt = part == 0 ? half_cols : ncol - half_cols;
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < C * cnt; e += nthr) {
+        const int i = e / cnt, col = cbeg + (e - (e / cnt) * cnt);
+        sXY[e] = col < V ? (i < L ? dVn[(size_t)i * V + col] : 0.f) : Y[(size_t)i * K + col - V];
+      }
+    });
+    ex.phase([&](int tid, int nthr) {
+      for (int cl = tid; cl < cnt; cl += nthr) {
+        for (int i = L - 2; i >= 0; --i) {
+          float x0 = sXY[(size_t)i * cnt + cl], x1 = 0.f;
+          int j = i + 1;
+          for (; j + 1 < L; j += 2) {
+            x0 = fmaf(-sAk[(size_t)j * C + i], sXY[(size_t)j * cnt + cl], x0);
+            x1 = fmaf(-sAk[(size_t)(j + 1) * C + i], sXY[(size_t)(j + 1) * cnt + cl], x1);
+          }
+          if (j < L) x0 = fmaf(-sAk[(size_t)j * C + i], sXY[(size_t)j * cnt + cl], x0);
+          sXY[(size_t)i * cnt + cl] = x0 + x1;
+        }
+      }
+    });
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < C * cnt; e += nthr) {
+        const int i = e / cnt, col = cbeg + (e - (e / cnt) * cnt);
+        if (col < V) X[(size_t)i * V + col] = sXY[e];
+        else Y[(size_t)i * K + col - V] = sXY[e];
+      }
+    });
+  }
+  // dv; the e^Gamma K part of dK and dGamma
   ex.phase([&](int tid, int nthr) {
+    KDA_UNROLL4
     for (int e = tid; e < C * V; e += nthr) {
       const int i = e / V, v = e - (e / V) * V;
       if (i < L) a.dv[((size_t)(t0 + i) * HV + hv) * V + v] = sB[i] * X[e];
     }
-    for (int i = tid; i < C; i += nthr) {
-      float db = 0.f;
-      if (i < L) {
-        for (int v = 0; v < V; ++v) db = fmaf(X[(size_t)i * V + v], vin(i, v), db);
-        for (int kk = 0; kk < K; ++kk) {
-          const size_t e = (size_t)i * K + kk;
-          db = fmaf(Y[e], EK[e], db);
-        }
-      }
-      sDB[i] = db;
-    }
+    KDA_UNROLL4
     for (int e = tid; e < C * K; e += nthr) {
       const int i = e / K;
       if (i < L) {
@@ -932,37 +1185,77 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
         dGam[e] += t * EK[e];
       }
     }
-    for (int u = tid; u < CB * CB; u += nthr) {
-      const int ib = u / CB, jb = u - (u / CB) * CB;
-      float acc[4][4] = {};
-      if (jb <= ib && 4 * ib < L) {
-        for (int v = 0; v < V4; v += 4) {
-          F4 xr[4], vr[4];
-          for (int y = 0; y < 4; ++y) {
-            const int i = 4 * ib + y, j = 4 * jb + y;
-            xr[y] = ld4w(X + (size_t)i * V, v, V, vecV);
-            vr[y] = j < L ? ld4i(a.v, a.dtype, in_row(j), v, V, vecV) : F4{0.f, 0.f, 0.f, 0.f};
+  });
+  // A^T dA = X (beta V)^T + Y (beta e^Gamma K)^T over 32-column slices of v, then of k, staged
+  // in shared memory and accumulated in sZ (lower blocks with the diagonal: its entries,
+  // without beta, are the WY part of dbeta)
+  {
+    constexpr int SLZ = 36;             // padded slice rows (see the products above)
+    float* sA = sT;                     // [C][SLZ] X (or Y) slice
+    float* sBt = sA + (size_t)C * SLZ;  // [C][SLZ] v (or e^Gamma K) slice
+    const int ntv = (V + 31) / 32, ntk = (K + 31) / 32;
+    for (int t = 0; t < ntv + ntk; ++t) {
+      const bool onv = t < ntv;
+      const int o0 = 32 * (onv ? t : t - ntv), len = onv ? V : K;
+      const int w = len - o0 < 32 ? len - o0 : 32;
+      const bool async = (onv ? vecV : vecK) && w == 32;
+      ex.phase([&](int tid, int nthr) {
+        for (int e = tid; e < C * 8; e += nthr) {
+          const int i = e >> 3, c4 = 4 * (e & 7);
+          const float* ar = (onv ? X + (size_t)i * V : Y + (size_t)i * K);
+          if (async) {
+            ex.copy16(sA + (size_t)i * SLZ + c4, ar + o0 + c4);
+          } else {
+            const F4 x = ld4w(ar, o0 + c4, len, false);
+            const float y[4] = {x.x, x.y, x.z, x.w};
+            st4(sA + (size_t)i * SLZ + c4, y);
           }
-          for (int y = 0; y < 4; ++y)
-            for (int x = 0; x < 4; ++x) acc[y][x] += dot4(xr[y], vr[x]);
+          F4 bx;
+          if (onv) {
+            bx = i < L ? ld4i(a.v, a.dtype, in_row(i), o0 + c4, V, async) : F4{0.f, 0.f, 0.f, 0.f};
+          } else {
+            bx = ld4w(EK + (size_t)i * K, o0 + c4, K, async);
+          }
+          const float y[4] = {bx.x, bx.y, bx.z, bx.w};
+          st4(sBt + (size_t)i * SLZ + c4, y);
         }
-        for (int kk = 0; kk < K4; kk += 4) {
-          F4 yr[4], er[4];
-          for (int y = 0; y < 4; ++y) {
-            yr[y] = ld4w(Y + (size_t)(4 * ib + y) * K, kk, K, vecK);
-            er[y] = ld4w(EK + (size_t)(4 * jb + y) * K, kk, K, vecK);
+        ex.copy_wait();
+      });
+      ex.phase([&](int tid, int nthr) {
+        for (int u = tid; u < CB * CB; u += nthr) {  // rows 4 ib .., columns jb + CB x
+          const int ib = u / CB, jb = u - (u / CB) * CB;
+          float acc[4][4];
+          for (int y = 0; y < 4; ++y)
+            for (int x = 0; x < 4; ++x)
+              acc[y][x] = t > 0 ? sZ[(size_t)(4 * ib + y) * ldz + jb + CB * x] : 0.f;
+          for (int c = 0; c < 32; c += 4) {
+            F4 xr[4], br[4];
+            for (int y = 0; y < 4; ++y) {
+              xr[y] = ld4(sA + (size_t)(4 * ib + y) * SLZ + c);
+              br[y] = ld4(sBt + (size_t)(jb + CB * y) * SLZ + c);
+            }
+            for (int y = 0; y < 4; ++y)
+              for (int x = 0; x < 4; ++x) acc[y][x] += dot4(xr[y], br[x]);
           }
           for (int y = 0; y < 4; ++y)
-            for (int x = 0; x < 4; ++x) acc[y][x] += dot4(yr[y], er[x]);
+            for (int x = 0; x < 4; ++x) sZ[(size_t)(4 * ib + y) * ldz + jb + CB * x] = acc[y][x];
+        }
+      });
+    }
+    // the diagonal is the WY part of dbeta; A^T dA = beta_j (...) strictly below it
+    ex.phase([&](int tid, int nthr) {
+      for (int e = tid; e < C * C; e += nthr) {
+        const int i = e / C, j = e - (e / C) * C;
+        float* z = sZ + (size_t)i * ldz + j;
+        if (j == i) {
+          sDB[i] = i < L ? *z : 0.f;
+          *z = 0.f;
+        } else {
+          *z = (i < L && j < i) ? sB[j] * *z : 0.f;
         }
       }
-      for (int y = 0; y < 4; ++y)
-        for (int x = 0; x < 4; ++x) {
-          const int i = 4 * ib + y, j = 4 * jb + x;
-          sZ[(size_t)i * ldz + j] = (i < L && j < i) ? sB[j] * acc[y][x] : 0.f;
-        }
-    }
-  });
+    });
+  }
   // dAkk = -(A^T dA A^T) masked strictly lower (row r of A^T dA A^T is A applied to row r of
   // A^T dA: forward substitution, one thread per row); dP = beta dAkk; dbeta += rowsum(dAkk P)
   ex.phase([&](int tid, int nthr) {
@@ -983,8 +1276,12 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     }
   });
   // block references rho (Gamma at each 16-row block's middle row), Q and K scaled by
-  // e^(Gamma - rho), and the range check of every exponent the blocked sums use
+  // e^(Gamma - rho), and the range check of every exponent the blocked sums use; dP transposed
   ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < C * C; e += nthr) {
+      const int i = e / C, j = e - (e / C) * C;
+      sZt[(size_t)j * lda + i] = sZ[(size_t)i * ldz + j];
+    }
     for (int e = tid; e < C * K; e += nthr) {
       const int i = e / K, kk = e - (e / K) * K;
       float qf = 0.f, kf = 0.f;
@@ -1022,20 +1319,26 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
         const int mid = (r0 + 7) < L - 1 ? r0 + 7 : L - 1;
         const float rho = Gam[(size_t)mid * K + kk];
         float s1[16], s2[16];
+KDA_UNROLL
         for (int x = 0; x < 16; ++x) { s1[x] = 0.f; s2[x] = 0.f; }
         const int jend = (r0 + 16 < L ? r0 + 16 : L);
         for (int j = 0; j < jend; ++j) {
           const float ke = Kn[(size_t)j * K + kk] * expf(rho - Gam[(size_t)j * K + kk]);
-          const float* da = sdA + (size_t)r0 * C + j;
-          const float* dz = sZ + (size_t)r0 * ldz + j;
-          for (int x = 0; x < 16; ++x) {  // rows r = r0 + x; sdA, sZ are zero above the diagonal
-            s1[x] = fmaf(da[(size_t)x * C], ke, s1[x]);
-            s2[x] = fmaf(dz[(size_t)x * ldz], ke, s2[x]);
+          const float* da = sdAt + (size_t)j * lda + r0;  // dAqk[r0 ..][j], zero for r < j
+          const float* dz = sZt + (size_t)j * lda + r0;   // dP[r0 ..][j], zero for r <= j
+KDA_UNROLL
+          for (int x = 0; x < 16; x += 4) {
+            const F4 av = ld4(da + x), zv = ld4(dz + x);
+            s1[x] = fmaf(av.x, ke, s1[x]); s1[x + 1] = fmaf(av.y, ke, s1[x + 1]);
+            s1[x + 2] = fmaf(av.z, ke, s1[x + 2]); s1[x + 3] = fmaf(av.w, ke, s1[x + 3]);
+            s2[x] = fmaf(zv.x, ke, s2[x]); s2[x + 1] = fmaf(zv.y, ke, s2[x + 1]);
+            s2[x + 2] = fmaf(zv.z, ke, s2[x + 2]); s2[x + 3] = fmaf(zv.w, ke, s2[x + 3]);
           }
         }
+KDA_UNROLL
         for (int x = 0; x < 16; ++x) {  // the (r, k) elements belong to this unit alone
           const int r = r0 + x;
-          if (r >= L) break;
+          if (r >= L) continue;
           const size_t e = (size_t)r * K + kk;
           const float f = expf(Gam[e] - rho);
           const float a1 = s1[x] * f, a2 = s2[x] * f;
@@ -1044,33 +1347,41 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
           dGam[e] += Qn[e] * a1 + Kn[e] * a2;
         }
         float s3[16], s4[16];
+KDA_UNROLL
         for (int x = 0; x < 16; ++x) { s3[x] = 0.f; s4[x] = 0.f; }
         for (int I = R; I < NB; ++I) {
           const int i0 = 16 * I;
           const int mi = (i0 + 7) < L - 1 ? i0 + 7 : L - 1;
           const float rhoI = Gam[(size_t)mi * K + kk];
           float qf[16], kf[16];
+KDA_UNROLL
           for (int y = 0; y < 16; ++y) {
             const bool in = i0 + y < L;
             qf[y] = in ? QF[(size_t)(i0 + y) * K + kk] : 0.f;
             kf[y] = in ? KF[(size_t)(i0 + y) * K + kk] : 0.f;
           }
+KDA_UNROLL
           for (int x = 0; x < 16; ++x) {
             const int r = r0 + x;
-            if (r >= L) break;
+            if (r >= L) continue;
             float t3 = 0.f, t4 = 0.f;
-            for (int y = 0; y < 16; ++y) {  // sdA[i][r] = 0 for i < r, sZ[i][r] = 0 for i <= r
-              t3 = fmaf(sdA[(size_t)(i0 + y) * C + r], qf[y], t3);
-              t4 = fmaf(sZ[(size_t)(i0 + y) * ldz + r], kf[y], t4);
+            const float* da = sdAt + (size_t)r * lda + i0;  // dAqk[i0 ..][r], zero for i < r
+            const float* dz = sZt + (size_t)r * lda + i0;   // dP[i0 ..][r], zero for i <= r
+KDA_UNROLL
+            for (int y = 0; y < 16; y += 4) {
+              const F4 av = ld4(da + y), zv = ld4(dz + y);
+              t3 = fmaf(av.x, qf[y], fmaf(av.y, qf[y + 1], fmaf(av.z, qf[y + 2], fmaf(av.w, qf[y + 3], t3))));
+              t4 = fmaf(zv.x, kf[y], fmaf(zv.y, kf[y + 1], fmaf(zv.z, kf[y + 2], fmaf(zv.w, kf[y + 3], t4))));
             }
             const float e = expf(rhoI - Gam[(size_t)r * K + kk]);
             s3[x] = fmaf(e, t3, s3[x]);
             s4[x] = fmaf(e, t4, s4[x]);
           }
         }
+KDA_UNROLL
         for (int x = 0; x < 16; ++x) {
           const int r = r0 + x;
-          if (r >= L) break;
+          if (r >= L) continue;
           const size_t e = (size_t)r * K + kk;
           dK[e] += s3[x] + s4[x];
           dGam[e] -= Kn[e] * (s3[x] + s4[x]);
@@ -1088,12 +1399,12 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
         float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
         for (int j = 0; j <= r; ++j) {
           const float kd = Kn[(size_t)j * K + kk] * expf(gr - Gam[(size_t)j * K + kk]);
-          s1 = fmaf(sdA[(size_t)r * C + j], kd, s1);
+          s1 = fmaf(sdAt[(size_t)j * lda + r], kd, s1);
           if (j < r) s2 = fmaf(sZ[(size_t)r * ldz + j], kd, s2);
         }
         for (int i = r; i < L; ++i) {
           const float ed = expf(Gam[(size_t)i * K + kk] - gr);
-          s3 = fmaf(sdA[(size_t)i * C + r], Qn[(size_t)i * K + kk] * ed, s3);
+          s3 = fmaf(sdAt[(size_t)r * lda + i], Qn[(size_t)i * K + kk] * ed, s3);
           if (i > r) s4 = fmaf(sZ[(size_t)i * ldz + r], Kn[(size_t)i * K + kk] * ed, s4);
         }
         dQ[e] += s1;
@@ -1107,11 +1418,7 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   ex.phase([&](int tid, int nthr) {
     float alog_part = 0.f;
     for (int kk = tid; kk < K; kk += nthr) {
-      float dgc = 0.f;
-      const float* sr = S + (size_t)kk * V;
-      const float* dr = dSp + (size_t)kk * V;
-      for (int v = 0; v < V; ++v) dgc = fmaf(sr[v], dr[v], dgc);
-      dgc *= Dc[kk];
+      float dgc = sDgc[kk] * Dc[kk];
       for (int i = 0; i < L; ++i) dgc += dKG[(size_t)i * K + kk];
       const float dt = (a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED)
                            ? a.dt_bias[(size_t)hv * K + kk] : 0.f;
@@ -1137,36 +1444,33 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     }
     sRed[tid] = alog_part;
   });
-  // dA_log; the L2-norm backward of q and k (one thread per row); dbeta
+  // dA_log; the L2-norm backward of q and k: partial sums over four channel segments of every
+  // row, then every element with its row's totals; dbeta
+  float* sNrm = sT;  // [2C][4][2] (sum x^2, sum x * d) per row and segment
+  const int seg = (K + 3) / 4;
   ex.phase([&](int tid, int nthr) {
     if (tid == 0 && a.dA_log != nullptr && has_alog) {
       float s = 0.f;
       for (int t = 0; t < nthr; ++t) s += sRed[t];
       ex.atomic_add(a.dA_log + hv, s);
     }
-    for (int r = tid; r < 2 * C; r += nthr) {
-      const int i = r < C ? r : r - C;
-      if (i >= L) continue;
-      const float* dx = (r < C ? dQ : dK) + (size_t)i * K;
-      const float mul = r < C ? a.scale : 1.f;  // Q = scale * q / |q|
-      const void* src = r < C ? a.q : a.k;
-      float* dst = (r < C ? a.dq : a.dk) + ((size_t)(t0 + i) * H + h) * K;
-      const size_t row = ((size_t)(t0 + i) * H + h) * K;
-      float inv = 1.f, dot = 0.f;
-      if (a.qk_l2norm) {
-        float ss = 0.f;
-        for (int kk = 0; kk < K; ++kk) {
+    for (int u = tid; u < 2 * C * 4; u += nthr) {
+      const int r = u >> 2, sg = u & 3, i = r < C ? r : r - C;
+      float ss = 0.f, sd = 0.f;
+      if (i < L && a.qk_l2norm) {
+        const float* dx = (r < C ? dQ : dK) + (size_t)i * K;
+        const float mul = r < C ? a.scale : 1.f;  // Q = scale * q / |q|
+        const void* src = r < C ? a.q : a.k;
+        const size_t row = ((size_t)(t0 + i) * H + h) * K;
+        const int k1 = (sg + 1) * seg < K ? (sg + 1) * seg : K;
+        for (int kk = sg * seg; kk < k1; ++kk) {
           const float x = ld_in(src, a.dtype, row + kk);
           ss = fmaf(x, x, ss);
+          sd = fmaf(x, mul * dx[kk], sd);
         }
-        inv = 1.0f / sqrtf(ss + kL2Eps);
-        for (int kk = 0; kk < K; ++kk) dot = fmaf(ld_in(src, a.dtype, row + kk) * inv, mul * dx[kk], dot);
       }
-      for (int kk = 0; kk < K; ++kk) {
-        const float d = mul * dx[kk];
-        const float val = a.qk_l2norm ? (d - ld_in(src, a.dtype, row + kk) * inv * dot) * inv : d;
-        if (p.G == 1) dst[kk] = val; else ex.atomic_add(dst + kk, val);
-      }
+      sNrm[2 * u] = ss;
+      sNrm[2 * u + 1] = sd;
     }
     for (int i = tid; i < L; i += nthr) {
       float db = sDB[i];
@@ -1175,6 +1479,27 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
               dsigmoid_f(ld_in(a.beta, a.dtype, (size_t)(t0 + i) * HV + hv));
       }
       a.dbeta[(size_t)(t0 + i) * HV + hv] = db;
+    }
+  });
+  ex.phase([&](int tid, int nthr) {
+    KDA_UNROLL4
+    for (int e = tid; e < 2 * C * K; e += nthr) {
+      const int r = e / K, kk = e - (e / K) * K, i = r < C ? r : r - C;
+      if (i >= L) continue;
+      const float* dx = (r < C ? dQ : dK) + (size_t)i * K;
+      const float mul = r < C ? a.scale : 1.f;
+      const void* src = r < C ? a.q : a.k;
+      float* dst = (r < C ? a.dq : a.dk) + ((size_t)(t0 + i) * H + h) * K;
+      const size_t row = ((size_t)(t0 + i) * H + h) * K;
+      const float d = mul * dx[kk];
+      float val = d;
+      if (a.qk_l2norm) {
+        const float* nr = sNrm + 8 * r;
+        const float ss = (nr[0] + nr[2]) + (nr[4] + nr[6]), sd = (nr[1] + nr[3]) + (nr[5] + nr[7]);
+        const float inv = 1.0f / sqrtf(ss + kL2Eps);
+        val = (d - ld_in(src, a.dtype, row + kk) * inv * (inv * sd)) * inv;
+      }
+      if (p.G == 1) dst[kk] = val; else ex.atomic_add(dst + kk, val);
     }
   });
 }

@@ -42,6 +42,8 @@ struct HostExec {
   }
   void atomic_add(float* p, float x) { *p += x; }
   void flag(unsigned int* s, unsigned int bits) { *s |= bits; }
+  void copy16(float* dst, const float* src) { memcpy(dst, src, 16); }
+  void copy_wait() {}
 };
 
 [[noreturn]] void die(const char* what, const std::string& detail) {
@@ -169,7 +171,8 @@ int main(int argc, char** argv) {
     free(sm);
   };
   for (int64_t c = 0; c < pl.nct; ++c)
-    for (int hv = 0; hv < pl.HV; ++hv) kda::bwd::prep_body(ex, a, c, hv);
+    for (int hv = 0; hv < pl.HV; ++hv)
+      with_smem(kda::bwd::prep_smem(pl), [&](float* sm) { kda::bwd::prep_body(ex, a, c, hv, sm); });
   for (int64_t bid = 0; bid < kda::bwd::state_blocks(pl); ++bid)
     with_smem(kda::bwd::states_smem(pl), [&](float* sm) { kda::bwd::states_body(ex, a, bid, sm); });
   for (int64_t bid = 0; bid < kda::bwd::state_blocks(pl); ++bid)
