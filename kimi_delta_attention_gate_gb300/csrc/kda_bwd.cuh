@@ -191,18 +191,30 @@ inline size_t dstate_smem(const Plan& p) {
 }
 // floats of the gradient stage's staging / scratch region: the back substitution's column
 // half, the 32-column slices of the products, the row-norm partials
+// The gradient stage's product slices: 32 columns of v per slice, rows 36 floats apart.
+constexpr int kGradSliceW = 32, kGradSliceLd = 36;
+// Scratch of the gradient stage once its product slices are done (behind beta P and A^T dA).
 inline size_t grads_scratch(const Plan& p) {
-  const size_t C = (size_t)p.C, K4 = (size_t)((p.K + 3) & ~3);
+  const size_t C = (size_t)p.C;
   size_t s = C * ((p.V + p.K + 1) / 2);
-  s = s > (2 * K4 + 3 * C) * 20 ? s : (2 * K4 + 3 * C) * 20;  // 16-column product slices
   s = s > 2 * C * 36 ? s : 2 * C * 36;                          // 32-column A^T dA slices
-  s = s > 16 * C ? s : 16 * C;
+  const size_t ng = (size_t)((p.K + 3) / 4), l2 = 2 * ng * (2 * C + 1) + 4 * C;
+  s = s > l2 ? s : l2;                                          // L2-norm backward sums
+  s = s > 4 * (size_t)p.K ? s : 4 * (size_t)p.K;                // gate backward half sums
   s = s > C * (C + 4) ? s : C * (C + 4);                        // dP transposed
   return s;
 }
+// The region the product slices are staged in, and that beta P, A^T dA and the scratch take
+// over afterwards.
+inline size_t grads_region(const Plan& p) {
+  const size_t C = (size_t)p.C, K4 = (size_t)((p.K + 3) & ~3);
+  const size_t slices = (2 * K4 + 3 * C) * kGradSliceLd;
+  const size_t after = C * C + C * (C + 1) + grads_scratch(p);
+  return slices > after ? slices : after;
+}
 inline size_t grads_smem(const Plan& p) {
-  return sizeof(float) * ((size_t)p.C * p.C + (size_t)p.C * (p.C + 4) + (size_t)p.C * (p.C + 1) + 2 * (size_t)p.C +
-                          kThreads + 4 + (size_t)((p.K + 3) & ~3) + grads_scratch(p));
+  return sizeof(float) * ((size_t)p.C * (p.C + 4) + 2 * (size_t)p.C + kThreads + 4 +
+                          (size_t)((p.K + 3) & ~3) + grads_region(p));
 }
 
 // ---- element helpers ------------------------------------------------------------------
@@ -223,10 +235,22 @@ KDA_HD float ld_in(const void* base, int dtype, size_t i) {
                           : bits_to_f32((uint32_t) static_cast<const uint16_t*>(base)[i] << 16);
 }
 
+// e^x through the hardware base-2 exponential on the GPU (a few ulp; every backward gradient
+// is checked to 1e-4 relative), the C library's expf on the host
+KDA_HD float fexp(float x) {
+#if defined(__CUDA_ARCH__)
+  return __expf(x);
+#else
+  return expf(x);
+#endif
+}
 KDA_HD float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
-// The sigmoid's derivative s(x) (1 - s(x)), as s(x) s(-x): no cancellation once s(x) rounds
-// to 1 (|x| beyond about 17 in fp32).
-KDA_HD float dsigmoid_f(float x) { return sigmoid_f(x) * sigmoid_f(-x); }
+// The sigmoid's derivative s(x) (1 - s(x)) = t / (1 + t)^2 with t = e^-|x| <= 1: one
+// exponential, and no cancellation once s(x) rounds to 1 (|x| beyond about 17 in fp32).
+KDA_HD float dsigmoid_f(float x) {
+  const float t = fexp(-fabsf(x)), d = 1.0f + t;
+  return t / (d * d);
+}
 // log(1 + e^x); above 20 the correction log1p(e^-x) < 2.1e-9 is below fp32 resolution of x.
 KDA_HD float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
 
@@ -349,6 +373,29 @@ KDA_HD float dot4(const F4& a, const F4& b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }
 
+// Elements e = tid, tid + nthr, ... < n, NB at a time: first every load of the NB elements
+// (ld(e) returns what an element needs), then the rest (st(e, loaded)).  The workspace arrays
+// an element reads and writes are distinct in fact but not provably so, which would keep the
+// compiler from moving one element's loads above the previous element's stores: each element
+// would wait out a full memory latency.  Grouping the loads lets NB of them overlap.
+template <int NB, class Ld, class St>
+KDA_BODY void batched(int tid, int nthr, int n, Ld ld, St st) {
+  using T = decltype(ld(0));
+  for (int e0 = tid; e0 < n; e0 += NB * nthr) {
+    T v[NB];
+    KDA_UNROLL
+    for (int u = 0; u < NB; ++u) {
+      const int e = e0 + u * nthr;
+      v[u] = e < n ? ld(e) : T{};
+    }
+    KDA_UNROLL
+    for (int u = 0; u < NB; ++u) {
+      const int e = e0 + u * nthr;
+      if (e < n) st(e, v[u]);
+    }
+  }
+}
+
 // ---- prep: per (chunk c, value head hv) ------------------------------------------------
 
 template <class Exec>
@@ -381,23 +428,24 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   // gate activation, q and k rows, beta; rows i >= L are zero
   ex.phase([&](int tid, int nthr) {
     if (tid == 0) sFlag[0] = 0.f;
-    KDA_UNROLL4
-    for (int e = tid; e < C * K; e += nthr) {
+    const bool has_dt = a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED;
+    batched<8>(tid, nthr, C * K, [&](int e) {
       const int i = e / K, kk = e - (e / K) * K;
-      float gv = 0.f, qv = 0.f, kv = 0.f;
+      F4 v{0.f, 0.f, 0.f, 0.f};  // raw g, q, k, dt_bias
       if (i < L) {
         const size_t tok = (size_t)(t0 + i);
-        const float dt = (a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED)
-                             ? a.dt_bias[(size_t)hv * K + kk] : 0.f;
-        gv = gate_f(a.gate_mode, ld_in(a.g, a.dtype, (tok * HV + hv) * K + kk), a_exp, dt,
-                    a.lower_bound);
-        qv = ld_in(a.q, a.dtype, (tok * H + h) * K + kk);
-        kv = ld_in(a.k, a.dtype, (tok * H + h) * K + kk);
+        v.x = ld_in(a.g, a.dtype, (tok * HV + hv) * K + kk);
+        v.y = ld_in(a.q, a.dtype, (tok * H + h) * K + kk);
+        v.z = ld_in(a.k, a.dtype, (tok * H + h) * K + kk);
+        v.w = has_dt ? a.dt_bias[(size_t)hv * K + kk] : 0.f;
       }
-      Gam[e] = gv;
-      Qn[e] = qv;
-      Kn[e] = kv;
-    }
+      return v;
+    }, [&](int e, const F4& v) {
+      const bool in = e / K < L;
+      Gam[e] = in ? gate_f(a.gate_mode, v.x, a_exp, v.w, a.lower_bound) : 0.f;
+      Qn[e] = v.y;
+      Kn[e] = v.z;
+    });
     for (int i = tid; i < C; i += nthr) {
       float bv = 0.f;
       if (i < L) {
@@ -412,10 +460,16 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   ex.phase([&](int tid, int nthr) {
     for (int kk = tid; kk < K; kk += nthr) {
       float acc = 0.f;
-      KDA_UNROLL4
-      for (int i = 0; i < L; ++i) {
-        acc += Gam[(size_t)i * K + kk];
-        Gam[(size_t)i * K + kk] = acc;
+      for (int i0 = 0; i0 < L; i0 += 8) {  // eight rows at a time, loads first
+        float g8[8];
+        KDA_UNROLL
+        for (int u = 0; u < 8; ++u) g8[u] = i0 + u < L ? Gam[(size_t)(i0 + u) * K + kk] : 0.f;
+        KDA_UNROLL
+        for (int u = 0; u < 8; ++u) {
+          if (i0 + u >= L) continue;
+          acc += g8[u];
+          Gam[(size_t)(i0 + u) * K + kk] = acc;
+        }
       }
     }
     for (int r = tid; r < 2 * C; r += nthr) {
@@ -435,8 +489,14 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
         mul = 1.0f / sqrtf((ss + ss2) + kL2Eps);
       }
       if (r < C) mul *= a.scale;
-      KDA_UNROLL4
-      for (int kk = 0; kk < K; ++kk) row[kk] *= mul;
+      for (int k0 = 0; k0 < K; k0 += 8) {
+        float x8[8];
+        KDA_UNROLL
+        for (int u = 0; u < 8; ++u) x8[u] = k0 + u < K ? row[k0 + u] : 0.f;
+        KDA_UNROLL
+        for (int u = 0; u < 8; ++u)
+          if (k0 + u < K) row[k0 + u] = x8[u] * mul;
+      }
     }
   });
   // e^gamma_C; Qg, Kg; the right-hand sides of W and U; the block-referenced operands of Aqk
@@ -451,46 +511,59 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   auto mid_row = [&](int B) { return (16 * B + 7) < L - 1 ? 16 * B + 7 : L - 1; };
   ex.phase([&](int tid, int nthr) {
     for (int kk = tid; kk < K; kk += nthr) Dc[kk] = expf(Gam[(size_t)(L - 1) * K + kk]);
-    KDA_UNROLL4
-    for (int e = tid; e < C * K; e += nthr) {
+    struct Row { float gi, gl, gm, q, k, be; };
+    batched<4>(tid, nthr, C * K, [&](int e) {
       const int i = e / K, kk = e - (e / K) * K;
+      Row r{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (i < L)
+        r = Row{Gam[e], Gam[(size_t)(L - 1) * K + kk], Gam[(size_t)mid_row(i >> 4) * K + kk], Qn[e],
+                Kn[e], Be[i]};
+      return r;
+    }, [&](int e, const Row& r) {
       float qg = 0.f, kg = 0.f, w = 0.f, qf = 0.f, kf = 0.f;
-      if (i < L) {
-        const float gi = Gam[e], eg = expf(gi);
-        qg = Qn[e] * eg;
-        kg = Kn[e] * expf(Gam[(size_t)(L - 1) * K + kk] - gi);
-        w = Be[i] * eg * Kn[e];
-        const float rel = gi - Gam[(size_t)mid_row(i >> 4) * K + kk];
+      if (e / K < L) {
+        const float eg = fexp(r.gi);
+        qg = r.q * eg;
+        kg = r.k * fexp(r.gl - r.gi);
+        w = r.be * eg * r.k;
+        const float rel = r.gi - r.gm;
         if (rel > 60.f) ex.atomic_add(sFlag, 1.f);
-        const float f = expf(rel);
-        qf = Qn[e] * f;
-        kf = Kn[e] * f;
+        const float f = fexp(rel);
+        qf = r.q * f;
+        kf = r.k * f;
       }
       Qg[e] = qg;
       Kg[e] = kg;
       W[e] = w;
       QFp[e] = qf;
       KFp[e] = kf;
-    }
-    KDA_UNROLL4
-    for (int e = tid; e < C * V; e += nthr) {
+    });
+    batched<8>(tid, nthr, C * V, [&](int e) {
       const int i = e / V, cc = e - (e / V) * V;
-      U[e] = i < L ? Be[i] * ld_in(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + cc) : 0.f;
-    }
-    KDA_UNROLL4
-    for (int e = tid; e < 8 * NB * (NB + 1) * K; e += nthr) {  // stacked rows of KI
+      return i < L ? Be[i] * ld_in(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + cc) : 0.f;
+    }, [&](int e, float u) { U[e] = u; });
+    // stacked rows of KI; block I's rows start at 8 I (I + 1): 0, 16, 48, 96
+    batched<8>(tid, nthr, 8 * NB * (NB + 1) * K, [&](int e) {
       const int row = e / K, kk = e - (e / K) * K;
-      // block I's rows start at 8 I (I + 1): 0, 16, 48, 96
       const int I = row >= 96 ? 3 : (row >= 48 ? 2 : (row >= 16 ? 1 : 0));
       const int j = row - 8 * I * (I + 1);
-      float v = 0.f;
+      F4 v{0.f, 0.f, 0.f, 0.f};  // Gamma at block I's middle row, Gamma_j, K_j
       if (j < L) {
-        const float ex_ = Gam[(size_t)mid_row(I) * K + kk] - Gam[(size_t)j * K + kk];
-        if (ex_ > 60.f) ex.atomic_add(sFlag, 1.f);
-        v = Kn[(size_t)j * K + kk] * expf(ex_);
+        v.x = Gam[(size_t)mid_row(I) * K + kk];
+        v.y = Gam[(size_t)j * K + kk];
+        v.z = Kn[(size_t)j * K + kk];
+        v.w = 1.f;
       }
-      KIp[e] = v;
-    }
+      return v;
+    }, [&](int e, const F4& v) {
+      float kv = 0.f;
+      if (v.w != 0.f) {
+        const float ex_ = v.x - v.y;
+        if (ex_ > 60.f) ex.atomic_add(sFlag, 1.f);
+        kv = v.z * fexp(ex_);
+      }
+      KIp[e] = kv;
+    });
   });
   const int CB = C / 4;
   const bool vecK = (K & 3) == 0;
@@ -503,6 +576,9 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
         if (jb <= ib && 4 * ib < L) {
           const int I = (4 * ib) >> 4;
           const float* KI = KIp + (size_t)(8 * I * (I + 1)) * K;
+#if defined(__CUDA_ARCH__)
+#pragma unroll 2
+#endif
           for (int kk = 0; kk < pad4(K); kk += 4) {
             F4 qf[4], kf[4], kj[4];
             for (int y = 0; y < 4; ++y) {
@@ -555,21 +631,26 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   float* sX = sP + (size_t)C * C;     // [C][K + V] the right-hand sides, then the solutions
   const int ncol = K + V;
   ex.phase([&](int tid, int nthr) {
-    KDA_UNROLL4
-    for (int e = tid; e < C * C; e += nthr) sP[e] = Be[e / C] * P[e];
-    KDA_UNROLL4
-    for (int e = tid; e < C * ncol; e += nthr) {
+    batched<8>(tid, nthr, C * C, [&](int e) { return Be[e / C] * P[e]; }, [&](int e, float v) { sP[e] = v; });
+    batched<8>(tid, nthr, C * ncol, [&](int e) {
       const int i = e / ncol, col = e - (e / ncol) * ncol;
-      sX[e] = col < K ? W[(size_t)i * K + col] : U[(size_t)i * V + col - K];
-    }
+      return col < K ? W[(size_t)i * K + col] : U[(size_t)i * V + col - K];
+    }, [&](int e, float v) { sX[e] = v; });
   });
   ex.phase([&](int tid, int nthr) {
     for (int col = tid; col < ncol; col += nthr) {
       for (int i = 1; i < L; ++i) {
-        float x = sX[(size_t)i * ncol + col];
         const float* pr = sP + (size_t)i * C;
-        for (int j = 0; j < i; ++j) x = fmaf(-pr[j], sX[(size_t)j * ncol + col], x);
-        sX[(size_t)i * ncol + col] = x;
+        float x0 = sX[(size_t)i * ncol + col], x1 = 0.f, x2 = 0.f, x3 = 0.f;
+        int j = 0;
+        for (; j + 3 < i; j += 4) {
+          x0 = fmaf(-pr[j], sX[(size_t)j * ncol + col], x0);
+          x1 = fmaf(-pr[j + 1], sX[(size_t)(j + 1) * ncol + col], x1);
+          x2 = fmaf(-pr[j + 2], sX[(size_t)(j + 2) * ncol + col], x2);
+          x3 = fmaf(-pr[j + 3], sX[(size_t)(j + 3) * ncol + col], x3);
+        }
+        for (; j < i; ++j) x0 = fmaf(-pr[j], sX[(size_t)j * ncol + col], x0);
+        sX[(size_t)i * ncol + col] = (x0 + x1) + (x2 + x3);
       }
     }
   });
@@ -953,15 +1034,16 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   const float* dSp = state_ptr(a, p.off_dh, c, hv);
   const int ldz = C + 1;                      // padded rows: the row-per-thread substitution
   const int lda = C + 4;                      // rows of the transposed tiles (16-byte aligned)
-  float* sAk = smem;                          // [C][C] beta_i P_ij
-  float* sdAt = sAk + (size_t)C * C;          // [C][lda] dAqk transposed: sdAt[j][i] = dAqk[i][j]
-  float* sZ = sdAt + (size_t)C * lda;         // [C][ldz] A^T dA, then A^T dA A^T, then dP
-  float* sB = sZ + (size_t)C * ldz;           // [C] beta
+  float* sdAt = smem;                         // [C][lda] dAqk transposed: sdAt[j][i] = dAqk[i][j]
+  float* sB = sdAt + (size_t)C * lda;         // [C] beta
   float* sDB = sB + C;                        // [C] gradient of beta (the value)
   float* sRed = sDB + C;                      // [kThreads] partial sums of dA_log
   float* sFlag = sRed + kThreads;             // [4] > 0: some block exponent out of range
   float* sDgc = sFlag + 4;                    // [K4] diagonal of S dS'^T
-  float* sT = sDgc + pad4(K);                 // staging / scratch (grads_scratch floats)
+  float* sRg = sDgc + pad4(K);                // the product slices' staging, then:
+  float* sAk = sRg;                           // [C][C] beta_i P_ij
+  float* sZ = sAk + (size_t)C * C;            // [C][ldz] A^T dA, then A^T dA A^T, then dP
+  float* sT = sZ + (size_t)C * ldz;           // scratch (grads_scratch floats)
   float* sXY = sT;                            // [C][(V + K + 1) / 2] back substitution columns
   float* sZt = sT;                            // [C][lda] dP transposed (the scratch is free then)
   const int ncol = V + K, half_cols = (ncol + 1) / 2;
@@ -972,13 +1054,9 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   // rows of the inputs dO and v (only rows < L exist)
   auto in_row = [&](int i) { return ((size_t)(t0 + i) * HV + hv) * V; };
 
-  // beta P, beta; the accumulators of the tiled products start at zero
+  // beta; the accumulators of the tiled products start at zero
   ex.phase([&](int tid, int nthr) {
-    for (int e = tid; e < C * C; e += nthr) {
-      const int i = e / C, j = e - (e / C) * C;
-      sAk[e] = Be[i] * P[e];
-      sdAt[(size_t)i * lda + j] = 0.f;
-    }
+    for (int e = tid; e < C * lda; e += nthr) sdAt[e] = 0.f;
     for (int i = tid; i < C; i += nthr) sB[i] = Be[i];
     for (int kk = tid; kk < K4; kk += nthr) sDgc[kk] = 0.f;
     if (tid == 0) sFlag[0] = 0.f;
@@ -986,11 +1064,11 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   // The products over v in 32-column slices staged in shared memory (16-byte asynchronous
   // copies where the rows allow them): dAqk = dO V_new^T (into sdAt), dQg = dO S^T,
   // dW = -dV_new S^T, dKg = V_new dS'^T (partial sums in the dQ, Y, dK slots of the block,
-  // read back and added per slice) and the diagonal of S dS'^T (gamma_C's gradient, sDgc)
-  // 16-column slices; rows are 20 floats (five 16-byte units) apart and a warp's lanes take
-  // consecutive rows, so that the lanes' 16-byte loads fall in distinct banks
-  constexpr int SW = 16, SL = 20;
-  float* sS = sT;                             // [K4][SL] S slice
+  // read back and added per slice) and the diagonal of S dS'^T (gamma_C's gradient, sDgc).
+  // Rows are 36 floats (nine 16-byte units) apart and a warp's lanes take consecutive rows, so
+  // that the lanes' 16-byte loads fall in distinct banks.
+  constexpr int SW = kGradSliceW, SL = kGradSliceLd;
+  float* sS = sRg;                            // [K4][SL] S slice
   float* sDs = sS + (size_t)K4 * SL;          // [K4][SL] dS' slice
   float* sDv = sDs + (size_t)K4 * SL;         // [C][SL] dV_new slice
   float* sVn = sDv + (size_t)C * SL;          // [C][SL] V_new slice
@@ -1113,27 +1191,32 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     });
   }
   // the direct terms of dQg, dW, dKg; e^Gamma K for the A^T dA product
+  struct Direct { float gi, gl, dqg, dkg, y, kg, qg, kn; };
   ex.phase([&](int tid, int nthr) {
-    KDA_UNROLL4
-    for (int e = tid; e < C * K; e += nthr) {
+    batched<8>(tid, nthr, C * C, [&](int e) { return Be[e / C] * P[e]; }, [&](int e, float v) { sAk[e] = v; });
+    batched<4>(tid, nthr, C * K, [&](int e) {
       const int i = e / K, kk = e - (e / K) * K;
-      float dq = 0.f, dk = 0.f, dg = 0.f, dkg_kg = 0.f, ekv = 0.f, yv = 0.f;
-      if (i < L) {
-        const float gi = Gam[e], eg = expf(gi), dqg = dQ[e], dkg = dK[e];
-        yv = Y[e];
-        dq = dqg * eg;
-        dk = dkg * expf(Gam[(size_t)(L - 1) * K + kk] - gi);
-        dkg_kg = dkg * Kg[e];
-        dg = dqg * Qg[e] - dkg_kg;
-        ekv = eg * Kn[e];
+      Direct d{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (i < L)
+        d = Direct{Gam[e], Gam[(size_t)(L - 1) * K + kk], dQ[e], dK[e], Y[e], Kg[e], Qg[e], Kn[e]};
+      return d;
+    }, [&](int e, const Direct& d) {
+      float dq = 0.f, dk = 0.f, dg = 0.f, dkg_kg = 0.f, ekv = 0.f;
+      if (e / K < L) {
+        const float eg = fexp(d.gi);
+        dq = d.dqg * eg;
+        dk = d.dkg * fexp(d.gl - d.gi);
+        dkg_kg = d.dkg * d.kg;
+        dg = d.dqg * d.qg - dkg_kg;
+        ekv = eg * d.kn;
       }
-      Y[e] = yv;
+      Y[e] = d.y;
       dQ[e] = dq;
       dK[e] = dk;
       dGam[e] = dg;
       dKG[e] = dkg_kg;
       EK[e] = ekv;
-    }
+    });
   });
   // X = A^T dV_new, Y = A^T dW: back substitution with (I + Diag(beta) P)^T on shared-memory
   // columns, in two halves of the V + K columns (one thread per column, two accumulators so
@@ -1142,22 +1225,24 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   for (int part = 0; part < 2; ++part) {
     const int cbeg = part == 0 ? 0 : half_cols, cnt = part == 0 ? half_cols : ncol - half_cols;
     ex.phase([&](int tid, int nthr) {
-      for (int e = tid; e < C * cnt; e += nthr) {
+      batched<8>(tid, nthr, C * cnt, [&](int e) {
         const int i = e / cnt, col = cbeg + (e - (e / cnt) * cnt);
-        sXY[e] = col < V ? (i < L ? dVn[(size_t)i * V + col] : 0.f) : Y[(size_t)i * K + col - V];
-      }
+        return col < V ? (i < L ? dVn[(size_t)i * V + col] : 0.f) : Y[(size_t)i * K + col - V];
+      }, [&](int e, float v) { sXY[e] = v; });
     });
     ex.phase([&](int tid, int nthr) {
       for (int cl = tid; cl < cnt; cl += nthr) {
         for (int i = L - 2; i >= 0; --i) {
-          float x0 = sXY[(size_t)i * cnt + cl], x1 = 0.f;
+          float x0 = sXY[(size_t)i * cnt + cl], x1 = 0.f, x2 = 0.f, x3 = 0.f;
           int j = i + 1;
-          for (; j + 1 < L; j += 2) {
+          for (; j + 3 < L; j += 4) {
             x0 = fmaf(-sAk[(size_t)j * C + i], sXY[(size_t)j * cnt + cl], x0);
             x1 = fmaf(-sAk[(size_t)(j + 1) * C + i], sXY[(size_t)(j + 1) * cnt + cl], x1);
+            x2 = fmaf(-sAk[(size_t)(j + 2) * C + i], sXY[(size_t)(j + 2) * cnt + cl], x2);
+            x3 = fmaf(-sAk[(size_t)(j + 3) * C + i], sXY[(size_t)(j + 3) * cnt + cl], x3);
           }
-          if (j < L) x0 = fmaf(-sAk[(size_t)j * C + i], sXY[(size_t)j * cnt + cl], x0);
-          sXY[(size_t)i * cnt + cl] = x0 + x1;
+          for (; j < L; ++j) x0 = fmaf(-sAk[(size_t)j * C + i], sXY[(size_t)j * cnt + cl], x0);
+          sXY[(size_t)i * cnt + cl] = (x0 + x1) + (x2 + x3);
         }
       }
     });
@@ -1170,21 +1255,18 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     });
   }
   // dv; the e^Gamma K part of dK and dGamma
+  struct DK { float y, g, dk, ek, dg; };
   ex.phase([&](int tid, int nthr) {
-    KDA_UNROLL4
-    for (int e = tid; e < C * V; e += nthr) {
+    batched<8>(tid, nthr, L * V, [&](int e) { return X[e]; }, [&](int e, float x) {
       const int i = e / V, v = e - (e / V) * V;
-      if (i < L) a.dv[((size_t)(t0 + i) * HV + hv) * V + v] = sB[i] * X[e];
-    }
-    KDA_UNROLL4
-    for (int e = tid; e < C * K; e += nthr) {
-      const int i = e / K;
-      if (i < L) {
-        const float t = sB[i] * Y[e];
-        dK[e] += t * expf(Gam[e]);
-        dGam[e] += t * EK[e];
-      }
-    }
+      a.dv[((size_t)(t0 + i) * HV + hv) * V + v] = sB[i] * x;
+    });
+    batched<4>(tid, nthr, L * K, [&](int e) { return DK{Y[e], Gam[e], dK[e], EK[e], dGam[e]}; },
+               [&](int e, const DK& d) {
+      const float t = sB[e / K] * d.y;
+      dK[e] = d.dk + t * fexp(d.g);
+      dGam[e] = d.dg + t * d.ek;
+    });
   });
   // A^T dA = X (beta V)^T + Y (beta e^Gamma K)^T over 32-column slices of v, then of k, staged
   // in shared memory and accumulated in sZ (lower blocks with the diagonal: its entries,
@@ -1262,9 +1344,17 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     for (int r = tid; r < L; r += nthr) {
       float* z = sZ + (size_t)r * ldz;
       for (int i = 1; i < r; ++i) {
-        float x = z[i];
-        for (int j = 0; j < i; ++j) x = fmaf(-sAk[(size_t)i * C + j], z[j], x);
-        z[i] = x;
+        const float* ar = sAk + (size_t)i * C;
+        float x0 = z[i], x1 = 0.f, x2 = 0.f, x3 = 0.f;
+        int j = 0;
+        for (; j + 3 < i; j += 4) {
+          x0 = fmaf(-ar[j], z[j], x0);
+          x1 = fmaf(-ar[j + 1], z[j + 1], x1);
+          x2 = fmaf(-ar[j + 2], z[j + 2], x2);
+          x3 = fmaf(-ar[j + 3], z[j + 3], x3);
+        }
+        for (; j < i; ++j) x0 = fmaf(-ar[j], z[j], x0);
+        z[i] = (x0 + x1) + (x2 + x3);
       }
       float db = 0.f;
       for (int i = 0; i < r; ++i) {
@@ -1282,27 +1372,45 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
       const int i = e / C, j = e - (e / C) * C;
       sZt[(size_t)j * lda + i] = sZ[(size_t)i * ldz + j];
     }
-    for (int e = tid; e < C * K; e += nthr) {
+    // Gamma at the middle rows of the (at most four) blocks, row i's own Gamma, q and k
+    struct Ref { float gm[4], gi, qn, kn; };
+    const int NBk = (L + 15) >> 4;
+    batched<4>(tid, nthr, C * K, [&](int e) {
       const int i = e / K, kk = e - (e / K) * K;
+      Ref r{{0.f, 0.f, 0.f, 0.f}, 0.f, 0.f, 0.f};
+      if (i < L) {
+        KDA_UNROLL
+        for (int R = 0; R < 4; ++R) {
+          const int mr = (16 * R + 7) < L - 1 ? 16 * R + 7 : L - 1;
+          if (R < NBk) r.gm[R] = Gam[(size_t)mr * K + kk];
+        }
+        r.gi = Gam[e];
+        r.qn = Qn[e];
+        r.kn = Kn[e];
+      }
+      return r;
+    }, [&](int e, const Ref& r) {
+      const int i = e / K;
       float qf = 0.f, kf = 0.f;
       if (i < L) {
         const int B = i >> 4;
-        const int mid = (16 * B + 7) < L - 1 ? 16 * B + 7 : L - 1;
-        const float gi = Gam[e], rho = Gam[(size_t)mid * K + kk];
-        bool bad = gi - rho > 60.f;
+        float rho = r.gm[0];
+        bool bad = false;
         // rho_R - Gamma_i for every block R whose rows see row i (R >= B)
-        for (int R = B; 16 * R < L; ++R) {
-          const int mr = (16 * R + 7) < L - 1 ? 16 * R + 7 : L - 1;
-          bad = bad || Gam[(size_t)mr * K + kk] - gi > 60.f;
+        KDA_UNROLL
+        for (int R = 0; R < 4; ++R) {
+          if (R == B) rho = r.gm[R];
+          if (R >= B && R < NBk) bad = bad || r.gm[R] - r.gi > 60.f;
         }
+        bad = bad || r.gi - rho > 60.f;
         if (bad) ex.atomic_add(sFlag, 1.f);
-        const float f = expf(gi - rho);
-        qf = Qn[e] * f;
-        kf = Kn[e] * f;
+        const float f = fexp(r.gi - rho);
+        qf = r.qn * f;
+        kf = r.kn * f;
       }
       QF[e] = qf;
       KF[e] = kf;
-    }
+    });
   });
   if (sFlag[0] == 0.f) {
     // the e^(Gamma_i - Gamma_j) terms of Aqk and P, one thread per (16-row block R, channel
@@ -1322,8 +1430,9 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
 KDA_UNROLL
         for (int x = 0; x < 16; ++x) { s1[x] = 0.f; s2[x] = 0.f; }
         const int jend = (r0 + 16 < L ? r0 + 16 : L);
+        KDA_UNROLL4
         for (int j = 0; j < jend; ++j) {
-          const float ke = Kn[(size_t)j * K + kk] * expf(rho - Gam[(size_t)j * K + kk]);
+          const float ke = Kn[(size_t)j * K + kk] * fexp(rho - Gam[(size_t)j * K + kk]);
           const float* da = sdAt + (size_t)j * lda + r0;  // dAqk[r0 ..][j], zero for r < j
           const float* dz = sZt + (size_t)j * lda + r0;   // dP[r0 ..][j], zero for r <= j
 KDA_UNROLL
@@ -1335,16 +1444,31 @@ KDA_UNROLL
             s2[x + 2] = fmaf(zv.z, ke, s2[x + 2]); s2[x + 3] = fmaf(zv.w, ke, s2[x + 3]);
           }
         }
+        // Gamma of the block's rows (also the exponents of the second part)
+        float gr[16];
 KDA_UNROLL
-        for (int x = 0; x < 16; ++x) {  // the (r, k) elements belong to this unit alone
-          const int r = r0 + x;
-          if (r >= L) continue;
-          const size_t e = (size_t)r * K + kk;
-          const float f = expf(Gam[e] - rho);
-          const float a1 = s1[x] * f, a2 = s2[x] * f;
-          dQ[e] += a1;
-          dK[e] += a2;
-          dGam[e] += Qn[e] * a1 + Kn[e] * a2;
+        for (int x = 0; x < 16; ++x) gr[x] = r0 + x < L ? Gam[(size_t)(r0 + x) * K + kk] : 0.f;
+        // the (r, k) elements belong to this unit alone; four rows at a time, loads first
+KDA_UNROLL
+        for (int x0 = 0; x0 < 16; x0 += 4) {
+          float q8[4], k8[4], dq8[4], dk8[4], dg8[4];
+KDA_UNROLL
+          for (int x = 0; x < 4; ++x) {
+            const int r = r0 + x0 + x;
+            const size_t e = (size_t)(r < L ? r : 0) * K + kk;
+            q8[x] = Qn[e]; k8[x] = Kn[e]; dq8[x] = dQ[e]; dk8[x] = dK[e]; dg8[x] = dGam[e];
+          }
+KDA_UNROLL
+          for (int x = 0; x < 4; ++x) {
+            const int r = r0 + x0 + x;
+            if (r >= L) continue;
+            const size_t e = (size_t)r * K + kk;
+            const float f = fexp(gr[x0 + x] - rho);
+            const float a1 = s1[x0 + x] * f, a2 = s2[x0 + x] * f;
+            dQ[e] = dq8[x] + a1;
+            dK[e] = dk8[x] + a2;
+            dGam[e] = dg8[x] + (q8[x] * a1 + k8[x] * a2);
+          }
         }
         float s3[16], s4[16];
 KDA_UNROLL
@@ -1373,18 +1497,29 @@ KDA_UNROLL
               t3 = fmaf(av.x, qf[y], fmaf(av.y, qf[y + 1], fmaf(av.z, qf[y + 2], fmaf(av.w, qf[y + 3], t3))));
               t4 = fmaf(zv.x, kf[y], fmaf(zv.y, kf[y + 1], fmaf(zv.z, kf[y + 2], fmaf(zv.w, kf[y + 3], t4))));
             }
-            const float e = expf(rhoI - Gam[(size_t)r * K + kk]);
+            const float e = fexp(rhoI - gr[x]);
             s3[x] = fmaf(e, t3, s3[x]);
             s4[x] = fmaf(e, t4, s4[x]);
           }
         }
 KDA_UNROLL
-        for (int x = 0; x < 16; ++x) {
-          const int r = r0 + x;
-          if (r >= L) continue;
-          const size_t e = (size_t)r * K + kk;
-          dK[e] += s3[x] + s4[x];
-          dGam[e] -= Kn[e] * (s3[x] + s4[x]);
+        for (int x0 = 0; x0 < 16; x0 += 8) {
+          float k8[8], dk8[8], dg8[8];
+KDA_UNROLL
+          for (int x = 0; x < 8; ++x) {
+            const int r = r0 + x0 + x;
+            const size_t e = (size_t)(r < L ? r : 0) * K + kk;
+            k8[x] = Kn[e]; dk8[x] = dK[e]; dg8[x] = dGam[e];
+          }
+KDA_UNROLL
+          for (int x = 0; x < 8; ++x) {
+            const int r = r0 + x0 + x;
+            if (r >= L) continue;
+            const size_t e = (size_t)r * K + kk;
+            const float s34 = s3[x0 + x] + s4[x0 + x];
+            dK[e] = dk8[x] + s34;
+            dGam[e] = dg8[x] - k8[x] * s34;
+          }
         }
       }
     });
@@ -1414,63 +1549,98 @@ KDA_UNROLL
     });
   }
   // reverse cumsum of dGamma (plus the gamma_C terms on the last row) and the gate backward,
-  // one thread per channel
+  // with each channel's rows in two halves: first every half's sums of dGamma and of the
+  // gamma_C terms, then each half's reverse cumsum from the total of the rows above it
+  const int hrows = (L + 1) / 2;
+  float* sHalf = sT;          // [2][K] sum of dGamma over the half's rows
+  float* sKgh = sT + 2 * K;   // [2][K] sum of the gamma_C terms over the half's rows
   ex.phase([&](int tid, int nthr) {
+    for (int u = tid; u < 2 * K; u += nthr) {
+      const int hf = u / K, kk = u - (u / K) * K;
+      const int i0 = hf * hrows, i1 = hf == 0 ? hrows : L;
+      float sg = 0.f, sk = 0.f;
+      KDA_UNROLL4
+      for (int i = i0; i < i1; ++i) {
+        sg += dGam[(size_t)i * K + kk];
+        sk += dKG[(size_t)i * K + kk];
+      }
+      sHalf[u] = sg;
+      sKgh[u] = sk;
+    }
+  });
+  ex.phase([&](int tid, int nthr) {
+    const bool gated = a.gate_mode == KDA_GATE_PLAIN || a.gate_mode == KDA_GATE_SAFE;
     float alog_part = 0.f;
-    for (int kk = tid; kk < K; kk += nthr) {
-      float dgc = sDgc[kk] * Dc[kk];
-      for (int i = 0; i < L; ++i) dgc += dKG[(size_t)i * K + kk];
+    for (int u = tid; u < 2 * K; u += nthr) {
+      const int hf = u / K, kk = u - (u / K) * K;
+      const int i0 = hf * hrows, i1 = hf == 0 ? hrows : L;
+      if (i1 <= i0) continue;
+      const float dgc = sDgc[kk] * Dc[kk] + (sKgh[kk] + sKgh[K + kk]);
       const float dt = (a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED)
                            ? a.dt_bias[(size_t)hv * K + kk] : 0.f;
-      float run = dgc, dt_part = 0.f;
-      for (int i = L - 1; i >= 0; --i) {
-        run += dGam[(size_t)i * K + kk];
-        const size_t gi = ((size_t)(t0 + i) * HV + hv) * K + kk;
-        float dx = run;
-        if (a.gate_mode == KDA_GATE_PLAIN) {
-          const float x = ld_in(a.g, a.dtype, gi) + dt;
-          dx = run * (-a_exp) * sigmoid_f(x);
-          alog_part = fmaf(run * (-a_exp), softplus_f(x), alog_part);
-        } else if (a.gate_mode == KDA_GATE_SAFE) {
-          const float x = ld_in(a.g, a.dtype, gi) + dt;
-          const float ds = run * a.lower_bound * dsigmoid_f(a_exp * x);
-          dx = ds * a_exp;
-          alog_part = fmaf(ds * a_exp, x, alog_part);
+      float run = hf == 0 ? dgc + sHalf[K + kk] : dgc, dt_part = 0.f;
+      for (int ie = i1 - 1; ie >= i0; ie -= 8) {  // eight rows at a time, loads first
+        float dgm[8], gx[8];
+        KDA_UNROLL
+        for (int x = 0; x < 8; ++x) {
+          const int i = ie - x;
+          dgm[x] = i >= i0 ? dGam[(size_t)i * K + kk] : 0.f;
+          gx[x] = (i >= i0 && gated) ? ld_in(a.g, a.dtype, ((size_t)(t0 + i) * HV + hv) * K + kk) : 0.f;
         }
-        a.dg[gi] = dx;
-        dt_part += dx;
+        KDA_UNROLL
+        for (int x = 0; x < 8; ++x) {
+          const int i = ie - x;
+          if (i < i0) continue;
+          run += dgm[x];
+          float dx = run;
+          if (a.gate_mode == KDA_GATE_PLAIN) {
+            const float xx = gx[x] + dt;
+            dx = run * (-a_exp) * sigmoid_f(xx);
+            alog_part = fmaf(run * (-a_exp), softplus_f(xx), alog_part);
+          } else if (a.gate_mode == KDA_GATE_SAFE) {
+            const float xx = gx[x] + dt;
+            const float ds = run * a.lower_bound * dsigmoid_f(a_exp * xx);
+            dx = ds * a_exp;
+            alog_part = fmaf(ds * a_exp, xx, alog_part);
+          }
+          a.dg[((size_t)(t0 + i) * HV + hv) * K + kk] = dx;
+          dt_part += dx;
+        }
       }
       if (a.ddt_bias != nullptr) ex.atomic_add(a.ddt_bias + (size_t)hv * K + kk, dt_part);
     }
     sRed[tid] = alog_part;
   });
-  // dA_log; the L2-norm backward of q and k: partial sums over four channel segments of every
-  // row, then every element with its row's totals; dbeta
-  float* sNrm = sT;  // [2C][4][2] (sum x^2, sum x * d) per row and segment
-  const int seg = (K + 3) / 4;
+  // dA_log; dbeta; the L2-norm backward of q and k: sums (x^2, x d) over four-channel pieces
+  // of every row, then per row, then every element with its row's factors
+  const int ng = (K + 3) / 4, ldp = 2 * C + 1;  // padded: both access orders conflict-free
+  float* sSS = sT;                              // [ng][ldp] sum x^2 of a piece
+  float* sSD = sSS + (size_t)ng * ldp;          // [ng][ldp] sum x d of a piece
+  float* sRowF = sSD + (size_t)ng * ldp;        // [2C][2]: 1 / |x|, sum x d / |x|
+  struct XD { F4 x, d; };
+  // piece u: row r (the q rows, then the k rows), channels 4 (u % ng) ..
+  auto load_piece = [&](int u) {
+    const int r = u / ng, c4 = 4 * (u - (u / ng) * ng), i = r < C ? r : r - C;
+    XD v{{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (i < L) {
+      v.d = ld4w((r < C ? dQ : dK) + (size_t)i * K, c4, K, vecK);
+      if (a.qk_l2norm) v.x = ld4i(r < C ? a.q : a.k, a.dtype, ((size_t)(t0 + i) * H + h) * K, c4, K, vecK);
+    }
+    return v;
+  };
   ex.phase([&](int tid, int nthr) {
     if (tid == 0 && a.dA_log != nullptr && has_alog) {
       float s = 0.f;
       for (int t = 0; t < nthr; ++t) s += sRed[t];
       ex.atomic_add(a.dA_log + hv, s);
     }
-    for (int u = tid; u < 2 * C * 4; u += nthr) {
-      const int r = u >> 2, sg = u & 3, i = r < C ? r : r - C;
-      float ss = 0.f, sd = 0.f;
-      if (i < L && a.qk_l2norm) {
-        const float* dx = (r < C ? dQ : dK) + (size_t)i * K;
+    if (a.qk_l2norm) {
+      batched<4>(tid, nthr, 2 * C * ng, load_piece, [&](int u, const XD& v) {
+        const int r = u / ng, g = u - (u / ng) * ng;
         const float mul = r < C ? a.scale : 1.f;  // Q = scale * q / |q|
-        const void* src = r < C ? a.q : a.k;
-        const size_t row = ((size_t)(t0 + i) * H + h) * K;
-        const int k1 = (sg + 1) * seg < K ? (sg + 1) * seg : K;
-        for (int kk = sg * seg; kk < k1; ++kk) {
-          const float x = ld_in(src, a.dtype, row + kk);
-          ss = fmaf(x, x, ss);
-          sd = fmaf(x, mul * dx[kk], sd);
-        }
-      }
-      sNrm[2 * u] = ss;
-      sNrm[2 * u + 1] = sd;
+        sSS[(size_t)g * ldp + r] = dot4(v.x, v.x);
+        sSD[(size_t)g * ldp + r] = dot4(v.x, F4{mul * v.d.x, mul * v.d.y, mul * v.d.z, mul * v.d.w});
+      });
     }
     for (int i = tid; i < L; i += nthr) {
       float db = sDB[i];
@@ -1481,26 +1651,35 @@ KDA_UNROLL
       a.dbeta[(size_t)(t0 + i) * HV + hv] = db;
     }
   });
-  ex.phase([&](int tid, int nthr) {
-    KDA_UNROLL4
-    for (int e = tid; e < 2 * C * K; e += nthr) {
-      const int r = e / K, kk = e - (e / K) * K, i = r < C ? r : r - C;
-      if (i >= L) continue;
-      const float* dx = (r < C ? dQ : dK) + (size_t)i * K;
-      const float mul = r < C ? a.scale : 1.f;
-      const void* src = r < C ? a.q : a.k;
-      float* dst = (r < C ? a.dq : a.dk) + ((size_t)(t0 + i) * H + h) * K;
-      const size_t row = ((size_t)(t0 + i) * H + h) * K;
-      const float d = mul * dx[kk];
-      float val = d;
-      if (a.qk_l2norm) {
-        const float* nr = sNrm + 8 * r;
-        const float ss = (nr[0] + nr[2]) + (nr[4] + nr[6]), sd = (nr[1] + nr[3]) + (nr[5] + nr[7]);
+  if (a.qk_l2norm) {
+    ex.phase([&](int tid, int nthr) {
+      for (int r = tid; r < 2 * C; r += nthr) {
+        float ss = 0.f, sd = 0.f;
+        for (int g = 0; g < ng; ++g) {
+          ss += sSS[(size_t)g * ldp + r];
+          sd += sSD[(size_t)g * ldp + r];
+        }
         const float inv = 1.0f / sqrtf(ss + kL2Eps);
-        val = (d - ld_in(src, a.dtype, row + kk) * inv * (inv * sd)) * inv;
+        sRowF[2 * r] = inv;
+        sRowF[2 * r + 1] = inv * sd;
       }
-      if (p.G == 1) dst[kk] = val; else ex.atomic_add(dst + kk, val);
-    }
+    });
+  }
+  ex.phase([&](int tid, int nthr) {
+    batched<4>(tid, nthr, 2 * C * ng, load_piece, [&](int u, const XD& v) {
+      const int r = u / ng, c4 = 4 * (u - (u / ng) * ng), i = r < C ? r : r - C;
+      if (i >= L) return;
+      const float mul = r < C ? a.scale : 1.f;
+      float* dst = (r < C ? a.dq : a.dk) + ((size_t)(t0 + i) * H + h) * K;
+      const float inv = a.qk_l2norm ? sRowF[2 * r] : 0.f, t = a.qk_l2norm ? sRowF[2 * r + 1] : 0.f;
+      KDA_UNROLL
+      for (int x = 0; x < 4; ++x) {
+        if (c4 + x >= K) break;
+        const float d = mul * f4at(v.d, x);
+        const float val = a.qk_l2norm ? (d - f4at(v.x, x) * inv * t) * inv : d;
+        if (p.G == 1) dst[c4 + x] = val; else ex.atomic_add(dst + c4 + x, val);
+      }
+    });
   });
 }
 
