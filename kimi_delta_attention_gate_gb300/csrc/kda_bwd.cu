@@ -31,6 +31,9 @@ struct GpuExec {
                  "l"(src)
                  : "memory");
   }
+  // close this thread's group of copies issued so far (they may stay in flight across phases)
+  __device__ __forceinline__ void copy_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+  // wait for every copy this thread has issued
   __device__ __forceinline__ void copy_wait() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   }

@@ -31,19 +31,38 @@ struct HostExec {
   int nthr = kda::bwd::kThreads;
   std::mt19937* rng = nullptr;
   std::vector<int> order;
+  int cur = 0;  // the thread whose share of the phase runs
+  // Asynchronous copies issued by each thread and not yet waited for: they land only at that
+  // thread's next copy_wait(), so that a read of their destination before it (by any thread)
+  // sees the poisoned contents, as it could on the GPU.
+  std::vector<std::vector<std::pair<float*, const float*>>> pending;
   template <class F>
   void phase(F&& f) {
     if ((int)order.size() != nthr) {
       order.resize(nthr);
       for (int t = 0; t < nthr; ++t) order[t] = t;
+      pending.resize(nthr);
     }
     std::shuffle(order.begin(), order.end(), *rng);
-    for (int t : order) f(t, nthr);
+    for (int t : order) {
+      cur = t;
+      f(t, nthr);
+    }
   }
   void atomic_add(float* p, float x) { *p += x; }
   void flag(unsigned int* s, unsigned int bits) { *s |= bits; }
-  void copy16(float* dst, const float* src) { memcpy(dst, src, 16); }
-  void copy_wait() {}
+  void copy16(float* dst, const float* src) { pending[cur].emplace_back(dst, src); }
+  void copy_commit() {}
+  void copy_wait() {
+    for (auto& c : pending[cur]) memcpy(c.first, c.second, 16);
+    pending[cur].clear();
+  }
+  // every copy must have been waited for by the end of a stage body
+  bool drained() const {
+    for (const auto& v : pending)
+      if (!v.empty()) return false;
+    return true;
+  }
 };
 
 [[noreturn]] void die(const char* what, const std::string& detail) {
@@ -168,6 +187,7 @@ int main(int argc, char** argv) {
     void* sm = malloc(bytes ? bytes : 1);
     poison(sm, bytes);
     run(static_cast<float*>(sm));
+    if (!ex.drained()) die("stage body ended with", "asynchronous copies not waited for");
     free(sm);
   };
   for (int64_t c = 0; c < pl.nct; ++c)
