@@ -39,7 +39,7 @@ struct GpuExec {
   }
 };
 
-__global__ void __launch_bounds__(kThreads) prep_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, 2) prep_kernel(const Args a) {
   extern __shared__ float smem[];
   GpuExec ex;
   prep_body(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);

@@ -176,9 +176,14 @@ inline int64_t state_blocks(const Plan& p) {
   return (int64_t)p.N * p.HV * ((p.V + kBV - 1) / kBV);
 }
 // Dynamic shared memory (bytes) of the stages.
-inline size_t prep_smem(const Plan& p) {
-  return sizeof(float) * ((size_t)p.C * p.C + (size_t)p.C * (p.K + p.V) + 4);
+// prep: the Gamma, q and k tiles ([C][K + 1] each) in the first phases; beta P and the
+// substitution's columns afterwards; then the exponent-range flag
+KDA_HD size_t prep_region(const Plan& p) {
+  const size_t C = (size_t)p.C;
+  const size_t early = 3 * C * (size_t)(p.K + 1), late = C * C + C * (size_t)(p.K + p.V);
+  return early > late ? early : late;
 }
+inline size_t prep_smem(const Plan& p) { return sizeof(float) * (prep_region(p) + 4); }
 inline size_t states_smem(const Plan& p) {
   const size_t K4 = (size_t)((p.K + 3) & ~3), C = (size_t)p.C;
   return sizeof(float) * (K4 * kBV + 2 * C * kBV + C * (K4 + 4) + C * K4 + K4);
@@ -423,7 +428,14 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   float* Dc = blk + b.decay;
   const bool has_alog = a.A_log != nullptr && a.gate_mode != KDA_GATE_PREGATED;
   const float a_exp = has_alog ? expf(a.A_log[hv]) : 1.0f;
-  float* sFlag = smem + (size_t)C * C + (size_t)C * (K + V);  // > 0: an exponent out of range
+  float* sFlag = smem + prep_region(p);  // > 0: an exponent out of range
+  // Gamma, q and k of the chunk stay in shared memory through the element-wise phases (rows
+  // K + 1 floats apart: both row- and column-wise walks are free of bank conflicts); their
+  // final values also go to the workspace, where the gradient stage reads them
+  const int ldq = K + 1;
+  float* sGam = smem;                   // [C][ldq]
+  float* sQn = sGam + (size_t)C * ldq;  // [C][ldq]
+  float* sKn = sQn + (size_t)C * ldq;   // [C][ldq]
 
   // gate activation, q and k rows, beta; rows i >= L are zero
   ex.phase([&](int tid, int nthr) {
@@ -441,10 +453,11 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       }
       return v;
     }, [&](int e, const F4& v) {
-      const bool in = e / K < L;
-      Gam[e] = in ? gate_f(a.gate_mode, v.x, a_exp, v.w, a.lower_bound) : 0.f;
-      Qn[e] = v.y;
-      Kn[e] = v.z;
+      const int i = e / K, kk = e - (e / K) * K;
+      const size_t o = (size_t)i * ldq + kk;
+      sGam[o] = i < L ? gate_f(a.gate_mode, v.x, a_exp, v.w, a.lower_bound) : 0.f;
+      sQn[o] = v.y;
+      sKn[o] = v.z;
     });
     for (int i = tid; i < C; i += nthr) {
       float bv = 0.f;
@@ -460,22 +473,15 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   ex.phase([&](int tid, int nthr) {
     for (int kk = tid; kk < K; kk += nthr) {
       float acc = 0.f;
-      for (int i0 = 0; i0 < L; i0 += 8) {  // eight rows at a time, loads first
-        float g8[8];
-        KDA_UNROLL
-        for (int u = 0; u < 8; ++u) g8[u] = i0 + u < L ? Gam[(size_t)(i0 + u) * K + kk] : 0.f;
-        KDA_UNROLL
-        for (int u = 0; u < 8; ++u) {
-          if (i0 + u >= L) continue;
-          acc += g8[u];
-          Gam[(size_t)(i0 + u) * K + kk] = acc;
-        }
+      for (int i = 0; i < L; ++i) {
+        acc += sGam[(size_t)i * ldq + kk];
+        sGam[(size_t)i * ldq + kk] = acc;
       }
     }
     for (int r = tid; r < 2 * C; r += nthr) {
       const int i = r < C ? r : r - C;
       if (i >= L) continue;
-      float* row = (r < C ? Qn : Kn) + (size_t)i * K;
+      float* row = (r < C ? sQn : sKn) + (size_t)i * ldq;
       float mul = 1.f;
       if (a.qk_l2norm) {
         float ss = 0.f, ss2 = 0.f;
@@ -489,14 +495,8 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
         mul = 1.0f / sqrtf((ss + ss2) + kL2Eps);
       }
       if (r < C) mul *= a.scale;
-      for (int k0 = 0; k0 < K; k0 += 8) {
-        float x8[8];
-        KDA_UNROLL
-        for (int u = 0; u < 8; ++u) x8[u] = k0 + u < K ? row[k0 + u] : 0.f;
-        KDA_UNROLL
-        for (int u = 0; u < 8; ++u)
-          if (k0 + u < K) row[k0 + u] = x8[u] * mul;
-      }
+      KDA_UNROLL4
+      for (int kk = 0; kk < K; ++kk) row[kk] *= mul;
     }
   });
   // e^gamma_C; Qg, Kg; the right-hand sides of W and U; the block-referenced operands of Aqk
@@ -510,14 +510,23 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   const int NB = (L + 15) >> 4;
   auto mid_row = [&](int B) { return (16 * B + 7) < L - 1 ? 16 * B + 7 : L - 1; };
   ex.phase([&](int tid, int nthr) {
-    for (int kk = tid; kk < K; kk += nthr) Dc[kk] = expf(Gam[(size_t)(L - 1) * K + kk]);
+    for (int kk = tid; kk < K; kk += nthr) Dc[kk] = expf(sGam[(size_t)(L - 1) * ldq + kk]);
+    for (int e = tid; e < C * K; e += nthr) {  // the final Gamma, Q and K rows to the workspace
+      const int i = e / K, kk = e - (e / K) * K;
+      const size_t o = (size_t)i * ldq + kk;
+      Gam[e] = sGam[o];
+      Qn[e] = sQn[o];
+      Kn[e] = sKn[o];
+    }
     struct Row { float gi, gl, gm, q, k, be; };
     batched<4>(tid, nthr, C * K, [&](int e) {
       const int i = e / K, kk = e - (e / K) * K;
       Row r{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (i < L)
-        r = Row{Gam[e], Gam[(size_t)(L - 1) * K + kk], Gam[(size_t)mid_row(i >> 4) * K + kk], Qn[e],
-                Kn[e], Be[i]};
+      if (i < L) {
+        const size_t o = (size_t)i * ldq + kk;
+        r = Row{sGam[o], sGam[(size_t)(L - 1) * ldq + kk], sGam[(size_t)mid_row(i >> 4) * ldq + kk],
+                sQn[o], sKn[o], Be[i]};
+      }
       return r;
     }, [&](int e, const Row& r) {
       float qg = 0.f, kg = 0.f, w = 0.f, qf = 0.f, kf = 0.f;
@@ -549,9 +558,9 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       const int j = row - 8 * I * (I + 1);
       F4 v{0.f, 0.f, 0.f, 0.f};  // Gamma at block I's middle row, Gamma_j, K_j
       if (j < L) {
-        v.x = Gam[(size_t)mid_row(I) * K + kk];
-        v.y = Gam[(size_t)j * K + kk];
-        v.z = Kn[(size_t)j * K + kk];
+        v.x = sGam[(size_t)mid_row(I) * ldq + kk];
+        v.y = sGam[(size_t)j * ldq + kk];
+        v.z = sKn[(size_t)j * ldq + kk];
         v.w = 1.f;
       }
       return v;
@@ -625,8 +634,7 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       }
     });
   }
-  // W and U: forward substitution with (I + Diag(beta) P) on shared-memory columns (one
-  // thread per column; the row of beta P is read by every thread at once)
+  // W and U: forward substitution with (I + Diag(beta) P) on shared-memory columns
   float* sP = smem;                   // [C][C] beta_i P_ij
   float* sX = sP + (size_t)C * C;     // [C][K + V] the right-hand sides, then the solutions
   const int ncol = K + V;
@@ -637,23 +645,50 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       return col < K ? W[(size_t)i * K + col] : U[(size_t)i * V + col - K];
     }, [&](int e, float v) { sX[e] = v; });
   });
-  ex.phase([&](int tid, int nthr) {
-    for (int col = tid; col < ncol; col += nthr) {
-      for (int i = 1; i < L; ++i) {
-        const float* pr = sP + (size_t)i * C;
-        float x0 = sX[(size_t)i * ncol + col], x1 = 0.f, x2 = 0.f, x3 = 0.f;
-        int j = 0;
-        for (; j + 3 < i; j += 4) {
-          x0 = fmaf(-pr[j], sX[(size_t)j * ncol + col], x0);
-          x1 = fmaf(-pr[j + 1], sX[(size_t)(j + 1) * ncol + col], x1);
-          x2 = fmaf(-pr[j + 2], sX[(size_t)(j + 2) * ncol + col], x2);
-          x3 = fmaf(-pr[j + 3], sX[(size_t)(j + 3) * ncol + col], x3);
+  // blocked by 16 rows: each block's rows solved within the block (one thread per column),
+  // then the later rows updated with the block's solution in 4 x 4 tiles (every thread)
+  for (int J = 0; J * 16 < L; ++J) {
+    const int j0 = 16 * J, jend = j0 + 16 < L ? j0 + 16 : L;
+    ex.phase([&](int tid, int nthr) {
+      for (int col = tid; col < ncol; col += nthr) {
+        for (int i = j0 + 1; i < jend; ++i) {
+          const float* pr = sP + (size_t)i * C;
+          float x = sX[(size_t)i * ncol + col];
+          for (int j = j0; j < i; ++j) x = fmaf(-pr[j], sX[(size_t)j * ncol + col], x);
+          sX[(size_t)i * ncol + col] = x;
         }
-        for (; j < i; ++j) x0 = fmaf(-pr[j], sX[(size_t)j * ncol + col], x0);
-        sX[(size_t)i * ncol + col] = (x0 + x1) + (x2 + x3);
       }
-    }
-  });
+    });
+    if (jend >= L) break;
+    ex.phase([&](int tid, int nthr) {
+      const int nr4 = (L - jend + 3) / 4, nc4 = (ncol + 3) / 4;
+      for (int u = tid; u < nr4 * nc4; u += nthr) {
+        const int i0 = jend + 4 * (u / nc4), c0 = 4 * (u - (u / nc4) * nc4);
+        float acc[4][4];
+        KDA_UNROLL
+        for (int y = 0; y < 4; ++y)
+          KDA_UNROLL
+          for (int x = 0; x < 4; ++x)
+            acc[y][x] = (i0 + y < L && c0 + x < ncol) ? sX[(size_t)(i0 + y) * ncol + c0 + x] : 0.f;
+        for (int j = j0; j < jend; ++j) {
+          float pv[4], xv[4];
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y) pv[y] = i0 + y < L ? sP[(size_t)(i0 + y) * C + j] : 0.f;
+          KDA_UNROLL
+          for (int x = 0; x < 4; ++x) xv[x] = c0 + x < ncol ? sX[(size_t)j * ncol + c0 + x] : 0.f;
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y)
+            KDA_UNROLL
+            for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(-pv[y], xv[x], acc[y][x]);
+        }
+        KDA_UNROLL
+        for (int y = 0; y < 4; ++y)
+          KDA_UNROLL
+          for (int x = 0; x < 4; ++x)
+            if (i0 + y < L && c0 + x < ncol) sX[(size_t)(i0 + y) * ncol + c0 + x] = acc[y][x];
+      }
+    });
+  }
   ex.phase([&](int tid, int nthr) {
     KDA_UNROLL4
     for (int e = tid; e < C * ncol; e += nthr) {
@@ -1219,9 +1254,10 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     });
   });
   // X = A^T dV_new, Y = A^T dW: back substitution with (I + Diag(beta) P)^T on shared-memory
-  // columns, in two halves of the V + K columns (one thread per column, two accumulators so
-  // that the dot products' dependent chains are half as long; the column of beta P is read by
-  // every thread at once)
+  // columns, in two halves of the V + K columns, blocked by 16 rows from the last block up:
+  // each block's rows solved within the block (one thread per column), then the rows above it
+  // updated with the block's solution in 4 x 4 tiles (every thread)
+  const int NBr = (L + 15) >> 4;
   for (int part = 0; part < 2; ++part) {
     const int cbeg = part == 0 ? 0 : half_cols, cnt = part == 0 ? half_cols : ncol - half_cols;
     ex.phase([&](int tid, int nthr) {
@@ -1230,22 +1266,47 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
         return col < V ? (i < L ? dVn[(size_t)i * V + col] : 0.f) : Y[(size_t)i * K + col - V];
       }, [&](int e, float v) { sXY[e] = v; });
     });
-    ex.phase([&](int tid, int nthr) {
-      for (int cl = tid; cl < cnt; cl += nthr) {
-        for (int i = L - 2; i >= 0; --i) {
-          float x0 = sXY[(size_t)i * cnt + cl], x1 = 0.f, x2 = 0.f, x3 = 0.f;
-          int j = i + 1;
-          for (; j + 3 < L; j += 4) {
-            x0 = fmaf(-sAk[(size_t)j * C + i], sXY[(size_t)j * cnt + cl], x0);
-            x1 = fmaf(-sAk[(size_t)(j + 1) * C + i], sXY[(size_t)(j + 1) * cnt + cl], x1);
-            x2 = fmaf(-sAk[(size_t)(j + 2) * C + i], sXY[(size_t)(j + 2) * cnt + cl], x2);
-            x3 = fmaf(-sAk[(size_t)(j + 3) * C + i], sXY[(size_t)(j + 3) * cnt + cl], x3);
+    for (int B = NBr - 1; B >= 0; --B) {
+      const int r0 = 16 * B, rend = r0 + 16 < L ? r0 + 16 : L;
+      ex.phase([&](int tid, int nthr) {  // rows r0 .. rend - 1 within the block
+        for (int cl = tid; cl < cnt; cl += nthr) {
+          for (int i = rend - 2; i >= r0; --i) {
+            float x = sXY[(size_t)i * cnt + cl];
+            for (int j = i + 1; j < rend; ++j) x = fmaf(-sAk[(size_t)j * C + i], sXY[(size_t)j * cnt + cl], x);
+            sXY[(size_t)i * cnt + cl] = x;
           }
-          for (; j < L; ++j) x0 = fmaf(-sAk[(size_t)j * C + i], sXY[(size_t)j * cnt + cl], x0);
-          sXY[(size_t)i * cnt + cl] = (x0 + x1) + (x2 + x3);
         }
-      }
-    });
+      });
+      if (B == 0) break;
+      ex.phase([&](int tid, int nthr) {  // rows 0 .. r0 - 1 minus the block's contribution
+        const int nct4 = (cnt + 3) / 4;
+        for (int u = tid; u < (r0 / 4) * nct4; u += nthr) {
+          const int i0 = 4 * (u / nct4), c0 = 4 * (u - (u / nct4) * nct4);
+          float acc[4][4];
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y)
+            KDA_UNROLL
+            for (int x = 0; x < 4; ++x)
+              acc[y][x] = c0 + x < cnt ? sXY[(size_t)(i0 + y) * cnt + c0 + x] : 0.f;
+          for (int j = r0; j < rend; ++j) {
+            float av[4], xv[4];
+            KDA_UNROLL
+            for (int y = 0; y < 4; ++y) av[y] = sAk[(size_t)j * C + i0 + y];
+            KDA_UNROLL
+            for (int x = 0; x < 4; ++x) xv[x] = c0 + x < cnt ? sXY[(size_t)j * cnt + c0 + x] : 0.f;
+            KDA_UNROLL
+            for (int y = 0; y < 4; ++y)
+              KDA_UNROLL
+              for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(-av[y], xv[x], acc[y][x]);
+          }
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y)
+            KDA_UNROLL
+            for (int x = 0; x < 4; ++x)
+              if (c0 + x < cnt) sXY[(size_t)(i0 + y) * cnt + c0 + x] = acc[y][x];
+        }
+      });
+    }
     ex.phase([&](int tid, int nthr) {
       for (int e = tid; e < C * cnt; e += nthr) {
         const int i = e / cnt, col = cbeg + (e - (e / cnt) * cnt);
@@ -1339,23 +1400,58 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     });
   }
   // dAkk = -(A^T dA A^T) masked strictly lower (row r of A^T dA A^T is A applied to row r of
-  // A^T dA: forward substitution, one thread per row); dP = beta dAkk; dbeta += rowsum(dAkk P)
+  // A^T dA: forward substitution along every row, entries i < r, blocked by 16 columns: each
+  // block solved within itself (one thread per row), then the later columns updated with it in
+  // 4 x 4 tiles of (rows, columns)); dP = beta dAkk; dbeta += rowsum(dAkk P).  A row's
+  // entries i >= r are zero throughout, so the updates need no mask on the summed columns.
+  for (int J = 0; J < NBr; ++J) {
+    const int j0 = 16 * J, jend = j0 + 16 < L ? j0 + 16 : L;
+    ex.phase([&](int tid, int nthr) {
+      for (int r = tid; r < L; r += nthr) {
+        float* z = sZ + (size_t)r * ldz;
+        const int iend = jend < r ? jend : r;
+        for (int i = j0 + 1; i < iend; ++i) {
+          const float* ar = sAk + (size_t)i * C;
+          float x = z[i];
+          for (int j = j0; j < i; ++j) x = fmaf(-ar[j], z[j], x);
+          z[i] = x;
+        }
+      }
+    });
+    if (jend >= L) break;
+    ex.phase([&](int tid, int nthr) {  // columns jend .. L - 1 of every row minus block J's part
+      const int nr4 = (L + 3) / 4, ni4 = (L - jend + 3) / 4;
+      for (int u = tid; u < nr4 * ni4; u += nthr) {
+        const int r0 = 4 * (u / ni4), i0 = jend + 4 * (u - (u / ni4) * ni4);
+        float acc[4][4];
+        KDA_UNROLL
+        for (int y = 0; y < 4; ++y)
+          KDA_UNROLL
+          for (int x = 0; x < 4; ++x) acc[y][x] = sZ[(size_t)(r0 + y) * ldz + i0 + x];
+        for (int j = j0; j < jend; ++j) {
+          float zv[4], av[4];
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y) zv[y] = sZ[(size_t)(r0 + y) * ldz + j];
+          KDA_UNROLL
+          for (int x = 0; x < 4; ++x) av[x] = i0 + x < C ? sAk[(size_t)(i0 + x) * C + j] : 0.f;
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y)
+            KDA_UNROLL
+            for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(-av[x], zv[y], acc[y][x]);
+        }
+        KDA_UNROLL
+        for (int y = 0; y < 4; ++y)
+          KDA_UNROLL
+          for (int x = 0; x < 4; ++x) {
+            const int r = r0 + y, i = i0 + x;
+            if (r < L && i < r) sZ[(size_t)r * ldz + i] = acc[y][x];
+          }
+      }
+    });
+  }
   ex.phase([&](int tid, int nthr) {
     for (int r = tid; r < L; r += nthr) {
       float* z = sZ + (size_t)r * ldz;
-      for (int i = 1; i < r; ++i) {
-        const float* ar = sAk + (size_t)i * C;
-        float x0 = z[i], x1 = 0.f, x2 = 0.f, x3 = 0.f;
-        int j = 0;
-        for (; j + 3 < i; j += 4) {
-          x0 = fmaf(-ar[j], z[j], x0);
-          x1 = fmaf(-ar[j + 1], z[j + 1], x1);
-          x2 = fmaf(-ar[j + 2], z[j + 2], x2);
-          x3 = fmaf(-ar[j + 3], z[j + 3], x3);
-        }
-        for (; j < i; ++j) x0 = fmaf(-ar[j], z[j], x0);
-        z[i] = (x0 + x1) + (x2 + x3);
-      }
       float db = 0.f;
       for (int i = 0; i < r; ++i) {
         const float d = -z[i];
