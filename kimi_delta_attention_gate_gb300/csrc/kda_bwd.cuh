@@ -374,6 +374,19 @@ KDA_HD F4 ld4i(const void* base, int dtype, size_t row, int off, int len, bool v
           off + 2 < len ? ld_in(base, dtype, row + off + 2) : 0.f,
           off + 3 < len ? ld_in(base, dtype, row + off + 3) : 0.f};
 }
+// Four consecutive shared-memory floats p[0..3], those at or past `avail` read as zero; one
+// 16-byte load when all four exist and `vec` (the address is 16-byte aligned).
+KDA_HD F4 lds4m(const float* p, int avail, bool vec) {
+  if (vec && avail >= 4) return ld4(p);
+  return {avail > 0 ? p[0] : 0.f, avail > 1 ? p[1] : 0.f, avail > 2 ? p[2] : 0.f, avail > 3 ? p[3] : 0.f};
+}
+KDA_HD void sts4m(float* p, const float (&v)[4], int avail, bool vec) {
+  if (vec && avail >= 4) {
+    st4(p, v);
+    return;
+  }
+  for (int x = 0; x < 4 && x < avail; ++x) p[x] = v[x];
+}
 KDA_HD float dot4(const F4& a, const F4& b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }
@@ -662,30 +675,29 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
     if (jend >= L) break;
     ex.phase([&](int tid, int nthr) {
       const int nr4 = (L - jend + 3) / 4, nc4 = (ncol + 3) / 4;
+      const bool vec = (ncol & 3) == 0;  // 16-byte rows: one load per four columns
       for (int u = tid; u < nr4 * nc4; u += nthr) {
         const int i0 = jend + 4 * (u / nc4), c0 = 4 * (u - (u / nc4) * nc4);
         float acc[4][4];
         KDA_UNROLL
-        for (int y = 0; y < 4; ++y)
+        for (int y = 0; y < 4; ++y) {
+          const F4 v = lds4m(sX + (size_t)(i0 + y) * ncol + c0, i0 + y < L ? ncol - c0 : 0, vec);
           KDA_UNROLL
-          for (int x = 0; x < 4; ++x)
-            acc[y][x] = (i0 + y < L && c0 + x < ncol) ? sX[(size_t)(i0 + y) * ncol + c0 + x] : 0.f;
+          for (int x = 0; x < 4; ++x) acc[y][x] = f4at(v, x);
+        }
         for (int j = j0; j < jend; ++j) {
-          float pv[4], xv[4];
+          float pv[4];
           KDA_UNROLL
           for (int y = 0; y < 4; ++y) pv[y] = i0 + y < L ? sP[(size_t)(i0 + y) * C + j] : 0.f;
-          KDA_UNROLL
-          for (int x = 0; x < 4; ++x) xv[x] = c0 + x < ncol ? sX[(size_t)j * ncol + c0 + x] : 0.f;
+          const F4 xv = lds4m(sX + (size_t)j * ncol + c0, ncol - c0, vec);
           KDA_UNROLL
           for (int y = 0; y < 4; ++y)
             KDA_UNROLL
-            for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(-pv[y], xv[x], acc[y][x]);
+            for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(-pv[y], f4at(xv, x), acc[y][x]);
         }
         KDA_UNROLL
         for (int y = 0; y < 4; ++y)
-          KDA_UNROLL
-          for (int x = 0; x < 4; ++x)
-            if (i0 + y < L && c0 + x < ncol) sX[(size_t)(i0 + y) * ncol + c0 + x] = acc[y][x];
+          if (i0 + y < L) sts4m(sX + (size_t)(i0 + y) * ncol + c0, acc[y], ncol - c0, vec);
       }
     });
   }
@@ -1280,30 +1292,26 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
       if (B == 0) break;
       ex.phase([&](int tid, int nthr) {  // rows 0 .. r0 - 1 minus the block's contribution
         const int nct4 = (cnt + 3) / 4;
+        const bool vec = (cnt & 3) == 0;  // 16-byte rows: one load per four columns
         for (int u = tid; u < (r0 / 4) * nct4; u += nthr) {
           const int i0 = 4 * (u / nct4), c0 = 4 * (u - (u / nct4) * nct4);
           float acc[4][4];
           KDA_UNROLL
-          for (int y = 0; y < 4; ++y)
+          for (int y = 0; y < 4; ++y) {
+            const F4 v = lds4m(sXY + (size_t)(i0 + y) * cnt + c0, cnt - c0, vec);
             KDA_UNROLL
-            for (int x = 0; x < 4; ++x)
-              acc[y][x] = c0 + x < cnt ? sXY[(size_t)(i0 + y) * cnt + c0 + x] : 0.f;
+            for (int x = 0; x < 4; ++x) acc[y][x] = f4at(v, x);
+          }
           for (int j = r0; j < rend; ++j) {
-            float av[4], xv[4];
-            KDA_UNROLL
-            for (int y = 0; y < 4; ++y) av[y] = sAk[(size_t)j * C + i0 + y];
-            KDA_UNROLL
-            for (int x = 0; x < 4; ++x) xv[x] = c0 + x < cnt ? sXY[(size_t)j * cnt + c0 + x] : 0.f;
+            const F4 av = ld4(sAk + (size_t)j * C + i0);  // C is a multiple of 4
+            const F4 xv = lds4m(sXY + (size_t)j * cnt + c0, cnt - c0, vec);
             KDA_UNROLL
             for (int y = 0; y < 4; ++y)
               KDA_UNROLL
-              for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(-av[y], xv[x], acc[y][x]);
+              for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(-f4at(av, y), f4at(xv, x), acc[y][x]);
           }
           KDA_UNROLL
-          for (int y = 0; y < 4; ++y)
-            KDA_UNROLL
-            for (int x = 0; x < 4; ++x)
-              if (c0 + x < cnt) sXY[(size_t)(i0 + y) * cnt + c0 + x] = acc[y][x];
+          for (int y = 0; y < 4; ++y) sts4m(sXY + (size_t)(i0 + y) * cnt + c0, acc[y], cnt - c0, vec);
         }
       });
     }
@@ -1421,8 +1429,8 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     if (jend >= L) break;
     ex.phase([&](int tid, int nthr) {  // columns jend .. L - 1 of every row minus block J's part
       const int nr4 = (L + 3) / 4, ni4 = (L - jend + 3) / 4;
-      for (int u = tid; u < nr4 * ni4; u += nthr) {
-        const int r0 = 4 * (u / ni4), i0 = jend + 4 * (u - (u / ni4) * ni4);
+      for (int u = tid; u < nr4 * ni4; u += nthr) {  // a warp's lanes: one column tile, many rows
+        const int i0 = jend + 4 * (u / nr4), r0 = 4 * (u - (u / nr4) * nr4);
         float acc[4][4];
         KDA_UNROLL
         for (int y = 0; y < 4; ++y)
