@@ -347,11 +347,12 @@ KDA_HD int pad4(int x) { return (x + 3) & ~3; }
 
 // Four consecutive elements off..off+3 of a row (fp32 workspace or an input tensor), zero
 // past `len`; `vec`: the row length is a multiple of 4, so that the four are one aligned
-// 16-byte (fp32) or 8-byte (bf16) load.
+// 16-byte (fp32) or 8-byte (bf16) load.  A plain (coherent) load: workspace rows are read in
+// the kernel that wrote them.
 KDA_HD F4 ld4w(const float* row, int off, int len, bool vec) {
   if (vec) {
 #if defined(__CUDA_ARCH__)
-    const float4 v = __ldg(reinterpret_cast<const float4*>(row + off));
+    const float4 v = *reinterpret_cast<const float4*>(row + off);
     return {v.x, v.y, v.z, v.w};
 #else
     return {row[off], row[off + 1], row[off + 2], row[off + 3]};
@@ -360,10 +361,14 @@ KDA_HD F4 ld4w(const float* row, int off, int len, bool vec) {
   return {off < len ? row[off] : 0.f, off + 1 < len ? row[off + 1] : 0.f,
           off + 2 < len ? row[off + 2] : 0.f, off + 3 < len ? row[off + 3] : 0.f};
 }
+// The same for an input tensor (read-only for the whole pass: the read-only data path).
 KDA_HD F4 ld4i(const void* base, int dtype, size_t row, int off, int len, bool vec) {
   if (vec) {
-    if (dtype == KDA_F32) return ld4w(static_cast<const float*>(base) + row, off, len, true);
 #if defined(__CUDA_ARCH__)
+    if (dtype == KDA_F32) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + row + off));
+      return {v.x, v.y, v.z, v.w};
+    }
     const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + row + off));
     return {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
             __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
@@ -445,6 +450,7 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   // Gamma, q and k of the chunk stay in shared memory through the element-wise phases (rows
   // K + 1 floats apart: both row- and column-wise walks are free of bank conflicts); their
   // final values also go to the workspace, where the gradient stage reads them
+  const bool vecK = (K & 3) == 0, vecV = (V & 3) == 0;  // rows of 16-byte (fp32) / 8-byte (bf16) pieces
   const int ldq = K + 1;
   float* sGam = smem;                   // [C][ldq]
   float* sQn = sGam + (size_t)C * ldq;  // [C][ldq]
@@ -454,23 +460,30 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   ex.phase([&](int tid, int nthr) {
     if (tid == 0) sFlag[0] = 0.f;
     const bool has_dt = a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED;
-    batched<8>(tid, nthr, C * K, [&](int e) {
-      const int i = e / K, kk = e - (e / K) * K;
-      F4 v{0.f, 0.f, 0.f, 0.f};  // raw g, q, k, dt_bias
+    // four channels per element: one 8-byte (bf16) or 16-byte (fp32) load per input row piece
+    struct GQK { F4 g, q, k; };
+    const int q4 = (K + 3) / 4;
+    batched<4>(tid, nthr, C * q4, [&](int e) {
+      const int i = e / q4, c4 = 4 * (e - (e / q4) * q4);
+      GQK v{{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       if (i < L) {
         const size_t tok = (size_t)(t0 + i);
-        v.x = ld_in(a.g, a.dtype, (tok * HV + hv) * K + kk);
-        v.y = ld_in(a.q, a.dtype, (tok * H + h) * K + kk);
-        v.z = ld_in(a.k, a.dtype, (tok * H + h) * K + kk);
-        v.w = has_dt ? a.dt_bias[(size_t)hv * K + kk] : 0.f;
+        v.g = ld4i(a.g, a.dtype, (tok * HV + hv) * K, c4, K, vecK);
+        v.q = ld4i(a.q, a.dtype, (tok * H + h) * K, c4, K, vecK);
+        v.k = ld4i(a.k, a.dtype, (tok * H + h) * K, c4, K, vecK);
       }
       return v;
-    }, [&](int e, const F4& v) {
-      const int i = e / K, kk = e - (e / K) * K;
-      const size_t o = (size_t)i * ldq + kk;
-      sGam[o] = i < L ? gate_f(a.gate_mode, v.x, a_exp, v.w, a.lower_bound) : 0.f;
-      sQn[o] = v.y;
-      sKn[o] = v.z;
+    }, [&](int e, const GQK& v) {
+      const int i = e / q4, c4 = 4 * (e - (e / q4) * q4);
+      const F4 dt = has_dt ? ld4w(a.dt_bias + (size_t)hv * K, c4, K, vecK) : F4{0.f, 0.f, 0.f, 0.f};
+      KDA_UNROLL
+      for (int x = 0; x < 4; ++x) {
+        if (c4 + x >= K) break;
+        const size_t o = (size_t)i * ldq + c4 + x;
+        sGam[o] = i < L ? gate_f(a.gate_mode, f4at(v.g, x), a_exp, f4at(dt, x), a.lower_bound) : 0.f;
+        sQn[o] = f4at(v.q, x);
+        sKn[o] = f4at(v.k, x);
+      }
     });
     for (int i = tid; i < C; i += nthr) {
       float bv = 0.f;
@@ -560,10 +573,21 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       QFp[e] = qf;
       KFp[e] = kf;
     });
-    batched<8>(tid, nthr, C * V, [&](int e) {
-      const int i = e / V, cc = e - (e / V) * V;
-      return i < L ? Be[i] * ld_in(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + cc) : 0.f;
-    }, [&](int e, float u) { U[e] = u; });
+    const int v4 = (V + 3) / 4;
+    batched<4>(tid, nthr, C * v4, [&](int e) {  // four columns of v per element
+      const int i = e / v4, c4 = 4 * (e - (e / v4) * v4);
+      return i < L ? ld4i(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V, c4, V, vecV)
+                   : F4{0.f, 0.f, 0.f, 0.f};
+    }, [&](int e, const F4& x) {
+      const int i = e / v4, c4 = 4 * (e - (e / v4) * v4);
+      const float b = i < L ? Be[i] : 0.f;
+      const float u[4] = {b * x.x, b * x.y, b * x.z, b * x.w};
+      if (vecV) {
+        st4(U + (size_t)i * V + c4, u);
+      } else {
+        for (int y = 0; y < 4 && c4 + y < V; ++y) U[(size_t)i * V + c4 + y] = u[y];
+      }
+    });
     // stacked rows of KI; block I's rows start at 8 I (I + 1): 0, 16, 48, 96
     batched<8>(tid, nthr, 8 * NB * (NB + 1) * K, [&](int e) {
       const int row = e / K, kk = e - (e / K) * K;
@@ -588,7 +612,6 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
     });
   });
   const int CB = C / 4;
-  const bool vecK = (K & 3) == 0;
   if (sFlag[0] == 0.f) {
     // Aqk (j <= i) and P (j < i) in 4 x 4 blocks: rows i of one 16-row block I, keys j
     ex.phase([&](int tid, int nthr) {
@@ -1238,31 +1261,45 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     });
   }
   // the direct terms of dQg, dW, dKg; e^Gamma K for the A^T dA product
-  struct Direct { float gi, gl, dqg, dkg, y, kg, qg, kn; };
+  // element: four consecutive channels of a row (one 16-byte load per array when K % 4 == 0)
+  struct Direct { F4 gi, gl, dqg, dkg, y, kg, qg, kn; };
   ex.phase([&](int tid, int nthr) {
     batched<8>(tid, nthr, C * C, [&](int e) { return Be[e / C] * P[e]; }, [&](int e, float v) { sAk[e] = v; });
-    batched<4>(tid, nthr, C * K, [&](int e) {
-      const int i = e / K, kk = e - (e / K) * K;
-      Direct d{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (i < L)
-        d = Direct{Gam[e], Gam[(size_t)(L - 1) * K + kk], dQ[e], dK[e], Y[e], Kg[e], Qg[e], Kn[e]};
+    const int q4 = (K + 3) / 4;
+    batched<2>(tid, nthr, C * q4, [&](int e) {
+      const int i = e / q4, c4 = 4 * (e - (e / q4) * q4);
+      const F4 z{0.f, 0.f, 0.f, 0.f};
+      Direct d{z, z, z, z, z, z, z, z};
+      if (i < L) {
+        const size_t r = (size_t)i * K;
+        d = Direct{ld4w(Gam + r, c4, K, vecK), ld4w(Gam + (size_t)(L - 1) * K, c4, K, vecK),
+                   ld4w(dQ + r, c4, K, vecK), ld4w(dK + r, c4, K, vecK), ld4w(Y + r, c4, K, vecK),
+                   ld4w(Kg + r, c4, K, vecK), ld4w(Qg + r, c4, K, vecK), ld4w(Kn + r, c4, K, vecK)};
+      }
       return d;
     }, [&](int e, const Direct& d) {
-      float dq = 0.f, dk = 0.f, dg = 0.f, dkg_kg = 0.f, ekv = 0.f;
-      if (e / K < L) {
-        const float eg = fexp(d.gi);
-        dq = d.dqg * eg;
-        dk = d.dkg * fexp(d.gl - d.gi);
-        dkg_kg = d.dkg * d.kg;
-        dg = d.dqg * d.qg - dkg_kg;
-        ekv = eg * d.kn;
+      const int i = e / q4, c4 = 4 * (e - (e / q4) * q4);
+      KDA_UNROLL
+      for (int x = 0; x < 4; ++x) {
+        if (c4 + x >= K) break;
+        float dq = 0.f, dk = 0.f, dg = 0.f, dkg_kg = 0.f, ekv = 0.f;
+        if (i < L) {
+          const float gi = f4at(d.gi, x), dqg = f4at(d.dqg, x), dkg = f4at(d.dkg, x);
+          const float eg = fexp(gi);
+          dq = dqg * eg;
+          dk = dkg * fexp(f4at(d.gl, x) - gi);
+          dkg_kg = dkg * f4at(d.kg, x);
+          dg = dqg * f4at(d.qg, x) - dkg_kg;
+          ekv = eg * f4at(d.kn, x);
+        }
+        const size_t o = (size_t)i * K + c4 + x;
+        Y[o] = f4at(d.y, x);
+        dQ[o] = dq;
+        dK[o] = dk;
+        dGam[o] = dg;
+        dKG[o] = dkg_kg;
+        EK[o] = ekv;
       }
-      Y[e] = d.y;
-      dQ[e] = dq;
-      dK[e] = dk;
-      dGam[e] = dg;
-      dKG[e] = dkg_kg;
-      EK[e] = ekv;
     });
   });
   // X = A^T dV_new, Y = A^T dW: back substitution with (I + Diag(beta) P)^T on shared-memory
