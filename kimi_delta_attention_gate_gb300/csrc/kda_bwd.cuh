@@ -202,11 +202,14 @@ constexpr int kGradSliceW = 32, kGradSliceLd = 36;
 inline size_t grads_scratch(const Plan& p) {
   const size_t C = (size_t)p.C;
   size_t s = C * ((p.V + p.K + 1) / 2);
-  s = s > 2 * C * 36 ? s : 2 * C * 36;                          // 32-column A^T dA slices
+  s = s > 2 * C * 68 ? s : 2 * C * 68;                          // 64-column A^T dA slices
   const size_t ng = (size_t)((p.K + 3) / 4), l2 = 2 * ng * (2 * C + 1) + 4 * C;
   s = s > l2 ? s : l2;                                          // L2-norm backward sums
   s = s > 4 * (size_t)p.K ? s : 4 * (size_t)p.K;                // gate backward half sums
-  s = s > C * (C + 4) ? s : C * (C + 4);                        // dP transposed
+  // dP transposed, then the block-referenced key rows beyond the C x C of beta P's region
+  const size_t kb_rows_in_ak = (C * C) / (size_t)p.K;
+  const size_t kb_tail = C > kb_rows_in_ak ? (C - kb_rows_in_ak) * (size_t)p.K : 0;
+  s = s > C * (C + 4) + kb_tail ? s : C * (C + 4) + kb_tail;
   return s;
 }
 // The region the product slices are staged in, and that beta P, A^T dA and the scratch take
@@ -1374,22 +1377,22 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
       dGam[e] = d.dg + t * d.ek;
     });
   });
-  // A^T dA = X (beta V)^T + Y (beta e^Gamma K)^T over 32-column slices of v, then of k, staged
+  // A^T dA = X (beta V)^T + Y (beta e^Gamma K)^T over 64-column slices of v, then of k, staged
   // in shared memory and accumulated in sZ (lower blocks with the diagonal: its entries,
   // without beta, are the WY part of dbeta)
   {
-    constexpr int SLZ = 36;             // padded slice rows (see the products above)
+    constexpr int ZW = 64, SLZ = 68;    // slice width; padded rows (17 16-byte units apart)
     float* sA = sT;                     // [C][SLZ] X (or Y) slice
     float* sBt = sA + (size_t)C * SLZ;  // [C][SLZ] v (or e^Gamma K) slice
-    const int ntv = (V + 31) / 32, ntk = (K + 31) / 32;
+    const int ntv = (V + ZW - 1) / ZW, ntk = (K + ZW - 1) / ZW;
     for (int t = 0; t < ntv + ntk; ++t) {
       const bool onv = t < ntv;
-      const int o0 = 32 * (onv ? t : t - ntv), len = onv ? V : K;
-      const int w = len - o0 < 32 ? len - o0 : 32;
-      const bool async = (onv ? vecV : vecK) && w == 32;
+      const int o0 = ZW * (onv ? t : t - ntv), len = onv ? V : K;
+      const int w = len - o0 < ZW ? len - o0 : ZW;
+      const bool async = (onv ? vecV : vecK) && w == ZW;
       ex.phase([&](int tid, int nthr) {
-        for (int e = tid; e < C * 8; e += nthr) {
-          const int i = e >> 3, c4 = 4 * (e & 7);
+        for (int e = tid; e < C * (ZW / 4); e += nthr) {
+          const int i = e / (ZW / 4), c4 = 4 * (e - (e / (ZW / 4)) * (ZW / 4));
           const float* ar = (onv ? X + (size_t)i * V : Y + (size_t)i * K);
           if (async) {
             ex.copy16(sA + (size_t)i * SLZ + c4, ar + o0 + c4);
@@ -1416,7 +1419,7 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
           for (int y = 0; y < 4; ++y)
             for (int x = 0; x < 4; ++x)
               acc[y][x] = t > 0 ? sZ[(size_t)(4 * ib + y) * ldz + jb + CB * x] : 0.f;
-          for (int c = 0; c < 32; c += 4) {
+          for (int c = 0; c < ZW; c += 4) {
             F4 xr[4], br[4];
             for (int y = 0; y < 4; ++y) {
               xr[y] = ld4(sA + (size_t)(4 * ib + y) * SLZ + c);
@@ -1507,7 +1510,13 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     }
   });
   // block references rho (Gamma at each 16-row block's middle row), Q and K scaled by
-  // e^(Gamma - rho), and the range check of every exponent the blocked sums use; dP transposed
+  // e^(Gamma - rho), the keys scaled by e^(rho - Gamma) (row j of block B: K_j e^(rho_B -
+  // Gamma_j), in shared memory: rows below kbA in beta P's dead region, the rest after dP^T),
+  // and the range check of every exponent the blocked sums use; dP transposed
+  const int kbA = (C * C) / K;
+  auto kb_row = [&](int j) -> float* {
+    return j < kbA ? sAk + (size_t)j * K : sT + (size_t)C * lda + (size_t)(j - kbA) * K;
+  };
   ex.phase([&](int tid, int nthr) {
     for (int e = tid; e < C * C; e += nthr) {
       const int i = e / C, j = e - (e / C) * C;
@@ -1543,11 +1552,18 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
           if (R == B) rho = r.gm[R];
           if (R >= B && R < NBk) bad = bad || r.gm[R] - r.gi > 60.f;
         }
+        // and rho_R - rho_B, the factor between a key's own reference and a later block's
+        KDA_UNROLL
+        for (int R = 0; R < 4; ++R)
+          if (R > B && R < NBk) bad = bad || r.gm[R] - rho > 60.f;
         bad = bad || r.gi - rho > 60.f;
         if (bad) ex.atomic_add(sFlag, 1.f);
         const float f = fexp(r.gi - rho);
         qf = r.qn * f;
         kf = r.kn * f;
+        kb_row(i)[e - (size_t)i * K] = r.kn * fexp(rho - r.gi);
+      } else {
+        kb_row(i)[e - (size_t)i * K] = 0.f;
       }
       QF[e] = qf;
       KF[e] = kf;
@@ -1571,18 +1587,24 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
 KDA_UNROLL
         for (int x = 0; x < 16; ++x) { s1[x] = 0.f; s2[x] = 0.f; }
         const int jend = (r0 + 16 < L ? r0 + 16 : L);
-        KDA_UNROLL4
-        for (int j = 0; j < jend; ++j) {
-          const float ke = Kn[(size_t)j * K + kk] * fexp(rho - Gam[(size_t)j * K + kk]);
-          const float* da = sdAt + (size_t)j * lda + r0;  // dAqk[r0 ..][j], zero for r < j
-          const float* dz = sZt + (size_t)j * lda + r0;   // dP[r0 ..][j], zero for r <= j
+        // K_j e^(rho_R - Gamma_j) = (K_j e^(rho_B - Gamma_j)) e^(rho_R - rho_B), B = j's block
+        for (int B = 0; B <= R; ++B) {
+          const int mb = (16 * B + 7) < L - 1 ? 16 * B + 7 : L - 1;
+          const float fb = B == R ? 1.f : fexp(rho - Gam[(size_t)mb * K + kk]);
+          const int j1 = 16 * B + 16 < jend ? 16 * B + 16 : jend;
+          KDA_UNROLL4
+          for (int j = 16 * B; j < j1; ++j) {
+            const float ke = kb_row(j)[kk] * fb;
+            const float* da = sdAt + (size_t)j * lda + r0;  // dAqk[r0 ..][j], zero for r < j
+            const float* dz = sZt + (size_t)j * lda + r0;   // dP[r0 ..][j], zero for r <= j
 KDA_UNROLL
-          for (int x = 0; x < 16; x += 4) {
-            const F4 av = ld4(da + x), zv = ld4(dz + x);
-            s1[x] = fmaf(av.x, ke, s1[x]); s1[x + 1] = fmaf(av.y, ke, s1[x + 1]);
-            s1[x + 2] = fmaf(av.z, ke, s1[x + 2]); s1[x + 3] = fmaf(av.w, ke, s1[x + 3]);
-            s2[x] = fmaf(zv.x, ke, s2[x]); s2[x + 1] = fmaf(zv.y, ke, s2[x + 1]);
-            s2[x + 2] = fmaf(zv.z, ke, s2[x + 2]); s2[x + 3] = fmaf(zv.w, ke, s2[x + 3]);
+            for (int x = 0; x < 16; x += 4) {
+              const F4 av = ld4(da + x), zv = ld4(dz + x);
+              s1[x] = fmaf(av.x, ke, s1[x]); s1[x + 1] = fmaf(av.y, ke, s1[x + 1]);
+              s1[x + 2] = fmaf(av.z, ke, s1[x + 2]); s1[x + 3] = fmaf(av.w, ke, s1[x + 3]);
+              s2[x] = fmaf(zv.x, ke, s2[x]); s2[x + 1] = fmaf(zv.y, ke, s2[x + 1]);
+              s2[x + 2] = fmaf(zv.z, ke, s2[x + 2]); s2[x + 3] = fmaf(zv.w, ke, s2[x + 3]);
+            }
           }
         }
         // Gamma of the block's rows (also the exponents of the second part)
