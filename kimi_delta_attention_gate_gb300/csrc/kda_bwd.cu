@@ -182,6 +182,10 @@ cudaError_t run_grads(const Args& a, cudaStream_t st) {
   return launch_smem(grads_kernel, dim3((unsigned)a.p.nct, (unsigned)a.p.HV), grads_smem(a.p), a, st);
 }
 
+}  // namespace
+cudaError_t run_states_tc(const Args& a, cudaStream_t st);  // kda_bwd_tc.cu
+namespace {
+
 struct Stage {
   const char* name;
   cudaError_t (*run)(const Args&, cudaStream_t);
@@ -196,7 +200,7 @@ int stages_for(const Plan& pl, Stage* out) {
   if (pl.varlen) out[n++] = {"chunk_table", run_chunk_table};
   if (pl.nct > 0) out[n++] = {"bwd_prep", run_prep};
   if (state_blocks(pl) > 0) {
-    out[n++] = {"bwd_states", run_states};
+    out[n++] = {"bwd_states", pl.tc_states ? run_states_tc : run_states};
     out[n++] = {"bwd_dstate", run_dstate};
   }
   if (pl.nct > 0) out[n++] = {"bwd_grads", run_grads};

@@ -59,6 +59,15 @@ constexpr int kThreads = 256;  // threads per block of every stage
 constexpr int kBV = 32;        // V columns per block of the two state stages
 constexpr float kL2Eps = 1e-6f;
 
+// Operand tiles of the tensor-core state stage, per (chunk, value head), for K = V = 128 and
+// C = 64, as bf16 high and low parts (x = hi + lo to ~2^-16): -W [64 tokens][128 channels]
+// (two 64-channel panels) and Kg^T [128 channels][64 tokens] (one panel), each part in the
+// 128-byte-swizzled K-major layout of the tensor cores' shared-memory operands.
+constexpr size_t kTileBytes = 65536;
+constexpr size_t kTileNegW = 0;       // hi at +0, lo at +16384
+constexpr size_t kTileKgT = 32768;    // hi at +32768, lo at +49152
+constexpr size_t kTileLo = 16384;
+
 // Float offsets of one (chunk, value head) block of the workspace.
 struct Block {
   size_t gam, qn, kn, qg, kg, w, y, dq, dk, dgam, dkg;  // [C][K]
@@ -104,6 +113,8 @@ struct Plan {
   size_t off_blocks;  // [nct][HV] blocks
   size_t off_h;       // fp32 [nct][HV][K][V]: the state before every chunk
   size_t off_dh;      // fp32 [nct][HV][K][V]: the gradient of the state after every chunk
+  int tc_states;      // the state stage runs on the tensor cores (K = V = 128, C = 64)
+  size_t off_tiles;   // [nct][HV] 64 KB operand tiles of that stage (when tc_states)
   size_t total_bytes;
   Block blk;
 };
@@ -138,6 +149,12 @@ inline Plan make_plan(const kda_fwd_params* f) {
   off += round256(states);
   p.off_dh = off;
   off += round256(states);
+  p.tc_states = p.K == 128 && p.V == 128 && p.C == 64;
+  if (p.tc_states) {
+    off = (off + 1023) / 1024 * 1024;
+    p.off_tiles = off;
+    off += kTileBytes * (size_t)p.nct * p.HV;
+  }
   p.total_bytes = off;
   return p;
 }
@@ -252,6 +269,45 @@ KDA_HD float fexp(float x) {
   return expf(x);
 #endif
 }
+// fp32 -> bf16 bits, rounded to nearest even (finite inputs)
+KDA_HD uint16_t bf16_bits_rn(float x) {
+  uint32_t u;
+  memcpy(&u, &x, sizeof u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+KDA_HD float bf16_to_f32(uint16_t h) {
+  const uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+// Byte offset of element (row, col < 64) in a 128-byte-swizzled panel: rows of 128 bytes in
+// groups of eight, the eight 16-byte chunks of row r permuted by chunk ^ (r % 8).
+KDA_HD uint32_t swz128(uint32_t row, uint32_t col) {
+  return (row >> 3) * 1024u + (row & 7u) * 128u + ((((col >> 3) ^ (row & 7u)) & 7u) << 4) +
+         ((col & 7u) << 1);
+}
+// Eight consecutive elements x[0..7] as bf16 hi + lo: one 16-byte chunk at byte offset `off`
+// of a tile's high part and one at the same offset of its low part
+KDA_HD void put_hilo8(char* tile, size_t off, const float (&x)[8]) {
+  uint16_t hi[8], lo[8];
+  for (int j = 0; j < 8; ++j) {
+    hi[j] = bf16_bits_rn(x[j]);
+    lo[j] = bf16_bits_rn(x[j] - bf16_to_f32(hi[j]));
+  }
+#if defined(__CUDA_ARCH__)
+  uint4 h, l;
+  memcpy(&h, hi, 16);
+  memcpy(&l, lo, 16);
+  *reinterpret_cast<uint4*>(tile + off) = h;
+  *reinterpret_cast<uint4*>(tile + off + kTileLo) = l;
+#else
+  memcpy(tile + off, hi, 16);
+  memcpy(tile + off + kTileLo, lo, 16);
+#endif
+}
+
 KDA_HD float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 // The sigmoid's derivative s(x) (1 - s(x)) = t / (1 + t)^2 with t = e^-|x| <= 1: one
 // exponential, and no cancellation once s(x) rounds to 1 (|x| beyond about 17 in fp32).
@@ -274,6 +330,11 @@ KDA_HD float gate_f(int mode, float graw, float a, float dt, float lb) {
 KDA_HD float* block_ptr(const Args& a, int64_t c, int hv) {
   return reinterpret_cast<float*>(a.ws + a.p.off_blocks) +
          ((size_t)c * a.p.HV + hv) * a.p.blk.floats;
+}
+
+// The tensor-core state stage's operand tiles of (chunk c, value head hv) (tc_states only).
+KDA_HD char* tile_ptr(const Args& a, int64_t c, int hv) {
+  return a.ws + a.p.off_tiles + ((size_t)c * a.p.HV + hv) * kTileBytes;
 }
 
 KDA_HD float* state_ptr(const Args& a, size_t off, int64_t c, int hv) {
@@ -733,6 +794,21 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       const int i = e / ncol, col = e - (e / ncol) * ncol;
       if (col < K) W[(size_t)i * K + col] = sX[e];
       else U[(size_t)i * V + col - K] = sX[e];
+    }
+    if (p.tc_states) {  // the tensor-core state stage's operand tiles (K = 128, C = 64)
+      char* tile = tile_ptr(a, c, hv);
+      for (int u = tid; u < C * (K / 8); u += nthr) {  // -W: row = token, 8 channels per chunk
+        const int i = u / (K / 8), k0 = 8 * (u - (u / (K / 8)) * (K / 8));
+        float x[8];
+        for (int j = 0; j < 8; ++j) x[j] = -sX[(size_t)i * ncol + k0 + j];
+        put_hilo8(tile, kTileNegW + (size_t)(k0 >> 6) * 8192 + swz128((uint32_t)i, (uint32_t)(k0 & 63)), x);
+      }
+      for (int u = tid; u < K * (C / 8); u += nthr) {  // Kg^T: row = channel, 8 tokens per chunk
+        const int kk = u / (C / 8), t0 = 8 * (u - (u / (C / 8)) * (C / 8));
+        float x[8];
+        for (int j = 0; j < 8; ++j) x[j] = Kg[(size_t)(t0 + j) * K + kk];
+        put_hilo8(tile, kTileKgT + swz128((uint32_t)kk, (uint32_t)t0), x);
+      }
     }
   });
 }
