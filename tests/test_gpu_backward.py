@@ -49,6 +49,26 @@ def test_full_head_dimensions():
     check(inp, chunk_form=True)
 
 
+def test_tensor_core_states_varlen_grouped_fp32():
+    """K = V = 128 at chunk 64 (the shapes whose state stage runs on the tensor cores) with fp32
+    inputs, two value heads on one q/k head, and a varlen batch: a sequence of three chunks, an
+    empty one, a one-token one and a ragged one of 159 tokens, then padding rows."""
+    inp = kin.make_inputs(bt.workload(B=1, T=300, H=1, HV=2, K=128, V=128, C=64, dtype="f32",
+                                      seed=61, varlen_n=4, varlen_max_len=100, h0_std=0.1))
+    inp.cu_seqlens[:] = np.array([0, 130, 130, 131, 290], dtype=np.int64)
+    errs, got = check(inp, chunk_form=True)
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert np.all(got[name][:, 290:] == 0), name
+
+
+def test_tensor_core_states_transposed_layout_and_negative_eigenvalues():
+    """The tensor-core state stage with [V, K] states and beta in (0, 2), two sequences."""
+    inp = kin.make_inputs(bt.workload(B=2, T=140, H=1, HV=1, K=128, V=128, C=64, dtype="bf16",
+                                      seed=62, h0_std=0.1))
+    inp.h0 = np.ascontiguousarray(np.swapaxes(inp.h0, -1, -2))
+    check(inp, state_v_first=True, allow_neg_eigval=True, chunk_form=True)
+
+
 def test_varlen_with_empty_sequences_and_padding():
     inp = kin.make_inputs(bt.workload(B=1, T=200, seed=44, varlen_n=5, varlen_max_len=60))
     inp.cu_seqlens[:] = np.array([0, 70, 70, 71, 135, 190], dtype=np.int64)
