@@ -183,7 +183,8 @@ cudaError_t run_grads(const Args& a, cudaStream_t st) {
 }
 
 }  // namespace
-cudaError_t run_states_tc(const Args& a, cudaStream_t st);  // kda_bwd_tc.cu
+cudaError_t run_states_tc(const Args& a, cudaStream_t st);   // kda_bwd_tc.cu
+cudaError_t run_dstate_tc(const Args& a, cudaStream_t st);   // kda_bwd_tc.cu
 namespace {
 
 struct Stage {
@@ -201,7 +202,7 @@ int stages_for(const Plan& pl, Stage* out) {
   if (pl.nct > 0) out[n++] = {"bwd_prep", run_prep};
   if (state_blocks(pl) > 0) {
     out[n++] = {"bwd_states", pl.tc_states ? run_states_tc : run_states};
-    out[n++] = {"bwd_dstate", run_dstate};
+    out[n++] = {"bwd_dstate", pl.tc_dstate ? run_dstate_tc : run_dstate};
   }
   if (pl.nct > 0) out[n++] = {"bwd_grads", run_grads};
   return n;

@@ -59,14 +59,20 @@ constexpr int kThreads = 256;  // threads per block of every stage
 constexpr int kBV = 32;        // V columns per block of the two state stages
 constexpr float kL2Eps = 1e-6f;
 
-// Operand tiles of the tensor-core state stage, per (chunk, value head), for K = V = 128 and
-// C = 64, as bf16 high and low parts (x = hi + lo to ~2^-16): -W [64 tokens][128 channels]
-// (two 64-channel panels) and Kg^T [128 channels][64 tokens] (one panel), each part in the
-// 128-byte-swizzled K-major layout of the tensor cores' shared-memory operands.
-constexpr size_t kTileBytes = 65536;
+// Operand tiles of the tensor-core state stages, per (chunk, value head), for K = V = 128 and
+// C = 64, as bf16 high and low parts (x = hi + lo to ~2^-16), each part in the 128-byte-
+// swizzled panel layout of the tensor cores' shared-memory operands: -W [64 tokens][128
+// channels] (two 64-channel panels) and Kg^T [128 channels][64 tokens] (one panel) for both
+// stages; Aqk [64 tokens][64 tokens] and Qg [64 tokens][128 channels] (two panels) for the
+// state-gradient stage when it runs on the tensor cores too.
+constexpr size_t kTileBytes = 65536;     // -W and Kg^T
+constexpr size_t kTileBytesDs = 114688;  // + Aqk and Qg
 constexpr size_t kTileNegW = 0;       // hi at +0, lo at +16384
 constexpr size_t kTileKgT = 32768;    // hi at +32768, lo at +49152
 constexpr size_t kTileLo = 16384;
+constexpr size_t kTileAqk = 65536;    // hi at +65536, lo at +73728
+constexpr size_t kTileAqkLo = 8192;
+constexpr size_t kTileQg = 81920;     // hi at +81920, lo at +98304
 
 // Float offsets of one (chunk, value head) block of the workspace.
 struct Block {
@@ -114,7 +120,9 @@ struct Plan {
   size_t off_h;       // fp32 [nct][HV][K][V]: the state before every chunk
   size_t off_dh;      // fp32 [nct][HV][K][V]: the gradient of the state after every chunk
   int tc_states;      // the state stage runs on the tensor cores (K = V = 128, C = 64)
-  size_t off_tiles;   // [nct][HV] 64 KB operand tiles of that stage (when tc_states)
+  int tc_dstate;      // and the state-gradient stage too (bf16 inputs as well)
+  size_t tile_bytes;  // operand tiles per (chunk, value head): kTileBytes or kTileBytesDs
+  size_t off_tiles;   // [nct][HV] operand tiles of those stages
   size_t total_bytes;
   Block blk;
 };
@@ -150,10 +158,12 @@ inline Plan make_plan(const kda_fwd_params* f) {
   p.off_dh = off;
   off += round256(states);
   p.tc_states = p.K == 128 && p.V == 128 && p.C == 64;
+  p.tc_dstate = p.tc_states && f->in_dtype == KDA_BF16;
   if (p.tc_states) {
+    p.tile_bytes = p.tc_dstate ? kTileBytesDs : kTileBytes;
     off = (off + 1023) / 1024 * 1024;
     p.off_tiles = off;
-    off += kTileBytes * (size_t)p.nct * p.HV;
+    off += p.tile_bytes * (size_t)p.nct * p.HV;
   }
   p.total_bytes = off;
   return p;
@@ -290,7 +300,7 @@ KDA_HD uint32_t swz128(uint32_t row, uint32_t col) {
 }
 // Eight consecutive elements x[0..7] as bf16 hi + lo: one 16-byte chunk at byte offset `off`
 // of a tile's high part and one at the same offset of its low part
-KDA_HD void put_hilo8(char* tile, size_t off, const float (&x)[8]) {
+KDA_HD void put_hilo8(char* tile, size_t off, const float (&x)[8], size_t lo_off = kTileLo) {
   uint16_t hi[8], lo[8];
   for (int j = 0; j < 8; ++j) {
     hi[j] = bf16_bits_rn(x[j]);
@@ -301,10 +311,10 @@ KDA_HD void put_hilo8(char* tile, size_t off, const float (&x)[8]) {
   memcpy(&h, hi, 16);
   memcpy(&l, lo, 16);
   *reinterpret_cast<uint4*>(tile + off) = h;
-  *reinterpret_cast<uint4*>(tile + off + kTileLo) = l;
+  *reinterpret_cast<uint4*>(tile + off + lo_off) = l;
 #else
   memcpy(tile + off, hi, 16);
-  memcpy(tile + off + kTileLo, lo, 16);
+  memcpy(tile + off + lo_off, lo, 16);
 #endif
 }
 
@@ -334,7 +344,7 @@ KDA_HD float* block_ptr(const Args& a, int64_t c, int hv) {
 
 // The tensor-core state stage's operand tiles of (chunk c, value head hv) (tc_states only).
 KDA_HD char* tile_ptr(const Args& a, int64_t c, int hv) {
-  return a.ws + a.p.off_tiles + ((size_t)c * a.p.HV + hv) * kTileBytes;
+  return a.ws + a.p.off_tiles + ((size_t)c * a.p.HV + hv) * a.p.tile_bytes;
 }
 
 KDA_HD float* state_ptr(const Args& a, size_t off, int64_t c, int hv) {
@@ -808,6 +818,20 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
         float x[8];
         for (int j = 0; j < 8; ++j) x[j] = Kg[(size_t)(t0 + j) * K + kk];
         put_hilo8(tile, kTileKgT + swz128((uint32_t)kk, (uint32_t)t0), x);
+      }
+      if (p.tc_dstate) {
+        for (int u = tid; u < C * (C / 8); u += nthr) {  // Aqk: row = token, 8 tokens per chunk
+          const int i = u / (C / 8), j0 = 8 * (u - (u / (C / 8)) * (C / 8));
+          float x[8];
+          for (int j = 0; j < 8; ++j) x[j] = Aqk[(size_t)i * C + j0 + j];
+          put_hilo8(tile, kTileAqk + swz128((uint32_t)i, (uint32_t)j0), x, kTileAqkLo);
+        }
+        for (int u = tid; u < C * (K / 8); u += nthr) {  // Qg: row = token, 8 channels per chunk
+          const int i = u / (K / 8), k0 = 8 * (u - (u / (K / 8)) * (K / 8));
+          float x[8];
+          for (int j = 0; j < 8; ++j) x[j] = Qg[(size_t)i * K + k0 + j];
+          put_hilo8(tile, kTileQg + (size_t)(k0 >> 6) * 8192 + swz128((uint32_t)i, (uint32_t)(k0 & 63)), x);
+        }
       }
     }
   });

@@ -16,6 +16,7 @@
 // thread issues the MMAs; warp 17: one thread issues the bulk copies.  Every wait is bounded
 // and reports KDA_DEV_TIMEOUT through the status word.
 
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "kda_bwd.cuh"
@@ -274,7 +275,358 @@ __global__ void __launch_bounds__(kStThreads, 1) states_tc_kernel(const Args a) 
   if (warp == kEpi) tmem_dealloc(tmem, 512);
 }
 
+// ======================================================================================
+// The state-gradient stage (backward-propagation steps 3-4) on the tensor cores, chunks in
+// reverse, with dS' (the gradient of the state after the chunk) in tensor memory:
+//   dV_new^T = dO^T Aqk + dS'^T Kg^T                      -> dV_new
+//   dS^T     = dS'^T Diag(e^gamma_C) + dO^T Qg + dV_new^T (-W)   (the next chunk's dS')
+// dO (bf16 input, exact) is the MN-major A operand of the two products that do not depend
+// on the chain, loaded by TMA; the chain's A operands (dS'^T, dV_new^T) are hi / lo pairs in
+// tensor memory; B operands are the hi / lo tiles (-W and Kg^T read as MN-major operands,
+// Aqk and Qg written for this stage).  Shared memory: the dO / Aqk / e^gamma_C part of a
+// chunk is double-buffered; Kg^T and the Qg / -W pair are single-buffered and refilled as
+// soon as the chunk's G1 (Kg^T) or G2 (Qg, -W) has read them.
+// ======================================================================================
+constexpr uint32_t DA_DO = 0;          // dO tile [64 tokens x 128 v] bf16, two MN panels
+constexpr uint32_t DA_AQK = 16384;     // Aqk hi, lo (8 KB each)
+constexpr uint32_t DA_D = 32768;       // e^gamma_C fp32 [128]
+constexpr uint32_t DA_BYTES = 32768 + 512;
+constexpr uint32_t DA_SLOT = 33792;
+constexpr uint32_t DS_KG = 2 * DA_SLOT;        // Kg^T hi, lo (16 KB each)
+constexpr uint32_t DS_QW = DS_KG + 32768;      // Qg hi, lo, then -W hi, lo (16 KB each)
+constexpr uint32_t DS_BAR = DS_QW + 65536;     // 12 barriers
+constexpr uint32_t DS_TMEM = DS_BAR + 96;
+constexpr uint32_t DS_SMEM = DS_TMEM + 16 + 1024;
+constexpr uint32_t TD_DV = 0;     // dV_new^T fp32 [128 v x 64 tokens]
+constexpr uint32_t TD_DS = 64;    // dS^T fp32 [128 v x 128 channels]
+constexpr uint32_t TD_DSA = 192;  // dS'^T bf16 pairs: hi 192..255, lo 256..319
+constexpr uint32_t TD_DVA = 320;  // dV_new^T bf16 pairs: hi 320..351, lo 352..383
+
+__global__ void __launch_bounds__(kStThreads, 1)
+    dstate_tc_kernel(const Args a, const __grid_constant__ CUtensorMap domap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1k(smem_raw);
+  const Plan& p = a.p;
+  const int HV = p.HV, V = p.V, K = p.K;
+  const int hv = (int)(blockIdx.x % HV);
+  const int n = (int)(blockIdx.x / HV);
+  int64_t bos, eos, cfirst;
+  if (!seq_range(a, n, bos, eos, cfirst)) {
+    if (threadIdx.x == 0) atomicOr(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const int64_t nch = (eos - bos + p.C - 1) / p.C;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t sbase = ((size_t)n * HV + hv) * (size_t)K * V;
+  if (nch == 0) {  // an empty sequence: dh0 is the incoming gradient itself
+    if (a.dh0 != nullptr)
+      for (int e = tid; e < K * V; e += blockDim.x)
+        a.dh0[sbase + e] = a.d_final_state != nullptr ? a.d_final_state[sbase + e] : 0.f;
+    return;
+  }
+  uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + DS_BAR);  // [2]
+  uint64_t* freedA = fullA + 2;                               // [2]
+  uint64_t* fullKG = fullA + 4;
+  uint64_t* freedKG = fullA + 5;
+  uint64_t* fullQW = fullA + 6;
+  uint64_t* freedQW = fullA + 7;
+  uint64_t* bar_dv = fullA + 8;    // G1 done: dV_new^T complete
+  uint64_t* bar_ds = fullA + 9;    // G2 done: the next dS'^T complete
+  uint64_t* bar_dvn = fullA + 10;  // epilogue: dV_new^T hi / lo written
+  uint64_t* bar_st = fullA + 11;   // epilogue: dS'^T hi / lo and dS'^T e^gamma_C written
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + DS_TMEM);
+  if (warp == kEpi) {
+    tmem_alloc(sTmem, 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 8; ++i) mbar_init(&fullA[i], 1);
+    mbar_init(bar_dv, 1);
+    mbar_init(bar_ds, 1);
+    mbar_init(bar_dvn, kEpi);
+    mbar_init(bar_st, kEpi);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  bool ok = true;
+  // iteration it processes chunk nch - 1 - it
+  auto chunk_of = [&](int64_t it) { return nch - 1 - it; };
+  auto slotA = [&](int64_t it) { return sm + (uint32_t)(it & 1) * DA_SLOT; };
+  auto parA = [](int64_t it) { return (uint32_t)((it >> 1) & 1); };
+  auto par1 = [](int64_t it) { return (uint32_t)(it & 1); };
+
+  if (warp == kEpi + 1) {
+    // ------------------------------- copy warp ---------------------------------------
+    if (lane == 0) {
+      const CUtensorMap* dmap = &domap;
+      auto issueA = [&](int64_t it) {  // dO tile, Aqk hi / lo, e^gamma_C of iteration it
+        const int64_t cl = chunk_of(it), c = cfirst + cl;
+        uint8_t* dst = slotA(it);
+        mbar_arrive_expect_tx(&fullA[it & 1], DA_BYTES);
+        const int32_t t0 = (int32_t)(bos + cl * p.C);
+        tma_load_3d(dst + DA_DO, dmap, 0, hv, t0, &fullA[it & 1]);
+        tma_load_3d(dst + DA_DO + 8192, dmap, 64, hv, t0, &fullA[it & 1]);
+        bulk_g2s(dst + DA_AQK, tile_ptr(a, c, hv) + kTileAqk, 16384u, &fullA[it & 1]);
+        bulk_g2s(dst + DA_D, block_ptr(a, c, hv) + p.blk.decay, 512u, &fullA[it & 1]);
+      };
+      auto issueKG = [&](int64_t it) {
+        mbar_arrive_expect_tx(fullKG, 32768u);
+        bulk_g2s(sm + DS_KG, tile_ptr(a, cfirst + chunk_of(it), hv) + kTileKgT, 32768u, fullKG);
+      };
+      auto issueQW = [&](int64_t it) {
+        const char* t = tile_ptr(a, cfirst + chunk_of(it), hv);
+        mbar_arrive_expect_tx(fullQW, 65536u);
+        bulk_g2s(sm + DS_QW, t + kTileQg, 32768u, fullQW);
+        bulk_g2s(sm + DS_QW + 32768, t + kTileNegW, 32768u, fullQW);
+      };
+      int64_t a_issued = 1, kg_issued = 1, qw_issued = 1;
+      issueA(0);
+      if (nch > 1) {
+        issueA(1);
+        a_issued = 2;
+      }
+      issueKG(0);
+      issueQW(0);
+      for (int64_t it = 0; it + 1 < nch; ++it) {
+        if (!mbar_wait(freedKG, par1(it))) { ok = false; break; }   // G1 of it has read Kg^T
+        issueKG(it + 1);
+        kg_issued = it + 2;
+        if (!mbar_wait(freedQW, par1(it))) { ok = false; break; }   // G2 of it has read Qg, -W
+        issueQW(it + 1);
+        qw_issued = it + 2;
+        if (it + 2 < nch) {                                          // and its dO / Aqk slot
+          if (!mbar_wait(&freedA[it & 1], parA(it))) { ok = false; break; }
+          issueA(it + 2);
+          a_issued = it + 3;
+        }
+      }
+      if (!ok) {
+        atomicOr(a.status, KDA_DEV_TIMEOUT);
+        // the copies in flight must land before the CTA's shared memory is released
+        for (int64_t it = a_issued > 2 ? a_issued - 2 : 0; it < a_issued; ++it)
+          mbar_wait(&fullA[it & 1], parA(it), 100000000ull);
+        mbar_wait(fullKG, par1(kg_issued - 1), 100000000ull);
+        mbar_wait(fullQW, par1(qw_issued - 1), 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kEpi) {
+    // -------------------------------- MMA warp ---------------------------------------
+    if (lane == 0) {
+      const uint32_t kg_hi = smem_u32(sm + DS_KG), kg_lo = kg_hi + 16384u;
+      const uint32_t qg_hi = smem_u32(sm + DS_QW), qg_lo = qg_hi + 16384u;
+      const uint32_t nw_hi = qg_hi + 32768u, nw_lo = qg_hi + 49152u;
+      // dO^T Aqk of iteration it into the dV_new^T accumulator (its first product): wait for
+      // the slot, zero the dO rows past the chunk's end (another sequence's tokens)
+      auto issue_doaqk = [&](int64_t it) -> bool {
+        if (!mbar_wait(&fullA[it & 1], parA(it))) return false;
+        uint8_t* sl = slotA(it);
+        const int64_t t0 = bos + chunk_of(it) * p.C;
+        const int L = (int)((eos - t0) < p.C ? (eos - t0) : p.C);
+        if (L < p.C) {
+          for (int e = L * 8; e < p.C * 8; ++e) {  // 8 16-byte pieces per 128-byte row
+            *reinterpret_cast<uint4*>(sl + DA_DO + (uint32_t)e * 16u) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sl + DA_DO + 8192u + (uint32_t)e * 16u) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_async_smem();
+        }
+        tc_fence_after();
+        const uint32_t dob = smem_u32(sl + DA_DO), aqb = smem_u32(sl + DA_AQK);
+        const uint32_t idesc = idesc_bf16(128, 64, true, true);
+#pragma unroll 1
+        for (int ks = 0; ks < 4; ++ks) {  // tokens t' 16 ks .. 16 ks + 15
+          const uint64_t ad = sdesc_sw128(dob + ks * 2048, 8192, 1024);
+          mma_bf16(tmem + TD_DV, ad, sdesc_sw128(aqb + ks * 2048, 8192, 1024), idesc, ks > 0);
+          mma_bf16(tmem + TD_DV, ad, sdesc_sw128(aqb + 8192 + ks * 2048, 8192, 1024), idesc, 1);
+        }
+        return true;
+      };
+      if (!issue_doaqk(0)) ok = false;
+      for (int64_t it = 0; it < nch && ok; ++it) {
+        const uint32_t dob = smem_u32(slotA(it) + DA_DO);
+        if (!mbar_wait(fullKG, par1(it))) { ok = false; break; }
+        // G1: needs dS'^T hi / lo (and the rescaled dS'^T already in the accumulator)
+        if (!mbar_wait_spin(bar_st, par1(it))) { ok = false; break; }
+        tc_fence_after();
+        {
+          const uint32_t idesc = idesc_bf16(128, 64, false, true);
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) {  // channels 16 ks .. 16 ks + 15 (rows of Kg^T)
+            const uint32_t bo = (uint32_t)ks * 2048u;
+            mma_bf16_ts(tmem + TD_DV, tmem + TD_DSA + 8 * ks, sdesc_sw128(kg_hi + bo, 8192, 1024), idesc, 1);
+            mma_bf16_ts(tmem + TD_DV, tmem + TD_DSA + 8 * ks, sdesc_sw128(kg_lo + bo, 8192, 1024), idesc, 1);
+            mma_bf16_ts(tmem + TD_DV, tmem + TD_DSA + 64 + 8 * ks, sdesc_sw128(kg_hi + bo, 8192, 1024), idesc, 1);
+          }
+        }
+        mma_commit(bar_dv);
+        mma_commit(freedKG);
+        // dO^T Qg into the dS^T accumulator while the epilogue turns dV_new^T into operands
+        if (!mbar_wait(fullQW, par1(it))) { ok = false; break; }
+        tc_fence_after();
+        {
+          const uint32_t idesc = idesc_bf16(128, 128, true, true);
+#pragma unroll 1
+          for (int ks = 0; ks < 4; ++ks) {  // tokens 16 ks .. 16 ks + 15
+            const uint64_t ad = sdesc_sw128(dob + ks * 2048, 8192, 1024);
+            mma_bf16(tmem + TD_DS, ad, sdesc_sw128(qg_hi + ks * 2048, 8192, 1024), idesc, 1);
+            mma_bf16(tmem + TD_DS, ad, sdesc_sw128(qg_lo + ks * 2048, 8192, 1024), idesc, 1);
+          }
+        }
+        // G2: needs dV_new^T hi / lo
+        if (!mbar_wait_spin(bar_dvn, par1(it))) { ok = false; break; }
+        tc_fence_after();
+        {
+          const uint32_t idesc = idesc_bf16(128, 128, false, true);
+#pragma unroll 1
+          for (int ks = 0; ks < 4; ++ks) {  // tokens 16 ks .. 16 ks + 15 (rows of -W)
+            const uint32_t bo = (uint32_t)ks * 2048u;
+            mma_bf16_ts(tmem + TD_DS, tmem + TD_DVA + 8 * ks, sdesc_sw128(nw_hi + bo, 8192, 1024), idesc, 1);
+            mma_bf16_ts(tmem + TD_DS, tmem + TD_DVA + 8 * ks, sdesc_sw128(nw_lo + bo, 8192, 1024), idesc, 1);
+            mma_bf16_ts(tmem + TD_DS, tmem + TD_DVA + 32 + 8 * ks, sdesc_sw128(nw_hi + bo, 8192, 1024), idesc, 1);
+          }
+        }
+        mma_commit(bar_ds);
+        mma_commit(freedQW);
+        mma_commit(&freedA[it & 1]);
+        if (it + 1 < nch && !issue_doaqk(it + 1)) { ok = false; break; }
+      }
+      if (!ok) atomicOr(a.status, KDA_DEV_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ epilogue warps -------------------------------------
+    const int q4 = warp & 3, part = warp >> 2;  // part: channels 32 part ..; tokens 16 part ..
+    const int v = 32 * q4 + lane;
+    const uint32_t lb = tmem_addr(tmem, 32 * q4, 0);
+    auto arrive = [&](uint64_t* bar) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
+    auto sidx = [&](int k) -> size_t {  // element (channel k, column v) of an external state
+      return sbase + (a.state_v_first ? (size_t)v * K + k : (size_t)k * V + v);
+    };
+    float D[32];  // dS'^T[v][32 part + j]: the gradient of the state after the chunk
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      D[j] = a.d_final_state == nullptr ? 0.f : a.d_final_state[sidx(32 * part + j)];
+    for (int64_t it = 0; it < nch && ok; ++it) {
+      const int64_t c = cfirst + chunk_of(it);
+      // dS'^T as hi / lo A operands of G1 and dS'^T Diag(e^gamma_C) into the accumulator
+      bool w = mbar_wait(&fullA[it & 1], parA(it));
+      {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) split2(D[2 * j], D[2 * j + 1], hi[j], lo[j]);
+        tmem_st16(lb + TD_DSA + 16 * part, hi);
+        tmem_st16(lb + TD_DSA + 64 + 16 * part, lo);
+        const float* dc = reinterpret_cast<const float*>(slotA(it) + DA_D) + 32 * part;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sc[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) sc[x] = __float_as_uint(D[16 * h + x] * dc[16 * h + x]);
+          tmem_st16(lb + TD_DS + 32 * part + 16 * h, sc);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      arrive(bar_st);
+      {  // dS' of this chunk out to the workspace, [K][V]
+        float* hd = state_ptr(a, p.off_dh, c, hv);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) hd[(size_t)(32 * part + j) * V + v] = D[j];
+      }
+      // dV_new^T -> hi / lo A operands of G2; out to the workspace
+      w = mbar_wait(bar_dv, par1(it)) && w;
+      tc_fence_after();
+      uint32_t r[16];
+      tmem_ld16(lb + TD_DV + 16 * part, r);
+      tmem_wait_ld();
+      {
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          split2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]), hi[j], lo[j]);
+        tmem_st8(lb + TD_DVA + 8 * part, hi);
+        tmem_st8(lb + TD_DVA + 32 + 8 * part, lo);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      arrive(bar_dvn);
+      {
+        float* dvn = block_ptr(a, c, hv) + p.blk.dvn;
+#pragma unroll
+        for (int x = 0; x < 16; ++x) dvn[(size_t)(16 * part + x) * V + v] = __uint_as_float(r[x]);
+      }
+      // the gradient of the state before this chunk: the previous chunk's dS'
+      w = mbar_wait(bar_ds, par1(it)) && w;
+      tc_fence_after();
+      {
+        uint32_t r0[16], r1[16];
+        tmem_ld16(lb + TD_DS + 32 * part, r0);
+        tmem_ld16(lb + TD_DS + 32 * part + 16, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          D[j] = __uint_as_float(r0[j]);
+          D[16 + j] = __uint_as_float(r1[j]);
+        }
+      }
+      if (!w) ok = false;
+    }
+    if (ok && a.dh0 != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a.dh0[sidx(32 * part + j)] = D[j];
+    }
+    if (!ok) atomicOr(a.status, KDA_DEV_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kEpi) tmem_dealloc(tmem, 512);
+}
+
+// Driver entry point for tensor-map encoding, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
 }  // namespace
+
+// The state-gradient stage on the tensor cores (bf16 dO): one CTA per (sequence, value head).
+cudaError_t run_dstate_tc(const Args& a, cudaStream_t st) {
+  const unsigned grid = (unsigned)((int64_t)a.p.N * a.p.HV);
+  if (grid == 0) return cudaSuccess;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // dO tiles: [64 tokens x 64 v] boxes with 128-byte swizzle (MN-major A operand panels)
+  CUtensorMap domap;
+  const cuuint64_t dims[3] = {(cuuint64_t)a.p.V, (cuuint64_t)a.p.HV, (cuuint64_t)a.p.ntok};
+  const cuuint64_t strides[2] = {(cuuint64_t)a.p.V * 2, (cuuint64_t)a.p.HV * a.p.V * 2};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(&domap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.d_o), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(dstate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)DS_SMEM);
+  if (e != cudaSuccess) return e;
+  dstate_tc_kernel<<<grid, kStThreads, DS_SMEM, st>>>(a, domap);
+  return cudaGetLastError();
+}
 
 // The state stage on the tensor cores: one CTA per (sequence, value head).
 cudaError_t run_states_tc(const Args& a, cudaStream_t st) {

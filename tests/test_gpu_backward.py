@@ -61,6 +61,17 @@ def test_tensor_core_states_varlen_grouped_fp32():
         assert np.all(got[name][:, 290:] == 0), name
 
 
+def test_tensor_core_states_and_gradients_varlen_grouped_bf16():
+    """The same batch with bf16 inputs, where the state-gradient stage also runs on the tensor
+    cores (dO loaded by TMA; the rows of the next sequence inside a ragged chunk zeroed)."""
+    inp = kin.make_inputs(bt.workload(B=1, T=300, H=1, HV=2, K=128, V=128, C=64, dtype="bf16",
+                                      seed=63, varlen_n=4, varlen_max_len=100, h0_std=0.1))
+    inp.cu_seqlens[:] = np.array([0, 130, 130, 131, 290], dtype=np.int64)
+    errs, got = check(inp, chunk_form=True)
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert np.all(got[name][:, 290:] == 0), name
+
+
 def test_tensor_core_states_transposed_layout_and_negative_eigenvalues():
     """The tensor-core state stage with [V, K] states and beta in (0, 2), two sequences."""
     inp = kin.make_inputs(bt.workload(B=2, T=140, H=1, HV=1, K=128, V=128, C=64, dtype="bf16",
