@@ -377,10 +377,13 @@ def fp32_alu_peak_tflops(sm_mhz: float = MAX_SM_MHZ) -> float:
     return N_SM * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
 
 
-def bwd_stage_flops(stage: str, C: int, K: int, V: int, nct: int, HV: int) -> float:
+def bwd_stage_flops(stage: str, C: int, K: int, V: int, nct: int, HV: int,
+                    vprod: bool = False) -> float:
     """Algorithmic flops of one launch of a backward kernel over nct chunks x HV value heads
     (every chunk full; a fused multiply-add counts 2, an exponential 0): the dot products and
-    triangular substitutions each kernel's stage computes."""
+    triangular substitutions each kernel's stage computes.  With `vprod` the products over v
+    (dAqk, dQg, dW, dKg, diag(S dS'^T)) run in their own stage, bwd_vprod, not in bwd_grads."""
+    vp = V * C * (C + 1) + 6 * C * K * V + 2 * K * V
     per = {
         # Aqk and P over j <= i (2 FMA + 1 mul per channel); W, U forward substitution
         "bwd_prep": 5 * K * C * (C + 1) / 2 + 3 * (K + V) * C * (C - 1) / 2,
@@ -390,8 +393,10 @@ def bwd_stage_flops(stage: str, C: int, K: int, V: int, nct: int, HV: int) -> fl
         "bwd_dstate": 2 * C * K * V + C * (C + 1) * V + 4 * C * K * V,
         # dAqk; dQg, dW, dKg; X, Y back substitution; A^T dA (strictly lower); the
         # e^(Gamma_i - Gamma_j) sums over rows and columns
-        "bwd_grads": (V * C * (C + 1) + 6 * C * K * V + (K + V) * C * (C - 1)
-                      + C * (C - 1) / 2 * (2 * V + 3 * K) + 5.5 * K * C * (C + 1)),
+        "bwd_grads": (vp + (K + V) * C * (C - 1)
+                      + C * (C - 1) / 2 * (2 * V + 3 * K) + 5.5 * K * C * (C + 1)
+                      - (vp if vprod else 0)),
+        "bwd_vprod": vp,
     }.get(stage, 0.0)
     return float(per) * nct * HV
 
@@ -474,14 +479,16 @@ def measure_backward(kb, kda, dev, stream, inp, t, gate, steps):
         nct = wl.B * ((wl.T + C - 1) // C)
     else:
         nct = int(np.sum((np.diff(inp.cu_seqlens) + C - 1) // C))
-    flops = {nm: bwd_stage_flops(nm, wl.chunk_size, wl.K, wl.V, nct, wl.HV) for nm in names}
+    vprod = "bwd_vprod" in names
+    flops = {nm: bwd_stage_flops(nm, wl.chunk_size, wl.K, wl.V, nct, wl.HV, vprod) for nm in names}
     kern = [i for i, nm in enumerate(names) if flops[nm] > 0]
     dom = max(kern, key=lambda i: stage_ms[i])
     peak = fp32_alu_peak_tflops()
     achieved = flops[names[dom]] / (stage_ms[dom] / 1e3) / 1e12
     total_flops = sum(flops.values())
     return {"workload": f"{wl.name} (the forward's workload), incoming gradients N(0, 1) seeded",
-            "entry": "kda_bwd", "arithmetic": "fp32 CUDA cores (bf16 inputs widened exactly)",
+            "entry": "kda_bwd", "arithmetic": ("fp32 accumulation; CUDA cores, and tcgen05 with bf16 hi/lo operand "
+                                               "splits in the state, state-gradient and v-product stages"),
             "value": inp.n_tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "steps": n, "gpu_launches_per_step": int(kb.kda_bwd_num_launches(p)),
             "workspace_bytes": int(ws.numel()),

@@ -80,7 +80,8 @@ kda_status kda_bwd_check(const kda_bwd_params* p);
 size_t kda_bwd_workspace_size(const kda_bwd_params* p);
 
 /* Number of kernel launches one kda_bwd call makes (0 if the parameters are invalid): the
-   chunk table (varlen only), prep, states, state gradient and gradients.  The zeroing of
+   chunk table (varlen only), prep, states, state gradient, the products over v (bf16 inputs
+   with K = V = 128 and chunk 64 only) and gradients.  The zeroing of
    the outputs (cudaMemsetAsync) is not counted.  Host only. */
 int32_t kda_bwd_num_launches(const kda_bwd_params* p);
 
@@ -89,7 +90,8 @@ int32_t kda_bwd_num_launches(const kda_bwd_params* p);
 int32_t kda_bwd_num_stages(const kda_bwd_params* p);
 
 /* Name of stage `stage` ("zero_outputs", "chunk_table", "bwd_prep", "bwd_states",
-   "bwd_dstate", "bwd_grads"); "" if out of range or the parameters are invalid. */
+   "bwd_dstate", "bwd_vprod", "bwd_grads"); "" if out of range or the parameters are
+   invalid. */
 const char* kda_bwd_stage_name(const kda_bwd_params* p, int32_t stage);
 
 /* Enqueue only stage `stage` of kda_bwd on `stream`.  Calling every stage in order on one

@@ -185,13 +185,14 @@ cudaError_t run_grads(const Args& a, cudaStream_t st) {
 }  // namespace
 cudaError_t run_states_tc(const Args& a, cudaStream_t st);   // kda_bwd_tc.cu
 cudaError_t run_dstate_tc(const Args& a, cudaStream_t st);   // kda_bwd_tc.cu
+cudaError_t run_vprod_tc(const Args& a, cudaStream_t st);    // kda_bwd_tc.cu
 namespace {
 
 struct Stage {
   const char* name;
   cudaError_t (*run)(const Args&, cudaStream_t);
 };
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 8;
 
 // The stages of one backward call, in order: the zeroing of the outputs (cudaMemsetAsync,
 // no kernel of this library), then the kernels.
@@ -204,6 +205,7 @@ int stages_for(const Plan& pl, Stage* out) {
     out[n++] = {"bwd_states", pl.tc_states ? run_states_tc : run_states};
     out[n++] = {"bwd_dstate", pl.tc_dstate ? run_dstate_tc : run_dstate};
   }
+  if (pl.nct > 0 && pl.tc_vprod) out[n++] = {"bwd_vprod", run_vprod_tc};
   if (pl.nct > 0) out[n++] = {"bwd_grads", run_grads};
   return n;
 }

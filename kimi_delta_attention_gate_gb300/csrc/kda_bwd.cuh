@@ -121,6 +121,9 @@ struct Plan {
   size_t off_dh;      // fp32 [nct][HV][K][V]: the gradient of the state after every chunk
   int tc_states;      // the state stage runs on the tensor cores (K = V = 128, C = 64)
   int tc_dstate;      // and the state-gradient stage too (bf16 inputs as well)
+  int tc_vprod;       // the gradient stage's V-reduced products run as their own tensor-core
+                      // stage (same shapes): dQg, dW, dKg into the dq, y, dk slots, dAqk into
+                      // the aqk slot, diag(S dS'^T) into the first K floats of the dkg slot
   size_t tile_bytes;  // operand tiles per (chunk, value head): kTileBytes or kTileBytesDs
   size_t off_tiles;   // [nct][HV] operand tiles of those stages
   size_t total_bytes;
@@ -159,6 +162,7 @@ inline Plan make_plan(const kda_fwd_params* f) {
   off += round256(states);
   p.tc_states = p.K == 128 && p.V == 128 && p.C == 64;
   p.tc_dstate = p.tc_states && f->in_dtype == KDA_BF16;
+  p.tc_vprod = p.tc_dstate;
   if (p.tc_states) {
     p.tile_bytes = p.tc_dstate ? kTileBytesDs : kTileBytes;
     off = (off + 1023) / 1024 * 1024;
@@ -1160,6 +1164,61 @@ KDA_BODY void dstate_body(Exec& ex, const Args& a, int64_t bid, float* smem) {
   }
 }
 
+// ---- vprod: per (chunk c, value head hv), when tc_vprod -------------------------------
+//
+// The gradient stage's products over v (backward-propagation step 5): dQg = dO S^T,
+// dW = -dV_new S^T, dKg = V_new dS'^T, dAqk = dO V_new^T (masked to j <= i < L) and the
+// diagonal of S dS'^T, written to the block for the gradient stage.  On the GPU a tensor-core
+// kernel (kda_bwd_tc.cu) computes them; this body, one output element per thread and step,
+// is their plain statement, which the host emulation runs in its place.
+template <class Exec>
+KDA_BODY void vprod_body(Exec& ex, const Args& a, int64_t c, int hv, float* /*smem*/) {
+  const Plan& p = a.p;
+  const int C = p.C, K = p.K, V = p.V, HV = p.HV;
+  int n, L;
+  int64_t t0;
+  if (!locate(a, c, n, t0, L)) {
+    ex.flag(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const Block& b = p.blk;
+  float* blk = block_ptr(a, c, hv);
+  const float* Vn = blk + b.vn;
+  const float* dVn = blk + b.dvn;
+  const float* S = state_ptr(a, p.off_h, c, hv);
+  const float* dSp = state_ptr(a, p.off_dh, c, hv);
+  auto dO = [&](int i, int v) {
+    return i < L ? ld_in(a.d_o, a.dtype, ((size_t)(t0 + i) * HV + hv) * V + v) : 0.f;
+  };
+  ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < C * K; e += nthr) {
+      const int i = e / K, kk = e - (e / K) * K;
+      float q = 0.f, w = 0.f, kg = 0.f;
+      for (int v = 0; v < V; ++v) {
+        const float s = S[(size_t)kk * V + v];
+        q = fmaf(dO(i, v), s, q);
+        w = fmaf(-dVn[(size_t)i * V + v], s, w);
+        kg = fmaf(Vn[(size_t)i * V + v], dSp[(size_t)kk * V + v], kg);
+      }
+      blk[b.dq + e] = q;
+      blk[b.y + e] = w;
+      blk[b.dk + e] = kg;
+    }
+    for (int e = tid; e < C * C; e += nthr) {
+      const int i = e / C, j = e - (e / C) * C;
+      float d = 0.f;
+      if (i < L && j <= i)
+        for (int v = 0; v < V; ++v) d = fmaf(dO(i, v), Vn[(size_t)j * V + v], d);
+      blk[b.aqk + e] = d;
+    }
+    for (int kk = tid; kk < K; kk += nthr) {
+      float d = 0.f;
+      for (int v = 0; v < V; ++v) d = fmaf(S[(size_t)kk * V + v], dSp[(size_t)kk * V + v], d);
+      blk[b.dkg + kk] = d;
+    }
+  });
+}
+
 // ---- grads: per (chunk c, value head hv) -----------------------------------------------
 //
 // The chunk's dense products (dAqk = dO V_new^T, dQg = dO S^T, dW = -dV_new S^T,
@@ -1227,11 +1286,21 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   // rows of the inputs dO and v (only rows < L exist)
   auto in_row = [&](int i) { return ((size_t)(t0 + i) * HV + hv) * V; };
 
-  // beta; the accumulators of the tiled products start at zero
+  // beta; the accumulators of the tiled products start at zero, or (products over v done by
+  // their own stage) take that stage's dAqk and diag(S dS'^T)
   ex.phase([&](int tid, int nthr) {
-    for (int e = tid; e < C * lda; e += nthr) sdAt[e] = 0.f;
+    if (p.tc_vprod) {
+      const float* dAqk = blk + b.aqk;
+      for (int e = tid; e < C * lda; e += nthr) {
+        const int j = e / lda, i = e - (e / lda) * lda;
+        sdAt[e] = i < C ? dAqk[(size_t)i * C + j] : 0.f;
+      }
+      for (int kk = tid; kk < K4; kk += nthr) sDgc[kk] = kk < K ? dKG[kk] : 0.f;
+    } else {
+      for (int e = tid; e < C * lda; e += nthr) sdAt[e] = 0.f;
+      for (int kk = tid; kk < K4; kk += nthr) sDgc[kk] = 0.f;
+    }
     for (int i = tid; i < C; i += nthr) sB[i] = Be[i];
-    for (int kk = tid; kk < K4; kk += nthr) sDgc[kk] = 0.f;
     if (tid == 0) sFlag[0] = 0.f;
   });
   // The products over v in 32-column slices staged in shared memory (16-byte asynchronous
@@ -1246,7 +1315,7 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   float* sDv = sDs + (size_t)K4 * SL;         // [C][SL] dV_new slice
   float* sVn = sDv + (size_t)C * SL;          // [C][SL] V_new slice
   float* sDo = sVn + (size_t)C * SL;          // [C][SL] dO slice
-  const int nvt = (V + SW - 1) / SW;
+  const int nvt = p.tc_vprod ? 0 : (V + SW - 1) / SW;
   for (int t = 0; t < nvt; ++t) {
     const int v0 = SW * t, w = V - v0 < SW ? V - v0 : SW;
     const bool async = vecV && w == SW;

@@ -587,6 +587,227 @@ __global__ void __launch_bounds__(kStThreads, 1)
   if (warp == kEpi) tmem_dealloc(tmem, 512);
 }
 
+// ======================================================================================
+// The gradient stage's products over v (backward-propagation step 5) on the tensor cores,
+// one CTA per (chunk, value head), M = 64 tokens:
+//   dQg = dO S^T, dW = -dV_new S^T            (step pair 1: B = S)
+//   dKg = V_new dS'^T, dAqk = dO V_new^T       (step pair 2: B = dS', V_new)
+// each over the 128 columns of v in two 64-column halves.  Per half, every thread splits
+// its share of the fp32 operands (the workspace's states, V_new, dV_new) into bf16 hi / lo
+// parts in the swizzled K-major layout, TMA brings the dO panel (an exact bf16 input), and
+// one thread issues the MMAs (two per K-step with dO as A, three otherwise).  The diagonal
+// of S dS'^T is summed while dS' is split.  Outputs go to the block's dq, y, dk, aqk and dkg
+// slots, where the gradient stage reads them.
+// ======================================================================================
+constexpr uint32_t VP_B = 0;          // B tile (S or dS') hi, lo: [128 rows k][64 v], 16 KB each
+constexpr uint32_t VP_A = 32768;      // A tile (dV_new or V_new) hi, lo: [64 rows t][64 v], 8 KB each
+constexpr uint32_t VP_DO = 49152;     // dO panel [64 t][64 v] bf16
+constexpr uint32_t VP_RED = 57344;    // [256] partial sums of diag(S dS'^T)
+constexpr uint32_t VP_BAR = 58368;    // bar_do, bar_mma
+constexpr uint32_t VP_TMEM = VP_BAR + 16;
+constexpr uint32_t VP_SMEM = VP_TMEM + 16 + 1024;
+constexpr int kVpThreads = 256;
+
+// hi / lo parts of eight consecutive fp32 values into the 16-byte chunks at `off` of a tile's
+// high part and at `off + lo` of its low part
+__device__ __forceinline__ void put8(uint8_t* tile, uint32_t off, uint32_t lo_off, const float4& x0,
+                                     const float4& x1) {
+  uint4 h, l;
+  split2(x0.x, x0.y, h.x, l.x);
+  split2(x0.z, x0.w, h.y, l.y);
+  split2(x1.x, x1.y, h.z, l.z);
+  split2(x1.z, x1.w, h.w, l.w);
+  *reinterpret_cast<uint4*>(tile + off) = h;
+  *reinterpret_cast<uint4*>(tile + off + lo_off) = l;
+}
+
+__global__ void __launch_bounds__(kVpThreads, 2)
+    vprod_tc_kernel(const Args a, const __grid_constant__ CUtensorMap domap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1k(smem_raw);
+  const Plan& p = a.p;
+  const int64_t c = blockIdx.x;
+  const int hv = blockIdx.y;
+  const int K = p.K, V = p.V, C = p.C;
+  int n, L;
+  int64_t t0;
+  if (!locate(a, c, n, t0, L)) {
+    if (threadIdx.x == 0) atomicOr(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bar_do = reinterpret_cast<uint64_t*>(sm + VP_BAR);
+  uint64_t* bar_mma = bar_do + 1;
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + VP_TMEM);
+  float* sRed = reinterpret_cast<float*>(sm + VP_RED);
+  if (warp == 0) {
+    tmem_alloc(sTmem, 256);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(bar_do, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  bool ok = true;
+  float* blk = block_ptr(a, c, hv);
+  const float* S = state_ptr(a, p.off_h, c, hv);
+  const float* dSp = state_ptr(a, p.off_dh, c, hv);
+  const float* Vn = blk + p.blk.vn;
+  const float* dVn = blk + p.blk.dvn;
+  float dgc = 0.f;  // this thread's part of diag(S dS'^T) for channel tid / 2
+  int do_open = -1, mma_open = -1;  // (thread 0) step of a copy / MMA group not yet seen done
+  const uint32_t b_hi = smem_u32(sm + VP_B), b_lo = b_hi + 16384u;
+  const uint32_t a_hi = smem_u32(sm + VP_A), a_lo = a_hi + 8192u;
+  const uint32_t do_b = smem_u32(sm + VP_DO);
+  for (int step = 0; step < 4 && ok; ++step) {
+    const int pair = step >> 1, h = step & 1;  // pair 0: B = S, A = dV_new; pair 1: dS', V_new
+    const int v0 = 64 * h;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(bar_do, 8192u);
+      tma_load_3d(sm + VP_DO, &domap, v0, hv, (int32_t)t0, bar_do);
+      do_open = step;
+    }
+    {  // B: channel row k = tid / 2, columns v0 + 32 (tid & 1) .. + 31
+      const int k = tid >> 1, c0 = 32 * (tid & 1);
+      const float* src = (pair == 0 ? S : dSp) + (size_t)k * V + v0 + c0;
+      const float* s2 = S + (size_t)k * V + v0 + c0;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const float4 x0 = *reinterpret_cast<const float4*>(src + 8 * g);
+        const float4 x1 = *reinterpret_cast<const float4*>(src + 8 * g + 4);
+        put8(sm + VP_B, swz128((uint32_t)k, (uint32_t)(c0 + 8 * g)), 16384u, x0, x1);
+        if (pair == 1) {
+          const float4 y0 = *reinterpret_cast<const float4*>(s2 + 8 * g);
+          const float4 y1 = *reinterpret_cast<const float4*>(s2 + 8 * g + 4);
+          dgc = fmaf(x0.x, y0.x, fmaf(x0.y, y0.y, fmaf(x0.z, y0.z, fmaf(x0.w, y0.w, dgc))));
+          dgc = fmaf(x1.x, y1.x, fmaf(x1.y, y1.y, fmaf(x1.z, y1.z, fmaf(x1.w, y1.w, dgc))));
+        }
+      }
+    }
+    {  // A: token row t = tid / 4, columns v0 + 16 (tid & 3) .. + 15
+      const int t = tid >> 2, c0 = 16 * (tid & 3);
+      const float* src = (pair == 0 ? dVn : Vn) + (size_t)t * V + v0 + c0;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const float4 x0 = *reinterpret_cast<const float4*>(src + 8 * g);
+        const float4 x1 = *reinterpret_cast<const float4*>(src + 8 * g + 4);
+        put8(sm + VP_A, swz128((uint32_t)t, (uint32_t)(c0 + 8 * g)), 8192u, x0, x1);
+      }
+    }
+    fence_async_smem();
+    // the dO panel; rows past the chunk's end (another sequence's tokens) become zero
+    if (!mbar_wait(bar_do, (uint32_t)(step & 1))) ok = false;
+    else if (tid == 0) do_open = -1;
+    if (L < C) {
+      for (int e = tid; e < (C - L) * 8; e += kVpThreads)
+        *reinterpret_cast<uint4*>(sm + VP_DO + (uint32_t)(L * 8 + e) * 16u) = make_uint4(0u, 0u, 0u, 0u);
+      fence_async_smem();
+    }
+    ok = named_bar_and(1, kVpThreads, ok);
+    if (tid == 0 && ok) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int ks = 0; ks < 4; ++ks) {  // v0 + 16 ks .. + 15
+        const uint32_t o = (uint32_t)ks * 32u;
+        const uint32_t acc = (h > 0 || ks > 0) ? 1u : 0u;
+        const uint64_t dA = sdesc_sw128(do_b + o, 16, 1024);
+        const uint64_t Ah = sdesc_sw128(a_hi + o, 16, 1024), Al = sdesc_sw128(a_lo + o, 16, 1024);
+        const uint64_t Bh = sdesc_sw128(b_hi + o, 16, 1024), Bl = sdesc_sw128(b_lo + o, 16, 1024);
+        if (pair == 0) {
+          const uint32_t id = idesc_bf16(64, 128), idn = idesc_bf16(64, 128, false, false, true);
+          mma_bf16(tmem + 0, dA, Bh, id, acc);        // dQg = dO S^T
+          mma_bf16(tmem + 0, dA, Bl, id, 1);
+          mma_bf16(tmem + 128, Ah, Bh, idn, acc);     // dW = -dV_new S^T
+          mma_bf16(tmem + 128, Ah, Bl, idn, 1);
+          mma_bf16(tmem + 128, Al, Bh, idn, 1);
+        } else {
+          const uint32_t id = idesc_bf16(64, 128), id64 = idesc_bf16(64, 64);
+          mma_bf16(tmem + 0, Ah, Bh, id, acc);        // dKg = V_new dS'^T
+          mma_bf16(tmem + 0, Ah, Bl, id, 1);
+          mma_bf16(tmem + 0, Al, Bh, id, 1);
+          mma_bf16(tmem + 128, dA, Ah, id64, acc);    // dAqk = dO V_new^T (B = the A tile)
+          mma_bf16(tmem + 128, dA, Al, id64, 1);
+        }
+      }
+      mma_commit(bar_mma);
+      mma_open = step;
+    }
+    if (ok) {
+      if (!mbar_wait(bar_mma, (uint32_t)(step & 1))) ok = false;
+      else if (tid == 0) mma_open = -1;
+      ok = named_bar_and(1, kVpThreads, ok);
+    }
+    tc_fence_after();
+    if (h == 1 && ok) {
+      // epilogue of the pair: row t = 16 q + lane (lanes 0-15 of TMEM quadrant q = warp % 4
+      // hold the M = 64 rows); warp / 4 picks the column half
+      const int q = warp & 3, half = warp >> 2, t = 16 * q + lane;
+      const uint32_t lb = tmem_addr(tmem, 32 * q, 0);
+      float* out0 = blk + (pair == 0 ? p.blk.dq : p.blk.dk);
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        uint32_t r[16];
+        tmem_ld16(lb + 64 * half + 16 * j, r);
+        tmem_wait_ld();
+        if (lane < 16) {
+          float4* d = reinterpret_cast<float4*>(out0 + (size_t)t * K + 64 * half + 16 * j);
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            d[x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                               __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+        }
+      }
+      if (pair == 0) {  // dW into the y slot
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[16];
+          tmem_ld16(lb + 128 + 64 * half + 16 * j, r);
+          tmem_wait_ld();
+          if (lane < 16) {
+            float4* d = reinterpret_cast<float4*>(blk + p.blk.y + (size_t)t * K + 64 * half + 16 * j);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              d[x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                                 __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+          }
+        }
+      } else {  // dAqk, masked to j <= t < L, into the aqk slot
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+          uint32_t r[16];
+          tmem_ld16(lb + 128 + 32 * half + 16 * j, r);
+          tmem_wait_ld();
+          if (lane < 16) {
+            const int jb = 32 * half + 16 * j;
+            float* d = blk + p.blk.aqk + (size_t)t * C + jb;
+#pragma unroll
+            for (int x = 0; x < 16; ++x) d[x] = (t < L && jb + x <= t) ? __uint_as_float(r[x]) : 0.f;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncthreads();  // the accumulators are read before the next pair's MMAs overwrite them
+    }
+  }
+  if (ok) {  // diag(S dS'^T): the two threads of each channel
+    sRed[tid] = dgc;
+    __syncthreads();
+    if (tid < K) blk[p.blk.dkg + tid] = sRed[2 * tid] + sRed[2 * tid + 1];
+  } else if (tid == 0) {
+    atomicOr(a.status, KDA_DEV_TIMEOUT);
+    // a copy or MMA group still in flight must end before shared and tensor memory go
+    if (do_open >= 0) mbar_wait(bar_do, (uint32_t)(do_open & 1), 100000000ull);
+    if (mma_open >= 0) mbar_wait(bar_mma, (uint32_t)(mma_open & 1), 100000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 // Driver entry point for tensor-map encoding, looked up once.
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -605,26 +826,47 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 
 }  // namespace
 
-// The state-gradient stage on the tensor cores (bf16 dO): one CTA per (sequence, value head).
-cudaError_t run_dstate_tc(const Args& a, cudaStream_t st) {
-  const unsigned grid = (unsigned)((int64_t)a.p.N * a.p.HV);
-  if (grid == 0) return cudaSuccess;
+namespace {
+// dO as [64 tokens x 64 v] boxes with 128-byte swizzle (one row of 128 bytes per token)
+bool make_do_map(const Args& a, CUtensorMap& m) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
-  if (enc == nullptr) return cudaErrorNotSupported;
-  // dO tiles: [64 tokens x 64 v] boxes with 128-byte swizzle (MN-major A operand panels)
-  CUtensorMap domap;
+  if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)a.p.V, (cuuint64_t)a.p.HV, (cuuint64_t)a.p.ntok};
   const cuuint64_t strides[2] = {(cuuint64_t)a.p.V * 2, (cuuint64_t)a.p.HV * a.p.V * 2};
   const cuuint32_t box[3] = {64, 1, 64};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(&domap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.d_o), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  return enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.d_o), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+// The state-gradient stage on the tensor cores (bf16 dO): one CTA per (sequence, value head).
+cudaError_t run_dstate_tc(const Args& a, cudaStream_t st) {
+  const unsigned grid = (unsigned)((int64_t)a.p.N * a.p.HV);
+  if (grid == 0) return cudaSuccess;
+  if (tmap_encoder() == nullptr) return cudaErrorNotSupported;
+  CUtensorMap domap;  // MN-major A operand panels of dO^T
+  if (!make_do_map(a, domap)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(dstate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)DS_SMEM);
   if (e != cudaSuccess) return e;
   dstate_tc_kernel<<<grid, kStThreads, DS_SMEM, st>>>(a, domap);
+  return cudaGetLastError();
+}
+
+// The gradient stage's products over v on the tensor cores (bf16 dO): one CTA per
+// (chunk, value head).
+cudaError_t run_vprod_tc(const Args& a, cudaStream_t st) {
+  if (a.p.nct == 0 || a.p.HV == 0) return cudaSuccess;
+  if (tmap_encoder() == nullptr) return cudaErrorNotSupported;
+  CUtensorMap domap;  // K-major A operand panels of dO
+  if (!make_do_map(a, domap)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(vprod_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)VP_SMEM);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)a.p.nct, (unsigned)a.p.HV);
+  vprod_tc_kernel<<<grid, kVpThreads, VP_SMEM, st>>>(a, domap);
   return cudaGetLastError();
 }
 

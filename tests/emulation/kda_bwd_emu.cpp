@@ -197,6 +197,10 @@ int main(int argc, char** argv) {
     with_smem(kda::bwd::states_smem(pl), [&](float* sm) { kda::bwd::states_body(ex, a, bid, sm); });
   for (int64_t bid = 0; bid < kda::bwd::state_blocks(pl); ++bid)
     with_smem(kda::bwd::dstate_smem(pl), [&](float* sm) { kda::bwd::dstate_body(ex, a, bid, sm); });
+  if (pl.tc_vprod)  // the products over v (a tensor-core stage on the GPU), plainly
+    for (int64_t c = 0; c < pl.nct; ++c)
+      for (int hv = 0; hv < pl.HV; ++hv)
+        with_smem(16, [&](float* sm) { kda::bwd::vprod_body(ex, a, c, hv, sm); });
   for (int64_t c = 0; c < pl.nct; ++c)
     for (int hv = 0; hv < pl.HV; ++hv)
       with_smem(kda::bwd::grads_smem(pl), [&](float* sm) { kda::bwd::grads_body(ex, a, c, hv, sm); });

@@ -149,6 +149,10 @@ def test_stage_lists(lib):
     assert kb.kda_bwd_num_launches(p) == kb.kda_bwd_num_stages(p) - 1
     assert kb.kda_bwd_stage_name(params(), 5) == "" and kb.kda_bwd_stage_name(params(), -1) == ""
     assert kb.kda_bwd_num_stages(params(dq=0)) == 0
+    # bf16 at K = V = 128, chunk 64: the products over v get a tensor-core stage of their own
+    assert names(params(fwd_V=128)) == ["zero_outputs", "bwd_prep", "bwd_states", "bwd_dstate",
+                                        "bwd_vprod", "bwd_grads"]
+    assert "bwd_vprod" not in names(params(fwd_V=128, fwd_in_dtype=kb.KDA_F32))
 
 
 def test_stage_rejects_small_workspace_before_cuda(lib):
