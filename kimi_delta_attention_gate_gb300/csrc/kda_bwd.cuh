@@ -463,6 +463,8 @@ KDA_HD F4 lds4m(const float* p, int avail, bool vec) {
   if (vec && avail >= 4) return ld4(p);
   return {avail > 0 ? p[0] : 0.f, avail > 1 ? p[1] : 0.f, avail > 2 ? p[2] : 0.f, avail > 3 ? p[3] : 0.f};
 }
+// The store counterpart (shared or global memory): p[0..3] = v, those at or past `avail`
+// left alone; one 16-byte store when all four exist and `vec`.
 KDA_HD void sts4m(float* p, const float (&v)[4], int avail, bool vec) {
   if (vec && avail >= 4) {
     st4(p, v);
@@ -1451,27 +1453,28 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
       return d;
     }, [&](int e, const Direct& d) {
       const int i = e / q4, c4 = 4 * (e - (e / q4) * q4);
+      float y[4], dq[4], dk[4], dg[4], dkg_kg[4], ekv[4];
       KDA_UNROLL
       for (int x = 0; x < 4; ++x) {
-        if (c4 + x >= K) break;
-        float dq = 0.f, dk = 0.f, dg = 0.f, dkg_kg = 0.f, ekv = 0.f;
+        y[x] = f4at(d.y, x);
+        dq[x] = dk[x] = dg[x] = dkg_kg[x] = ekv[x] = 0.f;
         if (i < L) {
           const float gi = f4at(d.gi, x), dqg = f4at(d.dqg, x), dkg = f4at(d.dkg, x);
           const float eg = fexp(gi);
-          dq = dqg * eg;
-          dk = dkg * fexp(f4at(d.gl, x) - gi);
-          dkg_kg = dkg * f4at(d.kg, x);
-          dg = dqg * f4at(d.qg, x) - dkg_kg;
-          ekv = eg * f4at(d.kn, x);
+          dq[x] = dqg * eg;
+          dk[x] = dkg * fexp(f4at(d.gl, x) - gi);
+          dkg_kg[x] = dkg * f4at(d.kg, x);
+          dg[x] = dqg * f4at(d.qg, x) - dkg_kg[x];
+          ekv[x] = eg * f4at(d.kn, x);
         }
-        const size_t o = (size_t)i * K + c4 + x;
-        Y[o] = f4at(d.y, x);
-        dQ[o] = dq;
-        dK[o] = dk;
-        dGam[o] = dg;
-        dKG[o] = dkg_kg;
-        EK[o] = ekv;
       }
+      const size_t o = (size_t)i * K + c4;
+      sts4m(Y + o, y, K - c4, vecK);
+      sts4m(dQ + o, dq, K - c4, vecK);
+      sts4m(dK + o, dk, K - c4, vecK);
+      sts4m(dGam + o, dg, K - c4, vecK);
+      sts4m(dKG + o, dkg_kg, K - c4, vecK);
+      sts4m(EK + o, ekv, K - c4, vecK);
     });
   });
   // X = A^T dV_new, Y = A^T dW: back substitution with (I + Diag(beta) P)^T on shared-memory
@@ -1739,118 +1742,135 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     });
   });
   if (sFlag[0] == 0.f) {
-    // the e^(Gamma_i - Gamma_j) terms of Aqk and P, one thread per (16-row block R, channel
-    // k), for the rows r of block R:
+    // the e^(Gamma_i - Gamma_j) terms of Aqk and P, one thread per (8-row half H of a 16-row
+    // block R, four channels k), for the rows r of H:
     //   s1 = sum_{j<=r} dAqk[r][j] K_j e^(G_r - G_j)   s2 = sum_{j<r} dP[r][j] K_j e^(G_r - G_j)
     //   s3 = sum_{i>=r} dAqk[i][r] Q_i e^(G_i - G_r)   s4 = sum_{i>r} dP[i][r] K_i e^(G_i - G_r)
-    // with e^(G_r - G_j) = e^(G_r - rho_R) e^(rho_R - G_j) and e^(G_i - G_r) =
-    // e^(G_i - rho_I) e^(rho_I - G_r) (I the block of i)
+    // with e^(G_r - G_j) = e^(G_r - rho_R) e^(rho_R - rho_B) e^(rho_B - G_j) (B the block of j)
+    // and e^(G_i - G_r) = e^(G_i - rho_I) e^(rho_I - rho_R) e^(rho_R - G_r) (I the block of i).
+    // A warp's lanes share (R, H) and take consecutive channel quads, so that every dAqk and
+    // dP value a lane loads is one broadcast word serving four channels.
     ex.phase([&](int tid, int nthr) {
-      const int NB = (L + 15) >> 4;
-      for (int u = tid; u < NB * K; u += nthr) {
-        const int R = u / K, kk = u - (u / K) * K;
-        const int r0 = 16 * R;
-        const int mid = (r0 + 7) < L - 1 ? r0 + 7 : L - 1;
-        const float rho = Gam[(size_t)mid * K + kk];
-        float s1[16], s2[16];
+      const int NB = (L + 15) >> 4, q4 = (K + 3) / 4;
+      for (int u = tid; u < NB * 2 * q4; u += nthr) {
+        const int rh = u / q4, k0 = 4 * (u - rh * q4);
+        const int R = rh >> 1, r0 = 16 * R + 8 * (rh & 1);
+        if (r0 >= L) continue;
+        const int nr = L - r0 < 8 ? L - r0 : 8;  // rows r0 .. r0 + nr - 1
+        auto mid = [&](int blk_) { return (16 * blk_ + 7) < L - 1 ? 16 * blk_ + 7 : L - 1; };
+        const F4 rho = ld4w(Gam + (size_t)mid(R) * K, k0, K, vecK);
+        float s[8][4], t[8][4];
 KDA_UNROLL
-        for (int x = 0; x < 16; ++x) { s1[x] = 0.f; s2[x] = 0.f; }
-        const int jend = (r0 + 16 < L ? r0 + 16 : L);
-        // K_j e^(rho_R - Gamma_j) = (K_j e^(rho_B - Gamma_j)) e^(rho_R - rho_B), B = j's block
+        for (int y = 0; y < 8; ++y)
+KDA_UNROLL
+          for (int x = 0; x < 4; ++x) { s[y][x] = 0.f; t[y][x] = 0.f; }
+        const int jend = r0 + nr;  // j <= r for the rows of this half
         for (int B = 0; B <= R; ++B) {
-          const int mb = (16 * B + 7) < L - 1 ? 16 * B + 7 : L - 1;
-          const float fb = B == R ? 1.f : fexp(rho - Gam[(size_t)mb * K + kk]);
+          F4 fb{1.f, 1.f, 1.f, 1.f};
+          if (B < R) {
+            const F4 gb = ld4w(Gam + (size_t)mid(B) * K, k0, K, vecK);
+            fb = F4{fexp(rho.x - gb.x), fexp(rho.y - gb.y), fexp(rho.z - gb.z), fexp(rho.w - gb.w)};
+          }
           const int j1 = 16 * B + 16 < jend ? 16 * B + 16 : jend;
           KDA_UNROLL4
           for (int j = 16 * B; j < j1; ++j) {
-            const float ke = kb_row(j)[kk] * fb;
+            const F4 kv = lds4m(kb_row(j) + k0, K - k0, vecK);
+            const float ke[4] = {kv.x * fb.x, kv.y * fb.y, kv.z * fb.z, kv.w * fb.w};
             const float* da = sdAt + (size_t)j * lda + r0;  // dAqk[r0 ..][j], zero for r < j
             const float* dz = sZt + (size_t)j * lda + r0;   // dP[r0 ..][j], zero for r <= j
+            const F4 a0 = ld4(da), a1 = ld4(da + 4), z0 = ld4(dz), z1 = ld4(dz + 4);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float zv[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
 KDA_UNROLL
-            for (int x = 0; x < 16; x += 4) {
-              const F4 av = ld4(da + x), zv = ld4(dz + x);
-              s1[x] = fmaf(av.x, ke, s1[x]); s1[x + 1] = fmaf(av.y, ke, s1[x + 1]);
-              s1[x + 2] = fmaf(av.z, ke, s1[x + 2]); s1[x + 3] = fmaf(av.w, ke, s1[x + 3]);
-              s2[x] = fmaf(zv.x, ke, s2[x]); s2[x + 1] = fmaf(zv.y, ke, s2[x + 1]);
-              s2[x + 2] = fmaf(zv.z, ke, s2[x + 2]); s2[x + 3] = fmaf(zv.w, ke, s2[x + 3]);
+            for (int y = 0; y < 8; ++y)
+KDA_UNROLL
+              for (int x = 0; x < 4; ++x) {
+                s[y][x] = fmaf(av[y], ke[x], s[y][x]);
+                t[y][x] = fmaf(zv[y], ke[x], t[y][x]);
+              }
+          }
+        }
+        // rows of this half: e^(G_r - rho_R) applied, then dQ += s1, dK += s2,
+        // dGamma += Q s1 + K s2 (the elements belong to this thread alone)
+KDA_UNROLL
+        for (int y0 = 0; y0 < 8; y0 += 2) {
+          F4 gr[2], qv[2], kv[2], dq[2], dk[2], dg[2];
+KDA_UNROLL
+          for (int y = 0; y < 2; ++y) {
+            const size_t o = (size_t)(r0 + (y0 + y < nr ? y0 + y : 0)) * K;
+            gr[y] = ld4w(Gam + o, k0, K, vecK);
+            qv[y] = ld4w(Qn + o, k0, K, vecK); kv[y] = ld4w(Kn + o, k0, K, vecK);
+            dq[y] = ld4w(dQ + o, k0, K, vecK); dk[y] = ld4w(dK + o, k0, K, vecK);
+            dg[y] = ld4w(dGam + o, k0, K, vecK);
+          }
+KDA_UNROLL
+          for (int y = 0; y < 2; ++y) {
+            if (y0 + y >= nr) continue;
+            const size_t o = (size_t)(r0 + y0 + y) * K + k0;
+            float nq[4], nk[4], ng4[4];
+KDA_UNROLL
+            for (int x = 0; x < 4; ++x) {
+              const float f = fexp(f4at(gr[y], x) - f4at(rho, x));
+              const float a1 = s[y0 + y][x] * f, a2 = t[y0 + y][x] * f;
+              nq[x] = f4at(dq[y], x) + a1;
+              nk[x] = f4at(dk[y], x) + a2;
+              ng4[x] = f4at(dg[y], x) + (f4at(qv[y], x) * a1 + f4at(kv[y], x) * a2);
             }
+            sts4m(dQ + o, nq, K - k0, vecK);
+            sts4m(dK + o, nk, K - k0, vecK);
+            sts4m(dGam + o, ng4, K - k0, vecK);
           }
         }
-        // Gamma of the block's rows (also the exponents of the second part)
-        float gr[16];
+        // s3 + s4 (their factors are the same): the rows i of every block I >= R, each row's
+        // Q e^(G - rho_I) and K e^(G - rho_I) scaled by e^(rho_I - rho_R)
 KDA_UNROLL
-        for (int x = 0; x < 16; ++x) gr[x] = r0 + x < L ? Gam[(size_t)(r0 + x) * K + kk] : 0.f;
-        // the (r, k) elements belong to this unit alone; four rows at a time, loads first
+        for (int y = 0; y < 8; ++y)
 KDA_UNROLL
-        for (int x0 = 0; x0 < 16; x0 += 4) {
-          float q8[4], k8[4], dq8[4], dk8[4], dg8[4];
-KDA_UNROLL
-          for (int x = 0; x < 4; ++x) {
-            const int r = r0 + x0 + x;
-            const size_t e = (size_t)(r < L ? r : 0) * K + kk;
-            q8[x] = Qn[e]; k8[x] = Kn[e]; dq8[x] = dQ[e]; dk8[x] = dK[e]; dg8[x] = dGam[e];
-          }
-KDA_UNROLL
-          for (int x = 0; x < 4; ++x) {
-            const int r = r0 + x0 + x;
-            if (r >= L) continue;
-            const size_t e = (size_t)r * K + kk;
-            const float f = fexp(gr[x0 + x] - rho);
-            const float a1 = s1[x0 + x] * f, a2 = s2[x0 + x] * f;
-            dQ[e] = dq8[x] + a1;
-            dK[e] = dk8[x] + a2;
-            dGam[e] = dg8[x] + (q8[x] * a1 + k8[x] * a2);
-          }
-        }
-        float s3[16], s4[16];
-KDA_UNROLL
-        for (int x = 0; x < 16; ++x) { s3[x] = 0.f; s4[x] = 0.f; }
+          for (int x = 0; x < 4; ++x) s[y][x] = 0.f;
         for (int I = R; I < NB; ++I) {
-          const int i0 = 16 * I;
-          const int mi = (i0 + 7) < L - 1 ? i0 + 7 : L - 1;
-          const float rhoI = Gam[(size_t)mi * K + kk];
-          float qf[16], kf[16];
-KDA_UNROLL
-          for (int y = 0; y < 16; ++y) {
-            const bool in = i0 + y < L;
-            qf[y] = in ? QF[(size_t)(i0 + y) * K + kk] : 0.f;
-            kf[y] = in ? KF[(size_t)(i0 + y) * K + kk] : 0.f;
+          F4 fi{1.f, 1.f, 1.f, 1.f};
+          if (I > R) {
+            const F4 gi = ld4w(Gam + (size_t)mid(I) * K, k0, K, vecK);
+            fi = F4{fexp(gi.x - rho.x), fexp(gi.y - rho.y), fexp(gi.z - rho.z), fexp(gi.w - rho.w)};
           }
+          const int ib = 16 * I > r0 ? 16 * I : r0, iend = 16 * I + 16 < L ? 16 * I + 16 : L;
+          KDA_UNROLL4
+          for (int i = ib; i < iend; ++i) {
+            const F4 qf = ld4w(QF + (size_t)i * K, k0, K, vecK), kf = ld4w(KF + (size_t)i * K, k0, K, vecK);
+            const float qe[4] = {qf.x * fi.x, qf.y * fi.y, qf.z * fi.z, qf.w * fi.w};
+            const float ke[4] = {kf.x * fi.x, kf.y * fi.y, kf.z * fi.z, kf.w * fi.w};
 KDA_UNROLL
-          for (int x = 0; x < 16; ++x) {
-            const int r = r0 + x;
-            if (r >= L) continue;
-            float t3 = 0.f, t4 = 0.f;
-            const float* da = sdAt + (size_t)r * lda + i0;  // dAqk[i0 ..][r], zero for i < r
-            const float* dz = sZt + (size_t)r * lda + i0;   // dP[i0 ..][r], zero for i <= r
+            for (int y = 0; y < 8; ++y) {
+              const float dav = sdAt[(size_t)(r0 + y) * lda + i];  // dAqk[i][r], zero for i < r
+              const float dzv = sZt[(size_t)(r0 + y) * lda + i];   // dP[i][r], zero for i <= r
 KDA_UNROLL
-            for (int y = 0; y < 16; y += 4) {
-              const F4 av = ld4(da + y), zv = ld4(dz + y);
-              t3 = fmaf(av.x, qf[y], fmaf(av.y, qf[y + 1], fmaf(av.z, qf[y + 2], fmaf(av.w, qf[y + 3], t3))));
-              t4 = fmaf(zv.x, kf[y], fmaf(zv.y, kf[y + 1], fmaf(zv.z, kf[y + 2], fmaf(zv.w, kf[y + 3], t4))));
+              for (int x = 0; x < 4; ++x) s[y][x] = fmaf(dav, qe[x], fmaf(dzv, ke[x], s[y][x]));
             }
-            const float e = fexp(rhoI - gr[x]);
-            s3[x] = fmaf(e, t3, s3[x]);
-            s4[x] = fmaf(e, t4, s4[x]);
           }
         }
 KDA_UNROLL
-        for (int x0 = 0; x0 < 16; x0 += 8) {
-          float k8[8], dk8[8], dg8[8];
+        for (int y0 = 0; y0 < 8; y0 += 4) {
+          F4 gr[4], kv[4], dk[4], dg[4];
 KDA_UNROLL
-          for (int x = 0; x < 8; ++x) {
-            const int r = r0 + x0 + x;
-            const size_t e = (size_t)(r < L ? r : 0) * K + kk;
-            k8[x] = Kn[e]; dk8[x] = dK[e]; dg8[x] = dGam[e];
+          for (int y = 0; y < 4; ++y) {
+            const size_t o = (size_t)(r0 + (y0 + y < nr ? y0 + y : 0)) * K;
+            gr[y] = ld4w(Gam + o, k0, K, vecK);
+            kv[y] = ld4w(Kn + o, k0, K, vecK); dk[y] = ld4w(dK + o, k0, K, vecK);
+            dg[y] = ld4w(dGam + o, k0, K, vecK);
           }
 KDA_UNROLL
-          for (int x = 0; x < 8; ++x) {
-            const int r = r0 + x0 + x;
-            if (r >= L) continue;
-            const size_t e = (size_t)r * K + kk;
-            const float s34 = s3[x0 + x] + s4[x0 + x];
-            dK[e] = dk8[x] + s34;
-            dGam[e] = dg8[x] - k8[x] * s34;
+          for (int y = 0; y < 4; ++y) {
+            if (y0 + y >= nr) continue;
+            const size_t o = (size_t)(r0 + y0 + y) * K + k0;
+            float nk[4], ng4[4];
+KDA_UNROLL
+            for (int x = 0; x < 4; ++x) {
+              const float s34 = s[y0 + y][x] * fexp(f4at(rho, x) - f4at(gr[y], x));
+              nk[x] = f4at(dk[y], x) + s34;
+              ng4[x] = f4at(dg[y], x) - f4at(kv[y], x) * s34;
+            }
+            sts4m(dK + o, nk, K - k0, vecK);
+            sts4m(dGam + o, ng4, K - k0, vecK);
           }
         }
       }
@@ -2004,12 +2024,18 @@ KDA_UNROLL
       const float mul = r < C ? a.scale : 1.f;
       float* dst = (r < C ? a.dq : a.dk) + ((size_t)(t0 + i) * H + h) * K;
       const float inv = a.qk_l2norm ? sRowF[2 * r] : 0.f, t = a.qk_l2norm ? sRowF[2 * r + 1] : 0.f;
+      float val[4];
       KDA_UNROLL
       for (int x = 0; x < 4; ++x) {
-        if (c4 + x >= K) break;
         const float d = mul * f4at(v.d, x);
-        const float val = a.qk_l2norm ? (d - f4at(v.x, x) * inv * t) * inv : d;
-        if (p.G == 1) dst[c4 + x] = val; else ex.atomic_add(dst + c4 + x, val);
+        val[x] = a.qk_l2norm ? (d - f4at(v.x, x) * inv * t) * inv : d;
+      }
+      if (p.G == 1) {
+        sts4m(dst + c4, val, K - c4, vecK);
+      } else {
+        KDA_UNROLL
+        for (int x = 0; x < 4; ++x)
+          if (c4 + x < K) ex.atomic_add(dst + c4 + x, val[x]);
       }
     });
   });
