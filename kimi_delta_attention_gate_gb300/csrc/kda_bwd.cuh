@@ -211,7 +211,9 @@ inline int64_t state_blocks(const Plan& p) {
 // substitution's columns afterwards; then the exponent-range flag
 KDA_HD size_t prep_region(const Plan& p) {
   const size_t C = (size_t)p.C;
-  const size_t early = 3 * C * (size_t)(p.K + 1), late = C * C + C * (size_t)(p.K + p.V);
+  const size_t NB = (C + 15) / 16;
+  const size_t early = 3 * C * (size_t)(p.K + 1) + (NB + NB * (NB - 1) / 2) * (size_t)p.K;
+  const size_t late = C * C + C * (size_t)(p.K + p.V);
   return early > late ? early : late;
 }
 inline size_t prep_smem(const Plan& p) { return sizeof(float) * (prep_region(p) + 4); }
@@ -535,6 +537,8 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   float* sGam = smem;                   // [C][ldq]
   float* sQn = sGam + (size_t)C * ldq;  // [C][ldq]
   float* sKn = sQn + (size_t)C * ldq;   // [C][ldq]
+  float* sRho = sKn + (size_t)C * ldq;  // [NB][K] Gamma at each 16-row block's middle row
+  float* sF = sRho + (size_t)((C + 15) / 16) * K;  // [NB (NB - 1) / 2][K] e^(rho_I - rho_B), B < I
 
   // gate activation, q and k rows, beta; rows i >= L are zero
   ex.phase([&](int tid, int nthr) {
@@ -605,14 +609,8 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       for (int kk = 0; kk < K; ++kk) row[kk] *= mul;
     }
   });
-  // e^gamma_C; Qg, Kg; the right-hand sides of W and U; the block-referenced operands of Aqk
-  // and P: QF = Q e^(Gamma - rho), KF = K e^(Gamma - rho) (rho: Gamma at the middle row of the
-  // row's 16-row block) and, for every block I, the stacked key rows KI_I[j] = K_j
-  // e^(rho_I - Gamma_j), j < 16 (I + 1), so that Aqk[i][j] = QF_i . KI_I[j] needs no
-  // exponential; any exponent beyond 60 sends the chunk to the direct evaluation
-  float* QFp = blk + b.y;             // [C][K] in the (here unused) gradient slots
-  float* KFp = QFp + (size_t)C * K;   // [C][K]
-  float* KIp = KFp + (size_t)C * K;   // [16 NB (NB + 1) / 2][K]
+  // e^gamma_C; Qg, Kg; the right-hand sides of W and U; the block references rho_B (Gamma at
+  // the middle row of each 16-row block)
   const int NB = (L + 15) >> 4;
   auto mid_row = [&](int B) { return (16 * B + 7) < L - 1 ? 16 * B + 7 : L - 1; };
   ex.phase([&](int tid, int nthr) {
@@ -624,34 +622,30 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       Qn[e] = sQn[o];
       Kn[e] = sKn[o];
     }
-    struct Row { float gi, gl, gm, q, k, be; };
+    for (int u = tid; u < NB * K; u += nthr) {
+      const int B = u / K;
+      sRho[u] = sGam[(size_t)mid_row(B) * ldq + (u - B * K)];
+    }
+    struct Row { float gi, gl, q, k, be; };
     batched<4>(tid, nthr, C * K, [&](int e) {
       const int i = e / K, kk = e - (e / K) * K;
-      Row r{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      Row r{0.f, 0.f, 0.f, 0.f, 0.f};
       if (i < L) {
         const size_t o = (size_t)i * ldq + kk;
-        r = Row{sGam[o], sGam[(size_t)(L - 1) * ldq + kk], sGam[(size_t)mid_row(i >> 4) * ldq + kk],
-                sQn[o], sKn[o], Be[i]};
+        r = Row{sGam[o], sGam[(size_t)(L - 1) * ldq + kk], sQn[o], sKn[o], Be[i]};
       }
       return r;
     }, [&](int e, const Row& r) {
-      float qg = 0.f, kg = 0.f, w = 0.f, qf = 0.f, kf = 0.f;
+      float qg = 0.f, kg = 0.f, w = 0.f;
       if (e / K < L) {
         const float eg = fexp(r.gi);
         qg = r.q * eg;
         kg = r.k * fexp(r.gl - r.gi);
         w = r.be * eg * r.k;
-        const float rel = r.gi - r.gm;
-        if (rel > 60.f) ex.atomic_add(sFlag, 1.f);
-        const float f = fexp(rel);
-        qf = r.q * f;
-        kf = r.k * f;
       }
       Qg[e] = qg;
       Kg[e] = kg;
       W[e] = w;
-      QFp[e] = qf;
-      KFp[e] = kf;
     });
     const int v4 = (V + 3) / 4;
     batched<4>(tid, nthr, C * v4, [&](int e) {  // four columns of v per element
@@ -668,53 +662,65 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
         for (int y = 0; y < 4 && c4 + y < V; ++y) U[(size_t)i * V + c4 + y] = u[y];
       }
     });
-    // stacked rows of KI; block I's rows start at 8 I (I + 1): 0, 16, 48, 96
-    batched<8>(tid, nthr, 8 * NB * (NB + 1) * K, [&](int e) {
-      const int row = e / K, kk = e - (e / K) * K;
-      const int I = row >= 96 ? 3 : (row >= 48 ? 2 : (row >= 16 ? 1 : 0));
-      const int j = row - 8 * I * (I + 1);
-      F4 v{0.f, 0.f, 0.f, 0.f};  // Gamma at block I's middle row, Gamma_j, K_j
-      if (j < L) {
-        v.x = sGam[(size_t)mid_row(I) * ldq + kk];
-        v.y = sGam[(size_t)j * ldq + kk];
-        v.z = sKn[(size_t)j * ldq + kk];
-        v.w = 1.f;
-      }
-      return v;
-    }, [&](int e, const F4& v) {
-      float kv = 0.f;
-      if (v.w != 0.f) {
-        const float ex_ = v.x - v.y;
-        if (ex_ > 60.f) ex.atomic_add(sFlag, 1.f);
-        kv = v.z * fexp(ex_);
-      }
-      KIp[e] = kv;
-    });
+  });
+  // The block-referenced operands of Aqk and P, in place in shared memory: QF = Q e^(Gamma -
+  // rho_B), KF = K e^(Gamma - rho_B) and KB = K e^(rho_B - Gamma) (B the row's block), and
+  // F_IB = e^(rho_I - rho_B) for B < I, so that Aqk[i][j] = sum_k QF_i KB_j F_IB and P[i][j] =
+  // sum_k KF_i KB_j F_IB with I, B the blocks of i, j need no exponential per (i, j, k).  Any
+  // exponent beyond 60 (QF, KB, F, or the product KB F = K e^(rho_I - Gamma_j)) sends the
+  // chunk to the direct evaluation.
+  ex.phase([&](int tid, int nthr) {
+    for (int u = tid; u < (NB * (NB - 1) / 2) * K; u += nthr) {
+      const int pr = u / K, kk = u - pr * K;
+      const int I = pr >= 3 ? (pr >= 6 ? 4 : 3) : (pr >= 1 ? 2 : 1);  // pr = I (I - 1) / 2 + B
+      const int B = pr - I * (I - 1) / 2;
+      const float d = sRho[(size_t)I * K + kk] - sRho[(size_t)B * K + kk];
+      if (d > 60.f) ex.atomic_add(sFlag, 1.f);
+      sF[u] = fexp(d);
+    }
+    for (int e = tid; e < L * K; e += nthr) {
+      const int i = e / K, kk = e - (e / K) * K, B = i >> 4;
+      const size_t o = (size_t)i * ldq + kk;
+      const float g = sGam[o], rho = sRho[(size_t)B * K + kk];
+      bool bad = g - rho > 60.f;
+      for (int I = B; I < NB; ++I) bad = bad || sRho[(size_t)I * K + kk] - g > 60.f;
+      if (bad) ex.atomic_add(sFlag, 1.f);
+      const float f = fexp(g - rho), kv = sKn[o];
+      sQn[o] *= f;
+      sKn[o] = kv * f;
+      sGam[o] = kv * fexp(rho - g);
+    }
   });
   const int CB = C / 4;
   if (sFlag[0] == 0.f) {
-    // Aqk (j <= i) and P (j < i) in 4 x 4 blocks: rows i of one 16-row block I, keys j
+    // Aqk (j <= i) and P (j < i) in 4 x 4 blocks: rows i of one 16-row block I, keys j of
+    // block B, over the channels of the shared-memory operands
     ex.phase([&](int tid, int nthr) {
       for (int u = tid; u < CB * CB; u += nthr) {
         const int ib = u / CB, jb = u - (u / CB) * CB;
         float aq[4][4] = {}, ak[4][4] = {};
         if (jb <= ib && 4 * ib < L) {
-          const int I = (4 * ib) >> 4;
-          const float* KI = KIp + (size_t)(8 * I * (I + 1)) * K;
-#if defined(__CUDA_ARCH__)
-#pragma unroll 2
-#endif
-          for (int kk = 0; kk < pad4(K); kk += 4) {
-            F4 qf[4], kf[4], kj[4];
+          const int I = ib >> 2, B = jb >> 2;
+          const float* fr = sF + (size_t)(B < I ? I * (I - 1) / 2 + B : 0) * K;
+          const float* qr = sQn + (size_t)(4 * ib) * ldq;
+          const float* kr = sKn + (size_t)(4 * ib) * ldq;
+          const float* br = sGam + (size_t)(4 * jb) * ldq;
+          KDA_UNROLL4
+          for (int kk = 0; kk < K; ++kk) {
+            const float f = B < I ? fr[kk] : 1.f;
+            float qf[4], kf[4], kb[4];
+            KDA_UNROLL
             for (int y = 0; y < 4; ++y) {
-              qf[y] = ld4w(QFp + (size_t)(4 * ib + y) * K, kk, K, vecK);
-              kf[y] = ld4w(KFp + (size_t)(4 * ib + y) * K, kk, K, vecK);
-              kj[y] = ld4w(KI + (size_t)(4 * jb + y) * K, kk, K, vecK);
+              qf[y] = qr[(size_t)y * ldq + kk];
+              kf[y] = kr[(size_t)y * ldq + kk];
+              kb[y] = br[(size_t)y * ldq + kk] * f;
             }
+            KDA_UNROLL
             for (int y = 0; y < 4; ++y)
+              KDA_UNROLL
               for (int x = 0; x < 4; ++x) {
-                aq[y][x] += dot4(qf[y], kj[x]);
-                ak[y][x] += dot4(kf[y], kj[x]);
+                aq[y][x] = fmaf(qf[y], kb[x], aq[y][x]);
+                ak[y][x] = fmaf(kf[y], kb[x], ak[y][x]);
               }
           }
         }
