@@ -78,7 +78,7 @@ constexpr size_t kTileQg = 81920;     // hi at +81920, lo at +98304
 struct Block {
   size_t gam, qn, kn, qg, kg, w, y, dq, dk, dgam, dkg;  // [C][K]
   size_t u, vn, dvn, x;                                  // [C][V]
-  size_t aqk, p;                                         // [C][C]
+  size_t aqk, p, ati;                                    // [C][C]
   size_t beta, decay;                                    // [C], [K]
   size_t floats;                                         // a multiple of 64 (256 bytes)
 };
@@ -104,6 +104,7 @@ KDA_HD Block block_layout(int C, int K, int V) {
   b.x = o; o += cv;     // X = A^T dV_new
   b.aqk = o; o += cc;   // Aqk
   b.p = o; o += cc;     // P (strictly lower, without beta)
+  b.ati = o; o += cc;   // A^T, A = (I + Diag(beta) P)^-1 (rows and columns >= L zero)
   b.beta = o; o += C;
   b.decay = o; o += K;  // e^gamma_C
   b.floats = (o + 63) / 64 * 64;
@@ -213,7 +214,7 @@ KDA_HD size_t prep_region(const Plan& p) {
   const size_t C = (size_t)p.C;
   const size_t NB = (C + 15) / 16;
   const size_t early = 3 * C * (size_t)(p.K + 1) + (NB + NB * (NB - 1) / 2) * (size_t)p.K;
-  const size_t late = C * C + C * (size_t)(p.K + p.V);
+  const size_t late = C * C + C * (C + 4) + C * (size_t)(p.K + p.V);
   return early > late ? early : late;
 }
 inline size_t prep_smem(const Plan& p) { return sizeof(float) * (prep_region(p) + 4); }
@@ -756,41 +757,48 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       }
     });
   }
-  // W and U: forward substitution with (I + Diag(beta) P) on shared-memory columns
+  // A = (I + Diag(beta) P)^-1 by forward substitution on the identity's columns, blocked by 16
+  // rows; then W = A (beta e^Gamma K) and U = A (beta V) as one dense product over the
+  // right-hand sides in shared memory; A^T goes to the workspace for the gradient stage
+  const int ldA = C + 4;              // 16-byte rows; the transposed walk is a 4-way conflict
   float* sP = smem;                   // [C][C] beta_i P_ij
-  float* sX = sP + (size_t)C * C;     // [C][K + V] the right-hand sides, then the solutions
-  const int ncol = K + V;
+  float* sA = sP + (size_t)C * C;     // [C][ldA] the identity, then A
+  float* sX = sA + (size_t)C * ldA;   // [C][K + V] the right-hand sides of W and U
+  const int nrhs = K + V;
   ex.phase([&](int tid, int nthr) {
     batched<8>(tid, nthr, C * C, [&](int e) { return Be[e / C] * P[e]; }, [&](int e, float v) { sP[e] = v; });
-    batched<8>(tid, nthr, C * ncol, [&](int e) {
-      const int i = e / ncol, col = e - (e / ncol) * ncol;
+    for (int e = tid; e < C * ldA; e += nthr) {
+      const int i = e / ldA, cc = e - (e / ldA) * ldA;
+      sA[e] = cc == i ? 1.f : 0.f;
+    }
+    batched<8>(tid, nthr, C * nrhs, [&](int e) {
+      const int i = e / nrhs, col = e - (e / nrhs) * nrhs;
       return col < K ? W[(size_t)i * K + col] : U[(size_t)i * V + col - K];
     }, [&](int e, float v) { sX[e] = v; });
   });
-  // blocked by 16 rows: each block's rows solved within the block (one thread per column),
-  // then the later rows updated with the block's solution in 4 x 4 tiles (every thread)
+  // each block's rows solved within the block (one thread per column), then the later rows
+  // updated with the block's solution in 4 x 4 tiles (every thread)
   for (int J = 0; J * 16 < L; ++J) {
     const int j0 = 16 * J, jend = j0 + 16 < L ? j0 + 16 : L;
     ex.phase([&](int tid, int nthr) {
-      for (int col = tid; col < ncol; col += nthr) {
+      for (int col = tid; col < jend; col += nthr) {  // A is lower triangular: columns < jend
         for (int i = j0 + 1; i < jend; ++i) {
           const float* pr = sP + (size_t)i * C;
-          float x = sX[(size_t)i * ncol + col];
-          for (int j = j0; j < i; ++j) x = fmaf(-pr[j], sX[(size_t)j * ncol + col], x);
-          sX[(size_t)i * ncol + col] = x;
+          float x = sA[(size_t)i * ldA + col];
+          for (int j = j0; j < i; ++j) x = fmaf(-pr[j], sA[(size_t)j * ldA + col], x);
+          sA[(size_t)i * ldA + col] = x;
         }
       }
     });
     if (jend >= L) break;
     ex.phase([&](int tid, int nthr) {
-      const int nr4 = (L - jend + 3) / 4, nc4 = (ncol + 3) / 4;
-      const bool vec = (ncol & 3) == 0;  // 16-byte rows: one load per four columns
+      const int nr4 = (L - jend + 3) / 4, nc4 = jend / 4;  // columns >= jend are still zero
       for (int u = tid; u < nr4 * nc4; u += nthr) {
         const int i0 = jend + 4 * (u / nc4), c0 = 4 * (u - (u / nc4) * nc4);
         float acc[4][4];
         KDA_UNROLL
         for (int y = 0; y < 4; ++y) {
-          const F4 v = lds4m(sX + (size_t)(i0 + y) * ncol + c0, i0 + y < L ? ncol - c0 : 0, vec);
+          const F4 v = ld4(sA + (size_t)(i0 + y) * ldA + c0);
           KDA_UNROLL
           for (int x = 0; x < 4; ++x) acc[y][x] = f4at(v, x);
         }
@@ -798,7 +806,7 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
           float pv[4];
           KDA_UNROLL
           for (int y = 0; y < 4; ++y) pv[y] = i0 + y < L ? sP[(size_t)(i0 + y) * C + j] : 0.f;
-          const F4 xv = lds4m(sX + (size_t)j * ncol + c0, ncol - c0, vec);
+          const F4 xv = ld4(sA + (size_t)j * ldA + c0);
           KDA_UNROLL
           for (int y = 0; y < 4; ++y)
             KDA_UNROLL
@@ -806,23 +814,67 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
         }
         KDA_UNROLL
         for (int y = 0; y < 4; ++y)
-          if (i0 + y < L) sts4m(sX + (size_t)(i0 + y) * ncol + c0, acc[y], ncol - c0, vec);
+          if (i0 + y < L) st4(sA + (size_t)(i0 + y) * ldA + c0, acc[y]);
       }
     });
   }
+  // [W | U] = A [beta e^Gamma K | beta V]: 4 x 4 tiles of (rows i, columns), sums over j <= i;
+  // a warp's lanes share the row tile (the A words are broadcasts) and take consecutive column
+  // quads; thread t pairs row tiles t' and CB - 1 - t' (long and short sums)
   ex.phase([&](int tid, int nthr) {
-    KDA_UNROLL4
-    for (int e = tid; e < C * ncol; e += nthr) {
-      const int i = e / ncol, col = e - (e / ncol) * ncol;
-      if (col < K) W[(size_t)i * K + col] = sX[e];
-      else U[(size_t)i * V + col - K] = sX[e];
+    const int nc4 = (nrhs + 3) / 4, CB4 = C / 4;
+    const bool vec = (nrhs & 3) == 0;
+    for (int u = tid; u < CB4 * nc4; u += nthr) {
+      const int t = u / nc4, c0 = 4 * (u - t * nc4);
+      const int ib = t < CB4 / 2 ? t : (CB4 + CB4 / 2 - 1 - t);
+      const int r0 = 4 * ib;
+      float acc[4][4];
+      KDA_UNROLL
+      for (int y = 0; y < 4; ++y)
+        KDA_UNROLL
+        for (int x = 0; x < 4; ++x) acc[y][x] = 0.f;
+      const int jend = r0 + 4 < L ? r0 + 4 : L;
+      KDA_UNROLL4
+      for (int j = 0; j < jend; ++j) {
+        float av[4];
+        KDA_UNROLL
+        for (int y = 0; y < 4; ++y) av[y] = r0 + y < L ? sA[(size_t)(r0 + y) * ldA + j] : 0.f;
+        const F4 xv = lds4m(sX + (size_t)j * nrhs + c0, nrhs - c0, vec);
+        KDA_UNROLL
+        for (int y = 0; y < 4; ++y)
+          KDA_UNROLL
+          for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(av[y], f4at(xv, x), acc[y][x]);
+      }
+      const bool whole = c0 + 4 <= nrhs;
+      KDA_UNROLL
+      for (int y = 0; y < 4; ++y) {
+        const size_t i = (size_t)(r0 + y);
+        if (whole && c0 + 4 <= K && vecK) {
+          st4(W + i * K + c0, acc[y]);
+        } else if (whole && c0 >= K && vecV && ((c0 - K) & 3) == 0) {
+          st4(U + i * V + (c0 - K), acc[y]);
+        } else {
+          for (int x = 0; x < 4 && c0 + x < nrhs; ++x) {
+            const int col = c0 + x;
+            if (col < K) W[i * K + col] = acc[y][x];
+            else U[i * V + col - K] = acc[y][x];
+          }
+        }
+      }
+    }
+  });
+  ex.phase([&](int tid, int nthr) {
+    float* ATi = blk + b.ati;  // ATi[c][i] = A[i][c]
+    for (int e = tid; e < C * C; e += nthr) {
+      const int cc = e / C, i = e - (e / C) * C;
+      ATi[e] = (i < L && cc < L) ? sA[(size_t)i * ldA + cc] : 0.f;
     }
     if (p.tc_states) {  // the tensor-core state stage's operand tiles (K = 128, C = 64)
       char* tile = tile_ptr(a, c, hv);
       for (int u = tid; u < C * (K / 8); u += nthr) {  // -W: row = token, 8 channels per chunk
         const int i = u / (K / 8), k0 = 8 * (u - (u / (K / 8)) * (K / 8));
         float x[8];
-        for (int j = 0; j < 8; ++j) x[j] = -sX[(size_t)i * ncol + k0 + j];
+        for (int j = 0; j < 8; ++j) x[j] = -W[(size_t)i * K + k0 + j];
         put_hilo8(tile, kTileNegW + (size_t)(k0 >> 6) * 8192 + swz128((uint32_t)i, (uint32_t)(k0 & 63)), x);
       }
       for (int u = tid; u < K * (C / 8); u += nthr) {  // Kg^T: row = channel, 8 tokens per chunk
@@ -1261,6 +1313,7 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   const float* P = blk + b.p;
   const float* Be = blk + b.beta;
   const float* Dc = blk + b.decay;
+  const float* ATi = blk + b.ati;
   float* Y = blk + b.y;
   float* X = blk + b.x;
   float* dQ = blk + b.dq;
@@ -1281,7 +1334,8 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   float* sFlag = sRed + kThreads;             // [4] > 0: some block exponent out of range
   float* sDgc = sFlag + 4;                    // [K4] diagonal of S dS'^T
   float* sRg = sDgc + pad4(K);                // the product slices' staging, then:
-  float* sAk = sRg;                           // [C][C] beta_i P_ij
+  float* sAt = sRg;                           // [C][C] A^T: sAt[j][i] = A[i][j]
+  float* sAk = sRg;                           // the same region, for the key rows later
   float* sZ = sAk + (size_t)C * C;            // [C][ldz] A^T dA, then A^T dA A^T, then dP
   float* sT = sZ + (size_t)C * ldz;           // scratch (grads_scratch floats)
   float* sXY = sT;                            // [C][(V + K + 1) / 2] back substitution columns
@@ -1444,7 +1498,7 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   // element: four consecutive channels of a row (one 16-byte load per array when K % 4 == 0)
   struct Direct { F4 gi, gl, dqg, dkg, y, kg, qg, kn; };
   ex.phase([&](int tid, int nthr) {
-    batched<8>(tid, nthr, C * C, [&](int e) { return Be[e / C] * P[e]; }, [&](int e, float v) { sAk[e] = v; });
+    batched<8>(tid, nthr, C * C, [&](int e) { return ATi[e]; }, [&](int e, float v) { sAt[e] = v; });
     const int q4 = (K + 3) / 4;
     batched<2>(tid, nthr, C * q4, [&](int e) {
       const int i = e / q4, c4 = 4 * (e - (e / q4) * q4);
@@ -1483,11 +1537,11 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
       sts4m(EK + o, ekv, K - c4, vecK);
     });
   });
-  // X = A^T dV_new, Y = A^T dW: back substitution with (I + Diag(beta) P)^T on shared-memory
-  // columns, in two halves of the V + K columns, blocked by 16 rows from the last block up:
-  // each block's rows solved within the block (one thread per column), then the rows above it
-  // updated with the block's solution in 4 x 4 tiles (every thread)
-  const int NBr = (L + 15) >> 4;
+  // X = A^T dV_new, Y = A^T dW with A^T from the recompute stage (sAt): dense products over
+  // the rows j >= i (A^T is upper triangular), in two halves of the V + K columns staged in
+  // shared memory, 4 x 4 tiles of (rows, columns); a warp's lanes share the row tile (the A^T
+  // words are broadcasts) and take consecutive column quads.  Thread t takes row tiles t' and
+  // CB - 1 - t' of its two items, so that the long and short sums pair up.
   for (int part = 0; part < 2; ++part) {
     const int cbeg = part == 0 ? 0 : half_cols, cnt = part == 0 ? half_cols : ncol - half_cols;
     ex.phase([&](int tid, int nthr) {
@@ -1496,48 +1550,46 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
         return col < V ? (i < L ? dVn[(size_t)i * V + col] : 0.f) : Y[(size_t)i * K + col - V];
       }, [&](int e, float v) { sXY[e] = v; });
     });
-    for (int B = NBr - 1; B >= 0; --B) {
-      const int r0 = 16 * B, rend = r0 + 16 < L ? r0 + 16 : L;
-      ex.phase([&](int tid, int nthr) {  // rows r0 .. rend - 1 within the block
-        for (int cl = tid; cl < cnt; cl += nthr) {
-          for (int i = rend - 2; i >= r0; --i) {
-            float x = sXY[(size_t)i * cnt + cl];
-            for (int j = i + 1; j < rend; ++j) x = fmaf(-sAk[(size_t)j * C + i], sXY[(size_t)j * cnt + cl], x);
-            sXY[(size_t)i * cnt + cl] = x;
-          }
-        }
-      });
-      if (B == 0) break;
-      ex.phase([&](int tid, int nthr) {  // rows 0 .. r0 - 1 minus the block's contribution
-        const int nct4 = (cnt + 3) / 4;
-        const bool vec = (cnt & 3) == 0;  // 16-byte rows: one load per four columns
-        for (int u = tid; u < (r0 / 4) * nct4; u += nthr) {
-          const int i0 = 4 * (u / nct4), c0 = 4 * (u - (u / nct4) * nct4);
-          float acc[4][4];
-          KDA_UNROLL
-          for (int y = 0; y < 4; ++y) {
-            const F4 v = lds4m(sXY + (size_t)(i0 + y) * cnt + c0, cnt - c0, vec);
-            KDA_UNROLL
-            for (int x = 0; x < 4; ++x) acc[y][x] = f4at(v, x);
-          }
-          for (int j = r0; j < rend; ++j) {
-            const F4 av = ld4(sAk + (size_t)j * C + i0);  // C is a multiple of 4
-            const F4 xv = lds4m(sXY + (size_t)j * cnt + c0, cnt - c0, vec);
-            KDA_UNROLL
-            for (int y = 0; y < 4; ++y)
-              KDA_UNROLL
-              for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(-f4at(av, y), f4at(xv, x), acc[y][x]);
-          }
-          KDA_UNROLL
-          for (int y = 0; y < 4; ++y) sts4m(sXY + (size_t)(i0 + y) * cnt + c0, acc[y], cnt - c0, vec);
-        }
-      });
-    }
     ex.phase([&](int tid, int nthr) {
-      for (int e = tid; e < C * cnt; e += nthr) {
-        const int i = e / cnt, col = cbeg + (e - (e / cnt) * cnt);
-        if (col < V) X[(size_t)i * V + col] = sXY[e];
-        else Y[(size_t)i * K + col - V] = sXY[e];
+      const int nc4 = (cnt + 3) / 4;
+      const bool vec = (cnt & 3) == 0;  // 16-byte rows: one load per four columns
+      for (int u = tid; u < CB * nc4; u += nthr) {
+        const int t = u / nc4, c0 = 4 * (u - t * nc4);
+        const int ib = t < CB / 2 ? t : (CB + CB / 2 - 1 - t);
+        const int r0 = 4 * ib;  // rows >= L come out zero (A^T's rows >= L are zero)
+        float acc[4][4];
+        KDA_UNROLL
+        for (int y = 0; y < 4; ++y)
+          KDA_UNROLL
+          for (int x = 0; x < 4; ++x) acc[y][x] = 0.f;
+        KDA_UNROLL4
+        for (int j = r0; j < L; ++j) {
+          float av[4];
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y) av[y] = sAt[(size_t)(r0 + y) * C + j];
+          const F4 xv = lds4m(sXY + (size_t)j * cnt + c0, cnt - c0, vec);
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y)
+            KDA_UNROLL
+            for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(av[y], f4at(xv, x), acc[y][x]);
+        }
+        const int col0 = cbeg + c0;
+        KDA_UNROLL
+        for (int y = 0; y < 4; ++y) {
+          const size_t i = (size_t)(r0 + y);
+          const bool whole = c0 + 4 <= cnt;
+          if (whole && col0 + 4 <= V && vecV && (col0 & 3) == 0) {
+            st4(X + i * V + col0, acc[y]);
+          } else if (whole && col0 >= V && vecK && ((col0 - V) & 3) == 0) {
+            st4(Y + i * K + (col0 - V), acc[y]);
+          } else {
+            for (int x = 0; x < 4 && c0 + x < cnt; ++x) {
+              const int col = col0 + x;
+              if (col < V) X[i * V + col] = acc[y][x];
+              else Y[i * K + col - V] = acc[y][x];
+            }
+          }
+        }
       }
     });
   }
@@ -1625,62 +1677,46 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
       }
     });
   }
-  // dAkk = -(A^T dA A^T) masked strictly lower (row r of A^T dA A^T is A applied to row r of
-  // A^T dA: forward substitution along every row, entries i < r, blocked by 16 columns: each
-  // block solved within itself (one thread per row), then the later columns updated with it in
-  // 4 x 4 tiles of (rows, columns)); dP = beta dAkk; dbeta += rowsum(dAkk P).  A row's
-  // entries i >= r are zero throughout, so the updates need no mask on the summed columns.
-  for (int J = 0; J < NBr; ++J) {
-    const int j0 = 16 * J, jend = j0 + 16 < L ? j0 + 16 : L;
-    ex.phase([&](int tid, int nthr) {
-      for (int r = tid; r < L; r += nthr) {
-        float* z = sZ + (size_t)r * ldz;
-        const int iend = jend < r ? jend : r;
-        for (int i = j0 + 1; i < iend; ++i) {
-          const float* ar = sAk + (size_t)i * C;
-          float x = z[i];
-          for (int j = j0; j < i; ++j) x = fmaf(-ar[j], z[j], x);
-          z[i] = x;
-        }
-      }
-    });
-    if (jend >= L) break;
-    ex.phase([&](int tid, int nthr) {  // columns jend .. L - 1 of every row minus block J's part
-      const int nr4 = (L + 3) / 4, ni4 = (L - jend + 3) / 4;
-      for (int u = tid; u < nr4 * ni4; u += nthr) {  // a warp's lanes: one column tile, many rows
-        const int i0 = jend + 4 * (u / nr4), r0 = 4 * (u - (u / nr4) * nr4);
-        float acc[4][4];
+  // dAkk = -(A^T dA A^T) masked strictly lower: M[r][i] = sum_j Z[r][j] A[i][j] for i < r with
+  // Z = A^T dA (sZ, strictly lower) and A lower triangular, so j < min(r, i + 1); 4 x 4 tiles
+  // of (rows r, columns i), a warp's lanes taking consecutive column tiles of one row tile
+  // (the Z words are broadcasts, the A^T rows 16-byte loads), into sM.  Then dP = beta dAkk
+  // (into sZ) and dbeta += rowsum(dAkk P).
+  float* sM = sT;  // [C][ldz]
+  ex.phase([&](int tid, int nthr) {
+    for (int u = tid; u < CB * CB; u += nthr) {
+      const int rb = u / CB, ib = u - rb * CB;
+      if (ib > rb || 4 * rb >= L) continue;
+      float acc[4][4];
+      KDA_UNROLL
+      for (int y = 0; y < 4; ++y)
+        KDA_UNROLL
+        for (int x = 0; x < 4; ++x) acc[y][x] = 0.f;
+      const int jend = 4 * ib + 4 < L ? 4 * ib + 4 : L;
+      KDA_UNROLL4
+      for (int j = 0; j < jend; ++j) {
+        float zv[4];
+        KDA_UNROLL
+        for (int y = 0; y < 4; ++y) zv[y] = sZ[(size_t)(4 * rb + y) * ldz + j];
+        const F4 av = ld4(sAt + (size_t)j * C + 4 * ib);  // A[4 ib ..][j]
         KDA_UNROLL
         for (int y = 0; y < 4; ++y)
           KDA_UNROLL
-          for (int x = 0; x < 4; ++x) acc[y][x] = sZ[(size_t)(r0 + y) * ldz + i0 + x];
-        for (int j = j0; j < jend; ++j) {
-          float zv[4], av[4];
-          KDA_UNROLL
-          for (int y = 0; y < 4; ++y) zv[y] = sZ[(size_t)(r0 + y) * ldz + j];
-          KDA_UNROLL
-          for (int x = 0; x < 4; ++x) av[x] = i0 + x < C ? sAk[(size_t)(i0 + x) * C + j] : 0.f;
-          KDA_UNROLL
-          for (int y = 0; y < 4; ++y)
-            KDA_UNROLL
-            for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(-av[x], zv[y], acc[y][x]);
-        }
-        KDA_UNROLL
-        for (int y = 0; y < 4; ++y)
-          KDA_UNROLL
-          for (int x = 0; x < 4; ++x) {
-            const int r = r0 + y, i = i0 + x;
-            if (r < L && i < r) sZ[(size_t)r * ldz + i] = acc[y][x];
-          }
+          for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(zv[y], f4at(av, x), acc[y][x]);
       }
-    });
-  }
+      KDA_UNROLL
+      for (int y = 0; y < 4; ++y)
+        KDA_UNROLL
+        for (int x = 0; x < 4; ++x) sM[(size_t)(4 * rb + y) * ldz + 4 * ib + x] = acc[y][x];
+    }
+  });
   ex.phase([&](int tid, int nthr) {
     for (int r = tid; r < L; r += nthr) {
       float* z = sZ + (size_t)r * ldz;
+      const float* m = sM + (size_t)r * ldz;
       float db = 0.f;
       for (int i = 0; i < r; ++i) {
-        const float d = -z[i];
+        const float d = -m[i];
         db = fmaf(d, P[(size_t)r * C + i], db);
         z[i] = sB[r] * d;
       }
