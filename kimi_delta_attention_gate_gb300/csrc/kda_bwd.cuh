@@ -610,8 +610,8 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       for (int kk = 0; kk < K; ++kk) row[kk] *= mul;
     }
   });
-  // e^gamma_C; Qg, Kg; the right-hand sides of W and U; the block references rho_B (Gamma at
-  // the middle row of each 16-row block)
+  // e^gamma_C; Qg, Kg; the right-hand side of W; the block references rho_B (Gamma at the
+  // middle row of each 16-row block)
   const int NB = (L + 15) >> 4;
   auto mid_row = [&](int B) { return (16 * B + 7) < L - 1 ? 16 * B + 7 : L - 1; };
   ex.phase([&](int tid, int nthr) {
@@ -647,21 +647,6 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       Qg[e] = qg;
       Kg[e] = kg;
       W[e] = w;
-    });
-    const int v4 = (V + 3) / 4;
-    batched<4>(tid, nthr, C * v4, [&](int e) {  // four columns of v per element
-      const int i = e / v4, c4 = 4 * (e - (e / v4) * v4);
-      return i < L ? ld4i(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V, c4, V, vecV)
-                   : F4{0.f, 0.f, 0.f, 0.f};
-    }, [&](int e, const F4& x) {
-      const int i = e / v4, c4 = 4 * (e - (e / v4) * v4);
-      const float b = i < L ? Be[i] : 0.f;
-      const float u[4] = {b * x.x, b * x.y, b * x.z, b * x.w};
-      if (vecV) {
-        st4(U + (size_t)i * V + c4, u);
-      } else {
-        for (int y = 0; y < 4 && c4 + y < V; ++y) U[(size_t)i * V + c4 + y] = u[y];
-      }
     });
   });
   // The block-referenced operands of Aqk and P, in place in shared memory: QF = Q e^(Gamma -
@@ -771,10 +756,19 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       const int i = e / ldA, cc = e - (e / ldA) * ldA;
       sA[e] = cc == i ? 1.f : 0.f;
     }
-    batched<8>(tid, nthr, C * nrhs, [&](int e) {
-      const int i = e / nrhs, col = e - (e / nrhs) * nrhs;
-      return col < K ? W[(size_t)i * K + col] : U[(size_t)i * V + col - K];
-    }, [&](int e, float v) { sX[e] = v; });
+    batched<8>(tid, nthr, C * K, [&](int e) { return W[e]; }, [&](int e, float v) {
+      sX[(size_t)(e / K) * nrhs + (e - (e / K) * K)] = v;
+    });
+    const int v4 = (V + 3) / 4;
+    batched<4>(tid, nthr, C * v4, [&](int e) {  // beta V, four columns of v per element
+      const int i = e / v4, c4 = 4 * (e - (e / v4) * v4);
+      return i < L ? ld4i(a.v, a.dtype, ((size_t)(t0 + i) * HV + hv) * V, c4, V, vecV)
+                   : F4{0.f, 0.f, 0.f, 0.f};
+    }, [&](int e, const F4& x) {
+      const int i = e / v4, c4 = 4 * (e - (e / v4) * v4);
+      const float bt = i < L ? Be[i] : 0.f;
+      for (int y = 0; y < 4 && c4 + y < V; ++y) sX[(size_t)i * nrhs + K + c4 + y] = bt * f4at(x, y);
+    });
   });
   // each block's rows solved within the block (one thread per column), then the later rows
   // updated with the block's solution in 4 x 4 tiles (every thread)
@@ -1496,27 +1490,26 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   }
   // the direct terms of dQg, dW, dKg; e^Gamma K for the A^T dA product
   // element: four consecutive channels of a row (one 16-byte load per array when K % 4 == 0)
-  struct Direct { F4 gi, gl, dqg, dkg, y, kg, qg, kn; };
+  struct Direct { F4 gi, gl, dqg, dkg, kg, qg, kn; };
   ex.phase([&](int tid, int nthr) {
     batched<8>(tid, nthr, C * C, [&](int e) { return ATi[e]; }, [&](int e, float v) { sAt[e] = v; });
     const int q4 = (K + 3) / 4;
     batched<2>(tid, nthr, C * q4, [&](int e) {
       const int i = e / q4, c4 = 4 * (e - (e / q4) * q4);
       const F4 z{0.f, 0.f, 0.f, 0.f};
-      Direct d{z, z, z, z, z, z, z, z};
+      Direct d{z, z, z, z, z, z, z};
       if (i < L) {
         const size_t r = (size_t)i * K;
         d = Direct{ld4w(Gam + r, c4, K, vecK), ld4w(Gam + (size_t)(L - 1) * K, c4, K, vecK),
-                   ld4w(dQ + r, c4, K, vecK), ld4w(dK + r, c4, K, vecK), ld4w(Y + r, c4, K, vecK),
+                   ld4w(dQ + r, c4, K, vecK), ld4w(dK + r, c4, K, vecK),
                    ld4w(Kg + r, c4, K, vecK), ld4w(Qg + r, c4, K, vecK), ld4w(Kn + r, c4, K, vecK)};
       }
       return d;
     }, [&](int e, const Direct& d) {
       const int i = e / q4, c4 = 4 * (e - (e / q4) * q4);
-      float y[4], dq[4], dk[4], dg[4], dkg_kg[4], ekv[4];
+      float dq[4], dk[4], dg[4], dkg_kg[4], ekv[4];
       KDA_UNROLL
       for (int x = 0; x < 4; ++x) {
-        y[x] = f4at(d.y, x);
         dq[x] = dk[x] = dg[x] = dkg_kg[x] = ekv[x] = 0.f;
         if (i < L) {
           const float gi = f4at(d.gi, x), dqg = f4at(d.dqg, x), dkg = f4at(d.dkg, x);
@@ -1529,7 +1522,7 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
         }
       }
       const size_t o = (size_t)i * K + c4;
-      sts4m(Y + o, y, K - c4, vecK);
+      if (i >= L) sts4m(Y + o, dq, K - c4, vecK);  // rows past the chunk's end: zero
       sts4m(dQ + o, dq, K - c4, vecK);
       sts4m(dK + o, dk, K - c4, vecK);
       sts4m(dGam + o, dg, K - c4, vecK);
@@ -1573,40 +1566,71 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
             KDA_UNROLL
             for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(av[y], f4at(xv, x), acc[y][x]);
         }
+        // X and dv = beta X; Y and its direct terms dK += beta Y e^Gamma, dGamma += beta Y
+        // e^Gamma K (rows < L)
         const int col0 = cbeg + c0;
-        KDA_UNROLL
-        for (int y = 0; y < 4; ++y) {
-          const size_t i = (size_t)(r0 + y);
-          const bool whole = c0 + 4 <= cnt;
-          if (whole && col0 + 4 <= V && vecV && (col0 & 3) == 0) {
+        const bool whole = c0 + 4 <= cnt;
+        if (whole && col0 + 4 <= V && vecV && (col0 & 3) == 0) {
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y) {
+            const size_t i = (size_t)(r0 + y);
             st4(X + i * V + col0, acc[y]);
-          } else if (whole && col0 >= V && vecK && ((col0 - V) & 3) == 0) {
-            st4(Y + i * K + (col0 - V), acc[y]);
-          } else {
+            if (r0 + y < L) {
+              const float bi = sB[r0 + y];
+              const float d[4] = {bi * acc[y][0], bi * acc[y][1], bi * acc[y][2], bi * acc[y][3]};
+              st4(a.dv + ((size_t)(t0 + i) * HV + hv) * V + col0, d);
+            }
+          }
+        } else if (whole && col0 >= V && vecK && ((col0 - V) & 3) == 0) {
+          const int k0 = col0 - V;
+          F4 gv[4], dkv[4], ekv[4], dgv[4];
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y) {
+            const size_t o = (size_t)(r0 + y < L ? r0 + y : 0) * K;
+            gv[y] = ld4w(Gam + o, k0, K, true); dkv[y] = ld4w(dK + o, k0, K, true);
+            ekv[y] = ld4w(EK + o, k0, K, true); dgv[y] = ld4w(dGam + o, k0, K, true);
+          }
+          KDA_UNROLL
+          for (int y = 0; y < 4; ++y) {
+            const size_t i = (size_t)(r0 + y);
+            st4(Y + i * K + k0, acc[y]);
+            if (r0 + y < L) {
+              const float bi = sB[r0 + y];
+              float nk[4], ng4[4];
+              KDA_UNROLL
+              for (int x = 0; x < 4; ++x) {
+                const float t = bi * acc[y][x];
+                nk[x] = f4at(dkv[y], x) + t * fexp(f4at(gv[y], x));
+                ng4[x] = f4at(dgv[y], x) + t * f4at(ekv[y], x);
+              }
+              st4(dK + i * K + k0, nk);
+              st4(dGam + i * K + k0, ng4);
+            }
+          }
+        } else {
+          for (int y = 0; y < 4; ++y) {
+            const size_t i = (size_t)(r0 + y);
             for (int x = 0; x < 4 && c0 + x < cnt; ++x) {
               const int col = col0 + x;
-              if (col < V) X[i * V + col] = acc[y][x];
-              else Y[i * K + col - V] = acc[y][x];
+              const float v = acc[y][x];
+              if (col < V) {
+                X[i * V + col] = v;
+                if (r0 + y < L) a.dv[((size_t)(t0 + i) * HV + hv) * V + col] = sB[r0 + y] * v;
+              } else {
+                const size_t e = i * K + (col - V);
+                Y[e] = v;
+                if (r0 + y < L) {
+                  const float t = sB[r0 + y] * v;
+                  dK[e] += t * fexp(Gam[e]);
+                  dGam[e] += t * EK[e];
+                }
+              }
             }
           }
         }
       }
     });
   }
-  // dv; the e^Gamma K part of dK and dGamma
-  struct DK { float y, g, dk, ek, dg; };
-  ex.phase([&](int tid, int nthr) {
-    batched<8>(tid, nthr, L * V, [&](int e) { return X[e]; }, [&](int e, float x) {
-      const int i = e / V, v = e - (e / V) * V;
-      a.dv[((size_t)(t0 + i) * HV + hv) * V + v] = sB[i] * x;
-    });
-    batched<4>(tid, nthr, L * K, [&](int e) { return DK{Y[e], Gam[e], dK[e], EK[e], dGam[e]}; },
-               [&](int e, const DK& d) {
-      const float t = sB[e / K] * d.y;
-      dK[e] = d.dk + t * fexp(d.g);
-      dGam[e] = d.dg + t * d.ek;
-    });
-  });
   // A^T dA = X (beta V)^T + Y (beta e^Gamma K)^T over 64-column slices of v, then of k, staged
   // in shared memory and accumulated in sZ (lower blocks with the diagonal: its entries,
   // without beta, are the WY part of dbeta)
@@ -1710,17 +1734,24 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
         for (int x = 0; x < 4; ++x) sM[(size_t)(4 * rb + y) * ldz + 4 * ib + x] = acc[y][x];
     }
   });
+  // (row r, one of nq column pieces) per thread; the pieces' dbeta sums meet in sRed and are
+  // added at the start of the next phase
+  const int nq = kThreads / C > 0 ? kThreads / C : 1, qw = (C + nq - 1) / nq;
   ex.phase([&](int tid, int nthr) {
-    for (int r = tid; r < L; r += nthr) {
-      float* z = sZ + (size_t)r * ldz;
-      const float* m = sM + (size_t)r * ldz;
+    for (int u = tid; u < nq * C; u += nthr) {
+      const int r = u / nq, q = u - (u / nq) * nq;
       float db = 0.f;
-      for (int i = 0; i < r; ++i) {
-        const float d = -m[i];
-        db = fmaf(d, P[(size_t)r * C + i], db);
-        z[i] = sB[r] * d;
+      if (r < L) {
+        float* z = sZ + (size_t)r * ldz;
+        const float* m = sM + (size_t)r * ldz;
+        const int ib = q * qw, ie = ib + qw < r ? ib + qw : r;
+        for (int i = ib; i < ie; ++i) {
+          const float d = -m[i];
+          db = fmaf(d, P[(size_t)r * C + i], db);
+          z[i] = sB[r] * d;
+        }
       }
-      sDB[r] += db;
+      sRed[u] = db;
     }
   });
   // block references rho (Gamma at each 16-row block's middle row), Q and K scaled by
@@ -1732,6 +1763,11 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     return j < kbA ? sAk + (size_t)j * K : sT + (size_t)C * lda + (size_t)(j - kbA) * K;
   };
   ex.phase([&](int tid, int nthr) {
+    for (int r = tid; r < L; r += nthr) {
+      float db = 0.f;
+      for (int q = 0; q < nq; ++q) db += sRed[(size_t)r * nq + q];
+      sDB[r] += db;
+    }
     for (int e = tid; e < C * C; e += nthr) {
       const int i = e / C, j = e - (e / C) * C;
       sZt[(size_t)j * lda + i] = sZ[(size_t)i * ldz + j];
