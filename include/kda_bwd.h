@@ -81,8 +81,10 @@ size_t kda_bwd_workspace_size(const kda_bwd_params* p);
 
 /* Number of kernel launches one kda_bwd call makes (0 if the parameters are invalid): the
    chunk table (varlen only), prep, states, state gradient, the products over v (bf16 inputs
-   with K = V = 128 and chunk 64 only) and gradients.  The zeroing of
-   the outputs (cudaMemsetAsync) is not counted.  Host only. */
+   with K = V = 128 and chunk 64 only) and gradients.  The zeroing stage (cudaMemsetAsync of
+   what atomics accumulate into, dA_log, ddt_bias and, with HV > H, dq and dk, and of the rows
+   no sequence covers; every other output element is written once by the kernels) is not
+   counted.  Host only. */
 int32_t kda_bwd_num_launches(const kda_bwd_params* p);
 
 /* Number of stages of kda_bwd for these parameters (0 if they are invalid): the zeroing of

@@ -131,19 +131,13 @@ Args make_args(const kda_bwd_params* p, const Plan& pl, unsigned int* status) {
 }
 
 cudaError_t run_zero(const Args& a, cudaStream_t st) {
-  const Plan& pl = a.p;
-  auto zero = [&](void* ptr, size_t bytes) {
-    return ptr == nullptr || bytes == 0 ? cudaSuccess : cudaMemsetAsync(ptr, 0, bytes, st);
-  };
-  const size_t ntok = (size_t)pl.ntok;
-  const struct { void* ptr; size_t bytes; } outs[] = {
-      {a.dq, ntok * pl.H * pl.K * sizeof(float)},     {a.dk, ntok * pl.H * pl.K * sizeof(float)},
-      {a.dv, ntok * pl.HV * pl.V * sizeof(float)},    {a.dg, ntok * pl.HV * pl.K * sizeof(float)},
-      {a.dbeta, ntok * pl.HV * sizeof(float)},        {a.dA_log, (size_t)pl.HV * sizeof(float)},
-      {a.ddt_bias, (size_t)pl.HV * pl.K * sizeof(float)},
-  };
-  for (auto& o : outs) {
-    cudaError_t e = zero(o.ptr, o.bytes);
+  float* outs[7] = {a.dq, a.dk, a.dv, a.dg, a.dbeta, a.dA_log, a.ddt_bias};
+  ZeroRange z[14];
+  const int n = zero_ranges(a.p, z);
+  for (int i = 0; i < n; ++i) {
+    float* base = outs[z[i].out];
+    if (base == nullptr || z[i].count == 0) continue;
+    cudaError_t e = cudaMemsetAsync(base + z[i].first, 0, z[i].count * sizeof(float), st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

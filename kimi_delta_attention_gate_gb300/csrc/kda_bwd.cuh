@@ -115,6 +115,7 @@ KDA_HD Block block_layout(int C, int K, int V) {
 struct Plan {
   int B, T, H, HV, K, V, C, N, G;
   int64_t ntok, nct;
+  int64_t cov_lo, cov_hi;  // the tokens the sequences cover: [cov_lo, cov_hi)
   int nc_per_seq, varlen;
   size_t off_table;   // int64 [N + 1] chunk offsets (varlen only)
   size_t off_blocks;  // [nct][HV] blocks
@@ -147,8 +148,12 @@ inline Plan make_plan(const kda_fwd_params* f) {
     for (int n = 0; n < f->N; ++n)
       nct += (f->cu_seqlens_host[n + 1] - f->cu_seqlens_host[n] + p.C - 1) / p.C;
     p.nct = nct;
+    p.cov_lo = f->cu_seqlens_host[0];
+    p.cov_hi = f->cu_seqlens_host[f->N];
   } else {
     p.nct = (int64_t)f->B * p.nc_per_seq;
+    p.cov_lo = 0;
+    p.cov_hi = p.ntok;
   }
   p.blk = block_layout(p.C, p.K, p.V);
   size_t off = 256;
@@ -172,6 +177,30 @@ inline Plan make_plan(const kda_fwd_params* f) {
   }
   p.total_bytes = off;
   return p;
+}
+
+// The parts of the outputs that must read zero before the stages run: what atomics
+// accumulate into (dA_log, ddt_bias and, with grouped heads, dq and dk) and the rows of the
+// tokens no sequence covers.  Every other output element is written exactly once by the
+// stages.  Entries: (output, first float, floats); returns their number (at most 14).
+enum ZeroOut { kZeroDq, kZeroDk, kZeroDv, kZeroDg, kZeroDbeta, kZeroDAlog, kZeroDdt };
+struct ZeroRange { int out; size_t first, count; };
+inline int zero_ranges(const Plan& p, ZeroRange* z) {
+  int n = 0;
+  const size_t lo = (size_t)p.cov_lo, hi = (size_t)p.cov_hi, nt = (size_t)p.ntok;
+  const size_t row[5] = {(size_t)p.H * p.K, (size_t)p.H * p.K, (size_t)p.HV * p.V,
+                         (size_t)p.HV * p.K, (size_t)p.HV};
+  for (int o = kZeroDq; o <= kZeroDbeta; ++o) {
+    if (p.G > 1 && (o == kZeroDq || o == kZeroDk)) {
+      z[n++] = {o, 0, nt * row[o]};
+      continue;
+    }
+    if (lo > 0) z[n++] = {o, 0, lo * row[o]};
+    if (hi < nt) z[n++] = {o, hi * row[o], (nt - hi) * row[o]};
+  }
+  z[n++] = {kZeroDAlog, 0, (size_t)p.HV};
+  z[n++] = {kZeroDdt, 0, (size_t)p.HV * p.K};
+  return n;
 }
 
 // Arguments of every stage (passed by value to the kernels).

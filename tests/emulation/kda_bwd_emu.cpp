@@ -167,6 +167,17 @@ int main(int argc, char** argv) {
   a.dA_log = geti("want_dA_log") ? zeros(f.HV) : nullptr;
   a.ddt_bias = geti("want_ddt_bias") ? zeros((size_t)f.HV * f.K) : nullptr;
   a.dh0 = geti("want_dh0") ? zeros(st) : nullptr;
+  {  // the outputs start as NaN except where the zeroing stage clears them: every element the
+     // stages must write and do not shows up in the results
+    float* outs[7] = {a.dq, a.dk, a.dv, a.dg, a.dbeta, a.dA_log, a.ddt_bias};
+    const size_t sizes[7] = {qk, qk, vv, gg, bb, (size_t)f.HV, (size_t)f.HV * f.K};
+    for (int o = 0; o < 7; ++o)
+      if (outs[o] != nullptr) poison(outs[o], sizes[o] * sizeof(float));
+    kda::bwd::ZeroRange z[14];
+    const int nz = kda::bwd::zero_ranges(pl, z);
+    for (int i = 0; i < nz; ++i)
+      if (outs[z[i].out] != nullptr) memset(outs[z[i].out] + z[i].first, 0, z[i].count * sizeof(float));
+  }
   a.ws = ws;
   a.status = &status;
 
