@@ -1941,17 +1941,27 @@ KDA_UNROLL
             fi = F4{fexp(gi.x - rho.x), fexp(gi.y - rho.y), fexp(gi.z - rho.z), fexp(gi.w - rho.w)};
           }
           const int ib = 16 * I > r0 ? 16 * I : r0, iend = 16 * I + 16 < L ? 16 * I + 16 : L;
-          KDA_UNROLL4
-          for (int i = ib; i < iend; ++i) {
-            const F4 qf = ld4w(QF + (size_t)i * K, k0, K, vecK), kf = ld4w(KF + (size_t)i * K, k0, K, vecK);
-            const float qe[4] = {qf.x * fi.x, qf.y * fi.y, qf.z * fi.z, qf.w * fi.w};
-            const float ke[4] = {kf.x * fi.x, kf.y * fi.y, kf.z * fi.z, kf.w * fi.w};
+          for (int i0 = ib; i0 < iend; i0 += 4) {  // four rows' loads in flight at a time
+            F4 qf[4], kf[4];
 KDA_UNROLL
-            for (int y = 0; y < 8; ++y) {
-              const float dav = sdAt[(size_t)(r0 + y) * lda + i];  // dAqk[i][r], zero for i < r
-              const float dzv = sZt[(size_t)(r0 + y) * lda + i];   // dP[i][r], zero for i <= r
+            for (int u = 0; u < 4; ++u) {
+              const size_t i = (size_t)(i0 + u < iend ? i0 + u : i0);
+              qf[u] = ld4w(QF + i * K, k0, K, vecK);
+              kf[u] = ld4w(KF + i * K, k0, K, vecK);
+            }
 KDA_UNROLL
-              for (int x = 0; x < 4; ++x) s[y][x] = fmaf(dav, qe[x], fmaf(dzv, ke[x], s[y][x]));
+            for (int u = 0; u < 4; ++u) {
+              if (i0 + u >= iend) break;
+              const int i = i0 + u;
+              const float qe[4] = {qf[u].x * fi.x, qf[u].y * fi.y, qf[u].z * fi.z, qf[u].w * fi.w};
+              const float ke[4] = {kf[u].x * fi.x, kf[u].y * fi.y, kf[u].z * fi.z, kf[u].w * fi.w};
+KDA_UNROLL
+              for (int y = 0; y < 8; ++y) {
+                const float dav = sdAt[(size_t)(r0 + y) * lda + i];  // dAqk[i][r], zero for i < r
+                const float dzv = sZt[(size_t)(r0 + y) * lda + i];   // dP[i][r], zero for i <= r
+KDA_UNROLL
+                for (int x = 0; x < 4; ++x) s[y][x] = fmaf(dav, qe[x], fmaf(dzv, ke[x], s[y][x]));
+              }
             }
           }
         }
