@@ -39,10 +39,11 @@ struct GpuExec {
   }
 };
 
+template <int SC, int SK, int SV>
 __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const Args a) {
   extern __shared__ float smem[];
   GpuExec ex;
-  prep_body(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);
+  prep_body<SC, SK, SV>(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);
 }
 
 __global__ void __launch_bounds__(kThreads) states_kernel(const Args a) {
@@ -57,11 +58,15 @@ __global__ void __launch_bounds__(kThreads) dstate_kernel(const Args a) {
   dstate_body(ex, a, (int64_t)blockIdx.x, smem);
 }
 
+template <int SC, int SK, int SV>
 __global__ void __launch_bounds__(kThreads, 2) grads_kernel(const Args a) {
   extern __shared__ float smem[];
   GpuExec ex;
-  grads_body(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);
+  grads_body<SC, SK, SV>(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);
 }
+
+// The common shape (chunk 64, K = V = 128) with its dimensions compiled in.
+bool common_shape(const Plan& p) { return p.C == 64 && p.K == 128 && p.V == 128; }
 
 thread_local char t_msg[512];
 
@@ -161,7 +166,9 @@ cudaError_t launch_smem(Kernel kernel, dim3 grid, size_t smem, const Args& a, cu
 }
 
 cudaError_t run_prep(const Args& a, cudaStream_t st) {
-  return launch_smem(prep_kernel, dim3((unsigned)a.p.nct, (unsigned)a.p.HV), prep_smem(a.p), a, st);
+  const dim3 grid((unsigned)a.p.nct, (unsigned)a.p.HV);
+  return common_shape(a.p) ? launch_smem(prep_kernel<64, 128, 128>, grid, prep_smem(a.p), a, st)
+                           : launch_smem(prep_kernel<0, 0, 0>, grid, prep_smem(a.p), a, st);
 }
 
 cudaError_t run_states(const Args& a, cudaStream_t st) {
@@ -173,7 +180,9 @@ cudaError_t run_dstate(const Args& a, cudaStream_t st) {
 }
 
 cudaError_t run_grads(const Args& a, cudaStream_t st) {
-  return launch_smem(grads_kernel, dim3((unsigned)a.p.nct, (unsigned)a.p.HV), grads_smem(a.p), a, st);
+  const dim3 grid((unsigned)a.p.nct, (unsigned)a.p.HV);
+  return common_shape(a.p) ? launch_smem(grads_kernel<64, 128, 128>, grid, grads_smem(a.p), a, st)
+                           : launch_smem(grads_kernel<0, 0, 0>, grid, grads_smem(a.p), a, st);
 }
 
 }  // namespace

@@ -533,10 +533,13 @@ KDA_BODY void batched(int tid, int nthr, int n, Ld ld, St st) {
 
 // ---- prep: per (chunk c, value head hv) ------------------------------------------------
 
-template <class Exec>
+// SC, SK, SV: the chunk size and head dimensions as compile-time constants (0: the plan's),
+// so that the index arithmetic of the common shape folds into shifts and multiplies.
+template <int SC = 0, int SK = 0, int SV = 0, class Exec>
 KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem) {
   const Plan& p = a.p;
-  const int C = p.C, K = p.K, V = p.V, H = p.H, HV = p.HV, h = hv / p.G;
+  const int C = SC ? SC : p.C, K = SK ? SK : p.K, V = SV ? SV : p.V;
+  const int H = p.H, HV = p.HV, h = hv / p.G;
   int n, L;
   int64_t t0;
   if (!locate(a, c, n, t0, L)) {
@@ -1314,10 +1317,13 @@ KDA_BODY void vprod_body(Exec& ex, const Args& a, int64_t c, int hv, float* /*sm
 // middle row), in which case the chunk evaluates every e^(Gamma_i - Gamma_j) directly.
 
 
-template <class Exec>
+// SC, SK, SV: the chunk size and head dimensions as compile-time constants (0: the plan's),
+// so that the index arithmetic of the common shape folds into shifts and multiplies.
+template <int SC = 0, int SK = 0, int SV = 0, class Exec>
 KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem) {
   const Plan& p = a.p;
-  const int C = p.C, K = p.K, V = p.V, H = p.H, HV = p.HV, h = hv / p.G;
+  const int C = SC ? SC : p.C, K = SK ? SK : p.K, V = SV ? SV : p.V;
+  const int H = p.H, HV = p.HV, h = hv / p.G;
   int n, L;
   int64_t t0;
   if (!locate(a, c, n, t0, L)) {
