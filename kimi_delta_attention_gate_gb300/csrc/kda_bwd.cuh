@@ -1934,61 +1934,84 @@ KDA_UNROLL
             sts4m(dGam + o, ng4, K - k0, vecK);
           }
         }
-        // s3 + s4 (their factors are the same): the rows i of every block I >= R, each row's
-        // Q e^(G - rho_I) and K e^(G - rho_I) scaled by e^(rho_I - rho_R)
-KDA_UNROLL
-        for (int y = 0; y < 8; ++y)
-KDA_UNROLL
-          for (int x = 0; x < 4; ++x) s[y][x] = 0.f;
-        for (int I = R; I < NB; ++I) {
-          F4 fi{1.f, 1.f, 1.f, 1.f};
-          if (I > R) {
-            const F4 gi = ld4w(Gam + (size_t)mid(I) * K, k0, K, vecK);
-            fi = F4{fexp(gi.x - rho.x), fexp(gi.y - rho.y), fexp(gi.z - rho.z), fexp(gi.w - rho.w)};
+      }
+    });
+    // s3 + s4 (their factors are the same) over slices of C channels, whose rows Q e^(G -
+    // rho_I) and K e^(G - rho_I) are first copied into shared memory (into the key rows'
+    // region and dP's row-major tile, both dead by now): one thread per (4-row group, channel
+    // quad of the slice), summing the rows i of every block I >= R, each scaled by
+    // e^(rho_I - rho_R), then dK += s34 e^(rho_R - G_r), dGamma -= K s34 e^(rho_R - G_r)
+    float* sQFs = sAk;  // [C][C]
+    float* sKFs = sZ;   // [C][C] (of C x ldz)
+    const int NBs = (L + 15) >> 4;
+    auto mid_s = [&](int blk_) { return (16 * blk_ + 7) < L - 1 ? 16 * blk_ + 7 : L - 1; };
+    for (int c0 = 0; c0 < K; c0 += C) {
+      const int W = K - c0 < C ? K - c0 : C, wq = (W + 3) / 4;
+      ex.phase([&](int tid, int nthr) {
+        if (vecK) {
+          for (int e = tid; e < C * wq; e += nthr) {
+            const int i = e / wq, x4 = 4 * (e - (e / wq) * wq);
+            ex.copy16(sQFs + (size_t)i * C + x4, QF + (size_t)i * K + c0 + x4);
+            ex.copy16(sKFs + (size_t)i * C + x4, KF + (size_t)i * K + c0 + x4);
           }
-          const int ib = 16 * I > r0 ? 16 * I : r0, iend = 16 * I + 16 < L ? 16 * I + 16 : L;
-          for (int i0 = ib; i0 < iend; i0 += 4) {  // four rows' loads in flight at a time
-            F4 qf[4], kf[4];
+          ex.copy_wait();
+        } else {
+          for (int e = tid; e < C * 4 * wq; e += nthr) {
+            const int i = e / (4 * wq), x = e - (e / (4 * wq)) * (4 * wq);
+            sQFs[(size_t)i * C + x] = x < W ? QF[(size_t)i * K + c0 + x] : 0.f;
+            sKFs[(size_t)i * C + x] = x < W ? KF[(size_t)i * K + c0 + x] : 0.f;
+          }
+        }
+      });
+      ex.phase([&](int tid, int nthr) {
+        for (int u = tid; u < (C / 4) * wq; u += nthr) {
+          const int g4 = u / wq, xq = 4 * (u - (u / wq) * wq);
+          const int r0 = 4 * g4, R = r0 >> 4, k0 = c0 + xq;
+          if (r0 >= L) continue;
+          const int nr = L - r0 < 4 ? L - r0 : 4;
+          const F4 rho = ld4w(Gam + (size_t)mid_s(R) * K, k0, K, vecK);
+          float sv[4][4];
 KDA_UNROLL
-            for (int u = 0; u < 4; ++u) {
-              const size_t i = (size_t)(i0 + u < iend ? i0 + u : i0);
-              qf[u] = ld4w(QF + i * K, k0, K, vecK);
-              kf[u] = ld4w(KF + i * K, k0, K, vecK);
+          for (int y = 0; y < 4; ++y)
+KDA_UNROLL
+            for (int x = 0; x < 4; ++x) sv[y][x] = 0.f;
+          for (int I = R; I < NBs; ++I) {
+            F4 fi{1.f, 1.f, 1.f, 1.f};
+            if (I > R) {
+              const F4 gi = ld4w(Gam + (size_t)mid_s(I) * K, k0, K, vecK);
+              fi = F4{fexp(gi.x - rho.x), fexp(gi.y - rho.y), fexp(gi.z - rho.z), fexp(gi.w - rho.w)};
             }
+            const int ib = 16 * I > r0 ? 16 * I : r0, iend = 16 * I + 16 < L ? 16 * I + 16 : L;
+            KDA_UNROLL4
+            for (int i = ib; i < iend; ++i) {
+              const F4 qf = ld4(sQFs + (size_t)i * C + xq), kf = ld4(sKFs + (size_t)i * C + xq);
+              const float qe[4] = {qf.x * fi.x, qf.y * fi.y, qf.z * fi.z, qf.w * fi.w};
+              const float ke[4] = {kf.x * fi.x, kf.y * fi.y, kf.z * fi.z, kf.w * fi.w};
 KDA_UNROLL
-            for (int u = 0; u < 4; ++u) {
-              if (i0 + u >= iend) break;
-              const int i = i0 + u;
-              const float qe[4] = {qf[u].x * fi.x, qf[u].y * fi.y, qf[u].z * fi.z, qf[u].w * fi.w};
-              const float ke[4] = {kf[u].x * fi.x, kf[u].y * fi.y, kf[u].z * fi.z, kf[u].w * fi.w};
-KDA_UNROLL
-              for (int y = 0; y < 8; ++y) {
+              for (int y = 0; y < 4; ++y) {
                 const float dav = sdAt[(size_t)(r0 + y) * lda + i];  // dAqk[i][r], zero for i < r
                 const float dzv = sZt[(size_t)(r0 + y) * lda + i];   // dP[i][r], zero for i <= r
 KDA_UNROLL
-                for (int x = 0; x < 4; ++x) s[y][x] = fmaf(dav, qe[x], fmaf(dzv, ke[x], s[y][x]));
+                for (int x = 0; x < 4; ++x) sv[y][x] = fmaf(dav, qe[x], fmaf(dzv, ke[x], sv[y][x]));
               }
             }
           }
-        }
-KDA_UNROLL
-        for (int y0 = 0; y0 < 8; y0 += 4) {
           F4 gr[4], kv[4], dk[4], dg[4];
 KDA_UNROLL
           for (int y = 0; y < 4; ++y) {
-            const size_t o = (size_t)(r0 + (y0 + y < nr ? y0 + y : 0)) * K;
+            const size_t o = (size_t)(r0 + (y < nr ? y : 0)) * K;
             gr[y] = ld4w(Gam + o, k0, K, vecK);
             kv[y] = ld4w(Kn + o, k0, K, vecK); dk[y] = ld4w(dK + o, k0, K, vecK);
             dg[y] = ld4w(dGam + o, k0, K, vecK);
           }
 KDA_UNROLL
           for (int y = 0; y < 4; ++y) {
-            if (y0 + y >= nr) continue;
-            const size_t o = (size_t)(r0 + y0 + y) * K + k0;
+            if (y >= nr) continue;
+            const size_t o = (size_t)(r0 + y) * K + k0;
             float nk[4], ng4[4];
 KDA_UNROLL
             for (int x = 0; x < 4; ++x) {
-              const float s34 = s[y0 + y][x] * fexp(f4at(rho, x) - f4at(gr[y], x));
+              const float s34 = sv[y][x] * fexp(f4at(rho, x) - f4at(gr[y], x));
               nk[x] = f4at(dk[y], x) + s34;
               ng4[x] = f4at(dg[y], x) - f4at(kv[y], x) * s34;
             }
@@ -1996,8 +2019,8 @@ KDA_UNROLL
             sts4m(dGam + o, ng4, K - k0, vecK);
           }
         }
-      }
-    });
+      });
+    }
   } else {
     // exact fallback: every e^(Gamma_i - Gamma_j) evaluated directly, one thread per (row
     // r, channel k): r as the row index i (dQ, dK) and as the column index j (dK)
