@@ -102,8 +102,12 @@ const char* kda_bwd_stage_name(const kda_bwd_params* p, int32_t stage);
 kda_status kda_bwd_stage(const kda_bwd_params* p, void* stream, int32_t stage);
 
 /* The backward pass, enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
-   Asynchronous: returns once the work is enqueued.  Returns KDA_ERR_CUDA if a launch
-   fails; kda_get_device_status reports inconsistent device-side cu_seqlens as for kda_fwd. */
+   Asynchronous: returns once the work is enqueued.  The state-gradient stage runs on a
+   library-owned stream (one per device, created on the first call) beside the state stage:
+   it is forked from `stream` after the recompute stage and joined back before the next
+   stage with events, so the call stays ordered on `stream` and can be captured into a CUDA
+   graph.  Returns KDA_ERR_CUDA if a launch fails or that stream cannot be created;
+   kda_get_device_status reports inconsistent device-side cu_seqlens as for kda_fwd. */
 kda_status kda_bwd(const kda_bwd_params* p, void* stream);
 
 #ifdef __cplusplus

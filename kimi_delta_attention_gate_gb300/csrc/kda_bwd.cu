@@ -4,6 +4,9 @@
 
 #include <stdarg.h>
 #include <stdio.h>
+#include <string.h>
+
+#include <mutex>
 
 #include "kda_bwd.cuh"
 #include "kda_internal.cuh"
@@ -213,6 +216,34 @@ int stages_for(const Plan& pl, Stage* out) {
   return n;
 }
 
+// The state stage (chunks in order) and the state-gradient stage (chunks in reverse) read only
+// what the recompute stage wrote and write disjoint workspace regions, so kda_bwd runs the
+// latter on a library-owned stream beside the former: each occupies one SM per (sequence,
+// value head) along its chain.  One stream and its fork / join events per device, created on
+// first use; enqueueing holds the context's lock, so concurrent calls cannot swap events.
+struct SideCtx {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideCtx g_side[64];
+
+SideCtx* side_ctx() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideCtx& c = g_side[dev];
+  std::lock_guard<std::mutex> lk(c.mu);
+  if (!c.ready) {
+    if (cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+    c.ready = true;
+  }
+  return &c;
+}
+
 // Checks (host), plan, workspace and the device status word; fills the kernel arguments.
 kda_status prepare(const kda_bwd_params* p, Args& a) {
   kda_status s = check(p);
@@ -294,8 +325,33 @@ kda_status kda_bwd(const kda_bwd_params* p, void* stream) {
   if (s != KDA_OK) return s;
   B::Stage st[B::kMaxStages];
   const int n = B::stages_for(a.p, st);
+  const cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+  int i_states = -1, i_dstate = -1;
   for (int i = 0; i < n; ++i) {
-    cudaError_t e = st[i].run(a, static_cast<cudaStream_t>(stream));
+    if (strcmp(st[i].name, "bwd_states") == 0) i_states = i;
+    if (strcmp(st[i].name, "bwd_dstate") == 0) i_dstate = i;
+  }
+  B::SideCtx* cx = (i_states >= 0 && i_dstate == i_states + 1) ? B::side_ctx() : nullptr;
+  if (i_states >= 0 && cx == nullptr)
+    return B::fail(KDA_ERR_CUDA, "could not create the backward's side stream");
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = cudaSuccess;
+    if (cx != nullptr && i == i_states) {
+      // states on the caller's stream, dstate on the side stream, both after the stages
+      // before them; the caller's stream then waits for both
+      std::lock_guard<std::mutex> lk(cx->mu);
+      if ((e = cudaEventRecord(cx->fork, s0)) == cudaSuccess &&
+          (e = cudaStreamWaitEvent(cx->side, cx->fork, 0)) == cudaSuccess &&
+          (e = st[i_dstate].run(a, cx->side)) == cudaSuccess &&
+          (e = cudaEventRecord(cx->join, cx->side)) == cudaSuccess &&
+          (e = st[i_states].run(a, s0)) == cudaSuccess)
+        e = cudaStreamWaitEvent(s0, cx->join, 0);
+      if (e != cudaSuccess)
+        return B::fail(KDA_ERR_CUDA, "bwd_states / bwd_dstate failed: %s", cudaGetErrorString(e));
+      ++i;  // dstate was enqueued with states
+      continue;
+    }
+    e = st[i].run(a, s0);
     if (e != cudaSuccess)
       return B::fail(KDA_ERR_CUDA, "%s failed: %s", st[i].name, cudaGetErrorString(e));
   }
