@@ -590,22 +590,27 @@ __global__ void __launch_bounds__(kStThreads, 1)
 // ======================================================================================
 // The gradient stage's products over v (backward-propagation step 5) on the tensor cores,
 // one CTA per (chunk, value head), M = 64 tokens:
-//   dQg = dO S^T, dW = -dV_new S^T            (step pair 1: B = S)
-//   dKg = V_new dS'^T, dAqk = dO V_new^T       (step pair 2: B = dS', V_new)
-// each over the 128 columns of v in two 64-column halves.  Per half, every thread splits
-// its share of the fp32 operands (the workspace's states, V_new, dV_new) into bf16 hi / lo
-// parts in the swizzled K-major layout, TMA brings the dO panel (an exact bf16 input), and
-// one thread issues the MMAs (two per K-step with dO as A, three otherwise).  The diagonal
-// of S dS'^T is summed while dS' is split.  Outputs go to the block's dq, y, dk, aqk and dkg
-// slots, where the gradient stage reads them.
+//   dQg = dO S^T, dW = -dV_new S^T            (steps 0, 1: B = S, A = dV_new)
+//   dKg = V_new dS'^T, dAqk = dO V_new^T       (steps 2, 3: B = dS', A = V_new)
+// each over the 128 columns of v in two 64-column halves (h = step % 2).  The fp32 rows of
+// a step's B and A operands (the workspace's states, V_new, dV_new) arrive in a staging
+// buffer by TMA while the previous step's MMAs and epilogue run; every thread then splits
+// its share of them into bf16 hi / lo parts in the swizzled K-major layout, TMA brings the dO
+// panel (an exact bf16 input), and one thread issues the MMAs (two per K-step with dO as A,
+// three otherwise).  The diagonal of S dS'^T is summed while dS' is split (S read from the
+// workspace directly).  Outputs go to the block's dq, y, dk, aqk and dkg slots, where the
+// gradient stage reads them.
 // ======================================================================================
 constexpr uint32_t VP_B = 0;          // B tile (S or dS') hi, lo: [128 rows k][64 v], 16 KB each
 constexpr uint32_t VP_A = 32768;      // A tile (dV_new or V_new) hi, lo: [64 rows t][64 v], 8 KB each
 constexpr uint32_t VP_DO = 49152;     // dO panel [64 t][64 v] bf16
-constexpr uint32_t VP_RED = 57344;    // [256] partial sums of diag(S dS'^T)
-constexpr uint32_t VP_BAR = 58368;    // bar_do, bar_mma
-constexpr uint32_t VP_TMEM = VP_BAR + 16;
+constexpr uint32_t VP_SB = 57344;     // fp32 staging of the B rows [128][64]
+constexpr uint32_t VP_SA = 90112;     // fp32 staging of the A rows [64][64]
+constexpr uint32_t VP_RED = 106496;   // [128][8] partial sums of diag(S dS'^T)
+constexpr uint32_t VP_BAR = 110592;   // bar_do, bar_mma, bar_stg
+constexpr uint32_t VP_TMEM = VP_BAR + 32;
 constexpr uint32_t VP_SMEM = VP_TMEM + 16 + 1024;
+constexpr uint32_t VP_STAGE_BYTES = 49152;
 constexpr int kVpThreads = 256;
 
 // hi / lo parts of eight consecutive fp32 values into the 16-byte chunks at `off` of a tile's
@@ -622,7 +627,9 @@ __device__ __forceinline__ void put8(uint8_t* tile, uint32_t off, uint32_t lo_of
 }
 
 __global__ void __launch_bounds__(kVpThreads, 2)
-    vprod_tc_kernel(const Args a, const __grid_constant__ CUtensorMap domap) {
+    vprod_tc_kernel(const Args a, const __grid_constant__ CUtensorMap domap,
+                    const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap dsmap,
+                    const __grid_constant__ CUtensorMap vnmap, const __grid_constant__ CUtensorMap dvnmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1k(smem_raw);
   const Plan& p = a.p;
@@ -638,8 +645,11 @@ __global__ void __launch_bounds__(kVpThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bar_do = reinterpret_cast<uint64_t*>(sm + VP_BAR);
   uint64_t* bar_mma = bar_do + 1;
+  uint64_t* bar_stg = bar_do + 2;
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + VP_TMEM);
   float* sRed = reinterpret_cast<float*>(sm + VP_RED);
+  const float* sSB = reinterpret_cast<const float*>(sm + VP_SB);
+  const float* sSA = reinterpret_cast<const float*>(sm + VP_SA);
   if (warp == 0) {
     tmem_alloc(sTmem, 256);
     tmem_relinquish();
@@ -647,6 +657,7 @@ __global__ void __launch_bounds__(kVpThreads, 2)
   if (tid == 0) {
     mbar_init(bar_do, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_stg, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -655,14 +666,23 @@ __global__ void __launch_bounds__(kVpThreads, 2)
   bool ok = true;
   float* blk = block_ptr(a, c, hv);
   const float* S = state_ptr(a, p.off_h, c, hv);
-  const float* dSp = state_ptr(a, p.off_dh, c, hv);
-  const float* Vn = blk + p.blk.vn;
-  const float* dVn = blk + p.blk.dvn;
-  float dgc = 0.f;  // this thread's part of diag(S dS'^T) for channel tid / 2
-  int do_open = -1, mma_open = -1;  // (thread 0) step of a copy / MMA group not yet seen done
+  const int32_t zc = (int32_t)(c * p.HV + hv);  // (chunk, value head) coordinate of the maps
+  // staging of step st: B rows (S, dS') and A rows (dV_new, V_new) of v half st % 2
+  auto issue_stage = [&](int st) {
+    const int32_t v0 = 64 * (st & 1);
+    mbar_arrive_expect_tx(bar_stg, VP_STAGE_BYTES);
+    tma_load_3d(sm + VP_SB, st < 2 ? &smap : &dsmap, v0, 0, zc, bar_stg);
+    tma_load_3d(sm + VP_SA, st < 2 ? &dvnmap : &vnmap, v0, 0, zc, bar_stg);
+  };
+  float dgc[4] = {0.f, 0.f, 0.f, 0.f};  // partials of diag(S dS'^T): rows (tid >> 3) + 32 i
+  int do_open = -1, mma_open = -1, stg_open = -1;  // (thread 0) issued, not yet seen done
   const uint32_t b_hi = smem_u32(sm + VP_B), b_lo = b_hi + 16384u;
   const uint32_t a_hi = smem_u32(sm + VP_A), a_lo = a_hi + 8192u;
   const uint32_t do_b = smem_u32(sm + VP_DO);
+  if (tid == 0) {
+    issue_stage(0);
+    stg_open = 0;
+  }
   for (int step = 0; step < 4 && ok; ++step) {
     const int pair = step >> 1, h = step & 1;  // pair 0: B = S, A = dV_new; pair 1: dS', V_new
     const int v0 = 64 * h;
@@ -671,44 +691,56 @@ __global__ void __launch_bounds__(kVpThreads, 2)
       tma_load_3d(sm + VP_DO, &domap, v0, hv, (int32_t)t0, bar_do);
       do_open = step;
     }
-    {  // B: channel row k = tid / 2, columns v0 + 32 (tid & 1) .. + 31
-      const int k = tid >> 1, c0 = 32 * (tid & 1);
-      const float* src = (pair == 0 ? S : dSp) + (size_t)k * V + v0 + c0;
-      const float* s2 = S + (size_t)k * V + v0 + c0;
+    // items: B (row r = (tid >> 3) + 32 i, columns v0 + 8 g ..), A (row t likewise), g = tid & 7
+    const int g = tid & 7, r_lo = tid >> 3;
+    float4 sd[4][2];  // S at the B items, for the diagonal (dS' steps)
+    if (pair == 1) {
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const float4 x0 = *reinterpret_cast<const float4*>(src + 8 * g);
-        const float4 x1 = *reinterpret_cast<const float4*>(src + 8 * g + 4);
-        put8(sm + VP_B, swz128((uint32_t)k, (uint32_t)(c0 + 8 * g)), 16384u, x0, x1);
+      for (int i = 0; i < 4; ++i) {
+        const float* src = S + (size_t)(r_lo + 32 * i) * V + v0 + 8 * g;
+        sd[i][0] = *reinterpret_cast<const float4*>(src);
+        sd[i][1] = *reinterpret_cast<const float4*>(src + 4);
+      }
+    }
+    if (!mbar_wait(bar_stg, (uint32_t)(step & 1))) ok = false;
+    else if (tid == 0) stg_open = -1;
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = r_lo + 32 * i;
+        const float4 x0 = *reinterpret_cast<const float4*>(sSB + r * 64 + 8 * g);
+        const float4 x1 = *reinterpret_cast<const float4*>(sSB + r * 64 + 8 * g + 4);
+        put8(sm + VP_B, swz128((uint32_t)r, (uint32_t)(8 * g)), 16384u, x0, x1);
         if (pair == 1) {
-          const float4 y0 = *reinterpret_cast<const float4*>(s2 + 8 * g);
-          const float4 y1 = *reinterpret_cast<const float4*>(s2 + 8 * g + 4);
-          dgc = fmaf(x0.x, y0.x, fmaf(x0.y, y0.y, fmaf(x0.z, y0.z, fmaf(x0.w, y0.w, dgc))));
-          dgc = fmaf(x1.x, y1.x, fmaf(x1.y, y1.y, fmaf(x1.z, y1.z, fmaf(x1.w, y1.w, dgc))));
+          const float4 y0 = sd[i][0], y1 = sd[i][1];
+          dgc[i] = fmaf(x0.x, y0.x, fmaf(x0.y, y0.y, fmaf(x0.z, y0.z, fmaf(x0.w, y0.w, dgc[i]))));
+          dgc[i] = fmaf(x1.x, y1.x, fmaf(x1.y, y1.y, fmaf(x1.z, y1.z, fmaf(x1.w, y1.w, dgc[i]))));
         }
       }
-    }
-    {  // A: token row t = tid / 4, columns v0 + 16 (tid & 3) .. + 15
-      const int t = tid >> 2, c0 = 16 * (tid & 3);
-      const float* src = (pair == 0 ? dVn : Vn) + (size_t)t * V + v0 + c0;
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const float4 x0 = *reinterpret_cast<const float4*>(src + 8 * g);
-        const float4 x1 = *reinterpret_cast<const float4*>(src + 8 * g + 4);
-        put8(sm + VP_A, swz128((uint32_t)t, (uint32_t)(c0 + 8 * g)), 8192u, x0, x1);
+      for (int i = 0; i < 2; ++i) {
+        const int t = r_lo + 32 * i;
+        const float4 x0 = *reinterpret_cast<const float4*>(sSA + t * 64 + 8 * g);
+        const float4 x1 = *reinterpret_cast<const float4*>(sSA + t * 64 + 8 * g + 4);
+        put8(sm + VP_A, swz128((uint32_t)t, (uint32_t)(8 * g)), 8192u, x0, x1);
       }
     }
-    fence_async_smem();
     // the dO panel; rows past the chunk's end (another sequence's tokens) become zero
-    if (!mbar_wait(bar_do, (uint32_t)(step & 1))) ok = false;
-    else if (tid == 0) do_open = -1;
-    if (L < C) {
+    if (ok) {
+      if (!mbar_wait(bar_do, (uint32_t)(step & 1))) ok = false;
+      else if (tid == 0) do_open = -1;
+    }
+    if (ok && L < C) {
       for (int e = tid; e < (C - L) * 8; e += kVpThreads)
         *reinterpret_cast<uint4*>(sm + VP_DO + (uint32_t)(L * 8 + e) * 16u) = make_uint4(0u, 0u, 0u, 0u);
-      fence_async_smem();
     }
-    ok = named_bar_and(1, kVpThreads, ok);
+    fence_async_smem();
+    ok = named_bar_and(1, kVpThreads, ok);  // operand tiles written, staging free
     if (tid == 0 && ok) {
+      if (step < 3) {  // the next step's rows arrive while this step's MMAs run
+        issue_stage(step + 1);
+        stg_open = step + 1;
+      }
       tc_fence_after();
 #pragma unroll 1
       for (int ks = 0; ks < 4; ++ks) {  // v0 + 16 ks .. + 15
@@ -793,13 +825,20 @@ __global__ void __launch_bounds__(kVpThreads, 2)
       __syncthreads();  // the accumulators are read before the next pair's MMAs overwrite them
     }
   }
-  if (ok) {  // diag(S dS'^T): the two threads of each channel
-    sRed[tid] = dgc;
+  if (ok) {  // diag(S dS'^T): the eight threads of each channel
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sRed[(size_t)((tid >> 3) + 32 * i) * 8 + (tid & 7)] = dgc[i];
     __syncthreads();
-    if (tid < K) blk[p.blk.dkg + tid] = sRed[2 * tid] + sRed[2 * tid + 1];
+    if (tid < K) {
+      float d = 0.f;
+#pragma unroll
+      for (int x = 0; x < 8; ++x) d += sRed[(size_t)tid * 8 + x];
+      blk[p.blk.dkg + tid] = d;
+    }
   } else if (tid == 0) {
     atomicOr(a.status, KDA_DEV_TIMEOUT);
-    // a copy or MMA group still in flight must end before shared and tensor memory go
+    // copies or an MMA group still in flight must end before shared and tensor memory go
+    if (stg_open >= 0) mbar_wait(bar_stg, (uint32_t)(stg_open & 1), 100000000ull);
     if (do_open >= 0) mbar_wait(bar_do, (uint32_t)(do_open & 1), 100000000ull);
     if (mma_open >= 0) mbar_wait(bar_mma, (uint32_t)(mma_open & 1), 100000000ull);
   }
@@ -839,6 +878,20 @@ bool make_do_map(const Args& a, CUtensorMap& m) {
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// fp32 rows of the workspace as [z][rows][cols] with z = chunk * HV + value head, rows
+// `row_stride` floats apart, z `z_stride` floats apart: [rows x 64] boxes, no swizzle
+bool make_rows_map(const Args& a, CUtensorMap& m, size_t off_bytes, int rows, int cols,
+                   size_t row_stride, size_t z_stride, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)(a.p.nct * a.p.HV)};
+  const cuuint64_t strides[2] = {(cuuint64_t)(row_stride * 4), (cuuint64_t)(z_stride * 4)};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.ws + off_bytes, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace
 
 // The state-gradient stage on the tensor cores (bf16 dO): one CTA per (sequence, value head).
@@ -862,11 +915,21 @@ cudaError_t run_vprod_tc(const Args& a, cudaStream_t st) {
   if (tmap_encoder() == nullptr) return cudaErrorNotSupported;
   CUtensorMap domap;  // K-major A operand panels of dO
   if (!make_do_map(a, domap)) return cudaErrorInvalidValue;
+  // the states (S before, dS' after each chunk: [K][V] per (chunk, value head)) and the
+  // V_new, dV_new rows of each block ([C][V])
+  const Plan& p = a.p;
+  const size_t kv = (size_t)p.K * p.V, blk0 = p.off_blocks;
+  CUtensorMap smap, dsmap, vnmap, dvnmap;
+  if (!make_rows_map(a, smap, p.off_h, p.K, p.V, p.V, kv, 128) ||
+      !make_rows_map(a, dsmap, p.off_dh, p.K, p.V, p.V, kv, 128) ||
+      !make_rows_map(a, vnmap, blk0 + 4 * p.blk.vn, p.C, p.V, p.V, p.blk.floats, 64) ||
+      !make_rows_map(a, dvnmap, blk0 + 4 * p.blk.dvn, p.C, p.V, p.V, p.blk.floats, 64))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(vprod_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)VP_SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)a.p.nct, (unsigned)a.p.HV);
-  vprod_tc_kernel<<<grid, kVpThreads, VP_SMEM, st>>>(a, domap);
+  vprod_tc_kernel<<<grid, kVpThreads, VP_SMEM, st>>>(a, domap, smap, dsmap, vnmap, dvnmap);
   return cudaGetLastError();
 }
 
