@@ -2127,9 +2127,9 @@ KDA_UNROLL
     return v;
   };
   ex.phase([&](int tid, int nthr) {
-    if (tid == 0 && a.dA_log != nullptr && has_alog) {
+    if (tid < 8 && a.dA_log != nullptr && has_alog) {  // eight partial sums, eight atomics
       float s = 0.f;
-      for (int t = 0; t < nthr; ++t) s += sRed[t];
+      for (int t = tid; t < nthr; t += 8) s += sRed[t];
       ex.atomic_add(a.dA_log + hv, s);
     }
     if (a.qk_l2norm) {
