@@ -1381,10 +1381,14 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   // their own stage) take that stage's dAqk and diag(S dS'^T)
   ex.phase([&](int tid, int nthr) {
     if (p.tc_vprod) {
-      const float* dAqk = blk + b.aqk;
-      for (int e = tid; e < C * lda; e += nthr) {
-        const int j = e / lda, i = e - (e / lda) * lda;
-        sdAt[e] = i < C ? dAqk[(size_t)i * C + j] : 0.f;
+      const float* dAqk = blk + b.aqk;  // rows read whole, written transposed
+      batched<8>(tid, nthr, C * C, [&](int e) { return dAqk[e]; }, [&](int e, float v) {
+        const int i = e / C, j = e - (e / C) * C;
+        sdAt[(size_t)j * lda + i] = v;
+      });
+      for (int e = tid; e < C * (lda - C); e += nthr) {
+        const int j = e / (lda - C), x = e - (e / (lda - C)) * (lda - C);
+        sdAt[(size_t)j * lda + C + x] = 0.f;
       }
       for (int kk = tid; kk < K4; kk += nthr) sDgc[kk] = kk < K ? dKG[kk] : 0.f;
     } else {
@@ -1573,10 +1577,28 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   for (int part = 0; part < 2; ++part) {
     const int cbeg = part == 0 ? 0 : half_cols, cnt = part == 0 ? half_cols : ncol - half_cols;
     ex.phase([&](int tid, int nthr) {
-      batched<8>(tid, nthr, C * cnt, [&](int e) {
-        const int i = e / cnt, col = cbeg + (e - (e / cnt) * cnt);
-        return col < V ? (i < L ? dVn[(size_t)i * V + col] : 0.f) : Y[(size_t)i * K + col - V];
-      }, [&](int e, float v) { sXY[e] = v; });
+      const bool onv = cbeg + cnt <= V, ony = cbeg >= V;
+      const int s0 = onv ? cbeg : cbeg - V;  // first source column
+      if (((onv && vecV) || (ony && vecK)) && (cnt & 3) == 0 && (s0 & 3) == 0) {
+        // whole rows of one array: 16-byte asynchronous copies (dV_new rows >= L are zero)
+        const int q = cnt / 4;
+        for (int e = tid; e < C * q; e += nthr) {
+          const int i = e / q, x4 = 4 * (e - (e / q) * q);
+          float* dst = sXY + (size_t)i * cnt + x4;
+          if (onv && i >= L) {
+            const float z[4] = {0.f, 0.f, 0.f, 0.f};
+            st4(dst, z);
+          } else {
+            ex.copy16(dst, onv ? dVn + (size_t)i * V + s0 + x4 : Y + (size_t)i * K + s0 + x4);
+          }
+        }
+        ex.copy_wait();
+      } else {
+        batched<8>(tid, nthr, C * cnt, [&](int e) {
+          const int i = e / cnt, col = cbeg + (e - (e / cnt) * cnt);
+          return col < V ? (i < L ? dVn[(size_t)i * V + col] : 0.f) : Y[(size_t)i * K + col - V];
+        }, [&](int e, float v) { sXY[e] = v; });
+      }
     });
     ex.phase([&](int tid, int nthr) {
       const int nc4 = (cnt + 3) / 4;
@@ -2057,10 +2079,20 @@ KDA_UNROLL
       const int hf = u / K, kk = u - (u / K) * K;
       const int i0 = hf * hrows, i1 = hf == 0 ? hrows : L;
       float sg = 0.f, sk = 0.f;
-      KDA_UNROLL4
-      for (int i = i0; i < i1; ++i) {
-        sg += dGam[(size_t)i * K + kk];
-        sk += dKG[(size_t)i * K + kk];
+      for (int ib = i0; ib < i1; ib += 8) {  // eight rows' loads at a time
+        float g8[8], k8[8];
+        KDA_UNROLL
+        for (int x = 0; x < 8; ++x) {
+          const int i = ib + x < i1 ? ib + x : i0;
+          g8[x] = dGam[(size_t)i * K + kk];
+          k8[x] = dKG[(size_t)i * K + kk];
+        }
+        KDA_UNROLL
+        for (int x = 0; x < 8; ++x)
+          if (ib + x < i1) {
+            sg += g8[x];
+            sk += k8[x];
+          }
       }
       sHalf[u] = sg;
       sKgh[u] = sk;
