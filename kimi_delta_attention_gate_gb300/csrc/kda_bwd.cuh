@@ -788,9 +788,17 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       const int i = e / ldA, cc = e - (e / ldA) * ldA;
       sA[e] = cc == i ? 1.f : 0.f;
     }
-    batched<8>(tid, nthr, C * K, [&](int e) { return W[e]; }, [&](int e, float v) {
-      sX[(size_t)(e / K) * nrhs + (e - (e / K) * K)] = v;
-    });
+    if (vecK && (nrhs & 3) == 0) {  // W's rows by 16-byte asynchronous copies
+      const int q = K / 4;
+      for (int e = tid; e < C * q; e += nthr) {
+        const int i = e / q, x4 = 4 * (e - (e / q) * q);
+        ex.copy16(sX + (size_t)i * nrhs + x4, W + (size_t)i * K + x4);
+      }
+    } else {
+      batched<8>(tid, nthr, C * K, [&](int e) { return W[e]; }, [&](int e, float v) {
+        sX[(size_t)(e / K) * nrhs + (e - (e / K) * K)] = v;
+      });
+    }
     const int v4 = (V + 3) / 4;
     batched<4>(tid, nthr, C * v4, [&](int e) {  // beta V, four columns of v per element
       const int i = e / v4, c4 = 4 * (e - (e / v4) * v4);
@@ -801,6 +809,7 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       const float bt = i < L ? Be[i] : 0.f;
       for (int y = 0; y < 4 && c4 + y < V; ++y) sX[(size_t)i * nrhs + K + c4 + y] = bt * f4at(x, y);
     });
+    ex.copy_wait();
   });
   // each block's rows solved within the block (one thread per column), then the later rows
   // updated with the block's solution in 4 x 4 tiles (every thread)
@@ -897,31 +906,46 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
     }
     if (p.tc_states) {  // the tensor-core state stage's operand tiles (K = 128, C = 64)
       char* tile = tile_ptr(a, c, hv);
-      for (int u = tid; u < C * (K / 8); u += nthr) {  // -W: row = token, 8 channels per chunk
-        const int i = u / (K / 8), k0 = 8 * (u - (u / (K / 8)) * (K / 8));
-        float x[8];
-        for (int j = 0; j < 8; ++j) x[j] = -W[(size_t)i * K + k0 + j];
-        put_hilo8(tile, kTileNegW + (size_t)(k0 >> 6) * 8192 + swz128((uint32_t)i, (uint32_t)(k0 & 63)), x);
-      }
-      for (int u = tid; u < K * (C / 8); u += nthr) {  // Kg^T: row = channel, 8 tokens per chunk
-        const int kk = u / (C / 8), t0 = 8 * (u - (u / (C / 8)) * (C / 8));
-        float x[8];
-        for (int j = 0; j < 8; ++j) x[j] = Kg[(size_t)(t0 + j) * K + kk];
-        put_hilo8(tile, kTileKgT + swz128((uint32_t)kk, (uint32_t)t0), x);
-      }
+      // eight consecutive floats of a row, loaded for four items per thread before any store
+      struct R8 { float v[8]; };
+      auto row8 = [&](const float* src, float sign) {
+        const F4 x0 = ld4w(src, 0, 8, true), x1 = ld4w(src, 4, 8, true);
+        return R8{{sign * x0.x, sign * x0.y, sign * x0.z, sign * x0.w,
+                   sign * x1.x, sign * x1.y, sign * x1.z, sign * x1.w}};
+      };
+      const int k8 = K / 8, c8 = C / 8;
+      batched<4>(tid, nthr, C * k8, [&](int u) {  // -W: row = token, 8 channels per piece
+        const int i = u / k8, k0 = 8 * (u - (u / k8) * k8);
+        return row8(W + (size_t)i * K + k0, -1.f);
+      }, [&](int u, const R8& x) {
+        const int i = u / k8, k0 = 8 * (u - (u / k8) * k8);
+        put_hilo8(tile, kTileNegW + (size_t)(k0 >> 6) * 8192 + swz128((uint32_t)i, (uint32_t)(k0 & 63)), x.v);
+      });
+      batched<4>(tid, nthr, K * c8, [&](int u) {  // Kg^T: row = channel, 8 tokens per piece
+        const int kk = u / c8, t0 = 8 * (u - (u / c8) * c8);
+        R8 x;
+        KDA_UNROLL
+        for (int j = 0; j < 8; ++j) x.v[j] = Kg[(size_t)(t0 + j) * K + kk];
+        return x;
+      }, [&](int u, const R8& x) {
+        const int kk = u / c8, t0 = 8 * (u - (u / c8) * c8);
+        put_hilo8(tile, kTileKgT + swz128((uint32_t)kk, (uint32_t)t0), x.v);
+      });
       if (p.tc_dstate) {
-        for (int u = tid; u < C * (C / 8); u += nthr) {  // Aqk: row = token, 8 tokens per chunk
-          const int i = u / (C / 8), j0 = 8 * (u - (u / (C / 8)) * (C / 8));
-          float x[8];
-          for (int j = 0; j < 8; ++j) x[j] = Aqk[(size_t)i * C + j0 + j];
-          put_hilo8(tile, kTileAqk + swz128((uint32_t)i, (uint32_t)j0), x, kTileAqkLo);
-        }
-        for (int u = tid; u < C * (K / 8); u += nthr) {  // Qg: row = token, 8 channels per chunk
-          const int i = u / (K / 8), k0 = 8 * (u - (u / (K / 8)) * (K / 8));
-          float x[8];
-          for (int j = 0; j < 8; ++j) x[j] = Qg[(size_t)i * K + k0 + j];
-          put_hilo8(tile, kTileQg + (size_t)(k0 >> 6) * 8192 + swz128((uint32_t)i, (uint32_t)(k0 & 63)), x);
-        }
+        batched<4>(tid, nthr, C * c8, [&](int u) {  // Aqk: row = token, 8 tokens per piece
+          const int i = u / c8, j0 = 8 * (u - (u / c8) * c8);
+          return row8(Aqk + (size_t)i * C + j0, 1.f);
+        }, [&](int u, const R8& x) {
+          const int i = u / c8, j0 = 8 * (u - (u / c8) * c8);
+          put_hilo8(tile, kTileAqk + swz128((uint32_t)i, (uint32_t)j0), x.v, kTileAqkLo);
+        });
+        batched<4>(tid, nthr, C * k8, [&](int u) {  // Qg: row = token, 8 channels per piece
+          const int i = u / k8, k0 = 8 * (u - (u / k8) * k8);
+          return row8(Qg + (size_t)i * K + k0, 1.f);
+        }, [&](int u, const R8& x) {
+          const int i = u / k8, k0 = 8 * (u - (u / k8) * k8);
+          put_hilo8(tile, kTileQg + (size_t)(k0 >> 6) * 8192 + swz128((uint32_t)i, (uint32_t)(k0 & 63)), x.v);
+        });
       }
     }
   });
