@@ -10,6 +10,7 @@
 
 #include "kda_bwd.cuh"
 #include "kda_internal.cuh"
+#include "tc_common.cuh"
 
 namespace kda {
 
@@ -18,7 +19,17 @@ unsigned int* device_status_word();  // kda_api.cu
 namespace bwd {
 namespace {
 
+// fp32 pair -> bf16 hi / lo pairs (x = hi + lo to about 2^-16)
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 struct GpuExec {
+  static constexpr bool kTensorCores = true;
   template <class F>
   __device__ __forceinline__ void phase(F&& f) {
     f((int)threadIdx.x, (int)blockDim.x);
@@ -39,6 +50,126 @@ struct GpuExec {
   // wait for every copy this thread has issued
   __device__ __forceinline__ void copy_wait() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  }
+
+  // Z = X V^T + Y (e^Gamma K)^T for chunk 64, K = V = 128 on the tensor cores (every thread of
+  // the block; called outside a phase): per 64-column slice of v, then of k, the rows of X
+  // (or Y) and of v (or e^Gamma K) become bf16 hi / lo tiles in the 128-byte-swizzled K-major
+  // layout (v in bf16 is exact: its high part alone), one thread issues the M = 64, N = 64
+  // MMAs (hi hi + lo hi + hi lo) into a tensor-memory accumulator, and the block waits for
+  // them before the next slice's tiles; then the accumulator's rows go to sZ.  scratch: at
+  // least 33 KB; sTc: 32 bytes (barrier, TMEM address).
+  __device__ void zprod(float* sZ, int ldz, float* scratch, float* sTc, const float* X,
+                        const float* Y, const void* v_in, size_t v_row0, size_t v_stride,
+                        int dtype, const float* EK, int L, unsigned int* status) {
+    using namespace tc;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint8_t* tiles = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(scratch) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sTc);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(sTc + 2);
+    if (warp == 0) {
+      tmem_alloc(slot, 64);
+      tmem_relinquish();
+    }
+    if (tid == 0) {
+      mbar_init(bar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    const uint32_t t_ah = smem_u32(tiles), t_al = t_ah + 8192u, t_bh = t_ah + 16384u,
+                   t_bl = t_ah + 24576u;
+    const bool v_exact = dtype == KDA_BF16;
+    bool ok = true;
+    int open = -1;  // (thread 0) the slice whose MMA group is issued and not yet seen done
+    for (int s = 0; s < 4 && ok; ++s) {
+      const bool onv = s < 2;
+      const int o0 = 64 * (s & 1);
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {  // rows r, 8-column groups g: 512 items
+        const int u = tid + 256 * it, r = u >> 3, g = u & 7;
+        const uint32_t off = swz128((uint32_t)r, (uint32_t)(8 * g));
+        {
+          const float* src = (onv ? X : Y) + (size_t)r * 128 + o0 + 8 * g;
+          const float4 x0 = *reinterpret_cast<const float4*>(src);
+          const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+          uint4 h, l;
+          split_pair(x0.x, x0.y, h.x, l.x);
+          split_pair(x0.z, x0.w, h.y, l.y);
+          split_pair(x1.x, x1.y, h.z, l.z);
+          split_pair(x1.z, x1.w, h.w, l.w);
+          *reinterpret_cast<uint4*>(tiles + off) = h;
+          *reinterpret_cast<uint4*>(tiles + 8192 + off) = l;
+        }
+        uint4 h = make_uint4(0u, 0u, 0u, 0u), l = h;
+        if (onv && v_exact) {
+          if (r < L)
+            h = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(v_in) + v_row0 +
+                                                     (size_t)r * v_stride + o0 + 8 * g));
+        } else {
+          float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+          if (!onv) {
+            const float* src = EK + (size_t)r * 128 + o0 + 8 * g;
+            x0 = *reinterpret_cast<const float4*>(src);
+            x1 = *reinterpret_cast<const float4*>(src + 4);
+          } else if (r < L) {
+            const float* src = static_cast<const float*>(v_in) + v_row0 + (size_t)r * v_stride + o0 + 8 * g;
+            x0 = __ldg(reinterpret_cast<const float4*>(src));
+            x1 = __ldg(reinterpret_cast<const float4*>(src + 4));
+          }
+          split_pair(x0.x, x0.y, h.x, l.x);
+          split_pair(x0.z, x0.w, h.y, l.y);
+          split_pair(x1.x, x1.y, h.z, l.z);
+          split_pair(x1.z, x1.w, h.w, l.w);
+        }
+        *reinterpret_cast<uint4*>(tiles + 16384 + off) = h;
+        *reinterpret_cast<uint4*>(tiles + 24576 + off) = l;
+      }
+      fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(64, 64);
+        const bool b_lo = !(onv && v_exact);
+#pragma unroll 1
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t o = (uint32_t)ks * 32u;
+          const uint64_t Ah = sdesc_sw128(t_ah + o, 16, 1024), Al = sdesc_sw128(t_al + o, 16, 1024);
+          const uint64_t Bh = sdesc_sw128(t_bh + o, 16, 1024), Bl = sdesc_sw128(t_bl + o, 16, 1024);
+          mma_bf16(tmem, Ah, Bh, id, (s > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16(tmem, Al, Bh, id, 1);
+          if (b_lo) mma_bf16(tmem, Ah, Bl, id, 1);
+        }
+        mma_commit(bar);
+        open = s;
+      }
+      if (!mbar_wait(bar, (uint32_t)(s & 1))) ok = false;
+      else if (tid == 0) open = -1;
+      ok = named_bar_and(1, (int)blockDim.x, ok);  // the tiles are free for the next slice
+      tc_fence_after();
+    }
+    if (ok) {  // rows 16 q + lane (lanes 0-15 of quadrant q = warp % 4); warp / 4: column half
+      const int q = warp & 3, half = warp >> 2, i = 16 * q + lane;
+      const uint32_t lb = tmem_addr(tmem, 32 * q, 0);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t r[16];
+        tmem_ld16(lb + 32 * half + 16 * j, r);
+        tmem_wait_ld();
+        if (lane < 16) {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) sZ[(size_t)i * ldz + 32 * half + 16 * j + x] = __uint_as_float(r[x]);
+        }
+      }
+    } else if (tid == 0) {
+      atomicOr(status, KDA_DEV_TIMEOUT);
+      if (open >= 0) mbar_wait(bar, (uint32_t)(open & 1), 100000000ull);  // in flight: ends first
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
   }
 };
 

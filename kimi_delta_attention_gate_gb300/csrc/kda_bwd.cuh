@@ -284,7 +284,7 @@ inline size_t grads_region(const Plan& p) {
   return slices > after ? slices : after;
 }
 inline size_t grads_smem(const Plan& p) {
-  return sizeof(float) * ((size_t)p.C * (p.C + 4) + 2 * (size_t)p.C + kThreads + 4 +
+  return sizeof(float) * ((size_t)p.C * (p.C + 4) + 2 * (size_t)p.C + kThreads + 12 +
                           (size_t)((p.K + 3) & ~3) + grads_region(p));
 }
 
@@ -1385,7 +1385,8 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   float* sDB = sB + C;                        // [C] gradient of beta (the value)
   float* sRed = sDB + C;                      // [kThreads] partial sums of dA_log
   float* sFlag = sRed + kThreads;             // [4] > 0: some block exponent out of range
-  float* sDgc = sFlag + 4;                    // [K4] diagonal of S dS'^T
+  float* sTc = sFlag + 4;                     // [8] the tensor-core product's barrier, TMEM slot
+  float* sDgc = sFlag + 12;                   // [K4] diagonal of S dS'^T
   float* sRg = sDgc + pad4(K);                // the product slices' staging, then:
   float* sAt = sRg;                           // [C][C] A^T: sAt[j][i] = A[i][j]
   float* sAk = sRg;                           // the same region, for the key rows later
@@ -1715,7 +1716,11 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   // A^T dA = X (beta V)^T + Y (beta e^Gamma K)^T over 64-column slices of v, then of k, staged
   // in shared memory and accumulated in sZ (lower blocks with the diagonal: its entries,
   // without beta, are the WY part of dbeta)
-  {
+  if constexpr (Exec::kTensorCores && SC == 64 && SK == 128 && SV == 128) {
+    // on the tensor cores: bf16 hi / lo operand tiles per 64-column slice in the scratch,
+    // the accumulator in tensor memory, then sZ
+    ex.zprod(sZ, ldz, sT, sTc, X, Y, a.v, in_row(0), (size_t)HV * V, a.dtype, EK, L, a.status);
+  } else {
     constexpr int ZW = 64, SLZ = 68;    // slice width; padded rows (17 16-byte units apart)
     float* sA = sT;                     // [C][SLZ] X (or Y) slice
     float* sBt = sA + (size_t)C * SLZ;  // [C][SLZ] v (or e^Gamma K) slice
@@ -1768,20 +1773,20 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
         }
       });
     }
-    // the diagonal is the WY part of dbeta; A^T dA = beta_j (...) strictly below it
-    ex.phase([&](int tid, int nthr) {
-      for (int e = tid; e < C * C; e += nthr) {
-        const int i = e / C, j = e - (e / C) * C;
-        float* z = sZ + (size_t)i * ldz + j;
-        if (j == i) {
-          sDB[i] = i < L ? *z : 0.f;
-          *z = 0.f;
-        } else {
-          *z = (i < L && j < i) ? sB[j] * *z : 0.f;
-        }
-      }
-    });
   }
+  // the diagonal is the WY part of dbeta; A^T dA = beta_j (...) strictly below it
+  ex.phase([&](int tid, int nthr) {
+    for (int e = tid; e < C * C; e += nthr) {
+      const int i = e / C, j = e - (e / C) * C;
+      float* z = sZ + (size_t)i * ldz + j;
+      if (j == i) {
+        sDB[i] = i < L ? *z : 0.f;
+        *z = 0.f;
+      } else {
+        *z = (i < L && j < i) ? sB[j] * *z : 0.f;
+      }
+    }
+  });
   // dAkk = -(A^T dA A^T) masked strictly lower: M[r][i] = sum_j Z[r][j] A[i][j] for i < r with
   // Z = A^T dA (sZ, strictly lower) and A lower triangular, so j < min(r, i + 1); 4 x 4 tiles
   // of (rows r, columns i), a warp's lanes taking consecutive column tiles of one row tile

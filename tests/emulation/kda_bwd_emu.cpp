@@ -28,6 +28,7 @@ using kda::bwd::Args;
 using kda::bwd::Plan;
 
 struct HostExec {
+  static constexpr bool kTensorCores = false;  // the CUDA-core forms of every product
   int nthr = kda::bwd::kThreads;
   std::mt19937* rng = nullptr;
   std::vector<int> order;
