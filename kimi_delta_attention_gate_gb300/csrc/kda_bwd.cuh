@@ -79,7 +79,8 @@ struct Block {
   size_t gam, qn, kn, qg, kg, w, y, dq, dk, dgam, dkg;  // [C][K]
   size_t u, vn, dvn, x;                                  // [C][V]
   size_t aqk, p, ati;                                    // [C][C]
-  size_t beta, decay;                                    // [C], [K]
+  size_t qf, kf, kb;                                     // [C][K] block-referenced rows
+  size_t beta, decay, flag;                              // [C], [K], [4]
   size_t floats;                                         // a multiple of 64 (256 bytes)
 };
 
@@ -105,8 +106,12 @@ KDA_HD Block block_layout(int C, int K, int V) {
   b.aqk = o; o += cc;   // Aqk
   b.p = o; o += cc;     // P (strictly lower, without beta)
   b.ati = o; o += cc;   // A^T, A = (I + Diag(beta) P)^-1 (rows and columns >= L zero)
+  b.qf = o; o += ck;    // Q e^(Gamma - rho_B), B the row's 16-row block (from prep)
+  b.kf = o; o += ck;    // K e^(Gamma - rho_B)
+  b.kb = o; o += ck;    // K e^(rho_B - Gamma)
   b.beta = o; o += C;
   b.decay = o; o += K;  // e^gamma_C
+  b.flag = o; o += 4;   // > 0: some block-referenced exponent out of range (from prep)
   b.floats = (o + 63) / 64 * 64;
   return b;
 }
@@ -681,12 +686,15 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       W[e] = w;
     });
   });
+  float* QFw = blk + b.qf;
+  float* KFw = blk + b.kf;
+  float* KBw = blk + b.kb;
   // The block-referenced operands of Aqk and P, in place in shared memory: QF = Q e^(Gamma -
   // rho_B), KF = K e^(Gamma - rho_B) and KB = K e^(rho_B - Gamma) (B the row's block), and
   // F_IB = e^(rho_I - rho_B) for B < I, so that Aqk[i][j] = sum_k QF_i KB_j F_IB and P[i][j] =
   // sum_k KF_i KB_j F_IB with I, B the blocks of i, j need no exponential per (i, j, k).  Any
   // exponent beyond 60 (QF, KB, F, or the product KB F = K e^(rho_I - Gamma_j)) sends the
-  // chunk to the direct evaluation.
+  // chunk to the direct evaluation.  The three go to the workspace too, with the range flag.
   ex.phase([&](int tid, int nthr) {
     for (int u = tid; u < (NB * (NB - 1) / 2) * K; u += nthr) {
       const int pr = u / K, kk = u - pr * K;
@@ -704,10 +712,16 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       for (int I = B; I < NB; ++I) bad = bad || sRho[(size_t)I * K + kk] - g > 60.f;
       if (bad) ex.atomic_add(sFlag, 1.f);
       const float f = fexp(g - rho), kv = sKn[o];
-      sQn[o] *= f;
-      sKn[o] = kv * f;
-      sGam[o] = kv * fexp(rho - g);
+      const float qf = sQn[o] * f, kf = kv * f, kb = kv * fexp(rho - g);
+      sQn[o] = qf;
+      sKn[o] = kf;
+      sGam[o] = kb;
+      // the same rows for the gradient stage's e^(Gamma_i - Gamma_j) sums
+      QFw[e] = qf;
+      KFw[e] = kf;
+      KBw[e] = kb;
     }
+    for (int e = L * K + tid; e < C * K; e += nthr) QFw[e] = KFw[e] = KBw[e] = 0.f;
   });
   const int CB = C / 4;
   if (sFlag[0] == 0.f) {
@@ -783,6 +797,7 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   float* sX = sA + (size_t)C * ldA;   // [C][K + V] the right-hand sides of W and U
   const int nrhs = K + V;
   ex.phase([&](int tid, int nthr) {
+    if (tid == 0) blk[b.flag] = sFlag[0];
     batched<8>(tid, nthr, C * C, [&](int e) { return Be[e / C] * P[e]; }, [&](int e, float v) { sP[e] = v; });
     for (int e = tid; e < C * ldA; e += nthr) {
       const int i = e / ldA, cc = e - (e / ldA) * ldA;
@@ -1374,8 +1389,9 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   float* dGam = blk + b.dgam;
   float* dKG = blk + b.dkg;
   float* EK = blk + b.w;   // e^Gamma K (the W slot: W is not needed any more)
-  float* QF = blk + b.qg;  // Q e^(Gamma - rho), K e^(Gamma - rho) once Qg, Kg are consumed
-  float* KF = blk + b.kg;
+  const float* QF = blk + b.qf;  // the recompute stage's block-referenced rows
+  const float* KF = blk + b.kf;
+  const float* KB = blk + b.kb;
   const float* S = state_ptr(a, p.off_h, c, hv);
   const float* dSp = state_ptr(a, p.off_dh, c, hv);
   const int ldz = C + 1;                      // padded rows: the row-per-thread substitution
@@ -1840,10 +1856,8 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
       sRed[u] = db;
     }
   });
-  // block references rho (Gamma at each 16-row block's middle row), Q and K scaled by
-  // e^(Gamma - rho), the keys scaled by e^(rho - Gamma) (row j of block B: K_j e^(rho_B -
-  // Gamma_j), in shared memory: rows below kbA in beta P's dead region, the rest after dP^T),
-  // and the range check of every exponent the blocked sums use; dP transposed
+  // the recompute stage's rows K_j e^(rho_B - Gamma_j) (B the block of j) in shared memory:
+  // rows below kbA in beta P's dead region, the rest after dP^T; its range flag; dP transposed
   const int kbA = (C * C) / K;
   auto kb_row = [&](int j) -> float* {
     return j < kbA ? sAk + (size_t)j * K : sT + (size_t)C * lda + (size_t)(j - kbA) * K;
@@ -1858,52 +1872,21 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
       const int i = e / C, j = e - (e / C) * C;
       sZt[(size_t)j * lda + i] = sZ[(size_t)i * ldz + j];
     }
-    // Gamma at the middle rows of the (at most four) blocks, row i's own Gamma, q and k
-    struct Ref { float gm[4], gi, qn, kn; };
-    const int NBk = (L + 15) >> 4;
-    batched<4>(tid, nthr, C * K, [&](int e) {
-      const int i = e / K, kk = e - (e / K) * K;
-      Ref r{{0.f, 0.f, 0.f, 0.f}, 0.f, 0.f, 0.f};
-      if (i < L) {
-        KDA_UNROLL
-        for (int R = 0; R < 4; ++R) {
-          const int mr = (16 * R + 7) < L - 1 ? 16 * R + 7 : L - 1;
-          if (R < NBk) r.gm[R] = Gam[(size_t)mr * K + kk];
-        }
-        r.gi = Gam[e];
-        r.qn = Qn[e];
-        r.kn = Kn[e];
+    // the recompute stage's K e^(rho_B - Gamma) rows and its range flag
+    if (tid == 0) sFlag[0] = blk[b.flag];
+    if (vecK) {
+      const int q = K / 4;
+      for (int e = tid; e < C * q; e += nthr) {
+        const int j = e / q, x4 = 4 * (e - (e / q) * q);
+        ex.copy16(kb_row(j) + x4, KB + (size_t)j * K + x4);
       }
-      return r;
-    }, [&](int e, const Ref& r) {
-      const int i = e / K;
-      float qf = 0.f, kf = 0.f;
-      if (i < L) {
-        const int B = i >> 4;
-        float rho = r.gm[0];
-        bool bad = false;
-        // rho_R - Gamma_i for every block R whose rows see row i (R >= B)
-        KDA_UNROLL
-        for (int R = 0; R < 4; ++R) {
-          if (R == B) rho = r.gm[R];
-          if (R >= B && R < NBk) bad = bad || r.gm[R] - r.gi > 60.f;
-        }
-        // and rho_R - rho_B, the factor between a key's own reference and a later block's
-        KDA_UNROLL
-        for (int R = 0; R < 4; ++R)
-          if (R > B && R < NBk) bad = bad || r.gm[R] - rho > 60.f;
-        bad = bad || r.gi - rho > 60.f;
-        if (bad) ex.atomic_add(sFlag, 1.f);
-        const float f = fexp(r.gi - rho);
-        qf = r.qn * f;
-        kf = r.kn * f;
-        kb_row(i)[e - (size_t)i * K] = r.kn * fexp(rho - r.gi);
-      } else {
-        kb_row(i)[e - (size_t)i * K] = 0.f;
+      ex.copy_wait();
+    } else {
+      for (int e = tid; e < C * K; e += nthr) {
+        const int j = e / K, kk = e - (e / K) * K;
+        kb_row(j)[kk] = KB[e];
       }
-      QF[e] = qf;
-      KF[e] = kf;
-    });
+    }
   });
   if (sFlag[0] == 0.f) {
     // the e^(Gamma_i - Gamma_j) terms of Aqk and P, one thread per (8-row half H of a 16-row

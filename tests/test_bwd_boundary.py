@@ -89,10 +89,11 @@ def test_output_o_and_states_of_the_forward_block_are_not_needed(lib):
 
 
 def test_workspace_follows_the_chunk_count(lib):
-    """Per (chunk, value head): the recomputed intermediates (with Aqk, P and A^T as C x C),
-    then the state before and the state gradient after the chunk (K V fp32 each)."""
+    """Per (chunk, value head): the recomputed intermediates (with Aqk, P and A^T as C x C and
+    the block-referenced Q / K rows as three C x K, plus a range flag), then the state before
+    and the state gradient after the chunk (K V fp32 each)."""
     C, K, V = 64, 128, 64
-    block = 4 * (11 * C * K + 4 * C * V + 3 * C * C + C + K)
+    block = 4 * (14 * C * K + 4 * C * V + 3 * C * C + C + K + 4)
     block = (block + 255) // 256 * 256
     per_chunk_head = block + 2 * 4 * K * V
     a = kb.kda_bwd_workspace_size(params(fwd_T=64))            # 2 sequences x 1 chunk x 4 heads
