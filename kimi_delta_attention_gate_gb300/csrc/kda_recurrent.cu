@@ -19,6 +19,7 @@
 // memory in fp32.
 
 #include "kda_internal.cuh"
+#include "tc_common.cuh"
 
 namespace kda {
 
@@ -414,6 +415,156 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_k128_kernel(const FwdAr
   }
 }
 
+// K = V = 128 with the [K][V] state layout, the state in shared memory: one CTA per (sequence,
+// value head) whose 64 KB state arrives by one bulk copy and leaves by one, so that the load /
+// store units only carry the token's vectors; thread t owns column v = t % 128 over the rows of
+// half t / 128, and a token is two passes over the state (S <- Diag(alpha) S with S^T k; then
+// S <- S + k u^T with S^T q), the halves' column sums meeting in shared memory.  64 KB + 3 KB of
+// shared memory: three CTAs per SM.
+constexpr uint32_t kBulkStateBytes = 128 * 128 * 4;
+constexpr size_t kBulkSmem = kBulkStateBytes + sizeof(float) * (4 * 128 + 2 * 256 + 2 * kWarps + 4) + 16;
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads) recurrent_k128_bulk_kernel(const FwdArgs a) {
+  constexpr int K = 128, V = 128;
+  extern __shared__ __align__(16) float rsm[];
+  float* sS = rsm;              // [K][V]
+  float* sQ = sS + K * V;       // [K] q, k as loaded; alpha; v
+  float* sK = sQ + K;
+  float* sA = sK + K;
+  float* sV = sA + K;
+  float* sP = sV + V;           // [2][V] half sums of S^T k
+  float* sO = sP + 2 * V;       // [2][V] half sums of S^T q
+  float* sPart = sO + 2 * V;    // [2][kWarps]
+  float* sBeta = sPart + 2 * kWarps;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sBeta + 4);
+  const Plan& p = a.plan;
+  const int HV = p.HV, H = p.H;
+  const int hv = (int)(blockIdx.x % HV);
+  const int n = (int)(blockIdx.x / HV);
+  const int h = hv / p.G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int v = tid & (V - 1), hf = tid >> 7;
+  int64_t bos, eos;
+  if (p.varlen) {
+    bos = a.cu_seqlens[n];
+    eos = a.cu_seqlens[n + 1];
+  } else {
+    bos = (int64_t)n * p.T;
+    eos = bos + p.T;
+  }
+  if (bos < 0 || eos < bos || eos > p.ntok) {
+    if (tid == 0) flag_status(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const Tin* gq = static_cast<const Tin*>(a.q);
+  const Tin* gk = static_cast<const Tin*>(a.k);
+  const Tin* gv = static_cast<const Tin*>(a.v);
+  const Tin* gg = static_cast<const Tin*>(a.g);
+  const Tin* gb = static_cast<const Tin*>(a.beta);
+  Tin* go = static_cast<Tin*>(a.o);
+  const size_t sbase = ((size_t)n * HV + hv) * (size_t)K * V;
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  bool pending = a.h0 != nullptr;  // the state's bulk copy has not been waited for yet
+  if (pending) {
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(bar, kBulkStateBytes);
+      tc::bulk_g2s(sS, a.h0 + sbase, kBulkStateBytes, bar);
+    }
+  } else {
+    for (int e = tid; e < K * V / 4; e += kThreads)
+      reinterpret_cast<float4*>(sS)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  bool ok = true;
+  const float a_exp = (a.gate_mode != KDA_GATE_PREGATED && a.A_log != nullptr) ? expf(a.A_log[hv]) : 1.f;
+  for (int64_t t = bos; t < eos; ++t) {
+    if (tid < K) {
+      const float qi = to_f32(gq[(t * H + h) * (int64_t)K + tid]);
+      const float ki = to_f32(gk[(t * H + h) * (int64_t)K + tid]);
+      const float gi = to_f32(gg[(t * HV + hv) * (int64_t)K + tid]);
+      const float dt = (a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED)
+                           ? a.dt_bias[(size_t)hv * K + tid] : 0.f;
+      sQ[tid] = qi;
+      sK[tid] = ki;
+      sA[tid] = expf(gate_exact(a.gate_mode, gi, a_exp, dt, a.lower_bound));
+      sV[tid] = to_f32(gv[(t * HV + hv) * (int64_t)V + tid]);
+      if (a.qk_l2norm) {
+        const float sq = warp_sum_all(qi * qi), sk = warp_sum_all(ki * ki);
+        if (lane == 0) {
+          sPart[warp] = sq;
+          sPart[kWarps + warp] = sk;
+        }
+      }
+    }
+    if (tid == 0) {
+      float b = to_f32(gb[t * HV + hv]);
+      if (a.beta_sigmoid) b = (a.allow_neg_eigval ? 2.f : 1.f) * sigmoid_exact(b);
+      sBeta[0] = b;
+    }
+    if (pending) {  // the first token's vectors were loaded while the state arrived
+      if (!tc::mbar_wait(bar, 0)) ok = false;
+      pending = false;
+    }
+    __syncthreads();
+    float qn = a.scale, kn = 1.f;
+    if (a.qk_l2norm) {
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int w = 0; w < K / 32; ++w) {
+        sq += sPart[w];
+        sk += sPart[kWarps + w];
+      }
+      qn *= rsqrtf(sq + 1e-6f);
+      kn = rsqrtf(sk + 1e-6f);
+    }
+    // S <- Diag(alpha) S and this half's rows of S^T k
+    float acc = 0.f;
+    float* col = sS + (size_t)(64 * hf) * V + v;
+#pragma unroll 8
+    for (int r = 0; r < 64; ++r) {
+      const float s_ = col[(size_t)r * V] * sA[64 * hf + r];
+      col[(size_t)r * V] = s_;
+      acc = fmaf(s_, sK[64 * hf + r], acc);
+    }
+    sP[hf * V + v] = acc;
+    __syncthreads();
+    // u = kn beta (v - kn S^T k); S <- S + k u^T (k_hat u^T with k_hat = kn k); S^T q
+    const float u = kn * (sBeta[0] * (sV[v] - kn * (sP[v] + sP[V + v])));
+    acc = 0.f;
+#pragma unroll 8
+    for (int r = 0; r < 64; ++r) {
+      const float s_ = fmaf(sK[64 * hf + r], u, col[(size_t)r * V]);
+      col[(size_t)r * V] = s_;
+      acc = fmaf(s_, sQ[64 * hf + r], acc);
+    }
+    sO[hf * V + v] = acc;
+    __syncthreads();
+    if (tid < V) go[(t * HV + hv) * (int64_t)V + tid] = from_f32<Tin>(qn * (sO[tid] + sO[V + tid]));
+    __syncthreads();  // the next token rewrites the shared vectors
+  }
+  if (pending && !tc::mbar_wait(bar, 0)) ok = false;  // no token: the state passes through
+  ok = __syncthreads_and(ok) != 0;
+  if (!ok) {
+    if (tid == 0) {
+      flag_status(a.status, KDA_DEV_TIMEOUT);
+      tc::mbar_wait(bar, 0, 100000000ull);  // the copy in flight lands before the CTA leaves
+    }
+    return;
+  }
+  if (a.final_state != nullptr) {
+    tc::fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc::bulk_s2g(a.final_state + sbase, sS, kBulkStateBytes);
+      tc::bulk_commit();
+      tc::bulk_wait_read0();
+    }
+  }
+}
+
 }  // namespace
 
 size_t recurrent_smem_bytes(int K) {
@@ -426,12 +577,20 @@ cudaError_t launch_recurrent(const FwdArgs& a, cudaStream_t s) {
     const int nvr = (p.V + kRegCols - 1) / kRegCols;
     const size_t blocks = (size_t)p.N * p.HV * nvr;
     if (blocks == 0) return cudaSuccess;
-    if (p.K == 128 && p.V == 128 && !a.state_v_first) {  // 16-byte state accesses
+    if (p.K == 128 && p.V == 128 && !a.state_v_first) {  // the state by bulk copies
       const unsigned nb = (unsigned)((size_t)p.N * p.HV);
-      if (a.dtype == KDA_BF16)
-        recurrent_k128_kernel<__nv_bfloat16><<<nb, kThreads, 0, s>>>(a);
-      else
-        recurrent_k128_kernel<float><<<nb, kThreads, 0, s>>>(a);
+      cudaError_t e;
+      if (a.dtype == KDA_BF16) {
+        e = cudaFuncSetAttribute(recurrent_k128_bulk_kernel<__nv_bfloat16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmem);
+        if (e != cudaSuccess) return e;
+        recurrent_k128_bulk_kernel<__nv_bfloat16><<<nb, kThreads, kBulkSmem, s>>>(a);
+      } else {
+        e = cudaFuncSetAttribute(recurrent_k128_bulk_kernel<float>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmem);
+        if (e != cudaSuccess) return e;
+        recurrent_k128_bulk_kernel<float><<<nb, kThreads, kBulkSmem, s>>>(a);
+      }
       return cudaGetLastError();
     }
     if (a.dtype == KDA_BF16)
