@@ -422,9 +422,11 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_k128_kernel(const FwdAr
 // S <- S + k u^T with S^T q), the halves' column sums meeting in shared memory.  64 KB + 3 KB of
 // shared memory: three CTAs per SM.
 constexpr uint32_t kBulkStateBytes = 128 * 128 * 4;
-constexpr size_t kBulkSmem = kBulkStateBytes + sizeof(float) * (4 * 128 + 2 * 256 + 2 * kWarps + 4) + 16;
+constexpr int kBulkThreads = 512, kBulkSplit = kBulkThreads / 128, kBulkRows = 128 / kBulkSplit;
+constexpr size_t kBulkSmem =
+    kBulkStateBytes + sizeof(float) * (4 * 128 + 2 * kBulkSplit * 128 + 2 * kWarps + 4) + 16;
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads) recurrent_k128_bulk_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(kBulkThreads) recurrent_k128_bulk_kernel(const FwdArgs a) {
   constexpr int K = 128, V = 128;
   extern __shared__ __align__(16) float rsm[];
   float* sS = rsm;              // [K][V]
@@ -432,9 +434,9 @@ __global__ void __launch_bounds__(kThreads) recurrent_k128_bulk_kernel(const Fwd
   float* sK = sQ + K;
   float* sA = sK + K;
   float* sV = sA + K;
-  float* sP = sV + V;           // [2][V] half sums of S^T k
-  float* sO = sP + 2 * V;       // [2][V] half sums of S^T q
-  float* sPart = sO + 2 * V;    // [2][kWarps]
+  float* sP = sV + V;                   // [kBulkSplit][V] partial sums of S^T k
+  float* sO = sP + kBulkSplit * V;      // [kBulkSplit][V] partial sums of S^T q
+  float* sPart = sO + kBulkSplit * V;   // [2][kWarps]
   float* sBeta = sPart + 2 * kWarps;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sBeta + 4);
   const Plan& p = a.plan;
@@ -443,7 +445,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_k128_bulk_kernel(const Fwd
   const int n = (int)(blockIdx.x / HV);
   const int h = hv / p.G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int v = tid & (V - 1), hf = tid >> 7;
+  const int v = tid & (V - 1), hf = tid >> 7;  // hf: this thread's group of kBulkRows rows
   int64_t bos, eos;
   if (p.varlen) {
     bos = a.cu_seqlens[n];
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_k128_bulk_kernel(const Fwd
       tc::bulk_g2s(sS, a.h0 + sbase, kBulkStateBytes, bar);
     }
   } else {
-    for (int e = tid; e < K * V / 4; e += kThreads)
+    for (int e = tid; e < K * V / 4; e += kBulkThreads)
       reinterpret_cast<float4*>(sS)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   bool ok = true;
@@ -522,27 +524,36 @@ __global__ void __launch_bounds__(kThreads) recurrent_k128_bulk_kernel(const Fwd
     }
     // S <- Diag(alpha) S and this half's rows of S^T k
     float acc = 0.f;
-    float* col = sS + (size_t)(64 * hf) * V + v;
+    const int r0 = kBulkRows * hf;
+    float* col = sS + (size_t)r0 * V + v;
 #pragma unroll 8
-    for (int r = 0; r < 64; ++r) {
-      const float s_ = col[(size_t)r * V] * sA[64 * hf + r];
+    for (int r = 0; r < kBulkRows; ++r) {
+      const float s_ = col[(size_t)r * V] * sA[r0 + r];
       col[(size_t)r * V] = s_;
-      acc = fmaf(s_, sK[64 * hf + r], acc);
+      acc = fmaf(s_, sK[r0 + r], acc);
     }
     sP[hf * V + v] = acc;
     __syncthreads();
     // u = kn beta (v - kn S^T k); S <- S + k u^T (k_hat u^T with k_hat = kn k); S^T q
-    const float u = kn * (sBeta[0] * (sV[v] - kn * (sP[v] + sP[V + v])));
+    float pk = 0.f;
+#pragma unroll
+    for (int x = 0; x < kBulkSplit; ++x) pk += sP[x * V + v];
+    const float u = kn * (sBeta[0] * (sV[v] - kn * pk));
     acc = 0.f;
 #pragma unroll 8
-    for (int r = 0; r < 64; ++r) {
-      const float s_ = fmaf(sK[64 * hf + r], u, col[(size_t)r * V]);
+    for (int r = 0; r < kBulkRows; ++r) {
+      const float s_ = fmaf(sK[r0 + r], u, col[(size_t)r * V]);
       col[(size_t)r * V] = s_;
-      acc = fmaf(s_, sQ[64 * hf + r], acc);
+      acc = fmaf(s_, sQ[r0 + r], acc);
     }
     sO[hf * V + v] = acc;
     __syncthreads();
-    if (tid < V) go[(t * HV + hv) * (int64_t)V + tid] = from_f32<Tin>(qn * (sO[tid] + sO[V + tid]));
+    if (tid < V) {
+      float o = 0.f;
+#pragma unroll
+      for (int x = 0; x < kBulkSplit; ++x) o += sO[x * V + tid];
+      go[(t * HV + hv) * (int64_t)V + tid] = from_f32<Tin>(qn * o);
+    }
     __syncthreads();  // the next token rewrites the shared vectors
   }
   if (pending && !tc::mbar_wait(bar, 0)) ok = false;  // no token: the state passes through
@@ -584,12 +595,12 @@ cudaError_t launch_recurrent(const FwdArgs& a, cudaStream_t s) {
         e = cudaFuncSetAttribute(recurrent_k128_bulk_kernel<__nv_bfloat16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmem);
         if (e != cudaSuccess) return e;
-        recurrent_k128_bulk_kernel<__nv_bfloat16><<<nb, kThreads, kBulkSmem, s>>>(a);
+        recurrent_k128_bulk_kernel<__nv_bfloat16><<<nb, kBulkThreads, kBulkSmem, s>>>(a);
       } else {
         e = cudaFuncSetAttribute(recurrent_k128_bulk_kernel<float>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmem);
         if (e != cudaSuccess) return e;
-        recurrent_k128_bulk_kernel<float><<<nb, kThreads, kBulkSmem, s>>>(a);
+        recurrent_k128_bulk_kernel<float><<<nb, kBulkThreads, kBulkSmem, s>>>(a);
       }
       return cudaGetLastError();
     }
