@@ -10,13 +10,14 @@
 // with q, k L2-normalised over K and beta = sigmoid(logit) (x2 with allow_neg_eigval) when
 // the flags ask for it.
 //
-// Two kernels.  For K <= 128 (recurrent_reg_kernel) the state lives in registers: one CTA per
-// (sequence, value head, 64 columns of V), each column held by 4 adjacent lanes that own its K
-// rows r = 4j + sub (32 fp32 values each), so that every reduction over K is two shuffles and
-// a token costs one block barrier; for decode the kernel is a stream of state
-// reads and writes.  For larger K (recurrent_kernel) one CTA per (sequence, value head, 32
-// columns of V); 8 warps split the K rows of the 32-column state tile, which stays in shared
-// memory in fp32.
+// Three kernels.  For K = V = 128 with the [K][V] state layout, the decode shape
+// (recurrent_k128_bulk_kernel), the state moves in and out of shared memory by one bulk copy
+// each.  Otherwise, for K <= 128 (recurrent_reg_kernel) the state lives in registers: one CTA
+// per (sequence, value head, 64 columns of V), each column held by 4 adjacent lanes that own
+// its K rows r = 4j + sub (32 fp32 values each), so that every reduction over K is two
+// shuffles and a token costs one block barrier.  For larger K (recurrent_kernel) one CTA per
+// (sequence, value head, 32 columns of V); 8 warps split the K rows of the 32-column state
+// tile, which stays in shared memory in fp32.
 
 #include "kda_internal.cuh"
 #include "tc_common.cuh"
@@ -276,142 +277,6 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_reg_kernel(const FwdArg
       const int r = kColLanes * j + sub;
       if (r < K) a.final_state[sidx(r)] = S[j];
     }
-  }
-}
-
-// K = V = 128 with the [K][V] state layout (the decode shape): one CTA per (sequence, value
-// head).  Warp w holds columns 16w..16w+15; lane = 4 x row lane rl + column group cg owns
-// columns 16w + 4cg .. +3 of rows 8j + rl (j < 16), so that every state access moves 16 bytes
-// and a warp instruction covers 8 rows x 64 contiguous bytes; reductions over K are three
-// shuffles (lane bits 2-4) per column.
-constexpr int kVecRows = 16;  // rows per lane
-template <typename Tin>
-__global__ void __launch_bounds__(kThreads, 2) recurrent_k128_kernel(const FwdArgs a) {
-  constexpr int K = 128, V = 128;
-  __shared__ float sQ[K], sK[K], sA[K];
-  __shared__ float sPart[2][kWarps];
-  __shared__ float sBeta;
-  const Plan& p = a.plan;
-  const int HV = p.HV, H = p.H;
-  const int hv = (int)(blockIdx.x % HV);
-  const int n = (int)(blockIdx.x / HV);
-  const int h = hv / p.G;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rl = lane >> 2, c0 = 16 * warp + 4 * (lane & 3);
-  int64_t bos, eos;
-  if (p.varlen) {
-    bos = a.cu_seqlens[n];
-    eos = a.cu_seqlens[n + 1];
-  } else {
-    bos = (int64_t)n * p.T;
-    eos = bos + p.T;
-  }
-  if (bos < 0 || eos < bos || eos > p.ntok) {
-    if (tid == 0) flag_status(a.status, KDA_DEV_BAD_SEQLENS);
-    return;
-  }
-  const Tin* gq = static_cast<const Tin*>(a.q);
-  const Tin* gk = static_cast<const Tin*>(a.k);
-  const Tin* gv = static_cast<const Tin*>(a.v);
-  const Tin* gg = static_cast<const Tin*>(a.g);
-  const Tin* gb = static_cast<const Tin*>(a.beta);
-  Tin* go = static_cast<Tin*>(a.o);
-  const size_t state_base = ((size_t)n * HV + hv) * (size_t)K * V + (size_t)rl * V + c0;
-  float4 S[kVecRows];  // rows 8j + rl, columns c0..c0+3
-#pragma unroll
-  for (int j = 0; j < kVecRows; ++j)
-    S[j] = a.h0 != nullptr
-               ? *reinterpret_cast<const float4*>(a.h0 + state_base + (size_t)8 * j * V)
-               : make_float4(0.f, 0.f, 0.f, 0.f);
-  const float a_exp = (a.gate_mode != KDA_GATE_PREGATED && a.A_log != nullptr) ? expf(a.A_log[hv]) : 1.f;
-
-  for (int64_t t = bos; t < eos; ++t) {
-    float qi = 0.f, ki = 0.f;
-    if (tid < K) {
-      qi = to_f32(gq[(t * H + h) * (int64_t)K + tid]);
-      ki = to_f32(gk[(t * H + h) * (int64_t)K + tid]);
-      const float gi = to_f32(gg[(t * HV + hv) * (int64_t)K + tid]);
-      const float dt = (a.dt_bias != nullptr && a.gate_mode != KDA_GATE_PREGATED)
-                           ? a.dt_bias[(size_t)hv * K + tid] : 0.f;
-      sQ[tid] = qi;
-      sK[tid] = ki;
-      sA[tid] = expf(gate_exact(a.gate_mode, gi, a_exp, dt, a.lower_bound));
-    }
-    float vv[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) vv[x] = to_f32(gv[(t * HV + hv) * (int64_t)V + c0 + x]);
-    if (a.qk_l2norm) {
-      const float sq = warp_sum_all(qi * qi), sk = warp_sum_all(ki * ki);
-      if (lane == 0) {
-        sPart[0][warp] = sq;
-        sPart[1][warp] = sk;
-      }
-    }
-    if (tid == 0) {
-      float b = to_f32(gb[t * HV + hv]);
-      if (a.beta_sigmoid) b = (a.allow_neg_eigval ? 2.f : 1.f) * sigmoid_exact(b);
-      sBeta = b;
-    }
-    __syncthreads();
-    float qn = a.scale, kn = 1.f;
-    if (a.qk_l2norm) {
-      float sq = 0.f, sk = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        sq += sPart[0][w];
-        sk += sPart[1][w];
-      }
-      qn *= rsqrtf(sq + 1e-6f);
-      kn = rsqrtf(sk + 1e-6f);
-    }
-    // S <- Diag(alpha) S and S^T k over this lane's rows, then over the 8 row lanes
-    float pp[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < kVecRows; ++j) {
-      const int r = 8 * j + rl;
-      const float al = sA[r], kr = sK[r];
-      S[j].x *= al; S[j].y *= al; S[j].z *= al; S[j].w *= al;
-      pp[0] = fmaf(S[j].x, kr, pp[0]);
-      pp[1] = fmaf(S[j].y, kr, pp[1]);
-      pp[2] = fmaf(S[j].z, kr, pp[2]);
-      pp[3] = fmaf(S[j].w, kr, pp[3]);
-    }
-    float ku[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) pp[x] += __shfl_xor_sync(0xffffffffu, pp[x], o);
-      ku[x] = kn * (sBeta * (vv[x] - kn * pp[x]));  // S <- S + k_hat u^T, k_hat = kn k
-    }
-    float oo[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < kVecRows; ++j) {
-      const int r = 8 * j + rl;
-      const float kr = sK[r], qr = sQ[r];
-      S[j].x = fmaf(kr, ku[0], S[j].x);
-      S[j].y = fmaf(kr, ku[1], S[j].y);
-      S[j].z = fmaf(kr, ku[2], S[j].z);
-      S[j].w = fmaf(kr, ku[3], S[j].w);
-      oo[0] = fmaf(S[j].x, qr, oo[0]);
-      oo[1] = fmaf(S[j].y, qr, oo[1]);
-      oo[2] = fmaf(S[j].z, qr, oo[2]);
-      oo[3] = fmaf(S[j].w, qr, oo[3]);
-    }
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) oo[x] += __shfl_xor_sync(0xffffffffu, oo[x], o);
-    }
-    if (rl == 0) {
-#pragma unroll
-      for (int x = 0; x < 4; ++x) go[(t * HV + hv) * (int64_t)V + c0 + x] = from_f32<Tin>(qn * oo[x]);
-    }
-    __syncthreads();  // the next token rewrites the shared vectors
-  }
-  if (a.final_state != nullptr) {
-#pragma unroll
-    for (int j = 0; j < kVecRows; ++j)
-      *reinterpret_cast<float4*>(a.final_state + state_base + (size_t)8 * j * V) = S[j];
   }
 }
 
