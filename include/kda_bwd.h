@@ -81,7 +81,8 @@ size_t kda_bwd_workspace_size(const kda_bwd_params* p);
 
 /* Number of kernel launches one kda_bwd call makes (0 if the parameters are invalid): the
    chunk table (varlen only), prep, states, state gradient, the products over v (bf16 inputs
-   with K = V = 128 and chunk 64 only) and gradients.  The zeroing stage (cudaMemsetAsync of
+   with K = V = 128 and chunk 64 only), gradients and gate (the gate, beta and L2-norm
+   backward).  The zeroing stage (cudaMemsetAsync of
    what atomics accumulate into, dA_log, ddt_bias and, with HV > H, dq and dk, and of the rows
    no sequence covers; every other output element is written once by the kernels) is not
    counted.  Host only. */
@@ -92,8 +93,8 @@ int32_t kda_bwd_num_launches(const kda_bwd_params* p);
 int32_t kda_bwd_num_stages(const kda_bwd_params* p);
 
 /* Name of stage `stage` ("zero_outputs", "chunk_table", "bwd_prep", "bwd_states",
-   "bwd_dstate", "bwd_vprod", "bwd_grads"); "" if out of range or the parameters are
-   invalid. */
+   "bwd_dstate", "bwd_vprod", "bwd_grads", "bwd_gate"); "" if out of range or the parameters
+   are invalid. */
 const char* kda_bwd_stage_name(const kda_bwd_params* p, int32_t stage);
 
 /* Enqueue only stage `stage` of kda_bwd on `stream`.  Calling every stage in order on one

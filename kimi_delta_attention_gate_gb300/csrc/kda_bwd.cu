@@ -199,6 +199,13 @@ __global__ void __launch_bounds__(kThreads, 2) grads_kernel(const Args a) {
   grads_body<SC, SK, SV>(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);
 }
 
+template <int SC, int SK, int SV>
+__global__ void __launch_bounds__(kThreads, 3) gate_kernel(const Args a) {
+  extern __shared__ float smem[];
+  GpuExec ex;
+  gate_body<SC, SK, SV>(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);
+}
+
 // The common shape (chunk 64, K = V = 128) with its dimensions compiled in.
 bool common_shape(const Plan& p) { return p.C == 64 && p.K == 128 && p.V == 128; }
 
@@ -313,6 +320,12 @@ cudaError_t run_dstate(const Args& a, cudaStream_t st) {
   return launch_smem(dstate_kernel, dim3((unsigned)state_blocks(a.p)), dstate_smem(a.p), a, st);
 }
 
+cudaError_t run_gate(const Args& a, cudaStream_t st) {
+  const dim3 grid((unsigned)a.p.nct, (unsigned)a.p.HV);
+  return common_shape(a.p) ? launch_smem(gate_kernel<64, 128, 128>, grid, gate_smem(a.p), a, st)
+                           : launch_smem(gate_kernel<0, 0, 0>, grid, gate_smem(a.p), a, st);
+}
+
 cudaError_t run_grads(const Args& a, cudaStream_t st) {
   const dim3 grid((unsigned)a.p.nct, (unsigned)a.p.HV);
   return common_shape(a.p) ? launch_smem(grads_kernel<64, 128, 128>, grid, grads_smem(a.p), a, st)
@@ -329,7 +342,7 @@ struct Stage {
   const char* name;
   cudaError_t (*run)(const Args&, cudaStream_t);
 };
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 9;
 
 // The stages of one backward call, in order: the zeroing of the outputs (cudaMemsetAsync,
 // no kernel of this library), then the kernels.
@@ -344,6 +357,7 @@ int stages_for(const Plan& pl, Stage* out) {
   }
   if (pl.nct > 0 && pl.tc_vprod) out[n++] = {"bwd_vprod", run_vprod_tc};
   if (pl.nct > 0) out[n++] = {"bwd_grads", run_grads};
+  if (pl.nct > 0) out[n++] = {"bwd_gate", run_gate};
   return n;
 }
 

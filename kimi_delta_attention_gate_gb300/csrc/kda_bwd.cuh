@@ -1362,7 +1362,7 @@ template <int SC = 0, int SK = 0, int SV = 0, class Exec>
 KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem) {
   const Plan& p = a.p;
   const int C = SC ? SC : p.C, K = SK ? SK : p.K, V = SV ? SV : p.V;
-  const int H = p.H, HV = p.HV, h = hv / p.G;
+  const int HV = p.HV;
   int n, L;
   int64_t t0;
   if (!locate(a, c, n, t0, L)) {
@@ -1380,7 +1380,6 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   const float* dVn = blk + b.dvn;
   const float* P = blk + b.p;
   const float* Be = blk + b.beta;
-  const float* Dc = blk + b.decay;
   const float* ATi = blk + b.ati;
   float* Y = blk + b.y;
   float* X = blk + b.x;
@@ -1411,8 +1410,6 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   float* sXY = sT;                            // [C][(V + K + 1) / 2] back substitution columns
   float* sZt = sT;                            // [C][lda] dP transposed (the scratch is free then)
   const int ncol = V + K, half_cols = (ncol + 1) / 2;
-  const bool has_alog = a.A_log != nullptr && a.gate_mode != KDA_GATE_PREGATED;
-  const float a_exp = has_alog ? expf(a.A_log[hv]) : 1.0f;
   const int K4 = pad4(K), CB = C / 4;
   const bool vecV = (V & 3) == 0, vecK = (K & 3) == 0;
   // rows of the inputs dO and v (only rows < L exist)
@@ -2080,6 +2077,60 @@ KDA_UNROLL
       }
     });
   }
+  // hand-over to the gate stage (through the X slot, dead by now): dbeta's WY and dAkk parts
+  // and diag(S dS'^T)
+  ex.phase([&](int tid, int nthr) {
+    for (int i = tid; i < C; i += nthr) X[i] = sDB[i];
+    for (int kk = tid; kk < K; kk += nthr) X[C + kk] = sDgc[kk];
+  });
+}
+
+// ---- gate: per (chunk c, value head hv), after grads -----------------------------------
+//
+// The reverse cumsum of dGamma with the gamma_C terms, the gate activation's backward (dg,
+// dA_log, ddt_bias), dbeta with the sigmoid's backward, and the L2-norm backward of q and k
+// (dq, dk): element-wise phases over the gradient stage's dGamma, dK, dQ rows, in a kernel of
+// their own so that their small shared memory and registers allow more blocks per SM.
+
+inline size_t gate_scratch(const Plan& p) {
+  const size_t C = (size_t)p.C, ng = (size_t)((p.K + 3) / 4);
+  const size_t l2 = 2 * ng * (2 * C + 1) + 4 * C, half = 4 * (size_t)p.K;
+  return l2 > half ? l2 : half;
+}
+inline size_t gate_smem(const Plan& p) {
+  return sizeof(float) * ((size_t)p.C + (size_t)((p.K + 3) & ~3) + kThreads + gate_scratch(p));
+}
+
+template <int SC = 0, int SK = 0, int SV = 0, class Exec>
+KDA_BODY void gate_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem) {
+  const Plan& p = a.p;
+  const int C = SC ? SC : p.C, K = SK ? SK : p.K;
+  const int H = p.H, HV = p.HV, h = hv / p.G;
+  int n, L;
+  int64_t t0;
+  if (!locate(a, c, n, t0, L)) {
+    ex.flag(a.status, KDA_DEV_BAD_SEQLENS);
+    return;
+  }
+  const Block& b = p.blk;
+  float* blk = block_ptr(a, c, hv);
+  const float* dGam = blk + b.dgam;
+  const float* dKG = blk + b.dkg;
+  const float* Dc = blk + b.decay;
+  const float* dQ = blk + b.dq;
+  const float* dK = blk + b.dk;
+  const float* X = blk + b.x;  // the gradient stage's hand-over
+  float* sDB = smem;                      // [C] gradient of beta (the value)
+  float* sDgc = sDB + C;                  // [K4] diagonal of S dS'^T
+  float* sRed = sDgc + pad4(K);           // [kThreads] partial sums of dA_log
+  float* sT = sRed + kThreads;            // scratch (gate_scratch floats)
+  const bool has_alog = a.A_log != nullptr && a.gate_mode != KDA_GATE_PREGATED;
+  const float a_exp = has_alog ? expf(a.A_log[hv]) : 1.0f;
+  const bool vecK = (K & 3) == 0;
+  ex.phase([&](int tid, int nthr) {
+    for (int i = tid; i < C; i += nthr) sDB[i] = X[i];
+    for (int kk = tid; kk < K; kk += nthr) sDgc[kk] = X[C + kk];
+  });
   // reverse cumsum of dGamma (plus the gamma_C terms on the last row) and the gate backward,
   // with each channel's rows in two halves: first every half's sums of dGamma and of the
   // gamma_C terms, then each half's reverse cumsum from the total of the rows above it

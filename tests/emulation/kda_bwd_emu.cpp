@@ -216,6 +216,9 @@ int main(int argc, char** argv) {
   for (int64_t c = 0; c < pl.nct; ++c)
     for (int hv = 0; hv < pl.HV; ++hv)
       with_smem(kda::bwd::grads_smem(pl), [&](float* sm) { kda::bwd::grads_body(ex, a, c, hv, sm); });
+  for (int64_t c = 0; c < pl.nct; ++c)
+    for (int hv = 0; hv < pl.HV; ++hv)
+      with_smem(kda::bwd::gate_smem(pl), [&](float* sm) { kda::bwd::gate_body(ex, a, c, hv, sm); });
 
   save(dir, "dq", a.dq, qk);
   save(dir, "dk", a.dk, qk);

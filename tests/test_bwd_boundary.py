@@ -45,7 +45,7 @@ def test_valid_parameters_pass(lib):
     p = params()
     assert kb.kda_bwd_check(p) == kb.KDA_OK
     assert kb.kda_bwd_workspace_size(p) > 0
-    assert kb.kda_bwd_num_launches(p) == 4                     # prep, states, dstate, grads
+    assert kb.kda_bwd_num_launches(p) == 5                     # prep, states, dstate, grads, gate
 
 
 @pytest.mark.parametrize("over,status", [
@@ -106,7 +106,7 @@ def test_varlen_launch_count_and_chunk_table(lib):
     p = params(fwd_B=1, fwd_T=200, fwd_N=3, fwd_cu_seqlens=FAKE)
     p.fwd.cu_seqlens_host = ctypes.addressof(cu)
     assert kb.kda_bwd_check(p) == kb.KDA_OK
-    assert kb.kda_bwd_num_launches(p) == 5                     # + the chunk table
+    assert kb.kda_bwd_num_launches(p) == 6                     # + the chunk table
 
 
 def test_no_tokens_launches_only_the_state_stages(lib):
@@ -141,18 +141,19 @@ def test_without_gpu_reports_cuda_error(lib):
 
 def test_stage_lists(lib):
     names = lambda p: [kb.kda_bwd_stage_name(p, i) for i in range(kb.kda_bwd_num_stages(p))]
-    assert names(params()) == ["zero_outputs", "bwd_prep", "bwd_states", "bwd_dstate", "bwd_grads"]
+    assert names(params()) == ["zero_outputs", "bwd_prep", "bwd_states", "bwd_dstate", "bwd_grads",
+                               "bwd_gate"]
     cu = (ctypes.c_int64 * 4)(0, 5, 64, 200)
     p = params(fwd_B=1, fwd_T=200, fwd_N=3, fwd_cu_seqlens=FAKE)
     p.fwd.cu_seqlens_host = ctypes.addressof(cu)
     assert names(p) == ["zero_outputs", "chunk_table", "bwd_prep", "bwd_states", "bwd_dstate",
-                        "bwd_grads"]
+                        "bwd_grads", "bwd_gate"]
     assert kb.kda_bwd_num_launches(p) == kb.kda_bwd_num_stages(p) - 1
-    assert kb.kda_bwd_stage_name(params(), 5) == "" and kb.kda_bwd_stage_name(params(), -1) == ""
+    assert kb.kda_bwd_stage_name(params(), 6) == "" and kb.kda_bwd_stage_name(params(), -1) == ""
     assert kb.kda_bwd_num_stages(params(dq=0)) == 0
     # bf16 at K = V = 128, chunk 64: the products over v get a tensor-core stage of their own
     assert names(params(fwd_V=128)) == ["zero_outputs", "bwd_prep", "bwd_states", "bwd_dstate",
-                                        "bwd_vprod", "bwd_grads"]
+                                        "bwd_vprod", "bwd_grads", "bwd_gate"]
     assert "bwd_vprod" not in names(params(fwd_V=128, fwd_in_dtype=kb.KDA_F32))
 
 
