@@ -82,7 +82,7 @@ def test_backward_measurement_logic_with_the_gpu_calls_faked(monkeypatch):
 
     clock = {"t": 0.0}
     per_stage_ms = {"zero_outputs": 0.5, "bwd_prep": 2.0, "bwd_states": 3.0, "bwd_dstate": 4.0,
-                    "bwd_grads": 10.0}
+                    "bwd_grads": 10.0, "bwd_gate": 1.0}
 
     class Event:
         def __init__(self, enable_timing=False):
@@ -139,5 +139,5 @@ def test_backward_measurement_logic_with_the_gpu_calls_faked(monkeypatch):
     assert roof["flops_per_launch"] == fl
     assert abs(roof["achieved"] - fl / 10e-3 / 1e12) < 1e-12
     assert abs(roof["peak"] - 80.54784) < 1e-9 and 0 < roof["frac"] < 1
-    assert out["gpu_launches_per_step"] == 4
+    assert out["gpu_launches_per_step"] == 5
     assert out["workspace_bytes"] > 0
