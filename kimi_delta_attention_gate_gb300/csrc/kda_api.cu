@@ -43,15 +43,15 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Pipelined schedule limits: segment only when at most this many (sequence, value head)
 // recurrences run (each takes one SM), with about kSegChunks chunks per segment (each
-// segment costs a few microseconds of launch and pipeline start-up; 8 segments of 128
-// chunks measured best for 1024 chunks).
+// segment costs a few microseconds of launch and recurrence start-up; with the intra-chunk
+// segments overlapping one another, 10 segments of ~102 chunks measured best for 1024
+// chunks: 1.757 ms against 1.771 for 8 and 1.764 for 12).
 constexpr int64_t kSegMaxRecurrences = 96;
-constexpr int64_t kSegChunks = 128;
-constexpr int kMaxSegments = 8;
+constexpr int64_t kSegChunks = 100;
+constexpr int kMaxSegments = 10;
 
-// Chunk boundary k (0..nseg) of the segments.  Device inputs: equal segments (with the two
-// kernels taking about the same time per chunk they measured best, 1.89 ms against 1.93 for
-// ramped ones).  Host inputs (ramp): weights 1, 2, 4, ..., 4, 2, 1, so that the first
+// Chunk boundary k (0..nseg) of the segments.  Device inputs: equal segments (measured best
+// against schedules with a larger first or smaller last segments).  Host inputs (ramp): weights 1, 2, 4, ..., 4, 2, 1, so that the first
 // segment's input copy, after which computing starts, and the last segment's compute and
 // output copy, which follow the last input byte, are short: the host link sets the pace.
 int64_t seg_bound(int64_t nct, int nseg, int k, bool ramp = false) {
@@ -243,7 +243,12 @@ struct SegHooks {
 // Segments k = 0..nseg-1: intra(k) on the caller's stream, recur(k) on the internal
 // high-priority stream after intra(k) and recur(k-1); the caller's stream then waits for
 // the last recurrence.  Stream order alone carries every dependency (no kernel waits on
-// another), so the schedule is also valid under stream capture.
+// another), so the schedule is also valid under stream capture.  intra(k), k > 0, is a
+// programmatic dependent of intra(k-1): the two share no data, and its CTAs fill the SMs
+// while intra(k-1)'s last wave drains instead of after it (1.845 -> 1.771 ms on 1024
+// chunks x 32 heads); the event that recur(k-1) waits on still marks the whole of
+// intra(k-1).  With hooks (input copies waited for before each intra kernel) every launch
+// keeps the full dependency.
 cudaError_t launch_pipelined_locked(PipeCtx* cx, const FwdArgs& a, cudaStream_t s,
                                     const char** what, SegHooks* hooks) {
   const Plan& pl = a.plan;
@@ -262,7 +267,7 @@ cudaError_t launch_pipelined_locked(PipeCtx* cx, const FwdArgs& a, cudaStream_t 
     *what = "input copies";
     if (hooks && (e = hooks->before_intra(*cx, k, ak.c_begin, ak.c_end)) != cudaSuccess) return e;
     *what = "tc_intra";
-    if ((e = launch_tc_intra(ak, s)) != cudaSuccess) return e;
+    if ((e = launch_tc_intra(ak, s, k > 0 && hooks == nullptr)) != cudaSuccess) return e;
     *what = "pipeline event";
     if ((e = cudaEventRecord(cx->seg[k], s)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(cx->rs, cx->seg[k], 0)) != cudaSuccess) return e;

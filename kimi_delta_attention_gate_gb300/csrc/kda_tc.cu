@@ -213,6 +213,11 @@ __global__ void __launch_bounds__(256, 2)
   const int h = hv / p.G;
   int n, L;
   int64_t t0;
+  // A launch of the next chunk range that was made dependent on this one programmatically
+  // may start its CTAs once every CTA of this grid has started (this grid's last wave then
+  // shares the SMs with that grid's first); no CTA of either reads what the other writes.
+  // Without such a launch the instruction does nothing.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (!locate_chunk(a, c, n, t0, L)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float* sBeta = reinterpret_cast<float*>(sm + P_BETA);
@@ -1159,7 +1164,9 @@ bool tc_eligible(const Plan& p, int dtype) {
 
 size_t tc_inter_block_bytes() { return BLOCK_BYTES; }
 
-cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s) {
+cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s) { return launch_tc_intra(a, s, false); }
+
+cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s, bool overlap_previous) {
   const Plan& p = a.plan;
   if (a.c_end <= a.c_begin) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
@@ -1187,12 +1194,25 @@ cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s) {
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)(a.c_end - a.c_begin), (unsigned)p.HV);
+  // overlap_previous: the kernel may start while the work enqueued before it on `s` (the
+  // previous chunk range's intra-chunk kernel, which triggers at its start) is still running
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = P_SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
   cudaError_t e;
 #define KDA_LAUNCH_INTRA(G)                                                                  \
   e = cudaFuncSetAttribute(tc_intra_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                            (int)P_SMEM);                                                     \
   if (e != cudaSuccess) return e;                                                            \
-  tc_intra_kernel<G><<<grid, 256, P_SMEM, s>>>(a, qmap, kmap, gmap);
+  e = cudaLaunchKernelEx(&cfg, tc_intra_kernel<G>, a, qmap, kmap, gmap);                     \
+  if (e != cudaSuccess) return e;
   if (a.gate_mode == KDA_GATE_SAFE) {
     KDA_LAUNCH_INTRA(KDA_GATE_SAFE)
   } else if (a.gate_mode == KDA_GATE_PLAIN) {

@@ -45,8 +45,8 @@ def test_host_entry_pipelined_long_sequence():
     assert_close(fs[:, [1]], rfs, "bf16", "final_state")
 
 
-def test_host_entry_pipelined_batch_five_segments():
-    """B=3 sequences over five segments (boundaries inside sequences)."""
+def test_host_entry_pipelined_batch_six_segments():
+    """B=3 sequences over six segments (boundaries inside sequences)."""
     same_as_device(kin.make_inputs(wl_(B=3, T=64 * 200 + 10, H=1, HV=1, dtype="bf16", seed=601)))
 
 

@@ -232,8 +232,8 @@ def test_tc_pipelined_one_long_sequence(gate):
     check_pipelined(kin.make_inputs(tc(T=64 * 256 + 37, gate=gate, seed=400 + gate)))
 
 
-def test_tc_pipelined_five_segments():
-    """640 chunks: five segments."""
+def test_tc_pipelined_six_segments():
+    """640 chunks: six segments."""
     check_pipelined(kin.make_inputs(tc(T=64 * 640, H=1, HV=1, seed=402)))
 
 
