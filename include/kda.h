@@ -127,14 +127,14 @@ kda_status kda_fwd_check(const kda_fwd_params* p);
    tokens cu_seqlens[N] .. B*T - 1) are set to zero, as the token recurrence
    defines them.  Returns KDA_ERR_CUDA if a launch fails.
    When few (sequence, value head) recurrences would leave most SMs idle (bf16
-   tensor-core path, N * HV <= 96, at least 256 chunks), the chunk range is cut
-   into up to 8 segments: the intra-chunk kernel of segment k+1 runs on `stream`
-   while the recurrence of segment k runs on a library-owned high-priority stream
-   of the current device, the fp32 state carried between segments in the
-   workspace.  The work is still ordered after everything enqueued on `stream`
-   before the call and before everything enqueued after it (event fork / join,
-   valid under stream capture); the results are bit-identical to the stages run
-   one after another.  kda_fwd_num_launches gives the kernel count. */
+   tensor-core path, N * HV <= 96, at least 200 chunks), the chunk range is cut into up
+   to 10 segments: the intra-chunk kernel of segment k+1 runs on `stream` (a programmatic
+   dependent of segment k's, with which it shares no data, so that it starts while that
+   one's last CTAs run) while the recurrence of segment k runs on a library-owned stream of
+   the highest priority, the fp32 state carried between segments in the workspace.  The
+   work is still ordered after everything enqueued on `stream` before the call and before
+   everything enqueued after it (event fork / join, valid under stream capture); results
+   are bit-identical to the stages run one by one (kda_fwd_num_launches: kernel count). */
 kda_status kda_fwd(const kda_fwd_params* p, void* stream);
 
 /* Number of kernel launches one kda_fwd call makes for these parameters (0 if

@@ -23,6 +23,12 @@ namespace kda {
 
 __device__ unsigned int g_device_status;
 
+// The intra-chunk kernel launch (kda_tc.cu) with overlap_previous: launched as a
+// programmatic dependent of the kernel before it on `s`, so that its CTAs may start while
+// that kernel's last CTAs run; only for a kernel that reads nothing the previous one writes
+// (the intra-chunk kernels of consecutive chunk ranges).
+cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s, bool overlap_previous);
+
 namespace {
 
 thread_local std::string t_last_error;

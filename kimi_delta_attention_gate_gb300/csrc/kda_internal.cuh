@@ -159,10 +159,6 @@ cudaError_t launch_recurrent(const FwdArgs& a, cudaStream_t s);
 bool tc_eligible(const Plan& p, int dtype);
 size_t tc_inter_block_bytes();
 cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s);
-// overlap_previous: launched as a programmatic dependent of the kernel before it on `s`, so
-// that its CTAs may start while that kernel's last CTAs run; for a kernel that does not read
-// what the previous one writes (the intra-chunk kernels of consecutive chunk ranges)
-cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s, bool overlap_previous);
 cudaError_t launch_tc_recur(const FwdArgs& a, cudaStream_t s);
 
 }  // namespace kda

@@ -1164,8 +1164,6 @@ bool tc_eligible(const Plan& p, int dtype) {
 
 size_t tc_inter_block_bytes() { return BLOCK_BYTES; }
 
-cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s) { return launch_tc_intra(a, s, false); }
-
 cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s, bool overlap_previous) {
   const Plan& p = a.plan;
   if (a.c_end <= a.c_begin) return cudaSuccess;
@@ -1223,6 +1221,8 @@ cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s, bool overlap_previ
 #undef KDA_LAUNCH_INTRA
   return cudaGetLastError();
 }
+
+cudaError_t launch_tc_intra(const FwdArgs& a, cudaStream_t s) { return launch_tc_intra(a, s, false); }
 
 cudaError_t launch_tc_recur(const FwdArgs& a, cudaStream_t s) {
   const Plan& p = a.plan;
