@@ -340,20 +340,27 @@ KDA_HD uint32_t swz128(uint32_t row, uint32_t col) {
          ((col & 7u) << 1);
 }
 // Eight consecutive elements x[0..7] as bf16 hi + lo: one 16-byte chunk at byte offset `off`
-// of a tile's high part and one at the same offset of its low part
+// of a tile's high part and one at the same offset of its low part.  On the GPU two elements
+// round in one instruction (cvt.rn.bf16x2.f32, round to nearest even as bf16_bits_rn: the same
+// bits for every finite value); the element with the lower index sits in the lower half.
 KDA_HD void put_hilo8(char* tile, size_t off, const float (&x)[8], size_t lo_off = kTileLo) {
+#if defined(__CUDA_ARCH__)
+  uint32_t h[4], l[4];
+  KDA_UNROLL
+  for (int j = 0; j < 4; ++j) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[j]) : "f"(x[2 * j + 1]), "f"(x[2 * j]));
+    const float r0 = x[2 * j] - __uint_as_float(h[j] << 16);
+    const float r1 = x[2 * j + 1] - __uint_as_float(h[j] & 0xFFFF0000u);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(l[j]) : "f"(r1), "f"(r0));
+  }
+  *reinterpret_cast<uint4*>(tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(tile + off + lo_off) = make_uint4(l[0], l[1], l[2], l[3]);
+#else
   uint16_t hi[8], lo[8];
   for (int j = 0; j < 8; ++j) {
     hi[j] = bf16_bits_rn(x[j]);
     lo[j] = bf16_bits_rn(x[j] - bf16_to_f32(hi[j]));
   }
-#if defined(__CUDA_ARCH__)
-  uint4 h, l;
-  memcpy(&h, hi, 16);
-  memcpy(&l, lo, 16);
-  *reinterpret_cast<uint4*>(tile + off) = h;
-  *reinterpret_cast<uint4*>(tile + off + lo_off) = l;
-#else
   memcpy(tile + off, hi, 16);
   memcpy(tile + off + lo_off, lo, 16);
 #endif
