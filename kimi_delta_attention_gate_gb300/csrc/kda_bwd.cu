@@ -30,6 +30,10 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 
 struct GpuExec {
   static constexpr bool kTensorCores = true;
+  // zprod's 64-column tensor-memory accumulator, allocated by the kernel when it starts: a
+  // block that allocated in its middle would wait for the other block resident on the SM
+  // until that one had allocated and relinquished its allocation permit too
+  uint32_t tmem_base = 0;
   template <class F>
   __device__ __forceinline__ void phase(F&& f) {
     f((int)threadIdx.x, (int)blockDim.x);
@@ -58,7 +62,7 @@ struct GpuExec {
   // layout (v in bf16 is exact: its high part alone), one thread issues the M = 64, N = 64
   // MMAs (hi hi + lo hi + hi lo) into a tensor-memory accumulator, and the block waits for
   // them before the next slice's tiles; then the accumulator's rows go to sZ.  scratch: at
-  // least 33 KB; sTc: 32 bytes (barrier, TMEM address).
+  // least 33 KB; sTc: 32 bytes (barrier); the accumulator: tmem_base.
   __device__ void zprod(float* sZ, int ldz, float* scratch, float* sTc, const float* X,
                         const float* Y, const void* v_in, size_t v_row0, size_t v_stride,
                         int dtype, const float* EK, int L, unsigned int* status) {
@@ -67,18 +71,13 @@ struct GpuExec {
     uint8_t* tiles = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(scratch) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(sTc);
-    uint32_t* slot = reinterpret_cast<uint32_t*>(sTc + 2);
-    if (warp == 0) {
-      tmem_alloc(slot, 64);
-      tmem_relinquish();
-    }
     if (tid == 0) {
       mbar_init(bar, 1);
       fence_mbar_init();
     }
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *slot;
+    const uint32_t tmem = tmem_base;
     const uint32_t t_ah = smem_u32(tiles), t_al = t_ah + 8192u, t_bh = t_ah + 16384u,
                    t_bl = t_ah + 24576u;
     const bool v_exact = dtype == KDA_BF16;
@@ -169,7 +168,6 @@ struct GpuExec {
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
   }
 };
 
@@ -196,7 +194,23 @@ template <int SC, int SK, int SV>
 __global__ void __launch_bounds__(kThreads, 2) grads_kernel(const Args a) {
   extern __shared__ float smem[];
   GpuExec ex;
+  constexpr bool kZprod = SC == 64 && SK == 128 && SV == 128;  // the shape zprod serves
+  __shared__ uint32_t tmem_slot;
+  if (kZprod) {
+    if (threadIdx.x < 32) {
+      tc::tmem_alloc(&tmem_slot, 64);
+      tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    ex.tmem_base = tmem_slot;
+  }
   grads_body<SC, SK, SV>(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);
+  if (kZprod) {
+    tc::tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) tc::tmem_dealloc(ex.tmem_base, 64);
+  }
 }
 
 template <int SC, int SK, int SV>

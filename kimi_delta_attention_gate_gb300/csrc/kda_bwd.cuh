@@ -1407,7 +1407,7 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   float* sDB = sB + C;                        // [C] gradient of beta (the value)
   float* sRed = sDB + C;                      // [kThreads] partial sums of dA_log
   float* sFlag = sRed + kThreads;             // [4] > 0: some block exponent out of range
-  float* sTc = sFlag + 4;                     // [8] the tensor-core product's barrier, TMEM slot
+  float* sTc = sFlag + 4;                     // [8] the tensor-core product's barrier
   float* sDgc = sFlag + 12;                   // [K4] diagonal of S dS'^T
   float* sRg = sDgc + pad4(K);                // the product slices' staging, then:
   float* sAt = sRg;                           // [C][C] A^T: sAt[j][i] = A[i][j]
