@@ -213,8 +213,11 @@ __global__ void __launch_bounds__(kThreads, 2) grads_kernel(const Args a) {
   }
 }
 
+// Five blocks per SM (48 registers, no spills): the element-wise phases wait on workspace
+// rows, and more blocks keep more of those loads in flight (2.82 ms at three blocks per SM,
+// 2.43 at four, 2.35 at five on the long workload; six spill)
 template <int SC, int SK, int SV>
-__global__ void __launch_bounds__(kThreads, 3) gate_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, 5) gate_kernel(const Args a) {
   extern __shared__ float smem[];
   GpuExec ex;
   gate_body<SC, SK, SV>(ex, a, (int64_t)blockIdx.x, (int)blockIdx.y, smem);
