@@ -1382,7 +1382,6 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
   const float* Qn = blk + b.qn;
   const float* Kn = blk + b.kn;
   const float* Qg = blk + b.qg;
-  const float* Kg = blk + b.kg;
   const float* Vn = blk + b.vn;
   const float* dVn = blk + b.dvn;
   const float* P = blk + b.p;
@@ -1573,34 +1572,36 @@ KDA_BODY void grads_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem
     });
   }
   // the direct terms of dQg, dW, dKg; e^Gamma K for the A^T dA product
-  // element: four consecutive channels of a row (one 16-byte load per array when K % 4 == 0)
-  struct Direct { F4 gi, gl, dqg, dkg, kg, qg, kn; };
+  // element: four consecutive channels of a row (one 16-byte load per array when K % 4 == 0).
+  // Kg = Kn e^(Gamma_L-1 - Gamma) is formed again here exactly as the recompute stage forms
+  // it (the same operands and operations, so the same bits) instead of being read back.
+  struct Direct { F4 gi, dqg, dkg, qg, kn; };
   ex.phase([&](int tid, int nthr) {
     batched<8>(tid, nthr, C * C, [&](int e) { return ATi[e]; }, [&](int e, float v) { sAt[e] = v; });
     const int q4 = (K + 3) / 4;
-    batched<2>(tid, nthr, C * q4, [&](int e) {
+    batched<3>(tid, nthr, C * q4, [&](int e) {
       const int i = e / q4, c4 = 4 * (e - (e / q4) * q4);
       const F4 z{0.f, 0.f, 0.f, 0.f};
-      Direct d{z, z, z, z, z, z, z};
+      Direct d{z, z, z, z, z};
       if (i < L) {
         const size_t r = (size_t)i * K;
-        d = Direct{ld4w(Gam + r, c4, K, vecK), ld4w(Gam + (size_t)(L - 1) * K, c4, K, vecK),
-                   ld4w(dQ + r, c4, K, vecK), ld4w(dK + r, c4, K, vecK),
-                   ld4w(Kg + r, c4, K, vecK), ld4w(Qg + r, c4, K, vecK), ld4w(Kn + r, c4, K, vecK)};
+        d = Direct{ld4w(Gam + r, c4, K, vecK), ld4w(dQ + r, c4, K, vecK), ld4w(dK + r, c4, K, vecK),
+                   ld4w(Qg + r, c4, K, vecK), ld4w(Kn + r, c4, K, vecK)};
       }
       return d;
     }, [&](int e, const Direct& d) {
       const int i = e / q4, c4 = 4 * (e - (e / q4) * q4);
+      const F4 gl = ld4w(Gam + (size_t)(L - 1) * K, c4, K, vecK);  // cached: the same row for all
       float dq[4], dk[4], dg[4], dkg_kg[4], ekv[4];
       KDA_UNROLL
       for (int x = 0; x < 4; ++x) {
         dq[x] = dk[x] = dg[x] = dkg_kg[x] = ekv[x] = 0.f;
         if (i < L) {
           const float gi = f4at(d.gi, x), dqg = f4at(d.dqg, x), dkg = f4at(d.dkg, x);
-          const float eg = fexp(gi);
+          const float eg = fexp(gi), egl = fexp(f4at(gl, x) - gi);
           dq[x] = dqg * eg;
-          dk[x] = dkg * fexp(f4at(d.gl, x) - gi);
-          dkg_kg[x] = dkg * f4at(d.kg, x);
+          dk[x] = dkg * egl;
+          dkg_kg[x] = dkg * (f4at(d.kn, x) * egl);
           dg[x] = dqg * f4at(d.qg, x) - dkg_kg[x];
           ekv[x] = eg * f4at(d.kn, x);
         }
