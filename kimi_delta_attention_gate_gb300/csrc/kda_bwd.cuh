@@ -366,6 +366,31 @@ KDA_HD void put_hilo8(char* tile, size_t off, const float (&x)[8], size_t lo_off
 #endif
 }
 
+// Four consecutive elements as bf16 hi + lo: the 8-byte half of a 16-byte chunk at `off` (its
+// first or second half: the column's bit 2 in swz128), the same in the low part.
+KDA_HD void put_hilo4(char* tile, size_t off, const float (&x)[4], size_t lo_off = kTileLo) {
+#if defined(__CUDA_ARCH__)
+  uint32_t h[2], l[2];
+  KDA_UNROLL
+  for (int j = 0; j < 2; ++j) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[j]) : "f"(x[2 * j + 1]), "f"(x[2 * j]));
+    const float r0 = x[2 * j] - __uint_as_float(h[j] << 16);
+    const float r1 = x[2 * j + 1] - __uint_as_float(h[j] & 0xFFFF0000u);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(l[j]) : "f"(r1), "f"(r0));
+  }
+  *reinterpret_cast<uint2*>(tile + off) = make_uint2(h[0], h[1]);
+  *reinterpret_cast<uint2*>(tile + off + lo_off) = make_uint2(l[0], l[1]);
+#else
+  uint16_t hi[4], lo[4];
+  for (int j = 0; j < 4; ++j) {
+    hi[j] = bf16_bits_rn(x[j]);
+    lo[j] = bf16_bits_rn(x[j] - bf16_to_f32(hi[j]));
+  }
+  memcpy(tile + off, hi, 8);
+  memcpy(tile + off + lo_off, lo, 8);
+#endif
+}
+
 KDA_HD float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 // The sigmoid's derivative s(x) (1 - s(x)) = t / (1 + t)^2 with t = e^-|x| <= 1: one
 // exponential, and no cancellation once s(x) rounds to 1 (|x| beyond about 17 in fp32).
@@ -692,6 +717,35 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       Kg[e] = kg;
       W[e] = w;
     });
+    if (p.tc_states) {  // the state stages' Kg^T and Qg operand tiles (K = 128, C = 64), formed
+                        // from shared memory exactly as Kg and Qg above (the same bits)
+      char* tile = tile_ptr(a, c, hv);
+      const int c8 = C / 8;
+      for (int u = tid; u < K * c8; u += nthr) {  // Kg^T: row = channel, 8 tokens per piece
+        const int kk = u / c8, tb = 8 * (u - (u / c8) * c8);
+        const float gl = sGam[(size_t)(L - 1) * ldq + kk];
+        float x[8];
+        KDA_UNROLL
+        for (int j = 0; j < 8; ++j) {
+          const size_t o = (size_t)(tb + j) * ldq + kk;
+          x[j] = tb + j < L ? sKn[o] * fexp(gl - sGam[o]) : 0.f;
+        }
+        put_hilo8(tile, kTileKgT + swz128((uint32_t)kk, (uint32_t)tb), x);
+      }
+      if (p.tc_dstate) {
+        const int k4 = K / 4;
+        for (int u = tid; u < C * k4; u += nthr) {  // Qg: row = token, 4 channels per half piece
+          const int i = u / k4, k0 = 4 * (u - (u / k4) * k4);
+          float x[4];
+          KDA_UNROLL
+          for (int j = 0; j < 4; ++j) {
+            const size_t o = (size_t)i * ldq + k0 + j;
+            x[j] = i < L ? sQn[o] * fexp(sGam[o]) : 0.f;
+          }
+          put_hilo4(tile, kTileQg + (size_t)(k0 >> 6) * 8192 + swz128((uint32_t)i, (uint32_t)(k0 & 63)), x);
+        }
+      }
+    }
   });
   float* QFw = blk + b.qf;
   float* KFw = blk + b.kf;
@@ -763,13 +817,19 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
               }
           }
         }
-        for (int y = 0; y < 4; ++y)
+        for (int y = 0; y < 4; ++y) {
+          float row[4];
           for (int x = 0; x < 4; ++x) {
             const int i = 4 * ib + y, j = 4 * jb + x;
             const size_t e = (size_t)i * C + j;
-            Aqk[e] = (i < L && j <= i) ? aq[y][x] : 0.f;
+            row[x] = (i < L && j <= i) ? aq[y][x] : 0.f;
+            Aqk[e] = row[x];
             P[e] = (i < L && j < i) ? ak[y][x] : 0.f;
           }
+          if (p.tc_dstate)  // the state-gradient stage's Aqk operand tile
+            put_hilo4(tile_ptr(a, c, hv), kTileAqk + swz128((uint32_t)(4 * ib + y), (uint32_t)(4 * jb)),
+                      row, kTileAqkLo);
+        }
       }
     });
   } else {
@@ -908,6 +968,11 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
         const size_t i = (size_t)(r0 + y);
         if (whole && c0 + 4 <= K && vecK) {
           st4(W + i * K + c0, acc[y]);
+          if (p.tc_states) {  // the state stage's -W operand tile
+            const float nw[4] = {-acc[y][0], -acc[y][1], -acc[y][2], -acc[y][3]};
+            put_hilo4(tile_ptr(a, c, hv), kTileNegW + (size_t)(c0 >> 6) * 8192 +
+                                              swz128((uint32_t)i, (uint32_t)(c0 & 63)), nw);
+          }
         } else if (whole && c0 >= K && vecV && ((c0 - K) & 3) == 0) {
           st4(U + i * V + (c0 - K), acc[y]);
         } else {
@@ -926,48 +991,16 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       const int cc = e / C, i = e - (e / C) * C;
       ATi[e] = (i < L && cc < L) ? sA[(size_t)i * ldA + cc] : 0.f;
     }
-    if (p.tc_states) {  // the tensor-core state stage's operand tiles (K = 128, C = 64)
+    // the state-gradient stage's Aqk tile was written with Aqk, except by the exact path
+    if (p.tc_dstate && sFlag[0] != 0.f) {
       char* tile = tile_ptr(a, c, hv);
-      // eight consecutive floats of a row, loaded for four items per thread before any store
-      struct R8 { float v[8]; };
-      auto row8 = [&](const float* src, float sign) {
+      const int c8 = C / 8;
+      for (int u = tid; u < C * c8; u += nthr) {  // row = token, 8 tokens per piece
+        const int i = u / c8, j0 = 8 * (u - (u / c8) * c8);
+        const float* src = Aqk + (size_t)i * C + j0;
         const F4 x0 = ld4w(src, 0, 8, true), x1 = ld4w(src, 4, 8, true);
-        return R8{{sign * x0.x, sign * x0.y, sign * x0.z, sign * x0.w,
-                   sign * x1.x, sign * x1.y, sign * x1.z, sign * x1.w}};
-      };
-      const int k8 = K / 8, c8 = C / 8;
-      batched<4>(tid, nthr, C * k8, [&](int u) {  // -W: row = token, 8 channels per piece
-        const int i = u / k8, k0 = 8 * (u - (u / k8) * k8);
-        return row8(W + (size_t)i * K + k0, -1.f);
-      }, [&](int u, const R8& x) {
-        const int i = u / k8, k0 = 8 * (u - (u / k8) * k8);
-        put_hilo8(tile, kTileNegW + (size_t)(k0 >> 6) * 8192 + swz128((uint32_t)i, (uint32_t)(k0 & 63)), x.v);
-      });
-      batched<4>(tid, nthr, K * c8, [&](int u) {  // Kg^T: row = channel, 8 tokens per piece
-        const int kk = u / c8, t0 = 8 * (u - (u / c8) * c8);
-        R8 x;
-        KDA_UNROLL
-        for (int j = 0; j < 8; ++j) x.v[j] = Kg[(size_t)(t0 + j) * K + kk];
-        return x;
-      }, [&](int u, const R8& x) {
-        const int kk = u / c8, t0 = 8 * (u - (u / c8) * c8);
-        put_hilo8(tile, kTileKgT + swz128((uint32_t)kk, (uint32_t)t0), x.v);
-      });
-      if (p.tc_dstate) {
-        batched<4>(tid, nthr, C * c8, [&](int u) {  // Aqk: row = token, 8 tokens per piece
-          const int i = u / c8, j0 = 8 * (u - (u / c8) * c8);
-          return row8(Aqk + (size_t)i * C + j0, 1.f);
-        }, [&](int u, const R8& x) {
-          const int i = u / c8, j0 = 8 * (u - (u / c8) * c8);
-          put_hilo8(tile, kTileAqk + swz128((uint32_t)i, (uint32_t)j0), x.v, kTileAqkLo);
-        });
-        batched<4>(tid, nthr, C * k8, [&](int u) {  // Qg: row = token, 8 channels per piece
-          const int i = u / k8, k0 = 8 * (u - (u / k8) * k8);
-          return row8(Qg + (size_t)i * K + k0, 1.f);
-        }, [&](int u, const R8& x) {
-          const int i = u / k8, k0 = 8 * (u - (u / k8) * k8);
-          put_hilo8(tile, kTileQg + (size_t)(k0 >> 6) * 8192 + swz128((uint32_t)i, (uint32_t)(k0 & 63)), x.v);
-        });
+        const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        put_hilo8(tile, kTileAqk + swz128((uint32_t)i, (uint32_t)j0), x, kTileAqkLo);
       }
     }
   });
