@@ -696,6 +696,9 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       const int B = u / K;
       sRho[u] = sGam[(size_t)mid_row(B) * ldq + (u - B * K)];
     }
+    // Kg's rows are read only by the CUDA-core state stages: on the GPU with both state stages
+    // on the tensor cores (which read its operand tile) nothing reads them
+    const bool kg_rows = !(Exec::kTensorCores && p.tc_states && p.tc_dstate);
     struct Row { float gi, gl, q, k, be; };
     batched<4>(tid, nthr, C * K, [&](int e) {
       const int i = e / K, kk = e - (e / K) * K;
@@ -714,7 +717,7 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
         w = r.be * eg * r.k;
       }
       Qg[e] = qg;
-      Kg[e] = kg;
+      if (kg_rows) Kg[e] = kg;
       W[e] = w;
     });
     if (p.tc_states) {  // the state stages' Kg^T and Qg operand tiles (K = 128, C = 64), formed
