@@ -790,7 +790,10 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
   const int CB = C / 4;
   if (sFlag[0] == 0.f) {
     // Aqk (j <= i) and P (j < i) in 4 x 4 blocks: rows i of one 16-row block I, keys j of
-    // block B, over the channels of the shared-memory operands
+    // block B, over the channels of the shared-memory operands.  Aqk's fp32 rows are read only by
+    // the CUDA-core state-gradient stage; with it and the v products on the tensor cores the
+    // slot receives dAqk instead, and Aqk leaves only as the operand tile.
+    const bool aqk_rows = !(Exec::kTensorCores && p.tc_dstate && p.tc_vprod);
     ex.phase([&](int tid, int nthr) {
       for (int u = tid; u < CB * CB; u += nthr) {
         const int ib = u / CB, jb = u - (u / CB) * CB;
@@ -826,7 +829,7 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
             const int i = 4 * ib + y, j = 4 * jb + x;
             const size_t e = (size_t)i * C + j;
             row[x] = (i < L && j <= i) ? aq[y][x] : 0.f;
-            Aqk[e] = row[x];
+            if (aqk_rows) Aqk[e] = row[x];
             P[e] = (i < L && j < i) ? ak[y][x] : 0.f;
           }
           if (p.tc_dstate)  // the state-gradient stage's Aqk operand tile
@@ -938,6 +941,9 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       }
     });
   }
+  // W's fp32 rows are read only by the CUDA-core state stages (both state stages on the tensor
+  // cores read the -W operand tile)
+  const bool w_rows = !(Exec::kTensorCores && p.tc_states && p.tc_dstate);
   // [W | U] = A [beta e^Gamma K | beta V]: 4 x 4 tiles of (rows i, columns), sums over j <= i;
   // a warp's lanes share the row tile (the A words are broadcasts) and take consecutive column
   // quads; thread t pairs row tiles t' and CB - 1 - t' (long and short sums)
@@ -970,7 +976,7 @@ KDA_BODY void prep_body(Exec& ex, const Args& a, int64_t c, int hv, float* smem)
       for (int y = 0; y < 4; ++y) {
         const size_t i = (size_t)(r0 + y);
         if (whole && c0 + 4 <= K && vecK) {
-          st4(W + i * K + c0, acc[y]);
+          if (w_rows) st4(W + i * K + c0, acc[y]);
           if (p.tc_states) {  // the state stage's -W operand tile
             const float nw[4] = {-acc[y][0], -acc[y][1], -acc[y][2], -acc[y][3]};
             put_hilo4(tile_ptr(a, c, hv), kTileNegW + (size_t)(c0 >> 6) * 8192 +
